@@ -1,0 +1,184 @@
+"""MoE expert-FFN oracle: routing, padded permutation, block-scaled GEMMs,
+fused SwiGLU + NVFP4 re-quantisation, and the routing-weighted combine.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+The pipeline follows the "NVFP4 MegaMoE Debug Log", section "NVFP4 MoE
+Pipeline": stage the activation to NVFP4, L1 GEMM into interleaved gate/up
+columns, SiLU(gate) * up, re-stage to NVFP4, L2 GEMM, scatter with routing
+weights.  The padded per-expert grouping is the "padded_dst" / "padded
+activated fp4" layout of "NVFP4-1.1 Approach, Part 2".
+
+Readings where the pages are silent:
+* routing: the k largest logits, ties to the lower expert index, slots in
+  descending-logit order; weights = softmax over the k selected logits;
+* grouping: rows of expert e in ascending token order, each group padded to a
+  multiple of 128 rows (the SF atom's M extent and the MMA's M); padding rows
+  hold zero nibbles and zero scales and are marked -1 in ``perm_token``;
+* GEMMs accumulate exactly (float64 on dequantised operands) and apply the fp32
+  ``alpha`` scalar (global scale 1 by default);
+* the L1 output is quantised from fp32 h (never from a BF16-rounded h);
+* L2 rows and the combined output are BF16 (round-to-nearest-even); the
+  combine sums the k slots in slot order.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import nvfp4
+
+ROW_ALIGN = 128
+
+
+# ------------------------------------------------------------ BF16 rounding --
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest BF16 value (8 significant bits, ties
+    to even), returned as float64.  Values stay in BF16's normal range here."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                       # x = m * 2^e, 0.5 <= |m| < 1
+    r = np.rint(m * 256.0) / 256.0            # 8 significant bits, half-even
+    return np.ldexp(r, e)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """uint16 BF16 encodings of values that are already BF16-representable."""
+    f = np.asarray(x, dtype=np.float32)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bf16_from_bits(b: np.ndarray) -> np.ndarray:
+    """float32 values of uint16 BF16 encodings."""
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ routing --
+def route_topk(logits: np.ndarray, k: int) -> tuple:
+    """(ids int32 [T,k], w float64 [T,k]): top-k experts and softmax over them."""
+    logits = np.asarray(logits, dtype=np.float32)
+    t_count, e_count = logits.shape
+    if not 0 < k <= e_count:
+        raise ValueError("need 0 < k <= E")
+    # a stable sort of -logit keeps equal logits in ascending expert order
+    order = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :k]
+    sel = np.take_along_axis(logits, order, axis=1).astype(np.float64)
+    z = np.exp(sel - sel[:, :1])
+    w = z / z.sum(axis=1, keepdims=True)
+    return order.astype(np.int32), w
+
+
+def permute(ids: np.ndarray, n_experts: int, align: int = ROW_ALIGN) -> dict:
+    """Group the (token, slot) pairs by expert, each group padded to ``align`` rows.
+
+    Returns counts [E], offsets [E+1] (padded, exclusive), perm_token [R_pad]
+    (token of each row, -1 on padding) and inv_perm [T,k] (row of each pair).
+    """
+    ids = np.asarray(ids, dtype=np.int64)
+    t_count, k = ids.shape
+    counts = np.zeros(n_experts, dtype=np.int64)
+    for e in ids.ravel():
+        counts[e] += 1
+    padded = -(-counts // align) * align
+    offsets = np.zeros(n_experts + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(padded)
+    perm_token = np.full(int(offsets[-1]), -1, dtype=np.int64)
+    inv_perm = np.zeros((t_count, k), dtype=np.int64)
+    fill = offsets[:-1].copy()
+    for t in range(t_count):
+        for j in range(k):
+            e = ids[t, j]
+            r = fill[e]
+            fill[e] += 1
+            perm_token[r] = t
+            inv_perm[t, j] = r
+    return dict(counts=counts.astype(np.int32), offsets=offsets.astype(np.int32),
+                perm_token=perm_token.astype(np.int32), inv_perm=inv_perm.astype(np.int32))
+
+
+def stage_activation(x: np.ndarray, perm_token: np.ndarray) -> tuple:
+    """Quantise x (fp32 view of the BF16 activations, [T,H]) into the permuted,
+    padded rows: (a1_q [R_pad, H/2], a1_sf row-major [R_pad, H/16]).  Padding
+    rows are zero."""
+    x = np.asarray(x, dtype=np.float32)
+    xq, xsf = nvfp4.quantize_rows(x)
+    r_pad = len(perm_token)
+    a_q = np.zeros((r_pad, xq.shape[1]), dtype=np.uint8)
+    a_sf = np.zeros((r_pad, xsf.shape[1]), dtype=np.uint8)
+    real = perm_token >= 0
+    a_q[real] = xq[perm_token[real]]
+    a_sf[real] = xsf[perm_token[real]]
+    return a_q, a_sf
+
+
+# -------------------------------------------------------------------- GEMMs --
+def expert_of_rows(offsets: np.ndarray) -> np.ndarray:
+    """Expert index of every padded row."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    return np.repeat(np.arange(len(offsets) - 1), np.diff(offsets))
+
+
+def grouped_gemm(a_deq: np.ndarray, offsets: np.ndarray, b_deq: np.ndarray,
+                 alpha: float = 1.0) -> np.ndarray:
+    """out[r, n] = alpha * sum_k a[r, k] * b_e[n, k] for the expert e owning row r
+    (float64; ``b_deq`` is [E, N, K])."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    out = np.zeros((a_deq.shape[0], b_deq.shape[1]), dtype=np.float64)
+    for e in range(len(offsets) - 1):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi > lo:
+            out[lo:hi] = a_deq[lo:hi] @ b_deq[e].T
+    return np.float64(np.float32(alpha)) * out
+
+
+def l1_swiglu_requant(g_full: np.ndarray) -> tuple:
+    """Fused L1 epilogue on the interleaved gate/up accumulator rows
+    (float64 [rows, 2I]): h = silu(g) * u -> fp32, then NVFP4 per 16.
+    Returns (a2_q [rows, I/2], a2_sf row-major [rows, I/16], h fp32 [rows, I])."""
+    g, u = nvfp4.deinterleave_gu8(g_full)
+    h = nvfp4.swiglu_h(g, u)
+    q, sf = nvfp4.quantize_rows(h)
+    return q, sf, h
+
+
+def combine(rows_bf16: np.ndarray, inv_perm: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y[t] = sum_j w[t,j] * rows[inv_perm[t,j]] (float64, slot order) -> BF16 values."""
+    rows = np.asarray(rows_bf16, dtype=np.float64)
+    t_count, k = inv_perm.shape
+    acc = np.zeros((t_count, rows.shape[1]), dtype=np.float64)
+    for j in range(k):
+        acc += np.asarray(w[:, j], dtype=np.float64)[:, None] * rows[inv_perm[:, j]]
+    return round_to_bf16(acc)
+
+
+# ---------------------------------------------------------- whole FFN path --
+def dequant_weights(w_q: np.ndarray, w_sf_rows: np.ndarray) -> np.ndarray:
+    """[E, N, K/2] nibbles + [E, N, K/16] row-major SF -> float64 [E, N, K]."""
+    e_count = w_q.shape[0]
+    return np.stack([nvfp4.dequantize_rows(w_q[e], w_sf_rows[e]) for e in range(e_count)])
+
+
+def quantize_weights(w: np.ndarray) -> tuple:
+    """fp32 [E, N, K] -> ([E, N, K/2] nibbles, [E, N, K/16] row-major SF)."""
+    qs, sfs = zip(*(nvfp4.quantize_rows(w[e]) for e in range(w.shape[0])))
+    return np.stack(qs), np.stack(sfs)
+
+
+def moe_ffn(x: np.ndarray, logits: np.ndarray, w1: np.ndarray, w2: np.ndarray, top_k: int,
+            alpha1: float = 1.0, alpha2: float = 1.0) -> dict:
+    """The whole path on CPU.  x: fp32 values of the BF16 activations [T,H];
+    logits fp32 [T,E]; w1 fp32 [E, 2I, H] (rows interleaved 8|8); w2 fp32 [E, H, I].
+    Returns every intermediate (all computed here, none supplied from outside)."""
+    e_count = w1.shape[0]
+    ids, w = route_topk(logits, top_k)
+    p = permute(ids, e_count)
+    a1_q, a1_sf = stage_activation(x, p["perm_token"])
+    w1_q, w1_sf = quantize_weights(w1)
+    w2_q, w2_sf = quantize_weights(w2)
+    g_full = grouped_gemm(nvfp4.dequantize_rows(a1_q, a1_sf), p["offsets"],
+                          dequant_weights(w1_q, w1_sf), alpha1)
+    a2_q, a2_sf, h = l1_swiglu_requant(g_full)
+    o = grouped_gemm(nvfp4.dequantize_rows(a2_q, a2_sf), p["offsets"],
+                     dequant_weights(w2_q, w2_sf), alpha2)
+    rows = round_to_bf16(o)
+    y = combine(rows, p["inv_perm"], w)
+    return dict(ids=ids, w=w, a1_q=a1_q, a1_sf=a1_sf, w1_q=w1_q, w1_sf=w1_sf, w2_q=w2_q,
+                w2_sf=w2_sf, g_full=g_full, h=h, a2_q=a2_q, a2_sf=a2_sf, rows=rows, y=y, **p)
