@@ -1,0 +1,233 @@
+/*
+ * nvfp4moe.h -- C ABI of libnvfp4moe.so, the NVFP4 mixture-of-experts expert FFN
+ * for GB300 (sm_103a).
+ *
+ * The path (the "NVFP4 MegaMoE Debug Log", section "NVFP4 MoE Pipeline"):
+ *   moe_route_permute      top-k routing, 128-padded expert grouping, and the
+ *                          activation staged to NVFP4 in permuted row order
+ *   nvfp4_moe_ffn_forward  L1 block-scaled grouped GEMM -> fused SwiGLU + NVFP4
+ *                          re-quantisation -> L2 block-scaled grouped GEMM
+ *   moe_combine            routing-weighted sum of each token's expert rows
+ * plus the building blocks nvfp4_quantize, nvfp4_sf_swizzle and
+ * nvfp4_grouped_gemm.
+ *
+ * Number formats (the "NVFP4-1.1 Approach, Part 2" notes):
+ *   - E2M1 values, two per byte, element 2i in the low nibble of byte i;
+ *   - one FP8 E4M3 scale (bias 7, max 448, no NaN emitted) per 16 consecutive
+ *     K elements: scale = E4M3_rne_satfinite(fp32(amax / 6)), values divided by
+ *     the decoded scale in fp32, then hs = rne(2 * min(|s|, 6)) and hs/2 snapped
+ *     to the E2M1 grid with ties to even (so s = 5.25 -> nibble 6);
+ *   - "swizzled" SF layout: the K-major atom of the Debug Log's "CUTLASS SF
+ *     Layout" -- 512-byte atoms of 128 rows x 4 scales, byte offset
+ *       ((mn/128) * ceil(K/64) + k_sf/4) * 512 + (mn%32)*16 + ((mn/32)%4)*4 + k_sf%4
+ *     with buffer size nvfp4_sf_bytes(rows, K) (the "Allocation" section's
+ *     size(filter_zeros(layout))); padding bytes are written as zero.
+ *
+ * Conventions for every call:
+ *   - Pointers named *_q, *_sf, rows*, y*, logits, x*, w*, topk_*, expert_*,
+ *     perm_*, inv_perm, workspace are DEVICE pointers owned by the caller; the
+ *     library never allocates or frees device memory and keeps no state between
+ *     calls apart from a per-device error word (a __device__ variable).
+ *   - All calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     never synchronise the host, except nvfp4_device_status.
+ *   - Host-side argument checks run before any CUDA call; on failure the call
+ *     returns the status, launches nothing and records a message that
+ *     nvfp4_last_error() returns (thread-local).
+ *   - Device-side problems (a bounded wait that timed out, an index out of range)
+ *     set bits in the per-device error word; nvfp4_device_status() reports them.
+ *   - Tensor-core kernels require an sm_100-family GPU (built for sm_103a).
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4_stream_t;   /* identical to cudaStream_t */
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum */
+  NVFP4_ERR_UNSUPPORTED = 2,   /* a size outside what the kernels handle */
+  NVFP4_ERR_ALIGNMENT = 3,     /* a pointer or leading dimension not 16-byte aligned */
+  NVFP4_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  NVFP4_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up */
+  NVFP4_ERR_DEVICE = 6         /* a device-side index check failed */
+} nvfp4_status;
+
+typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_F32 = 1 } nvfp4_in_dtype;
+
+typedef enum {
+  NVFP4_MODE_PLAIN = 0,        /* quantise the input values themselves */
+  NVFP4_MODE_SWIGLU_GU8 = 1    /* input holds gate/up columns interleaved 8|8;
+                                  quantise h = silu(g) * u */
+} nvfp4_quant_mode;
+
+typedef enum {
+  NVFP4_EPI_SWIGLU_NVFP4 = 0,  /* SwiGLU on interleaved 8|8 columns, then NVFP4 */
+  NVFP4_EPI_BF16 = 1           /* alpha * acc rounded to BF16 */
+} nvfp4_epilogue;
+
+/* Bytes of a swizzled SF buffer for a rows x cols matrix (cols in elements):
+ * ceil(rows/128) * ceil(cols/64) * 512.  Returns 0 for non-positive sizes. */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+
+/* Rows to allocate for the permuted, 128-padded activation of T tokens routed
+ * top-k over E experts: the largest possible sum over experts of
+ * ceil(count_e / 128) * 128.  A multiple of 128. */
+int64_t moe_padded_rows_max(int32_t T, int32_t E, int32_t top_k);
+
+/* Bytes of device workspace moe_route_permute needs. */
+size_t moe_route_permute_workspace(int32_t T, int32_t H, int32_t E, int32_t top_k);
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_quantize -- per-16 NVFP4 quantiser ("NVFP4-1.1 Approach, Part 2": the
+ * quantize_nvfp4 kernel and the deinterleave + quantise kernel; the E4M3 cast
+ * and E2M1 nibble rules above).
+ *   in          rows x in_cols values, row stride in_ld_elems elements; in_cols =
+ *               out_cols (PLAIN) or 2*out_cols (SWIGLU_GU8, BF16 only:
+ *               columns [g0(8) u0(8) g1(8) u1(8) ...]).  16-byte aligned, and
+ *               in_ld_elems * element size a multiple of 16.
+ *   out_cols    quantised columns per row, a positive multiple of 16.
+ *   q_out       rows x out_cols/2 bytes, row-major (written).
+ *   sf_out      nvfp4_sf_bytes(rows, out_cols) bytes, swizzled (every byte written,
+ *               padding as zero).
+ *   h_debug     NULL, or rows x out_cols fp32: the values that were quantised.
+ * PLAIN mode is bit-exact against the specification above.  SWIGLU_GU8 computes
+ * silu with the fast exponential, so h may differ from a float64 evaluation by
+ * a few ulp, which can move a value across a rounding boundary.
+ * -------------------------------------------------------------------------- */
+nvfp4_status nvfp4_quantize(const void* in, nvfp4_in_dtype dtype, nvfp4_quant_mode mode,
+                            int64_t rows, int64_t out_cols, int64_t in_ld_elems,
+                            uint8_t* q_out, uint8_t* sf_out, float* h_debug,
+                            nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_sf_swizzle -- the SF remap of the "NVFP4 MegaMoE Debug Log" ("What the
+ * forward mapping does", "Source strides"): for every (mn, k_sf) < (mn_rows, k_sf_cols),
+ *   forward (inverse == 0): swz[offset(mn, k_sf)] = lin[mn*stride_mn + k_sf*stride_ksf]
+ *   inverse (inverse != 0): lin[mn*stride_mn + k_sf*stride_ksf] = swz[offset(mn, k_sf)]
+ * SFA (row-major M x K_sf) uses strides (K_sf, 1); SFB stored K_sf x N uses (1, N).
+ * The forward direction writes every byte of the nvfp4_sf_bytes(mn_rows, 16*k_sf_cols)
+ * buffer (padding as zero); the inverse writes only the addressed bytes.
+ * Strides are in bytes and must be positive.
+ * -------------------------------------------------------------------------- */
+nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_sf_cols,
+                              int64_t stride_mn, int64_t stride_ksf, uint8_t* sf_out,
+                              int inverse, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_permute -- routing plus "stage_activation" into the padded
+ * per-expert layout ("NVFP4 MegaMoE Debug Log", "NVFP4 MoE Pipeline";
+ * "NVFP4-1.1 Approach, Part 2", padded_dst gather / scatter).
+ *   logits      fp32 [T, E] router logits.
+ *   x_bf16      BF16 [T, H] activations (16-byte aligned).
+ *   topk_ids    int32 [T, top_k]: the top_k largest logits per token, in
+ *               descending order, ties to the lower expert index.
+ *   topk_w      fp32 [T, top_k]: softmax over the selected logits.
+ *   expert_counts   int32 [E]: routed rows per expert.
+ *   expert_offsets  int32 [E+1]: exclusive prefix sum of ceil(count/128)*128.
+ *   perm_token  int32 [R_max] (R_max = moe_padded_rows_max): token of each padded
+ *               row; -1 on padding rows inside a group; rows at or past
+ *               expert_offsets[E] are not written.  Within an expert, rows are in
+ *               ascending token order (deterministic, no atomics in the order).
+ *   inv_perm    int32 [T, top_k]: padded row of each (token, slot).
+ *   a1_q        [R_max, H/2] NVFP4 rows of x in permuted order; padding rows
+ *               inside groups are zero.
+ *   a1_sf       nvfp4_sf_bytes(R_max, H) bytes, swizzled, zero on padding rows.
+ *   workspace   >= moe_route_permute_workspace(T, H, E, top_k) bytes, 256-aligned.
+ * Limits: 1 <= E <= 1024, 1 <= top_k <= min(E, 32), H a positive multiple of 64,
+ * T >= 0 (T == 0 writes zero offsets and counts).
+ * -------------------------------------------------------------------------- */
+nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t T, int32_t H,
+                               int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
+                               int32_t* expert_counts, int32_t* expert_offsets,
+                               int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
+                               uint8_t* a1_sf, void* workspace, size_t workspace_bytes,
+                               nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_grouped_gemm -- block-scaled NVFP4 grouped GEMM on the tcgen05 tensor
+ * cores (the L1 "fused_swiglu" and L2 GEMMs of "NVFP4-1.1 Approach, Part 2"):
+ *   acc[r, n] = sum_k dq(A)[r, k] * dq(B_g)[n, k] for the group g owning row r,
+ * with dq(x) = e2m1(x) * e4m3(scale of x's 16-block).
+ *   a_q, a_sf   A: [rows_max, K/2] bytes, SF swizzled for rows_max x K.
+ *   group_offsets  device int32 [G+1] row offsets (multiples of 128) or NULL for
+ *               one group of rows_max rows.
+ *   group_counts   device int32 [G] real rows per group, or NULL: rows of a group
+ *               at or past its count are computed but not stored (with NULL
+ *               offsets, pass NULL; all rows_max rows are stored).
+ *   b_q, b_sf   B: [G, N, K/2] bytes; SF swizzled per group (N x K each,
+ *               nvfp4_sf_bytes(N, K) bytes apart).
+ *   alpha       fp32 scalar applied to acc.
+ *   epilogue    NVFP4_EPI_SWIGLU_NVFP4: N columns interleaved 8|8 as gate/up;
+ *               h = silu(alpha*g) * (alpha*u) quantised as in nvfp4_quantize ->
+ *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
+ *               swizzled; h_debug NULL or fp32 [rows_max, N/2].
+ *               NVFP4_EPI_BF16: out_bf16 BF16 [rows_max, N].
+ * Limits: K a positive multiple of 256, N a positive multiple of 128, rows_max a
+ * positive multiple of 128, all pointers 16-byte aligned.
+ * -------------------------------------------------------------------------- */
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,
+                                const int32_t* group_offsets, const int32_t* group_counts,
+                                int32_t G, int32_t N, int32_t K, const uint8_t* b_q,
+                                const uint8_t* b_sf, float alpha, nvfp4_epilogue epilogue,
+                                uint8_t* out_q, uint8_t* out_sf, void* out_bf16,
+                                float* h_debug, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_moe_ffn_forward -- L1 GEMM with the fused SwiGLU + NVFP4 epilogue, then
+ * the L2 GEMM ("NVFP4 MegaMoE Debug Log", "NVFP4 MoE Pipeline"; the fused FP4
+ * epilogue planned in "NVFP4-1.1 Approach, Part 2").
+ *   a1_q, a1_sf, expert_offsets, expert_counts: as written by moe_route_permute.
+ *   w1_q, w1_sf  [E, 2I, H/2] with rows interleaved 8|8 (gate rows, then up rows,
+ *                per 16), SF per expert (2I x H).
+ *   w2_q, w2_sf  [E, H, I/2], SF per expert (H x I).
+ *   a2_q, a2_sf  [rows_max, I/2] and SF(rows_max x I): the re-quantised SwiGLU
+ *                output (written for real rows only).
+ *   rows_out     BF16 [rows_max, H]: alpha2 * L2 rows (real rows only).
+ *   h_debug      NULL or fp32 [rows_max, I] (pre-quantisation h).
+ * Limits: H and I positive multiples of 256, rows_max a positive multiple of 128.
+ * -------------------------------------------------------------------------- */
+nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
+                                   const int32_t* expert_offsets, const int32_t* expert_counts,
+                                   int32_t E, int32_t H, int32_t I, int64_t rows_max,
+                                   const uint8_t* w1_q, const uint8_t* w1_sf,
+                                   const uint8_t* w2_q, const uint8_t* w2_sf, float alpha1,
+                                   float alpha2, uint8_t* a2_q, uint8_t* a2_sf,
+                                   void* rows_out_bf16, float* h_debug, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_combine -- "scatter with routing weights" ("NVFP4 MegaMoE Debug Log",
+ * "NVFP4 MoE Pipeline"): y[t, :] = bf16( sum_{j < top_k} w[t, j] * rows[inv_perm[t, j], :] ),
+ * accumulated in fp32 in slot order.
+ *   rows_bf16   BF16 [*, H]; inv_perm int32 [T, top_k]; topk_w fp32 [T, top_k];
+ *   y_bf16      BF16 [T, H].  H a positive multiple of 8; pointers 16-byte aligned.
+ * -------------------------------------------------------------------------- */
+nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w,
+                         int32_t T, int32_t H, int32_t top_k, void* y_bf16,
+                         nvfp4_stream_t stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* nvfp4_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error word:
+ * NVFP4_OK, NVFP4_ERR_TIMEOUT (a bounded wait gave up), NVFP4_ERR_DEVICE (an index
+ * check failed) or NVFP4_ERR_CUDA (the stream itself reported an error). */
+nvfp4_status nvfp4_device_status(nvfp4_stream_t stream);
+
+/* Self-test of the failure path: launches one warp that waits on *flag (device
+ * int32) until it becomes non-zero or `limit_ns` nanoseconds pass, then records a
+ * timeout in the error word and returns.  Nothing in the library sets *flag. */
+nvfp4_status nvfp4_selftest_bounded_wait(const int32_t* flag, int64_t limit_ns,
+                                         nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

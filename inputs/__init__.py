@@ -25,6 +25,7 @@ prefill    T=16384, rest as decode, logits N(0,1) + 1.5 ln(Zipf(1.2) rank
 
 Activations are N(0,1) rounded to BF16, weights N(0,0.02) fp32 (the weights
 are quantised to NVFP4 by each side's own quantiser), router logits fp32.
+Expert weights come from one seeded pool (``moe_weight_pool``).
 """
 from __future__ import annotations
 
@@ -85,17 +86,60 @@ def moe_x(spec: dict):
     return to_bf16(a)
 
 
+POOL_MAX = 1 << 26          # values in the shared weight pool of the large workloads
+
+
+def moe_weight_pool(spec: dict):
+    """Expert weights are windows of one seeded N(0,1) fp32 pool.
+
+    Returns (pool, w1_off [E], w2_off [E]); expert e's W1 is
+    pool[w1_off[e] : w1_off[e] + 2I*H] * 0.02 viewed as [2I, H], W2 likewise
+    [H, I].  When all experts fit in POOL_MAX values the windows are disjoint
+    (every weight an independent draw); above that (the 256-expert workloads,
+    11.3 G weights) the windows sit at seeded offsets in a 2^26-value pool and
+    overlap, which keeps each window N(0, 0.02) while making the draw cheap.
+    The pool carries one window's worth of wrap-around so every window is a
+    contiguous slice.
+    """
+    key = (spec["seed"], spec["E"], spec["H"], spec["I"])
+    hit = _POOL_CACHE.get(key)
+    if hit is not None:
+        return hit
+    E, H, I = spec["E"], spec["H"], spec["I"]
+    n1, n2 = 2 * I * H, H * I
+    total = E * (n1 + n2)
+    if total <= POOL_MAX:
+        pool = _rng(spec["seed"], _W1).standard_normal(total, dtype=np.float32)
+        w1_off = np.arange(E, dtype=np.int64) * n1
+        w2_off = E * n1 + np.arange(E, dtype=np.int64) * n2
+    else:
+        base = _rng(spec["seed"], _W1).standard_normal(POOL_MAX, dtype=np.float32)
+        pool = np.concatenate([base, base[:max(n1, n2)]])
+        orng = _rng(spec["seed"], _W2)
+        w1_off = orng.integers(0, POOL_MAX, size=E, dtype=np.int64)
+        w2_off = orng.integers(0, POOL_MAX, size=E, dtype=np.int64)
+    _POOL_CACHE.clear()
+    _POOL_CACHE[key] = (pool, w1_off, w2_off)
+    return _POOL_CACHE[key]
+
+
+_POOL_CACHE: dict = {}
+WEIGHT_STD = np.float32(0.02)
+
+
 def moe_w1(spec: dict, e: int) -> np.ndarray:
     """fp32 [2I, H] for expert e; rows are already interleaved 8|8 (rows 16g..16g+7
     are gate rows 8g..8g+7, rows 16g+8..16g+15 the matching up rows)."""
-    return (_rng(spec["seed"], _W1, e).standard_normal((2 * spec["I"], spec["H"]),
-                                                        dtype=np.float32) * np.float32(0.02))
+    pool, w1_off, _ = moe_weight_pool(spec)
+    n = 2 * spec["I"] * spec["H"]
+    return (pool[w1_off[e]:w1_off[e] + n] * WEIGHT_STD).reshape(2 * spec["I"], spec["H"])
 
 
 def moe_w2(spec: dict, e: int) -> np.ndarray:
     """fp32 [H, I] for expert e."""
-    return (_rng(spec["seed"], _W2, e).standard_normal((spec["H"], spec["I"]),
-                                                        dtype=np.float32) * np.float32(0.02))
+    pool, _, w2_off = moe_weight_pool(spec)
+    n = spec["H"] * spec["I"]
+    return (pool[w2_off[e]:w2_off[e] + n] * WEIGHT_STD).reshape(spec["H"], spec["I"])
 
 
 def moe_all_weights(spec: dict):

@@ -1,0 +1,158 @@
+"""Python binding of libnvfp4moe.so, the GB300 (sm_103a) NVFP4 MoE expert FFN.
+
+Argument marshalling only: every function here passes device pointers, sizes
+and the current CUDA stream to the C ABI declared in ``include/nvfp4moe.h``
+and raises ``Nvfp4Error`` on a non-zero status.  Every step of the path runs in
+the library's CUDA kernels; there is no CPU fallback, and importing a function
+fails loudly when the library is not built.
+
+PyTorch provides device memory and streams (``torch.cuda.current_stream()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "Nvfp4Error", "lib_path", "load", "sf_bytes", "moe_padded_rows_max",
+    "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
+    "moe_route_permute", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
+    "moe_combine", "nvfp4_device_status", "nvfp4_selftest_bounded_wait",
+    "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
+]
+
+MODE_PLAIN, MODE_SWIGLU_GU8 = 0, 1
+IN_BF16, IN_F32 = 0, 1
+EPI_SWIGLU_NVFP4, EPI_BF16 = 0, 1
+
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CUDA", 5: "TIMEOUT", 6: "DEVICE"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libnvfp4moe.so")
+
+
+_vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "nvfp4_sf_bytes": (_sz, [_i64, _i64]),
+    "moe_padded_rows_max": (_i64, [_i32, _i32, _i32]),
+    "moe_route_permute_workspace": (_sz, [_i32, _i32, _i32, _i32]),
+    "nvfp4_quantize": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "nvfp4_sf_swizzle": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i64, _vp, ctypes.c_int, _vp]),
+    "moe_route_permute": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _sz, _vp]),
+    "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _f32,
+                                          ctypes.c_int, _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_moe_ffn_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp,
+                                             _f32, _f32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "nvfp4_last_error": (ctypes.c_char_p, []),
+    "nvfp4_device_status": (ctypes.c_int, [_vp]),
+    "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
+}
+
+
+def load():
+    """Load the in-tree library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m nvfp4_block_scaled_moe_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise Nvfp4Error(status, load().nvfp4_last_error().decode())
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ----------------------------------------------------------------- sizes --
+def sf_bytes(rows: int, cols: int) -> int:
+    return load().nvfp4_sf_bytes(rows, cols)
+
+
+def moe_padded_rows_max(T: int, E: int, top_k: int) -> int:
+    return load().moe_padded_rows_max(T, E, top_k)
+
+
+def moe_route_permute_workspace(T: int, H: int, E: int, top_k: int) -> int:
+    return load().moe_route_permute_workspace(T, H, E, top_k)
+
+
+# ----------------------------------------------------------------- calls --
+def nvfp4_quantize(inp, out_cols, mode, q_out, sf_out, h_debug=None, in_ld=None, stream=None):
+    """inp: BF16 or fp32 [rows, in_cols] CUDA tensor (rows may be strided)."""
+    dtype = IN_BF16 if inp.dtype == torch.bfloat16 else IN_F32
+    ld = inp.stride(0) if in_ld is None else in_ld
+    _check(load().nvfp4_quantize(_p(inp), dtype, mode, inp.shape[0], out_cols, ld, _p(q_out), _p(sf_out),
+                                 _p(h_debug), _stream(stream)))
+
+
+def nvfp4_sf_swizzle(sf_in, mn_rows, k_sf_cols, stride_mn, stride_ksf, sf_out, inverse=False, stream=None):
+    _check(load().nvfp4_sf_swizzle(_p(sf_in), mn_rows, k_sf_cols, stride_mn, stride_ksf, _p(sf_out),
+                                   1 if inverse else 0, _stream(stream)))
+
+
+def moe_route_permute(logits, x, top_k, topk_ids, topk_w, expert_counts, expert_offsets, perm_token, inv_perm,
+                      a1_q, a1_sf, workspace, stream=None):
+    T, E = logits.shape
+    H = x.shape[1]
+    _check(load().moe_route_permute(_p(logits), _p(x), T, H, E, top_k, _p(topk_ids), _p(topk_w),
+                                    _p(expert_counts), _p(expert_offsets), _p(perm_token), _p(inv_perm),
+                                    _p(a1_q), _p(a1_sf), _p(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)))
+
+
+def nvfp4_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, alpha, epilogue,
+                       out_q=None, out_sf=None, out_bf16=None, h_debug=None, stream=None):
+    _check(load().nvfp4_grouped_gemm(_p(a_q), _p(a_sf), rows_max, _p(group_offsets), _p(group_counts), G, N, K,
+                                     _p(b_q), _p(b_sf), alpha, epilogue, _p(out_q), _p(out_sf), _p(out_bf16),
+                                     _p(h_debug), _stream(stream)))
+
+
+def nvfp4_moe_ffn_forward(a1_q, a1_sf, expert_offsets, expert_counts, E, H, I, rows_max, w1_q, w1_sf, w2_q, w2_sf,
+                          alpha1, alpha2, a2_q, a2_sf, rows_out, h_debug=None, stream=None):
+    _check(load().nvfp4_moe_ffn_forward(_p(a1_q), _p(a1_sf), _p(expert_offsets), _p(expert_counts), E, H, I,
+                                        rows_max, _p(w1_q), _p(w1_sf), _p(w2_q), _p(w2_sf), alpha1, alpha2,
+                                        _p(a2_q), _p(a2_sf), _p(rows_out), _p(h_debug), _stream(stream)))
+
+
+def moe_combine(rows, inv_perm, topk_w, y, stream=None):
+    T, top_k = inv_perm.shape
+    H = y.shape[1]
+    _check(load().moe_combine(_p(rows), _p(inv_perm), _p(topk_w), T, H, top_k, _p(y), _stream(stream)))
+
+
+def nvfp4_device_status(stream=None):
+    _check(load().nvfp4_device_status(_stream(stream)))
+
+
+def nvfp4_selftest_bounded_wait(flag, limit_ns, stream=None):
+    _check(load().nvfp4_selftest_bounded_wait(_p(flag), limit_ns, _stream(stream)))

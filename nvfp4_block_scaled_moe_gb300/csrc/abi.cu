@@ -1,0 +1,270 @@
+// The extern "C" boundary of libnvfp4moe.so: argument checks (before any CUDA
+// call), status codes, thread-local error messages, the per-device error word
+// and the bounded-wait self-test.  Compute lives in quantize.cu, route.cu and
+// gemm.cu.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+__device__ unsigned g_error_word;
+
+static thread_local char g_msg[512] = "";
+
+nvfp4_status fail(nvfp4_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+nvfp4_status fail_cuda(cudaError_t e, const char* where) {
+  return fail(NVFP4_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+unsigned* device_error_word() {
+  static unsigned* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) addr[dev] = static_cast<unsigned*>(p);
+  }
+  return addr[dev];
+}
+
+__global__ void selftest_wait_kernel(const volatile int32_t* flag, int64_t limit_ns, unsigned* err) {
+  if (threadIdx.x != 0) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (*flag == 0) {
+    if (globaltimer_ns() - t0 > static_cast<uint64_t>(limit_ns)) {
+      raise_error(err, kErrTimeout);
+      return;
+    }
+  }
+}
+
+cudaError_t selftest_wait_launch(const int32_t* flag, int64_t limit_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(flag, limit_ns, device_error_word());
+  return cudaGetLastError();
+}
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+#define CHECK_ARG(cond, ...)                                         \
+  do {                                                               \
+    if (!(cond)) return fail(NVFP4_ERR_INVALID_ARG, __VA_ARGS__);   \
+  } while (0)
+#define CHECK_SUP(cond, ...)                                         \
+  do {                                                               \
+    if (!(cond)) return fail(NVFP4_ERR_UNSUPPORTED, __VA_ARGS__);   \
+  } while (0)
+#define CHECK_AL(cond, ...)                                          \
+  do {                                                               \
+    if (!(cond)) return fail(NVFP4_ERR_ALIGNMENT, __VA_ARGS__);     \
+  } while (0)
+
+extern "C" {
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 63) / 64) * 512u;
+}
+
+int64_t moe_padded_rows_max(int32_t T, int32_t E, int32_t top_k) {
+  if (T <= 0 || E <= 0 || top_k <= 0) return 0;
+  const int64_t routed = static_cast<int64_t>(T) * top_k;
+  const int64_t groups = routed < E ? routed : E;
+  return ((routed + 127 * groups) / 128) * 128;
+}
+
+size_t moe_route_permute_workspace(int32_t T, int32_t H, int32_t E, int32_t top_k) {
+  (void)top_k;
+  if (T < 0 || H <= 0 || E <= 0) return 0;
+  const size_t n_chunks = (static_cast<size_t>(T) + kRouteChunk - 1) / kRouteChunk;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  return up(n_chunks * E * sizeof(int32_t)) + up(static_cast<size_t>(T) * H / 2) + up(static_cast<size_t>(T) * H / 16) + 256;
+}
+
+const char* nvfp4_last_error(void) { return g_msg; }
+
+nvfp4_status nvfp4_quantize(const void* in, nvfp4_in_dtype dtype, nvfp4_quant_mode mode, int64_t rows,
+                            int64_t out_cols, int64_t in_ld_elems, uint8_t* q_out, uint8_t* sf_out,
+                            float* h_debug, nvfp4_stream_t stream) {
+  CHECK_ARG(in && q_out && sf_out, "nvfp4_quantize: null pointer");
+  CHECK_ARG(dtype == NVFP4_IN_BF16 || dtype == NVFP4_IN_F32, "nvfp4_quantize: bad dtype %d", (int)dtype);
+  CHECK_ARG(mode == NVFP4_MODE_PLAIN || mode == NVFP4_MODE_SWIGLU_GU8, "nvfp4_quantize: bad mode %d", (int)mode);
+  CHECK_ARG(rows > 0 && out_cols > 0, "nvfp4_quantize: rows and out_cols must be positive");
+  CHECK_SUP(out_cols % 16 == 0, "nvfp4_quantize: out_cols=%lld is not a multiple of 16", (long long)out_cols);
+  CHECK_SUP(mode == NVFP4_MODE_PLAIN || dtype == NVFP4_IN_BF16, "nvfp4_quantize: SWIGLU_GU8 takes BF16 input");
+  const int64_t in_cols = mode == NVFP4_MODE_SWIGLU_GU8 ? 2 * out_cols : out_cols;
+  CHECK_ARG(in_ld_elems >= in_cols, "nvfp4_quantize: in_ld_elems=%lld < %lld", (long long)in_ld_elems,
+            (long long)in_cols);
+  const int64_t esize = dtype == NVFP4_IN_BF16 ? 2 : 4;
+  CHECK_AL(al16(in) && (in_ld_elems * esize) % 16 == 0, "nvfp4_quantize: input not 16-byte aligned");
+  CHECK_AL((reinterpret_cast<uintptr_t>(q_out) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sf_out) & 3u) == 0,
+           "nvfp4_quantize: outputs must be 4-byte aligned");
+  CHECK_AL(h_debug == nullptr || al16(h_debug), "nvfp4_quantize: h_debug not 16-byte aligned");
+  cudaError_t e = quantize_launch(in, dtype, mode, rows, out_cols, in_ld_elems, q_out, sf_out, 0, h_debug,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_quantize");
+}
+
+nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_sf_cols, int64_t stride_mn,
+                              int64_t stride_ksf, uint8_t* sf_out, int inverse, nvfp4_stream_t stream) {
+  CHECK_ARG(sf_in && sf_out, "nvfp4_sf_swizzle: null pointer");
+  CHECK_ARG(mn_rows > 0 && k_sf_cols > 0, "nvfp4_sf_swizzle: sizes must be positive");
+  CHECK_ARG(stride_mn > 0 && stride_ksf > 0, "nvfp4_sf_swizzle: strides must be positive");
+  CHECK_AL(inverse || (reinterpret_cast<uintptr_t>(sf_out) & 3u) == 0,
+           "nvfp4_sf_swizzle: swizzled output must be 4-byte aligned");
+  cudaError_t e = sf_swizzle_launch(sf_in, mn_rows, k_sf_cols, stride_mn, stride_ksf, sf_out, inverse,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_sf_swizzle");
+}
+
+nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t T, int32_t H, int32_t E,
+                               int32_t top_k, int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
+                               int32_t* expert_offsets, int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
+                               uint8_t* a1_sf, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  CHECK_ARG(T >= 0, "moe_route_permute: T=%d", T);
+  CHECK_ARG(expert_counts && expert_offsets && workspace, "moe_route_permute: null pointer");
+  CHECK_ARG(T == 0 || (logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_q && a1_sf),
+            "moe_route_permute: null pointer");
+  CHECK_SUP(E >= 1 && E <= 1024, "moe_route_permute: E=%d outside [1, 1024]", E);
+  CHECK_SUP(top_k >= 1 && top_k <= E && top_k <= 32, "moe_route_permute: top_k=%d outside [1, min(E, 32)]", top_k);
+  CHECK_SUP(H > 0 && H % 64 == 0, "moe_route_permute: H=%d is not a positive multiple of 64", H);
+  CHECK_AL(al16(workspace) && (T == 0 || (al16(x_bf16) && al16(a1_q) && al16(a1_sf))),
+           "moe_route_permute: x, a1_q, a1_sf and workspace must be 16-byte aligned");
+  const size_t need = moe_route_permute_workspace(T, H, E, top_k);
+  CHECK_ARG(workspace_bytes >= need, "moe_route_permute: workspace %zu < %zu bytes", workspace_bytes, need);
+  RouteBuffers b;
+  b.logits = logits;
+  b.x = x_bf16;
+  b.T = T;
+  b.H = H;
+  b.E = E;
+  b.top_k = top_k;
+  b.topk_ids = topk_ids;
+  b.topk_w = topk_w;
+  b.counts = expert_counts;
+  b.offsets = expert_offsets;
+  b.perm_token = perm_token;
+  b.inv_perm = inv_perm;
+  b.a1_q = a1_q;
+  b.a1_sf = a1_sf;
+  b.rows_max = moe_padded_rows_max(T, E, top_k);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t n_chunks = (static_cast<size_t>(T) + kRouteChunk - 1) / kRouteChunk;
+  b.chunk_hist = reinterpret_cast<int32_t*>(ws);
+  ws += up(n_chunks * E * sizeof(int32_t));
+  b.x_q = ws;
+  ws += up(static_cast<size_t>(T) * H / 2);
+  b.x_sf = ws;
+  cudaError_t e = route_permute_launch(b, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_route_permute");
+}
+
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,
+                                const int32_t* group_offsets, const int32_t* group_counts, int32_t G, int32_t N,
+                                int32_t K, const uint8_t* b_q, const uint8_t* b_sf, float alpha,
+                                nvfp4_epilogue epilogue, uint8_t* out_q, uint8_t* out_sf, void* out_bf16,
+                                float* h_debug, nvfp4_stream_t stream) {
+  CHECK_ARG(a_q && a_sf && b_q && b_sf, "nvfp4_grouped_gemm: null operand");
+  CHECK_ARG(epilogue == NVFP4_EPI_SWIGLU_NVFP4 || epilogue == NVFP4_EPI_BF16, "nvfp4_grouped_gemm: bad epilogue");
+  CHECK_ARG(epilogue != NVFP4_EPI_SWIGLU_NVFP4 || (out_q && out_sf), "nvfp4_grouped_gemm: null NVFP4 output");
+  CHECK_ARG(epilogue != NVFP4_EPI_BF16 || out_bf16, "nvfp4_grouped_gemm: null BF16 output");
+  CHECK_ARG(group_offsets || !group_counts, "nvfp4_grouped_gemm: group_counts needs group_offsets");
+  CHECK_ARG(G >= 1 && N > 0 && K > 0 && rows_max > 0, "nvfp4_grouped_gemm: sizes must be positive");
+  CHECK_SUP(group_offsets || G == 1, "nvfp4_grouped_gemm: NULL group_offsets means G == 1");
+  CHECK_SUP(K % 256 == 0, "nvfp4_grouped_gemm: K=%d is not a multiple of 256", K);
+  CHECK_SUP(N % 128 == 0, "nvfp4_grouped_gemm: N=%d is not a multiple of 128", N);
+  CHECK_SUP(rows_max % 128 == 0 && rows_max < (int64_t(1) << 31), "nvfp4_grouped_gemm: rows_max=%lld",
+            (long long)rows_max);
+  CHECK_SUP(static_cast<int64_t>(G) * N < (int64_t(1) << 31), "nvfp4_grouped_gemm: G*N too large");
+  CHECK_AL(al16(a_q) && al16(a_sf) && al16(b_q) && al16(b_sf), "nvfp4_grouped_gemm: operands not 16-byte aligned");
+  CHECK_AL((!out_q || al16(out_q)) && (!out_sf || al16(out_sf)) && (!out_bf16 || al16(out_bf16)) &&
+               (!h_debug || al16(h_debug)),
+           "nvfp4_grouped_gemm: outputs not 16-byte aligned");
+  GemmArgs a;
+  a.a_q = a_q;
+  a.a_sf = a_sf;
+  a.rows_max = rows_max;
+  a.offsets = group_offsets;
+  a.counts = group_counts;
+  a.G = G;
+  a.N = N;
+  a.K = K;
+  a.b_q = b_q;
+  a.b_sf = b_sf;
+  a.alpha = alpha;
+  a.epilogue = epilogue;
+  a.out_q = out_q;
+  a.out_sf = out_sf;
+  a.out_bf16 = out_bf16;
+  a.h_debug = h_debug;
+  return gemm_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf, const int32_t* expert_offsets,
+                                   const int32_t* expert_counts, int32_t E, int32_t H, int32_t I, int64_t rows_max,
+                                   const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
+                                   const uint8_t* w2_sf, float alpha1, float alpha2, uint8_t* a2_q, uint8_t* a2_sf,
+                                   void* rows_out_bf16, float* h_debug, nvfp4_stream_t stream) {
+  CHECK_ARG(expert_offsets && expert_counts, "nvfp4_moe_ffn_forward: null expert offsets/counts");
+  CHECK_ARG(a2_q && a2_sf && rows_out_bf16, "nvfp4_moe_ffn_forward: null output");
+  CHECK_SUP(H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0,
+            "nvfp4_moe_ffn_forward: H=%d and I=%d must be positive multiples of 256", H, I);
+  nvfp4_status st = nvfp4_grouped_gemm(a1_q, a1_sf, rows_max, expert_offsets, expert_counts, E, 2 * I, H, w1_q,
+                                       w1_sf, alpha1, NVFP4_EPI_SWIGLU_NVFP4, a2_q, a2_sf, nullptr, h_debug,
+                                       stream);
+  if (st != NVFP4_OK) return st;
+  return nvfp4_grouped_gemm(a2_q, a2_sf, rows_max, expert_offsets, expert_counts, E, H, I, w2_q, w2_sf, alpha2,
+                            NVFP4_EPI_BF16, nullptr, nullptr, rows_out_bf16, nullptr, stream);
+}
+
+nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w, int32_t T,
+                         int32_t H, int32_t top_k, void* y_bf16, nvfp4_stream_t stream) {
+  CHECK_ARG(T >= 0 && top_k >= 1, "moe_combine: T=%d top_k=%d", T, top_k);
+  CHECK_ARG(T == 0 || (rows_bf16 && inv_perm && topk_w && y_bf16), "moe_combine: null pointer");
+  CHECK_SUP(H > 0 && H % 8 == 0, "moe_combine: H=%d is not a positive multiple of 8", H);
+  CHECK_AL(T == 0 || (al16(rows_bf16) && al16(y_bf16)), "moe_combine: rows and y must be 16-byte aligned");
+  cudaError_t e = combine_launch(rows_bf16, inv_perm, topk_w, T, H, top_k, y_bf16,
+                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_combine");
+}
+
+nvfp4_status nvfp4_device_status(nvfp4_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "nvfp4_device_status: stream");
+  unsigned word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+  if (e != cudaSuccess) return fail_cuda(e, "nvfp4_device_status: read");
+  if (word == 0) return NVFP4_OK;
+  const unsigned zero = 0;
+  e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+  if (e != cudaSuccess) return fail_cuda(e, "nvfp4_device_status: clear");
+  if (word & kErrTimeout) return fail(NVFP4_ERR_TIMEOUT, "device: a bounded wait timed out (word 0x%x)", word);
+  return fail(NVFP4_ERR_DEVICE, "device: an index check failed (word 0x%x)", word);
+}
+
+nvfp4_status nvfp4_selftest_bounded_wait(const int32_t* flag, int64_t limit_ns, nvfp4_stream_t stream) {
+  CHECK_ARG(flag != nullptr, "nvfp4_selftest_bounded_wait: null flag");
+  CHECK_ARG(limit_ns > 0 && limit_ns <= 10000000000ll, "nvfp4_selftest_bounded_wait: limit_ns outside (0, 10 s]");
+  cudaError_t e = selftest_wait_launch(flag, limit_ns, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_selftest_bounded_wait");
+}
+
+}  // extern "C"

@@ -1,0 +1,299 @@
+// Device helpers shared by the NVFP4 MoE kernels (sm_103a): NVFP4 numerics,
+// bounded mbarrier waits, TMA / bulk copies and tcgen05 (TMEM, block-scaled MMA)
+// wrappers written as inline PTX.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// ------------------------------------------------------------ error word --
+// Bits of the per-device error word (a __device__ variable owned by abi.cu,
+// passed to kernels as a pointer).
+enum : unsigned { kErrTimeout = 1u, kErrBounds = 2u };
+
+// A bounded wait gives up after this long; no legitimate wait in these kernels
+// comes within orders of magnitude of it.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+__device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
+  if (err != nullptr) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// --------------------------------------------------------- NVFP4 numerics --
+// E4M3 encode of a non-negative fp32 with round-to-nearest-even and saturation
+// to 448 (cvt ... satfinite never produces the exp=15/mant=7 NaN for finite input).
+__device__ __forceinline__ uint32_t e4m3_from_f32(float x) {
+  uint16_t packed;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(packed) : "f"(0.0f), "f"(x));
+  return packed & 0xFFu;   // the second source operand lands in the low byte
+}
+
+// Exact value of a non-negative E4M3 code (bias 7; e == 0 is m * 2^-9).
+__device__ __forceinline__ float f32_from_e4m3(uint32_t code) {
+  const uint32_t e = (code >> 3) & 0xFu, m = code & 7u;
+  return e == 0 ? static_cast<float>(m) * 0.001953125f
+                : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Pack eight half-step values (each a signed multiple of 0.5 in [-6, 6]) into
+// eight E2M1 nibbles, element 2i in the low nibble of byte i.  Every input is
+// already on the half-step grid, so the conversion's round-to-nearest-even only
+// resolves the grid ties 2.5 -> 2, 3.5 -> 4, 5 -> 4 (ties to the even mantissa).
+__device__ __forceinline__ uint32_t e2m1x8_from_halfsteps(const float (&v)[8]) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return out;
+}
+
+// Block scale of a 16-block from its amax: E4M3(fp32(amax / 6)).
+struct BlockScale {
+  uint32_t code;  // E4M3 byte
+  float d;        // decoded scale (0 for a zero scale)
+  float r;        // correctly rounded 1/d, 0 for a zero scale
+};
+
+__device__ __forceinline__ BlockScale block_scale(float amax) {
+  BlockScale s;
+  s.code = e4m3_from_f32(__fdiv_rn(amax, 6.0f));
+  s.d = f32_from_e4m3(s.code);
+  s.r = s.d > 0.0f ? __frcp_rn(s.d) : 0.0f;
+  return s;
+}
+
+// Signed half step of x / d: copysign(rne(2 * min(|x / d|, 6)) / 2, x).
+// |x| / d is the IEEE-correctly-rounded fp32 quotient, obtained from the
+// correctly rounded reciprocal r with one FMA residual correction (Markstein's
+// division theorem: q' = RN(q + (a - b q) y) equals RN(a / b) when y = RN(1/b)
+// and q is within one ulp).  With d == 0 (r == 0) the magnitude is 0.
+__device__ __forceinline__ float signed_halfstep(float x, const BlockScale& s) {
+  const float a = fabsf(x);
+  const float q0 = a * s.r;
+  const float rem = fmaf(-q0, s.d, a);
+  const float q = fmaf(rem, s.r, q0);
+  const float hs = rintf(fminf(q, 6.0f) * 2.0f);
+  return copysignf(hs * 0.5f, x);
+}
+
+// Quantise eight values of one half-block with that block's scale.
+__device__ __forceinline__ uint32_t quantize8(const float (&h)[8], const BlockScale& s) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = signed_halfstep(h[i], s);
+  return e2m1x8_from_halfsteps(v);
+}
+
+// silu(g) * u with the fast exponential (the SwiGLU of the L1 epilogue).
+__device__ __forceinline__ float swiglu(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// Byte offset of the SF word holding scales (row, 4*k4 .. 4*k4+3) in the
+// swizzled layout with k4_total 64-element column groups.
+__device__ __forceinline__ uint64_t sf_word_offset(uint64_t row, uint32_t k4, uint32_t k4_total) {
+  return ((row >> 7) * k4_total + k4) * 512ull + (row & 31u) * 16u + ((row >> 5) & 3u) * 4u;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& w, float (&f)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// ------------------------------------------------------------- mbarriers --
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase of `bar` with the given parity, but never forever: give up
+// when *abort is set by another role, or after kWaitLimitNs (then set *abort and
+// the timeout bit).  Returns true if the phase completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         unsigned* err, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        raise_error(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------- TMA / bulk --
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// 2-D tiled load; x (innermost, in elements) must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Contiguous global -> shared copy; both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05 --
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Copy a 32-row x 16-byte shared-memory tile into TMEM, replicated to all four
+// 32-lane groups (the scale-factor staging of the block-scaled MMA).
+__device__ __forceinline__ void tc_copy_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T, E2M1 x E2M1 with one UE4M3 scale per 16 K
+// elements of A rows (sfa_tmem) and B rows (sfb_tmem); K = 64 per instruction.
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Load 32 consecutive fp32 columns of this thread's TMEM lane and wait for them.
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format, version 1) for a K-major
+// operand tile written by TMA with 128-byte swizzle: 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;             // leading offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;     // stride between 8-row groups
+  d |= static_cast<uint64_t>(1u) << 46;             // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;             // 128-byte swizzle
+  return d;
+}
+
+// Descriptor for a scale-factor atom: unswizzled 8 x 16-byte core matrices,
+// consecutive along M|N, 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format code 1), both
+// K-major, UE4M3 scales, scale-factor ids 0, dense K = 64.
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t m, uint32_t n) {
+  return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+}  // namespace nvfp4

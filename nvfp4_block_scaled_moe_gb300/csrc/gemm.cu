@@ -1,0 +1,405 @@
+// Block-scaled NVFP4 grouped GEMM on the sm_100-family tensor cores (tcgen05),
+// with two fused epilogues:
+//   * SwiGLU + NVFP4 re-quantisation (the L1 "fused_swiglu" kernel of "NVFP4-1.1
+//     Approach, Part 2", in the fp4 mode the pages planned but could not build:
+//     gate subtile -> SiLU in registers, up subtile -> SwiGLU, every 16 values ->
+//     amax, E4M3 scale, E2M1 nibbles, written straight to global memory with the
+//     scales in the swizzled MMA layout);
+//   * alpha * acc -> BF16 rows (the L2 GEMM).
+//
+// Shape of the work: a tile is 128 rows x 128 columns of the output; the K loop
+// runs in stages of 256 elements (128 bytes of E2M1 per row = one 128-byte
+// swizzle row).  Rows are grouped (experts): group g owns rows
+// [offsets[g], offsets[g+1]) (multiples of 128) and multiplies with B_g.
+//
+// One persistent CTA per SM, 6 warps, warp-specialised:
+//   warp 0     TMA producer: A and B tiles (2-D tensor maps, 128-byte swizzle) and
+//              the scale-factor atoms (contiguous 2 KiB bulk copies) into a
+//              6-stage shared-memory ring;
+//   warp 1     TMEM owner and MMA issuer: copies the stage's scale atoms into
+//              TMEM (tcgen05.cp 32x128b.warpx4) and issues four
+//              tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X (M=128, N=128,
+//              K=64) per stage into a double-buffered fp32 accumulator;
+//   warps 2-5  epilogue: tcgen05.ld 32x32b (one TMEM lane = one output row per
+//              thread, so a 16-block's amax needs no shuffles), math, stores.
+// Lessons kept from the pages' pipeline notes: the first MMA of a tile does not
+// accumulate; only the warps that need the TMEM address wait for it; barrier
+// arrival counts are in the units that actually arrive.
+// Every wait is bounded (a timeout sets the error word and lets the CTA exit).
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 256;         // elements
+constexpr int kStages = 6;
+constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
+constexpr uint32_t kBBytes = kBN * kBK / 2;            // 16 KiB
+constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms of 512 B
+constexpr uint32_t kSfbBytes = kBN * (kBK / 16);       // 2 KiB
+constexpr uint32_t kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr int kMaxGroups = 1024;
+
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
+constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
+constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;     // full, empty, tfull[2], tempty[2], drain
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
+constexpr uint32_t kOffGroups = kOffMisc + 16;
+constexpr uint32_t kSmemBytes = kOffGroups + (kMaxGroups + 1) * 4 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// TMEM columns: two 128-column fp32 accumulators, then per stage 16 columns of
+// A scales (4 atoms x 4 columns) and 16 of B scales.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemSf = 2 * kBN;
+static_assert(kTmemSf + kStages * 32 <= kTmemCols, "TMEM budget");
+
+struct Params {
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  const int32_t* offsets;
+  const int32_t* counts;
+  int32_t G, N, K;
+  int32_t n_tiles, k_blocks;
+  int64_t rows_max;
+  int64_t sfb_group_bytes;
+  float alpha;
+  uint8_t* out_q;
+  uint8_t* out_sf;
+  __nv_bfloat16* out_bf16;
+  float* h_debug;
+  unsigned* err;
+};
+
+__device__ __forceinline__ int find_group(const int32_t* off, int G, int64_t row) {
+  int lo = 0, hi = G;                 // last g < G with off[g] <= row
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= row) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int kEpi>
+__global__ void __launch_bounds__(192, 1)
+    nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kOffGroups);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);      // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i <= p.G; i += blockDim.x)
+    s_off[i] = p.offsets != nullptr ? __ldg(p.offsets + i) : (i == 0 ? 0 : static_cast<int32_t>(p.rows_max));
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // the grouped rows must be a 128-aligned prefix of the allocation
+  const int64_t total_rows = s_off[p.G];
+  int64_t num_tiles = 0;
+  if (total_rows >= 0 && total_rows <= p.rows_max && (total_rows % kBM) == 0) {
+    num_tiles = (total_rows / kBM) * p.n_tiles;
+  } else if (threadIdx.x == 0) {
+    raise_error(p.err, kErrBounds);
+  }
+  const int32_t k4 = p.K / 64;        // scale atoms per 128-row band
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, filled = 0, fill_parity = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int64_t mt = tile / p.n_tiles;
+        const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
+        const int g = find_group(s_off, p.G, mt * kBM);
+        const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
+        const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(nt) * k4) * 512;
+        for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], kStageTx);
+          tma_load_2d(smem + kOffA + stage * kABytes, &tmap_a, &full[stage], kb * (kBK / 2),
+                      static_cast<int32_t>(mt * kBM));
+          tma_load_2d(smem + kOffB + stage * kBBytes, &tmap_b, &full[stage], kb * (kBK / 2),
+                      g * p.N + nt * kBN);
+          bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa + kb * 4 * 512, kSfaBytes, &full[stage]);
+          bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb + kb * 4 * 512, kSfbBytes, &full[stage]);
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA can exit
+        int no_abort = 0;
+        for (int s = 0; s < kStages; ++s)
+          if ((filled >> s) & 1u) mbar_wait(&full[s], (fill_parity >> s) & 1u, &no_abort, nullptr, 50000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t sfa_t = tmem_base + kTmemSf + stage * 32;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+          const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_copy_sf(sfa_t + 4 * j, sdesc_sf(sfa_s + 512 * j));
+            tc_copy_sf(sfb_t + 4 * j, sdesc_sf(sfb_s + 512 * j));
+          }
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + kOffA + stage * kABytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + kOffB + stage * kBBytes));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // K advance of 64 E2M1 = 32 bytes inside the 128-byte swizzle row
+            tc_mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 4 * j,
+                        (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // every MMA issued by this thread has completed before the CTA moves on
+      tc_commit(drain);
+      int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort, p.err, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t quad = warp & 3;                // TMEM lanes 32*quad .. +31
+    const uint32_t row_in_tile = quad * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int64_t mt = tile / p.n_tiles;
+      const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
+      const int64_t grow = mt * kBM + row_in_tile;
+      const int g = find_group(s_off, p.G, mt * kBM);
+      bool valid = true;
+      if (p.counts != nullptr) valid = (grow - s_off[g]) < __ldg(p.counts + g);
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + acc * kBN;
+      if constexpr (kEpi == NVFP4_EPI_SWIGLU_NVFP4) {
+        const int32_t out_cols = p.N / 2;
+        uint32_t sf_word = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_load32(t_row + 32 * c, v);
+          // columns: gate(8) up(8) gate(8) up(8) -> 16 consecutive outputs
+          float h0[8], h1[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            h0[i] = swiglu(p.alpha * v[i], p.alpha * v[8 + i]);
+            h1[i] = swiglu(p.alpha * v[16 + i], p.alpha * v[24 + i]);
+          }
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(h0[i]), fabsf(h1[i])));
+          const BlockScale s = block_scale(amax);
+          const uint32_t lo = quantize8(h0, s), hi = quantize8(h1, s);
+          sf_word |= s.code << (8 * c);
+          if (valid) {
+            const int64_t col = static_cast<int64_t>(nt) * 64 + 16 * c;
+            *reinterpret_cast<uint2*>(p.out_q + grow * (out_cols / 2) + col / 2) = make_uint2(lo, hi);
+            if (p.h_debug != nullptr) {
+              float4* hp = reinterpret_cast<float4*>(p.h_debug + grow * out_cols + col);
+              hp[0] = make_float4(h0[0], h0[1], h0[2], h0[3]);
+              hp[1] = make_float4(h0[4], h0[5], h0[6], h0[7]);
+              hp[2] = make_float4(h1[0], h1[1], h1[2], h1[3]);
+              hp[3] = make_float4(h1[4], h1[5], h1[6], h1[7]);
+            }
+          }
+        }
+        if (valid)
+          *reinterpret_cast<uint32_t*>(p.out_sf + sf_word_offset(grow, nt, p.n_tiles)) = sf_word;
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_load32(t_row + 32 * c, v);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + grow * p.N + static_cast<int64_t>(nt) * kBN + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 o;
+              o.x = pack_bf16x2(p.alpha * v[8 * q + 0], p.alpha * v[8 * q + 1]);
+              o.y = pack_bf16x2(p.alpha * v[8 * q + 2], p.alpha * v[8 * q + 3]);
+              o.z = pack_bf16x2(p.alpha * v[8 * q + 4], p.alpha * v[8 * q + 5]);
+              o.w = pack_bf16x2(p.alpha * v[8 * q + 6], p.alpha * v[8 * q + 7]);
+              dst[q] = o;
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// rows x row_bytes uint8 matrix, box of 128 bytes x box_rows rows, 128-byte swizzle
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool attr_set[2] = {false, false};
+};
+
+DeviceInfo& device_info(int dev) {
+  static DeviceInfo info[64];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = info[dev & 63];
+  if (d.sms == 0) cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  return d;
+}
+
+template <int kEpi>
+cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t stream,
+                   DeviceInfo& info) {
+  if (!info.attr_set[kEpi]) {
+    cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_kernel<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    info.attr_set[kEpi] = true;
+  }
+  nvf4_gemm_kernel<kEpi><<<grid, 192, kSmemBytes, stream>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
+  if (a.G > kMaxGroups) return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: G=%d exceeds %d", a.G, kMaxGroups);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  DeviceInfo& info = device_info(dev);
+  if (info.sms <= 0) return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: no SM count for device %d", dev);
+
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, a.a_q, static_cast<uint64_t>(a.rows_max), static_cast<uint64_t>(a.K) / 2, kBM) ||
+      !make_map(&mb, a.b_q, static_cast<uint64_t>(a.G) * a.N, static_cast<uint64_t>(a.K) / 2, kBN))
+    return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: cuTensorMapEncodeTiled failed");
+
+  Params p;
+  p.a_sf = a.a_sf;
+  p.b_sf = a.b_sf;
+  p.offsets = a.offsets;
+  p.counts = a.counts;
+  p.G = a.offsets != nullptr ? a.G : 1;
+  p.N = a.N;
+  p.K = a.K;
+  p.n_tiles = a.N / kBN;
+  p.k_blocks = a.K / kBK;
+  p.rows_max = a.rows_max;
+  p.sfb_group_bytes = static_cast<int64_t>(a.N / 128) * (a.K / 64) * 512;
+  p.alpha = a.alpha;
+  p.out_q = a.out_q;
+  p.out_sf = a.out_sf;
+  p.out_bf16 = static_cast<__nv_bfloat16*>(a.out_bf16);
+  p.h_debug = a.h_debug;
+  p.err = device_error_word();
+
+  const int64_t max_tiles = (a.rows_max / kBM) * p.n_tiles;
+  const int grid = static_cast<int>(max_tiles < info.sms ? max_tiles : info.sms);
+  if (grid <= 0) return NVFP4_OK;
+  e = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? launch<NVFP4_EPI_SWIGLU_NVFP4>(ma, mb, p, grid, stream, info)
+                                           : launch<NVFP4_EPI_BF16>(ma, mb, p, grid, stream, info);
+  if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm launch");
+  return NVFP4_OK;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,72 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nvfp4moe.h"
+
+namespace nvfp4 {
+
+// per-device error word (abi.cu): device address for the current device
+unsigned* device_error_word();
+
+cudaError_t quantize_launch(const void* in, int dtype, int mode, int64_t rows, int64_t cols, int64_t ld,
+                            uint8_t* q, uint8_t* sf, int sf_linear, float* h_dbg, cudaStream_t stream);
+
+cudaError_t sf_swizzle_launch(const uint8_t* in, int64_t mn_rows, int64_t k_sf, int64_t s_mn, int64_t s_k,
+                              uint8_t* out, int inverse, cudaStream_t stream);
+
+struct RouteBuffers {
+  const float* logits;
+  const void* x;
+  int32_t T, H, E, top_k;
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm_token;
+  int32_t* inv_perm;
+  uint8_t* a1_q;
+  uint8_t* a1_sf;
+  int64_t rows_max;
+  // workspace carve-up
+  int32_t* chunk_hist;   // [n_chunks, E]
+  uint8_t* x_q;          // [T, H/2]
+  uint8_t* x_sf;         // [T, H/16] row-major
+};
+
+constexpr int kRouteChunk = 128;   // tokens per routing block
+
+cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream);
+
+cudaError_t combine_launch(const void* rows, const int32_t* inv_perm, const float* w, int32_t T, int32_t H,
+                           int32_t top_k, void* y, cudaStream_t stream);
+
+struct GemmArgs {
+  const uint8_t* a_q;
+  const uint8_t* a_sf;
+  int64_t rows_max;
+  const int32_t* offsets;
+  const int32_t* counts;
+  int32_t G, N, K;
+  const uint8_t* b_q;
+  const uint8_t* b_sf;
+  float alpha;
+  int epilogue;
+  uint8_t* out_q;
+  uint8_t* out_sf;
+  void* out_bf16;
+  float* h_debug;
+};
+
+// Returns a status; writes a message with set_error_message on failure.
+nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
+
+cudaError_t selftest_wait_launch(const int32_t* flag, int64_t limit_ns, cudaStream_t stream);
+
+// error-message helpers (abi.cu)
+nvfp4_status fail(nvfp4_status st, const char* fmt, ...);
+nvfp4_status fail_cuda(cudaError_t e, const char* where);
+
+}  // namespace nvfp4

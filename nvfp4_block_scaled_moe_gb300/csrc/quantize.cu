@@ -1,0 +1,173 @@
+// Standalone NVFP4 quantiser (plain and SwiGLU-of-interleaved-gate/up modes)
+// and the scale-factor swizzle.
+//
+// "NVFP4-1.1 Approach, Part 2": the quantize_nvfp4 kernel (BF16 -> packed E2M1 +
+// E4M3 per 16) and the deinterleave + quantise kernel that reads L1 output
+// interleaved at granularity 8.  Here the SwiGLU mode computes silu(g) * u from
+// each gate/up pair in the same pass.  "NVFP4 MegaMoE Debug Log": the SF remap
+// (forward mapping with explicit source strides) for the swizzle kernel.
+//
+// Layout of the quantiser's work: one thread owns 8 consecutive output values
+// (16-byte loads of BF16, 32-byte of fp32 or gate+up), a lane pair owns one
+// 16-block (amax by one warp shuffle), a lane octet owns one 64-column group,
+// whose four scale bytes form one 32-bit word of the swizzled layout.
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+template <int kMode, int kDtype>
+__device__ __forceinline__ void load_values(const void* in, int64_t row, int64_t ld, int64_t c0,
+                                            float (&h)[8]) {
+  if (kMode == NVFP4_MODE_SWIGLU_GU8) {
+    // output columns c0..c0+7 (c0 % 8 == 0): gate at 2*c0 .. +7, up at 2*c0+8 .. +15
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + 2 * c0);
+    const uint4 gw = __ldg(p), uw = __ldg(p + 1);
+    float g[8], u[8];
+    bf16x8_to_f32(gw, g);
+    bf16x8_to_f32(uw, u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = swiglu(g[i], u[i]);
+  } else if (kDtype == NVFP4_IN_BF16) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + c0));
+    bf16x8_to_f32(w, h);
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(in) + row * ld + c0);
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    h[0] = a.x; h[1] = a.y; h[2] = a.z; h[3] = a.w;
+    h[4] = b.x; h[5] = b.y; h[6] = b.z; h[7] = b.w;
+  }
+}
+
+// One warp per (row, 256-column segment).  rows_pad >= rows covers the zero
+// padding rows of the swizzled SF; sf_linear selects a plain row-major SF
+// output ([rows, cols/16], used for staging x in moe_route_permute; requires
+// cols % 64 == 0).
+template <int kMode, int kDtype>
+__global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ in, int64_t rows,
+                                                       int64_t cols, int64_t ld, int64_t rows_pad,
+                                                       uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                       int sf_linear, float* __restrict__ h_dbg) {
+  const int lane = threadIdx.x & 31;
+  const int64_t segs = (cols + 255) / 256;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (warp >= rows_pad * segs) return;
+  const int64_t row = warp / segs;
+  const int64_t seg = warp - row * segs;
+  const int64_t c0 = seg * 256 + lane * 8;
+  const bool in_row = row < rows;
+  const bool active = in_row && c0 < cols;
+
+  float h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = 0.0f;
+  if (active) load_values<kMode, kDtype>(in, row, ld, c0, h);
+
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  const BlockScale s = block_scale(amax);
+
+  if (active) {
+    const uint32_t nib = quantize8(h, s);
+    *reinterpret_cast<uint32_t*>(q + row * (cols / 2) + c0 / 2) = nib;
+    if (h_dbg != nullptr) {
+      float4* hp = reinterpret_cast<float4*>(h_dbg + row * cols + c0);
+      hp[0] = make_float4(h[0], h[1], h[2], h[3]);
+      hp[1] = make_float4(h[4], h[5], h[6], h[7]);
+    }
+  }
+
+  // gather the octet's four scale bytes (lanes 8w, 8w+2, 8w+4, 8w+6) into one word
+  const uint32_t code = active ? s.code : 0u;
+  const int base = lane & ~7;
+  const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, code, base);
+  const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, code, base + 2);
+  const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
+  const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, code, base + 6);
+  const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  const int64_t k4 = seg * 4 + (lane >> 3);        // 64-column group of this octet
+  const int64_t k4_total = (cols + 63) / 64;
+  if ((lane & 7) == 0 && k4 < k4_total) {
+    if (sf_linear) {
+      if (in_row) *reinterpret_cast<uint32_t*>(sf + row * (cols / 16) + k4 * 4) = word;
+    } else {
+      *reinterpret_cast<uint32_t*>(sf + sf_word_offset(row, k4, k4_total)) = word;
+    }
+  }
+}
+
+template <int kMode, int kDtype>
+static cudaError_t launch_quantize(const void* in, int64_t rows, int64_t cols, int64_t ld,
+                                   int64_t rows_pad, uint8_t* q, uint8_t* sf, int sf_linear,
+                                   float* h_dbg, cudaStream_t stream) {
+  const int64_t warps = rows_pad * ((cols + 255) / 256);
+  const int64_t blocks = (warps + 7) / 8;
+  if (blocks == 0) return cudaSuccess;
+  quantize_kernel<kMode, kDtype><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      in, rows, cols, ld, rows_pad, q, sf, sf_linear, h_dbg);
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_launch(const void* in, int dtype, int mode, int64_t rows, int64_t cols, int64_t ld,
+                            uint8_t* q, uint8_t* sf, int sf_linear, float* h_dbg, cudaStream_t stream) {
+  const int64_t rows_pad = sf_linear ? rows : ((rows + 127) / 128) * 128;
+  if (mode == NVFP4_MODE_SWIGLU_GU8)
+    return launch_quantize<NVFP4_MODE_SWIGLU_GU8, NVFP4_IN_BF16>(in, rows, cols, ld, rows_pad, q, sf,
+                                                                 sf_linear, h_dbg, stream);
+  if (dtype == NVFP4_IN_BF16)
+    return launch_quantize<NVFP4_MODE_PLAIN, NVFP4_IN_BF16>(in, rows, cols, ld, rows_pad, q, sf, sf_linear,
+                                                            h_dbg, stream);
+  return launch_quantize<NVFP4_MODE_PLAIN, NVFP4_IN_F32>(in, rows, cols, ld, rows_pad, q, sf, sf_linear,
+                                                         h_dbg, stream);
+}
+
+// ------------------------------------------------------------ SF swizzle --
+// Forward: one thread per 32-bit word of the swizzled buffer (row, k4), reading
+// four strided source bytes (zero outside mn_rows x k_sf_cols).
+__global__ void sf_swizzle_fwd_kernel(const uint8_t* __restrict__ lin, int64_t mn_rows, int64_t k_sf,
+                                      int64_t s_mn, int64_t s_k, uint8_t* __restrict__ swz,
+                                      int64_t rows_pad, int64_t k4_total) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows_pad * k4_total) return;
+  const int64_t row = i / k4_total;
+  const int64_t k4 = i - row * k4_total;
+  uint32_t word = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int64_t k = k4 * 4 + j;
+    if (row < mn_rows && k < k_sf) word |= static_cast<uint32_t>(lin[row * s_mn + k * s_k]) << (8 * j);
+  }
+  *reinterpret_cast<uint32_t*>(swz + sf_word_offset(row, static_cast<uint32_t>(k4), static_cast<uint32_t>(k4_total))) = word;
+}
+
+// Inverse: one thread per addressed scale.
+__global__ void sf_swizzle_inv_kernel(const uint8_t* __restrict__ swz, int64_t mn_rows, int64_t k_sf,
+                                      int64_t s_mn, int64_t s_k, uint8_t* __restrict__ lin,
+                                      int64_t k4_total) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= mn_rows * k_sf) return;
+  const int64_t row = i / k_sf;
+  const int64_t k = i - row * k_sf;
+  const uint64_t off = sf_word_offset(row, static_cast<uint32_t>(k >> 2), static_cast<uint32_t>(k4_total)) + (k & 3);
+  lin[row * s_mn + k * s_k] = swz[off];
+}
+
+cudaError_t sf_swizzle_launch(const uint8_t* in, int64_t mn_rows, int64_t k_sf, int64_t s_mn, int64_t s_k,
+                              uint8_t* out, int inverse, cudaStream_t stream) {
+  const int64_t k4_total = (k_sf + 3) / 4;
+  if (!inverse) {
+    const int64_t rows_pad = ((mn_rows + 127) / 128) * 128;
+    const int64_t n = rows_pad * k4_total;
+    sf_swizzle_fwd_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        in, mn_rows, k_sf, s_mn, s_k, out, rows_pad, k4_total);
+  } else {
+    const int64_t n = mn_rows * k_sf;
+    sf_swizzle_inv_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        in, mn_rows, k_sf, s_mn, s_k, out, k4_total);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

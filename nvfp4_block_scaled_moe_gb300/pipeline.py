@@ -1,0 +1,97 @@
+"""Device buffers and the three-call forward of the NVFP4 MoE expert FFN.
+
+Plumbing only: PyTorch allocates device memory; every step is one call into
+libnvfp4moe.so (route + permute + stage, L1/SwiGLU/requant/L2, combine).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import (MODE_PLAIN, moe_combine, moe_padded_rows_max, moe_route_permute,
+               moe_route_permute_workspace, nvfp4_moe_ffn_forward, nvfp4_quantize, sf_bytes)
+
+
+@dataclass
+class MoeShape:
+    T: int
+    H: int
+    I: int
+    E: int
+    top_k: int
+
+    @property
+    def rows_max(self) -> int:
+        return moe_padded_rows_max(self.T, self.E, self.top_k)
+
+
+class MoeBuffers:
+    """Every output and intermediate of one forward, sized for the worst case."""
+
+    def __init__(self, s: MoeShape, device="cuda"):
+        u8, i32, f32 = torch.uint8, torch.int32, torch.float32
+        R = max(s.rows_max, 128)
+        self.shape = s
+        self.rows_max = R
+        self.topk_ids = torch.empty((s.T, s.top_k), dtype=i32, device=device)
+        self.topk_w = torch.empty((s.T, s.top_k), dtype=f32, device=device)
+        self.counts = torch.empty(s.E, dtype=i32, device=device)
+        self.offsets = torch.empty(s.E + 1, dtype=i32, device=device)
+        self.perm_token = torch.empty(R, dtype=i32, device=device)
+        self.inv_perm = torch.empty((s.T, s.top_k), dtype=i32, device=device)
+        self.a1_q = torch.empty((R, s.H // 2), dtype=u8, device=device)
+        self.a1_sf = torch.empty(sf_bytes(R, s.H), dtype=u8, device=device)
+        self.a2_q = torch.empty((R, s.I // 2), dtype=u8, device=device)
+        self.a2_sf = torch.empty(sf_bytes(R, s.I), dtype=u8, device=device)
+        self.rows_out = torch.empty((R, s.H), dtype=torch.bfloat16, device=device)
+        self.y = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=device)
+        self.workspace = torch.empty(moe_route_permute_workspace(s.T, s.H, s.E, s.top_k), dtype=u8, device=device)
+        self.h_debug = None
+
+    def enable_h_debug(self):
+        self.h_debug = torch.empty((self.rows_max, self.shape.I), dtype=torch.float32, device=self.a2_q.device)
+
+
+class MoeWeights:
+    """Expert weights in NVFP4: W1 [E, 2I, H] (rows interleaved 8|8) and W2 [E, H, I],
+    each expert's SF swizzled for its own N x K matrix."""
+
+    def __init__(self, s: MoeShape, device="cuda"):
+        u8 = torch.uint8
+        self.shape = s
+        self.w1_q = torch.empty((s.E, 2 * s.I, s.H // 2), dtype=u8, device=device)
+        self.w1_sf = torch.empty((s.E, sf_bytes(2 * s.I, s.H)), dtype=u8, device=device)
+        self.w2_q = torch.empty((s.E, s.H, s.I // 2), dtype=u8, device=device)
+        self.w2_sf = torch.empty((s.E, sf_bytes(s.H, s.I)), dtype=u8, device=device)
+
+    def set_expert(self, e: int, w1_f32: torch.Tensor, w2_f32: torch.Tensor):
+        """Quantise one expert's fp32 weights (CUDA tensors) with the library's quantiser."""
+        s = self.shape
+        nvfp4_quantize(w1_f32, s.H, MODE_PLAIN, self.w1_q[e], self.w1_sf[e])
+        nvfp4_quantize(w2_f32, s.I, MODE_PLAIN, self.w2_q[e], self.w2_sf[e])
+
+    def set_from_pool(self, pool: torch.Tensor, w1_off, w2_off, std: float):
+        """Quantise every expert from windows of a device fp32 pool: expert e's W1 is
+        pool[w1_off[e] : + 2I*H] * std viewed [2I, H], W2 likewise [H, I]."""
+        s = self.shape
+        n1, n2 = 2 * s.I * s.H, s.H * s.I
+        scale = torch.tensor(std, dtype=torch.float32, device=pool.device)
+        for e in range(s.E):
+            o1, o2 = int(w1_off[e]), int(w2_off[e])
+            w1 = (pool[o1:o1 + n1] * scale).view(2 * s.I, s.H)
+            w2 = (pool[o2:o2 + n2] * scale).view(s.H, s.I)
+            self.set_expert(e, w1, w2)
+
+
+def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
+                alpha1: float = 1.0, alpha2: float = 1.0) -> torch.Tensor:
+    """y = MoE-FFN(x): route + permute + stage, L1 + SwiGLU + requant + L2, combine."""
+    s = b.shape
+    moe_route_permute(logits, x, s.top_k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
+                      b.inv_perm, b.a1_q, b.a1_sf, b.workspace)
+    if s.T > 0:
+        nvfp4_moe_ffn_forward(b.a1_q, b.a1_sf, b.offsets, b.counts, s.E, s.H, s.I, b.rows_max, w.w1_q, w.w1_sf,
+                              w.w2_q, w.w2_sf, alpha1, alpha2, b.a2_q, b.a2_sf, b.rows_out, b.h_debug)
+        moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
+    return b.y

@@ -182,3 +182,42 @@ def moe_ffn(x: np.ndarray, logits: np.ndarray, w1: np.ndarray, w2: np.ndarray, t
     y = combine(rows, p["inv_perm"], w)
     return dict(ids=ids, w=w, a1_q=a1_q, a1_sf=a1_sf, w1_q=w1_q, w1_sf=w1_sf, w2_q=w2_q,
                 w2_sf=w2_sf, g_full=g_full, h=h, a2_q=a2_q, a2_sf=a2_sf, rows=rows, y=y, **p)
+
+
+def moe_ffn_tokens(x_rows: np.ndarray, logits_rows: np.ndarray, w1_of, w2_of, top_k: int,
+                   alpha1: float = 1.0, alpha2: float = 1.0, cache: dict | None = None) -> dict:
+    """The same path for a few sampled tokens, one at a time (every step is
+    row-independent: a token's output depends only on its own row, its routing
+    and its experts' weights).  ``w1_of(e)`` / ``w2_of(e)`` return expert e's fp32
+    weights; their quantised, dequantised forms are cached in ``cache``.
+    Returns ids, w, a2 rows (q, row-major sf) per (token, slot), and y (BF16 values)."""
+    cache = {} if cache is None else cache
+
+    def deq(kind, e, fn):
+        key = (kind, e)
+        if key not in cache:
+            q, sf = nvfp4.quantize_rows(fn(e))
+            cache[key] = nvfp4.dequantize_rows(q, sf)
+        return cache[key]
+
+    ids, w = route_topk(logits_rows, top_k)
+    xq, xsf = nvfp4.quantize_rows(np.asarray(x_rows, dtype=np.float32))
+    a1 = nvfp4.dequantize_rows(xq, xsf)
+    n_tok = len(x_rows)
+    y, a2_q, a2_sf, h_all = [], [], [], []
+    for t in range(n_tok):
+        acc = None
+        for j in range(top_k):
+            e = int(ids[t, j])
+            g_full = np.float64(np.float32(alpha1)) * (a1[t:t + 1] @ deq("w1", e, w1_of).T)
+            q, sf, h = l1_swiglu_requant(g_full)
+            o = np.float64(np.float32(alpha2)) * (nvfp4.dequantize_rows(q, sf) @ deq("w2", e, w2_of).T)
+            row = round_to_bf16(o)[0]
+            acc = w[t, j] * row if acc is None else acc + w[t, j] * row
+            a2_q.append(q[0])
+            a2_sf.append(sf[0])
+            h_all.append(h[0])
+        y.append(round_to_bf16(acc))
+    return dict(ids=ids, w=w, a2_q=np.array(a2_q).reshape(n_tok, top_k, -1),
+                a2_sf=np.array(a2_sf).reshape(n_tok, top_k, -1), h=np.array(h_all).reshape(n_tok, top_k, -1),
+                y=np.array(y))

@@ -1,0 +1,101 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads without a GPU,
+exports every function include/nvfp4moe.h declares, and rejects bad arguments
+on the host before any CUDA call (no compute is launched here)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4moe.h")
+
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b([a-z][a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_block_scaled_moe_gb300 import build, load
+    build.build()
+    return load()
+
+
+def test_header_declares_the_five_path_calls():
+    names = declared_functions()
+    for n in ("nvfp4_quantize", "nvfp4_sf_swizzle", "moe_route_permute", "nvfp4_moe_ffn_forward", "moe_combine"):
+        assert n in names
+
+
+@needs_nvcc
+def test_library_exports_every_declared_function(lib):
+    raw = ctypes.CDLL(os.path.join(ROOT, "nvfp4_block_scaled_moe_gb300", "libnvfp4moe.so"))
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+@needs_nvcc
+def test_size_helpers(lib):
+    assert lib.nvfp4_sf_bytes(128, 64) == 512
+    assert lib.nvfp4_sf_bytes(129, 65) == 2 * 2 * 512
+    assert lib.nvfp4_sf_bytes(0, 64) == 0
+    # worst case: every group padded by 127 rows, result a multiple of 128
+    r = lib.moe_padded_rows_max(16384, 256, 8)
+    assert r % 128 == 0 and r >= 16384 * 8 and r <= 16384 * 8 + 127 * 256
+    assert lib.moe_padded_rows_max(1, 256, 8) == 1024        # 8 rows, each its own group
+    assert lib.moe_route_permute_workspace(256, 7168, 256, 8) >= 256 * 7168 // 2
+
+
+@needs_nvcc
+def test_host_validation_without_gpu(lib):
+    import nvfp4_block_scaled_moe_gb300 as nv
+    vp = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(4096 + 64)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    p = vp(base)
+    odd = vp(base + 1)
+    # null input
+    assert lib.nvfp4_quantize(None, 0, 0, 4, 16, 16, p, p, None, None) == 1
+    # out_cols not a multiple of 16
+    assert lib.nvfp4_quantize(p, 0, 0, 4, 24, 24, p, p, None, None) == 2
+    # misaligned input
+    assert lib.nvfp4_quantize(odd, 0, 0, 4, 16, 16, p, p, None, None) == 3
+    # SwiGLU mode needs BF16
+    assert lib.nvfp4_quantize(p, 1, 1, 4, 16, 32, p, p, None, None) == 2
+    assert lib.nvfp4_sf_swizzle(p, 4, 4, 0, 1, p, 0, None) == 1
+    # K not a multiple of 256, N not a multiple of 128, G without offsets
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 200, p, p, 1.0, 1, None, None, p, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 96, 256, p, p, 1.0, 1, None, None, p, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 128, 256, p, p, 1.0, 1, None, None, p, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, 7, None, None, p, None, None) == 1
+    # routing limits
+    assert lib.moe_route_permute(p, p, 8, 64, 2000, 2, p, p, p, p, p, p, p, p, p, 1 << 20, None) == 2
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 9, p, p, p, p, p, p, p, p, p, 1 << 20, None) == 2
+    assert lib.moe_route_permute(p, p, 8, 60, 8, 2, p, p, p, p, p, p, p, p, p, 1 << 20, None) == 2
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, p, p, p, 16, None) == 1
+    assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, p, p, p, None, None) == 2
+    assert lib.moe_combine(p, p, p, 4, 12, 2, p, None) == 2
+    assert lib.nvfp4_selftest_bounded_wait(None, 10, None) == 1
+    assert b"selftest" in lib.nvfp4_last_error()
+    with pytest.raises(nv.Nvfp4Error) as ei:
+        nv._check(2)
+    assert ei.value.status == 2
+
+
+def test_product_package_has_no_cpu_fallback():
+    """The binding refuses to run without the built library and never imports the oracle."""
+    src_dir = os.path.join(ROOT, "nvfp4_block_scaled_moe_gb300")
+    for dirpath, _, files in os.walk(src_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.replace("# oracle", ""), f
+                assert "inputs" not in re.findall(r"^\s*(?:from|import)\s+(\w+)", text, flags=re.M), f

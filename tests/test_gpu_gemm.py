@@ -1,0 +1,156 @@
+"""GPU parity: nvfp4_grouped_gemm (tcgen05 block-scaled MMA) against the oracle's
+float64 GEMM on dequantised operands.
+
+Operands are random packed E2M1 bytes with random (non-uniform) E4M3 scales
+straight from the seeded generator; the device swizzles its own copy of the
+scales with nvfp4_sf_swizzle, so nothing the oracle computes reaches the GPU.
+Bounds: BF16 rows and SwiGLU h within relative Frobenius 2e-3 (and nearly all
+BF16 values identical); re-quantised nibbles within the 0.1% / one-step bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from oracle import moe as omoe
+from oracle import nvfp4 as onv
+
+from gpu_util import built_lib, compare_requantised, dev, host, rel_frobenius
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    built_lib()
+    import nvfp4_block_scaled_moe_gb300 as nv
+    return nv
+
+
+def _swizzled(nv, sf_lin):
+    rows, k_sf = sf_lin.shape
+    out = torch.empty(nv.sf_bytes(rows, 16 * k_sf), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_sf_swizzle(dev(sf_lin), rows, k_sf, k_sf, 1, out)
+    return out
+
+
+def _operands(nv, seed, rows_max, group_sizes, N, K, sf_range=(0x30, 0x44)):
+    a_q, a_sf = inputs.random_nvfp4_operand(seed, 0, rows_max, K, *sf_range)
+    G = len(group_sizes)
+    bq, bsf = zip(*(inputs.random_nvfp4_operand(seed, 1 + g, N, K, *sf_range) for g in range(G)))
+    b_q, b_sf = np.stack(bq), np.stack(bsf)
+    d = dict(a_q=dev(a_q), a_sf=_swizzled(nv, a_sf), b_q=dev(b_q),
+             b_sf=torch.stack([_swizzled(nv, b_sf[g]) for g in range(G)]))
+    offs = np.concatenate([[0], np.cumsum(group_sizes)]).astype(np.int32)
+    a_deq = onv.dequantize_rows(a_q, a_sf)
+    b_deq = np.stack([onv.dequantize_rows(b_q[g], b_sf[g]) for g in range(G)])
+    return d, offs, a_deq, b_deq
+
+
+def _valid_rows(offs, counts):
+    rows = []
+    for g in range(len(offs) - 1):
+        rows.extend(range(offs[g], offs[g] + counts[g]))
+    return np.array(rows, dtype=np.int64)
+
+
+CASES_BF16 = [
+    # (group padded sizes, counts or None, N, K, alpha)
+    ([128], None, 128, 256, 1.0),                     # one tile, one K stage
+    ([256], None, 256, 512, 1.0),
+    ([128, 0, 384, 128], [100, 0, 300, 128], 384, 768, 0.75),
+    ([128] * 40, [128 - (i % 7) for i in range(40)], 1024, 1280, 1.0),   # > one wave of tiles
+]
+
+
+@pytest.mark.parametrize("sizes,counts,N,K,alpha", CASES_BF16)
+def test_gemm_bf16_epilogue(nv, sizes, counts, N, K, alpha):
+    rows_max = sum(sizes) + 128
+    d, offs, a_deq, b_deq = _operands(nv, 11 + N + K, rows_max, sizes, N, K)
+    out = torch.full((rows_max, N), 12345.0, dtype=torch.bfloat16, device="cuda")
+    if counts is None:
+        assert len(sizes) == 1
+        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], sizes[0], None, None, 1, N, K, d["b_q"], d["b_sf"], alpha,
+                              nv.EPI_BF16, out_bf16=out)
+        valid = np.arange(sizes[0])
+    else:
+        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), dev(np.array(counts, np.int32)),
+                              len(sizes), N, K, d["b_q"], d["b_sf"], alpha, nv.EPI_BF16, out_bf16=out)
+        valid = _valid_rows(offs, counts)
+    nv.nvfp4_device_status()
+    ref = omoe.round_to_bf16(omoe.grouped_gemm(a_deq[:offs[-1]], offs, b_deq, alpha))
+    got = out.float().cpu().numpy()
+    assert rel_frobenius(got[valid], ref[valid]) <= 2e-3
+    assert np.mean(got[valid] == ref[valid]) > 0.97
+    mask = np.ones(rows_max, bool)
+    mask[valid] = False
+    assert np.all(got[mask] == 12345.0)               # nothing stored outside the real rows
+
+
+CASES_SWIGLU = [
+    ([128], None, 128, 256, 1.0),
+    ([256, 128], [200, 128], 512, 1024, 1.25),
+    ([128, 128, 0, 256], [1, 128, 0, 129], 256, 512, 0.5),
+]
+
+
+@pytest.mark.parametrize("sizes,counts,N,K,alpha", CASES_SWIGLU)
+def test_gemm_swiglu_nvfp4_epilogue(nv, sizes, counts, N, K, alpha):
+    rows_max = sum(sizes)
+    d, offs, a_deq, b_deq = _operands(nv, 7 + N + K, rows_max, sizes, N, K)
+    I = N // 2
+    q = torch.full((rows_max, I // 2), 0x77, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(nv.sf_bytes(rows_max, I), dtype=torch.uint8, device="cuda")
+    h = torch.zeros((rows_max, I), dtype=torch.float32, device="cuda")
+    if counts is None:
+        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, None, None, 1, N, K, d["b_q"], d["b_sf"], alpha,
+                              nv.EPI_SWIGLU_NVFP4, out_q=q, out_sf=sf, h_debug=h)
+        valid = np.arange(rows_max)
+    else:
+        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), dev(np.array(counts, np.int32)),
+                              len(sizes), N, K, d["b_q"], d["b_sf"], alpha, nv.EPI_SWIGLU_NVFP4, out_q=q,
+                              out_sf=sf, h_debug=h)
+        valid = _valid_rows(offs, counts)
+    nv.nvfp4_device_status()
+    g_full = omoe.grouped_gemm(a_deq, offs, b_deq, alpha)
+    oq, osf, oh = omoe.l1_swiglu_requant(g_full)
+    gh = host(h)
+    assert rel_frobenius(gh[valid], oh[valid]) <= 2e-3
+    gsf = onv.unswizzle_sf(host(sf), rows_max, I // 16)
+    res = compare_requantised(host(q)[valid], gsf[valid], oq[valid], osf[valid])
+    assert res["ok"], res
+    untouched = np.ones(rows_max, bool)
+    untouched[valid] = False
+    assert np.all(host(q)[untouched] == 0x77)
+
+
+def test_gemm_uniform_vs_random_scales_both_match(nv):
+    """All-equal scales hide a wrong scale layout; random ones expose it.  Both must match."""
+    for sf_range in ((0x38, 0x38), (0x28, 0x50)):
+        d, offs, a_deq, b_deq = _operands(nv, 3, 256, [256], 256, 512, sf_range)
+        out = torch.empty((256, 256), dtype=torch.bfloat16, device="cuda")
+        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], 256, None, None, 1, 256, 512, d["b_q"], d["b_sf"], 1.0,
+                              nv.EPI_BF16, out_bf16=out)
+        ref = omoe.round_to_bf16(omoe.grouped_gemm(a_deq, offs, b_deq))
+        assert rel_frobenius(out.float().cpu().numpy(), ref) <= 2e-3, sf_range
+
+
+def test_gemm_one_hot_locates_nibbles_and_scales(nv):
+    """A single nonzero A element at (r, k) and a single nonzero B element at (n, k):
+    the product appears only at (r, n), scaled by both blocks' scales."""
+    K, N, M = 512, 128, 128
+    rng = np.random.default_rng(9)
+    for r, n, k in ((0, 0, 0), (5, 77, 37), (127, 127, 511), (64, 3, 300), (33, 96, 64)):
+        a_q = np.zeros((M, K // 2), np.uint8)
+        b_q = np.zeros((1, N, K // 2), np.uint8)
+        a_q[r, k // 2] = (0x3 << 4) if k % 2 else 0x3          # 1.5
+        b_q[0, n, k // 2] = (0x6 << 4) if k % 2 else 0x6       # 4.0
+        a_sf = rng.integers(0x30, 0x40, (M, K // 16), dtype=np.uint8)
+        b_sf = rng.integers(0x30, 0x40, (N, K // 16), dtype=np.uint8)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        nv.nvfp4_grouped_gemm(dev(a_q), _swizzled(nv, a_sf), M, None, None, 1, N, K, dev(b_q),
+                              _swizzled(nv, b_sf)[None], 1.0, nv.EPI_BF16, out_bf16=out)
+        got = out.float().cpu().numpy()
+        expect = np.zeros((M, N))
+        expect[r, n] = 1.5 * 4.0 * onv.e4m3_decode(a_sf[r, k // 16]) * onv.e4m3_decode(b_sf[n, k // 16])
+        assert np.array_equal(got, omoe.round_to_bf16(expect)), (r, n, k)

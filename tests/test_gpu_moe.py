@@ -1,0 +1,116 @@
+"""GPU parity of the whole path (route_permute -> L1 + SwiGLU + requant -> L2 ->
+combine) against the fully CPU-quantised oracle.
+
+Small workloads (the tiny configuration and ragged variants) are compared on
+every output; the full-size decode and prefill workloads, run in the launch
+configuration the benchmark times, are compared on sampled tokens that the
+oracle computes one by one, plus invariants that hold at any size.
+Bounds (from the path's specification): weights, routing, permutation and the
+staged activation bit-exact; fused-epilogue h within relative Frobenius 2e-3;
+re-quantised nibbles <= 0.1% different by <= one E2M1 step; y within relative
+Frobenius 2e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from oracle import moe as omoe
+from oracle import nvfp4 as onv
+
+from gpu_util import built_lib, compare_requantised, dev, host, rel_frobenius
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    built_lib()
+    import nvfp4_block_scaled_moe_gb300 as nv
+    from nvfp4_block_scaled_moe_gb300 import pipeline
+    return nv, pipeline
+
+
+def _gpu_setup(pipeline, spec):
+    s = pipeline.MoeShape(T=spec["T"], H=spec["H"], I=spec["I"], E=spec["E"], top_k=spec["top_k"])
+    w = pipeline.MoeWeights(s)
+    pool, o1, o2 = inputs.moe_weight_pool(spec)
+    w.set_from_pool(torch.from_numpy(pool).cuda(), o1, o2, float(inputs.WEIGHT_STD))
+    b = pipeline.MoeBuffers(s)
+    return s, w, b
+
+
+SMALL = [dict(inputs.CONFIGS["tiny"]),
+         inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=21),
+         inputs.moe_spec(T=200, H=256, I=512, E=5, top_k=3, seed=22, zipf=True)]
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=["tiny", "ragged300", "zipf200"])
+def test_moe_end_to_end_small(nv, spec):
+    nv, pipeline = nv
+    s, w, b = _gpu_setup(pipeline, spec)
+    b.enable_h_debug()
+    x_t, x = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    y = pipeline.moe_forward(x_t.cuda(), dev(logits), w, b)
+    nv.nvfp4_device_status()
+    w1, w2 = inputs.moe_all_weights(spec)
+    o = omoe.moe_ffn(x, logits, w1, w2, spec["top_k"])
+    E, H, I = spec["E"], spec["H"], spec["I"]
+    # weights quantised on the GPU: bit-exact
+    assert np.array_equal(host(w.w1_q), o["w1_q"]) and np.array_equal(host(w.w2_q), o["w2_q"])
+    for e in range(E):
+        assert np.array_equal(onv.unswizzle_sf(host(w.w1_sf[e]), 2 * I, H // 16), o["w1_sf"][e])
+        assert np.array_equal(onv.unswizzle_sf(host(w.w2_sf[e]), H, I // 16), o["w2_sf"][e])
+    # routing, permutation, staged activation: bit-exact
+    assert np.array_equal(host(b.topk_ids), o["ids"])
+    assert np.array_equal(host(b.offsets), o["offsets"])
+    R = int(o["offsets"][-1])
+    assert np.array_equal(host(b.perm_token)[:R], o["perm_token"])
+    assert np.array_equal(host(b.inv_perm), o["inv_perm"])
+    assert np.array_equal(host(b.a1_q)[:R], o["a1_q"])
+    real = o["perm_token"] >= 0
+    # fused L1 epilogue
+    gh = host(b.h_debug)[:R]
+    assert rel_frobenius(gh[real], o["h"][real]) <= 2e-3
+    gsf = onv.unswizzle_sf(host(b.a2_sf), R, I // 16)
+    res = compare_requantised(host(b.a2_q)[:R][real], gsf[real], o["a2_q"][real], o["a2_sf"][real])
+    assert res["ok"], res
+    # L2 rows and the combined output
+    rows = b.rows_out.float().cpu().numpy()[:R]
+    assert rel_frobenius(rows[real], o["rows"][real]) <= 2e-2
+    assert rel_frobenius(y.float().cpu().numpy(), o["y"]) <= 2e-2
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_moe_full_size_sampled_tokens(nv, name):
+    nv, pipeline = nv
+    spec = dict(inputs.CONFIGS[name])
+    s, w, b = _gpu_setup(pipeline, spec)
+    x_t, x = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    y = pipeline.moe_forward(x_t.cuda(), dev(logits), w, b)
+    nv.nvfp4_device_status()
+    T, k, E = spec["T"], spec["top_k"], spec["E"]
+    # invariants at full size
+    counts, offs = host(b.counts), host(b.offsets)
+    inv, perm = host(b.inv_perm), host(b.perm_token)
+    ids = host(b.topk_ids)
+    assert counts.sum() == T * k and np.all(offs % 128 == 0)
+    assert np.all(np.diff(offs) == -(-counts // 128) * 128)
+    assert np.array_equal(perm[inv.ravel()], np.repeat(np.arange(T), k))
+    e_of_row = np.searchsorted(offs, inv, side="right") - 1
+    assert np.array_equal(e_of_row, ids)
+    # sampled tokens, computed one by one by the oracle
+    pick = np.random.default_rng(spec["seed"]).choice(T, size=4, replace=False)
+    tok = omoe.moe_ffn_tokens(x[pick], logits[pick], lambda e: inputs.moe_w1(spec, e),
+                              lambda e: inputs.moe_w2(spec, e), k)
+    assert np.array_equal(ids[pick], tok["ids"])
+    assert np.allclose(host(b.topk_w)[pick], tok["w"], rtol=2e-6, atol=1e-7)
+    rows = inv[pick].ravel()
+    a2_sf = onv.unswizzle_sf(host(b.a2_sf), b.rows_max, spec["I"] // 16)[rows]
+    res = compare_requantised(host(b.a2_q)[rows], a2_sf, tok["a2_q"].reshape(len(rows), -1),
+                              tok["a2_sf"].reshape(len(rows), -1))
+    assert res["ok"], res
+    got = y.float().cpu().numpy()[pick]
+    assert rel_frobenius(got, tok["y"]) <= 2e-2

@@ -1,0 +1,141 @@
+"""GPU parity: nvfp4_quantize and nvfp4_sf_swizzle against the oracle.
+
+PLAIN mode must be bit-exact (nibbles and swizzled scale bytes, padding
+included).  SWIGLU_GU8 uses the fast exponential for silu, so its h differs from
+the oracle's float64 silu by a few ulp: planted blocks with exact h must match
+bit for bit, the rest within the re-quantisation bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from oracle import nvfp4 as onv
+
+from gpu_util import built_lib, compare_requantised, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    built_lib()
+    import nvfp4_block_scaled_moe_gb300 as nv
+    return nv
+
+
+def _run_plain(nv, x_t, out_cols):
+    rows = x_t.shape[0]
+    q = torch.full((rows, out_cols // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    sf = torch.full((nv.sf_bytes(rows, out_cols),), 0xCD, dtype=torch.uint8, device="cuda")
+    h = torch.empty((rows, out_cols), dtype=torch.float32, device="cuda")
+    nv.nvfp4_quantize(x_t, out_cols, nv.MODE_PLAIN, q, sf, h_debug=h)
+    nv.nvfp4_device_status()
+    return host(q), host(sf), host(h)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (3, 48), (128, 256), (300, 1024), (257, 80), (130, 208)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_plain_bit_exact(nv, rows, cols, dtype):
+    x = inputs.plain_input_with_ties(rows * 7 + cols, rows, cols, dtype=dtype)
+    x_t = dev(x, torch.bfloat16 if dtype == "bf16" else torch.float32)
+    q, sf, h = _run_plain(nv, x_t, cols)
+    oq, osf = onv.quantize_rows(x)
+    assert np.array_equal(h, x)
+    assert np.array_equal(q, oq)
+    assert np.array_equal(sf, onv.swizzle_sf_fast(osf))      # padding bytes written as 0
+
+
+def test_plain_every_e4m3_tie_and_sign_of_zero(nv):
+    # block maxima 6 * m for every midpoint m between consecutive E4M3 values (and
+    # just above / below it): fp32(amax / 6) lands exactly on the tie
+    pos = np.array([onv.e4m3_decode(c) for c in range(0x7F)])
+    mids = (pos[:-1] + pos[1:]) / 2
+    eps = 2.0 ** -18
+    targets = np.concatenate([mids, mids * (1 + eps), mids * (1 - eps), pos, [500.0, 1e4]])
+    rows = len(targets)
+    rng = np.random.default_rng(0)
+    x = (rng.uniform(-1, 1, (rows, 16)) * targets[:, None] * 6).astype(np.float32)
+    x[:, 5] = (6 * targets).astype(np.float32)
+    x[:, 6] = -0.0
+    x[:, 7] = np.float32(-1e-30)
+    q, sf, _ = _run_plain(nv, dev(x), 16)
+    oq, osf = onv.quantize_rows(x)
+    assert np.array_equal(sf, onv.swizzle_sf_fast(osf))
+    assert np.array_equal(q, oq)
+    nib = onv.unpack_nibbles(q)
+    assert np.all(nib[:, 6] == 8) and np.all(nib[:, 7] == 8)     # -0 and tiny negatives keep the sign
+
+
+def test_plain_all_half_steps(nv):
+    # every scaled magnitude on the quarter grid 0 .. 7 with both signs, scale 1
+    m = np.arange(0, 29) * 0.25
+    vals = np.concatenate([m, -m])
+    vals = np.concatenate([vals, np.zeros((-len(vals)) % 15)])
+    blocks = vals.reshape(-1, 15)
+    x = np.concatenate([np.full((len(blocks), 1), 6.0), blocks], axis=1).astype(np.float32)
+    q, sf, _ = _run_plain(nv, dev(x), 16)
+    oq, osf = onv.quantize_rows(x)
+    assert np.array_equal(q, oq) and np.array_equal(sf, onv.swizzle_sf_fast(osf))
+
+
+def test_strided_input_rows(nv):
+    x = inputs.plain_input_with_ties(5, 64, 512)
+    big = np.zeros((64, 640), np.float32)
+    big[:, :512] = x
+    t = dev(big)
+    q = torch.empty((64, 256), dtype=torch.uint8, device="cuda")
+    sf = torch.empty(nv.sf_bytes(64, 512), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_quantize(t, 512, nv.MODE_PLAIN, q, sf, in_ld=640)
+    oq, osf = onv.quantize_rows(x)
+    assert np.array_equal(host(q), oq) and np.array_equal(host(sf), onv.swizzle_sf_fast(osf))
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 256), (300, 512), (129, 2048)])
+def test_swiglu_gu8_within_requant_bound(nv, rows, cols):
+    gu_t, plant = inputs.quantizer_input(dict(seed=rows + cols), rows=rows, cols=cols)
+    gu = gu_t.float().numpy()
+    q = torch.empty((rows, cols // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty(nv.sf_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    h = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    nv.nvfp4_quantize(gu_t.cuda(), cols, nv.MODE_SWIGLU_GU8, q, sf, h_debug=h)
+    nv.nvfp4_device_status()
+    oq, osf, oh = onv.quantize_swiglu_gu8(gu)
+    gh = host(h)
+    # fast silu: a few ulp of relative error on h
+    rel = np.abs(gh - oh) / np.maximum(np.abs(oh), 1e-30)
+    assert np.quantile(rel, 0.999) < 1e-5 and rel.max() < 1e-4
+    gsf = onv.unswizzle_sf(host(sf), rows, cols // 16)
+    res = compare_requantised(host(q), gsf, oq, osf)
+    assert res["ok"], res
+    # planted exact blocks: h is exact on both sides, so the codes are identical
+    nb = cols // 16
+    for blk in plant["midpoint"]:
+        r, b = divmod(int(blk), nb)
+        assert np.array_equal(gh[r, 16 * b:16 * b + 16], oh[r, 16 * b:16 * b + 16])
+        assert gsf[r, b] == osf[r, b]
+        assert np.array_equal(host(q)[r, 8 * b:8 * b + 8], oq[r, 8 * b:8 * b + 8])
+    # the whole padded SF buffer is written: padding rows are zero
+    full = host(sf)
+    pad = np.ones(len(full), bool)
+    pad[[onv.sf_offset(m, k, cols // 16) for m in range(rows) for k in range(cols // 16)]] = False
+    assert not full[pad].any()
+
+
+@pytest.mark.parametrize("mn,k_sf", [(1, 1), (100, 7), (128, 4), (300, 28), (513, 9)])
+def test_sf_swizzle_forward_and_inverse(nv, mn, k_sf):
+    rng = np.random.default_rng(mn + 100 * k_sf)
+    lin = rng.integers(1, 256, (mn, k_sf), dtype=np.uint8)
+    expect = onv.swizzle_sf_fast(lin)
+    # SFA convention: row-major (mn, k_sf), strides (k_sf, 1)
+    out = torch.full((len(expect),), 0xEE, dtype=torch.uint8, device="cuda")
+    nv.nvfp4_sf_swizzle(dev(lin), mn, k_sf, k_sf, 1, out)
+    assert np.array_equal(host(out), expect)
+    # SFB convention: stored (k_sf, mn) after a transpose, strides (1, mn)
+    out2 = torch.full((len(expect),), 0xEE, dtype=torch.uint8, device="cuda")
+    nv.nvfp4_sf_swizzle(dev(np.ascontiguousarray(lin.T)), mn, k_sf, 1, mn, out2)
+    assert np.array_equal(host(out2), expect)
+    back = torch.zeros((mn, k_sf), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_sf_swizzle(out, mn, k_sf, k_sf, 1, back, inverse=True)
+    nv.nvfp4_device_status()
+    assert np.array_equal(host(back), lin)

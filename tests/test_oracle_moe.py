@@ -184,3 +184,19 @@ def test_moe_ffn_tiny_config_runs_and_is_consistent():
     t = 7
     acc = sum(out["w"][t, j] * out["rows"][out["inv_perm"][t, j]] for j in range(2))
     assert np.array_equal(out["y"][t], moe.round_to_bf16(acc))
+
+
+def test_per_token_path_equals_whole_batch():
+    spec = inputs.moe_spec(T=50, H=256, I=256, E=4, top_k=2, seed=12)
+    _, x = inputs.moe_x(spec)
+    w1, w2 = inputs.moe_all_weights(spec)
+    logits = inputs.moe_logits(spec)
+    full = moe.moe_ffn(x, logits, w1, w2, 2, alpha1=0.5, alpha2=2.0)
+    pick = [0, 7, 49]
+    tok = moe.moe_ffn_tokens(x[pick], logits[pick], lambda e: w1[e], lambda e: w2[e], 2, alpha1=0.5, alpha2=2.0)
+    assert np.array_equal(tok["y"], full["y"][pick])
+    for i, t in enumerate(pick):
+        for j in range(2):
+            r = full["inv_perm"][t, j]
+            assert np.array_equal(tok["a2_q"][i, j], full["a2_q"][r])
+            assert np.array_equal(tok["a2_sf"][i, j], full["a2_sf"][r])
