@@ -1,0 +1,355 @@
+"""Benchmark of the NVFP4 MoE expert FFN on GB300.
+
+One step = one pass of the whole path over one batch: moe_route_permute
+(top-k routing, padded permutation, NVFP4 staging of x) -> L1 grouped GEMM with
+the fused SwiGLU + NVFP4 epilogue -> L2 grouped GEMM -> moe_combine.  The
+default workload is the prefill batch: T=16384 tokens, H=7168, I=2048, E=256
+experts, top-8, Zipf-skewed routing (seeded synthetic data).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is whole-job TFLOP/s of the FFN
+(algorithmic FLOPs 6*k*H*I per token, padding rows not credited) with inputs
+resident in HBM; `e2e` repeats the measurement with the inputs copied from
+pinned host memory and the output copied back inside the timed region.
+Under torchrun each rank runs its own batch (weak scaling, no data-path
+collective); the timed region is bracketed by barriers and the max over ranks
+is taken.  `--impl reference` times the CPU oracle on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import inputs  # noqa: E402
+
+METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs HBM"
+WORKLOAD = "prefill"
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense ratio (FP4 / BF16 tensor peak)
+
+
+# ------------------------------------------------------------------ helpers --
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sustained=p["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def ffn_flops(T: int, H: int, I: int, k: int) -> tuple:
+    l1 = 2.0 * T * k * (2 * I) * H
+    l2 = 2.0 * T * k * I * H
+    return l1, l2
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a host scalar over ranks (the only collective: timing, never data)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------- the oracle arm --
+class OracleArm:
+    """The CPU oracle, as it stands, on sampled tokens of the workload (inputs drawn
+    once, outside any timing; expert dequantisations cached as the oracle allows)."""
+
+    def __init__(self, spec: dict, seed: int = 1234):
+        self.spec = spec
+        _, self.x = inputs.moe_x(spec)
+        self.logits = inputs.moe_logits(spec)
+        self.order = np.random.default_rng(seed).permutation(spec["T"])
+        self.next = 0
+        self.cache: dict = {}
+
+    def run(self, budget_s: float, max_tokens: int) -> dict:
+        from oracle import moe as omoe
+        spec = self.spec
+        done, t0 = 0, time.perf_counter()
+        while done < max_tokens:
+            t = self.order[self.next % len(self.order)]
+            self.next += 1
+            omoe.moe_ffn_tokens(self.x[[t]], self.logits[[t]], lambda e: inputs.moe_w1(spec, e),
+                                lambda e: inputs.moe_w2(spec, e), spec["top_k"], cache=self.cache)
+            done += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        l1, l2 = ffn_flops(done, spec["H"], spec["I"], spec["top_k"])
+        return dict(tokens=done, seconds=dt, tflops=(l1 + l2) / dt / 1e12, tokens_per_s=done / dt)
+
+
+def run_reference(args, world: int, rank: int) -> None:
+    if rank != 0:
+        return
+    spec = dict(inputs.CONFIGS[WORKLOAD])
+    arm = OracleArm(spec)
+    tok, sec = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        r = arm.run(budget_s=0.0, max_tokens=1)
+        if i >= args.warmup:
+            tok += r["tokens"]
+            sec += r["seconds"]
+    l1, l2 = ffn_flops(tok, spec["H"], spec["I"], spec["top_k"])
+    value = (l1 + l2) / sec / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_name(spec), "step": "oracle on one sampled token per step"},
+        "tokens_per_s": tok / sec,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{tok} sampled tokens of the prefill batch, one per step, expert "
+                                   "dequantisation cached across steps"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def _workload_name(spec: dict) -> str:
+    return (f"prefill NVFP4 MoE FFN T={spec['T']} H={spec['H']} I={spec['I']} E={spec['E']} "
+            f"top-{spec['top_k']} Zipf(1.2)-skewed routing")
+
+
+# ------------------------------------------------------------ our GPU arm --
+def run_ours(args, world: int, rank: int, local: int) -> None:
+    import torch
+
+    import nvfp4_block_scaled_moe_gb300 as nv
+    from nvfp4_block_scaled_moe_gb300 import build as nvbuild
+    from nvfp4_block_scaled_moe_gb300 import pipeline
+
+    nvbuild.build()
+    nv.load()
+    torch.cuda.set_device(local)
+    spec = dict(inputs.CONFIGS[WORKLOAD])
+    spec["seed"] = spec["seed"] + 1000 * rank if rank else spec["seed"]     # each rank its own batch
+    T, H, I, E, k = spec["T"], spec["H"], spec["I"], spec["E"], spec["top_k"]
+    s = pipeline.MoeShape(T=T, H=H, I=I, E=E, top_k=k)
+    w = pipeline.MoeWeights(s)
+    pool, o1, o2 = inputs.moe_weight_pool(spec)
+    w.set_from_pool(torch.from_numpy(pool).cuda(), o1, o2, float(inputs.WEIGHT_STD))
+    b = pipeline.MoeBuffers(s)
+    x_t, _ = inputs.moe_x(spec)
+    logits_np = inputs.moe_logits(spec)
+    x_d = x_t.cuda()
+    logits_d = torch.from_numpy(logits_np).cuda()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    R = b.rows_max
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+
+    def step(events=None):
+        if events:
+            events[0].record(stream)
+        nv.moe_route_permute(logits_d, x_d, k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
+                             b.inv_perm, b.a1_q, b.a1_sf, b.workspace)
+        if events:
+            events[1].record(stream)
+        nv.nvfp4_grouped_gemm(b.a1_q, b.a1_sf, R, b.offsets, b.counts, E, 2 * I, H, w.w1_q, w.w1_sf, 1.0,
+                              nv.EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf)
+        if events:
+            events[2].record(stream)
+        nv.nvfp4_grouped_gemm(b.a2_q, b.a2_sf, R, b.offsets, b.counts, E, H, I, w.w2_q, w.w2_sf, 1.0,
+                              nv.EPI_BF16, out_bf16=b.rows_out)
+        if events:
+            events[3].record(stream)
+        nv.moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
+        if events:
+            events[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    nv.nvfp4_device_status()
+    torch.cuda.synchronize()
+
+    # ---- timed region: inputs resident in HBM
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    nv.nvfp4_device_status()
+    ms_local = start.elapsed_time(end)
+    ms = max_over_ranks(ms_local, world)
+    per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+           for j, name in enumerate(("route_permute", "l1_gemm_swiglu_nvfp4", "l2_gemm_bf16", "combine"))}
+
+    l1, l2 = ffn_flops(T, H, I, k)
+    step_flops = l1 + l2
+    value = world * args.steps * step_flops / (ms * 1e-3) / 1e12
+    tokens_per_s = world * args.steps * T / (ms * 1e-3)
+
+    # ---- end to end: pinned host inputs copied in, y copied out, every step
+    x_h = x_t.pin_memory()
+    logits_h = torch.from_numpy(logits_np).pin_memory()
+    y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    barrier(world)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(args.steps):
+        x_d.copy_(x_h, non_blocking=True)
+        logits_d.copy_(logits_h, non_blocking=True)
+        step()
+        y_h.copy_(b.y, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(s0.elapsed_time(s1), world)
+    e2e_value = world * args.steps * step_flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    pk = peaks()
+    fp4_peak = pk["bf16_sustained"] * FP4_OVER_BF16
+    l1_ms = per["l1_gemm_swiglu_nvfp4"]
+    achieved = l1 / (l1_ms * 1e-3) / 1e12
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r = OracleArm(dict(inputs.CONFIGS[WORKLOAD])).run(budget_s=args.cpu_budget, max_tokens=4096)
+        cpu = {"value": r["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{r['tokens']} sampled tokens of the prefill batch in {r['seconds']:.1f} s "
+                         "(float64 numpy; BLAS threads = cores, elementwise single-threaded)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> fp32 accum", "data": "synthetic",
+        "config": {"workload": _workload_name(spec), "tokens_per_rank": T, "rows_padded_max": R,
+                   "l2_policy": "inputs larger than L2 (5.7 GB of expert weights, 0.6 GB staged activations)",
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "tokens_per_s": tokens_per_s,
+        "kernel_ms": per,
+        "roofline": {"kernel": "nvf4_gemm_kernel<SwiGLU+NVFP4> (L1)", "bound": "tensor",
+                     "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
+                     "peak_source": f"{pk['source']} bf16 sustained {pk['bf16_sustained']} x {FP4_OVER_BF16:g} "
+                                    "(nominal FP4/BF16 dense ratio)",
+                     "algorithmic": "2*T*k*(2I)*H FLOP per launch (real rows only)",
+                     "traffic": None},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
+                "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": 8 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -67,7 +67,7 @@ CASES_BF16 = [
 def test_gemm_bf16_epilogue(nv, sizes, counts, N, K, alpha):
     rows_max = sum(sizes) + 128
     d, offs, a_deq, b_deq = _operands(nv, 11 + N + K, rows_max, sizes, N, K)
-    out = torch.full((rows_max, N), 12345.0, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((rows_max, N), 12288.0, dtype=torch.bfloat16, device="cuda")
     if counts is None:
         assert len(sizes) == 1
         nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], sizes[0], None, None, 1, N, K, d["b_q"], d["b_sf"], alpha,
@@ -84,7 +84,7 @@ def test_gemm_bf16_epilogue(nv, sizes, counts, N, K, alpha):
     assert np.mean(got[valid] == ref[valid]) > 0.97
     mask = np.ones(rows_max, bool)
     mask[valid] = False
-    assert np.all(got[mask] == 12345.0)               # nothing stored outside the real rows
+    assert np.all(got[mask] == 12288.0)               # nothing stored outside the real rows
 
 
 CASES_SWIGLU = [
