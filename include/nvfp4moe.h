@@ -151,6 +151,30 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
                                nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_route_permute_static -- moe_route_permute for callers that cannot allocate
+ * device memory (an engine that hands out all memory from a pool reserved up
+ * front, code under an allocator that must not see extra allocations, or a
+ * host path where cudaMalloc, which may synchronise the device, is not
+ * allowed).  The source pages have no counterpart of this call.
+ *   Arguments and outputs are those of moe_route_permute, without the
+ *   workspace: the scratch lives in a fixed 16 MiB device array inside the
+ *   library, reserved on every GPU that loads the library until the process
+ *   exits.  The call performs no cudaMalloc, cudaFree or other allocation.
+ *   Limit: moe_route_permute_workspace(T, H, E, top_k) <= 16 MiB (about 4100
+ *   tokens at H = 7168, E = 256); larger problems return NVFP4_ERR_UNSUPPORTED.
+ *   All calls on a device share the array and leave its contents behind (the
+ *   kernels overwrite every scratch byte before reading it); calls that overlap
+ *   on the GPU race on the array.  The first call on each device looks up the
+ *   array's device address (cudaGetSymbolAddress, with that device current):
+ *   make that first call before any stream capture.
+ * -------------------------------------------------------------------------- */
+nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, int32_t T, int32_t H,
+                                      int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
+                                      int32_t* expert_counts, int32_t* expert_offsets,
+                                      int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
+                                      uint8_t* a1_sf, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * nvfp4_grouped_gemm -- block-scaled NVFP4 grouped GEMM on the tcgen05 tensor
  * cores (the L1 "fused_swiglu" and L2 GEMMs of "NVFP4-1.1 Approach, Part 2"):
  *   acc[r, n] = sum_k dq(A)[r, k] * dq(B_g)[n, k] for the group g owning row r,

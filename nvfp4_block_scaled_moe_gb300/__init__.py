@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "Nvfp4Error", "lib_path", "load", "sf_bytes", "moe_padded_rows_max",
     "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
-    "moe_route_permute", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
+    "moe_route_permute", "moe_route_permute_static", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
     "moe_combine", "nvfp4_device_status", "nvfp4_selftest_bounded_wait",
     "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
 ]
@@ -57,6 +57,8 @@ _SIGS = {
     "nvfp4_moe_ffn_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp,
                                              _f32, _f32, _vp, _vp, _vp, _vp, _vp]),
     "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "moe_route_permute_static": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                _vp, _vp, _vp]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
@@ -128,6 +130,17 @@ def moe_route_permute(logits, x, top_k, topk_ids, topk_w, expert_counts, expert_
                                     _p(expert_counts), _p(expert_offsets), _p(perm_token), _p(inv_perm),
                                     _p(a1_q), _p(a1_sf), _p(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream)))
+
+
+def moe_route_permute_static(logits, x, top_k, topk_ids, topk_w, expert_counts, expert_offsets, perm_token,
+                             inv_perm, a1_q, a1_sf, stream=None):
+    """moe_route_permute with the library's fixed device scratch instead of a
+    caller workspace, for callers that cannot allocate (see include/nvfp4moe.h)."""
+    T, E = logits.shape
+    H = x.shape[1]
+    _check(load().moe_route_permute_static(_p(logits), _p(x), T, H, E, top_k, _p(topk_ids), _p(topk_w),
+                                           _p(expert_counts), _p(expert_offsets), _p(perm_token), _p(inv_perm),
+                                           _p(a1_q), _p(a1_sf), _stream(stream)))
 
 
 def nvfp4_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, alpha, epilogue,

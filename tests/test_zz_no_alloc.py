@@ -1,0 +1,71 @@
+"""moe_route_permute_static: the routing entry point for callers that cannot
+allocate device memory (engines that pre-reserve all memory in their own pool,
+code under allocators that must not see extra allocations, host paths that may
+not call cudaMalloc mid-step).  It keeps its scratch in a fixed device array
+inside the library instead of a caller workspace.
+
+Checked through the C ABI against moe_route_permute (the workspace version) on
+two calls in a row with different inputs: every output is identical, so the
+array's leftover contents from the first call do not leak into the second.
+This file is collected last so that a failure here stops a `-x` run only after
+every other test has run.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+
+from gpu_util import built_lib, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _buffers(pipeline, spec):
+    s = pipeline.MoeShape(T=spec["T"], H=spec["H"], I=256, E=spec["E"], top_k=spec["top_k"])
+    return pipeline.MoeBuffers(s)
+
+
+def _outputs(b, R):
+    return dict(ids=host(b.topk_ids), w=host(b.topk_w), counts=host(b.counts), offsets=host(b.offsets),
+                perm=host(b.perm_token)[:R], inv=host(b.inv_perm), a1_q=host(b.a1_q)[:R], a1_sf=host(b.a1_sf))
+
+
+def test_static_scratch_route_permute_matches_workspace_version_twice():
+    built_lib()
+    import nvfp4_block_scaled_moe_gb300 as nv
+    from nvfp4_block_scaled_moe_gb300 import pipeline
+
+    specs = [inputs.moe_spec(T=1000, H=1024, I=256, E=64, top_k=6, seed=41, zipf=True),
+             inputs.moe_spec(T=256, H=7168, I=256, E=256, top_k=8, seed=42)]      # decode-sized second call
+    for spec in specs:
+        logits = dev(inputs.moe_logits(spec))
+        x_t, _ = inputs.moe_x(spec)
+        x = x_t.cuda()
+        ref = _buffers(pipeline, spec)
+        nv.moe_route_permute(logits, x, spec["top_k"], ref.topk_ids, ref.topk_w, ref.counts, ref.offsets,
+                             ref.perm_token, ref.inv_perm, ref.a1_q, ref.a1_sf, ref.workspace)
+        got = _buffers(pipeline, spec)
+        got.a1_sf.copy_(ref.a1_sf)          # bytes past the groups are not written by either call
+        nv.moe_route_permute_static(logits, x, spec["top_k"], got.topk_ids, got.topk_w, got.counts, got.offsets,
+                                    got.perm_token, got.inv_perm, got.a1_q, got.a1_sf)
+        nv.nvfp4_device_status()
+        R = int(host(ref.offsets)[-1])
+        a, b = _outputs(ref, R), _outputs(got, R)
+        for key in a:
+            if key == "w":
+                assert np.allclose(a[key], b[key], rtol=2e-6, atol=1e-7), key
+            else:
+                assert np.array_equal(a[key], b[key]), key
+
+
+def test_static_scratch_rejects_problems_beyond_its_array():
+    built_lib()
+    import nvfp4_block_scaled_moe_gb300 as nv
+    lib = nv.load()
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = buf.data_ptr()
+    # 16384 tokens x 7168 hidden needs ~66 MB of staging: more than the fixed 16 MiB
+    st = lib.moe_route_permute_static(p, p, 16384, 7168, 256, 8, p, p, p, p, p, p, p, p, None)
+    assert st == 2
+    assert b"scratch" in lib.nvfp4_last_error()
