@@ -170,7 +170,8 @@ class OracleArm:
 def run_reference(args, world: int, rank: int) -> None:
     if rank != 0:
         return
-    spec = dict(inputs.CONFIGS[WORKLOAD])
+    name = args.workload if args.workload in ("prefill", "decode") else WORKLOAD
+    spec = dict(inputs.CONFIGS[name])
     arm = OracleArm(spec)
     tok, sec = 0, 0.0
     for i in range(args.warmup + args.steps):
@@ -185,19 +186,20 @@ def run_reference(args, world: int, rank: int) -> None:
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / max(args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": _workload_name(spec), "step": "oracle on one sampled token per step"},
+        "config": {"workload": _workload_name(spec, name), "step": "oracle on one sampled token per step"},
         "tokens_per_s": tok / sec,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{tok} sampled tokens of the prefill batch, one per step, expert "
+                         "sample": f"{tok} sampled tokens of the {name} batch, one per step, expert "
                                    "dequantisation cached across steps"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
 
-def _workload_name(spec: dict) -> str:
-    return (f"prefill NVFP4 MoE FFN T={spec['T']} H={spec['H']} I={spec['I']} E={spec['E']} "
-            f"top-{spec['top_k']} Zipf(1.2)-skewed routing")
+def _workload_name(spec: dict, name: str = WORKLOAD) -> str:
+    routing = "Zipf(1.2)-skewed routing" if spec.get("zipf") else "N(0,1) routing logits"
+    return (f"{name} NVFP4 MoE FFN T={spec['T']} H={spec['H']} I={spec['I']} E={spec['E']} "
+            f"top-{spec['top_k']} {routing}")
 
 
 # ------------------------------------------------------------ our GPU arm --
@@ -211,7 +213,7 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     nvbuild.build()
     nv.load()
     torch.cuda.set_device(local)
-    spec = dict(inputs.CONFIGS[WORKLOAD])
+    spec = dict(inputs.CONFIGS[args.workload])
     spec["seed"] = spec["seed"] + 1000 * rank if rank else spec["seed"]     # each rank its own batch
     T, H, I, E, k = spec["T"], spec["H"], spec["I"], spec["E"], spec["top_k"]
     s = pipeline.MoeShape(T=T, H=H, I=I, E=E, top_k=k)
@@ -305,15 +307,15 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     achieved = l1 / (l1_ms * 1e-3) / 1e12
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        r = OracleArm(dict(inputs.CONFIGS[WORKLOAD])).run(budget_s=args.cpu_budget, max_tokens=4096)
+        r = OracleArm(dict(inputs.CONFIGS[args.workload])).run(budget_s=args.cpu_budget, max_tokens=4096)
         cpu = {"value": r["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{r['tokens']} sampled tokens of the prefill batch in {r['seconds']:.1f} s "
+               "sample": f"{r['tokens']} sampled tokens of the {args.workload} batch in {r['seconds']:.1f} s "
                          "(float64 numpy; BLAS threads = cores, elementwise single-threaded)"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> fp32 accum", "data": "synthetic",
-        "config": {"workload": _workload_name(spec), "tokens_per_rank": T, "rows_padded_max": R,
+        "config": {"workload": _workload_name(spec, args.workload), "tokens_per_rank": T, "rows_padded_max": R,
                    "l2_policy": "inputs larger than L2 (5.7 GB of expert weights, 0.6 GB staged activations)",
                    "parallelism": f"replicas x{world} (independent batches)"},
         "tokens_per_s": tokens_per_s,
@@ -333,6 +335,128 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     print(json.dumps(line))
 
 
+def _flush_l2(buf):
+    buf.add_(1)                         # writes 256 MiB: evicts the 129 MB L2
+
+
+def run_dense(args, world: int, rank: int, local: int) -> None:
+    """The single-expert dense L1: A 8192 x 7168 x B 4096 x 7168 NVFP4 with the fused
+    SwiGLU + NVFP4 epilogue -> 8192 x 2048 NVFP4.  Inputs (44 MB) fit in L2, so L2 is
+    flushed between steps and each step is timed by its own CUDA events."""
+    import torch
+
+    import nvfp4_block_scaled_moe_gb300 as nv
+    from nvfp4_block_scaled_moe_gb300 import build as nvbuild
+
+    nvbuild.build()
+    torch.cuda.set_device(local)
+    spec = dict(inputs.CONFIGS["dense"])
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    a, bw = inputs.dense_inputs(spec)
+    a_d, b_d = torch.from_numpy(a).cuda(), torch.from_numpy(bw).cuda()
+    a_q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    a_sf = torch.empty(nv.sf_bytes(M, K), dtype=torch.uint8, device="cuda")
+    b_q = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    b_sf = torch.empty(nv.sf_bytes(N, K), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_quantize(a_d, K, nv.MODE_PLAIN, a_q, a_sf)
+    nv.nvfp4_quantize(b_d, K, nv.MODE_PLAIN, b_q, b_sf)
+    del a_d, b_d
+    out_q = torch.empty((M, N // 4), dtype=torch.uint8, device="cuda")
+    out_sf = torch.empty(nv.sf_bytes(M, N // 2), dtype=torch.uint8, device="cuda")
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_SWIGLU_NVFP4,
+                              out_q=out_q, out_sf=out_sf)
+
+    for _ in range(args.warmup):
+        step()
+    nv.nvfp4_device_status()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        _flush_l2(flush)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    nv.nvfp4_device_status()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    flops = 2.0 * M * N * K
+    tflops = flops / (ms * 1e-3) / 1e12
+    pk = peaks()
+    fp4_peak = pk["bf16"] * FP4_OVER_BF16
+    print(json.dumps({
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> fp32 accum", "data": "synthetic",
+        "config": {"workload": f"dense NVFP4 GEMM M={M} N={N} K={K} + SwiGLU + NVFP4 requant",
+                   "l2_policy": "L2 flushed (256 MiB write) before every step; per-step CUDA events"},
+        "roofline": {"kernel": "nvf4_gemm_kernel<SwiGLU+NVFP4>", "bound": "tensor", "achieved": tflops,
+                     "peak": fp4_peak, "unit": "TFLOP/s", "frac": tflops / fp4_peak,
+                     "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} x {FP4_OVER_BF16:g}",
+                     "algorithmic": "2*M*N*K FLOP per launch", "traffic": None},
+        "gpu_launches": args.steps, "clocks": clk}))
+
+
+def run_quantizer(args, world: int, rank: int, local: int) -> None:
+    """The standalone SwiGLU + NVFP4 quantiser on BF16 gate/up (32768, 2 x 2048):
+    HBM-bound, 306 MB moved per launch (inputs larger than L2)."""
+    import torch
+
+    import nvfp4_block_scaled_moe_gb300 as nv
+    from nvfp4_block_scaled_moe_gb300 import build as nvbuild
+
+    nvbuild.build()
+    torch.cuda.set_device(local)
+    spec = dict(inputs.CONFIGS["quantizer"])
+    rows, cols = spec["rows"], spec["cols"]
+    gu, _ = inputs.quantizer_input(spec)
+    gu_d = gu.cuda()
+    q = torch.empty((rows, cols // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty(nv.sf_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        nv.nvfp4_quantize(gu_d, cols, nv.MODE_SWIGLU_GU8, q, sf)
+
+    for _ in range(args.warmup):
+        step()
+    nv.nvfp4_device_status()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    nv.nvfp4_device_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = rows * 2 * cols * 2 + rows * cols // 2 + nv.sf_bytes(rows, cols)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    pk = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> nvfp4",
+        "data": "synthetic",
+        "config": {"workload": f"SwiGLU+NVFP4 quantiser BF16 gate/up ({rows}, 2x{cols})",
+                   "l2_policy": "inputs larger than L2 (268 MB read per step)"},
+        "roofline": {"kernel": "quantize_kernel<SWIGLU_GU8>", "bound": "hbm", "achieved": gbs,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                     "algorithmic": f"{nbytes} bytes per launch (input read + nibbles + SF written)",
+                     "traffic": None},
+        "gpu_launches": args.steps, "clocks": clk}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -341,12 +465,19 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("prefill", "decode", "dense", "quantizer"), default=WORKLOAD,
+                    help="prefill (default) and decode time the whole MoE FFN step; dense times the L1 GEMM of "
+                         "one 8192-row expert; quantizer the standalone SwiGLU + NVFP4 quantiser")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload == "dense":
+        run_dense(args, world, rank, local)
+    elif args.workload == "quantizer":
+        run_quantizer(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -178,6 +178,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// All 32 lanes wait; the result is the same on every lane (false if any gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              unsigned* err, uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, abort, err, limit_ns);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// One lane of a converged warp (the lowest active one) is elected.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ----------------------------------------------------------- TMA / bulk --
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

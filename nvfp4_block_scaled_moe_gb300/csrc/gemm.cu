@@ -140,63 +140,71 @@ __global__ void __launch_bounds__(192, 1)
   }
   const int32_t k4 = p.K / 64;        // scale atoms per 128-row band
 
+  // The producer and MMA warps run their loops with all 32 lanes converged, so
+  // every descriptor, coordinate and TMEM address is warp-uniform (held in the
+  // uniform datapath); one elected lane issues the TMA / tcgen05 instructions.
+  const uint32_t tmem_u = __shfl_sync(0xFFFFFFFFu, tmem_base, 0);
+  const int64_t tiles_u = __shfl_sync(0xFFFFFFFFu, num_tiles, 0);
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, filled = 0, fill_parity = 0;
-      bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int64_t mt = tile / p.n_tiles;
-        const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
-        const int g = find_group(s_off, p.G, mt * kBM);
-        const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
-        const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(nt) * k4) * 512;
-        for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+    uint32_t stage = 0, phase = 0, filled = 0, fill_parity = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < tiles_u && ok; tile += gridDim.x) {
+      const int64_t mt = tile / p.n_tiles;
+      const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
+      const int g = __shfl_sync(0xFFFFFFFFu, find_group(s_off, p.G, mt * kBM), 0);
+      const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
+      const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(nt) * k4) * 512;
+      for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+        ok = mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.err);
+        if (!ok) break;
+        if (elect_one()) {
           mbar_arrive_expect_tx(&full[stage], kStageTx);
           tma_load_2d(smem + kOffA + stage * kABytes, &tmap_a, &full[stage], kb * (kBK / 2),
                       static_cast<int32_t>(mt * kBM));
-          tma_load_2d(smem + kOffB + stage * kBBytes, &tmap_b, &full[stage], kb * (kBK / 2),
-                      g * p.N + nt * kBN);
+          tma_load_2d(smem + kOffB + stage * kBBytes, &tmap_b, &full[stage], kb * (kBK / 2), g * p.N + nt * kBN);
           bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa + kb * 4 * 512, kSfaBytes, &full[stage]);
           bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb + kb * 4 * 512, kSfbBytes, &full[stage]);
-          filled |= 1u << stage;
-          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        __syncwarp();
+        filled |= 1u << stage;
+        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) {
-        // let the copies already in flight land before the CTA can exit
-        int no_abort = 0;
-        for (int s = 0; s < kStages; ++s)
-          if ((filled >> s) & 1u) mbar_wait(&full[s], (fill_parity >> s) & 1u, &no_abort, nullptr, 50000000ull);
-      }
+    }
+    if (!ok) {
+      // let the copies already in flight land before the CTA can exit
+      int no_abort = 0;
+      for (int s = 0; s < kStages; ++s)
+        if ((filled >> s) & 1u) mbar_wait(&full[s], (fill_parity >> s) & 1u, &no_abort, nullptr, 50000000ull);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+    constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < tiles_u && ok; tile += gridDim.x) {
+      ok = mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_u + acc * kBN;
+      for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+        ok = mbar_wait_warp(&full[stage], phase, abort_flag, p.err);
+        if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
-          tc_fence_after_sync();
-          const uint32_t sfa_t = tmem_base + kTmemSf + stage * 32;
-          const uint32_t sfb_t = sfa_t + 16;
-          const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
-          const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
+        const uint32_t sfa_t = tmem_u + kTmemSf + stage * 32;
+        const uint32_t sfb_t = sfa_t + 16;
+        const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+        const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
+        const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + kOffA + stage * kABytes));
+        const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + kOffB + stage * kBBytes));
+        if (elect_one()) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             tc_copy_sf(sfa_t + 4 * j, sdesc_sf(sfa_s + 512 * j));
             tc_copy_sf(sfb_t + 4 * j, sdesc_sf(sfb_s + 512 * j));
           }
-          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + kOffA + stage * kABytes));
-          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + kOffB + stage * kBBytes));
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // K advance of 64 E2M1 = 32 bytes inside the 128-byte swizzle row
@@ -204,18 +212,21 @@ __global__ void __launch_bounds__(192, 1)
                         (kb | j) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit(&tfull[acc]);
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
-      // every MMA issued by this thread has completed before the CTA moves on
-      tc_commit(drain);
-      int no_abort = 0;
-      mbar_wait(drain, 0, &no_abort, p.err, 100000000ull);
+      if (!ok) break;
+      if (elect_one()) tc_commit(&tfull[acc]);
+      __syncwarp();
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
     }
+    // every MMA issued by the elected lane has completed before the CTA moves on
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    int no_abort = 0;
+    mbar_wait(drain, 0, &no_abort, p.err, 100000000ull);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
