@@ -7,25 +7,29 @@
 //     scales in the swizzled MMA layout);
 //   * alpha * acc -> BF16 rows (the L2 GEMM).
 //
-// Shape of the work: a tile is 128 rows x 128 columns of the output; the K loop
-// runs in stages of 256 elements (128 bytes of E2M1 per row = one 128-byte
-// swizzle row).  Rows are grouped (experts): group g owns rows
-// [offsets[g], offsets[g+1]) (multiples of 128) and multiplies with B_g.
+// Shape of the work: a tile is 128 rows x 256 columns of the output (one
+// tcgen05.mma of M=128, N=256, K=64 per 64 K elements -- the N=256 shape keeps
+// the tensor pipe busiest); the K loop runs in stages of 256 elements (128
+// bytes of E2M1 per row = one 128-byte swizzle row).  Rows are grouped
+// (experts): group g owns rows [offsets[g], offsets[g+1]) (multiples of 128)
+// and multiplies with B_g.
 //
-// One persistent CTA per SM, 6 warps, warp-specialised:
-//   warp 0     TMA producer: A and B tiles (2-D tensor maps, 128-byte swizzle) and
-//              the scale-factor atoms (contiguous 2 KiB bulk copies) into a
-//              6-stage shared-memory ring;
-//   warp 1     TMEM owner and MMA issuer: copies the stage's scale atoms into
-//              TMEM (tcgen05.cp 32x128b.warpx4) and issues four
-//              tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X (M=128, N=128,
-//              K=64) per stage into a double-buffered fp32 accumulator;
-//   warps 2-5  epilogue: tcgen05.ld 32x32b (one TMEM lane = one output row per
-//              thread, so a 16-block's amax needs no shuffles), math, stores.
-// Lessons kept from the pages' pipeline notes: the first MMA of a tile does not
-// accumulate; only the warps that need the TMEM address wait for it; barrier
-// arrival counts are in the units that actually arrive.
-// Every wait is bounded (a timeout sets the error word and lets the CTA exit).
+// One persistent CTA per SM, 10 warps, warp-specialised:
+//   warp 0     TMA producer: A (128 rows) and B (256 rows) tiles through 2-D tensor
+//              maps with 128-byte swizzle, and the scale-factor atoms (contiguous
+//              2 KiB bulk copies) into a 4-stage shared-memory ring;
+//   warp 1     TMEM owner and MMA issuer: copies the stage's scale atoms into TMEM
+//              (tcgen05.cp 32x128b.warpx4) and issues four tcgen05.mma kind::mxf4nvf4
+//              block_scale scale_vec::4X per stage into the fp32 accumulator;
+//   warps 2-9  epilogue, two warps per TMEM lane quadrant (one output row per
+//              thread, 128 accumulator columns per warp).  Each warp copies its
+//              columns from TMEM into registers and releases the accumulator at
+//              once, so the next tile's MMAs run while it computes and stores.
+// The producer and MMA warps run converged with warp-uniform operands and issue
+// through one elected lane.  Lessons kept from the pages' pipeline notes: the
+// first MMA of a tile does not accumulate; barrier arrival counts are in the
+// units that actually arrive.  Every wait is bounded (a timeout sets the error
+// word and lets the CTA exit).
 #include <mutex>
 
 #include "common.cuh"
@@ -34,12 +38,14 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 256;         // elements
-constexpr int kStages = 6;
+constexpr int kBM = 128, kBN = 256, kBK = 256;         // elements
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
-constexpr uint32_t kBBytes = kBN * kBK / 2;            // 16 KiB
+constexpr uint32_t kBBytes = kBN * kBK / 2;            // 32 KiB
 constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms of 512 B
-constexpr uint32_t kSfbBytes = kBN * (kBK / 16);       // 2 KiB
+constexpr uint32_t kSfbBytes = kBN * (kBK / 16);       // 4 KiB: 2 bands x 4 atoms
 constexpr uint32_t kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 constexpr int kMaxGroups = 1024;
 
@@ -48,17 +54,19 @@ constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;     // full, empty, tfull[2], tempty[2], drain
+constexpr uint32_t kNumBars = 2 * kStages + 3;         // full, empty, tfull, tempty, drain
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
 constexpr uint32_t kOffGroups = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kOffGroups + (kMaxGroups + 1) * 4 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffB % 1024 == 0 && kOffSfa % 1024 == 0, "swizzled tiles need 1 KiB alignment");
 
-// TMEM columns: two 128-column fp32 accumulators, then per stage 16 columns of
-// A scales (4 atoms x 4 columns) and 16 of B scales.
+// TMEM columns: the 256-column fp32 accumulator, then per stage 16 columns of
+// A scales (4 atoms x 4 columns) and 32 of B scales (2 bands x 4 atoms x 4).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemSf = 2 * kBN;
-static_assert(kTmemSf + kStages * 32 <= kTmemCols, "TMEM budget");
+constexpr uint32_t kTmemSf = kBN;
+constexpr uint32_t kTmemSfStage = 48;
+static_assert(kTmemSf + kStages * kTmemSfStage <= kTmemCols, "TMEM budget");
 
 struct Params {
   const uint8_t* a_sf;
@@ -86,8 +94,60 @@ __device__ __forceinline__ int find_group(const int32_t* off, int G, int64_t row
   return lo;
 }
 
+// L1 epilogue for one thread's row: 128 interleaved gate/up accumulator columns
+// (4 chunks of g(8) u(8) g(8) u(8)) -> 64 SwiGLU outputs -> 4 NVFP4 blocks.
+__device__ __forceinline__ void epilogue_swiglu(const float (&v)[4][32], float alpha, bool valid, int64_t grow,
+                                                int64_t col0, int32_t out_cols, uint32_t k4, uint32_t k4_total,
+                                                uint8_t* out_q, uint8_t* out_sf, float* h_debug) {
+  uint32_t sf_word = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float h0[8], h1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h0[i] = swiglu(alpha * v[c][i], alpha * v[c][8 + i]);
+      h1[i] = swiglu(alpha * v[c][16 + i], alpha * v[c][24 + i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(h0[i]), fabsf(h1[i])));
+    const BlockScale s = block_scale(amax);
+    const uint32_t lo = quantize8(h0, s), hi = quantize8(h1, s);
+    sf_word |= s.code << (8 * c);
+    if (valid) {
+      const int64_t col = col0 + 16 * c;
+      *reinterpret_cast<uint2*>(out_q + grow * (out_cols / 2) + col / 2) = make_uint2(lo, hi);
+      if (h_debug != nullptr) {
+        float4* hp = reinterpret_cast<float4*>(h_debug + grow * out_cols + col);
+        hp[0] = make_float4(h0[0], h0[1], h0[2], h0[3]);
+        hp[1] = make_float4(h0[4], h0[5], h0[6], h0[7]);
+        hp[2] = make_float4(h1[0], h1[1], h1[2], h1[3]);
+        hp[3] = make_float4(h1[4], h1[5], h1[6], h1[7]);
+      }
+    }
+  }
+  if (valid) *reinterpret_cast<uint32_t*>(out_sf + sf_word_offset(grow, k4, k4_total)) = sf_word;
+}
+
+// L2 epilogue for one thread's row: alpha * 128 accumulator columns -> BF16.
+__device__ __forceinline__ void epilogue_bf16(const float (&v)[4][32], float alpha, __nv_bfloat16* dst_row) {
+  uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 o;
+      o.x = pack_bf16x2(alpha * v[c][8 * q + 0], alpha * v[c][8 * q + 1]);
+      o.y = pack_bf16x2(alpha * v[c][8 * q + 2], alpha * v[c][8 * q + 3]);
+      o.z = pack_bf16x2(alpha * v[c][8 * q + 4], alpha * v[c][8 * q + 5]);
+      o.w = pack_bf16x2(alpha * v[c][8 * q + 6], alpha * v[c][8 * q + 7]);
+      dst[4 * c + q] = o;
+    }
+  }
+}
+
 template <int kEpi>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -95,8 +155,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + kOffGroups);
@@ -107,10 +167,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);      // one arrival per epilogue warp
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, kEpiWarps);    // one arrival per epilogue warp
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -154,7 +212,8 @@ __global__ void __launch_bounds__(192, 1)
       const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
       const int g = __shfl_sync(0xFFFFFFFFu, find_group(s_off, p.G, mt * kBM), 0);
       const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
-      const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(nt) * k4) * 512;
+      const uint8_t* sfb0 = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(2 * nt) * k4) * 512;
+      const uint8_t* sfb1 = sfb0 + static_cast<int64_t>(k4) * 512;
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.err);
         if (!ok) break;
@@ -164,7 +223,9 @@ __global__ void __launch_bounds__(192, 1)
                       static_cast<int32_t>(mt * kBM));
           tma_load_2d(smem + kOffB + stage * kBBytes, &tmap_b, &full[stage], kb * (kBK / 2), g * p.N + nt * kBN);
           bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa + kb * 4 * 512, kSfaBytes, &full[stage]);
-          bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb + kb * 4 * 512, kSfbBytes, &full[stage]);
+          bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb0 + kb * 4 * 512, kSfbBytes / 2, &full[stage]);
+          bulk_load(smem + kOffSfb + stage * kSfbBytes + kSfbBytes / 2, sfb1 + kb * 4 * 512, kSfbBytes / 2,
+                    &full[stage]);
         }
         __syncwarp();
         filled |= 1u << stage;
@@ -182,18 +243,17 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
-    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; tile < tiles_u && ok; tile += gridDim.x) {
-      ok = mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err);
+      ok = mbar_wait_warp(tempty, acc_phase ^ 1u, abort_flag, p.err);
       if (!ok) break;
       tc_fence_after_sync();
-      const uint32_t d_tmem = tmem_u + acc * kBN;
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&full[stage], phase, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t sfa_t = tmem_u + kTmemSf + stage * 32;
+        const uint32_t sfa_t = tmem_u + kTmemSf + stage * kTmemSfStage;
         const uint32_t sfb_t = sfa_t + 16;
         const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
         const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
@@ -203,12 +263,13 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             tc_copy_sf(sfa_t + 4 * j, sdesc_sf(sfa_s + 512 * j));
-            tc_copy_sf(sfb_t + 4 * j, sdesc_sf(sfb_s + 512 * j));
+            tc_copy_sf(sfb_t + 8 * j, sdesc_sf(sfb_s + 512 * j));                      // B rows 0..127
+            tc_copy_sf(sfb_t + 8 * j + 4, sdesc_sf(sfb_s + kSfbBytes / 2 + 512 * j));  // B rows 128..255
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // K advance of 64 E2M1 = 32 bytes inside the 128-byte swizzle row
-            tc_mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 4 * j,
+            tc_mma_nvf4(tmem_u, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
                         (kb | j) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
@@ -217,10 +278,9 @@ __global__ void __launch_bounds__(192, 1)
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      if (elect_one()) tc_commit(&tfull[acc]);
+      if (elect_one()) tc_commit(tfull);
       __syncwarp();
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      acc_phase ^= 1u;
     }
     // every MMA issued by the elected lane has completed before the CTA moves on
     if (elect_one()) tc_commit(drain);
@@ -231,8 +291,9 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t quad = warp & 3;                // TMEM lanes 32*quad .. +31
+    const uint32_t half = (warp - 2) >> 2;         // accumulator columns 128*half .. +127
     const uint32_t row_in_tile = quad * 32 + lane;
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int64_t mt = tile / p.n_tiles;
       const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
@@ -240,67 +301,23 @@ __global__ void __launch_bounds__(192, 1)
       const int g = find_group(s_off, p.G, mt * kBM);
       bool valid = true;
       if (p.counts != nullptr) valid = (grow - s_off[g]) < __ldg(p.counts + g);
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      if (!mbar_wait(tfull, acc_phase, abort_flag, p.err)) break;
       tc_fence_after_sync();
-      const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + acc * kBN;
-      if constexpr (kEpi == NVFP4_EPI_SWIGLU_NVFP4) {
-        const int32_t out_cols = p.N / 2;
-        uint32_t sf_word = 0;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_load32(t_row + 32 * c, v);
-          // columns: gate(8) up(8) gate(8) up(8) -> 16 consecutive outputs
-          float h0[8], h1[8];
+      float v[4][32];
+      const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + half * 128u;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            h0[i] = swiglu(p.alpha * v[i], p.alpha * v[8 + i]);
-            h1[i] = swiglu(p.alpha * v[16 + i], p.alpha * v[24 + i]);
-          }
-          float amax = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(h0[i]), fabsf(h1[i])));
-          const BlockScale s = block_scale(amax);
-          const uint32_t lo = quantize8(h0, s), hi = quantize8(h1, s);
-          sf_word |= s.code << (8 * c);
-          if (valid) {
-            const int64_t col = static_cast<int64_t>(nt) * 64 + 16 * c;
-            *reinterpret_cast<uint2*>(p.out_q + grow * (out_cols / 2) + col / 2) = make_uint2(lo, hi);
-            if (p.h_debug != nullptr) {
-              float4* hp = reinterpret_cast<float4*>(p.h_debug + grow * out_cols + col);
-              hp[0] = make_float4(h0[0], h0[1], h0[2], h0[3]);
-              hp[1] = make_float4(h0[4], h0[5], h0[6], h0[7]);
-              hp[2] = make_float4(h1[0], h1[1], h1[2], h1[3]);
-              hp[3] = make_float4(h1[4], h1[5], h1[6], h1[7]);
-            }
-          }
-        }
-        if (valid)
-          *reinterpret_cast<uint32_t*>(p.out_sf + sf_word_offset(grow, nt, p.n_tiles)) = sf_word;
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_load32(t_row + 32 * c, v);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + grow * p.N + static_cast<int64_t>(nt) * kBN + 32 * c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 o;
-              o.x = pack_bf16x2(p.alpha * v[8 * q + 0], p.alpha * v[8 * q + 1]);
-              o.y = pack_bf16x2(p.alpha * v[8 * q + 2], p.alpha * v[8 * q + 3]);
-              o.z = pack_bf16x2(p.alpha * v[8 * q + 4], p.alpha * v[8 * q + 5]);
-              o.w = pack_bf16x2(p.alpha * v[8 * q + 6], p.alpha * v[8 * q + 7]);
-              dst[q] = o;
-            }
-          }
-        }
-      }
+      for (int c = 0; c < 4; ++c) tmem_load32(t_row + 32 * c, v[c]);
+      // the accumulator is in registers: hand it back to the MMA warp
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive(tempty);
+      acc_phase ^= 1u;
+      if constexpr (kEpi == NVFP4_EPI_SWIGLU_NVFP4) {
+        epilogue_swiglu(v, p.alpha, valid, grow, static_cast<int64_t>(nt) * (kBN / 2) + half * 64, p.N / 2,
+                        2 * nt + half, static_cast<uint32_t>(p.N / 128), p.out_q, p.out_sf, p.h_debug);
+      } else {
+        if (valid) epilogue_bf16(v, p.alpha, p.out_bf16 + grow * p.N + static_cast<int64_t>(nt) * kBN + half * 128);
+      }
     }
   }
 
@@ -366,7 +383,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p
     if (e != cudaSuccess) return e;
     info.attr_set[kEpi] = true;
   }
-  nvf4_gemm_kernel<kEpi><<<grid, 192, kSmemBytes, stream>>>(ma, mb, p);
+  nvf4_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 

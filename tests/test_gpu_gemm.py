@@ -56,9 +56,9 @@ def _valid_rows(offs, counts):
 
 CASES_BF16 = [
     # (group padded sizes, counts or None, N, K, alpha)
-    ([128], None, 128, 256, 1.0),                     # one tile, one K stage
-    ([256], None, 256, 512, 1.0),
-    ([128, 0, 384, 128], [100, 0, 300, 128], 384, 768, 0.75),
+    ([128], None, 256, 256, 1.0),                     # one tile, one K stage
+    ([256], None, 512, 512, 1.0),
+    ([128, 0, 384, 128], [100, 0, 300, 128], 768, 768, 0.75),
     ([128] * 40, [128 - (i % 7) for i in range(40)], 1024, 1280, 1.0),   # > one wave of tiles
 ]
 
@@ -88,7 +88,7 @@ def test_gemm_bf16_epilogue(nv, sizes, counts, N, K, alpha):
 
 
 CASES_SWIGLU = [
-    ([128], None, 128, 256, 1.0),
+    ([128], None, 256, 256, 1.0),
     ([256, 128], [200, 128], 512, 1024, 1.25),
     ([128, 128, 0, 256], [1, 128, 0, 129], 256, 512, 0.5),
 ]
@@ -138,9 +138,9 @@ def test_gemm_uniform_vs_random_scales_both_match(nv):
 def test_gemm_one_hot_locates_nibbles_and_scales(nv):
     """A single nonzero A element at (r, k) and a single nonzero B element at (n, k):
     the product appears only at (r, n), scaled by both blocks' scales."""
-    K, N, M = 512, 128, 128
+    K, N, M = 512, 256, 128
     rng = np.random.default_rng(9)
-    for r, n, k in ((0, 0, 0), (5, 77, 37), (127, 127, 511), (64, 3, 300), (33, 96, 64)):
+    for r, n, k in ((0, 0, 0), (5, 77, 37), (127, 255, 511), (64, 3, 300), (33, 200, 64), (100, 128, 130)):
         a_q = np.zeros((M, K // 2), np.uint8)
         b_q = np.zeros((1, N, K // 2), np.uint8)
         a_q[r, k // 2] = (0x3 << 4) if k % 2 else 0x3          # 1.5
