@@ -62,33 +62,49 @@ __device__ __forceinline__ uint32_t e2m1x8_from_halfsteps(const float (&v)[8]) {
   return out;
 }
 
-// Block scale of a 16-block from its amax: E4M3(fp32(amax / 6)).
+// RN(a / 6) for a >= 0 without a division routine.  y = RN(1/6) = 0x3E2AAAAB
+// (1/6 = 1.0101...b x 2^-3; the 24th significant bit and a nonzero tail round the
+// 23-bit fraction 0x2AAAAA up).  Markstein's theorem: with y = RN(1/b), q a
+// faithful approximation of a/b and r = a - b*q (exact through the FMA),
+// RN(q + r*y) = RN(a/b).  Results below 2^-126 may differ, which cannot change an
+// E4M3 code (everything below 2^-10 encodes as 0).
+__device__ __forceinline__ float div6_rn(float a) {
+  const float y = __uint_as_float(0x3E2AAAABu);
+  const float q0 = a * y;
+  const float r = fmaf(-q0, 6.0f, a);
+  return fmaf(r, y, q0);
+}
+
+// Block scale of a 16-block from its amax: E4M3(fp32(amax / 6)).  Kept as
+// d2 = d/2 and r2 = RN(1/d2) = 2 RN(1/d) (exact scalings) so that the per-value
+// path yields the half-step count 2|x|/d directly.
 struct BlockScale {
   uint32_t code;  // E4M3 byte
-  float d;        // decoded scale (0 for a zero scale)
-  float r;        // correctly rounded 1/d, 0 for a zero scale
+  float d2;       // decoded scale / 2 (0 for a zero scale)
+  float r2;       // RN(2 / decoded scale), 0 for a zero scale
 };
 
 __device__ __forceinline__ BlockScale block_scale(float amax) {
   BlockScale s;
-  s.code = e4m3_from_f32(__fdiv_rn(amax, 6.0f));
-  s.d = f32_from_e4m3(s.code);
-  s.r = s.d > 0.0f ? __frcp_rn(s.d) : 0.0f;
+  s.code = e4m3_from_f32(div6_rn(amax));
+  s.d2 = 0.5f * f32_from_e4m3(s.code);
+  s.r2 = s.d2 > 0.0f ? __frcp_rn(s.d2) : 0.0f;
   return s;
 }
 
 // Signed half step of x / d: copysign(rne(2 * min(|x / d|, 6)) / 2, x).
-// |x| / d is the IEEE-correctly-rounded fp32 quotient, obtained from the
-// correctly rounded reciprocal r with one FMA residual correction (Markstein's
-// division theorem: q' = RN(q + (a - b q) y) equals RN(a / b) when y = RN(1/b)
-// and q is within one ulp).  With d == 0 (r == 0) the magnitude is 0.
+// q = RN(|x| / d2) = RN(2|x| / d) = 2 RN(|x| / d) is the IEEE quotient, obtained
+// from the correctly rounded reciprocal r2 with one FMA residual correction
+// (Markstein, as in div6_rn).  min(q, 12) is rounded to an integer with ties to
+// even by adding 1.5 * 2^23 (every float in [2^23, 2^24) is an integer), and
+// (t - 1.5 * 2^23) / 2 is exact.  With a zero scale (r2 == 0) the magnitude is 0.
 __device__ __forceinline__ float signed_halfstep(float x, const BlockScale& s) {
   const float a = fabsf(x);
-  const float q0 = a * s.r;
-  const float rem = fmaf(-q0, s.d, a);
-  const float q = fmaf(rem, s.r, q0);
-  const float hs = rintf(fminf(q, 6.0f) * 2.0f);
-  return copysignf(hs * 0.5f, x);
+  const float q0 = a * s.r2;
+  const float rem = fmaf(-q0, s.d2, a);
+  const float q = fmaf(rem, s.r2, q0);
+  const float t = fminf(q, 12.0f) + 12582912.0f;
+  return copysignf(fmaf(t, 0.5f, -6291456.0f), x);
 }
 
 // Quantise eight values of one half-block with that block's scale.

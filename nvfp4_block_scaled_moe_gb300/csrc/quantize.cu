@@ -39,21 +39,19 @@ __device__ __forceinline__ void load_values(const void* in, int64_t row, int64_t
   }
 }
 
-// One warp per (row, 256-column segment).  rows_pad >= rows covers the zero
-// padding rows of the swizzled SF; sf_linear selects a plain row-major SF
-// output ([rows, cols/16], used for staging x in moe_route_permute; requires
-// cols % 64 == 0).
+// One warp per (row, 256-column segment): blockIdx.x is the row (rows_pad >=
+// rows covers the zero padding rows of the swizzled SF), blockIdx.y * 8 + warp the
+// segment.  sf_linear selects a plain row-major SF output ([rows, cols/16], used
+// for staging x in moe_route_permute; requires cols % 64 == 0).
 template <int kMode, int kDtype>
 __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ in, int64_t rows,
                                                        int64_t cols, int64_t ld, int64_t rows_pad,
                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                        int sf_linear, float* __restrict__ h_dbg) {
   const int lane = threadIdx.x & 31;
-  const int64_t segs = (cols + 255) / 256;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (warp >= rows_pad * segs) return;
-  const int64_t row = warp / segs;
-  const int64_t seg = warp - row * segs;
+  const int64_t seg = static_cast<int64_t>(blockIdx.y) * 8 + (threadIdx.x >> 5);
+  if (seg * 256 >= cols) return;
+  const int64_t row = blockIdx.x;
   const int64_t c0 = seg * 256 + lane * 8;
   const bool in_row = row < rows;
   const bool active = in_row && c0 < cols;
@@ -102,11 +100,10 @@ template <int kMode, int kDtype>
 static cudaError_t launch_quantize(const void* in, int64_t rows, int64_t cols, int64_t ld,
                                    int64_t rows_pad, uint8_t* q, uint8_t* sf, int sf_linear,
                                    float* h_dbg, cudaStream_t stream) {
-  const int64_t warps = rows_pad * ((cols + 255) / 256);
-  const int64_t blocks = (warps + 7) / 8;
-  if (blocks == 0) return cudaSuccess;
-  quantize_kernel<kMode, kDtype><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      in, rows, cols, ld, rows_pad, q, sf, sf_linear, h_dbg);
+  const int64_t segs = (cols + 255) / 256;
+  if (rows_pad == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(rows_pad), static_cast<unsigned>((segs + 7) / 8));
+  quantize_kernel<kMode, kDtype><<<grid, 256, 0, stream>>>(in, rows, cols, ld, rows_pad, q, sf, sf_linear, h_dbg);
   return cudaGetLastError();
 }
 
