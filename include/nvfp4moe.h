@@ -139,7 +139,8 @@ nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_s
  *   a1_q        [R_max, H/2] NVFP4 rows of x in permuted order; padding rows
  *               inside groups are zero.
  *   a1_sf       nvfp4_sf_bytes(R_max, H) bytes, swizzled, zero on padding rows.
- *   workspace   >= moe_route_permute_workspace(T, H, E, top_k) bytes, 256-aligned.
+ *   workspace   >= moe_route_permute_workspace(T, H, E, top_k) bytes, 16-byte
+ *               aligned (per-chunk expert histograms, cleared by the call).
  * Limits: 1 <= E <= 1024, 1 <= top_k <= min(E, 32), H a positive multiple of 64,
  * T >= 0 (T == 0 writes zero offsets and counts).
  * -------------------------------------------------------------------------- */
@@ -160,10 +161,10 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
  *   workspace: the scratch lives in a fixed 16 MiB device array inside the
  *   library, reserved on every GPU that loads the library until the process
  *   exits.  The call performs no cudaMalloc, cudaFree or other allocation.
- *   Limit: moe_route_permute_workspace(T, H, E, top_k) <= 16 MiB (about 4100
- *   tokens at H = 7168, E = 256); larger problems return NVFP4_ERR_UNSUPPORTED.
- *   All calls on a device share the array and leave its contents behind (the
- *   kernels overwrite every scratch byte before reading it); calls that overlap
+ *   Limit: moe_route_permute_workspace(T, H, E, top_k) <= 16 MiB (about 2
+ *   million tokens at E = 256); larger problems return NVFP4_ERR_UNSUPPORTED.
+ *   All calls on a device share the array and leave its contents behind (each
+ *   call clears the part it counts into first); calls that overlap
  *   on the GPU race on the array.  The first call on each device looks up the
  *   array's device address (cudaGetSymbolAddress, with that device current):
  *   make that first call before any stream capture.

@@ -93,9 +93,7 @@ int64_t moe_padded_rows_max(int32_t T, int32_t E, int32_t top_k) {
 size_t moe_route_permute_workspace(int32_t T, int32_t H, int32_t E, int32_t top_k) {
   (void)top_k;
   if (T < 0 || H <= 0 || E <= 0) return 0;
-  const size_t n_chunks = (static_cast<size_t>(T) + kRouteChunk - 1) / kRouteChunk;
-  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  return up(n_chunks * E * sizeof(int32_t)) + up(static_cast<size_t>(T) * H / 2) + up(static_cast<size_t>(T) * H / 16) + 256;
+  return route_workspace_bytes(T, E);
 }
 
 const char* nvfp4_last_error(void) { return g_msg; }
@@ -165,14 +163,7 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
   b.a1_q = a1_q;
   b.a1_sf = a1_sf;
   b.rows_max = moe_padded_rows_max(T, E, top_k);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t n_chunks = (static_cast<size_t>(T) + kRouteChunk - 1) / kRouteChunk;
-  b.chunk_hist = reinterpret_cast<int32_t*>(ws);
-  ws += up(n_chunks * E * sizeof(int32_t));
-  b.x_q = ws;
-  ws += up(static_cast<size_t>(T) * H / 2);
-  b.x_sf = ws;
+  route_carve_workspace(b, workspace);
   cudaError_t e = route_permute_launch(b, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_route_permute");
 }

@@ -30,13 +30,14 @@ struct RouteBuffers {
   uint8_t* a1_q;
   uint8_t* a1_sf;
   int64_t rows_max;
-  // workspace carve-up
-  int32_t* chunk_hist;   // [n_chunks, E]
-  uint8_t* x_q;          // [T, H/2]
-  uint8_t* x_sf;         // [T, H/16] row-major
+  int32_t* chunk_hist;   // workspace: [n_chunks, E] expert counts per token chunk
 };
 
-constexpr int kRouteChunk = 128;   // tokens per routing block
+constexpr int kRouteChunk = 128;   // tokens per routing chunk
+
+// Workspace bytes of moe_route_permute and its carve-up (the chunk histogram).
+size_t route_workspace_bytes(int32_t T, int32_t E);
+void route_carve_workspace(RouteBuffers& b, void* workspace);
 
 cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream);
 

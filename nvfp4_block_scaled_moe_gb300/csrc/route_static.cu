@@ -5,18 +5,19 @@
 // front, code running under a custom allocator that must not see extra
 // allocations, or a host path that is not allowed to call cudaMalloc (which can
 // synchronise the device) in the middle of a step.  For them this entry point
-// keeps the routing scratch (per-chunk expert histograms and the NVFP4 staging
-// copy of x) in one file-scope device array of kStaticScratchBytes, which the
+// keeps the routing scratch (the per-chunk expert histograms) in one
+// file-scope device array of kStaticScratchBytes, which the
 // CUDA module reserves on every GPU that loads the library for the life of the
 // process.  The entry point itself calls no cudaMalloc, cudaFree or allocating
 // library routine.
 //
 // Rules for callers:
 //   * the scratch limit: moe_route_permute_workspace(T, H, E, top_k) must not
-//     exceed kStaticScratchBytes (16 MiB; e.g. up to ~4100 tokens at H = 7168,
-//     E = 256); larger problems are rejected with NVFP4_ERR_UNSUPPORTED;
+//     exceed kStaticScratchBytes (16 MiB: ceil(T/128) * E * 4 bytes, e.g. up to
+//     about 2 million tokens at E = 256); larger problems are rejected with
+//     NVFP4_ERR_UNSUPPORTED;
 //   * every call on a device shares the one array and leaves its contents
-//     behind; the kernels overwrite every scratch byte they later read, so no
+//     behind; each call clears the histogram it uses before counting, so no
 //     state leaks between calls, but calls that overlap on the GPU (on two
 //     streams, or from two host threads without ordering) race on the array;
 //   * the first call on each device looks up the array's device address with
@@ -101,13 +102,7 @@ extern "C" nvfp4_status moe_route_permute_static(const float* logits, const void
   b.a1_q = a1_q;
   b.a1_sf = a1_sf;
   b.rows_max = moe_padded_rows_max(T, E, top_k);
-  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t n_chunks = (static_cast<size_t>(T) + kRouteChunk - 1) / kRouteChunk;
-  b.chunk_hist = reinterpret_cast<int32_t*>(ws);
-  ws += up(n_chunks * E * sizeof(int32_t));
-  b.x_q = ws;
-  ws += up(static_cast<size_t>(T) * H / 2);
-  b.x_sf = ws;
+  route_carve_workspace(b, ws);
   cudaError_t e = route_permute_launch(b, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_route_permute_static");
 }

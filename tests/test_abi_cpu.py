@@ -51,7 +51,9 @@ def test_size_helpers(lib):
     r = lib.moe_padded_rows_max(16384, 256, 8)
     assert r % 128 == 0 and r >= 16384 * 8 and r <= 16384 * 8 + 127 * 256
     assert lib.moe_padded_rows_max(1, 256, 8) == 1024        # 8 rows, each its own group
-    assert lib.moe_route_permute_workspace(256, 7168, 256, 8) >= 256 * 7168 // 2
+    # the workspace holds one int32 expert count per (128-token chunk, expert)
+    assert lib.moe_route_permute_workspace(256, 7168, 256, 8) >= 2 * 256 * 4
+    assert lib.moe_route_permute_workspace(16384, 7168, 256, 8) >= 128 * 256 * 4
 
 
 @needs_nvcc
