@@ -194,7 +194,8 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
  *               swizzled; h_debug NULL or fp32 [rows_max, N/2].
  *               NVFP4_EPI_BF16: out_bf16 BF16 [rows_max, N].
- * Limits: K a positive multiple of 256, N a positive multiple of 256, rows_max a
+ * Limits: K a positive multiple of 256, N a positive multiple of 256 (SWIGLU) or
+ * 128 (BF16), rows_max a
  * positive multiple of 128, all pointers 16-byte aligned.
  * -------------------------------------------------------------------------- */
 nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,

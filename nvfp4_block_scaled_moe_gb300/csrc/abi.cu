@@ -181,7 +181,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
   CHECK_ARG(G >= 1 && N > 0 && K > 0 && rows_max > 0, "nvfp4_grouped_gemm: sizes must be positive");
   CHECK_SUP(group_offsets || G == 1, "nvfp4_grouped_gemm: NULL group_offsets means G == 1");
   CHECK_SUP(K % 256 == 0, "nvfp4_grouped_gemm: K=%d is not a multiple of 256", K);
-  CHECK_SUP(N % 256 == 0, "nvfp4_grouped_gemm: N=%d is not a multiple of 256", N);
+  CHECK_SUP(N % (epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? 256 : 128) == 0,
+            "nvfp4_grouped_gemm: N=%d is not a multiple of %d", N, epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? 256 : 128);
   CHECK_SUP(rows_max % 128 == 0 && rows_max < (int64_t(1) << 31), "nvfp4_grouped_gemm: rows_max=%lld",
             (long long)rows_max);
   CHECK_SUP(static_cast<int64_t>(G) * N < (int64_t(1) << 31), "nvfp4_grouped_gemm: G*N too large");

@@ -38,35 +38,45 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 256;         // elements
-constexpr int kStages = 4;
+constexpr int kBM = 128, kBK = 256;                    // elements
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
-constexpr uint32_t kBBytes = kBN * kBK / 2;            // 32 KiB
 constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms of 512 B
-constexpr uint32_t kSfbBytes = kBN * (kBK / 16);       // 4 KiB: 2 bands x 4 atoms
-constexpr uint32_t kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 constexpr int kMaxGroups = 1024;
-
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kOffA + kStages * kABytes;
-constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
-constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr uint32_t kNumBars = 2 * kStages + 3;         // full, empty, tfull, tempty, drain
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
-constexpr uint32_t kOffGroups = kOffMisc + 16;
-constexpr uint32_t kSmemBytes = kOffGroups + (kMaxGroups + 1) * 4 + 1024;   // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffB % 1024 == 0 && kOffSfa % 1024 == 0, "swizzled tiles need 1 KiB alignment");
-
-// TMEM columns: the 256-column fp32 accumulator, then per stage 16 columns of
-// A scales (4 atoms x 4 columns) and 32 of B scales (2 bands x 4 atoms x 4).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemSf = kBN;
-constexpr uint32_t kTmemSfStage = 48;
-static_assert(kTmemSf + kStages * kTmemSfStage <= kTmemCols, "TMEM budget");
+
+// Tile configuration by output-tile width BN:
+//   BN = 256 (the L1 / SwiGLU kernel, long K): one 256-column accumulator, 4 stages;
+//   BN = 128 (the BF16 kernel, L2's short K = I): two 128-column accumulators so
+//     the next tile's MMAs overlap the hand-off of the previous one, 6 stages.
+// TMEM: the accumulators first, then per stage 16 columns of A scales (4 atoms x
+// 4 columns) and 16 per 128-row band of B scales.
+template <int BN>
+struct Cfg {
+  static constexpr int kBN = BN;
+  static constexpr int kAcc = BN == 256 ? 1 : 2;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kBands = BN / 128;
+  static constexpr int kChunks = BN / 64;              // 32-column chunks per epilogue warp
+  static constexpr uint32_t kBBytes = BN * kBK / 2;
+  static constexpr uint32_t kSfbBytes = BN * (kBK / 16);
+  static constexpr uint32_t kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr uint32_t kOffA = 0;
+  static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+  static constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
+  static constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
+  static constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
+  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kAcc + 1;   // full, empty, tfull, tempty, drain
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;     // tmem slot, abort flag
+  static constexpr uint32_t kOffGroups = kOffMisc + 16;
+  static constexpr uint32_t kSmemBytes = kOffGroups + (kMaxGroups + 1) * 4 + 1024;   // + alignment slack
+  static constexpr uint32_t kTmemSf = kAcc * BN;
+  static constexpr uint32_t kTmemSfStage = 16 + 16 * kBands;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOffB % 1024 == 0 && kOffSfa % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+  static_assert(kTmemSf + kStages * kTmemSfStage <= kTmemCols, "TMEM budget");
+};
 
 struct Params {
   const uint8_t* a_sf;
@@ -129,11 +139,12 @@ __device__ __forceinline__ void epilogue_swiglu(const float (&v)[4][32], float a
   if (valid) *reinterpret_cast<uint32_t*>(out_sf + sf_word_offset(grow, k4, k4_total)) = sf_word;
 }
 
-// L2 epilogue for one thread's row: alpha * 128 accumulator columns -> BF16.
-__device__ __forceinline__ void epilogue_bf16(const float (&v)[4][32], float alpha, __nv_bfloat16* dst_row) {
+// L2 epilogue for one thread's row: alpha * (32 * kChunks) accumulator columns -> BF16.
+template <int kChunks>
+__device__ __forceinline__ void epilogue_bf16(const float (&v)[kChunks][32], float alpha, __nv_bfloat16* dst_row) {
   uint4* dst = reinterpret_cast<uint4*>(dst_row);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint4 o;
@@ -146,20 +157,26 @@ __device__ __forceinline__ void epilogue_bf16(const float (&v)[4][32], float alp
   }
 }
 
-template <int kEpi>
+template <int kEpi, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const Params p) {
+  using C = Cfg<BN>;
+  constexpr int kStages = C::kStages, kAcc = C::kAcc, kBN = C::kBN, kBands = C::kBands;
+  constexpr uint32_t kBBytes = C::kBBytes, kSfbBytes = C::kSfbBytes, kStageTx = C::kStageTx;
+  constexpr uint32_t kOffA = C::kOffA, kOffB = C::kOffB, kOffSfa = C::kOffSfa, kOffSfb = C::kOffSfb;
+  constexpr uint32_t kTmemSf = C::kTmemSf, kTmemSfStage = C::kTmemSfStage;
+  static_assert(kEpi != NVFP4_EPI_SWIGLU_NVFP4 || BN == 256, "the SwiGLU epilogue uses 256-column tiles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* drain = tempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kOffGroups);
+  uint64_t* tempty = tfull + kAcc;
+  uint64_t* drain = tempty + kAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + C::kOffGroups);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -167,8 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, kEpiWarps);    // one arrival per epilogue warp
+    for (int a = 0; a < kAcc; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps);    // one arrival per epilogue warp
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -212,8 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
       const int g = __shfl_sync(0xFFFFFFFFu, find_group(s_off, p.G, mt * kBM), 0);
       const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
-      const uint8_t* sfb0 = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(2 * nt) * k4) * 512;
-      const uint8_t* sfb1 = sfb0 + static_cast<int64_t>(k4) * 512;
+      const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(kBands * nt) * k4) * 512;
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.err);
         if (!ok) break;
@@ -223,9 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       static_cast<int32_t>(mt * kBM));
           tma_load_2d(smem + kOffB + stage * kBBytes, &tmap_b, &full[stage], kb * (kBK / 2), g * p.N + nt * kBN);
           bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa + kb * 4 * 512, kSfaBytes, &full[stage]);
-          bulk_load(smem + kOffSfb + stage * kSfbBytes, sfb0 + kb * 4 * 512, kSfbBytes / 2, &full[stage]);
-          bulk_load(smem + kOffSfb + stage * kSfbBytes + kSfbBytes / 2, sfb1 + kb * 4 * 512, kSfbBytes / 2,
-                    &full[stage]);
+#pragma unroll
+          for (int b = 0; b < kBands; ++b)     // one 2 KiB run of 4 atoms per 128-row band of B
+            bulk_load(smem + kOffSfb + stage * kSfbBytes + b * 2048, sfb + (b * k4 + kb * 4) * 512, 2048,
+                      &full[stage]);
         }
         __syncwarp();
         filled |= 1u << stage;
@@ -243,12 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_nvf4(kBM, kBN);
-    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; tile < tiles_u && ok; tile += gridDim.x) {
-      ok = mbar_wait_warp(tempty, acc_phase ^ 1u, abort_flag, p.err);
+      ok = mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err);
       if (!ok) break;
       tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_u + acc * kBN;
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&full[stage], phase, abort_flag, p.err);
         if (!ok) break;
@@ -263,13 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             tc_copy_sf(sfa_t + 4 * j, sdesc_sf(sfa_s + 512 * j));
-            tc_copy_sf(sfb_t + 8 * j, sdesc_sf(sfb_s + 512 * j));                      // B rows 0..127
-            tc_copy_sf(sfb_t + 8 * j + 4, sdesc_sf(sfb_s + kSfbBytes / 2 + 512 * j));  // B rows 128..255
+#pragma unroll
+            for (int b = 0; b < kBands; ++b)   // B rows 128b .. 128b+127
+              tc_copy_sf(sfb_t + 4 * kBands * j + 4 * b, sdesc_sf(sfb_s + 2048 * b + 512 * j));
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // K advance of 64 E2M1 = 32 bytes inside the 128-byte swizzle row
-            tc_mma_nvf4(tmem_u, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
+            tc_mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 4 * kBands * j,
                         (kb | j) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
@@ -278,9 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      if (elect_one()) tc_commit(tfull);
+      if (elect_one()) tc_commit(&tfull[acc]);
       __syncwarp();
-      acc_phase ^= 1u;
+      if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
     }
     // every MMA issued by the elected lane has completed before the CTA moves on
     if (elect_one()) tc_commit(drain);
@@ -291,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t quad = warp & 3;                // TMEM lanes 32*quad .. +31
-    const uint32_t half = (warp - 2) >> 2;         // accumulator columns 128*half .. +127
+    const uint32_t half = (warp - 2) >> 2;         // accumulator columns (kBN/2)*half .. +kBN/2-1
     const uint32_t row_in_tile = quad * 32 + lane;
-    uint32_t acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int64_t mt = tile / p.n_tiles;
       const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
@@ -301,22 +322,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = find_group(s_off, p.G, mt * kBM);
       bool valid = true;
       if (p.counts != nullptr) valid = (grow - s_off[g]) < __ldg(p.counts + g);
-      if (!mbar_wait(tfull, acc_phase, abort_flag, p.err)) break;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after_sync();
-      float v[4][32];
-      const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + half * 128u;
+      float v[C::kChunks][32];
+      const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + acc * kBN + half * (kBN / 2);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_load32(t_row + 32 * c, v[c]);
+      for (int c = 0; c < C::kChunks; ++c) tmem_load32(t_row + 32 * c, v[c]);
       // the accumulator is in registers: hand it back to the MMA warp
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-      acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
       if constexpr (kEpi == NVFP4_EPI_SWIGLU_NVFP4) {
         epilogue_swiglu(v, p.alpha, valid, grow, static_cast<int64_t>(nt) * (kBN / 2) + half * 64, p.N / 2,
                         2 * nt + half, static_cast<uint32_t>(p.N / 128), p.out_q, p.out_sf, p.h_debug);
       } else {
-        if (valid) epilogue_bf16(v, p.alpha, p.out_bf16 + grow * p.N + static_cast<int64_t>(nt) * kBN + half * 128);
+        if (valid)
+          epilogue_bf16<C::kChunks>(v, p.alpha,
+                                    p.out_bf16 + grow * p.N + static_cast<int64_t>(nt) * kBN + half * (kBN / 2));
       }
     }
   }
@@ -362,7 +385,7 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_by
 
 struct DeviceInfo {
   int sms = 0;
-  bool attr_set[2] = {false, false};
+  bool attr_set[3] = {false, false, false};
 };
 
 DeviceInfo& device_info(int dev) {
@@ -374,16 +397,17 @@ DeviceInfo& device_info(int dev) {
   return d;
 }
 
-template <int kEpi>
+template <int kEpi, int BN>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t stream,
                    DeviceInfo& info) {
-  if (!info.attr_set[kEpi]) {
-    cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_kernel<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : (BN == 256 ? 1 : 2);
+  if (!info.attr_set[slot]) {
+    cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_kernel<kEpi, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg<BN>::kSmemBytes));
     if (e != cudaSuccess) return e;
-    info.attr_set[kEpi] = true;
+    info.attr_set[slot] = true;
   }
-  nvf4_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+  nvf4_gemm_kernel<kEpi, BN><<<grid, kThreads, Cfg<BN>::kSmemBytes, stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
@@ -397,9 +421,15 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   DeviceInfo& info = device_info(dev);
   if (info.sms <= 0) return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: no SM count for device %d", dev);
 
+  // 128x256 tiles whenever N allows (an N=256 MMA does twice an N=128 MMA's work
+  // for about 1.4x its issue cost, which outweighs the single-buffered
+  // accumulator's hand-off); BF16 outputs with N an odd multiple of 128 use
+  // 128x128 tiles with a double-buffered accumulator.
+  const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
+  const int bn = (swiglu || a.N % 256 == 0) ? 256 : 128;
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.a_q, static_cast<uint64_t>(a.rows_max), static_cast<uint64_t>(a.K) / 2, kBM) ||
-      !make_map(&mb, a.b_q, static_cast<uint64_t>(a.G) * a.N, static_cast<uint64_t>(a.K) / 2, kBN))
+      !make_map(&mb, a.b_q, static_cast<uint64_t>(a.G) * a.N, static_cast<uint64_t>(a.K) / 2, bn))
     return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: cuTensorMapEncodeTiled failed");
 
   Params p;
@@ -410,7 +440,7 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   p.G = a.offsets != nullptr ? a.G : 1;
   p.N = a.N;
   p.K = a.K;
-  p.n_tiles = a.N / kBN;
+  p.n_tiles = a.N / bn;
   p.k_blocks = a.K / kBK;
   p.rows_max = a.rows_max;
   p.sfb_group_bytes = static_cast<int64_t>(a.N / 128) * (a.K / 64) * 512;
@@ -424,8 +454,9 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   const int64_t max_tiles = (a.rows_max / kBM) * p.n_tiles;
   const int grid = static_cast<int>(max_tiles < info.sms ? max_tiles : info.sms);
   if (grid <= 0) return NVFP4_OK;
-  e = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? launch<NVFP4_EPI_SWIGLU_NVFP4>(ma, mb, p, grid, stream, info)
-                                           : launch<NVFP4_EPI_BF16>(ma, mb, p, grid, stream, info);
+  e = swiglu      ? launch<NVFP4_EPI_SWIGLU_NVFP4, 256>(ma, mb, p, grid, stream, info)
+      : bn == 256 ? launch<NVFP4_EPI_BF16, 256>(ma, mb, p, grid, stream, info)
+                  : launch<NVFP4_EPI_BF16, 128>(ma, mb, p, grid, stream, info);
   if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm launch");
   return NVFP4_OK;
 }

@@ -73,9 +73,10 @@ def test_host_validation_without_gpu(lib):
     # SwiGLU mode needs BF16
     assert lib.nvfp4_quantize(p, 1, 1, 4, 16, 32, p, p, None, None) == 2
     assert lib.nvfp4_sf_swizzle(p, 4, 4, 0, 1, p, 0, None) == 1
-    # K not a multiple of 256, N not a multiple of 128, G without offsets
+    # K not a multiple of 256; N not a multiple of 128 (BF16) / 256 (SwiGLU); G without offsets
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 200, p, p, 1.0, 1, None, None, p, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, 1, None, None, p, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 192, 256, p, p, 1.0, 1, None, None, p, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, 0, p, p, None, None, None) == 2
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 256, 256, p, p, 1.0, 1, None, None, p, None, None) == 2
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, 7, None, None, p, None, None) == 1
     # routing limits

@@ -56,8 +56,9 @@ def _valid_rows(offs, counts):
 
 CASES_BF16 = [
     # (group padded sizes, counts or None, N, K, alpha)
-    ([128], None, 256, 256, 1.0),                     # one tile, one K stage
+    ([128], None, 128, 256, 1.0),                     # one tile, one K stage
     ([256], None, 512, 512, 1.0),
+    ([384], None, 384, 1024, 1.0),                    # odd number of 128-column tiles
     ([128, 0, 384, 128], [100, 0, 300, 128], 768, 768, 0.75),
     ([128] * 40, [128 - (i % 7) for i in range(40)], 1024, 1280, 1.0),   # > one wave of tiles
 ]
