@@ -115,9 +115,13 @@ __device__ __forceinline__ uint32_t quantize8(const float (&h)[8], const BlockSc
   return e2m1x8_from_halfsteps(v);
 }
 
-// silu(g) * u with the fast exponential (the SwiGLU of the L1 epilogue).
+// silu(g) * u = g * u / (1 + 2^(-g * log2(e))), with the SFU's ex2.approx and
+// rcp.approx (a few ulp; g -> -inf gives a signed zero, g -> +inf gives g * u).
 __device__ __forceinline__ float swiglu(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return g * r * u;
 }
 
 // Byte offset of the SF word holding scales (row, 4*k4 .. 4*k4+3) in the

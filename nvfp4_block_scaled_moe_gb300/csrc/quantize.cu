@@ -7,87 +7,107 @@
 // each gate/up pair in the same pass.  "NVFP4 MegaMoE Debug Log": the SF remap
 // (forward mapping with explicit source strides) for the swizzle kernel.
 //
-// Layout of the quantiser's work: one thread owns 8 consecutive output values
-// (16-byte loads of BF16, 32-byte of fp32 or gate+up), a lane pair owns one
-// 16-block (amax by one warp shuffle), a lane octet owns one 64-column group,
-// whose four scale bytes form one 32-bit word of the swizzled layout.
+// Layout of the quantiser's work: one thread owns one 16-block (32 bytes of BF16,
+// 64 of fp32 or gate+up), a lane quad owns one 64-column group, whose four scale
+// bytes form one 32-bit word of the swizzled layout.
 #include "common.cuh"
 #include "internal.h"
 
 namespace nvfp4 {
 
+// Load the 16 values of output block c0 .. c0+15 (c0 % 16 == 0) of a row.
 template <int kMode, int kDtype>
-__device__ __forceinline__ void load_values(const void* in, int64_t row, int64_t ld, int64_t c0,
-                                            float (&h)[8]) {
+__device__ __forceinline__ void load_block(const void* in, int64_t row, int64_t ld, int64_t c0, float (&h)[16]) {
   if (kMode == NVFP4_MODE_SWIGLU_GU8) {
-    // output columns c0..c0+7 (c0 % 8 == 0): gate at 2*c0 .. +7, up at 2*c0+8 .. +15
+    // interleaved columns 2*c0 .. 2*c0+31: g0(8) u0(8) g1(8) u1(8)
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + 2 * c0);
-    const uint4 gw = __ldg(p), uw = __ldg(p + 1);
+    const uint4 g0 = __ldg(p), u0 = __ldg(p + 1), g1 = __ldg(p + 2), u1 = __ldg(p + 3);
     float g[8], u[8];
-    bf16x8_to_f32(gw, g);
-    bf16x8_to_f32(uw, u);
+    bf16x8_to_f32(g0, g);
+    bf16x8_to_f32(u0, u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) h[i] = swiglu(g[i], u[i]);
+    bf16x8_to_f32(g1, g);
+    bf16x8_to_f32(u1, u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[8 + i] = swiglu(g[i], u[i]);
   } else if (kDtype == NVFP4_IN_BF16) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + c0));
-    bf16x8_to_f32(w, h);
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + c0);
+    float lo[8], hi[8];
+    bf16x8_to_f32(__ldg(p), lo);
+    bf16x8_to_f32(__ldg(p + 1), hi);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h[i] = lo[i];
+      h[8 + i] = hi[i];
+    }
   } else {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(in) + row * ld + c0);
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    h[0] = a.x; h[1] = a.y; h[2] = a.z; h[3] = a.w;
-    h[4] = b.x; h[5] = b.y; h[6] = b.z; h[7] = b.w;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = __ldg(p + q);
+      h[4 * q] = v.x;
+      h[4 * q + 1] = v.y;
+      h[4 * q + 2] = v.z;
+      h[4 * q + 3] = v.w;
+    }
   }
 }
 
-// One warp per (row, 256-column segment): blockIdx.x is the row (rows_pad >=
-// rows covers the zero padding rows of the swizzled SF), blockIdx.y * 8 + warp the
-// segment.  sf_linear selects a plain row-major SF output ([rows, cols/16], used
-// for staging x in moe_route_permute; requires cols % 64 == 0).
+// One thread per 16-block (no shuffle for the amax; one block scale per thread),
+// one warp per 512-column segment: blockIdx.x is the row (rows_pad >= rows
+// covers the zero padding rows of the swizzled SF), blockIdx.y * (warps per
+// block) + warp the segment.  Lanes 4w .. 4w+3 own one 64-column group, whose four scale bytes form
+// one 32-bit word of the swizzled layout.  sf_linear selects a plain row-major
+// SF output ([rows, cols/16]; requires cols % 64 == 0).
 template <int kMode, int kDtype>
 __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ in, int64_t rows,
                                                        int64_t cols, int64_t ld, int64_t rows_pad,
                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                        int sf_linear, float* __restrict__ h_dbg) {
   const int lane = threadIdx.x & 31;
-  const int64_t seg = static_cast<int64_t>(blockIdx.y) * 8 + (threadIdx.x >> 5);
-  if (seg * 256 >= cols) return;
+  const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (seg * 512 >= cols) return;
   const int64_t row = blockIdx.x;
-  const int64_t c0 = seg * 256 + lane * 8;
+  const int64_t c0 = seg * 512 + lane * 16;
   const bool in_row = row < rows;
   const bool active = in_row && c0 < cols;
 
-  float h[8];
+  float h[16];
+  if (active) {
+    load_block<kMode, kDtype>(in, row, ld, c0, h);
+  } else {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) h[i] = 0.0f;
-  if (active) load_values<kMode, kDtype>(in, row, ld, c0, h);
-
+    for (int i = 0; i < 16; ++i) h[i] = 0.0f;
+  }
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(h[i]));
   const BlockScale s = block_scale(amax);
 
   if (active) {
-    const uint32_t nib = quantize8(h, s);
-    *reinterpret_cast<uint32_t*>(q + row * (cols / 2) + c0 / 2) = nib;
+    float lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lo[i] = h[i];
+      hi[i] = h[8 + i];
+    }
+    *reinterpret_cast<uint2*>(q + row * (cols / 2) + c0 / 2) = make_uint2(quantize8(lo, s), quantize8(hi, s));
     if (h_dbg != nullptr) {
       float4* hp = reinterpret_cast<float4*>(h_dbg + row * cols + c0);
-      hp[0] = make_float4(h[0], h[1], h[2], h[3]);
-      hp[1] = make_float4(h[4], h[5], h[6], h[7]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hp[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     }
   }
 
-  // gather the octet's four scale bytes (lanes 8w, 8w+2, 8w+4, 8w+6) into one word
+  // gather the quad's four scale bytes (lanes 4w .. 4w+3) into one word at lane 4w
   const uint32_t code = active ? s.code : 0u;
-  const int base = lane & ~7;
-  const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, code, base);
-  const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, code, base + 2);
-  const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
-  const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, code, base + 6);
-  const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-  const int64_t k4 = seg * 4 + (lane >> 3);        // 64-column group of this octet
+  const uint32_t word = code | (__shfl_down_sync(0xFFFFFFFFu, code, 1) << 8) |
+                        (__shfl_down_sync(0xFFFFFFFFu, code, 2) << 16) |
+                        (__shfl_down_sync(0xFFFFFFFFu, code, 3) << 24);
+  const int64_t k4 = seg * 8 + (lane >> 2);          // 64-column group of this quad
   const int64_t k4_total = (cols + 63) / 64;
-  if ((lane & 7) == 0 && k4 < k4_total) {
+  if ((lane & 3) == 0 && k4 < k4_total) {
     if (sf_linear) {
       if (in_row) *reinterpret_cast<uint32_t*>(sf + row * (cols / 16) + k4 * 4) = word;
     } else {
@@ -100,10 +120,12 @@ template <int kMode, int kDtype>
 static cudaError_t launch_quantize(const void* in, int64_t rows, int64_t cols, int64_t ld,
                                    int64_t rows_pad, uint8_t* q, uint8_t* sf, int sf_linear,
                                    float* h_dbg, cudaStream_t stream) {
-  const int64_t segs = (cols + 255) / 256;
+  const int64_t segs = (cols + 511) / 512;
   if (rows_pad == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(rows_pad), static_cast<unsigned>((segs + 7) / 8));
-  quantize_kernel<kMode, kDtype><<<grid, 256, 0, stream>>>(in, rows, cols, ld, rows_pad, q, sf, sf_linear, h_dbg);
+  const int warps = static_cast<int>(segs < 8 ? segs : 8);      // no idle warps on short rows
+  const dim3 grid(static_cast<unsigned>(rows_pad), static_cast<unsigned>((segs + warps - 1) / warps));
+  quantize_kernel<kMode, kDtype><<<grid, 32 * warps, 0, stream>>>(in, rows, cols, ld, rows_pad, q, sf, sf_linear,
+                                                                  h_dbg);
   return cudaGetLastError();
 }
 
