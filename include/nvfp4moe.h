@@ -72,6 +72,13 @@ typedef enum {
   NVFP4_EPI_BF16 = 1           /* alpha * acc rounded to BF16 */
 } nvfp4_epilogue;
 
+/* Output-tile kernels of nvfp4_grouped_gemm (see nvfp4_set_gemm_tiles). */
+typedef enum {
+  NVFP4_GEMM_TILES_AUTO = 0,   /* by shape: CTA pairs when groups average >= 256 rows */
+  NVFP4_GEMM_TILES_SINGLE = 1, /* one CTA per 128-row tile */
+  NVFP4_GEMM_TILES_PAIR = 2    /* two CTAs (a cluster) per 256-row tile, where N % 256 == 0 */
+} nvfp4_gemm_tiles;
+
 /* Bytes of a swizzled SF buffer for a rows x cols matrix (cols in elements):
  * ceil(rows/128) * ceil(cols/64) * 512.  Returns 0 for non-positive sizes. */
 size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
@@ -194,6 +201,10 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
  *               swizzled; h_debug NULL or fp32 [rows_max, N/2].
  *               NVFP4_EPI_BF16: out_bf16 BF16 [rows_max, N].
+ * Two kernels compute this (nvfp4_set_gemm_tiles): 128-row tiles on single CTAs,
+ * or, when N % 256 == 0, 256-row tiles on CTA pairs (a 2-CTA cluster sharing one
+ * cta_group::2 MMA, each CTA loading half of B), which pairs consecutive 128-row
+ * blocks of a group.  Both give the same results bit for bit.
  * Limits: K a positive multiple of 256, N a positive multiple of 256 (SWIGLU) or
  * 128 (BF16), rows_max a
  * positive multiple of 128, all pointers 16-byte aligned.
@@ -204,6 +215,16 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 const uint8_t* b_sf, float alpha, nvfp4_epilogue epilogue,
                                 uint8_t* out_q, uint8_t* out_sf, void* out_bf16,
                                 float* h_debug, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_set_gemm_tiles -- process-wide choice of nvfp4_grouped_gemm's tile kernel
+ * (also used by nvfp4_moe_ffn_forward): NVFP4_GEMM_TILES_AUTO (the default),
+ * _SINGLE or _PAIR (_PAIR falls back to single CTAs where N % 256 != 0).  A
+ * tuning and testing control with no counterpart in the source pages; results
+ * do not depend on it.  Takes effect for calls made after it returns;
+ * NVFP4_ERR_INVALID_ARG for another value.
+ * -------------------------------------------------------------------------- */
+nvfp4_status nvfp4_set_gemm_tiles(int32_t mode);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_moe_ffn_forward -- L1 GEMM with the fused SwiGLU + NVFP4 epilogue, then

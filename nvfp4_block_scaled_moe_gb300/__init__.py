@@ -19,7 +19,7 @@ __all__ = [
     "Nvfp4Error", "lib_path", "load", "sf_bytes", "moe_padded_rows_max",
     "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
     "moe_route_permute", "moe_route_permute_static", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
-    "moe_combine", "nvfp4_device_status", "nvfp4_selftest_bounded_wait",
+    "moe_combine", "nvfp4_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_set_gemm_tiles",
     "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
 ]
 
@@ -62,6 +62,7 @@ _SIGS = {
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
+    "nvfp4_set_gemm_tiles": (ctypes.c_int, [ctypes.c_int32]),
 }
 
 
@@ -165,6 +166,13 @@ def moe_combine(rows, inv_perm, topk_w, y, stream=None):
 
 def nvfp4_device_status(stream=None):
     _check(load().nvfp4_device_status(_stream(stream)))
+
+
+GEMM_TILES_AUTO, GEMM_TILES_SINGLE, GEMM_TILES_PAIR = 0, 1, 2
+
+
+def nvfp4_set_gemm_tiles(mode):
+    _check(load().nvfp4_set_gemm_tiles(mode))
 
 
 def nvfp4_selftest_bounded_wait(flag, limit_ns, stream=None):

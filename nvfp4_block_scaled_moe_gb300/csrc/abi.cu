@@ -252,6 +252,8 @@ nvfp4_status nvfp4_device_status(nvfp4_stream_t stream) {
   return fail(NVFP4_ERR_DEVICE, "device: an index check failed (word 0x%x)", word);
 }
 
+nvfp4_status nvfp4_set_gemm_tiles(int32_t mode) { return set_gemm_tiles(mode); }
+
 nvfp4_status nvfp4_selftest_bounded_wait(const int32_t* flag, int64_t limit_ns, nvfp4_stream_t stream) {
   CHECK_ARG(flag != nullptr, "nvfp4_selftest_bounded_wait: null flag");
   CHECK_ARG(limit_ns > 0 && limit_ns <= 10000000000ll, "nvfp4_selftest_bounded_wait: limit_ns outside (0, 10 s]");

@@ -30,6 +30,7 @@
 // first MMA of a tile does not accumulate; barrier arrival counts are in the
 // units that actually arrive.  Every wait is bounded (a timeout sets the error
 // word and lets the CTA exit).
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -370,18 +371,26 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// rows x row_bytes uint8 matrix, box of 128 bytes x box_rows rows, 128-byte swizzle
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows) {
+}  // namespace
+
+// rows x cols matrix of elem_bytes-sized elements (row-major, rows contiguous),
+// box of box_cols x box_rows, optionally with 128-byte swizzle.
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t elem_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {row_bytes, rows};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * elem_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
+
+std::atomic<int> g_gemm_tiles{NVFP4_GEMM_TILES_AUTO};
 
 struct DeviceInfo {
   int sms = 0;
@@ -424,12 +433,21 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   // 128x256 tiles whenever N allows (an N=256 MMA does twice an N=128 MMA's work
   // for about 1.4x its issue cost, which outweighs the single-buffered
   // accumulator's hand-off); BF16 outputs with N an odd multiple of 128 use
-  // 128x128 tiles with a double-buffered accumulator.
+  // 128x128 tiles with a double-buffered accumulator.  Groups averaging two or
+  // more 128-row blocks go to the CTA-pair kernel (256x256 tiles, gemm_pair.cu);
+  // thinner groups (decode-sized batches) would leave half of many pair tiles empty.
   const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
   const int bn = (swiglu || a.N % 256 == 0) ? 256 : 128;
+  const int mode = g_gemm_tiles.load(std::memory_order_relaxed);
+  const int64_t groups = a.offsets != nullptr ? a.G : 1;
+  const bool pair = bn == 256 && (mode == NVFP4_GEMM_TILES_PAIR ||
+                                  (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
+  if (pair) return gemm_pair_launch(a, info.sms, dev, stream);
   CUtensorMap ma, mb;
-  if (!make_map(&ma, a.a_q, static_cast<uint64_t>(a.rows_max), static_cast<uint64_t>(a.K) / 2, kBM) ||
-      !make_map(&mb, a.b_q, static_cast<uint64_t>(a.G) * a.N, static_cast<uint64_t>(a.K) / 2, bn))
+  if (!make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q, static_cast<uint64_t>(a.rows_max),
+                    static_cast<uint64_t>(a.K) / 2, 1, 128, kBM, true) ||
+      !make_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_q, static_cast<uint64_t>(a.G) * a.N,
+                    static_cast<uint64_t>(a.K) / 2, 1, 128, bn, true))
     return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: cuTensorMapEncodeTiled failed");
 
   Params p;
@@ -458,6 +476,13 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
       : bn == 256 ? launch<NVFP4_EPI_BF16, 256>(ma, mb, p, grid, stream, info)
                   : launch<NVFP4_EPI_BF16, 128>(ma, mb, p, grid, stream, info);
   if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status set_gemm_tiles(int mode) {
+  if (mode != NVFP4_GEMM_TILES_AUTO && mode != NVFP4_GEMM_TILES_SINGLE && mode != NVFP4_GEMM_TILES_PAIR)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_set_gemm_tiles: unknown mode %d", mode);
+  g_gemm_tiles.store(mode, std::memory_order_relaxed);
   return NVFP4_OK;
 }
 

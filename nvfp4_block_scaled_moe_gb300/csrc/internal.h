@@ -1,6 +1,7 @@
 // Host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,6 +64,13 @@ struct GemmArgs {
 
 // Returns a status; writes a message with set_error_message on failure.
 nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
+// The CTA-pair kernel (N % 256 == 0); sms and dev of the current device.
+nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t stream);
+nvfp4_status set_gemm_tiles(int mode);
+
+// 2-D tensor map of a row-major rows x cols matrix (gemm.cu).
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t elem_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 cudaError_t selftest_wait_launch(const int32_t* flag, int64_t limit_ns, cudaStream_t stream);
 

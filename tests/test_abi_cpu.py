@@ -88,6 +88,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.moe_combine(p, p, p, 4, 12, 2, p, None) == 2
     assert lib.nvfp4_selftest_bounded_wait(None, 10, None) == 1
     assert b"selftest" in lib.nvfp4_last_error()
+    # tile-kernel choice: three modes, anything else refused; the default restored
+    assert lib.nvfp4_set_gemm_tiles(3) == 1 and lib.nvfp4_set_gemm_tiles(-1) == 1
+    for mode in (2, 1, 0):
+        assert lib.nvfp4_set_gemm_tiles(mode) == 0
     with pytest.raises(nv.Nvfp4Error) as ei:
         nv._check(2)
     assert ei.value.status == 2

@@ -6,7 +6,12 @@ straight from the seeded generator; the device swizzles its own copy of the
 scales with nvfp4_sf_swizzle, so nothing the oracle computes reaches the GPU.
 Bounds: BF16 rows and SwiGLU h within relative Frobenius 2e-3 (and nearly all
 BF16 values identical); re-quantised nibbles within the 0.1% / one-step bound.
+Every case runs on both tile kernels (single CTAs with 128-row tiles, CTA pairs
+with 256-row tiles where N % 256 == 0); each must meet the bounds, and the two
+must agree bit for bit (same per-element K order of the same MMAs).
 """
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -47,6 +52,26 @@ def _operands(nv, seed, rows_max, group_sizes, N, K, sf_range=(0x30, 0x44)):
     return d, offs, a_deq, b_deq
 
 
+@contextlib.contextmanager
+def _tiles(nv, mode):
+    nv.nvfp4_set_gemm_tiles(mode)
+    try:
+        yield
+    finally:
+        nv.nvfp4_set_gemm_tiles(nv.GEMM_TILES_AUTO)
+
+
+def _both_kernels(nv, run):
+    """run() -> tuple of host arrays, on each tile kernel; asserts they are identical."""
+    outs = []
+    for mode in (nv.GEMM_TILES_SINGLE, nv.GEMM_TILES_PAIR):
+        with _tiles(nv, mode):
+            outs.append(run())
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b), "single-CTA and CTA-pair kernels differ"
+    return outs[0]
+
+
 def _valid_rows(offs, counts):
     rows = []
     for g in range(len(offs) - 1):
@@ -61,6 +86,7 @@ CASES_BF16 = [
     ([384], None, 384, 1024, 1.0),                    # odd number of 128-column tiles
     ([128, 0, 384, 128], [100, 0, 300, 128], 768, 768, 0.75),
     ([128] * 40, [128 - (i % 7) for i in range(40)], 1024, 1280, 1.0),   # > one wave of tiles
+    ([1024, 384, 640], [1024, 383, 600], 1792, 768, 1.0),                 # pairs, odd tails, > one wave
 ]
 
 
@@ -68,19 +94,22 @@ CASES_BF16 = [
 def test_gemm_bf16_epilogue(nv, sizes, counts, N, K, alpha):
     rows_max = sum(sizes) + 128
     d, offs, a_deq, b_deq = _operands(nv, 11 + N + K, rows_max, sizes, N, K)
-    out = torch.full((rows_max, N), 12288.0, dtype=torch.bfloat16, device="cuda")
-    if counts is None:
-        assert len(sizes) == 1
-        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], sizes[0], None, None, 1, N, K, d["b_q"], d["b_sf"], alpha,
-                              nv.EPI_BF16, out_bf16=out)
-        valid = np.arange(sizes[0])
-    else:
-        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), dev(np.array(counts, np.int32)),
-                              len(sizes), N, K, d["b_q"], d["b_sf"], alpha, nv.EPI_BF16, out_bf16=out)
-        valid = _valid_rows(offs, counts)
-    nv.nvfp4_device_status()
+
+    def run():
+        out = torch.full((rows_max, N), 12288.0, dtype=torch.bfloat16, device="cuda")
+        if counts is None:
+            nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], sizes[0], None, None, 1, N, K, d["b_q"], d["b_sf"], alpha,
+                                  nv.EPI_BF16, out_bf16=out)
+        else:
+            nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), dev(np.array(counts, np.int32)),
+                                  len(sizes), N, K, d["b_q"], d["b_sf"], alpha, nv.EPI_BF16, out_bf16=out)
+        nv.nvfp4_device_status()
+        return (out.float().cpu().numpy(),)
+
+    assert counts is not None or len(sizes) == 1
+    valid = np.arange(sizes[0]) if counts is None else _valid_rows(offs, counts)
+    (got,) = _both_kernels(nv, run)
     ref = omoe.round_to_bf16(omoe.grouped_gemm(a_deq[:offs[-1]], offs, b_deq, alpha))
-    got = out.float().cpu().numpy()
     assert rel_frobenius(got[valid], ref[valid]) <= 2e-3
     assert np.mean(got[valid] == ref[valid]) > 0.97
     mask = np.ones(rows_max, bool)
@@ -92,6 +121,7 @@ CASES_SWIGLU = [
     ([128], None, 256, 256, 1.0),
     ([256, 128], [200, 128], 512, 1024, 1.25),
     ([128, 128, 0, 256], [1, 128, 0, 129], 256, 512, 0.5),
+    ([768, 384, 128], [768, 300, 127], 1024, 512, 1.0),
 ]
 
 
@@ -100,58 +130,73 @@ def test_gemm_swiglu_nvfp4_epilogue(nv, sizes, counts, N, K, alpha):
     rows_max = sum(sizes)
     d, offs, a_deq, b_deq = _operands(nv, 7 + N + K, rows_max, sizes, N, K)
     I = N // 2
-    q = torch.full((rows_max, I // 2), 0x77, dtype=torch.uint8, device="cuda")
-    sf = torch.zeros(nv.sf_bytes(rows_max, I), dtype=torch.uint8, device="cuda")
-    h = torch.zeros((rows_max, I), dtype=torch.float32, device="cuda")
-    if counts is None:
-        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, None, None, 1, N, K, d["b_q"], d["b_sf"], alpha,
-                              nv.EPI_SWIGLU_NVFP4, out_q=q, out_sf=sf, h_debug=h)
-        valid = np.arange(rows_max)
-    else:
-        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), dev(np.array(counts, np.int32)),
-                              len(sizes), N, K, d["b_q"], d["b_sf"], alpha, nv.EPI_SWIGLU_NVFP4, out_q=q,
-                              out_sf=sf, h_debug=h)
-        valid = _valid_rows(offs, counts)
-    nv.nvfp4_device_status()
+
+    def run(with_h):
+        q = torch.full((rows_max, I // 2), 0x77, dtype=torch.uint8, device="cuda")
+        sf = torch.zeros(nv.sf_bytes(rows_max, I), dtype=torch.uint8, device="cuda")
+        h = torch.zeros((rows_max, I), dtype=torch.float32, device="cuda") if with_h else None
+        if counts is None:
+            nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, None, None, 1, N, K, d["b_q"], d["b_sf"], alpha,
+                                  nv.EPI_SWIGLU_NVFP4, out_q=q, out_sf=sf, h_debug=h)
+        else:
+            nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), dev(np.array(counts, np.int32)),
+                                  len(sizes), N, K, d["b_q"], d["b_sf"], alpha, nv.EPI_SWIGLU_NVFP4, out_q=q,
+                                  out_sf=sf, h_debug=h)
+        nv.nvfp4_device_status()
+        return (host(q), host(sf)) + ((host(h),) if with_h else ())
+
+    valid = np.arange(rows_max) if counts is None else _valid_rows(offs, counts)
+    gq, gsf_sw, gh = _both_kernels(nv, lambda: run(True))
+    nq, nsf, = _both_kernels(nv, lambda: run(False))          # the h_debug stores change nothing else
+    assert np.array_equal(nq, gq) and np.array_equal(nsf, gsf_sw)
     g_full = omoe.grouped_gemm(a_deq, offs, b_deq, alpha)
     oq, osf, oh = omoe.l1_swiglu_requant(g_full)
-    gh = host(h)
     assert rel_frobenius(gh[valid], oh[valid]) <= 2e-3
-    gsf = onv.unswizzle_sf(host(sf), rows_max, I // 16)
-    res = compare_requantised(host(q)[valid], gsf[valid], oq[valid], osf[valid])
+    gsf = onv.unswizzle_sf(gsf_sw, rows_max, I // 16)
+    res = compare_requantised(gq[valid], gsf[valid], oq[valid], osf[valid])
     assert res["ok"], res
     untouched = np.ones(rows_max, bool)
     untouched[valid] = False
-    assert np.all(host(q)[untouched] == 0x77)
+    assert np.all(gq[untouched] == 0x77)
 
 
 def test_gemm_uniform_vs_random_scales_both_match(nv):
     """All-equal scales hide a wrong scale layout; random ones expose it.  Both must match."""
     for sf_range in ((0x38, 0x38), (0x28, 0x50)):
         d, offs, a_deq, b_deq = _operands(nv, 3, 256, [256], 256, 512, sf_range)
-        out = torch.empty((256, 256), dtype=torch.bfloat16, device="cuda")
-        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], 256, None, None, 1, 256, 512, d["b_q"], d["b_sf"], 1.0,
-                              nv.EPI_BF16, out_bf16=out)
+
+        def run():
+            out = torch.empty((256, 256), dtype=torch.bfloat16, device="cuda")
+            nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], 256, None, None, 1, 256, 512, d["b_q"], d["b_sf"], 1.0,
+                                  nv.EPI_BF16, out_bf16=out)
+            return (out.float().cpu().numpy(),)
+
+        (got,) = _both_kernels(nv, run)
         ref = omoe.round_to_bf16(omoe.grouped_gemm(a_deq, offs, b_deq))
-        assert rel_frobenius(out.float().cpu().numpy(), ref) <= 2e-3, sf_range
+        assert rel_frobenius(got, ref) <= 2e-3, sf_range
 
 
 def test_gemm_one_hot_locates_nibbles_and_scales(nv):
     """A single nonzero A element at (r, k) and a single nonzero B element at (n, k):
     the product appears only at (r, n), scaled by both blocks' scales."""
-    K, N, M = 512, 256, 128
+    K, N, M = 512, 256, 256
     rng = np.random.default_rng(9)
-    for r, n, k in ((0, 0, 0), (5, 77, 37), (127, 255, 511), (64, 3, 300), (33, 200, 64), (100, 128, 130)):
+    for r, n, k in ((0, 0, 0), (5, 77, 37), (127, 255, 511), (64, 3, 300), (33, 200, 64), (100, 128, 130),
+                    (128, 0, 0), (200, 255, 17), (255, 129, 480)):                 # rows of the odd CTA
         a_q = np.zeros((M, K // 2), np.uint8)
         b_q = np.zeros((1, N, K // 2), np.uint8)
         a_q[r, k // 2] = (0x3 << 4) if k % 2 else 0x3          # 1.5
         b_q[0, n, k // 2] = (0x6 << 4) if k % 2 else 0x6       # 4.0
         a_sf = rng.integers(0x30, 0x40, (M, K // 16), dtype=np.uint8)
         b_sf = rng.integers(0x30, 0x40, (N, K // 16), dtype=np.uint8)
-        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        nv.nvfp4_grouped_gemm(dev(a_q), _swizzled(nv, a_sf), M, None, None, 1, N, K, dev(b_q),
-                              _swizzled(nv, b_sf)[None], 1.0, nv.EPI_BF16, out_bf16=out)
-        got = out.float().cpu().numpy()
+
+        def run():
+            out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            nv.nvfp4_grouped_gemm(dev(a_q), _swizzled(nv, a_sf), M, None, None, 1, N, K, dev(b_q),
+                                  _swizzled(nv, b_sf)[None], 1.0, nv.EPI_BF16, out_bf16=out)
+            return (out.float().cpu().numpy(),)
+
+        (got,) = _both_kernels(nv, run)
         expect = np.zeros((M, N))
         expect[r, n] = 1.5 * 4.0 * onv.e4m3_decode(a_sf[r, k // 16]) * onv.e4m3_decode(b_sf[n, k // 16])
         assert np.array_equal(got, omoe.round_to_bf16(expect)), (r, n, k)
