@@ -205,43 +205,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// Bounded wait at cluster scope: pairs with arrivals released by the other CTA
-// of a cluster (mbarrier.arrive.release.cluster on this CTA's barrier).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                 unsigned* err, uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        raise_error(err, kErrTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                      unsigned* err) {
-  const bool ok = mbar_wait_cluster(bar, parity, abort, err);
-  return __all_sync(0xFFFFFFFFu, ok);
-}
-
 // ---------------------------------------------------------------- clusters --
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -263,9 +226,12 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
 }
 
 // One arrival on a barrier given by its shared::cluster address (possibly in the
-// other CTA of the cluster), releasing this thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// other CTA of the cluster).  Used to hand TMEM back after tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync, which order the TMEM reads; the default
+// (CTA-scope) release is enough for that and measurably cheaper than a
+// cluster-scope release.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // One lane of a converged warp (the lowest active one) is elected.
@@ -437,6 +403,33 @@ __device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
 }
+
+// Load 128 consecutive fp32 columns of this thread's TMEM lane (one instruction)
+// and wait for them.
+#define NVFP4_R32(o) "=r"(r[o + 0]), "=r"(r[o + 1]), "=r"(r[o + 2]), "=r"(r[o + 3]), "=r"(r[o + 4]), \
+    "=r"(r[o + 5]), "=r"(r[o + 6]), "=r"(r[o + 7]), "=r"(r[o + 8]), "=r"(r[o + 9]), "=r"(r[o + 10]),        \
+    "=r"(r[o + 11]), "=r"(r[o + 12]), "=r"(r[o + 13]), "=r"(r[o + 14]), "=r"(r[o + 15]), "=r"(r[o + 16]),   \
+    "=r"(r[o + 17]), "=r"(r[o + 18]), "=r"(r[o + 19]), "=r"(r[o + 20]), "=r"(r[o + 21]), "=r"(r[o + 22]),   \
+    "=r"(r[o + 23]), "=r"(r[o + 24]), "=r"(r[o + 25]), "=r"(r[o + 26]), "=r"(r[o + 27]), "=r"(r[o + 28]),   \
+    "=r"(r[o + 29]), "=r"(r[o + 30]), "=r"(r[o + 31])
+__device__ __forceinline__ void tmem_load128(uint32_t taddr, float (&v)[4][32]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+      "%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,"
+      "%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,"
+      "%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,"
+      "%126,%127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : NVFP4_R32(0), NVFP4_R32(32), NVFP4_R32(64), NVFP4_R32(96)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i >> 5][i & 31] = __uint_as_float(r[i]);
+}
+#undef NVFP4_R32
 
 // Load 32 consecutive fp32 columns of this thread's TMEM lane and wait for them.
 __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {

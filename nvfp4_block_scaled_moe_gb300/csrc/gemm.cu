@@ -440,8 +440,9 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   const int bn = (swiglu || a.N % 256 == 0) ? 256 : 128;
   const int mode = g_gemm_tiles.load(std::memory_order_relaxed);
   const int64_t groups = a.offsets != nullptr ? a.G : 1;
-  const bool pair = bn == 256 && (mode == NVFP4_GEMM_TILES_PAIR ||
-                                  (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
+  const bool pair = bn == 256 && groups <= kPairMaxGroups &&
+                    (mode == NVFP4_GEMM_TILES_PAIR ||
+                     (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
   if (pair) return gemm_pair_launch(a, info.sms, dev, stream);
   CUtensorMap ma, mb;
   if (!make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q, static_cast<uint64_t>(a.rows_max),

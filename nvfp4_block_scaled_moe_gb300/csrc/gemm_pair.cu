@@ -25,9 +25,10 @@
 //              the pair, commits multicast to both CTAs' barriers); idle on the
 //              odd CTA after the collective TMEM allocation;
 //   warps 2-9  epilogue on this CTA's 128 accumulator rows, as in gemm.cu,
-//              except that complete 32-row slices leave through shared memory
-//              and TMA stores (one write of whole lines instead of 32 partial
-//              lines per store instruction).
+//              except that complete 32-row slices leave through shared memory:
+//              BF16 rows are staged 64 columns at a time and written back with
+//              each store instruction covering four whole 128-byte lines (instead
+//              of 32 partial lines); SwiGLU nibble rows leave by TMA store.
 // Every wait is bounded; a timeout sets the error word and the pair drains
 // and exits together (the final cluster barrier keeps each CTA's shared
 // memory alive while the other may still address it).
@@ -42,7 +43,7 @@ namespace {
 constexpr int kBM = 128, kBN = 256, kBK = 256;        // rows per CTA, columns, K per stage
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kMaxGroups = 1024;
+constexpr int kMaxGroups = kPairMaxGroups;             // larger G uses the single-CTA kernel
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
 constexpr uint32_t kBBytes = 128 * kBK / 2;            // 16 KiB: this CTA's 128 B rows
 constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms
@@ -51,14 +52,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = kBN;                      // scale columns follow the accumulator
 constexpr uint32_t kTmemSfStage = 16 + 32;             // A: 4 atoms x 4 columns; B: 2 bands x 16
 
-// Per epilogue: stage count and the staging buffer of one warp's TMA stores.
-//   SwiGLU: 32 rows x 32 bytes of nibbles (one 1 KiB box per tile);
-//   BF16:   two 32-row x 64-column boxes (2 x 4 KiB, 128-byte swizzle).
+// Per epilogue: the staging buffer of one warp's output slice.
+//   SwiGLU: 32 rows x 32 bytes of nibbles (one 1 KiB TMA-store box per tile);
+//   BF16:   32 rows x 64 columns (4 KiB, 16-byte chunks XOR-swizzled by row).
 template <int kEpi>
 struct PairCfg {
   static constexpr bool kSwiglu = kEpi == NVFP4_EPI_SWIGLU_NVFP4;
-  static constexpr int kStages = kSwiglu ? 5 : 4;
-  static constexpr uint32_t kStageBufBytes = kSwiglu ? 1024 : 8192;
+  static constexpr int kStages = 5;
+  static constexpr uint32_t kStageBufBytes = kSwiglu ? 1024 : 4096;
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
   static constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
@@ -68,7 +69,7 @@ struct PairCfg {
   static constexpr uint32_t kNumBars = 2 * kStages + 3;                    // full, empty, tfull, tempty, drain
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;             // tmem slot, abort flag
   static constexpr uint32_t kOffGroups = kOffMisc + 16;                    // row offsets, then pair prefix
-  static constexpr uint32_t kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;
+  static constexpr uint32_t kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kOffB % 1024 == 0 && kOffSfa % 1024 == 0 && kOffOut % 1024 == 0, "1 KiB alignment");
   static_assert(kTmemSf + kStages * kTmemSfStage <= kTmemCols, "TMEM budget");
@@ -176,8 +177,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tmap_out, const PairParams p) {
   using C = PairCfg<kEpi>;
   constexpr int kStages = C::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // the swizzled tiles need a 1 KiB-aligned base; every CTA sees the same base,
+  // so a misaligned one stops all of them here, before any pair traffic
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t tile = cluster_id; tile < tiles_u && ok; tile += n_clusters) {
-      ok = mbar_wait_cluster_warp(tempty, acc_phase ^ 1u, abort_flag, p.err);
+      ok = mbar_wait_warp(tempty, acc_phase ^ 1u, abort_flag, p.err);
       if (!ok) break;
       tc_fence_after_sync();
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
@@ -375,16 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       float v[4][32];
       const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + half * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_load32(t_row + 32 * c, v[c]);
+      tmem_load128(t_row, v);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tempty);
+      if (lane == 0) mbar_arrive_remote(leader_tempty);
       acc_phase ^= 1u;
 
       // whole 32-row slices leave by TMA store; a slice with missing rows stores row by row
       const bool staged = __all_sync(0xFFFFFFFFu, valid);
-      if (staged) {
+      if (C::kSwiglu && staged) {
         if (lane == 0 && stores_pending) bulk_wait_read_all();
         __syncwarp();
       }
@@ -403,10 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         if (staged) {
-          // two boxes of 32 rows x 64 columns, 128-byte swizzled rows
+          // two passes of 32 rows x 64 columns through the staging buffer: each
+          // thread writes its row's 8 chunks of 16 bytes (chunk q of row r at
+          // slot q ^ (r & 7), so 8 consecutive rows cover all banks), then each
+          // store instruction takes 4 rows x 8 chunks = four whole 128-byte lines
+          const int sub = lane >> 3, chunk = lane & 7;
+          const int64_t x = static_cast<int64_t>(t.nt) * kBN + half * 128;
+          uint8_t* my_row = stage_buf + lane * 128;
 #pragma unroll
           for (int box = 0; box < 2; ++box) {
-            uint8_t* row_base = stage_buf + box * 4096 + lane * 128;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const float* f = &v[2 * box + (q >> 2)][8 * (q & 3)];
@@ -415,18 +425,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               o.y = pack_bf16x2(p.alpha * f[2], p.alpha * f[3]);
               o.z = pack_bf16x2(p.alpha * f[4], p.alpha * f[5]);
               o.w = pack_bf16x2(p.alpha * f[6], p.alpha * f[7]);
-              *reinterpret_cast<uint4*>(row_base + ((q ^ (lane & 7)) << 4)) = o;
+              *reinterpret_cast<uint4*>(my_row + ((q ^ (lane & 7)) << 4)) = o;
             }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int row = 4 * i + sub;
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(stage_buf + row * 128 + ((chunk ^ (row & 7)) << 4));
+              *reinterpret_cast<uint4*>(p.out_bf16 + (static_cast<int64_t>(y) + row) * p.N + x + box * 64 +
+                                        chunk * 8) = val;
+            }
+            __syncwarp();
           }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int32_t x = t.nt * kBN + half * 128;
-            tma_store_2d(&tmap_out, stage_buf, x, y);
-            tma_store_2d(&tmap_out, stage_buf + 4096, x + 64, y);
-            bulk_commit_group();
-          }
-          stores_pending = true;
         } else if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + grow * p.N + static_cast<int64_t>(t.nt) * kBN +
                                                 half * 128);
