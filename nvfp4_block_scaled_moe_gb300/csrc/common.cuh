@@ -92,19 +92,21 @@ __device__ __forceinline__ BlockScale block_scale(float amax) {
   return s;
 }
 
-// Signed half step of x / d: copysign(rne(2 * min(|x / d|, 6)) / 2, x).
-// q = RN(|x| / d2) = RN(2|x| / d) = 2 RN(|x| / d) is the IEEE quotient, obtained
-// from the correctly rounded reciprocal r2 with one FMA residual correction
-// (Markstein, as in div6_rn).  min(q, 12) is rounded to an integer with ties to
-// even by adding 1.5 * 2^23 (every float in [2^23, 2^24) is an integer), and
-// (t - 1.5 * 2^23) / 2 is exact.  With a zero scale (r2 == 0) the magnitude is 0.
+// Signed half step of x / d: rne(2 * x / d) / 2, which the E2M1 conversion then
+// maps onto its grid (saturating above 6).
+// q = RN(x / d2) = RN(2x / d) is the IEEE quotient, obtained from the correctly
+// rounded reciprocal r2 with one FMA residual correction (Markstein, as in
+// div6_rn).  The residual is taken as q0 * d2 - x and subtracted, which gives the
+// same q and keeps the sign of a zero quotient (x = -0 or a zero scale -> -0).
+// rintf (cvt.rni) rounds q to an integer with ties to even and keeps the sign, so
+// a negative x whose magnitude rounds to 0 yields -0 (the E2M1 code 0x8).  For
+// |q| <= 12 this equals copysign(rne(2 * min(|x / d|, 6)), x) / 2; above, both
+// give a value >= 6 that the saturating conversion turns into the code of 6.
 __device__ __forceinline__ float signed_halfstep(float x, const BlockScale& s) {
-  const float a = fabsf(x);
-  const float q0 = a * s.r2;
-  const float rem = fmaf(-q0, s.d2, a);
-  const float q = fmaf(rem, s.r2, q0);
-  const float t = fminf(q, 12.0f) + 12582912.0f;
-  return copysignf(fmaf(t, 0.5f, -6291456.0f), x);
+  const float q0 = x * s.r2;
+  const float rem = fmaf(q0, s.d2, -x);
+  const float q = fmaf(-rem, s.r2, q0);
+  return rintf(q) * 0.5f;
 }
 
 // Quantise eight values of one half-block with that block's scale.

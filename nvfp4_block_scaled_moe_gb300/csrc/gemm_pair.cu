@@ -433,8 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int row = 4 * i + sub;
               const uint4 val =
                   *reinterpret_cast<const uint4*>(stage_buf + row * 128 + ((chunk ^ (row & 7)) << 4));
-              *reinterpret_cast<uint4*>(p.out_bf16 + (static_cast<int64_t>(y) + row) * p.N + x + box * 64 +
-                                        chunk * 8) = val;
+              // streaming store: the rows are read back only by the combine, from HBM
+              __stcs(reinterpret_cast<uint4*>(p.out_bf16 + (static_cast<int64_t>(y) + row) * p.N + x + box * 64 +
+                                              chunk * 8),
+                     val);
             }
             __syncwarp();
           }
