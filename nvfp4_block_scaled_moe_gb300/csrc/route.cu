@@ -41,8 +41,10 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 }
 
 // ------------------------------------------------------------------ top-k --
-// One warp per token: each lane holds the logits of experts lane + 32j and its
-// best remaining key; k rounds of a warp max over the lanes' best keys.
+// One warp per token: each lane holds the logits of experts lane + 32j
+// (j < kKeys, kKeys = ceil(E / 32)) and its best remaining key; k rounds of a warp
+// max over the lanes' best keys.
+template <int kKeys>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int32_t T,
                                                          int32_t E, int32_t k, int32_t* __restrict__ ids,
                                                          float* __restrict__ w,
@@ -50,9 +52,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int lane = threadIdx.x & 31;
   const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
-  uint64_t key[32];
+  uint64_t key[kKeys];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < kKeys; ++j) {
     const int e = lane + 32 * j;
     key[j] = e < E ? topk_key(__ldg(logits + t * E + e), e) : 0ull;
   }
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   auto local_best = [&]() {
     uint64_t b = 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+    for (int j = 0; j < kKeys; ++j)
       if (!((taken >> j) & 1u) && key[j] > b) b = key[j];
     return b;
   };
@@ -93,6 +95,18 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     w[t * k + lane] = z / sum;
     atomicAdd(&chunk_hist[(t / kRouteChunk) * E + my_e], 1);
   }
+}
+
+static cudaError_t launch_topk(const RouteBuffers& b, cudaStream_t stream) {
+  const dim3 grid((b.T + 7) / 8), block(256);
+  const int keys = (b.E + 31) / 32;
+  if (keys <= 1) route_topk_kernel<1><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
+  else if (keys <= 2) route_topk_kernel<2><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
+  else if (keys <= 4) route_topk_kernel<4><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
+  else if (keys <= 8) route_topk_kernel<8><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
+  else if (keys <= 16) route_topk_kernel<16><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
+  else route_topk_kernel<32><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- offsets --
@@ -207,64 +221,78 @@ __global__ void __launch_bounds__(128) route_assign_kernel(const int32_t* __rest
 
 // ---------------------------------------------------------------- scatter --
 // Quantise x (PLAIN, per 16 along H) and write the bytes into each of the token's
-// k permuted rows.  Grid (T, ceil(H/256 / 8)); one warp per 256-value segment;
-// one thread per 8 values, a lane pair per 16-block, a lane octet per scale word.
+// k permuted rows.  Grid (T, ceil(H/1024 / warps)); one warp per 1024-value
+// segment, one thread per two 16-blocks: its 16 bytes of nibbles go to each row
+// in one store (a warp writes 512 contiguous bytes), and a lane pair's four
+// scale bytes form one word of the swizzled layout.  H % 64 == 0, so a lane pair
+// is either wholly inside the row or wholly past its end.
 __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int32_t H,
                                                             int32_t k, const int32_t* __restrict__ inv_perm,
                                                             uint8_t* __restrict__ a_q,
                                                             uint8_t* __restrict__ a_sf) {
   const int lane = threadIdx.x & 31;
-  const int64_t seg = static_cast<int64_t>(blockIdx.y) * 8 + (threadIdx.x >> 5);
-  if (seg * 256 >= H) return;
+  const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (seg * 1024 >= H) return;
   const int64_t t = blockIdx.x;
-  const int64_t c0 = seg * 256 + lane * 8;
+  const int64_t c0 = seg * 1024 + lane * 32;
   const bool active = c0 < H;
-  float h[8];
+  uint4 nib = make_uint4(0, 0, 0, 0);
+  uint32_t codes = 0;
   if (active) {
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(x + t * H + c0)), h);
-  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H + c0);
+    uint4 raw[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = 0.0f;
+    for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
+    uint32_t w[4];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {            // two 16-blocks of 16 values
+      float lo[8], hi[8];
+      bf16x8_to_f32(raw[2 * b], lo);
+      bf16x8_to_f32(raw[2 * b + 1], hi);
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
+      const BlockScale s = block_scale(amax);
+      w[2 * b] = quantize8(lo, s);
+      w[2 * b + 1] = quantize8(hi, s);
+      codes |= s.code << (8 * b);
+    }
+    nib = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  const BlockScale s = block_scale(amax);
-  const uint32_t nib = quantize8(h, s);
-  const uint32_t code = active ? s.code : 0u;
-  const int base = lane & ~7;
-  const uint32_t word = __shfl_sync(0xFFFFFFFFu, code, base) | (__shfl_sync(0xFFFFFFFFu, code, base + 2) << 8) |
-                        (__shfl_sync(0xFFFFFFFFu, code, base + 4) << 16) |
-                        (__shfl_sync(0xFFFFFFFFu, code, base + 6) << 24);
-  const uint32_t k4 = static_cast<uint32_t>(seg * 4 + (lane >> 3));
+  // lanes 2m, 2m+1 own one 64-column group: codes of its four blocks in order
+  const uint32_t word = codes | (__shfl_down_sync(0xFFFFFFFFu, codes, 1) << 16);
+  const uint32_t k4 = static_cast<uint32_t>(c0 / 64);
   const uint32_t k4_total = static_cast<uint32_t>(H / 64);
   for (int j = 0; j < k; ++j) {
     const int64_t r = __ldg(inv_perm + t * k + j);
-    if (active) *reinterpret_cast<uint32_t*>(a_q + r * (H / 2) + c0 / 2) = nib;
-    if ((lane & 7) == 0 && k4 < k4_total)
-      *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, k4, k4_total)) = word;
+    if (active) {
+      *reinterpret_cast<uint4*>(a_q + r * (H / 2) + c0 / 2) = nib;
+      if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, k4, k4_total)) = word;
+    }
   }
 }
 
 // -------------------------------------------------------------- pad fill --
-// One block per expert: zero the nibbles and scale words of the padding rows
-// [offsets[e] + counts[e], offsets[e+1]).
+// Zero the nibbles and scale words of the padding rows [offsets[e] + counts[e],
+// offsets[e+1]) of every expert: blockIdx.y = expert, blockIdx.x strides over its
+// padding (at most 127 rows).
 __global__ void __launch_bounds__(256) route_padfill_kernel(const int32_t* __restrict__ counts,
                                                             const int32_t* __restrict__ offsets, int32_t H,
                                                             uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf) {
-  const int e = blockIdx.x;
+  const int e = blockIdx.y;
   const int64_t lo = __ldg(offsets + e) + __ldg(counts + e);
   const int64_t hi = __ldg(offsets + e + 1);
   const int n16 = H / 32;                 // 16-byte chunks per row
   const int k4_total = H / 64;
   const int64_t nq = (hi - lo) * n16;
-  for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = first; i < nq; i += stride) {
     const int64_t r = lo + i / n16;
     reinterpret_cast<uint4*>(a_q + r * (H / 2))[i % n16] = make_uint4(0, 0, 0, 0);
   }
   const int64_t ns = (hi - lo) * k4_total;
-  for (int64_t i = threadIdx.x; i < ns; i += blockDim.x) {
+  for (int64_t i = first; i < ns; i += stride) {
     const int64_t r = lo + i / k4_total;
     *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, static_cast<uint32_t>(i % k4_total), k4_total)) = 0u;
   }
@@ -275,19 +303,24 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
   if (n_chunks > 0) {
     cudaError_t e = cudaMemsetAsync(b.chunk_hist, 0, static_cast<size_t>(n_chunks) * b.E * sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
-    route_topk_kernel<<<(b.T + 7) / 8, 256, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w,
-                                                         b.chunk_hist);
+    e = launch_topk(b, stream);
+    if (e != cudaSuccess) return e;
   }
   route_offsets_kernel<<<1, 1024, 0, stream>>>(b.chunk_hist, n_chunks, b.E, b.counts, b.offsets, b.perm_token);
   if (n_chunks > 0) {
     const size_t smem = (2 * static_cast<size_t>(b.E) + static_cast<size_t>(kRouteChunk) * b.top_k) * sizeof(int32_t);
     route_assign_kernel<<<n_chunks, 128, smem, stream>>>(b.topk_ids, b.T, b.E, b.top_k, b.chunk_hist, b.offsets,
                                                          b.perm_token, b.inv_perm);
-    route_padfill_kernel<<<b.E, 256, 0, stream>>>(b.counts, b.offsets, b.H, b.a1_q, b.a1_sf);
-    const int64_t segs = (b.H + 255) / 256;
-    const dim3 grid(static_cast<unsigned>(b.T), static_cast<unsigned>((segs + 7) / 8));
-    route_scatter_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k, b.inv_perm,
-                                                   b.a1_q, b.a1_sf);
+    // up to 127 padding rows per expert: enough blocks per expert to cover them
+    const int64_t pad_chunks = 127LL * (b.H / 32);
+    const unsigned per_expert = static_cast<unsigned>((pad_chunks + 256 * 8 - 1) / (256 * 8));
+    route_padfill_kernel<<<dim3(per_expert, static_cast<unsigned>(b.E)), 256, 0, stream>>>(b.counts, b.offsets, b.H,
+                                                                                          b.a1_q, b.a1_sf);
+    const int64_t segs = (b.H + 1023) / 1024;
+    const int warps = static_cast<int>(segs < 8 ? segs : 8);     // no idle warps on short rows
+    const dim3 grid(static_cast<unsigned>(b.T), static_cast<unsigned>((segs + warps - 1) / warps));
+    route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k,
+                                                          b.inv_perm, b.a1_q, b.a1_sf);
   }
   return cudaGetLastError();
 }
