@@ -347,7 +347,10 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                    "parallelism": f"replicas x{world} (independent batches)"},
         "tokens_per_s": tokens_per_s,
         "kernel_ms": per,
-        "roofline": {"kernel": "nvf4_gemm_kernel<SwiGLU+NVFP4> (L1)", "bound": "tensor",
+        "roofline": {"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
+                                if args.workload == WORKLOAD else
+                                "L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_kernel<0, 256> (single CTAs)"),
+                     "bound": "tensor",
                      "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
                      "peak_source": f"{pk['source']} bf16 sustained {pk['bf16_sustained']} x {FP4_OVER_BF16:g} "
                                     "(nominal FP4/BF16 dense ratio)",
@@ -434,7 +437,8 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
         "config": {"workload": f"dense NVFP4 GEMM M={M} N={N} K={K} + SwiGLU + NVFP4 requant",
                    "l2_policy": "L2 flushed (256 MiB write) before every step; per-step CUDA events",
                    "launch": "each step a one-launch CUDA graph replayed after the flush"},
-        "roofline": {"kernel": "nvf4_gemm_kernel<SwiGLU+NVFP4>", "bound": "tensor", "achieved": tflops,
+        "roofline": {"kernel": "nvf4_gemm_pair_kernel<0> (SwiGLU + NVFP4 epilogue, CTA pairs)", "bound": "tensor",
+                     "achieved": tflops,
                      "peak": fp4_peak, "unit": "TFLOP/s", "frac": tflops / fp4_peak,
                      "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} x {FP4_OVER_BF16:g}",
                      "algorithmic": "2*M*N*K FLOP per launch", "traffic": None},
