@@ -200,3 +200,50 @@ def test_gemm_one_hot_locates_nibbles_and_scales(nv):
         expect = np.zeros((M, N))
         expect[r, n] = 1.5 * 4.0 * onv.e4m3_decode(a_sf[r, k // 16]) * onv.e4m3_decode(b_sf[n, k // 16])
         assert np.array_equal(got, omoe.round_to_bf16(expect)), (r, n, k)
+
+
+def test_dense_config_full_size_sampled_rows(nv):
+    """The dense L1 workload at full size (8192 x 4096 x 7168, seeded as bench.py
+    runs it, the same launch: tile kernel by default, SwiGLU + NVFP4 epilogue).
+    The GPU-quantised operands are bit-exact (all of B, sampled rows of A); on
+    sampled output rows h matches the float64 GEMM of the dequantised operands,
+    the re-quantised codes stay within the bound, and they are bit-exact against
+    the oracle fed the kernel's own h.  Without h_debug the bytes are the same."""
+    spec = dict(inputs.CONFIGS["dense"])
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    I = N // 2
+    a, bw = inputs.dense_inputs(spec)
+    a_d, b_d = torch.from_numpy(a).cuda(), torch.from_numpy(bw).cuda()
+    a_q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    a_sf = torch.empty(nv.sf_bytes(M, K), dtype=torch.uint8, device="cuda")
+    b_q = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    b_sf = torch.empty(nv.sf_bytes(N, K), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_quantize(a_d, K, nv.MODE_PLAIN, a_q, a_sf)
+    nv.nvfp4_quantize(b_d, K, nv.MODE_PLAIN, b_q, b_sf)
+    out_q = torch.empty((M, I // 2), dtype=torch.uint8, device="cuda")
+    out_sf = torch.empty(nv.sf_bytes(M, I), dtype=torch.uint8, device="cuda")
+    h = torch.empty((M, I), dtype=torch.float32, device="cuda")
+    nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_SWIGLU_NVFP4,
+                          out_q=out_q, out_sf=out_sf, h_debug=h)
+    q2, sf2 = torch.empty_like(out_q), torch.empty_like(out_sf)
+    nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_SWIGLU_NVFP4,
+                          out_q=q2, out_sf=sf2)
+    nv.nvfp4_device_status()
+    assert torch.equal(out_q, q2) and torch.equal(out_sf, sf2)
+    ob_q, ob_sf = onv.quantize_rows(bw)
+    assert np.array_equal(host(b_q), ob_q)
+    assert np.array_equal(onv.unswizzle_sf(host(b_sf), N, K // 16), ob_sf)
+    pick = np.unique(np.concatenate([np.random.default_rng(12).choice(M, 22, replace=False), [0, M - 1]]))
+    oa_q, oa_sf = onv.quantize_rows(a[pick])
+    assert np.array_equal(host(a_q)[pick], oa_q)
+    assert np.array_equal(onv.unswizzle_sf(host(a_sf), M, K // 16)[pick], oa_sf)
+    g = onv.dequantize_rows(oa_q, oa_sf) @ onv.dequantize_rows(ob_q, ob_sf).T
+    oq, osf, oh = omoe.l1_swiglu_requant(g)
+    gh = host(h)[pick]
+    assert rel_frobenius(gh, oh) <= 2e-3
+    gq = host(out_q)[pick]
+    gsf = onv.unswizzle_sf(host(out_sf), M, I // 16)[pick]
+    res = compare_requantised(gq, gsf, oq, osf)
+    assert res["ok"], res
+    hq, hsf = onv.quantize_rows(gh)
+    assert np.array_equal(hq, gq) and np.array_equal(hsf, gsf)

@@ -139,3 +139,48 @@ def test_sf_swizzle_forward_and_inverse(nv, mn, k_sf):
     nv.nvfp4_sf_swizzle(out, mn, k_sf, k_sf, 1, back, inverse=True)
     nv.nvfp4_device_status()
     assert np.array_equal(host(back), lin)
+
+
+def test_quantizer_config_full_size(nv):
+    """The SwiGLU + NVFP4 quantiser workload at full size (32768 x 2 x 2048, seeded
+    as bench.py runs it).  Sampled rows (random ones and rows holding planted
+    blocks): the codes are bit-exact against the oracle fed the kernel's own fp32
+    h, h matches the float64 oracle, and the codes stay within the re-quantisation
+    bound of the oracle's own.  Every planted tie block (h exact on both sides)
+    is compared code for code.  The timed launch (no h_debug) writes the same bytes."""
+    spec = dict(inputs.CONFIGS["quantizer"])
+    rows, cols = spec["rows"], spec["cols"]
+    nb = cols // 16
+    gu_t, plant = inputs.quantizer_input(spec)
+    gu_d = gu_t.cuda()
+    q = torch.empty((rows, cols // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty(nv.sf_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    h = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    nv.nvfp4_quantize(gu_d, cols, nv.MODE_SWIGLU_GU8, q, sf, h_debug=h)
+    q2, sf2 = torch.empty_like(q), torch.empty_like(sf)
+    nv.nvfp4_quantize(gu_d, cols, nv.MODE_SWIGLU_GU8, q2, sf2)
+    nv.nvfp4_device_status()
+    assert torch.equal(q, q2) and torch.equal(sf, sf2)
+    gq, gh = host(q), host(h)
+    gsf = onv.unswizzle_sf(host(sf), rows, nb)
+    rng = np.random.default_rng(11)
+    planted_rows = np.unique(np.concatenate([plant[k] // nb for k in ("tiny", "saturate", "midpoint")]))
+    pick = np.unique(np.concatenate([rng.choice(rows, 192, replace=False),
+                                     rng.choice(planted_rows, 192, replace=False), [0, rows - 1]]))
+    # identical fp32 inputs -> identical codes
+    oq_h, osf_h = onv.quantize_rows(gh[pick])
+    assert np.array_equal(oq_h, gq[pick]) and np.array_equal(osf_h, gsf[pick])
+    # h against float64, codes within the bound of the oracle's own
+    gu = gu_t[torch.from_numpy(pick)].float().numpy()
+    oq, osf, oh = onv.quantize_swiglu_gu8(gu)
+    rel = np.abs(gh[pick] - oh) / np.maximum(np.abs(oh), 1e-30)
+    assert np.quantile(rel, 0.999) < 1e-5 and rel.max() < 1e-4
+    res = compare_requantised(gq[pick], gsf[pick], oq, osf)
+    assert res["ok"], res
+    # every planted tie block, each as a one-block row for the oracle
+    r, b = np.divmod(plant["midpoint"], nb)
+    chunks = gu_t.view(rows, nb, 32)[torch.from_numpy(r), torch.from_numpy(b)].float().numpy()
+    pq, psf, ph = onv.quantize_swiglu_gu8(chunks)
+    assert np.array_equal(gh.reshape(rows, nb, 16)[r, b], ph)
+    assert np.array_equal(gsf[r, b], psf[:, 0])
+    assert np.array_equal(gq.reshape(rows, nb, 8)[r, b], pq)
