@@ -17,6 +17,10 @@ Readings where the pages are silent:
   hold zero nibbles and zero scales and are marked -1 in ``perm_token``;
 * GEMMs accumulate exactly (float64 on dequantised operands) and apply the fp32
   ``alpha`` scalar (global scale 1 by default);
+* two-level scale (optional): per-tensor encode scales g (``nvfp4.global_scale``)
+  for x and for each expert's W1 and W2, and a given encode scale for the L1
+  output; each GEMM then applies fp32(alpha / fp32(g_A * g_B[e])) to the
+  product of the one-level dequantised operands ("alpha = igs * global_sf");
 * the L1 output is quantised from fp32 h (never from a BF16-rounded h);
 * L2 rows and the combined output are BF16 (round-to-nearest-even); the
   combine sums the k slots in slot order.
@@ -94,12 +98,12 @@ def permute(ids: np.ndarray, n_experts: int, align: int = ROW_ALIGN) -> dict:
                 perm_token=perm_token.astype(np.int32), inv_perm=inv_perm.astype(np.int32))
 
 
-def stage_activation(x: np.ndarray, perm_token: np.ndarray) -> tuple:
+def stage_activation(x: np.ndarray, perm_token: np.ndarray, gscale=None) -> tuple:
     """Quantise x (fp32 view of the BF16 activations, [T,H]) into the permuted,
     padded rows: (a1_q [R_pad, H/2], a1_sf row-major [R_pad, H/16]).  Padding
-    rows are zero."""
+    rows are zero.  ``gscale``: the two-level encode scale of x, if any."""
     x = np.asarray(x, dtype=np.float32)
-    xq, xsf = nvfp4.quantize_rows(x)
+    xq, xsf = nvfp4.quantize_rows(x, gscale)
     r_pad = len(perm_token)
     a_q = np.zeros((r_pad, xq.shape[1]), dtype=np.uint8)
     a_sf = np.zeros((r_pad, xsf.shape[1]), dtype=np.uint8)
@@ -116,26 +120,39 @@ def expert_of_rows(offsets: np.ndarray) -> np.ndarray:
     return np.repeat(np.arange(len(offsets) - 1), np.diff(offsets))
 
 
+def two_level_alpha(alpha: float, ga, gb) -> np.float32:
+    """fp32(alpha / fp32(ga * gb)): a GEMM's alpha under encode scales ga, gb."""
+    return np.float32(np.float32(alpha) / np.float32(np.float32(ga) * np.float32(gb)))
+
+
 def grouped_gemm(a_deq: np.ndarray, offsets: np.ndarray, b_deq: np.ndarray,
-                 alpha: float = 1.0) -> np.ndarray:
-    """out[r, n] = alpha * sum_k a[r, k] * b_e[n, k] for the expert e owning row r
-    (float64; ``b_deq`` is [E, N, K])."""
+                 alpha: float = 1.0, a_gscale=None, b_gscale=None) -> np.ndarray:
+    """out[r, n] = alpha_e * sum_k a[r, k] * b_e[n, k] for the expert e owning row r
+    (float64; ``b_deq`` is [E, N, K]), the operands dequantised at one level.
+    alpha_e = alpha, or two_level_alpha(alpha, a_gscale, b_gscale[e]) when either
+    encode scale is given."""
     offsets = np.asarray(offsets, dtype=np.int64)
     out = np.zeros((a_deq.shape[0], b_deq.shape[1]), dtype=np.float64)
     for e in range(len(offsets) - 1):
         lo, hi = offsets[e], offsets[e + 1]
         if hi > lo:
-            out[lo:hi] = a_deq[lo:hi] @ b_deq[e].T
-    return np.float64(np.float32(alpha)) * out
+            if a_gscale is None and b_gscale is None:
+                alpha_e = np.float32(alpha)
+            else:
+                alpha_e = two_level_alpha(alpha, 1.0 if a_gscale is None else a_gscale,
+                                          1.0 if b_gscale is None else b_gscale[e])
+            out[lo:hi] = np.float64(alpha_e) * (a_deq[lo:hi] @ b_deq[e].T)
+    return out
 
 
-def l1_swiglu_requant(g_full: np.ndarray) -> tuple:
+def l1_swiglu_requant(g_full: np.ndarray, out_gscale=None) -> tuple:
     """Fused L1 epilogue on the interleaved gate/up accumulator rows
-    (float64 [rows, 2I]): h = silu(g) * u -> fp32, then NVFP4 per 16.
+    (float64 [rows, 2I]): h = silu(g) * u -> fp32, then NVFP4 per 16 (of
+    fp32(h * out_gscale) under a two-level encode scale).
     Returns (a2_q [rows, I/2], a2_sf row-major [rows, I/16], h fp32 [rows, I])."""
     g, u = nvfp4.deinterleave_gu8(g_full)
     h = nvfp4.swiglu_h(g, u)
-    q, sf = nvfp4.quantize_rows(h)
+    q, sf = nvfp4.quantize_rows(h, out_gscale)
     return q, sf, h
 
 
@@ -156,52 +173,75 @@ def dequant_weights(w_q: np.ndarray, w_sf_rows: np.ndarray) -> np.ndarray:
     return np.stack([nvfp4.dequantize_rows(w_q[e], w_sf_rows[e]) for e in range(e_count)])
 
 
-def quantize_weights(w: np.ndarray) -> tuple:
-    """fp32 [E, N, K] -> ([E, N, K/2] nibbles, [E, N, K/16] row-major SF)."""
-    qs, sfs = zip(*(nvfp4.quantize_rows(w[e]) for e in range(w.shape[0])))
+def quantize_weights(w: np.ndarray, gscales=None) -> tuple:
+    """fp32 [E, N, K] -> ([E, N, K/2] nibbles, [E, N, K/16] row-major SF), each
+    expert under its own encode scale gscales[e] if given."""
+    qs, sfs = zip(*(nvfp4.quantize_rows(w[e], None if gscales is None else gscales[e])
+                    for e in range(w.shape[0])))
     return np.stack(qs), np.stack(sfs)
 
 
+def two_level_scales(x: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> dict:
+    """Encode scales of the two-level scheme: x's and every expert's W1 and W2."""
+    return dict(x=nvfp4.global_scale(x),
+                w1=np.array([nvfp4.global_scale(w1[e]) for e in range(w1.shape[0])], dtype=np.float32),
+                w2=np.array([nvfp4.global_scale(w2[e]) for e in range(w2.shape[0])], dtype=np.float32))
+
+
 def moe_ffn(x: np.ndarray, logits: np.ndarray, w1: np.ndarray, w2: np.ndarray, top_k: int,
-            alpha1: float = 1.0, alpha2: float = 1.0) -> dict:
+            alpha1: float = 1.0, alpha2: float = 1.0, a2_gscale=None) -> dict:
     """The whole path on CPU.  x: fp32 values of the BF16 activations [T,H];
     logits fp32 [T,E]; w1 fp32 [E, 2I, H] (rows interleaved 8|8); w2 fp32 [E, H, I].
+    With ``a2_gscale`` (the L1 output's encode scale, given as a calibrated
+    constant) the path runs the two-level scheme: x, W1 and W2 get their own
+    encode scales (two_level_scales) and every GEMM's alpha follows.
     Returns every intermediate (all computed here, none supplied from outside)."""
     e_count = w1.shape[0]
     ids, w = route_topk(logits, top_k)
     p = permute(ids, e_count)
-    a1_q, a1_sf = stage_activation(x, p["perm_token"])
-    w1_q, w1_sf = quantize_weights(w1)
-    w2_q, w2_sf = quantize_weights(w2)
+    gs = two_level_scales(x, w1, w2) if a2_gscale is not None else dict(x=None, w1=None, w2=None)
+    a1_q, a1_sf = stage_activation(x, p["perm_token"], gs["x"])
+    w1_q, w1_sf = quantize_weights(w1, gs["w1"])
+    w2_q, w2_sf = quantize_weights(w2, gs["w2"])
     g_full = grouped_gemm(nvfp4.dequantize_rows(a1_q, a1_sf), p["offsets"],
-                          dequant_weights(w1_q, w1_sf), alpha1)
-    a2_q, a2_sf, h = l1_swiglu_requant(g_full)
+                          dequant_weights(w1_q, w1_sf), alpha1, gs["x"], gs["w1"])
+    a2_q, a2_sf, h = l1_swiglu_requant(g_full, a2_gscale)
     o = grouped_gemm(nvfp4.dequantize_rows(a2_q, a2_sf), p["offsets"],
-                     dequant_weights(w2_q, w2_sf), alpha2)
+                     dequant_weights(w2_q, w2_sf), alpha2, a2_gscale, gs["w2"])
     rows = round_to_bf16(o)
     y = combine(rows, p["inv_perm"], w)
     return dict(ids=ids, w=w, a1_q=a1_q, a1_sf=a1_sf, w1_q=w1_q, w1_sf=w1_sf, w2_q=w2_q,
-                w2_sf=w2_sf, g_full=g_full, h=h, a2_q=a2_q, a2_sf=a2_sf, rows=rows, y=y, **p)
+                w2_sf=w2_sf, g_full=g_full, h=h, a2_q=a2_q, a2_sf=a2_sf, rows=rows, y=y, gscales=gs, **p)
 
 
 def moe_ffn_tokens(x_rows: np.ndarray, logits_rows: np.ndarray, w1_of, w2_of, top_k: int,
-                   alpha1: float = 1.0, alpha2: float = 1.0, cache: dict | None = None) -> dict:
+                   alpha1: float = 1.0, alpha2: float = 1.0, cache: dict | None = None,
+                   two_level: dict | None = None) -> dict:
     """The same path for a few sampled tokens, one at a time (every step is
     row-independent: a token's output depends only on its own row, its routing
     and its experts' weights).  ``w1_of(e)`` / ``w2_of(e)`` return expert e's fp32
     weights; their quantised, dequantised forms are cached in ``cache``.
-    Returns ids, w, a2 rows (q, row-major sf) per (token, slot), and y (BF16 values)."""
+    Returns ids, w, a2 rows (q, row-major sf) per (token, slot), and y (BF16 values).
+    ``two_level``: dict(x=g_x of the whole batch, a2=the L1 output's encode scale);
+    each expert's weight encode scales are computed from its weights."""
     cache = {} if cache is None else cache
 
     def deq(kind, e, fn):
-        key = (kind, e)
+        key = (kind, e, two_level is not None)
         if key not in cache:
-            q, sf = nvfp4.quantize_rows(fn(e))
-            cache[key] = nvfp4.dequantize_rows(q, sf)
+            wt = fn(e)
+            g = nvfp4.global_scale(wt) if two_level is not None else None
+            q, sf = nvfp4.quantize_rows(wt, g)
+            cache[key] = (nvfp4.dequantize_rows(q, sf), np.float32(1.0) if g is None else g)
         return cache[key]
 
+    def alpha_of(alpha, ga, gb):
+        return np.float32(alpha) if two_level is None else two_level_alpha(alpha, ga, gb)
+
+    gx = None if two_level is None else two_level["x"]
+    ga2 = None if two_level is None else two_level["a2"]
     ids, w = route_topk(logits_rows, top_k)
-    xq, xsf = nvfp4.quantize_rows(np.asarray(x_rows, dtype=np.float32))
+    xq, xsf = nvfp4.quantize_rows(np.asarray(x_rows, dtype=np.float32), gx)
     a1 = nvfp4.dequantize_rows(xq, xsf)
     n_tok = len(x_rows)
     y, a2_q, a2_sf, h_all = [], [], [], []
@@ -209,9 +249,11 @@ def moe_ffn_tokens(x_rows: np.ndarray, logits_rows: np.ndarray, w1_of, w2_of, to
         acc = None
         for j in range(top_k):
             e = int(ids[t, j])
-            g_full = np.float64(np.float32(alpha1)) * (a1[t:t + 1] @ deq("w1", e, w1_of).T)
-            q, sf, h = l1_swiglu_requant(g_full)
-            o = np.float64(np.float32(alpha2)) * (nvfp4.dequantize_rows(q, sf) @ deq("w2", e, w2_of).T)
+            w1d, g1 = deq("w1", e, w1_of)
+            w2d, g2 = deq("w2", e, w2_of)
+            g_full = np.float64(alpha_of(alpha1, gx, g1)) * (a1[t:t + 1] @ w1d.T)
+            q, sf, h = l1_swiglu_requant(g_full, ga2)
+            o = np.float64(alpha_of(alpha2, ga2, g2)) * (nvfp4.dequantize_rows(q, sf) @ w2d.T)
             row = round_to_bf16(o)[0]
             acc = w[t, j] * row if acc is None else acc + w[t, j] * row
             a2_q.append(q[0])

@@ -188,13 +188,38 @@ def quantize_block(v) -> tuple:
     return packed, sf
 
 
-def quantize_rows(x: np.ndarray) -> tuple:
+# Two-level scale (the pages' pipeline carries a per-tensor fp32 global scale
+# next to the per-16 E4M3 scales -- "NVFP4 MegaMoE Debug Log", "NVFP4 MoE
+# Pipeline": stage_activation returns an input_global_scale and each GEMM's alpha
+# is input global scale x weight global scale; the pages print no formula).
+# Reading taken here: an encode scale g multiplies the tensor before the per-16
+# quantisation, chosen so the tensor's amax lands on the top of the E4M3 x E2M1
+# range (6 * 448); dequantisation divides by g.
+GLOBAL_RANGE = np.float32(6.0 * 448.0)
+
+
+def global_scale(x: np.ndarray) -> np.float32:
+    """g = fp32(2688 / amax(|x|)); 1 when amax is 0 or the quotient is not finite."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    if amax == 0:
+        return np.float32(1.0)
+    with np.errstate(over="ignore", divide="ignore"):
+        g = np.float32(GLOBAL_RANGE / amax)
+    return g if np.isfinite(g) else np.float32(1.0)
+
+
+def quantize_rows(x: np.ndarray, gscale=None) -> tuple:
     """Vectorised per-16 quantiser over the last axis.
 
     x: fp32 [rows, cols] (cols % 16 == 0).  Returns (q uint8 [rows, cols/2],
-    sf uint8 [rows, cols/16]) with the SF in plain row-major order.
+    sf uint8 [rows, cols/16]) with the SF in plain row-major order.  With an
+    encode scale ``gscale`` (two-level scheme) the quantised values are
+    fp32(x * gscale), rounded once.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
+    if gscale is not None:
+        x = (x * np.float32(gscale)).astype(np.float32)
     rows, cols = x.shape
     if cols % BLOCK:
         raise ValueError("cols must be a multiple of 16")
@@ -215,8 +240,9 @@ def quantize_rows(x: np.ndarray) -> tuple:
     return q, sf
 
 
-def dequantize_rows(q: np.ndarray, sf: np.ndarray) -> np.ndarray:
-    """float64 [rows, 2*q.shape[1]] from packed nibbles and row-major SF bytes."""
+def dequantize_rows(q: np.ndarray, sf: np.ndarray, gscale=None) -> np.ndarray:
+    """float64 [rows, 2*q.shape[1]] from packed nibbles and row-major SF bytes
+    (divided by the encode scale ``gscale`` of the two-level scheme, if given)."""
     q = np.asarray(q, dtype=np.uint8)
     rows, half = q.shape
     nib = np.empty((rows, 2 * half), dtype=np.uint8)
@@ -225,7 +251,8 @@ def dequantize_rows(q: np.ndarray, sf: np.ndarray) -> np.ndarray:
     table = np.array([e2m1_decode(n) for n in range(16)], dtype=np.float64)
     vals = table[nib]
     scale = E4M3_TABLE_F32[np.asarray(sf, dtype=np.uint8)].astype(np.float64)
-    return vals * np.repeat(scale, BLOCK, axis=1)
+    out = vals * np.repeat(scale, BLOCK, axis=1)
+    return out if gscale is None else out / np.float64(np.float32(gscale))
 
 
 def unpack_nibbles(q: np.ndarray) -> np.ndarray:
@@ -320,9 +347,10 @@ def swiglu_h(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
     return (silu64(gate) * np.asarray(up, dtype=np.float64)).astype(np.float32)
 
 
-def quantize_swiglu_gu8(gu: np.ndarray) -> tuple:
-    """The standalone SwiGLU + NVFP4 quantiser: interleaved gate/up -> (q, sf_row_major, h)."""
+def quantize_swiglu_gu8(gu: np.ndarray, gscale=None) -> tuple:
+    """The standalone SwiGLU + NVFP4 quantiser: interleaved gate/up -> (q, sf_row_major, h).
+    h is returned unscaled; an encode scale applies to the quantised values only."""
     g, u = deinterleave_gu8(gu)
     h = swiglu_h(g, u)
-    q, sf = quantize_rows(h)
+    q, sf = quantize_rows(h, gscale)
     return q, sf, h
