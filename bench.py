@@ -242,7 +242,8 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     spec["seed"] = spec["seed"] + 1000 * rank if rank else spec["seed"]     # each rank its own batch
     T, H, I, E, k = spec["T"], spec["H"], spec["I"], spec["E"], spec["top_k"]
     s = pipeline.MoeShape(T=T, H=H, I=I, E=E, top_k=k)
-    w = pipeline.MoeWeights(s)
+    two = args.two_level
+    w = pipeline.MoeWeights(s, two_level=two)
     pool, o1, o2 = inputs.moe_weight_pool(spec)
     w.set_from_pool(torch.from_numpy(pool).cuda(), o1, o2, float(inputs.WEIGHT_STD))
     b = pipeline.MoeBuffers(s)
@@ -250,25 +251,34 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     logits_np = inputs.moe_logits(spec)
     x_d = x_t.cuda()
     logits_d = torch.from_numpy(logits_np).cuda()
+    if two:
+        # the L1 output's encode scale, calibrated once on this batch (setup, untimed)
+        pipeline.calibrate_a2_scale(x_d, logits_d, w, b)
+        b.h_debug = None
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
     R = b.rows_max
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
 
+    gs1 = dict(a_global_scale=b.x_gs, b_global_scale=w.w1_gs, out_global_scale=b.a2_gs) if two else {}
+    gs2 = dict(a_global_scale=b.a2_gs, b_global_scale=w.w2_gs) if two else {}
+
     def step(events=None):
         if events:
             events[0].record(stream)
+        if two:                                  # x's encode scale, per batch (timed with routing)
+            nv.nvfp4_global_scale(x_d, b.x_gs)
         nv.moe_route_permute(logits_d, x_d, k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
-                             b.inv_perm, b.a1_q, b.a1_sf, b.workspace)
+                             b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_global_scale=b.x_gs if two else None)
         if events:
             events[1].record(stream)
         nv.nvfp4_grouped_gemm(b.a1_q, b.a1_sf, R, b.offsets, b.counts, E, 2 * I, H, w.w1_q, w.w1_sf, 1.0,
-                              nv.EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf)
+                              nv.EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf, **gs1)
         if events:
             events[2].record(stream)
         nv.nvfp4_grouped_gemm(b.a2_q, b.a2_sf, R, b.offsets, b.counts, E, H, I, w.w2_q, w.w2_sf, 1.0,
-                              nv.EPI_BF16, out_bf16=b.rows_out)
+                              nv.EPI_BF16, out_bf16=b.rows_out, **gs2)
         if events:
             events[3].record(stream)
         nv.moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
@@ -344,7 +354,10 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> fp32 accum", "data": "synthetic",
         "config": {"workload": _workload_name(spec, args.workload), "tokens_per_rank": T, "rows_padded_max": R,
                    "l2_policy": "inputs larger than L2 (5.7 GB of expert weights, 0.6 GB staged activations)",
-                   "parallelism": f"replicas x{world} (independent batches)"},
+                   "parallelism": f"replicas x{world} (independent batches)",
+                   "scales": ("two-level: per-tensor encode scales for x (computed each step), W1/W2 "
+                              "(per expert) and the L1 output (calibrated once), plus the per-16 E4M3 scales"
+                              if args.two_level else "per-16 E4M3 block scales (global scale 1)")},
         "tokens_per_s": tokens_per_s,
         "kernel_ms": per,
         "roofline": {"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
@@ -359,7 +372,7 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                      "traffic_unit": "bytes per launch (dram read + write)"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
                 "d2h_bytes_per_step": T * H * 2},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": (10 if args.two_level else 8) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -516,6 +529,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--two-level", action="store_true",
+                    help="prefill/decode with the two-level scale (per-tensor encode scales next to the per-16 "
+                         "ones); the CPU baseline stays the one-level oracle")
     ap.add_argument("--workload", choices=("prefill", "decode", "dense", "quantizer"), default=WORKLOAD,
                     help="prefill (default) and decode time the whole MoE FFN step; dense times the L1 GEMM of "
                          "one 8192-row expert; quantizer the standalone SwiGLU + NVFP4 quantiser")

@@ -92,6 +92,31 @@ int64_t moe_padded_rows_max(int32_t T, int32_t E, int32_t top_k);
 /* Bytes of device workspace moe_route_permute needs. */
 size_t moe_route_permute_workspace(int32_t T, int32_t H, int32_t E, int32_t top_k);
 
+/* Two-level scale.  The pages' pipeline carries a per-tensor fp32 global scale
+ * beside the per-16 E4M3 scales ("NVFP4 MegaMoE Debug Log", "NVFP4 MoE Pipeline":
+ * stage_activation returns an input_global_scale; each GEMM's alpha is
+ * igs * global_sf) but prints no formula.  This library's reading: an encode
+ * scale g (a device fp32 scalar, or one per expert for weights) multiplies the
+ * tensor before the per-16 quantisation, i.e. the quantised values are
+ * fp32(v * g); a quantised value decodes as e2m1 * e4m3 / g.  Every argument
+ * named *global_scale below is such an encode scale, passed as a device
+ * pointer; NULL means g = 1 (the one-level scheme, bit for bit).  The pages' igs
+ * and global_sf are the reciprocals 1/g. */
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_global_scale -- g = fp32(2688 / amax |in|), the encode scale that puts
+ * the tensor's largest magnitude at the top of the E2M1 x E4M3 range (6 x 448);
+ * g = 1 when amax is 0 or the quotient is not finite (the dynamic
+ * input_global_scale of the pages' stage_activation).
+ *   in          rows x cols BF16 or fp32 values, row stride in_ld_elems elements,
+ *               16-byte aligned with in_ld_elems * element size a multiple of 16.
+ *   cols        a positive multiple of 8.
+ *   g_out       device fp32 scalar (written; also used as the reduction's
+ *               accumulator, so it must not alias the input).
+ * -------------------------------------------------------------------------- */
+nvfp4_status nvfp4_global_scale(const void* in, nvfp4_in_dtype dtype, int64_t rows, int64_t cols,
+                                int64_t in_ld_elems, float* g_out, nvfp4_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * nvfp4_quantize -- per-16 NVFP4 quantiser ("NVFP4-1.1 Approach, Part 2": the
  * quantize_nvfp4 kernel and the deinterleave + quantise kernel; the E4M3 cast
@@ -104,15 +129,18 @@ size_t moe_route_permute_workspace(int32_t T, int32_t H, int32_t E, int32_t top_
  *   q_out       rows x out_cols/2 bytes, row-major (written).
  *   sf_out      nvfp4_sf_bytes(rows, out_cols) bytes, swizzled (every byte written,
  *               padding as zero).
- *   h_debug     NULL, or rows x out_cols fp32: the values that were quantised.
+ *   global_scale  NULL or the device fp32 encode scale g (two-level scale): the
+ *               quantised values are fp32(h * g).
+ *   h_debug     NULL, or rows x out_cols fp32: the values h before g is applied.
  * PLAIN mode is bit-exact against the specification above.  SWIGLU_GU8 computes
  * silu with the fast exponential, so h may differ from a float64 evaluation by
- * a few ulp, which can move a value across a rounding boundary.
+ * a few ulp, which can move a value across a rounding boundary; the codes are
+ * bit-exact against the specification applied to the h it reports.
  * -------------------------------------------------------------------------- */
 nvfp4_status nvfp4_quantize(const void* in, nvfp4_in_dtype dtype, nvfp4_quant_mode mode,
                             int64_t rows, int64_t out_cols, int64_t in_ld_elems,
-                            uint8_t* q_out, uint8_t* sf_out, float* h_debug,
-                            nvfp4_stream_t stream);
+                            uint8_t* q_out, uint8_t* sf_out, const float* global_scale,
+                            float* h_debug, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_sf_swizzle -- the SF remap of the "NVFP4 MegaMoE Debug Log" ("What the
@@ -147,6 +175,7 @@ nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_s
  *   a1_q        [R_max, H/2] NVFP4 rows of x in permuted order; padding rows
  *               inside groups are zero.
  *   a1_sf       nvfp4_sf_bytes(R_max, H) bytes, swizzled, zero on padding rows.
+ *   x_global_scale  NULL or x's device encode scale g (the rows hold fp32(x * g)).
  *   workspace   >= moe_route_permute_workspace(T, H, E, top_k) bytes, 16-byte
  *               aligned (per-chunk expert histograms, cleared by the call).
  * Limits: 1 <= E <= 1024, 1 <= top_k <= min(E, 32), H a positive multiple of 64,
@@ -156,8 +185,8 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
                                int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
                                int32_t* expert_counts, int32_t* expert_offsets,
                                int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                               uint8_t* a1_sf, void* workspace, size_t workspace_bytes,
-                               nvfp4_stream_t stream);
+                               uint8_t* a1_sf, const float* x_global_scale, void* workspace,
+                               size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_route_permute_static -- moe_route_permute for callers that cannot allocate
@@ -181,7 +210,8 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
                                       int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
                                       int32_t* expert_counts, int32_t* expert_offsets,
                                       int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                                      uint8_t* a1_sf, nvfp4_stream_t stream);
+                                      uint8_t* a1_sf, const float* x_global_scale,
+                                      nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_grouped_gemm -- block-scaled NVFP4 grouped GEMM on the tcgen05 tensor
@@ -197,6 +227,12 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *   b_q, b_sf   B: [G, N, K/2] bytes; SF swizzled per group (N x K each,
  *               nvfp4_sf_bytes(N, K) bytes apart).
  *   alpha       fp32 scalar applied to acc.
+ *   a_global_scale, b_global_scale  NULL or the two-level encode scales of A
+ *               (device scalar) and of each group's B (device fp32 [G]): group g
+ *               then applies alpha_g = alpha / (g_A * g_B[g]) (one IEEE quotient
+ *               of alpha by the fp32 product) in place of alpha.
+ *   out_global_scale  NULL or the encode scale of the SwiGLU output: the
+ *               re-quantised values are fp32(h * g) (h_debug keeps h).
  *   epilogue    NVFP4_EPI_SWIGLU_NVFP4: N columns interleaved 8|8 as gate/up;
  *               h = silu(alpha*g) * (alpha*u) quantised as in nvfp4_quantize ->
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
@@ -213,9 +249,10 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
 nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,
                                 const int32_t* group_offsets, const int32_t* group_counts,
                                 int32_t G, int32_t N, int32_t K, const uint8_t* b_q,
-                                const uint8_t* b_sf, float alpha, nvfp4_epilogue epilogue,
-                                uint8_t* out_q, uint8_t* out_sf, void* out_bf16,
-                                float* h_debug, nvfp4_stream_t stream);
+                                const uint8_t* b_sf, float alpha, const float* a_global_scale,
+                                const float* b_global_scale, const float* out_global_scale,
+                                nvfp4_epilogue epilogue, uint8_t* out_q, uint8_t* out_sf,
+                                void* out_bf16, float* h_debug, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_set_gemm_tiles -- process-wide choice of nvfp4_grouped_gemm's tile kernel
@@ -240,6 +277,13 @@ nvfp4_status nvfp4_set_gemm_tiles(int32_t mode);
  *                output (written for real rows only).
  *   rows_out     BF16 [rows_max, H]: alpha2 * L2 rows (real rows only).
  *   h_debug      NULL or fp32 [rows_max, I] (pre-quantisation h).
+ *   x_global_scale, w1_global_scale [E], a2_global_scale, w2_global_scale [E]:
+ *                NULL or the two-level encode scales of A1, W1, A2 and W2
+ *                (device fp32).  L1 applies alpha1 / (g_x * g_w1[e]) and
+ *                re-quantises fp32(h * g_a2); L2 applies alpha2 / (g_a2 * g_w2[e])
+ *                (the pages' alpha = igs * global_sf).  g_a2 is an input: the
+ *                fused epilogue quantises each tile as it is produced, before the
+ *                tensor's amax exists, so the scale is calibrated ahead.
  * Limits: H and I positive multiples of 256, rows_max a positive multiple of 128.
  * -------------------------------------------------------------------------- */
 nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
@@ -247,7 +291,9 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
                                    int32_t E, int32_t H, int32_t I, int64_t rows_max,
                                    const uint8_t* w1_q, const uint8_t* w1_sf,
                                    const uint8_t* w2_q, const uint8_t* w2_sf, float alpha1,
-                                   float alpha2, uint8_t* a2_q, uint8_t* a2_sf,
+                                   float alpha2, const float* x_global_scale,
+                                   const float* w1_global_scale, const float* a2_global_scale,
+                                   const float* w2_global_scale, uint8_t* a2_q, uint8_t* a2_sf,
                                    void* rows_out_bf16, float* h_debug, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------

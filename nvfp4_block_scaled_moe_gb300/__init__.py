@@ -20,6 +20,7 @@ __all__ = [
     "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
     "moe_route_permute", "moe_route_permute_static", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
     "moe_combine", "nvfp4_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_set_gemm_tiles",
+    "nvfp4_global_scale",
     "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
 ]
 
@@ -48,17 +49,19 @@ _SIGS = {
     "nvfp4_sf_bytes": (_sz, [_i64, _i64]),
     "moe_padded_rows_max": (_i64, [_i32, _i32, _i32]),
     "moe_route_permute_workspace": (_sz, [_i32, _i32, _i32, _i32]),
-    "nvfp4_quantize": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "nvfp4_quantize": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                      _vp]),
+    "nvfp4_global_scale": (ctypes.c_int, [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp]),
     "nvfp4_sf_swizzle": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i64, _vp, ctypes.c_int, _vp]),
     "moe_route_permute": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                         _vp, _vp, _sz, _vp]),
+                                         _vp, _vp, _vp, _sz, _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _f32,
-                                          ctypes.c_int, _vp, _vp, _vp, _vp, _vp]),
+                                          _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_moe_ffn_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp,
-                                             _f32, _f32, _vp, _vp, _vp, _vp, _vp]),
+                                             _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "moe_route_permute_static": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
-                                                _vp, _vp, _vp]),
+                                                _vp, _vp, _vp, _vp]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
@@ -110,12 +113,22 @@ def moe_route_permute_workspace(T: int, H: int, E: int, top_k: int) -> int:
 
 
 # ----------------------------------------------------------------- calls --
-def nvfp4_quantize(inp, out_cols, mode, q_out, sf_out, h_debug=None, in_ld=None, stream=None):
-    """inp: BF16 or fp32 [rows, in_cols] CUDA tensor (rows may be strided)."""
+def nvfp4_quantize(inp, out_cols, mode, q_out, sf_out, h_debug=None, in_ld=None, stream=None, global_scale=None):
+    """inp: BF16 or fp32 [rows, in_cols] CUDA tensor (rows may be strided);
+    global_scale: None or a device fp32 scalar tensor (two-level encode scale)."""
     dtype = IN_BF16 if inp.dtype == torch.bfloat16 else IN_F32
     ld = inp.stride(0) if in_ld is None else in_ld
     _check(load().nvfp4_quantize(_p(inp), dtype, mode, inp.shape[0], out_cols, ld, _p(q_out), _p(sf_out),
-                                 _p(h_debug), _stream(stream)))
+                                 _p(global_scale), _p(h_debug), _stream(stream)))
+
+
+def nvfp4_global_scale(inp, g_out, cols=None, in_ld=None, stream=None):
+    """g_out (device fp32 scalar) = 2688 / amax |inp| (1 for an all-zero tensor)."""
+    dtype = IN_BF16 if inp.dtype == torch.bfloat16 else IN_F32
+    rows = inp.shape[0] if inp.dim() > 1 else 1
+    cols = (inp.shape[-1] if inp.dim() > 1 else inp.numel()) if cols is None else cols
+    ld = (inp.stride(0) if inp.dim() > 1 else cols) if in_ld is None else in_ld
+    _check(load().nvfp4_global_scale(_p(inp), dtype, rows, cols, ld, _p(g_out), _stream(stream)))
 
 
 def nvfp4_sf_swizzle(sf_in, mn_rows, k_sf_cols, stride_mn, stride_ksf, sf_out, inverse=False, stream=None):
@@ -124,38 +137,43 @@ def nvfp4_sf_swizzle(sf_in, mn_rows, k_sf_cols, stride_mn, stride_ksf, sf_out, i
 
 
 def moe_route_permute(logits, x, top_k, topk_ids, topk_w, expert_counts, expert_offsets, perm_token, inv_perm,
-                      a1_q, a1_sf, workspace, stream=None):
+                      a1_q, a1_sf, workspace, stream=None, x_global_scale=None):
     T, E = logits.shape
     H = x.shape[1]
     _check(load().moe_route_permute(_p(logits), _p(x), T, H, E, top_k, _p(topk_ids), _p(topk_w),
                                     _p(expert_counts), _p(expert_offsets), _p(perm_token), _p(inv_perm),
-                                    _p(a1_q), _p(a1_sf), _p(workspace), workspace.numel() * workspace.element_size(),
-                                    _stream(stream)))
+                                    _p(a1_q), _p(a1_sf), _p(x_global_scale), _p(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def moe_route_permute_static(logits, x, top_k, topk_ids, topk_w, expert_counts, expert_offsets, perm_token,
-                             inv_perm, a1_q, a1_sf, stream=None):
+                             inv_perm, a1_q, a1_sf, stream=None, x_global_scale=None):
     """moe_route_permute with the library's fixed device scratch instead of a
     caller workspace, for callers that cannot allocate (see include/nvfp4moe.h)."""
     T, E = logits.shape
     H = x.shape[1]
     _check(load().moe_route_permute_static(_p(logits), _p(x), T, H, E, top_k, _p(topk_ids), _p(topk_w),
                                            _p(expert_counts), _p(expert_offsets), _p(perm_token), _p(inv_perm),
-                                           _p(a1_q), _p(a1_sf), _stream(stream)))
+                                           _p(a1_q), _p(a1_sf), _p(x_global_scale), _stream(stream)))
 
 
 def nvfp4_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, alpha, epilogue,
-                       out_q=None, out_sf=None, out_bf16=None, h_debug=None, stream=None):
+                       out_q=None, out_sf=None, out_bf16=None, h_debug=None, stream=None, a_global_scale=None,
+                       b_global_scale=None, out_global_scale=None):
     _check(load().nvfp4_grouped_gemm(_p(a_q), _p(a_sf), rows_max, _p(group_offsets), _p(group_counts), G, N, K,
-                                     _p(b_q), _p(b_sf), alpha, epilogue, _p(out_q), _p(out_sf), _p(out_bf16),
+                                     _p(b_q), _p(b_sf), alpha, _p(a_global_scale), _p(b_global_scale),
+                                     _p(out_global_scale), epilogue, _p(out_q), _p(out_sf), _p(out_bf16),
                                      _p(h_debug), _stream(stream)))
 
 
 def nvfp4_moe_ffn_forward(a1_q, a1_sf, expert_offsets, expert_counts, E, H, I, rows_max, w1_q, w1_sf, w2_q, w2_sf,
-                          alpha1, alpha2, a2_q, a2_sf, rows_out, h_debug=None, stream=None):
+                          alpha1, alpha2, a2_q, a2_sf, rows_out, h_debug=None, stream=None, x_global_scale=None,
+                          w1_global_scale=None, a2_global_scale=None, w2_global_scale=None):
     _check(load().nvfp4_moe_ffn_forward(_p(a1_q), _p(a1_sf), _p(expert_offsets), _p(expert_counts), E, H, I,
                                         rows_max, _p(w1_q), _p(w1_sf), _p(w2_q), _p(w2_sf), alpha1, alpha2,
-                                        _p(a2_q), _p(a2_sf), _p(rows_out), _p(h_debug), _stream(stream)))
+                                        _p(x_global_scale), _p(w1_global_scale), _p(a2_global_scale),
+                                        _p(w2_global_scale), _p(a2_q), _p(a2_sf), _p(rows_out), _p(h_debug),
+                                        _stream(stream)))
 
 
 def moe_combine(rows, inv_perm, topk_w, y, stream=None):

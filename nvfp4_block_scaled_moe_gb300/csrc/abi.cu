@@ -58,6 +58,7 @@ cudaError_t selftest_wait_launch(const int32_t* flag, int64_t limit_ns, cudaStre
 }
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace nvfp4
 
@@ -100,7 +101,7 @@ const char* nvfp4_last_error(void) { return g_msg; }
 
 nvfp4_status nvfp4_quantize(const void* in, nvfp4_in_dtype dtype, nvfp4_quant_mode mode, int64_t rows,
                             int64_t out_cols, int64_t in_ld_elems, uint8_t* q_out, uint8_t* sf_out,
-                            float* h_debug, nvfp4_stream_t stream) {
+                            const float* global_scale, float* h_debug, nvfp4_stream_t stream) {
   CHECK_ARG(in && q_out && sf_out, "nvfp4_quantize: null pointer");
   CHECK_ARG(dtype == NVFP4_IN_BF16 || dtype == NVFP4_IN_F32, "nvfp4_quantize: bad dtype %d", (int)dtype);
   CHECK_ARG(mode == NVFP4_MODE_PLAIN || mode == NVFP4_MODE_SWIGLU_GU8, "nvfp4_quantize: bad mode %d", (int)mode);
@@ -115,9 +116,28 @@ nvfp4_status nvfp4_quantize(const void* in, nvfp4_in_dtype dtype, nvfp4_quant_mo
   CHECK_AL((reinterpret_cast<uintptr_t>(q_out) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sf_out) & 3u) == 0,
            "nvfp4_quantize: outputs must be 4-byte aligned");
   CHECK_AL(h_debug == nullptr || al16(h_debug), "nvfp4_quantize: h_debug not 16-byte aligned");
-  cudaError_t e = quantize_launch(in, dtype, mode, rows, out_cols, in_ld_elems, q_out, sf_out, 0, h_debug,
-                                  reinterpret_cast<cudaStream_t>(stream));
+  CHECK_AL(al4(global_scale), "nvfp4_quantize: global_scale not 4-byte aligned");
+  cudaError_t e = quantize_launch(in, dtype, mode, rows, out_cols, in_ld_elems, q_out, sf_out, 0, global_scale,
+                                  h_debug, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_quantize");
+}
+
+nvfp4_status nvfp4_global_scale(const void* in, nvfp4_in_dtype dtype, int64_t rows, int64_t cols,
+                                int64_t in_ld_elems, float* g_out, nvfp4_stream_t stream) {
+  CHECK_ARG(in && g_out, "nvfp4_global_scale: null pointer");
+  CHECK_ARG(dtype == NVFP4_IN_BF16 || dtype == NVFP4_IN_F32, "nvfp4_global_scale: bad dtype %d", (int)dtype);
+  CHECK_ARG(rows > 0 && cols > 0, "nvfp4_global_scale: rows and cols must be positive");
+  CHECK_SUP(cols % 8 == 0, "nvfp4_global_scale: cols=%lld is not a multiple of 8", (long long)cols);
+  CHECK_ARG(in_ld_elems >= cols, "nvfp4_global_scale: in_ld_elems=%lld < cols", (long long)in_ld_elems);
+  const int64_t esize = dtype == NVFP4_IN_BF16 ? 2 : 4;
+  CHECK_AL(al16(in) && (in_ld_elems * esize) % 16 == 0, "nvfp4_global_scale: input not 16-byte aligned");
+  CHECK_AL(al4(g_out), "nvfp4_global_scale: g_out not 4-byte aligned");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail_cuda(e, "nvfp4_global_scale: device query");
+  e = global_scale_launch(in, dtype, rows, cols, in_ld_elems, g_out, sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_global_scale");
 }
 
 nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_sf_cols, int64_t stride_mn,
@@ -135,7 +155,8 @@ nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_s
 nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t T, int32_t H, int32_t E,
                                int32_t top_k, int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
                                int32_t* expert_offsets, int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                               uint8_t* a1_sf, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+                               uint8_t* a1_sf, const float* x_global_scale, void* workspace, size_t workspace_bytes,
+                               nvfp4_stream_t stream) {
   CHECK_ARG(T >= 0, "moe_route_permute: T=%d", T);
   CHECK_ARG(expert_counts && expert_offsets && workspace, "moe_route_permute: null pointer");
   CHECK_ARG(T == 0 || (logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_q && a1_sf),
@@ -145,6 +166,7 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
   CHECK_SUP(H > 0 && H % 64 == 0, "moe_route_permute: H=%d is not a positive multiple of 64", H);
   CHECK_AL(al16(workspace) && (T == 0 || (al16(x_bf16) && al16(a1_q) && al16(a1_sf))),
            "moe_route_permute: x, a1_q, a1_sf and workspace must be 16-byte aligned");
+  CHECK_AL(al4(x_global_scale), "moe_route_permute: x_global_scale not 4-byte aligned");
   const size_t need = moe_route_permute_workspace(T, H, E, top_k);
   CHECK_ARG(workspace_bytes >= need, "moe_route_permute: workspace %zu < %zu bytes", workspace_bytes, need);
   RouteBuffers b;
@@ -162,6 +184,7 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
   b.inv_perm = inv_perm;
   b.a1_q = a1_q;
   b.a1_sf = a1_sf;
+  b.x_gscale = x_global_scale;
   b.rows_max = moe_padded_rows_max(T, E, top_k);
   route_carve_workspace(b, workspace);
   cudaError_t e = route_permute_launch(b, reinterpret_cast<cudaStream_t>(stream));
@@ -171,8 +194,9 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
 nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,
                                 const int32_t* group_offsets, const int32_t* group_counts, int32_t G, int32_t N,
                                 int32_t K, const uint8_t* b_q, const uint8_t* b_sf, float alpha,
-                                nvfp4_epilogue epilogue, uint8_t* out_q, uint8_t* out_sf, void* out_bf16,
-                                float* h_debug, nvfp4_stream_t stream) {
+                                const float* a_global_scale, const float* b_global_scale,
+                                const float* out_global_scale, nvfp4_epilogue epilogue, uint8_t* out_q,
+                                uint8_t* out_sf, void* out_bf16, float* h_debug, nvfp4_stream_t stream) {
   CHECK_ARG(a_q && a_sf && b_q && b_sf, "nvfp4_grouped_gemm: null operand");
   CHECK_ARG(epilogue == NVFP4_EPI_SWIGLU_NVFP4 || epilogue == NVFP4_EPI_BF16, "nvfp4_grouped_gemm: bad epilogue");
   CHECK_ARG(epilogue != NVFP4_EPI_SWIGLU_NVFP4 || (out_q && out_sf), "nvfp4_grouped_gemm: null NVFP4 output");
@@ -190,6 +214,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
   CHECK_AL((!out_q || al16(out_q)) && (!out_sf || al16(out_sf)) && (!out_bf16 || al16(out_bf16)) &&
                (!h_debug || al16(h_debug)),
            "nvfp4_grouped_gemm: outputs not 16-byte aligned");
+  CHECK_AL(al4(a_global_scale) && al4(b_global_scale) && al4(out_global_scale),
+           "nvfp4_grouped_gemm: global scales not 4-byte aligned");
   GemmArgs a;
   a.a_q = a_q;
   a.a_sf = a_sf;
@@ -202,6 +228,9 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
   a.b_q = b_q;
   a.b_sf = b_sf;
   a.alpha = alpha;
+  a.a_gscale = a_global_scale;
+  a.b_gscale = b_global_scale;
+  a.out_gscale = out_global_scale;
   a.epilogue = epilogue;
   a.out_q = out_q;
   a.out_sf = out_sf;
@@ -213,18 +242,21 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
 nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf, const int32_t* expert_offsets,
                                    const int32_t* expert_counts, int32_t E, int32_t H, int32_t I, int64_t rows_max,
                                    const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
-                                   const uint8_t* w2_sf, float alpha1, float alpha2, uint8_t* a2_q, uint8_t* a2_sf,
-                                   void* rows_out_bf16, float* h_debug, nvfp4_stream_t stream) {
+                                   const uint8_t* w2_sf, float alpha1, float alpha2, const float* x_global_scale,
+                                   const float* w1_global_scale, const float* a2_global_scale,
+                                   const float* w2_global_scale, uint8_t* a2_q, uint8_t* a2_sf, void* rows_out_bf16,
+                                   float* h_debug, nvfp4_stream_t stream) {
   CHECK_ARG(expert_offsets && expert_counts, "nvfp4_moe_ffn_forward: null expert offsets/counts");
   CHECK_ARG(a2_q && a2_sf && rows_out_bf16, "nvfp4_moe_ffn_forward: null output");
   CHECK_SUP(H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0,
             "nvfp4_moe_ffn_forward: H=%d and I=%d must be positive multiples of 256", H, I);
   nvfp4_status st = nvfp4_grouped_gemm(a1_q, a1_sf, rows_max, expert_offsets, expert_counts, E, 2 * I, H, w1_q,
-                                       w1_sf, alpha1, NVFP4_EPI_SWIGLU_NVFP4, a2_q, a2_sf, nullptr, h_debug,
-                                       stream);
+                                       w1_sf, alpha1, x_global_scale, w1_global_scale, a2_global_scale,
+                                       NVFP4_EPI_SWIGLU_NVFP4, a2_q, a2_sf, nullptr, h_debug, stream);
   if (st != NVFP4_OK) return st;
   return nvfp4_grouped_gemm(a2_q, a2_sf, rows_max, expert_offsets, expert_counts, E, H, I, w2_q, w2_sf, alpha2,
-                            NVFP4_EPI_BF16, nullptr, nullptr, rows_out_bf16, nullptr, stream);
+                            a2_global_scale, w2_global_scale, nullptr, NVFP4_EPI_BF16, nullptr, nullptr,
+                            rows_out_bf16, nullptr, stream);
 }
 
 nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w, int32_t T,

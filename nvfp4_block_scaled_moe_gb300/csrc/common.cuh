@@ -109,6 +109,16 @@ __device__ __forceinline__ float signed_halfstep(float x, const BlockScale& s) {
   return rintf(q) * 0.5f;
 }
 
+// alpha of group g under the two-level encode scales of A (scalar) and B (per
+// group): alpha / (ga * gb[g]) as one IEEE quotient; alpha itself when neither
+// scale is given.
+__device__ __forceinline__ float group_alpha(float alpha, const float* ga, const float* gb, int g) {
+  if (ga == nullptr && gb == nullptr) return alpha;
+  const float a = ga != nullptr ? __ldg(ga) : 1.0f;
+  const float b = gb != nullptr ? __ldg(gb + g) : 1.0f;
+  return __fdiv_rn(alpha, a * b);
+}
+
 // Quantise eight values of one half-block with that block's scale.
 __device__ __forceinline__ uint32_t quantize8(const float (&h)[8], const BlockScale& s) {
   float v[8];

@@ -89,6 +89,9 @@ struct Params {
   int64_t rows_max;
   int64_t sfb_group_bytes;
   float alpha;
+  const float* a_gs;          // two-level encode scales (null = 1): A, B per group, SwiGLU output
+  const float* b_gs;
+  const float* out_gs;
   uint8_t* out_q;
   uint8_t* out_sf;
   __nv_bfloat16* out_bf16;
@@ -106,10 +109,12 @@ __device__ __forceinline__ int find_group(const int32_t* off, int G, int64_t row
 }
 
 // L1 epilogue for one thread's row: 128 interleaved gate/up accumulator columns
-// (4 chunks of g(8) u(8) g(8) u(8)) -> 64 SwiGLU outputs -> 4 NVFP4 blocks.
-__device__ __forceinline__ void epilogue_swiglu(const float (&v)[4][32], float alpha, bool valid, int64_t grow,
-                                                int64_t col0, int32_t out_cols, uint32_t k4, uint32_t k4_total,
-                                                uint8_t* out_q, uint8_t* out_sf, float* h_debug) {
+// (4 chunks of g(8) u(8) g(8) u(8)) -> 64 SwiGLU outputs -> 4 NVFP4 blocks (of
+// fp32(h * g_out) under a two-level encode scale; h_debug keeps h).
+__device__ __forceinline__ void epilogue_swiglu(const float (&v)[4][32], float alpha, const float* out_gs,
+                                                bool valid, int64_t grow, int64_t col0, int32_t out_cols,
+                                                uint32_t k4, uint32_t k4_total, uint8_t* out_q, uint8_t* out_sf,
+                                                float* h_debug) {
   uint32_t sf_word = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -119,23 +124,29 @@ __device__ __forceinline__ void epilogue_swiglu(const float (&v)[4][32], float a
       h0[i] = swiglu(alpha * v[c][i], alpha * v[c][8 + i]);
       h1[i] = swiglu(alpha * v[c][16 + i], alpha * v[c][24 + i]);
     }
+    const int64_t col = col0 + 16 * c;
+    if (valid && h_debug != nullptr) {
+      float4* hp = reinterpret_cast<float4*>(h_debug + grow * out_cols + col);
+      hp[0] = make_float4(h0[0], h0[1], h0[2], h0[3]);
+      hp[1] = make_float4(h0[4], h0[5], h0[6], h0[7]);
+      hp[2] = make_float4(h1[0], h1[1], h1[2], h1[3]);
+      hp[3] = make_float4(h1[4], h1[5], h1[6], h1[7]);
+    }
+    if (out_gs != nullptr) {
+      const float g = __ldg(out_gs);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        h0[i] *= g;
+        h1[i] *= g;
+      }
+    }
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(h0[i]), fabsf(h1[i])));
     const BlockScale s = block_scale(amax);
     const uint32_t lo = quantize8(h0, s), hi = quantize8(h1, s);
     sf_word |= s.code << (8 * c);
-    if (valid) {
-      const int64_t col = col0 + 16 * c;
-      *reinterpret_cast<uint2*>(out_q + grow * (out_cols / 2) + col / 2) = make_uint2(lo, hi);
-      if (h_debug != nullptr) {
-        float4* hp = reinterpret_cast<float4*>(h_debug + grow * out_cols + col);
-        hp[0] = make_float4(h0[0], h0[1], h0[2], h0[3]);
-        hp[1] = make_float4(h0[4], h0[5], h0[6], h0[7]);
-        hp[2] = make_float4(h1[0], h1[1], h1[2], h1[3]);
-        hp[3] = make_float4(h1[4], h1[5], h1[6], h1[7]);
-      }
-    }
+    if (valid) *reinterpret_cast<uint2*>(out_q + grow * (out_cols / 2) + col / 2) = make_uint2(lo, hi);
   }
   if (valid) *reinterpret_cast<uint32_t*>(out_sf + sf_word_offset(grow, k4, k4_total)) = sf_word;
 }
@@ -334,12 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
       if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+      const float alpha = group_alpha(p.alpha, p.a_gs, p.b_gs, g);
       if constexpr (kEpi == NVFP4_EPI_SWIGLU_NVFP4) {
-        epilogue_swiglu(v, p.alpha, valid, grow, static_cast<int64_t>(nt) * (kBN / 2) + half * 64, p.N / 2,
+        epilogue_swiglu(v, alpha, p.out_gs, valid, grow, static_cast<int64_t>(nt) * (kBN / 2) + half * 64, p.N / 2,
                         2 * nt + half, static_cast<uint32_t>(p.N / 128), p.out_q, p.out_sf, p.h_debug);
       } else {
         if (valid)
-          epilogue_bf16<C::kChunks>(v, p.alpha,
+          epilogue_bf16<C::kChunks>(v, alpha,
                                     p.out_bf16 + grow * p.N + static_cast<int64_t>(nt) * kBN + half * (kBN / 2));
       }
     }
@@ -464,6 +476,9 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   p.rows_max = a.rows_max;
   p.sfb_group_bytes = static_cast<int64_t>(a.N / 128) * (a.K / 64) * 512;
   p.alpha = a.alpha;
+  p.a_gs = a.a_gscale;
+  p.b_gs = a.b_gscale;
+  p.out_gs = a.out_gscale;
   p.out_q = a.out_q;
   p.out_sf = a.out_sf;
   p.out_bf16 = static_cast<__nv_bfloat16*>(a.out_bf16);

@@ -85,6 +85,9 @@ struct PairParams {
   int64_t rows_max;
   int64_t sfb_group_bytes;
   float alpha;
+  const float* a_gs;          // two-level encode scales (null = 1): A, B per group, SwiGLU output
+  const float* b_gs;
+  const float* out_gs;
   uint8_t* out_q;
   uint8_t* out_sf;
   __nv_bfloat16* out_bf16;
@@ -137,13 +140,6 @@ __device__ __forceinline__ void swiglu_row(const float (&v)[4][32], float alpha,
       h0[i] = swiglu(alpha * v[c][i], alpha * v[c][8 + i]);
       h1[i] = swiglu(alpha * v[c][16 + i], alpha * v[c][24 + i]);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(h0[i]), fabsf(h1[i])));
-    const BlockScale s = block_scale(amax);
-    w[2 * c] = quantize8(h0, s);
-    w[2 * c + 1] = quantize8(h1, s);
-    sf_word |= s.code << (8 * c);
     if (valid && p.h_debug != nullptr) {
       float4* hp = reinterpret_cast<float4*>(p.h_debug + grow * out_cols + col0 + 16 * c);
       hp[0] = make_float4(h0[0], h0[1], h0[2], h0[3]);
@@ -151,6 +147,21 @@ __device__ __forceinline__ void swiglu_row(const float (&v)[4][32], float alpha,
       hp[2] = make_float4(h1[0], h1[1], h1[2], h1[3]);
       hp[3] = make_float4(h1[4], h1[5], h1[6], h1[7]);
     }
+    if (p.out_gs != nullptr) {                // two-level scale: quantise fp32(h * g)
+      const float g = __ldg(p.out_gs);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        h0[i] *= g;
+        h1[i] *= g;
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(h0[i]), fabsf(h1[i])));
+    const BlockScale s = block_scale(amax);
+    w[2 * c] = quantize8(h0, s);
+    w[2 * c + 1] = quantize8(h1, s);
+    sf_word |= s.code << (8 * c);
   }
   if (direct) {
     if (valid) {
@@ -388,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc_phase ^= 1u;
 
       // whole 32-row slices leave by TMA store; a slice with missing rows stores row by row
+      const float alpha = group_alpha(p.alpha, p.a_gs, p.b_gs, t.g);
       const bool staged = __all_sync(0xFFFFFFFFu, valid);
       if (C::kSwiglu && staged) {
         if (lane == 0 && stores_pending) bulk_wait_read_all();
@@ -395,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int32_t y = static_cast<int32_t>(t.block * kBM + quad * 32);
       if constexpr (C::kSwiglu) {
-        swiglu_row(v, p.alpha, valid, !staged, grow, static_cast<int64_t>(t.nt) * (kBN / 2) + half * 64, p.N / 2,
+        swiglu_row(v, alpha, valid, !staged, grow, static_cast<int64_t>(t.nt) * (kBN / 2) + half * 64, p.N / 2,
                    2 * t.nt + half, static_cast<uint32_t>(p.N / 128), stage_buf + lane * 32, p);
         if (staged) {
           fence_async_smem();
@@ -421,10 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 8; ++q) {
               const float* f = &v[2 * box + (q >> 2)][8 * (q & 3)];
               uint4 o;
-              o.x = pack_bf16x2(p.alpha * f[0], p.alpha * f[1]);
-              o.y = pack_bf16x2(p.alpha * f[2], p.alpha * f[3]);
-              o.z = pack_bf16x2(p.alpha * f[4], p.alpha * f[5]);
-              o.w = pack_bf16x2(p.alpha * f[6], p.alpha * f[7]);
+              o.x = pack_bf16x2(alpha * f[0], alpha * f[1]);
+              o.y = pack_bf16x2(alpha * f[2], alpha * f[3]);
+              o.z = pack_bf16x2(alpha * f[4], alpha * f[5]);
+              o.w = pack_bf16x2(alpha * f[6], alpha * f[7]);
               *reinterpret_cast<uint4*>(my_row + ((q ^ (lane & 7)) << 4)) = o;
             }
             __syncwarp();
@@ -448,10 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 o;
-              o.x = pack_bf16x2(p.alpha * v[c][8 * q + 0], p.alpha * v[c][8 * q + 1]);
-              o.y = pack_bf16x2(p.alpha * v[c][8 * q + 2], p.alpha * v[c][8 * q + 3]);
-              o.z = pack_bf16x2(p.alpha * v[c][8 * q + 4], p.alpha * v[c][8 * q + 5]);
-              o.w = pack_bf16x2(p.alpha * v[c][8 * q + 6], p.alpha * v[c][8 * q + 7]);
+              o.x = pack_bf16x2(alpha * v[c][8 * q + 0], alpha * v[c][8 * q + 1]);
+              o.y = pack_bf16x2(alpha * v[c][8 * q + 2], alpha * v[c][8 * q + 3]);
+              o.z = pack_bf16x2(alpha * v[c][8 * q + 4], alpha * v[c][8 * q + 5]);
+              o.w = pack_bf16x2(alpha * v[c][8 * q + 6], alpha * v[c][8 * q + 7]);
               dst[4 * c + q] = o;
             }
           }
@@ -564,6 +576,9 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   p.rows_max = a.rows_max;
   p.sfb_group_bytes = static_cast<int64_t>(a.N / 128) * (a.K / 64) * 512;
   p.alpha = a.alpha;
+  p.a_gs = a.a_gscale;
+  p.b_gs = a.b_gscale;
+  p.out_gs = a.out_gscale;
   p.out_q = a.out_q;
   p.out_sf = a.out_sf;
   p.out_bf16 = static_cast<__nv_bfloat16*>(a.out_bf16);

@@ -13,7 +13,12 @@ namespace nvfp4 {
 unsigned* device_error_word();
 
 cudaError_t quantize_launch(const void* in, int dtype, int mode, int64_t rows, int64_t cols, int64_t ld,
-                            uint8_t* q, uint8_t* sf, int sf_linear, float* h_dbg, cudaStream_t stream);
+                            uint8_t* q, uint8_t* sf, int sf_linear, const float* gscale, float* h_dbg,
+                            cudaStream_t stream);
+
+// g_out = 2688 / amax over the matrix (1 for an all-zero one); cols % 8 == 0.
+cudaError_t global_scale_launch(const void* in, int dtype, int64_t rows, int64_t cols, int64_t ld, float* g_out,
+                                int sms, cudaStream_t stream);
 
 cudaError_t sf_swizzle_launch(const uint8_t* in, int64_t mn_rows, int64_t k_sf, int64_t s_mn, int64_t s_k,
                               uint8_t* out, int inverse, cudaStream_t stream);
@@ -30,6 +35,7 @@ struct RouteBuffers {
   int32_t* inv_perm;
   uint8_t* a1_q;
   uint8_t* a1_sf;
+  const float* x_gscale;   // two-level encode scale of x (device scalar) or null
   int64_t rows_max;
   int32_t* chunk_hist;   // workspace: [n_chunks, E] expert counts per token chunk
 };
@@ -55,6 +61,9 @@ struct GemmArgs {
   const uint8_t* b_q;
   const uint8_t* b_sf;
   float alpha;
+  const float* a_gscale;   // two-level encode scales (device): A's scalar, B's per group,
+  const float* b_gscale;   // and the SwiGLU output's scalar; null = 1
+  const float* out_gscale;
   int epilogue;
   uint8_t* out_q;
   uint8_t* out_sf;

@@ -10,6 +10,11 @@
 // Layout of the quantiser's work: one thread owns one 16-block (32 bytes of BF16,
 // 64 of fp32 or gate+up), a lane quad owns one 64-column group, whose four scale
 // bytes form one 32-bit word of the swizzled layout.
+//
+// Two-level scale ("NVFP4 MoE Pipeline": stage_activation returns an
+// input_global_scale next to the per-16 scales): with an encode scale g the
+// quantised values are fp32(v * g); nvfp4_global_scale computes g = 2688 / amax
+// (6 x 448, the top of the E2M1 x E4M3 range) in two launches.
 #include "common.cuh"
 #include "internal.h"
 
@@ -60,11 +65,12 @@ __device__ __forceinline__ void load_block(const void* in, int64_t row, int64_t 
 // block) + warp the segment.  Lanes 4w .. 4w+3 own one 64-column group, whose four scale bytes form
 // one 32-bit word of the swizzled layout.  sf_linear selects a plain row-major
 // SF output ([rows, cols/16]; requires cols % 64 == 0).
-template <int kMode, int kDtype>
+template <int kMode, int kDtype, bool kScaled>
 __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ in, int64_t rows,
                                                        int64_t cols, int64_t ld, int64_t rows_pad,
                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                       int sf_linear, float* __restrict__ h_dbg) {
+                                                       int sf_linear, const float* __restrict__ gscale,
+                                                       float* __restrict__ h_dbg) {
   const int lane = threadIdx.x & 31;
   const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (seg * 512 >= cols) return;
@@ -76,6 +82,16 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   float h[16];
   if (active) {
     load_block<kMode, kDtype>(in, row, ld, c0, h);
+    if (h_dbg != nullptr) {
+      float4* hp = reinterpret_cast<float4*>(h_dbg + row * cols + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hp[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    }
+    if (kScaled) {
+      const float g = __ldg(gscale);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] *= g;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) h[i] = 0.0f;
@@ -93,11 +109,6 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
       hi[i] = h[8 + i];
     }
     *reinterpret_cast<uint2*>(q + row * (cols / 2) + c0 / 2) = make_uint2(quantize8(lo, s), quantize8(hi, s));
-    if (h_dbg != nullptr) {
-      float4* hp = reinterpret_cast<float4*>(h_dbg + row * cols + c0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) hp[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-    }
   }
 
   // gather the quad's four scale bytes (lanes 4w .. 4w+3) into one word at lane 4w
@@ -119,27 +130,120 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
 template <int kMode, int kDtype>
 static cudaError_t launch_quantize(const void* in, int64_t rows, int64_t cols, int64_t ld,
                                    int64_t rows_pad, uint8_t* q, uint8_t* sf, int sf_linear,
-                                   float* h_dbg, cudaStream_t stream) {
+                                   const float* gscale, float* h_dbg, cudaStream_t stream) {
   const int64_t segs = (cols + 511) / 512;
   if (rows_pad == 0) return cudaSuccess;
   const int warps = static_cast<int>(segs < 8 ? segs : 8);      // no idle warps on short rows
   const dim3 grid(static_cast<unsigned>(rows_pad), static_cast<unsigned>((segs + warps - 1) / warps));
-  quantize_kernel<kMode, kDtype><<<grid, 32 * warps, 0, stream>>>(in, rows, cols, ld, rows_pad, q, sf, sf_linear,
-                                                                  h_dbg);
+  if (gscale != nullptr)
+    quantize_kernel<kMode, kDtype, true><<<grid, 32 * warps, 0, stream>>>(in, rows, cols, ld, rows_pad, q, sf,
+                                                                          sf_linear, gscale, h_dbg);
+  else
+    quantize_kernel<kMode, kDtype, false><<<grid, 32 * warps, 0, stream>>>(in, rows, cols, ld, rows_pad, q, sf,
+                                                                           sf_linear, nullptr, h_dbg);
   return cudaGetLastError();
 }
 
 cudaError_t quantize_launch(const void* in, int dtype, int mode, int64_t rows, int64_t cols, int64_t ld,
-                            uint8_t* q, uint8_t* sf, int sf_linear, float* h_dbg, cudaStream_t stream) {
+                            uint8_t* q, uint8_t* sf, int sf_linear, const float* gscale, float* h_dbg,
+                            cudaStream_t stream) {
   const int64_t rows_pad = sf_linear ? rows : ((rows + 127) / 128) * 128;
   if (mode == NVFP4_MODE_SWIGLU_GU8)
     return launch_quantize<NVFP4_MODE_SWIGLU_GU8, NVFP4_IN_BF16>(in, rows, cols, ld, rows_pad, q, sf,
-                                                                 sf_linear, h_dbg, stream);
+                                                                 sf_linear, gscale, h_dbg, stream);
   if (dtype == NVFP4_IN_BF16)
     return launch_quantize<NVFP4_MODE_PLAIN, NVFP4_IN_BF16>(in, rows, cols, ld, rows_pad, q, sf, sf_linear,
-                                                            h_dbg, stream);
+                                                            gscale, h_dbg, stream);
   return launch_quantize<NVFP4_MODE_PLAIN, NVFP4_IN_F32>(in, rows, cols, ld, rows_pad, q, sf, sf_linear,
-                                                         h_dbg, stream);
+                                                         gscale, h_dbg, stream);
+}
+
+// ---------------------------------------------------------- global scale --
+// amax over a rows x cols matrix (row stride ld): grid-stride over 8-value
+// chunks, four independent 16-byte loads in flight per thread per step, a block
+// max, one atomicMax on the float bits (non-negative floats order like their
+// bit patterns) into *out, which the launcher zeroed.
+template <int kDtype, bool kContig>
+__device__ __forceinline__ float chunk_amax(const void* in, int64_t i, int64_t chunks_per_row, int64_t ld) {
+  // contiguous rows (ld == cols): chunk i starts at element 8i, no division
+  const int64_t r = kContig ? 0 : i / chunks_per_row;
+  const int64_t c = kContig ? 8 * i : (i - r * chunks_per_row) * 8;
+  float v[8];
+  if (kDtype == NVFP4_IN_BF16) {
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + r * ld + c)), v);
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(in) + r * ld + c);
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+  return m;
+}
+
+template <int kDtype, bool kContig>
+__global__ void __launch_bounds__(256) tensor_amax_kernel(const void* __restrict__ in, int64_t rows, int64_t cols,
+                                                          int64_t ld, unsigned* __restrict__ out) {
+  const int64_t chunks_per_row = cols / 8;
+  const int64_t n = rows * chunks_per_row;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  float m = 0.0f;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n; i += 4 * stride) {
+    const float m0 = chunk_amax<kDtype, kContig>(in, i, chunks_per_row, ld);
+    const float m1 = chunk_amax<kDtype, kContig>(in, i + stride, chunks_per_row, ld);
+    const float m2 = chunk_amax<kDtype, kContig>(in, i + 2 * stride, chunks_per_row, ld);
+    const float m3 = chunk_amax<kDtype, kContig>(in, i + 3 * stride, chunks_per_row, ld);
+    m = fmaxf(m, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+  }
+  for (; i < n; i += stride) m = fmaxf(m, chunk_amax<kDtype, kContig>(in, i, chunks_per_row, ld));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  __shared__ float warp_max[8];
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = 0.0f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) b = fmaxf(b, warp_max[w]);
+    atomicMax(out, __float_as_uint(b));
+  }
+}
+
+// *g = 2688 / amax (IEEE quotient), or 1 when amax is 0 or the quotient is not finite.
+__global__ void global_scale_finalize_kernel(float* g) {
+  const float amax = __uint_as_float(*reinterpret_cast<const unsigned*>(g));
+  float v = amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
+  if (!isfinite(v)) v = 1.0f;
+  *g = v;
+}
+
+cudaError_t global_scale_launch(const void* in, int dtype, int64_t rows, int64_t cols, int64_t ld, float* g_out,
+                                int sms, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(g_out, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int64_t n = rows * (cols / 8);
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  unsigned* acc = reinterpret_cast<unsigned*>(g_out);
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (ld == cols) {
+    if (dtype == NVFP4_IN_BF16)
+      tensor_amax_kernel<NVFP4_IN_BF16, true><<<grid, 256, 0, stream>>>(in, rows, cols, ld, acc);
+    else
+      tensor_amax_kernel<NVFP4_IN_F32, true><<<grid, 256, 0, stream>>>(in, rows, cols, ld, acc);
+  } else {
+    if (dtype == NVFP4_IN_BF16)
+      tensor_amax_kernel<NVFP4_IN_BF16, false><<<grid, 256, 0, stream>>>(in, rows, cols, ld, acc);
+    else
+      tensor_amax_kernel<NVFP4_IN_F32, false><<<grid, 256, 0, stream>>>(in, rows, cols, ld, acc);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  global_scale_finalize_kernel<<<1, 1, 0, stream>>>(g_out);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ SF swizzle --

@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(128) route_assign_kernel(const int32_t* __rest
 // is either wholly inside the row or wholly past its end.
 __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int32_t H,
                                                             int32_t k, const int32_t* __restrict__ inv_perm,
+                                                            const float* __restrict__ gscale,
                                                             uint8_t* __restrict__ a_q,
                                                             uint8_t* __restrict__ a_sf) {
   const int lane = threadIdx.x & 31;
@@ -249,6 +250,14 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
       float lo[8], hi[8];
       bf16x8_to_f32(raw[2 * b], lo);
       bf16x8_to_f32(raw[2 * b + 1], hi);
+      if (gscale != nullptr) {               // two-level scale: quantise fp32(x * g)
+        const float g = __ldg(gscale);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          lo[i] *= g;
+          hi[i] *= g;
+        }
+      }
       float amax = 0.0f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
@@ -320,7 +329,7 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
     const int warps = static_cast<int>(segs < 8 ? segs : 8);     // no idle warps on short rows
     const dim3 grid(static_cast<unsigned>(b.T), static_cast<unsigned>((segs + warps - 1) / warps));
     route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k,
-                                                          b.inv_perm, b.a1_q, b.a1_sf);
+                                                          b.inv_perm, b.x_gscale, b.a1_q, b.a1_sf);
   }
   return cudaGetLastError();
 }

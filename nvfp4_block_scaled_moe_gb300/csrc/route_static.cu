@@ -61,7 +61,8 @@ extern "C" nvfp4_status moe_route_permute_static(const float* logits, const void
                                                   int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
                                                   int32_t* expert_counts, int32_t* expert_offsets,
                                                   int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                                                  uint8_t* a1_sf, nvfp4_stream_t stream) {
+                                                  uint8_t* a1_sf, const float* x_global_scale,
+                                                  nvfp4_stream_t stream) {
   if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: T=%d", T);
   if (!expert_counts || !expert_offsets)
     return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: null pointer");
@@ -76,6 +77,8 @@ extern "C" nvfp4_status moe_route_permute_static(const float* logits, const void
                         reinterpret_cast<uintptr_t>(a1_sf);
   if (T > 0 && (mis & 15u) != 0)
     return fail(NVFP4_ERR_ALIGNMENT, "moe_route_permute_static: x, a1_q and a1_sf must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(x_global_scale) & 3u) != 0)
+    return fail(NVFP4_ERR_ALIGNMENT, "moe_route_permute_static: x_global_scale not 4-byte aligned");
   const size_t need = moe_route_permute_workspace(T, H, E, top_k);
   if (need > kStaticScratchBytes)
     return fail(NVFP4_ERR_UNSUPPORTED,
@@ -101,6 +104,7 @@ extern "C" nvfp4_status moe_route_permute_static(const float* logits, const void
   b.inv_perm = inv_perm;
   b.a1_q = a1_q;
   b.a1_sf = a1_sf;
+  b.x_gscale = x_global_scale;
   b.rows_max = moe_padded_rows_max(T, E, top_k);
   route_carve_workspace(b, ws);
   cudaError_t e = route_permute_launch(b, reinterpret_cast<cudaStream_t>(stream));

@@ -2,6 +2,14 @@
 
 Plumbing only: PyTorch allocates device memory; every step is one call into
 libnvfp4moe.so (route + permute + stage, L1/SwiGLU/requant/L2, combine).
+
+Two-level scale (optional): the pages' pipeline carries per-tensor global scales
+("NVFP4 MoE Pipeline": stage_activation returns an input_global_scale; alpha =
+igs * global_sf).  Here every tensor gets a device fp32 encode scale g (see
+include/nvfp4moe.h): the weights one per expert, computed from their fp32 values
+when they are quantised; x one per forward, computed on the device before the
+routing call; the L1 output one calibrated ahead (``calibrate_a2_scale``), since
+the fused epilogue quantises each tile before the tensor's amax exists.
 """
 from __future__ import annotations
 
@@ -10,7 +18,8 @@ from dataclasses import dataclass
 import torch
 
 from . import (MODE_PLAIN, moe_combine, moe_padded_rows_max, moe_route_permute,
-               moe_route_permute_workspace, nvfp4_moe_ffn_forward, nvfp4_quantize, sf_bytes)
+               moe_route_permute_workspace, nvfp4_global_scale, nvfp4_moe_ffn_forward, nvfp4_quantize,
+               sf_bytes)
 
 
 @dataclass
@@ -48,28 +57,40 @@ class MoeBuffers:
         self.y = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=device)
         self.workspace = torch.empty(moe_route_permute_workspace(s.T, s.H, s.E, s.top_k), dtype=u8, device=device)
         self.h_debug = None
+        self.x_gs = torch.ones(1, dtype=f32, device=device)       # x's encode scale (two-level forwards)
+        self.a2_gs = None                                         # L1 output's encode scale, once calibrated
 
     def enable_h_debug(self):
-        self.h_debug = torch.empty((self.rows_max, self.shape.I), dtype=torch.float32, device=self.a2_q.device)
+        # zeros: the GEMM writes h only for real rows
+        self.h_debug = torch.zeros((self.rows_max, self.shape.I), dtype=torch.float32, device=self.a2_q.device)
 
 
 class MoeWeights:
     """Expert weights in NVFP4: W1 [E, 2I, H] (rows interleaved 8|8) and W2 [E, H, I],
     each expert's SF swizzled for its own N x K matrix."""
 
-    def __init__(self, s: MoeShape, device="cuda"):
+    def __init__(self, s: MoeShape, device="cuda", two_level: bool = False):
         u8 = torch.uint8
         self.shape = s
         self.w1_q = torch.empty((s.E, 2 * s.I, s.H // 2), dtype=u8, device=device)
         self.w1_sf = torch.empty((s.E, sf_bytes(2 * s.I, s.H)), dtype=u8, device=device)
         self.w2_q = torch.empty((s.E, s.H, s.I // 2), dtype=u8, device=device)
         self.w2_sf = torch.empty((s.E, sf_bytes(s.H, s.I)), dtype=u8, device=device)
+        # per-expert encode scales of the two-level scheme (None: one level)
+        self.w1_gs = torch.ones(s.E, dtype=torch.float32, device=device) if two_level else None
+        self.w2_gs = torch.ones(s.E, dtype=torch.float32, device=device) if two_level else None
 
     def set_expert(self, e: int, w1_f32: torch.Tensor, w2_f32: torch.Tensor):
-        """Quantise one expert's fp32 weights (CUDA tensors) with the library's quantiser."""
+        """Quantise one expert's fp32 weights (CUDA tensors) with the library's quantiser
+        (two-level: under encode scales computed from those weights on the device)."""
         s = self.shape
-        nvfp4_quantize(w1_f32, s.H, MODE_PLAIN, self.w1_q[e], self.w1_sf[e])
-        nvfp4_quantize(w2_f32, s.I, MODE_PLAIN, self.w2_q[e], self.w2_sf[e])
+        g1 = g2 = None
+        if self.w1_gs is not None:
+            g1, g2 = self.w1_gs[e:e + 1], self.w2_gs[e:e + 1]
+            nvfp4_global_scale(w1_f32, g1)
+            nvfp4_global_scale(w2_f32, g2)
+        nvfp4_quantize(w1_f32, s.H, MODE_PLAIN, self.w1_q[e], self.w1_sf[e], global_scale=g1)
+        nvfp4_quantize(w2_f32, s.I, MODE_PLAIN, self.w2_q[e], self.w2_sf[e], global_scale=g2)
 
     def set_from_pool(self, pool: torch.Tensor, w1_off, w2_off, std: float):
         """Quantise every expert from windows of a device fp32 pool: expert e's W1 is
@@ -85,13 +106,39 @@ class MoeWeights:
 
 
 def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
-                alpha1: float = 1.0, alpha2: float = 1.0) -> torch.Tensor:
-    """y = MoE-FFN(x): route + permute + stage, L1 + SwiGLU + requant + L2, combine."""
+                alpha1: float = 1.0, alpha2: float = 1.0, two_level: bool = False) -> torch.Tensor:
+    """y = MoE-FFN(x): route + permute + stage, L1 + SwiGLU + requant + L2, combine.
+    two_level: x's encode scale is computed here, the weights' are those of ``w``
+    (built with two_level=True) and the L1 output's is ``b.a2_gs`` (None: 1)."""
     s = b.shape
+    x_gs = None
+    if two_level:
+        if w.w1_gs is None:
+            raise ValueError("two-level forward needs weights quantised with two_level=True")
+        if s.T > 0:
+            nvfp4_global_scale(x, b.x_gs)
+        x_gs = b.x_gs
     moe_route_permute(logits, x, s.top_k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
-                      b.inv_perm, b.a1_q, b.a1_sf, b.workspace)
+                      b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_global_scale=x_gs)
     if s.T > 0:
         nvfp4_moe_ffn_forward(b.a1_q, b.a1_sf, b.offsets, b.counts, s.E, s.H, s.I, b.rows_max, w.w1_q, w.w1_sf,
-                              w.w2_q, w.w2_sf, alpha1, alpha2, b.a2_q, b.a2_sf, b.rows_out, b.h_debug)
+                              w.w2_q, w.w2_sf, alpha1, alpha2, b.a2_q, b.a2_sf, b.rows_out, b.h_debug,
+                              x_global_scale=x_gs, w1_global_scale=w.w1_gs if two_level else None,
+                              a2_global_scale=b.a2_gs if two_level else None,
+                              w2_global_scale=w.w2_gs if two_level else None)
         moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
     return b.y
+
+
+def calibrate_a2_scale(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
+                       alpha1: float = 1.0) -> torch.Tensor:
+    """Set b.a2_gs = 2688 / amax of the L1 output h of this batch (two-level): one
+    forward with the L1 output at scale 1 and h recorded, then a device reduction."""
+    saved_h, saved_gs = b.h_debug, b.a2_gs
+    b.enable_h_debug()
+    b.a2_gs = None
+    moe_forward(x, logits, w, b, alpha1=alpha1, two_level=True)
+    gs = torch.ones(1, dtype=torch.float32, device=b.y.device) if saved_gs is None else saved_gs
+    nvfp4_global_scale(b.h_debug, gs)
+    b.h_debug, b.a2_gs = saved_h, gs
+    return gs
