@@ -37,7 +37,7 @@ except ImportError:                     # pragma: no cover
     torch = None
 
 # stream ids
-_LOGITS, _X, _W1, _W2, _PLANT, _GU, _DENSE_A, _DENSE_B, _RAND_OP = range(9)
+_LOGITS, _X, _W1, _W2, _PLANT, _GU, _DENSE_A, _DENSE_B, _RAND_OP, _SHARED = range(10)
 
 CONFIGS = {
     "tiny": dict(kind="moe", T=128, H=512, I=256, E=8, top_k=2, seed=0, zipf=False),
@@ -140,6 +140,16 @@ def moe_w2(spec: dict, e: int) -> np.ndarray:
     pool, _, w2_off = moe_weight_pool(spec)
     n = spec["H"] * spec["I"]
     return (pool[w2_off[e]:w2_off[e] + n] * WEIGHT_STD).reshape(spec["H"], spec["I"])
+
+
+def moe_shared_weights(spec: dict, i_shared: int | None = None):
+    """A shared expert's fp32 weights (W1 [2*Is, H] interleaved 8|8 like the routed
+    experts, W2 [H, Is]), N(0, 0.02) on their own stream; Is defaults to I."""
+    i_s = spec["I"] if i_shared is None else i_shared
+    rng = _rng(spec["seed"], _SHARED)
+    w1 = rng.standard_normal((2 * i_s, spec["H"]), dtype=np.float32) * WEIGHT_STD
+    w2 = rng.standard_normal((spec["H"], i_s), dtype=np.float32) * WEIGHT_STD
+    return w1, w2
 
 
 def moe_all_weights(spec: dict):

@@ -24,6 +24,11 @@ Readings where the pages are silent:
 * the L1 output is quantised from fp32 h (never from a BF16-rounded h);
 * L2 rows and the combined output are BF16 (round-to-nearest-even); the
   combine sums the k slots in slot order.
+* shared expert (optional): a dense FFN of every token through the same NVFP4
+  steps (stage x per 16, L1 + SwiGLU + re-quantisation, L2 -> BF16 rows S); its
+  row is added after the k routed slots, before the one rounding:
+  y = bf16(sum_j w_j * O_j + S).  The pages' checkpoint notes list a shared
+  expert beside the routed ones and print nothing about its combination.
 """
 from __future__ import annotations
 
@@ -156,14 +161,33 @@ def l1_swiglu_requant(g_full: np.ndarray, out_gscale=None) -> tuple:
     return q, sf, h
 
 
-def combine(rows_bf16: np.ndarray, inv_perm: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """y[t] = sum_j w[t,j] * rows[inv_perm[t,j]] (float64, slot order) -> BF16 values."""
+def combine(rows_bf16: np.ndarray, inv_perm: np.ndarray, w: np.ndarray,
+            shared_bf16: np.ndarray | None = None) -> np.ndarray:
+    """y[t] = sum_j w[t,j] * rows[inv_perm[t,j]] (+ shared[t]) (float64, slot order,
+    the shared row last) -> BF16 values."""
     rows = np.asarray(rows_bf16, dtype=np.float64)
     t_count, k = inv_perm.shape
     acc = np.zeros((t_count, rows.shape[1]), dtype=np.float64)
     for j in range(k):
         acc += np.asarray(w[:, j], dtype=np.float64)[:, None] * rows[inv_perm[:, j]]
+    if shared_bf16 is not None:
+        acc += np.asarray(shared_bf16, dtype=np.float64)
     return round_to_bf16(acc)
+
+
+def shared_expert_rows(x: np.ndarray, w1s: np.ndarray, w2s: np.ndarray,
+                       alpha1: float = 1.0, alpha2: float = 1.0) -> dict:
+    """The shared expert on every token row of x (fp32 [T,H]): NVFP4 staging of x,
+    L1 + SwiGLU + re-quantisation, L2 -> BF16 rows S [T,H].  The same steps as one
+    routed expert holding all T rows."""
+    xq, xsf = nvfp4.quantize_rows(np.asarray(x, dtype=np.float32))
+    w1q, w1sf = nvfp4.quantize_rows(w1s)
+    w2q, w2sf = nvfp4.quantize_rows(w2s)
+    g_full = np.float64(np.float32(alpha1)) * (nvfp4.dequantize_rows(xq, xsf) @ nvfp4.dequantize_rows(w1q, w1sf).T)
+    a2q, a2sf, h = l1_swiglu_requant(g_full)
+    o = np.float64(np.float32(alpha2)) * (nvfp4.dequantize_rows(a2q, a2sf) @ nvfp4.dequantize_rows(w2q, w2sf).T)
+    return dict(x_q=xq, x_sf=xsf, w1_q=w1q, w1_sf=w1sf, w2_q=w2q, w2_sf=w2sf, h=h, a2_q=a2q, a2_sf=a2sf,
+                rows=round_to_bf16(o))
 
 
 # ---------------------------------------------------------- whole FFN path --
@@ -189,12 +213,13 @@ def two_level_scales(x: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> dict:
 
 
 def moe_ffn(x: np.ndarray, logits: np.ndarray, w1: np.ndarray, w2: np.ndarray, top_k: int,
-            alpha1: float = 1.0, alpha2: float = 1.0, a2_gscale=None) -> dict:
+            alpha1: float = 1.0, alpha2: float = 1.0, a2_gscale=None, shared=None) -> dict:
     """The whole path on CPU.  x: fp32 values of the BF16 activations [T,H];
     logits fp32 [T,E]; w1 fp32 [E, 2I, H] (rows interleaved 8|8); w2 fp32 [E, H, I].
     With ``a2_gscale`` (the L1 output's encode scale, given as a calibrated
     constant) the path runs the two-level scheme: x, W1 and W2 get their own
     encode scales (two_level_scales) and every GEMM's alpha follows.
+    ``shared``: None or (w1s, w2s), a shared expert added to every token's output.
     Returns every intermediate (all computed here, none supplied from outside)."""
     e_count = w1.shape[0]
     ids, w = route_topk(logits, top_k)
@@ -209,21 +234,24 @@ def moe_ffn(x: np.ndarray, logits: np.ndarray, w1: np.ndarray, w2: np.ndarray, t
     o = grouped_gemm(nvfp4.dequantize_rows(a2_q, a2_sf), p["offsets"],
                      dequant_weights(w2_q, w2_sf), alpha2, a2_gscale, gs["w2"])
     rows = round_to_bf16(o)
-    y = combine(rows, p["inv_perm"], w)
+    sh = None if shared is None else shared_expert_rows(x, shared[0], shared[1], alpha1, alpha2)
+    y = combine(rows, p["inv_perm"], w, None if sh is None else sh["rows"])
     return dict(ids=ids, w=w, a1_q=a1_q, a1_sf=a1_sf, w1_q=w1_q, w1_sf=w1_sf, w2_q=w2_q,
-                w2_sf=w2_sf, g_full=g_full, h=h, a2_q=a2_q, a2_sf=a2_sf, rows=rows, y=y, gscales=gs, **p)
+                w2_sf=w2_sf, g_full=g_full, h=h, a2_q=a2_q, a2_sf=a2_sf, rows=rows, y=y, gscales=gs,
+                shared=sh, **p)
 
 
 def moe_ffn_tokens(x_rows: np.ndarray, logits_rows: np.ndarray, w1_of, w2_of, top_k: int,
                    alpha1: float = 1.0, alpha2: float = 1.0, cache: dict | None = None,
-                   two_level: dict | None = None) -> dict:
+                   two_level: dict | None = None, shared=None) -> dict:
     """The same path for a few sampled tokens, one at a time (every step is
     row-independent: a token's output depends only on its own row, its routing
     and its experts' weights).  ``w1_of(e)`` / ``w2_of(e)`` return expert e's fp32
     weights; their quantised, dequantised forms are cached in ``cache``.
     Returns ids, w, a2 rows (q, row-major sf) per (token, slot), and y (BF16 values).
     ``two_level``: dict(x=g_x of the whole batch, a2=the L1 output's encode scale);
-    each expert's weight encode scales are computed from its weights."""
+    each expert's weight encode scales are computed from its weights.
+    ``shared``: None or (w1s, w2s), a shared expert added to every token's output."""
     cache = {} if cache is None else cache
 
     def deq(kind, e, fn):
@@ -259,6 +287,8 @@ def moe_ffn_tokens(x_rows: np.ndarray, logits_rows: np.ndarray, w1_of, w2_of, to
             a2_q.append(q[0])
             a2_sf.append(sf[0])
             h_all.append(h[0])
+        if shared is not None:
+            acc = acc + shared_expert_rows(x_rows[t:t + 1], shared[0], shared[1], alpha1, alpha2)["rows"][0]
         y.append(round_to_bf16(acc))
     return dict(ids=ids, w=w, a2_q=np.array(a2_q).reshape(n_tok, top_k, -1),
                 a2_sf=np.array(a2_sf).reshape(n_tok, top_k, -1), h=np.array(h_all).reshape(n_tok, top_k, -1),
