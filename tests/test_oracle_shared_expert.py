@@ -41,12 +41,12 @@ def test_zero_shared_expert_changes_nothing():
 
 
 def test_combine_adds_the_shared_row_last():
-    rows = np.array([[1.0, 2.0], [3.0, -4.0], [0.5, 0.25]], dtype=np.float64)
+    rows = np.array([[1.0, 2.0], [3.0, -4.0], [0.5, 0.5]], dtype=np.float64)
     inv = np.array([[1, 0], [2, 1]])
     w = np.array([[0.5, 0.5], [1.0, 0.0]], dtype=np.float32)
     shared = np.array([[10.0, -1.0], [0.0, 96.0]])
     y = omoe.combine(rows, inv, w, shared)
-    assert np.array_equal(y, np.array([[12.0, -2.0], [0.5, 96.25]]))
+    assert np.array_equal(y, np.array([[12.0, -2.0], [0.5, 96.5]]))   # all exact in BF16
 
 
 def test_tokens_path_matches_batch_path_with_shared_expert():
