@@ -255,11 +255,17 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         # the L1 output's encode scale, calibrated once on this batch (setup, untimed)
         pipeline.calibrate_a2_scale(x_d, logits_d, w, b)
         b.h_debug = None
+    sh = None
+    if args.shared_expert:
+        sh = pipeline.SharedExpert(s, I)
+        w1s, w2s = inputs.moe_shared_weights(spec, I)
+        sh.set_weights(torch.from_numpy(w1s).cuda(), torch.from_numpy(w2s).cuda())
+        del w1s, w2s
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
     R = b.rows_max
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
 
     gs1 = dict(a_global_scale=b.x_gs, b_global_scale=w.w1_gs, out_global_scale=b.a2_gs) if two else {}
     gs2 = dict(a_global_scale=b.a2_gs, b_global_scale=w.w2_gs) if two else {}
@@ -281,9 +287,12 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                               nv.EPI_BF16, out_bf16=b.rows_out, **gs2)
         if events:
             events[3].record(stream)
-        nv.moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
+        shared_rows = None if sh is None else sh.forward(x_d)
         if events:
             events[4].record(stream)
+        nv.moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y, shared=shared_rows)
+        if events:
+            events[5].record(stream)
 
     # the clock sampler starts before the warm-up so that no idle gap (in which the
     # GPU drops its clocks) separates the warm-up from the timed region
@@ -309,11 +318,15 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     nv.nvfp4_device_status()
     ms_local = start.elapsed_time(end)
     ms = max_over_ranks(ms_local, world)
+    names = ("route_permute", "l1_gemm_swiglu_nvfp4", "l2_gemm_bf16", "shared_expert", "combine")
     per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-           for j, name in enumerate(("route_permute", "l1_gemm_swiglu_nvfp4", "l2_gemm_bf16", "combine"))}
+           for j, name in enumerate(names) if name != "shared_expert" or sh is not None}
 
     l1, l2 = ffn_flops(T, H, I, k)
     step_flops = l1 + l2
+    if sh is not None:                      # the shared expert: one dense L1 + L2 per token
+        shared_l1, shared_l2 = ffn_flops(T, H, I, 1)
+        step_flops += shared_l1 + shared_l2
     value = world * args.steps * step_flops / (ms * 1e-3) / 1e12
     tokens_per_s = world * args.steps * T / (ms * 1e-3)
 
@@ -357,7 +370,9 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                    "parallelism": f"replicas x{world} (independent batches)",
                    "scales": ("two-level: per-tensor encode scales for x (computed each step), W1/W2 "
                               "(per expert) and the L1 output (calibrated once), plus the per-16 E4M3 scales"
-                              if args.two_level else "per-16 E4M3 block scales (global scale 1)")},
+                              if args.two_level else "per-16 E4M3 block scales (global scale 1)"),
+                   "shared_expert": (f"one shared expert (I={I}) on every token, FLOPs credited"
+                                     if args.shared_expert else "none")},
         "tokens_per_s": tokens_per_s,
         "kernel_ms": per,
         "roofline": {"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
@@ -372,7 +387,7 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                      "traffic_unit": "bytes per launch (dram read + write)"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
                 "d2h_bytes_per_step": T * H * 2},
-        "gpu_launches": (10 if args.two_level else 8) * args.steps,
+        "gpu_launches": (8 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -529,6 +544,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared-expert", action="store_true",
+                    help="prefill/decode plus one shared expert (a dense NVFP4 FFN of every token, I = the "
+                         "routed experts' I) added in the combine")
     ap.add_argument("--two-level", action="store_true",
                     help="prefill/decode with the two-level scale (per-tensor encode scales next to the per-16 "
                          "ones); the CPU baseline stays the one-level oracle")

@@ -298,14 +298,17 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
 
 /* ---------------------------------------------------------------------------
  * moe_combine -- "scatter with routing weights" ("NVFP4 MegaMoE Debug Log",
- * "NVFP4 MoE Pipeline"): y[t, :] = bf16( sum_{j < top_k} w[t, j] * rows[inv_perm[t, j], :] ),
- * accumulated in fp32 in slot order.
+ * "NVFP4 MoE Pipeline"): y[t, :] = bf16( sum_{j < top_k} w[t, j] * rows[inv_perm[t, j], :]
+ *                                        + shared[t, :] ),
+ * accumulated in fp32 in slot order, the shared row last.
  *   rows_bf16   BF16 [*, H]; inv_perm int32 [T, top_k]; topk_w fp32 [T, top_k];
+ *   shared_bf16 NULL or BF16 [T, H]: a shared expert's output rows (the pages'
+ *               checkpoint notes list a shared expert beside the routed ones).
  *   y_bf16      BF16 [T, H].  H a positive multiple of 8; pointers 16-byte aligned.
  * -------------------------------------------------------------------------- */
 nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w,
-                         int32_t T, int32_t H, int32_t top_k, void* y_bf16,
-                         nvfp4_stream_t stream);
+                         int32_t T, int32_t H, int32_t top_k, const void* shared_bf16,
+                         void* y_bf16, nvfp4_stream_t stream);
 
 /* Message of the last failing call on this host thread ("" if none). */
 const char* nvfp4_last_error(void);

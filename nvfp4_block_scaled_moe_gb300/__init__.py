@@ -59,7 +59,7 @@ _SIGS = {
                                           _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_moe_ffn_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp,
                                              _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
-    "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_route_permute_static": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                                 _vp, _vp, _vp, _vp]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -176,10 +176,11 @@ def nvfp4_moe_ffn_forward(a1_q, a1_sf, expert_offsets, expert_counts, E, H, I, r
                                         _stream(stream)))
 
 
-def moe_combine(rows, inv_perm, topk_w, y, stream=None):
+def moe_combine(rows, inv_perm, topk_w, y, stream=None, shared=None):
     T, top_k = inv_perm.shape
     H = y.shape[1]
-    _check(load().moe_combine(_p(rows), _p(inv_perm), _p(topk_w), T, H, top_k, _p(y), _stream(stream)))
+    _check(load().moe_combine(_p(rows), _p(inv_perm), _p(topk_w), T, H, top_k, _p(shared), _p(y),
+                              _stream(stream)))
 
 
 def nvfp4_device_status(stream=None):

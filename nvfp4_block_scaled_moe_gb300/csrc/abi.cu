@@ -260,12 +260,13 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf, co
 }
 
 nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w, int32_t T,
-                         int32_t H, int32_t top_k, void* y_bf16, nvfp4_stream_t stream) {
+                         int32_t H, int32_t top_k, const void* shared_bf16, void* y_bf16, nvfp4_stream_t stream) {
   CHECK_ARG(T >= 0 && top_k >= 1, "moe_combine: T=%d top_k=%d", T, top_k);
   CHECK_ARG(T == 0 || (rows_bf16 && inv_perm && topk_w && y_bf16), "moe_combine: null pointer");
   CHECK_SUP(H > 0 && H % 8 == 0, "moe_combine: H=%d is not a positive multiple of 8", H);
   CHECK_AL(T == 0 || (al16(rows_bf16) && al16(y_bf16)), "moe_combine: rows and y must be 16-byte aligned");
-  cudaError_t e = combine_launch(rows_bf16, inv_perm, topk_w, T, H, top_k, y_bf16,
+  CHECK_AL(al16(shared_bf16), "moe_combine: shared rows must be 16-byte aligned");
+  cudaError_t e = combine_launch(rows_bf16, inv_perm, topk_w, T, H, top_k, shared_bf16, y_bf16,
                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_combine");
 }

@@ -49,7 +49,7 @@ void route_carve_workspace(RouteBuffers& b, void* workspace);
 cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream);
 
 cudaError_t combine_launch(const void* rows, const int32_t* inv_perm, const float* w, int32_t T, int32_t H,
-                           int32_t top_k, void* y, cudaStream_t stream);
+                           int32_t top_k, const void* shared, void* y, cudaStream_t stream);
 
 struct GemmArgs {
   const uint8_t* a_q;

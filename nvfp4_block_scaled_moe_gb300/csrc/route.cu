@@ -336,10 +336,12 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
 
 // ---------------------------------------------------------------- combine --
 // One block per token; each thread accumulates 8 columns over the k slots in
-// slot order (fp32 FMA) and rounds once to BF16.
+// slot order (fp32 FMA), then the token's shared-expert row if there is one, and
+// rounds once to BF16.
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ rows,
                                                       const int32_t* __restrict__ inv_perm,
                                                       const float* __restrict__ w, int32_t H, int32_t k,
+                                                      const __nv_bfloat16* __restrict__ shared,
                                                       __nv_bfloat16* __restrict__ y) {
   const int64_t t = blockIdx.x;
   const int n8 = H / 8;
@@ -355,6 +357,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
     }
+    if (shared != nullptr) {
+      float v[8];
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(shared + t * H) + c), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
     o.y = pack_bf16x2(acc[2], acc[3]);
@@ -365,10 +373,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
 }
 
 cudaError_t combine_launch(const void* rows, const int32_t* inv_perm, const float* w, int32_t T, int32_t H,
-                           int32_t top_k, void* y, cudaStream_t stream) {
+                           int32_t top_k, const void* shared, void* y, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   combine_kernel<<<T, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(rows), inv_perm, w, H, top_k,
-                                        static_cast<__nv_bfloat16*>(y));
+                                        static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(y));
   return cudaGetLastError();
 }
 

@@ -17,9 +17,9 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (MODE_PLAIN, moe_combine, moe_padded_rows_max, moe_route_permute,
-               moe_route_permute_workspace, nvfp4_global_scale, nvfp4_moe_ffn_forward, nvfp4_quantize,
-               sf_bytes)
+from . import (EPI_BF16, EPI_SWIGLU_NVFP4, MODE_PLAIN, moe_combine, moe_padded_rows_max, moe_route_permute,
+               moe_route_permute_workspace, nvfp4_global_scale, nvfp4_grouped_gemm, nvfp4_moe_ffn_forward,
+               nvfp4_quantize, sf_bytes)
 
 
 @dataclass
@@ -105,11 +105,47 @@ class MoeWeights:
             self.set_expert(e, w1, w2)
 
 
+class SharedExpert:
+    """A shared expert: one dense NVFP4 FFN (W1 [2*Is, H] interleaved 8|8, W2 [H, Is])
+    applied to every token, with its buffers for T tokens (rows padded to 128)."""
+
+    def __init__(self, s: MoeShape, i_shared: int, device="cuda"):
+        u8 = torch.uint8
+        self.shape, self.I = s, i_shared
+        self.rows = max(128, -(-s.T // 128) * 128)
+        self.w1_q = torch.empty((1, 2 * i_shared, s.H // 2), dtype=u8, device=device)
+        self.w1_sf = torch.empty((1, sf_bytes(2 * i_shared, s.H)), dtype=u8, device=device)
+        self.w2_q = torch.empty((1, s.H, i_shared // 2), dtype=u8, device=device)
+        self.w2_sf = torch.empty((1, sf_bytes(s.H, i_shared)), dtype=u8, device=device)
+        # rows past T stay zero (nibbles) / zero-scaled (SF): they compute to zero
+        self.x_q = torch.zeros((self.rows, s.H // 2), dtype=u8, device=device)
+        self.x_sf = torch.zeros(sf_bytes(self.rows, s.H), dtype=u8, device=device)
+        self.a2_q = torch.empty((self.rows, i_shared // 2), dtype=u8, device=device)
+        self.a2_sf = torch.empty(sf_bytes(self.rows, i_shared), dtype=u8, device=device)
+        self.out = torch.empty((self.rows, s.H), dtype=torch.bfloat16, device=device)
+
+    def set_weights(self, w1_f32: torch.Tensor, w2_f32: torch.Tensor):
+        nvfp4_quantize(w1_f32, self.shape.H, MODE_PLAIN, self.w1_q[0], self.w1_sf[0])
+        nvfp4_quantize(w2_f32, self.I, MODE_PLAIN, self.w2_q[0], self.w2_sf[0])
+
+    def forward(self, x: torch.Tensor, alpha1: float = 1.0, alpha2: float = 1.0) -> torch.Tensor:
+        """out[:T] = the shared FFN of x: NVFP4 staging, L1 + SwiGLU + requant, L2 (dense GEMMs)."""
+        s = self.shape
+        nvfp4_quantize(x, s.H, MODE_PLAIN, self.x_q, self.x_sf)
+        nvfp4_grouped_gemm(self.x_q, self.x_sf, self.rows, None, None, 1, 2 * self.I, s.H, self.w1_q, self.w1_sf,
+                           alpha1, EPI_SWIGLU_NVFP4, out_q=self.a2_q, out_sf=self.a2_sf)
+        nvfp4_grouped_gemm(self.a2_q, self.a2_sf, self.rows, None, None, 1, s.H, self.I, self.w2_q, self.w2_sf,
+                           alpha2, EPI_BF16, out_bf16=self.out)
+        return self.out
+
+
 def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
-                alpha1: float = 1.0, alpha2: float = 1.0, two_level: bool = False) -> torch.Tensor:
+                alpha1: float = 1.0, alpha2: float = 1.0, two_level: bool = False,
+                shared: SharedExpert | None = None) -> torch.Tensor:
     """y = MoE-FFN(x): route + permute + stage, L1 + SwiGLU + requant + L2, combine.
     two_level: x's encode scale is computed here, the weights' are those of ``w``
-    (built with two_level=True) and the L1 output's is ``b.a2_gs`` (None: 1)."""
+    (built with two_level=True) and the L1 output's is ``b.a2_gs`` (None: 1).
+    shared: a shared expert whose rows the combine adds to every token (one level)."""
     s = b.shape
     x_gs = None
     if two_level:
@@ -126,7 +162,8 @@ def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuff
                               x_global_scale=x_gs, w1_global_scale=w.w1_gs if two_level else None,
                               a2_global_scale=b.a2_gs if two_level else None,
                               w2_global_scale=w.w2_gs if two_level else None)
-        moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
+        shared_rows = None if shared is None else shared.forward(x, alpha1, alpha2)
+        moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y, shared=shared_rows)
     return b.y
 
 

@@ -90,7 +90,8 @@ def test_host_validation_without_gpu(lib):
     assert lib.moe_route_permute(p, p, 8, 60, 8, 2, p, p, p, p, p, p, p, p, None, p, 1 << 20, None) == 2
     assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, p, p, None, p, 16, None) == 1
     assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None) == 2
-    assert lib.moe_combine(p, p, p, 4, 12, 2, p, None) == 2
+    assert lib.moe_combine(p, p, p, 4, 12, 2, None, p, None) == 2
+    assert lib.moe_combine(p, p, p, 4, 16, 2, vp(base + 8), p, None) == 3     # misaligned shared rows
     assert lib.nvfp4_selftest_bounded_wait(None, 10, None) == 1
     assert b"selftest" in lib.nvfp4_last_error()
     # tile-kernel choice: three modes, anything else refused; the default restored
