@@ -161,6 +161,14 @@ def l1_swiglu_requant(g_full: np.ndarray, out_gscale=None) -> tuple:
     return q, sf, h
 
 
+def l1_swiglu_bf16(g_full: np.ndarray) -> np.ndarray:
+    """The compact BF16 L1 output (the pages' "compact SwiGLU output" plan): h =
+    silu(g) * u from the interleaved accumulator rows, fp32, then rounded to BF16
+    [rows, I] (no re-quantisation)."""
+    g, u = nvfp4.deinterleave_gu8(g_full)
+    return round_to_bf16(nvfp4.swiglu_h(g, u))
+
+
 def combine(rows_bf16: np.ndarray, inv_perm: np.ndarray, w: np.ndarray,
             shared_bf16: np.ndarray | None = None) -> np.ndarray:
     """y[t] = sum_j w[t,j] * rows[inv_perm[t,j]] (+ shared[t]) (float64, slot order,

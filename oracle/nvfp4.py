@@ -347,6 +347,16 @@ def swiglu_h(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
     return (silu64(gate) * np.asarray(up, dtype=np.float64)).astype(np.float32)
 
 
+def quantize_deinterleave_gu8(gu: np.ndarray, gscale=None) -> tuple:
+    """The pages' deinterleave + quantise (Approach Part 2, K2 as they run it): from
+    columns interleaved at granularity 8, keep the second 8 of every 16 (the up /
+    already-SwiGLU'd slots) and quantise them per 16 -> (q, sf_row_major, kept values)."""
+    _, up = deinterleave_gu8(gu)
+    kept = np.asarray(up, dtype=np.float32)
+    q, sf = quantize_rows(kept, gscale)
+    return q, sf, kept
+
+
 def quantize_swiglu_gu8(gu: np.ndarray, gscale=None) -> tuple:
     """The standalone SwiGLU + NVFP4 quantiser: interleaved gate/up -> (q, sf_row_major, h).
     h is returned unscaled; an encode scale applies to the quantised values only."""
