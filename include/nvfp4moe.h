@@ -63,13 +63,20 @@ typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_F32 = 1 } nvfp4_in_dtype;
 
 typedef enum {
   NVFP4_MODE_PLAIN = 0,        /* quantise the input values themselves */
-  NVFP4_MODE_SWIGLU_GU8 = 1    /* input holds gate/up columns interleaved 8|8;
+  NVFP4_MODE_SWIGLU_GU8 = 1,   /* input holds gate/up columns interleaved 8|8;
                                   quantise h = silu(g) * u */
+  NVFP4_MODE_DEINTERLEAVE_GU8 = 2 /* input interleaved 8|8 as above; quantise the
+                                  second 8 of every 16 columns as they are (the
+                                  pages' deinterleave + quantise of an L1 output
+                                  whose up slots already hold SwiGLU values) */
 } nvfp4_quant_mode;
 
 typedef enum {
   NVFP4_EPI_SWIGLU_NVFP4 = 0,  /* SwiGLU on interleaved 8|8 columns, then NVFP4 */
-  NVFP4_EPI_BF16 = 1           /* alpha * acc rounded to BF16 */
+  NVFP4_EPI_BF16 = 1,          /* alpha * acc rounded to BF16 */
+  NVFP4_EPI_SWIGLU_BF16 = 2    /* SwiGLU on interleaved 8|8 columns, written as compact
+                                  BF16 [rows_max, N/2] (the pages' compact SwiGLU
+                                  output; no re-quantisation) */
 } nvfp4_epilogue;
 
 /* Output-tile kernels of nvfp4_grouped_gemm (see nvfp4_set_gemm_tiles). */
@@ -122,9 +129,9 @@ nvfp4_status nvfp4_global_scale(const void* in, nvfp4_in_dtype dtype, int64_t ro
  * quantize_nvfp4 kernel and the deinterleave + quantise kernel; the E4M3 cast
  * and E2M1 nibble rules above).
  *   in          rows x in_cols values, row stride in_ld_elems elements; in_cols =
- *               out_cols (PLAIN) or 2*out_cols (SWIGLU_GU8, BF16 only:
- *               columns [g0(8) u0(8) g1(8) u1(8) ...]).  16-byte aligned, and
- *               in_ld_elems * element size a multiple of 16.
+ *               out_cols (PLAIN) or 2*out_cols (SWIGLU_GU8 and DEINTERLEAVE_GU8,
+ *               BF16 only: columns [g0(8) u0(8) g1(8) u1(8) ...]).  16-byte
+ *               aligned, and in_ld_elems * element size a multiple of 16.
  *   out_cols    quantised columns per row, a positive multiple of 16.
  *   q_out       rows x out_cols/2 bytes, row-major (written).
  *   sf_out      nvfp4_sf_bytes(rows, out_cols) bytes, swizzled (every byte written,
@@ -238,12 +245,14 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
  *               swizzled; h_debug NULL or fp32 [rows_max, N/2].
  *               NVFP4_EPI_BF16: out_bf16 BF16 [rows_max, N].
+ *               NVFP4_EPI_SWIGLU_BF16: h as above, rounded to BF16 into out_bf16
+ *               [rows_max, N/2] (out_global_scale does not apply).
  * Two kernels compute this (nvfp4_set_gemm_tiles): 128-row tiles on single CTAs,
  * or, when N % 256 == 0, 256-row tiles on CTA pairs (a 2-CTA cluster sharing one
  * cta_group::2 MMA, each CTA loading half of B), which pairs consecutive 128-row
  * blocks of a group.  Both give the same results bit for bit.
- * Limits: K a positive multiple of 256, N a positive multiple of 256 (SWIGLU) or
- * 128 (BF16), rows_max a
+ * Limits: K a positive multiple of 256, N a positive multiple of 256 (the SwiGLU
+ * epilogues) or 128 (BF16), rows_max a
  * positive multiple of 128, all pointers 16-byte aligned.
  * -------------------------------------------------------------------------- */
 nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,

@@ -24,9 +24,9 @@ __all__ = [
     "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
 ]
 
-MODE_PLAIN, MODE_SWIGLU_GU8 = 0, 1
+MODE_PLAIN, MODE_SWIGLU_GU8, MODE_DEINTERLEAVE_GU8 = 0, 1, 2
 IN_BF16, IN_F32 = 0, 1
-EPI_SWIGLU_NVFP4, EPI_BF16 = 0, 1
+EPI_SWIGLU_NVFP4, EPI_BF16, EPI_SWIGLU_BF16 = 0, 1, 2
 
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CUDA", 5: "TIMEOUT", 6: "DEVICE"}
 

@@ -104,11 +104,12 @@ nvfp4_status nvfp4_quantize(const void* in, nvfp4_in_dtype dtype, nvfp4_quant_mo
                             const float* global_scale, float* h_debug, nvfp4_stream_t stream) {
   CHECK_ARG(in && q_out && sf_out, "nvfp4_quantize: null pointer");
   CHECK_ARG(dtype == NVFP4_IN_BF16 || dtype == NVFP4_IN_F32, "nvfp4_quantize: bad dtype %d", (int)dtype);
-  CHECK_ARG(mode == NVFP4_MODE_PLAIN || mode == NVFP4_MODE_SWIGLU_GU8, "nvfp4_quantize: bad mode %d", (int)mode);
+  CHECK_ARG(mode == NVFP4_MODE_PLAIN || mode == NVFP4_MODE_SWIGLU_GU8 || mode == NVFP4_MODE_DEINTERLEAVE_GU8,
+            "nvfp4_quantize: bad mode %d", (int)mode);
   CHECK_ARG(rows > 0 && out_cols > 0, "nvfp4_quantize: rows and out_cols must be positive");
   CHECK_SUP(out_cols % 16 == 0, "nvfp4_quantize: out_cols=%lld is not a multiple of 16", (long long)out_cols);
-  CHECK_SUP(mode == NVFP4_MODE_PLAIN || dtype == NVFP4_IN_BF16, "nvfp4_quantize: SWIGLU_GU8 takes BF16 input");
-  const int64_t in_cols = mode == NVFP4_MODE_SWIGLU_GU8 ? 2 * out_cols : out_cols;
+  CHECK_SUP(mode == NVFP4_MODE_PLAIN || dtype == NVFP4_IN_BF16, "nvfp4_quantize: the GU8 modes take BF16 input");
+  const int64_t in_cols = mode == NVFP4_MODE_PLAIN ? out_cols : 2 * out_cols;
   CHECK_ARG(in_ld_elems >= in_cols, "nvfp4_quantize: in_ld_elems=%lld < %lld", (long long)in_ld_elems,
             (long long)in_cols);
   const int64_t esize = dtype == NVFP4_IN_BF16 ? 2 : 4;
@@ -198,15 +199,16 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 const float* out_global_scale, nvfp4_epilogue epilogue, uint8_t* out_q,
                                 uint8_t* out_sf, void* out_bf16, float* h_debug, nvfp4_stream_t stream) {
   CHECK_ARG(a_q && a_sf && b_q && b_sf, "nvfp4_grouped_gemm: null operand");
-  CHECK_ARG(epilogue == NVFP4_EPI_SWIGLU_NVFP4 || epilogue == NVFP4_EPI_BF16, "nvfp4_grouped_gemm: bad epilogue");
+  CHECK_ARG(epilogue == NVFP4_EPI_SWIGLU_NVFP4 || epilogue == NVFP4_EPI_BF16 || epilogue == NVFP4_EPI_SWIGLU_BF16,
+            "nvfp4_grouped_gemm: bad epilogue");
   CHECK_ARG(epilogue != NVFP4_EPI_SWIGLU_NVFP4 || (out_q && out_sf), "nvfp4_grouped_gemm: null NVFP4 output");
-  CHECK_ARG(epilogue != NVFP4_EPI_BF16 || out_bf16, "nvfp4_grouped_gemm: null BF16 output");
+  CHECK_ARG(epilogue == NVFP4_EPI_SWIGLU_NVFP4 || out_bf16, "nvfp4_grouped_gemm: null BF16 output");
   CHECK_ARG(group_offsets || !group_counts, "nvfp4_grouped_gemm: group_counts needs group_offsets");
   CHECK_ARG(G >= 1 && N > 0 && K > 0 && rows_max > 0, "nvfp4_grouped_gemm: sizes must be positive");
   CHECK_SUP(group_offsets || G == 1, "nvfp4_grouped_gemm: NULL group_offsets means G == 1");
   CHECK_SUP(K % 256 == 0, "nvfp4_grouped_gemm: K=%d is not a multiple of 256", K);
-  CHECK_SUP(N % (epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? 256 : 128) == 0,
-            "nvfp4_grouped_gemm: N=%d is not a multiple of %d", N, epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? 256 : 128);
+  CHECK_SUP(N % (epilogue == NVFP4_EPI_BF16 ? 128 : 256) == 0,
+            "nvfp4_grouped_gemm: N=%d is not a multiple of %d", N, epilogue == NVFP4_EPI_BF16 ? 128 : 256);
   CHECK_SUP(rows_max % 128 == 0 && rows_max < (int64_t(1) << 31), "nvfp4_grouped_gemm: rows_max=%lld",
             (long long)rows_max);
   CHECK_SUP(static_cast<int64_t>(G) * N < (int64_t(1) << 31), "nvfp4_grouped_gemm: G*N too large");

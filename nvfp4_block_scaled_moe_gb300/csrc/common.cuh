@@ -156,6 +156,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
+// The compact BF16 SwiGLU output of one thread's row: 128 interleaved gate/up
+// accumulator columns (4 chunks of g(8) u(8) g(8) u(8)) -> 64 values of
+// silu(alpha g) * (alpha u), rounded to BF16 and stored as 8 x 16 bytes at dst.
+__device__ __forceinline__ void swiglu_bf16_row(const float (&v)[4][32], float alpha, __nv_bfloat16* dst) {
+  uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = 16 * half + 2 * i;
+        w[i] = pack_bf16x2(swiglu(alpha * v[c][j], alpha * v[c][j + 8]),
+                           swiglu(alpha * v[c][j + 1], alpha * v[c][j + 9]));
+      }
+      out[2 * c + half] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // ------------------------------------------------------------- mbarriers --
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

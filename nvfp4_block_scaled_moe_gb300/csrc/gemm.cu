@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kBBytes = C::kBBytes, kSfbBytes = C::kSfbBytes, kStageTx = C::kStageTx;
   constexpr uint32_t kOffA = C::kOffA, kOffB = C::kOffB, kOffSfa = C::kOffSfa, kOffSfb = C::kOffSfb;
   constexpr uint32_t kTmemSf = C::kTmemSf, kTmemSfStage = C::kTmemSfStage;
-  static_assert(kEpi != NVFP4_EPI_SWIGLU_NVFP4 || BN == 256, "the SwiGLU epilogue uses 256-column tiles");
+  static_assert(kEpi == NVFP4_EPI_BF16 || BN == 256, "the SwiGLU epilogues use 256-column tiles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -349,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kEpi == NVFP4_EPI_SWIGLU_NVFP4) {
         epilogue_swiglu(v, alpha, p.out_gs, valid, grow, static_cast<int64_t>(nt) * (kBN / 2) + half * 64, p.N / 2,
                         2 * nt + half, static_cast<uint32_t>(p.N / 128), p.out_q, p.out_sf, p.h_debug);
+      } else if constexpr (kEpi == NVFP4_EPI_SWIGLU_BF16) {
+        if (valid)
+          swiglu_bf16_row(v, alpha, p.out_bf16 + grow * (p.N / 2) + static_cast<int64_t>(nt) * (kBN / 2) + half * 64);
       } else {
         if (valid)
           epilogue_bf16<C::kChunks>(v, alpha,
@@ -406,7 +409,7 @@ std::atomic<int> g_gemm_tiles{NVFP4_GEMM_TILES_AUTO};
 
 struct DeviceInfo {
   int sms = 0;
-  bool attr_set[3] = {false, false, false};
+  bool attr_set[4] = {false, false, false, false};
 };
 
 DeviceInfo& device_info(int dev) {
@@ -421,7 +424,7 @@ DeviceInfo& device_info(int dev) {
 template <int kEpi, int BN>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t stream,
                    DeviceInfo& info) {
-  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : (BN == 256 ? 1 : 2);
+  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_SWIGLU_BF16 ? 3 : (BN == 256 ? 1 : 2);
   if (!info.attr_set[slot]) {
     cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_kernel<kEpi, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg<BN>::kSmemBytes));
@@ -448,7 +451,7 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   // 128x128 tiles with a double-buffered accumulator.  Groups averaging two or
   // more 128-row blocks go to the CTA-pair kernel (256x256 tiles, gemm_pair.cu);
   // thinner groups (decode-sized batches) would leave half of many pair tiles empty.
-  const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
+  const bool swiglu = a.epilogue != NVFP4_EPI_BF16;
   const int bn = (swiglu || a.N % 256 == 0) ? 256 : 128;
   const int mode = g_gemm_tiles.load(std::memory_order_relaxed);
   const int64_t groups = a.offsets != nullptr ? a.G : 1;
@@ -488,9 +491,10 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   const int64_t max_tiles = (a.rows_max / kBM) * p.n_tiles;
   const int grid = static_cast<int>(max_tiles < info.sms ? max_tiles : info.sms);
   if (grid <= 0) return NVFP4_OK;
-  e = swiglu      ? launch<NVFP4_EPI_SWIGLU_NVFP4, 256>(ma, mb, p, grid, stream, info)
-      : bn == 256 ? launch<NVFP4_EPI_BF16, 256>(ma, mb, p, grid, stream, info)
-                  : launch<NVFP4_EPI_BF16, 128>(ma, mb, p, grid, stream, info);
+  e = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? launch<NVFP4_EPI_SWIGLU_NVFP4, 256>(ma, mb, p, grid, stream, info)
+      : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? launch<NVFP4_EPI_SWIGLU_BF16, 256>(ma, mb, p, grid, stream, info)
+      : bn == 256                           ? launch<NVFP4_EPI_BF16, 256>(ma, mb, p, grid, stream, info)
+                                            : launch<NVFP4_EPI_BF16, 128>(ma, mb, p, grid, stream, info);
   if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm launch");
   return NVFP4_OK;
 }

@@ -418,6 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           stores_pending = true;
         }
+      } else if constexpr (kEpi == NVFP4_EPI_SWIGLU_BF16) {
+        if (valid)
+          swiglu_bf16_row(v, alpha, p.out_bf16 + grow * (p.N / 2) + static_cast<int64_t>(t.nt) * (kBN / 2) + half * 64);
       } else {
         if (staged) {
           // two passes of 32 rows x 64 columns through the staging buffer: each
@@ -484,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct PairDeviceInfo {
-  bool attr_set[2] = {false, false};
-  int max_clusters[2] = {0, 0};
+  bool attr_set[3] = {false, false, false};
+  int max_clusters[3] = {0, 0, 0};
 };
 
 PairDeviceInfo& pair_info(int dev) {
@@ -502,7 +505,7 @@ template <int kEpi>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : 1;
+  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2;
   constexpr uint32_t smem = PairCfg<kEpi>::kSmemBytes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -558,9 +561,9 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   if (swiglu)
     ok = ok && make_tmap_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.out_q, static_cast<uint64_t>(a.rows_max),
                             static_cast<uint64_t>(a.N) / 4, 1, 32, 32, false);
-  else
+  else   // BF16 outputs: [rows_max, N], or [rows_max, N/2] for the compact SwiGLU output
     ok = ok && make_tmap_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out_bf16, static_cast<uint64_t>(a.rows_max),
-                            static_cast<uint64_t>(a.N), 2, 64, 32, true);
+                            static_cast<uint64_t>(a.epilogue == NVFP4_EPI_BF16 ? a.N : a.N / 2), 2, 64, 32, true);
   if (!ok) return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: cuTensorMapEncodeTiled failed");
 
   PairParams p;
@@ -592,7 +595,9 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   if (max_tiles <= 0) return NVFP4_OK;
   const cudaError_t e =
       swiglu ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
-             : launch_pair<NVFP4_EPI_BF16>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream);
+      : a.epilogue == NVFP4_EPI_SWIGLU_BF16
+          ? launch_pair<NVFP4_EPI_SWIGLU_BF16>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
+          : launch_pair<NVFP4_EPI_BF16>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream);
   if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm (CTA pairs) launch");
   return NVFP4_OK;
 }

@@ -36,6 +36,17 @@ __device__ __forceinline__ void load_block(const void* in, int64_t row, int64_t 
     bf16x8_to_f32(u1, u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) h[8 + i] = swiglu(g[i], u[i]);
+  } else if (kMode == NVFP4_MODE_DEINTERLEAVE_GU8) {
+    // interleaved columns 2*c0 .. 2*c0+31: keep u0(8) and u1(8) as they are
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + 2 * c0);
+    float lo[8], hi[8];
+    bf16x8_to_f32(__ldg(p + 1), lo);
+    bf16x8_to_f32(__ldg(p + 3), hi);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h[i] = lo[i];
+      h[8 + i] = hi[i];
+    }
   } else if (kDtype == NVFP4_IN_BF16) {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + c0);
     float lo[8], hi[8];
@@ -151,6 +162,9 @@ cudaError_t quantize_launch(const void* in, int dtype, int mode, int64_t rows, i
   if (mode == NVFP4_MODE_SWIGLU_GU8)
     return launch_quantize<NVFP4_MODE_SWIGLU_GU8, NVFP4_IN_BF16>(in, rows, cols, ld, rows_pad, q, sf,
                                                                  sf_linear, gscale, h_dbg, stream);
+  if (mode == NVFP4_MODE_DEINTERLEAVE_GU8)
+    return launch_quantize<NVFP4_MODE_DEINTERLEAVE_GU8, NVFP4_IN_BF16>(in, rows, cols, ld, rows_pad, q, sf,
+                                                                       sf_linear, gscale, h_dbg, stream);
   if (dtype == NVFP4_IN_BF16)
     return launch_quantize<NVFP4_MODE_PLAIN, NVFP4_IN_BF16>(in, rows, cols, ld, rows_pad, q, sf, sf_linear,
                                                             gscale, h_dbg, stream);

@@ -26,7 +26,10 @@ def nv():
 
 
 def _replayed(fn, outs):
-    """Run fn eagerly, snapshot outs; zero them, capture fn, replay twice; compare."""
+    """Zero outs, run fn eagerly, snapshot; zero again, capture fn, replay twice;
+    compare (regions a call leaves unwritten stay zero on both sides)."""
+    for o in outs:
+        o.zero_()
     fn()
     torch.cuda.synchronize()
     eager = [o.clone() for o in outs]
