@@ -246,7 +246,7 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     w = pipeline.MoeWeights(s, two_level=two)
     pool, o1, o2 = inputs.moe_weight_pool(spec)
     w.set_from_pool(torch.from_numpy(pool).cuda(), o1, o2, float(inputs.WEIGHT_STD))
-    b = pipeline.MoeBuffers(s)
+    b = pipeline.MoeBuffers(s, gather=args.gather)
     x_t, _ = inputs.moe_x(spec)
     logits_np = inputs.moe_logits(spec)
     x_d = x_t.cuda()
@@ -269,6 +269,7 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
 
     gs1 = dict(a_global_scale=b.x_gs, b_global_scale=w.w1_gs, out_global_scale=b.a2_gs) if two else {}
     gs2 = dict(a_global_scale=b.a2_gs, b_global_scale=w.w2_gs) if two else {}
+    gather1 = dict(a_gather=b.perm_token, a_gather_rows=T) if b.gather else {}
 
     def step(events=None):
         if events:
@@ -276,11 +277,13 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         if two:                                  # x's encode scale, per batch (timed with routing)
             nv.nvfp4_global_scale(x_d, b.x_gs)
         nv.moe_route_permute(logits_d, x_d, k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
-                             b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_global_scale=b.x_gs if two else None)
+                             b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_global_scale=b.x_gs if two else None,
+                             x_q=b.x_q)
         if events:
             events[1].record(stream)
-        nv.nvfp4_grouped_gemm(b.a1_q, b.a1_sf, R, b.offsets, b.counts, E, 2 * I, H, w.w1_q, w.w1_sf, 1.0,
-                              nv.EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf, **gs1)
+        nv.nvfp4_grouped_gemm(b.x_q if b.gather else b.a1_q, b.a1_sf, R, b.offsets, b.counts, E, 2 * I, H,
+                              w.w1_q, w.w1_sf, 1.0, nv.EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf, **gs1,
+                              **gather1)
         if events:
             events[2].record(stream)
         nv.nvfp4_grouped_gemm(b.a2_q, b.a2_sf, R, b.offsets, b.counts, E, H, I, w.w2_q, w.w2_sf, 1.0,
@@ -544,6 +547,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gather", action=argparse.BooleanOptionalAction, default=False,
+                    help="L1 gathers its A rows from x quantised once in token order (TMA gather4) instead of a "
+                         "permuted copy written by the routing call")
     ap.add_argument("--shared-expert", action="store_true",
                     help="prefill/decode plus one shared expert (a dense NVFP4 FFN of every token, I = the "
                          "routed experts' I) added in the combine")

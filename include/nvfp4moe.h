@@ -180,8 +180,12 @@ nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_s
  *               ascending token order (deterministic, no atomics in the order).
  *   inv_perm    int32 [T, top_k]: padded row of each (token, slot).
  *   a1_q        [R_max, H/2] NVFP4 rows of x in permuted order; padding rows
- *               inside groups are zero.
+ *               inside groups are zero.  May be NULL when x_q is given (the
+ *               permuted copy is then not written).
  *   a1_sf       nvfp4_sf_bytes(R_max, H) bytes, swizzled, zero on padding rows.
+ *   x_q         NULL, or [T, H/2]: the same NVFP4 rows in token order, for an L1
+ *               GEMM that gathers its A rows through perm_token (the
+ *               permuted copy of a1_q is then never materialised).
  *   x_global_scale  NULL or x's device encode scale g (the rows hold fp32(x * g)).
  *   workspace   >= moe_route_permute_workspace(T, H, E, top_k) bytes, 16-byte
  *               aligned (per-chunk expert histograms, cleared by the call).
@@ -192,8 +196,8 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
                                int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
                                int32_t* expert_counts, int32_t* expert_offsets,
                                int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                               uint8_t* a1_sf, const float* x_global_scale, void* workspace,
-                               size_t workspace_bytes, nvfp4_stream_t stream);
+                               uint8_t* a1_sf, uint8_t* x_q, const float* x_global_scale,
+                               void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_route_permute_static -- moe_route_permute for callers that cannot allocate
@@ -217,7 +221,7 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
                                       int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
                                       int32_t* expert_counts, int32_t* expert_offsets,
                                       int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                                      uint8_t* a1_sf, const float* x_global_scale,
+                                      uint8_t* a1_sf, uint8_t* x_q, const float* x_global_scale,
                                       nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -240,6 +244,13 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *               of alpha by the fp32 product) in place of alpha.
  *   out_global_scale  NULL or the encode scale of the SwiGLU output: the
  *               re-quantised values are fp32(h * g) (h_debug keeps h).
+ *   a_gather, a_gather_rows  NULL, or device int32 [rows_max] (16-byte aligned):
+ *               row r of A is row a_gather[r] of a_q, which then has
+ *               a_gather_rows rows (loaded with TMA tile::gather4; moe_route_permute's
+ *               perm_token over its x_q).  An entry < 0 marks a row whose scales
+ *               in a_sf are zero (group padding) and reads row 0; an entry past
+ *               the end reads row 0 and sets the device error word.  a_sf keeps
+ *               the rows_max-row layout.
  *   epilogue    NVFP4_EPI_SWIGLU_NVFP4: N columns interleaved 8|8 as gate/up;
  *               h = silu(alpha*g) * (alpha*u) quantised as in nvfp4_quantize ->
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
@@ -261,7 +272,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 const uint8_t* b_sf, float alpha, const float* a_global_scale,
                                 const float* b_global_scale, const float* out_global_scale,
                                 nvfp4_epilogue epilogue, uint8_t* out_q, uint8_t* out_sf,
-                                void* out_bf16, float* h_debug, nvfp4_stream_t stream);
+                                void* out_bf16, float* h_debug, const int32_t* a_gather,
+                                int64_t a_gather_rows, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_set_gemm_tiles -- process-wide choice of nvfp4_grouped_gemm's tile kernel
@@ -293,6 +305,9 @@ nvfp4_status nvfp4_set_gemm_tiles(int32_t mode);
  *                (the pages' alpha = igs * global_sf).  g_a2 is an input: the
  *                fused epilogue quantises each tile as it is produced, before the
  *                tensor's amax exists, so the scale is calibrated ahead.
+ *   a1_gather, a1_gather_rows  NULL, or L1 gathers its A rows: a1_q is
+ *                moe_route_permute's x_q [T, H/2] and a1_gather its perm_token
+ *                (a1_gather_rows = T); see nvfp4_grouped_gemm.
  * Limits: H and I positive multiples of 256, rows_max a positive multiple of 128.
  * -------------------------------------------------------------------------- */
 nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
@@ -303,7 +318,8 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
                                    float alpha2, const float* x_global_scale,
                                    const float* w1_global_scale, const float* a2_global_scale,
                                    const float* w2_global_scale, uint8_t* a2_q, uint8_t* a2_sf,
-                                   void* rows_out_bf16, float* h_debug, nvfp4_stream_t stream);
+                                   void* rows_out_bf16, float* h_debug, const int32_t* a1_gather,
+                                   int64_t a1_gather_rows, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_combine -- "scatter with routing weights" ("NVFP4 MegaMoE Debug Log",

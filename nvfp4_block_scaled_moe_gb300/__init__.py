@@ -54,14 +54,15 @@ _SIGS = {
     "nvfp4_global_scale": (ctypes.c_int, [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp]),
     "nvfp4_sf_swizzle": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i64, _vp, ctypes.c_int, _vp]),
     "moe_route_permute": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                         _vp, _vp, _vp, _sz, _vp]),
+                                         _vp, _vp, _vp, _vp, _sz, _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _f32,
-                                          _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp]),
+                                          _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "nvfp4_moe_ffn_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp,
-                                             _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+                                             _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                             _vp]),
     "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_route_permute_static": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
-                                                _vp, _vp, _vp, _vp]),
+                                                _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
@@ -137,43 +138,44 @@ def nvfp4_sf_swizzle(sf_in, mn_rows, k_sf_cols, stride_mn, stride_ksf, sf_out, i
 
 
 def moe_route_permute(logits, x, top_k, topk_ids, topk_w, expert_counts, expert_offsets, perm_token, inv_perm,
-                      a1_q, a1_sf, workspace, stream=None, x_global_scale=None):
+                      a1_q, a1_sf, workspace, stream=None, x_global_scale=None, x_q=None):
     T, E = logits.shape
     H = x.shape[1]
     _check(load().moe_route_permute(_p(logits), _p(x), T, H, E, top_k, _p(topk_ids), _p(topk_w),
                                     _p(expert_counts), _p(expert_offsets), _p(perm_token), _p(inv_perm),
-                                    _p(a1_q), _p(a1_sf), _p(x_global_scale), _p(workspace),
+                                    _p(a1_q), _p(a1_sf), _p(x_q), _p(x_global_scale), _p(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def moe_route_permute_static(logits, x, top_k, topk_ids, topk_w, expert_counts, expert_offsets, perm_token,
-                             inv_perm, a1_q, a1_sf, stream=None, x_global_scale=None):
+                             inv_perm, a1_q, a1_sf, stream=None, x_global_scale=None, x_q=None):
     """moe_route_permute with the library's fixed device scratch instead of a
     caller workspace, for callers that cannot allocate (see include/nvfp4moe.h)."""
     T, E = logits.shape
     H = x.shape[1]
     _check(load().moe_route_permute_static(_p(logits), _p(x), T, H, E, top_k, _p(topk_ids), _p(topk_w),
                                            _p(expert_counts), _p(expert_offsets), _p(perm_token), _p(inv_perm),
-                                           _p(a1_q), _p(a1_sf), _p(x_global_scale), _stream(stream)))
+                                           _p(a1_q), _p(a1_sf), _p(x_q), _p(x_global_scale), _stream(stream)))
 
 
 def nvfp4_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, alpha, epilogue,
                        out_q=None, out_sf=None, out_bf16=None, h_debug=None, stream=None, a_global_scale=None,
-                       b_global_scale=None, out_global_scale=None):
+                       b_global_scale=None, out_global_scale=None, a_gather=None, a_gather_rows=0):
     _check(load().nvfp4_grouped_gemm(_p(a_q), _p(a_sf), rows_max, _p(group_offsets), _p(group_counts), G, N, K,
                                      _p(b_q), _p(b_sf), alpha, _p(a_global_scale), _p(b_global_scale),
                                      _p(out_global_scale), epilogue, _p(out_q), _p(out_sf), _p(out_bf16),
-                                     _p(h_debug), _stream(stream)))
+                                     _p(h_debug), _p(a_gather), a_gather_rows, _stream(stream)))
 
 
 def nvfp4_moe_ffn_forward(a1_q, a1_sf, expert_offsets, expert_counts, E, H, I, rows_max, w1_q, w1_sf, w2_q, w2_sf,
                           alpha1, alpha2, a2_q, a2_sf, rows_out, h_debug=None, stream=None, x_global_scale=None,
-                          w1_global_scale=None, a2_global_scale=None, w2_global_scale=None):
+                          w1_global_scale=None, a2_global_scale=None, w2_global_scale=None, a1_gather=None,
+                          a1_gather_rows=0):
     _check(load().nvfp4_moe_ffn_forward(_p(a1_q), _p(a1_sf), _p(expert_offsets), _p(expert_counts), E, H, I,
                                         rows_max, _p(w1_q), _p(w1_sf), _p(w2_q), _p(w2_sf), alpha1, alpha2,
                                         _p(x_global_scale), _p(w1_global_scale), _p(a2_global_scale),
                                         _p(w2_global_scale), _p(a2_q), _p(a2_sf), _p(rows_out), _p(h_debug),
-                                        _stream(stream)))
+                                        _p(a1_gather), a1_gather_rows, _stream(stream)))
 
 
 def moe_combine(rows, inv_perm, topk_w, y, stream=None, shared=None):

@@ -156,16 +156,16 @@ nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_s
 nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t T, int32_t H, int32_t E,
                                int32_t top_k, int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
                                int32_t* expert_offsets, int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                               uint8_t* a1_sf, const float* x_global_scale, void* workspace, size_t workspace_bytes,
-                               nvfp4_stream_t stream) {
+                               uint8_t* a1_sf, uint8_t* x_q, const float* x_global_scale, void* workspace,
+                               size_t workspace_bytes, nvfp4_stream_t stream) {
   CHECK_ARG(T >= 0, "moe_route_permute: T=%d", T);
   CHECK_ARG(expert_counts && expert_offsets && workspace, "moe_route_permute: null pointer");
-  CHECK_ARG(T == 0 || (logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_q && a1_sf),
-            "moe_route_permute: null pointer");
+  CHECK_ARG(T == 0 || (logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_sf && (a1_q || x_q)),
+            "moe_route_permute: null pointer (a1_q and x_q may not both be null)");
   CHECK_SUP(E >= 1 && E <= 1024, "moe_route_permute: E=%d outside [1, 1024]", E);
   CHECK_SUP(top_k >= 1 && top_k <= E && top_k <= 32, "moe_route_permute: top_k=%d outside [1, min(E, 32)]", top_k);
   CHECK_SUP(H > 0 && H % 64 == 0, "moe_route_permute: H=%d is not a positive multiple of 64", H);
-  CHECK_AL(al16(workspace) && (T == 0 || (al16(x_bf16) && al16(a1_q) && al16(a1_sf))),
+  CHECK_AL(al16(workspace) && (T == 0 || (al16(x_bf16) && al16(a1_q) && al16(a1_sf) && al16(x_q))),
            "moe_route_permute: x, a1_q, a1_sf and workspace must be 16-byte aligned");
   CHECK_AL(al4(x_global_scale), "moe_route_permute: x_global_scale not 4-byte aligned");
   const size_t need = moe_route_permute_workspace(T, H, E, top_k);
@@ -185,6 +185,7 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
   b.inv_perm = inv_perm;
   b.a1_q = a1_q;
   b.a1_sf = a1_sf;
+  b.x_q = x_q;
   b.x_gscale = x_global_scale;
   b.rows_max = moe_padded_rows_max(T, E, top_k);
   route_carve_workspace(b, workspace);
@@ -197,8 +198,12 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 int32_t K, const uint8_t* b_q, const uint8_t* b_sf, float alpha,
                                 const float* a_global_scale, const float* b_global_scale,
                                 const float* out_global_scale, nvfp4_epilogue epilogue, uint8_t* out_q,
-                                uint8_t* out_sf, void* out_bf16, float* h_debug, nvfp4_stream_t stream) {
+                                uint8_t* out_sf, void* out_bf16, float* h_debug, const int32_t* a_gather,
+                                int64_t a_gather_rows, nvfp4_stream_t stream) {
   CHECK_ARG(a_q && a_sf && b_q && b_sf, "nvfp4_grouped_gemm: null operand");
+  CHECK_ARG(!a_gather || (a_gather_rows > 0 && a_gather_rows < (int64_t(1) << 31)),
+            "nvfp4_grouped_gemm: a_gather_rows=%lld", (long long)a_gather_rows);
+  CHECK_AL(al16(a_gather), "nvfp4_grouped_gemm: a_gather not 16-byte aligned");
   CHECK_ARG(epilogue == NVFP4_EPI_SWIGLU_NVFP4 || epilogue == NVFP4_EPI_BF16 || epilogue == NVFP4_EPI_SWIGLU_BF16,
             "nvfp4_grouped_gemm: bad epilogue");
   CHECK_ARG(epilogue != NVFP4_EPI_SWIGLU_NVFP4 || (out_q && out_sf), "nvfp4_grouped_gemm: null NVFP4 output");
@@ -222,6 +227,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
   a.a_q = a_q;
   a.a_sf = a_sf;
   a.rows_max = rows_max;
+  a.a_gather = a_gather;
+  a.a_rows = a_gather ? a_gather_rows : rows_max;
   a.offsets = group_offsets;
   a.counts = group_counts;
   a.G = G;
@@ -247,18 +254,20 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf, co
                                    const uint8_t* w2_sf, float alpha1, float alpha2, const float* x_global_scale,
                                    const float* w1_global_scale, const float* a2_global_scale,
                                    const float* w2_global_scale, uint8_t* a2_q, uint8_t* a2_sf, void* rows_out_bf16,
-                                   float* h_debug, nvfp4_stream_t stream) {
+                                   float* h_debug, const int32_t* a1_gather, int64_t a1_gather_rows,
+                                   nvfp4_stream_t stream) {
   CHECK_ARG(expert_offsets && expert_counts, "nvfp4_moe_ffn_forward: null expert offsets/counts");
   CHECK_ARG(a2_q && a2_sf && rows_out_bf16, "nvfp4_moe_ffn_forward: null output");
   CHECK_SUP(H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0,
             "nvfp4_moe_ffn_forward: H=%d and I=%d must be positive multiples of 256", H, I);
   nvfp4_status st = nvfp4_grouped_gemm(a1_q, a1_sf, rows_max, expert_offsets, expert_counts, E, 2 * I, H, w1_q,
                                        w1_sf, alpha1, x_global_scale, w1_global_scale, a2_global_scale,
-                                       NVFP4_EPI_SWIGLU_NVFP4, a2_q, a2_sf, nullptr, h_debug, stream);
+                                       NVFP4_EPI_SWIGLU_NVFP4, a2_q, a2_sf, nullptr, h_debug, a1_gather,
+                                       a1_gather_rows, stream);
   if (st != NVFP4_OK) return st;
   return nvfp4_grouped_gemm(a2_q, a2_sf, rows_max, expert_offsets, expert_counts, E, H, I, w2_q, w2_sf, alpha2,
                             a2_global_scale, w2_global_scale, nullptr, NVFP4_EPI_BF16, nullptr, nullptr,
-                            rows_out_bf16, nullptr, stream);
+                            rows_out_bf16, nullptr, nullptr, 0, stream);
 }
 
 nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w, int32_t T,

@@ -305,6 +305,45 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Gather of four rows y.x .. y.w (each one 128-byte box row of a map whose box
+// is 128 bytes x 1 row) into consecutive 128-byte rows at dst (which keeps the
+// map's swizzle, as a 4-row tile at that address would); x as for tma_load_2d.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x, int4 y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w)
+      : "memory");
+}
+
+// The same, completing on the barrier at cluster address `bar` (cta_group::2).
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* map, uint32_t bar, int32_t x, int4 y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(bar), "r"(x), "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w)
+      : "memory");
+}
+
+// Source rows of one 128-row block of A under a gather index: lane l gets the
+// entries of rows 4l .. 4l+3.  Entries < 0 mark rows whose scales are zero
+// (group padding) and read row 0; entries >= a_rows set the bounds bit and read
+// row 0 too, so no copy leaves the matrix.
+__device__ __forceinline__ int4 gather_rows4(const int32_t* index, int64_t block, int64_t a_rows, unsigned* err,
+                                             int lane) {
+  int4 r = __ldg(reinterpret_cast<const int4*>(index + block * 128) + lane);
+  int* v = reinterpret_cast<int*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (v[i] >= a_rows) {
+      raise_error(err, kErrBounds);
+      v[i] = 0;
+    }
+    if (v[i] < 0) v[i] = 0;
+  }
+  return r;
+}
+
 // Contiguous global -> shared copy; both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(

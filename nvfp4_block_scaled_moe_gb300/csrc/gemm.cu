@@ -82,6 +82,8 @@ struct Cfg {
 struct Params {
   const uint8_t* a_sf;
   const uint8_t* b_sf;
+  const int32_t* a_gather;    // null, or the source row in A of every padded row
+  int64_t a_rows;
   const int32_t* offsets;
   const int32_t* counts;
   int32_t G, N, K;
@@ -244,13 +246,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = __shfl_sync(0xFFFFFFFFu, find_group(s_off, p.G, mt * kBM), 0);
       const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
       const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(kBands * nt) * k4) * 512;
+      const bool gather = p.a_gather != nullptr;
+      const int4 rows4 = gather ? gather_rows4(p.a_gather, mt, p.a_rows, p.err, lane) : make_int4(0, 0, 0, 0);
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.err);
         if (!ok) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[stage], kStageTx);
-          tma_load_2d(smem + kOffA + stage * kABytes, &tmap_a, &full[stage], kb * (kBK / 2),
-                      static_cast<int32_t>(mt * kBM));
+          if (!gather)
+            tma_load_2d(smem + kOffA + stage * kABytes, &tmap_a, &full[stage], kb * (kBK / 2),
+                        static_cast<int32_t>(mt * kBM));
           tma_load_2d(smem + kOffB + stage * kBBytes, &tmap_b, &full[stage], kb * (kBK / 2), g * p.N + nt * kBN);
           bulk_load(smem + kOffSfa + stage * kSfaBytes, sfa + kb * 4 * 512, kSfaBytes, &full[stage]);
 #pragma unroll
@@ -258,6 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_load(smem + kOffSfb + stage * kSfbBytes + b * 2048, sfb + (b * k4 + kb * 4) * 512, 2048,
                       &full[stage]);
         }
+        __syncwarp();
+        // gathered A: every lane copies its 4 rows (the byte count is in the expect_tx above)
+        if (gather) tma_gather4(smem + kOffA + stage * kABytes + lane * 512, &tmap_a, &full[stage], kb * (kBK / 2),
+                                rows4);
         __syncwarp();
         filled |= 1u << stage;
         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -460,8 +469,10 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
                      (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
   if (pair) return gemm_pair_launch(a, info.sms, dev, stream);
   CUtensorMap ma, mb;
-  if (!make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q, static_cast<uint64_t>(a.rows_max),
-                    static_cast<uint64_t>(a.K) / 2, 1, 128, kBM, true) ||
+  const bool gather = a.a_gather != nullptr;      // gathered A rows: a one-row box for tile::gather4
+  if (!make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q,
+                    static_cast<uint64_t>(gather ? a.a_rows : a.rows_max), static_cast<uint64_t>(a.K) / 2, 1, 128,
+                    gather ? 1 : kBM, true) ||
       !make_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_q, static_cast<uint64_t>(a.G) * a.N,
                     static_cast<uint64_t>(a.K) / 2, 1, 128, bn, true))
     return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: cuTensorMapEncodeTiled failed");
@@ -469,6 +480,8 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   Params p;
   p.a_sf = a.a_sf;
   p.b_sf = a.b_sf;
+  p.a_gather = a.a_gather;
+  p.a_rows = a.a_rows;
   p.offsets = a.offsets;
   p.counts = a.counts;
   p.G = a.offsets != nullptr ? a.G : 1;

@@ -78,6 +78,8 @@ struct PairCfg {
 struct PairParams {
   const uint8_t* a_sf;
   const uint8_t* b_sf;
+  const int32_t* a_gather;    // null, or the source row in A of every padded row
+  int64_t a_rows;
   const int32_t* offsets;
   const int32_t* counts;
   int32_t G, N, K;
@@ -289,15 +291,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t sfb_base = g * p.sfb_group_bytes + static_cast<int64_t>(2 * t.nt) * k4 * 512;
       // the even CTA always has rows; both CTAs load B and its scales
       const uint32_t tx = 2 * (kBBytes + kSfbBytes) + (kABytes + kSfaBytes) + (odd_rows ? kABytes + kSfaBytes : 0u);
+      const bool gather = p.a_gather != nullptr;
+      const int4 rows4 = gather && has_rows ? gather_rows4(p.a_gather, block, p.a_rows, p.err, lane)
+                                            : make_int4(0, 0, 0, 0);
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.err);
         if (!ok) break;
+        const uint32_t bar = leader_full + 8u * stage;
         if (elect_one()) {
-          const uint32_t bar = leader_full + 8u * stage;
           if (leader) mbar_arrive_expect_tx(&full[stage], tx);
           if (has_rows) {
-            tma_load_2d_pair(smem + C::kOffA + stage * kABytes, &tmap_a, bar, kb * (kBK / 2),
-                             static_cast<int32_t>(block * kBM));
+            if (!gather)
+              tma_load_2d_pair(smem + C::kOffA + stage * kABytes, &tmap_a, bar, kb * (kBK / 2),
+                               static_cast<int32_t>(block * kBM));
             tma_load_2d_pair(smem + C::kOffSfa + stage * kSfaBytes, &tmap_sfa, bar, 0, sfa_row + kb * 8);
           }
           tma_load_2d_pair(smem + C::kOffB + stage * kBBytes, &tmap_b, bar, kb * (kBK / 2),
@@ -307,6 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(smem + C::kOffSfb + stage * kSfbBytes + b * 2048, &tmap_sfb, bar, 0,
                              static_cast<int32_t>((sfb_base + (static_cast<int64_t>(b) * k4 + kb * 4) * 512) / kSfRow));
         }
+        __syncwarp();
+        // gathered A: every lane copies its 4 rows (the bytes are in the pair's expect_tx)
+        if (gather && has_rows)
+          tma_gather4_pair(smem + C::kOffA + stage * kABytes + lane * 512, &tmap_a, bar, kb * (kBK / 2), rows4);
         __syncwarp();
         filled |= 1u << stage;
         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -550,8 +560,10 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   CUtensorMap ma, mb, msa, msb, mo;
   const uint64_t sfa_bytes = static_cast<uint64_t>(a.rows_max / 128) * (a.K / 64) * 512;
   const uint64_t sfb_bytes = static_cast<uint64_t>(a.G) * (a.N / 128) * (a.K / 64) * 512;
-  bool ok = make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q, static_cast<uint64_t>(a.rows_max),
-                         static_cast<uint64_t>(a.K) / 2, 1, 128, 128, true) &&
+  const bool gather = a.a_gather != nullptr;      // gathered A rows: a one-row box for tile::gather4
+  bool ok = make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q,
+                         static_cast<uint64_t>(gather ? a.a_rows : a.rows_max), static_cast<uint64_t>(a.K) / 2, 1,
+                         128, gather ? 1 : 128, true) &&
             make_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_q, static_cast<uint64_t>(a.G) * a.N,
                          static_cast<uint64_t>(a.K) / 2, 1, 128, 128, true) &&
             make_tmap_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_sf, sfa_bytes / kSfRow, kSfRow, 1, kSfRow, 8,
@@ -569,6 +581,8 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   PairParams p;
   p.a_sf = a.a_sf;
   p.b_sf = a.b_sf;
+  p.a_gather = a.a_gather;
+  p.a_rows = a.a_rows;
   p.offsets = a.offsets;
   p.counts = a.counts;
   p.G = a.offsets != nullptr ? a.G : 1;

@@ -33,8 +33,9 @@ struct RouteBuffers {
   int32_t* offsets;
   int32_t* perm_token;
   int32_t* inv_perm;
-  uint8_t* a1_q;
+  uint8_t* a1_q;           // permuted rows (null: not written)
   uint8_t* a1_sf;
+  uint8_t* x_q;            // token-order rows of x (null: not written)
   const float* x_gscale;   // two-level encode scale of x (device scalar) or null
   int64_t rows_max;
   int32_t* chunk_hist;   // workspace: [n_chunks, E] expert counts per token chunk
@@ -55,6 +56,8 @@ struct GemmArgs {
   const uint8_t* a_q;
   const uint8_t* a_sf;
   int64_t rows_max;
+  const int32_t* a_gather;  // null, or the a_q row of every padded row (< 0: a zero-scale row)
+  int64_t a_rows;           // rows of a_q under a gather index
   const int32_t* offsets;
   const int32_t* counts;
   int32_t G, N, K;

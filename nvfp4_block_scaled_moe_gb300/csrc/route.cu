@@ -230,7 +230,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
                                                             int32_t k, const int32_t* __restrict__ inv_perm,
                                                             const float* __restrict__ gscale,
                                                             uint8_t* __restrict__ a_q,
-                                                            uint8_t* __restrict__ a_sf) {
+                                                            uint8_t* __restrict__ a_sf,
+                                                            uint8_t* __restrict__ x_q) {
   const int lane = threadIdx.x & 31;
   const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (seg * 1024 >= H) return;
@@ -272,19 +273,22 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
   const uint32_t word = codes | (__shfl_down_sync(0xFFFFFFFFu, codes, 1) << 16);
   const uint32_t k4 = static_cast<uint32_t>(c0 / 64);
   const uint32_t k4_total = static_cast<uint32_t>(H / 64);
+  // token-order rows (read by a gathering L1) and / or the permuted copies; the
+  // scale words always go to the permuted, padded layout
+  if (active && x_q != nullptr) *reinterpret_cast<uint4*>(x_q + t * (H / 2) + c0 / 2) = nib;
   for (int j = 0; j < k; ++j) {
     const int64_t r = __ldg(inv_perm + t * k + j);
     if (active) {
-      *reinterpret_cast<uint4*>(a_q + r * (H / 2) + c0 / 2) = nib;
+      if (a_q != nullptr) *reinterpret_cast<uint4*>(a_q + r * (H / 2) + c0 / 2) = nib;
       if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, k4, k4_total)) = word;
     }
   }
 }
 
 // -------------------------------------------------------------- pad fill --
-// Zero the nibbles and scale words of the padding rows [offsets[e] + counts[e],
-// offsets[e+1]) of every expert: blockIdx.y = expert, blockIdx.x strides over its
-// padding (at most 127 rows).
+// Zero the scale words (and, when the permuted copy is written, the nibbles) of
+// the padding rows [offsets[e] + counts[e], offsets[e+1]) of every expert:
+// blockIdx.y = expert, blockIdx.x strides over its padding (at most 127 rows).
 __global__ void __launch_bounds__(256) route_padfill_kernel(const int32_t* __restrict__ counts,
                                                             const int32_t* __restrict__ offsets, int32_t H,
                                                             uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf) {
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(256) route_padfill_kernel(const int32_t* __res
   const int64_t hi = __ldg(offsets + e + 1);
   const int n16 = H / 32;                 // 16-byte chunks per row
   const int k4_total = H / 64;
-  const int64_t nq = (hi - lo) * n16;
+  const int64_t nq = a_q != nullptr ? (hi - lo) * n16 : 0;     // no permuted copy: scales only
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int64_t i = first; i < nq; i += stride) {
@@ -329,7 +333,7 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
     const int warps = static_cast<int>(segs < 8 ? segs : 8);     // no idle warps on short rows
     const dim3 grid(static_cast<unsigned>(b.T), static_cast<unsigned>((segs + warps - 1) / warps));
     route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k,
-                                                          b.inv_perm, b.x_gscale, b.a1_q, b.a1_sf);
+                                                          b.inv_perm, b.x_gscale, b.a1_q, b.a1_sf, b.x_q);
   }
   return cudaGetLastError();
 }

@@ -61,20 +61,20 @@ extern "C" nvfp4_status moe_route_permute_static(const float* logits, const void
                                                   int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
                                                   int32_t* expert_counts, int32_t* expert_offsets,
                                                   int32_t* perm_token, int32_t* inv_perm, uint8_t* a1_q,
-                                                  uint8_t* a1_sf, const float* x_global_scale,
+                                                  uint8_t* a1_sf, uint8_t* x_q, const float* x_global_scale,
                                                   nvfp4_stream_t stream) {
   if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: T=%d", T);
   if (!expert_counts || !expert_offsets)
     return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: null pointer");
-  if (T > 0 && !(logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_q && a1_sf))
-    return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: null pointer");
+  if (T > 0 && !(logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_sf && (a1_q || x_q)))
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: null pointer (a1_q and x_q may not both be null)");
   if (E < 1 || E > 1024) return fail(NVFP4_ERR_UNSUPPORTED, "moe_route_permute_static: E=%d outside [1, 1024]", E);
   if (top_k < 1 || top_k > E || top_k > 32)
     return fail(NVFP4_ERR_UNSUPPORTED, "moe_route_permute_static: top_k=%d outside [1, min(E, 32)]", top_k);
   if (H <= 0 || H % 64 != 0)
     return fail(NVFP4_ERR_UNSUPPORTED, "moe_route_permute_static: H=%d is not a positive multiple of 64", H);
   const uintptr_t mis = reinterpret_cast<uintptr_t>(x_bf16) | reinterpret_cast<uintptr_t>(a1_q) |
-                        reinterpret_cast<uintptr_t>(a1_sf);
+                        reinterpret_cast<uintptr_t>(a1_sf) | reinterpret_cast<uintptr_t>(x_q);
   if (T > 0 && (mis & 15u) != 0)
     return fail(NVFP4_ERR_ALIGNMENT, "moe_route_permute_static: x, a1_q and a1_sf must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(x_global_scale) & 3u) != 0)
@@ -104,6 +104,7 @@ extern "C" nvfp4_status moe_route_permute_static(const float* logits, const void
   b.inv_perm = inv_perm;
   b.a1_q = a1_q;
   b.a1_sf = a1_sf;
+  b.x_q = x_q;
   b.x_gscale = x_global_scale;
   b.rows_max = moe_padded_rows_max(T, E, top_k);
   route_carve_workspace(b, ws);

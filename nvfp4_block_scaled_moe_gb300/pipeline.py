@@ -36,9 +36,11 @@ class MoeShape:
 
 
 class MoeBuffers:
-    """Every output and intermediate of one forward, sized for the worst case."""
+    """Every output and intermediate of one forward, sized for the worst case.
+    gather: the routing call writes x's NVFP4 rows once in token order (x_q) and
+    L1 gathers its A rows through perm_token, instead of a permuted copy a1_q."""
 
-    def __init__(self, s: MoeShape, device="cuda"):
+    def __init__(self, s: MoeShape, device="cuda", gather: bool = False):
         u8, i32, f32 = torch.uint8, torch.int32, torch.float32
         R = max(s.rows_max, 128)
         self.shape = s
@@ -49,7 +51,9 @@ class MoeBuffers:
         self.offsets = torch.empty(s.E + 1, dtype=i32, device=device)
         self.perm_token = torch.empty(R, dtype=i32, device=device)
         self.inv_perm = torch.empty((s.T, s.top_k), dtype=i32, device=device)
-        self.a1_q = torch.empty((R, s.H // 2), dtype=u8, device=device)
+        self.gather = gather
+        self.a1_q = None if gather else torch.empty((R, s.H // 2), dtype=u8, device=device)
+        self.x_q = torch.empty((max(s.T, 1), s.H // 2), dtype=u8, device=device) if gather else None
         self.a1_sf = torch.empty(sf_bytes(R, s.H), dtype=u8, device=device)
         self.a2_q = torch.empty((R, s.I // 2), dtype=u8, device=device)
         self.a2_sf = torch.empty(sf_bytes(R, s.I), dtype=u8, device=device)
@@ -62,7 +66,7 @@ class MoeBuffers:
 
     def enable_h_debug(self):
         # zeros: the GEMM writes h only for real rows
-        self.h_debug = torch.zeros((self.rows_max, self.shape.I), dtype=torch.float32, device=self.a2_q.device)
+        self.h_debug = torch.zeros((self.rows_max, self.shape.I), dtype=torch.float32, device=self.a2_sf.device)
 
 
 class MoeWeights:
@@ -155,13 +159,15 @@ def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuff
             nvfp4_global_scale(x, b.x_gs)
         x_gs = b.x_gs
     moe_route_permute(logits, x, s.top_k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
-                      b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_global_scale=x_gs)
+                      b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_global_scale=x_gs, x_q=b.x_q)
     if s.T > 0:
-        nvfp4_moe_ffn_forward(b.a1_q, b.a1_sf, b.offsets, b.counts, s.E, s.H, s.I, b.rows_max, w.w1_q, w.w1_sf,
-                              w.w2_q, w.w2_sf, alpha1, alpha2, b.a2_q, b.a2_sf, b.rows_out, b.h_debug,
-                              x_global_scale=x_gs, w1_global_scale=w.w1_gs if two_level else None,
+        gather = dict(a1_gather=b.perm_token, a1_gather_rows=s.T) if b.gather else {}
+        nvfp4_moe_ffn_forward(b.x_q if b.gather else b.a1_q, b.a1_sf, b.offsets, b.counts, s.E, s.H, s.I,
+                              b.rows_max, w.w1_q, w.w1_sf, w.w2_q, w.w2_sf, alpha1, alpha2, b.a2_q, b.a2_sf,
+                              b.rows_out, b.h_debug, x_global_scale=x_gs,
+                              w1_global_scale=w.w1_gs if two_level else None,
                               a2_global_scale=b.a2_gs if two_level else None,
-                              w2_global_scale=w.w2_gs if two_level else None)
+                              w2_global_scale=w.w2_gs if two_level else None, **gather)
         shared_rows = None if shared is None else shared.forward(x, alpha1, alpha2)
         moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y, shared=shared_rows)
     return b.y

@@ -79,17 +79,26 @@ def test_host_validation_without_gpu(lib):
     assert lib.nvfp4_global_scale(p, 0, 4, 16, 16, vp(base + 2), None) == 3
     assert lib.nvfp4_sf_swizzle(p, 4, 4, 0, 1, p, 0, None) == 1
     # K not a multiple of 256; N not a multiple of 128 (BF16) / 256 (SwiGLU); G without offsets
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 200, p, p, 1.0, None, None, None, 1, None, None, p, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 192, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, None, None, None, 0, p, p, None, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 7, None, None, p, None, None) == 1
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 200, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 192, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, None, None, None, 0, p, p, None, None, None, 0, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 7, None, None, p, None, None, 0, None) == 1
     # routing limits
-    assert lib.moe_route_permute(p, p, 8, 64, 2000, 2, p, p, p, p, p, p, p, p, None, p, 1 << 20, None) == 2
-    assert lib.moe_route_permute(p, p, 8, 64, 8, 9, p, p, p, p, p, p, p, p, None, p, 1 << 20, None) == 2
-    assert lib.moe_route_permute(p, p, 8, 60, 8, 2, p, p, p, p, p, p, p, p, None, p, 1 << 20, None) == 2
-    assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, p, p, None, p, 16, None) == 1
-    assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None) == 2
+    assert lib.moe_route_permute(p, p, 8, 64, 2000, 2, p, p, p, p, p, p, p, p, None, None, p, 1 << 20, None) == 2
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 9, p, p, p, p, p, p, p, p, None, None, p, 1 << 20, None) == 2
+    assert lib.moe_route_permute(p, p, 8, 60, 8, 2, p, p, p, p, p, p, p, p, None, None, p, 1 << 20, None) == 2
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, p, p, None, None, p, 16, None) == 1
+    # neither permuted rows nor token-order rows requested; misaligned token-order rows
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, None, p, None, None, p, 1 << 20, None) == 1
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, None, p, vp(base + 4), None, p, 1 << 20,
+                                 None) == 3
+    # gathered A: a row count is required, the index must be 16-byte aligned
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
+                                  None, p, 0, None) == 1
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
+                                  None, vp(base + 4), 64, None) == 3
+    assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None, 0, None) == 2
     assert lib.moe_combine(p, p, p, 4, 12, 2, None, p, None) == 2
     assert lib.moe_combine(p, p, p, 4, 16, 2, vp(base + 8), p, None) == 3     # misaligned shared rows
     assert lib.nvfp4_selftest_bounded_wait(None, 10, None) == 1

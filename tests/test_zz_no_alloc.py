@@ -66,6 +66,6 @@ def test_static_scratch_rejects_problems_beyond_its_array():
     buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     p = buf.data_ptr()
     # 2^20 tokens over 1024 experts need 32 MiB of chunk histograms: more than the fixed 16 MiB
-    st = lib.moe_route_permute_static(p, p, 1 << 20, 7168, 1024, 8, p, p, p, p, p, p, p, p, None, None)
+    st = lib.moe_route_permute_static(p, p, 1 << 20, 7168, 1024, 8, p, p, p, p, p, p, p, p, None, None, None)
     assert st == 2
     assert b"scratch" in lib.nvfp4_last_error()
