@@ -250,7 +250,8 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *               perm_token over its x_q).  An entry < 0 marks a row whose scales
  *               in a_sf are zero (group padding) and reads row 0; an entry past
  *               the end reads row 0 and sets the device error word.  a_sf keeps
- *               the rows_max-row layout.
+ *               the rows_max-row layout.  Supported with NVFP4_EPI_SWIGLU_NVFP4
+ *               (the L1 GEMM); NVFP4_ERR_UNSUPPORTED otherwise.
  *   epilogue    NVFP4_EPI_SWIGLU_NVFP4: N columns interleaved 8|8 as gate/up;
  *               h = silu(alpha*g) * (alpha*u) quantised as in nvfp4_quantize ->
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)

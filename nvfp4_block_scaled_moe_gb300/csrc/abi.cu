@@ -204,6 +204,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
   CHECK_ARG(!a_gather || (a_gather_rows > 0 && a_gather_rows < (int64_t(1) << 31)),
             "nvfp4_grouped_gemm: a_gather_rows=%lld", (long long)a_gather_rows);
   CHECK_AL(al16(a_gather), "nvfp4_grouped_gemm: a_gather not 16-byte aligned");
+  CHECK_SUP(!a_gather || epilogue == NVFP4_EPI_SWIGLU_NVFP4,
+            "nvfp4_grouped_gemm: gathered A rows are supported with the SwiGLU + NVFP4 epilogue (L1)");
   CHECK_ARG(epilogue == NVFP4_EPI_SWIGLU_NVFP4 || epilogue == NVFP4_EPI_BF16 || epilogue == NVFP4_EPI_SWIGLU_BF16,
             "nvfp4_grouped_gemm: bad epilogue");
   CHECK_ARG(epilogue != NVFP4_EPI_SWIGLU_NVFP4 || (out_q && out_sf), "nvfp4_grouped_gemm: null NVFP4 output");

@@ -171,7 +171,9 @@ __device__ __forceinline__ void epilogue_bf16(const float (&v)[kChunks][32], flo
   }
 }
 
-template <int kEpi, int BN>
+// kGather: A rows come through p.a_gather (tile::gather4); a separate
+// instantiation, so the default kernels carry none of its code.
+template <int kEpi, int BN, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const Params p) {
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = __shfl_sync(0xFFFFFFFFu, find_group(s_off, p.G, mt * kBM), 0);
       const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
       const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(kBands * nt) * k4) * 512;
-      const bool gather = p.a_gather != nullptr;
+      constexpr bool gather = kGather;
       const int4 rows4 = gather ? gather_rows4(p.a_gather, mt, p.a_rows, p.err, lane) : make_int4(0, 0, 0, 0);
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.err);
@@ -265,9 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // gathered A: every lane copies its 4 rows (the byte count is in the expect_tx above)
-        if (gather) tma_gather4(smem + kOffA + stage * kABytes + lane * 512, &tmap_a, &full[stage], kb * (kBK / 2),
-                                rows4);
-        __syncwarp();
+        if constexpr (gather) {
+          tma_gather4(smem + kOffA + stage * kABytes + lane * 512, &tmap_a, &full[stage], kb * (kBK / 2), rows4);
+          __syncwarp();
+        }
         filled |= 1u << stage;
         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -418,7 +421,7 @@ std::atomic<int> g_gemm_tiles{NVFP4_GEMM_TILES_AUTO};
 
 struct DeviceInfo {
   int sms = 0;
-  bool attr_set[4] = {false, false, false, false};
+  bool attr_set[5] = {false, false, false, false, false};
 };
 
 DeviceInfo& device_info(int dev) {
@@ -430,17 +433,19 @@ DeviceInfo& device_info(int dev) {
   return d;
 }
 
-template <int kEpi, int BN>
+template <int kEpi, int BN, bool kGather = false>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t stream,
                    DeviceInfo& info) {
-  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_SWIGLU_BF16 ? 3 : (BN == 256 ? 1 : 2);
+  constexpr int slot = kGather ? 4
+                       : kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_SWIGLU_BF16 ? 3 : (BN == 256 ? 1 : 2);
   if (!info.attr_set[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_kernel<kEpi, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_kernel<kEpi, BN, kGather>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg<BN>::kSmemBytes));
     if (e != cudaSuccess) return e;
     info.attr_set[slot] = true;
   }
-  nvf4_gemm_kernel<kEpi, BN><<<grid, kThreads, Cfg<BN>::kSmemBytes, stream>>>(ma, mb, p);
+  nvf4_gemm_kernel<kEpi, BN, kGather><<<grid, kThreads, Cfg<BN>::kSmemBytes, stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
@@ -504,7 +509,8 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   const int64_t max_tiles = (a.rows_max / kBM) * p.n_tiles;
   const int grid = static_cast<int>(max_tiles < info.sms ? max_tiles : info.sms);
   if (grid <= 0) return NVFP4_OK;
-  e = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? launch<NVFP4_EPI_SWIGLU_NVFP4, 256>(ma, mb, p, grid, stream, info)
+  e = gather                                ? launch<NVFP4_EPI_SWIGLU_NVFP4, 256, true>(ma, mb, p, grid, stream, info)
+      : a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? launch<NVFP4_EPI_SWIGLU_NVFP4, 256>(ma, mb, p, grid, stream, info)
       : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? launch<NVFP4_EPI_SWIGLU_BF16, 256>(ma, mb, p, grid, stream, info)
       : bn == 256                           ? launch<NVFP4_EPI_BF16, 256>(ma, mb, p, grid, stream, info)
                                             : launch<NVFP4_EPI_BF16, 128>(ma, mb, p, grid, stream, info);

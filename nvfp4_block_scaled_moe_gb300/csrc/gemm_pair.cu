@@ -183,7 +183,9 @@ __device__ __forceinline__ void swiglu_row(const float (&v)[4][32], float alpha,
 // run of four atoms is a box of 8 rows.
 constexpr int kSfRow = 256;
 
-template <int kEpi>
+// kGather: A rows come through p.a_gather (tile::gather4); a separate
+// instantiation, so the default kernels carry none of its code.
+template <int kEpi, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t sfb_base = g * p.sfb_group_bytes + static_cast<int64_t>(2 * t.nt) * k4 * 512;
       // the even CTA always has rows; both CTAs load B and its scales
       const uint32_t tx = 2 * (kBBytes + kSfbBytes) + (kABytes + kSfaBytes) + (odd_rows ? kABytes + kSfaBytes : 0u);
-      const bool gather = p.a_gather != nullptr;
+      constexpr bool gather = kGather;
       const int4 rows4 = gather && has_rows ? gather_rows4(p.a_gather, block, p.a_rows, p.err, lane)
                                             : make_int4(0, 0, 0, 0);
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
@@ -315,9 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // gathered A: every lane copies its 4 rows (the bytes are in the pair's expect_tx)
-        if (gather && has_rows)
+        if (kGather && has_rows) {
           tma_gather4_pair(smem + C::kOffA + stage * kABytes + lane * 512, &tmap_a, bar, kb * (kBK / 2), rows4);
-        __syncwarp();
+          __syncwarp();
+        }
         filled |= 1u << stage;
         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -497,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct PairDeviceInfo {
-  bool attr_set[3] = {false, false, false};
-  int max_clusters[3] = {0, 0, 0};
+  bool attr_set[4] = {false, false, false, false};
+  int max_clusters[4] = {0, 0, 0, 0};
 };
 
 PairDeviceInfo& pair_info(int dev) {
@@ -511,11 +514,11 @@ std::mutex& pair_mutex() {
   return mu;
 }
 
-template <int kEpi>
+template <int kEpi, bool kGather = false>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2;
+  constexpr int slot = kGather ? 3 : kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2;
   constexpr uint32_t smem = PairCfg<kEpi>::kSmemBytes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -533,12 +536,12 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     std::lock_guard<std::mutex> lock(pair_mutex());
     PairDeviceInfo& info = pair_info(dev);
     if (!info.attr_set[slot]) {
-      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather>, &cfg);
       if (e != cudaSuccess) return e;
       info.max_clusters[slot] = n;
       info.attr_set[slot] = true;
@@ -549,7 +552,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   int64_t clusters = max_clusters < num_tiles ? max_clusters : num_tiles;
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi>, ma, mb, msa, msb, mo, p);
+  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather>, ma, mb, msa, msb, mo, p);
 }
 
 }  // namespace
@@ -608,7 +611,8 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   const int64_t max_tiles = max_pairs * p.n_tiles;
   if (max_tiles <= 0) return NVFP4_OK;
   const cudaError_t e =
-      swiglu ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
+      gather   ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4, true>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
+      : swiglu ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
       : a.epilogue == NVFP4_EPI_SWIGLU_BF16
           ? launch_pair<NVFP4_EPI_SWIGLU_BF16>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
           : launch_pair<NVFP4_EPI_BF16>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream);

@@ -98,6 +98,9 @@ def test_host_validation_without_gpu(lib):
                                   None, p, 0, None) == 1
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
                                   None, vp(base + 4), 64, None) == 3
+    # gathered A with an epilogue other than SwiGLU + NVFP4 (the L1 GEMM's) is not built
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
+                                  None, p, 64, None) == 2
     assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None, 0, None) == 2
     assert lib.moe_combine(p, p, p, 4, 12, 2, None, p, None) == 2
     assert lib.moe_combine(p, p, p, 4, 16, 2, vp(base + 8), p, None) == 3     # misaligned shared rows
