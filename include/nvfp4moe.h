@@ -83,8 +83,10 @@ typedef enum {
 typedef enum {
   NVFP4_GEMM_TILES_AUTO = 0,   /* by shape: CTA pairs when groups average >= 256 rows */
   NVFP4_GEMM_TILES_SINGLE = 1, /* one CTA per 128-row tile */
-  NVFP4_GEMM_TILES_PAIR = 2    /* two CTAs (a cluster) per 256-row tile, where N % 256 == 0
+  NVFP4_GEMM_TILES_PAIR = 2,   /* two CTAs (a cluster) per 256-row tile, where N % 256 == 0
                                   and G <= 512 */
+  NVFP4_GEMM_TILES_QUAD = 3    /* clusters of two such pairs side by side along N, sharing
+                                  the A rows, where also N % 512 == 0 (else as _PAIR) */
 } nvfp4_gemm_tiles;
 
 /* Bytes of a swizzled SF buffer for a rows x cols matrix (cols in elements):
@@ -279,8 +281,9 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
 /* ---------------------------------------------------------------------------
  * nvfp4_set_gemm_tiles -- process-wide choice of nvfp4_grouped_gemm's tile kernel
  * (also used by nvfp4_moe_ffn_forward): NVFP4_GEMM_TILES_AUTO (the default),
- * _SINGLE or _PAIR (_PAIR falls back to single CTAs where N % 256 != 0 or
- * G > 512).  A
+ * _SINGLE, _PAIR or _QUAD (_PAIR and _QUAD fall back to single CTAs where
+ * N % 256 != 0 or G > 512; _QUAD falls back to lone pairs where N % 512 != 0
+ * or A rows are gathered; _AUTO never uses _QUAD's clusters).  A
  * tuning and testing control with no counterpart in the source pages; results
  * do not depend on it.  Takes effect for calls made after it returns;
  * NVFP4_ERR_INVALID_ARG for another value.

@@ -106,9 +106,9 @@ def test_host_validation_without_gpu(lib):
     assert lib.moe_combine(p, p, p, 4, 16, 2, vp(base + 8), p, None) == 3     # misaligned shared rows
     assert lib.nvfp4_selftest_bounded_wait(None, 10, None) == 1
     assert b"selftest" in lib.nvfp4_last_error()
-    # tile-kernel choice: three modes, anything else refused; the default restored
-    assert lib.nvfp4_set_gemm_tiles(3) == 1 and lib.nvfp4_set_gemm_tiles(-1) == 1
-    for mode in (2, 1, 0):
+    # tile-kernel choice: four modes, anything else refused; the default restored
+    assert lib.nvfp4_set_gemm_tiles(4) == 1 and lib.nvfp4_set_gemm_tiles(-1) == 1
+    for mode in (3, 2, 1, 0):
         assert lib.nvfp4_set_gemm_tiles(mode) == 0
     with pytest.raises(nv.Nvfp4Error) as ei:
         nv._check(2)

@@ -62,13 +62,15 @@ def _tiles(nv, mode):
 
 
 def _both_kernels(nv, run):
-    """run() -> tuple of host arrays, on each tile kernel; asserts they are identical."""
+    """run() -> tuple of host arrays, on each tile kernel (single CTAs, lone CTA
+    pairs, two-pair clusters where N allows); asserts they are identical."""
     outs = []
-    for mode in (nv.GEMM_TILES_SINGLE, nv.GEMM_TILES_PAIR):
+    for mode in (nv.GEMM_TILES_SINGLE, nv.GEMM_TILES_PAIR, nv.GEMM_TILES_QUAD):
         with _tiles(nv, mode):
             outs.append(run())
-    for a, b in zip(*outs):
-        assert np.array_equal(a, b), "single-CTA and CTA-pair kernels differ"
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert np.array_equal(a, b), "the tile kernels differ"
     return outs[0]
 
 
