@@ -402,9 +402,11 @@ def _flush_l2(buf):
 
 
 def run_dense(args, world: int, rank: int, local: int) -> None:
-    """The single-expert dense L1: A 8192 x 7168 x B 4096 x 7168 NVFP4 with the fused
-    SwiGLU + NVFP4 epilogue -> 8192 x 2048 NVFP4.  Inputs (44 MB) fit in L2, so L2 is
-    flushed between steps and each step is timed by its own CUDA events."""
+    """One dense NVFP4 GEMM: the single-expert L1 (A 8192 x 7168 x B 4096 x 7168 with
+    the fused SwiGLU + NVFP4 epilogue -> 8192 x 2048 NVFP4), or with --workload
+    dense_l2 the prefill batch's L2 shape as one group (A 16384 x 2048 x B 7168 x 2048
+    -> 16384 x 7168 BF16).  Inputs fit in L2, so L2 is flushed between steps and each
+    step is timed by its own CUDA events."""
     import torch
 
     import nvfp4_block_scaled_moe_gb300 as nv
@@ -412,8 +414,9 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
 
     nvbuild.build()
     torch.cuda.set_device(local)
-    spec = dict(inputs.CONFIGS["dense"])
+    spec = dict(inputs.CONFIGS[args.workload])
     M, N, K = spec["M"], spec["N"], spec["K"]
+    bf16_out = spec.get("epilogue") == "bf16"
     a, bw = inputs.dense_inputs(spec)
     a_d, b_d = torch.from_numpy(a).cuda(), torch.from_numpy(bw).cuda()
     a_q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
@@ -425,12 +428,17 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
     del a_d, b_d
     out_q = torch.empty((M, N // 4), dtype=torch.uint8, device="cuda")
     out_sf = torch.empty(nv.sf_bytes(M, N // 2), dtype=torch.uint8, device="cuda")
+    out_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda") if bf16_out else None
     flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step():
-        nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_SWIGLU_NVFP4,
-                              out_q=out_q, out_sf=out_sf)
+        if bf16_out:
+            nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_BF16,
+                                  out_bf16=out_bf16)
+        else:
+            nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_SWIGLU_NVFP4,
+                                  out_q=out_q, out_sf=out_sf)
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
@@ -465,10 +473,12 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> fp32 accum", "data": "synthetic",
-        "config": {"workload": f"dense NVFP4 GEMM M={M} N={N} K={K} + SwiGLU + NVFP4 requant",
+        "config": {"workload": f"dense NVFP4 GEMM M={M} N={N} K={K} + "
+                               + ("BF16 output" if bf16_out else "SwiGLU + NVFP4 requant"),
                    "l2_policy": "L2 flushed (256 MiB write) before every step; per-step CUDA events",
                    "launch": "each step a one-launch CUDA graph replayed after the flush"},
-        "roofline": {"kernel": "nvf4_gemm_pair_kernel<0> (SwiGLU + NVFP4 epilogue, CTA pairs)", "bound": "tensor",
+        "roofline": {"kernel": ("nvf4_gemm_pair_kernel<1> (BF16 epilogue, CTA pairs)" if bf16_out else
+                                "nvf4_gemm_pair_kernel<0> (SwiGLU + NVFP4 epilogue, CTA pairs)"), "bound": "tensor",
                      "achieved": tflops,
                      "peak": fp4_peak, "unit": "TFLOP/s", "frac": tflops / fp4_peak,
                      "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} x {FP4_OVER_BF16:g}",
@@ -556,16 +566,17 @@ def main():
     ap.add_argument("--two-level", action="store_true",
                     help="prefill/decode with the two-level scale (per-tensor encode scales next to the per-16 "
                          "ones); the CPU baseline stays the one-level oracle")
-    ap.add_argument("--workload", choices=("prefill", "decode", "dense", "quantizer"), default=WORKLOAD,
+    ap.add_argument("--workload", choices=("prefill", "decode", "dense", "dense_l2", "quantizer"), default=WORKLOAD,
                     help="prefill (default) and decode time the whole MoE FFN step; dense times the L1 GEMM of "
-                         "one 8192-row expert; quantizer the standalone SwiGLU + NVFP4 quantiser")
+                         "one 8192-row expert, dense_l2 the prefill L2 GEMM shape as one group; quantizer the "
+                         "standalone SwiGLU + NVFP4 quantiser")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
-    elif args.workload == "dense":
+    elif args.workload in ("dense", "dense_l2"):
         run_dense(args, world, rank, local)
     elif args.workload == "quantizer":
         run_quantizer(args, world, rank, local)

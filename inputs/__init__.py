@@ -43,6 +43,8 @@ CONFIGS = {
     "tiny": dict(kind="moe", T=128, H=512, I=256, E=8, top_k=2, seed=0, zipf=False),
     "quantizer": dict(kind="quant", rows=32768, cols=2048, seed=1),
     "dense": dict(kind="dense", M=8192, N=4096, K=7168, seed=2),
+    # the prefill batch's L2 GEMM as one dense group: 16384 rows x H=7168 x I=2048, BF16 out
+    "dense_l2": dict(kind="dense", M=16384, N=7168, K=2048, seed=5, epilogue="bf16"),
     "decode": dict(kind="moe", T=256, H=7168, I=2048, E=256, top_k=8, seed=3, zipf=False),
     "prefill": dict(kind="moe", T=16384, H=7168, I=2048, E=256, top_k=8, seed=4, zipf=True),
 }

@@ -41,25 +41,37 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 256;        // rows per CTA, columns, K per stage
+constexpr int kBM = 128, kBK = 256;                    // rows per CTA, K per stage
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxGroups = kPairMaxGroups;             // larger G uses the single-CTA kernel
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
-constexpr uint32_t kBBytes = 128 * kBK / 2;            // 16 KiB: this CTA's 128 B rows
 constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms
-constexpr uint32_t kSfbBytes = kBN * (kBK / 16);       // 4 KiB: 2 bands x 4 atoms
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemSf = kBN;                      // scale columns follow the accumulator
-constexpr uint32_t kTmemSfStage = 16 + 32;             // A: 4 atoms x 4 columns; B: 2 bands x 16
 
+// A pair tile is 256 rows x kBNP columns.  kBNP = 256: one accumulator of 256
+// TMEM columns per CTA (a second does not fit beside the scale factors), so the
+// MMAs of the next tile wait for the epilogue to drain it.  kBNP = 128 (BF16
+// epilogue only): two accumulators of 128 columns, so the next tile's MMAs run
+// while the epilogue drains the last one, at the price of more operand traffic
+// per output (each CTA loads 64 B rows per 128 columns instead of 128 per 256).
+//
 // Per epilogue: the staging buffer of one warp's output slice.
 //   SwiGLU: 32 rows x 32 bytes of nibbles (one 1 KiB TMA-store box per tile);
 //   BF16:   32 rows x 64 columns (4 KiB, 16-byte chunks XOR-swizzled by row).
-template <int kEpi>
+template <int kEpi, int kBNP>
 struct PairCfg {
+  static_assert(kBNP == 256 || (kBNP == 128 && kEpi == NVFP4_EPI_BF16), "tile widths");
   static constexpr bool kSwiglu = kEpi == NVFP4_EPI_SWIGLU_NVFP4;
-  static constexpr int kStages = 5;
+  static constexpr int kBN = kBNP;                                   // columns of a pair tile
+  static constexpr int kAcc = kBNP == 256 ? 1 : 2;                   // accumulators in TMEM
+  static constexpr int kBands = kBNP / 128;                          // 128-row bands of B's scale atoms
+  static constexpr int kChunks = kBNP / 64;                          // 32-column chunks per epilogue warp
+  static constexpr uint32_t kBBytes = (kBNP / 2) * kBK / 2;          // this CTA's half of the B rows
+  static constexpr uint32_t kSfbBytes = kBNP * (kBK / 16);           // scale atoms of every B row
+  static constexpr uint32_t kTmemSf = kAcc * kBNP;                   // scale columns follow the accumulators
+  static constexpr uint32_t kTmemSfStage = 16 + 16 * kBands;         // A: 4 atoms x 4 columns; B: 4 per band
+  static constexpr int kStages = kBNP == 256 ? 5 : 6;
   static constexpr uint32_t kStageBufBytes = kSwiglu ? 1024 : 4096;
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
@@ -67,7 +79,7 @@ struct PairCfg {
   static constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
   static constexpr uint32_t kOffOut = kOffSfb + kStages * kSfbBytes;
   static constexpr uint32_t kOffBar = kOffOut + kEpiWarps * kStageBufBytes;
-  static constexpr uint32_t kNumBars = 2 * kStages + 3;                    // full, empty, tfull, tempty, drain
+  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kAcc + 1;         // full, empty, tfull, tempty, drain
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;             // tmem slot, abort flag
   static constexpr uint32_t kOffGroups = kOffMisc + 16;                    // row offsets, then pair prefix
   static constexpr uint32_t kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4;
@@ -188,18 +200,22 @@ __device__ __forceinline__ void swiglu_row(const float (&v)[4][32], float alpha,
 constexpr int kSfRow = 256;
 
 // kGather: A rows come through p.a_gather (tile::gather4); a separate
-// instantiation, so the default kernels carry none of its code.
+// instantiation, so the default kernels carry none of its code.  kBNP: the pair
+// tile's columns (see PairCfg).
 // kPairs = 2: clusters of two pairs (4 CTAs) side by side along N.  Both pairs
 // multiply the same A rows, so each CTA loads half of its 128 A rows (and half
 // of their scale atoms) and multicasts them to its counterpart in the other
 // pair: a third less operand traffic per SM than a lone pair.
-template <int kEpi, bool kGather, int kPairs>
+template <int kEpi, bool kGather, int kPairs, int kBNP>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                           const __grid_constant__ CUtensorMap tmap_out, const PairParams p) {
-  using C = PairCfg<kEpi>;
-  constexpr int kStages = C::kStages;
+  using C = PairCfg<kEpi, kBNP>;
+  constexpr int kStages = C::kStages, kAcc = C::kAcc, kBN = C::kBN, kBands = C::kBands;
+  constexpr uint32_t kBBytes = C::kBBytes, kSfbBytes = C::kSfbBytes;
+  constexpr uint32_t kTmemSf = C::kTmemSf, kTmemSfStage = C::kTmemSfStage;
+  static_assert(kPairs == 1 || kBNP == 256, "two-pair clusters use 256-column pair tiles");
   extern __shared__ __align__(1024) uint8_t smem[];
   // the swizzled tiles need a 1 KiB-aligned base; every CTA sees the same base,
   // so a misaligned one stops all of them here, before any pair traffic
@@ -210,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* drain = tempty + 1;
+  uint64_t* tempty = tfull + kAcc;
+  uint64_t* drain = tempty + kAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + C::kOffGroups);
@@ -230,8 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);                // the even CTA's: expect_tx of the pair's bytes
       mbar_init(&empty[s], kPairs);          // every pair's MMA commit: the stage is refilled across pairs
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, 2 * kEpiWarps);          // every epilogue warp of both CTAs (used on the even CTA)
+    for (int a = 0; a < kAcc; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * kEpiWarps);    // every epilogue warp of both CTAs (used on the even CTA)
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -301,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool odd_rows = __shfl_sync(0xFFFFFFFFu, odd.has_rows, 0);
       // SF rows (256 bytes) of this block's A atoms and of the tile's two B bands
       const int32_t sfa_row = static_cast<int32_t>(block * k4 * (512 / kSfRow));
-      const int64_t sfb_base = g * p.sfb_group_bytes + static_cast<int64_t>(2 * t.nt) * k4 * 512;
+      const int64_t sfb_base = g * p.sfb_group_bytes + static_cast<int64_t>(kBands * t.nt) * k4 * 512;
       // the even CTA always has rows; both CTAs load B and its scales
       const uint32_t tx = 2 * (kBBytes + kSfbBytes) + (kABytes + kSfaBytes) + (odd_rows ? kABytes + kSfaBytes : 0u);
       constexpr bool gather = kGather;
@@ -329,12 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tma_load_2d_pair(smem + C::kOffB + stage * kBBytes, &tmap_b, bar, kb * (kBK / 2),
-                           g * p.N + t.nt * kBN + static_cast<int32_t>(rank) * 128);
-          // B's scale bands: this CTA loads band `rank` into both CTAs of the pair
-          tma_load_2d_pair_mc(smem + C::kOffSfb + stage * kSfbBytes + rank * 2048, &tmap_sfb, bar, 0,
-                              static_cast<int32_t>((sfb_base + (static_cast<int64_t>(rank) * k4 + kb * 4) * 512) /
-                                                   kSfRow),
-                              pair_mask);
+                           g * p.N + t.nt * kBN + static_cast<int32_t>(rank) * (kBN / 2));
+          // B's scale atoms: this CTA loads half of them (band `rank` of two, or
+          // atoms 2*rank, +1 of one band) into both CTAs of the pair
+          const int64_t sfb_src = kBands == 2 ? (static_cast<int64_t>(rank) * k4 + kb * 4) * 512
+                                              : (static_cast<int64_t>(kb) * 4 + 2 * rank) * 512;
+          tma_load_2d_pair_mc(smem + C::kOffSfb + stage * kSfbBytes + rank * (kSfbBytes / 2), &tmap_sfb, bar, 0,
+                              static_cast<int32_t>((sfb_base + sfb_src) / kSfRow), pair_mask);
         }
         __syncwarp();
         // gathered A: every lane copies its 4 rows (the bytes are in the pair's expect_tx)
@@ -364,12 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && leader) {
     // ---------------------------------------------------- MMA issuer (pair)
     constexpr uint32_t idesc = idesc_nvf4(2 * kBM, kBN);
-    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t tile = cluster_id; tile < tiles_u && ok; tile += n_clusters) {
-      ok = mbar_wait_warp(tempty, acc_phase ^ 1u, abort_flag, p.err);
+      ok = mbar_wait_warp(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err);
       if (!ok) break;
       tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_u + acc * kBN;
       for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
         ok = mbar_wait_warp(&full[stage], phase, abort_flag, p.err);
         if (!ok) break;
@@ -385,11 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) {
             tc_copy_sf_pair(sfa_t + 4 * j, sdesc_sf(sfa_s + 512 * j));
 #pragma unroll
-            for (int b = 0; b < 2; ++b) tc_copy_sf_pair(sfb_t + 8 * j + 4 * b, sdesc_sf(sfb_s + 2048 * b + 512 * j));
+            for (int b = 0; b < kBands; ++b)
+              tc_copy_sf_pair(sfb_t + 4 * kBands * j + 4 * b, sdesc_sf(sfb_s + 2048 * b + 512 * j));
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tc_mma_nvf4_pair(tmem_u, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
+            tc_mma_nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 4 * kBands * j,
                              (kb | j) != 0 ? 1u : 0u);
           tc_commit_pair_mc(&empty[stage], kPairs == 2 ? 0xF : 0x3);
         }
@@ -397,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      if (elect_one()) tc_commit_pair_mc(tfull, pair_mask);
+      if (elect_one()) tc_commit_pair_mc(&tfull[acc], pair_mask);
       __syncwarp();
-      acc_phase ^= 1u;
+      if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
     }
     if (elect_one()) tc_commit_pair(drain);
     __syncwarp();
@@ -411,26 +432,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t quad = warp & 3;                // TMEM lanes 32*quad .. +31
-    const uint32_t half = (warp - 2) >> 2;         // accumulator columns 128*half .. +127
+    const uint32_t half = (warp - 2) >> 2;         // accumulator columns (kBN/2)*half .. +kBN/2-1
     const uint32_t row_in_tile = quad * 32 + lane;
     const uint32_t leader_tempty = mapa_shared(tempty, crank & ~1u);
     uint8_t* stage_buf = smem + C::kOffOut + (warp - 2) * C::kStageBufBytes;
-    uint32_t acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0;
     bool stores_pending = false;
     for (int64_t tile = cluster_id; tile < num_tiles; tile += n_clusters) {
       const TileRows t = tile_rows<kPairs>(s_off, s_pair, p, tile, rank, pair_id);
       const int64_t grow = t.block * kBM + row_in_tile;
       bool valid = t.has_rows;
       if (valid && p.counts != nullptr) valid = (grow - s_off[t.g]) < __ldg(p.counts + t.g);
-      if (!mbar_wait(tfull, acc_phase, abort_flag, p.err)) break;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after_sync();
-      float v[4][32];
-      const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + half * 128;
-      tmem_load128(t_row, v);
+      float v[C::kChunks][32];
+      const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + acc * kBN + half * (kBN / 2);
+      if constexpr (C::kChunks == 4) tmem_load128(t_row, v);
+      else tmem_load64(t_row, v);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(leader_tempty);
-      acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive_remote(leader_tempty + 8u * acc);
+      if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
 
       // whole 32-row slices leave by TMA store; a slice with missing rows stores row by row
       const float alpha = group_alpha(p.alpha, p.a_gs, p.b_gs, t.g);
@@ -457,15 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           swiglu_bf16_row(v, alpha, p.out_bf16 + grow * (p.N / 2) + static_cast<int64_t>(t.nt) * (kBN / 2) + half * 64);
       } else {
         if (staged) {
-          // two passes of 32 rows x 64 columns through the staging buffer: each
+          // passes of 32 rows x 64 columns through the staging buffer: each
           // thread writes its row's 8 chunks of 16 bytes (chunk q of row r at
           // slot q ^ (r & 7), so 8 consecutive rows cover all banks), then each
           // store instruction takes 4 rows x 8 chunks = four whole 128-byte lines
           const int sub = lane >> 3, chunk = lane & 7;
-          const int64_t x = static_cast<int64_t>(t.nt) * kBN + half * 128;
+          const int64_t x = static_cast<int64_t>(t.nt) * kBN + half * (kBN / 2);
           uint8_t* my_row = stage_buf + lane * 128;
 #pragma unroll
-          for (int box = 0; box < 2; ++box) {
+          for (int box = 0; box < C::kChunks / 2; ++box) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const float* f = &v[2 * box + (q >> 2)][8 * (q & 3)];
@@ -491,9 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + grow * p.N + static_cast<int64_t>(t.nt) * kBN +
-                                                half * 128);
+                                                half * (kBN / 2));
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < C::kChunks; ++c) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 o;
@@ -521,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct PairDeviceInfo {
-  bool attr_set[7] = {};
-  int max_clusters[7] = {};
+  bool attr_set[8] = {};
+  int max_clusters[8] = {};
 };
 
 PairDeviceInfo& pair_info(int dev) {
@@ -535,15 +557,17 @@ std::mutex& pair_mutex() {
   return mu;
 }
 
-template <int kEpi, bool kGather, int kPairs>
+template <int kEpi, bool kGather, int kPairs, int kBNP>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  constexpr int slot = kGather ? 3 : (kPairs == 2 ? 4 : 0) + (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0
-                                                            : kEpi == NVFP4_EPI_BF16        ? 1
-                                                                                            : 2);
+  constexpr int slot = kBNP == 128 ? 7
+                       : kGather   ? 3
+                                   : (kPairs == 2 ? 4 : 0) + (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0
+                                                              : kEpi == NVFP4_EPI_BF16        ? 1
+                                                                                              : 2);
   constexpr int kCtas = 2 * kPairs;
-  constexpr uint32_t smem = PairCfg<kEpi>::kSmemBytes;
+  constexpr uint32_t smem = PairCfg<kEpi, kBNP>::kSmemBytes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -560,12 +584,12 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     std::lock_guard<std::mutex> lock(pair_mutex());
     PairDeviceInfo& info = pair_info(dev);
     if (!info.attr_set[slot]) {
-      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather, kPairs, kBNP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       cfg.gridDim = dim3(static_cast<unsigned>(sms / kCtas * kCtas), 1, 1);
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs, kBNP>, &cfg);
       if (e != cudaSuccess) return e;
       info.max_clusters[slot] = n;
       info.attr_set[slot] = true;
@@ -576,15 +600,17 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   int64_t clusters = max_clusters < num_tiles ? max_clusters : num_tiles;
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(static_cast<unsigned>(kCtas * clusters), 1, 1);
-  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, ma, mb, msa, msb, mo, p);
+  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs, kBNP>, ma, mb, msa, msb, mo, p);
 }
 
 }  // namespace
 
-nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cudaStream_t stream) {
+nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int bn, int sms, int dev, cudaStream_t stream) {
   if (a.G > kMaxGroups) return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: G=%d exceeds %d", a.G, kMaxGroups);
-  if (pairs != 1 && (pairs != 2 || a.a_gather != nullptr || a.N % (2 * kBN) != 0))
+  if (pairs != 1 && (pairs != 2 || a.a_gather != nullptr || a.N % 512 != 0 || bn != 256))
     return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: no %d-pair clusters for this call", pairs);
+  if (bn != 256 && (bn != 128 || a.epilogue != NVFP4_EPI_BF16 || a.a_gather != nullptr))
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: no %d-column pair tiles for this call", bn);
   const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
   CUtensorMap ma, mb, msa, msb, mo;
   const uint64_t sfa_bytes = static_cast<uint64_t>(a.rows_max / 128) * (a.K / 64) * 512;
@@ -594,11 +620,11 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
                          static_cast<uint64_t>(gather ? a.a_rows : a.rows_max), static_cast<uint64_t>(a.K) / 2, 1,
                          128, gather ? 1 : 128 / pairs, true) &&
             make_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_q, static_cast<uint64_t>(a.G) * a.N,
-                         static_cast<uint64_t>(a.K) / 2, 1, 128, 128, true) &&
+                         static_cast<uint64_t>(a.K) / 2, 1, 128, static_cast<uint32_t>(bn / 2), true) &&
             make_tmap_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_sf, sfa_bytes / kSfRow, kSfRow, 1, kSfRow,
                          8 / pairs, false) &&
-            make_tmap_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_sf, sfb_bytes / kSfRow, kSfRow, 1, kSfRow, 8,
-                         false);
+            make_tmap_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_sf, sfb_bytes / kSfRow, kSfRow, 1, kSfRow,
+                         static_cast<uint32_t>(bn / 32), false);      // half of a tile's B scale atoms
   if (swiglu)
     ok = ok && make_tmap_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.out_q, static_cast<uint64_t>(a.rows_max),
                             static_cast<uint64_t>(a.N) / 4, 1, 32, 32, false);
@@ -617,7 +643,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
   p.G = a.offsets != nullptr ? a.G : 1;
   p.N = a.N;
   p.K = a.K;
-  p.n_tiles = a.N / (kBN * pairs);          // column tiles of a cluster
+  p.n_tiles = a.N / (bn * pairs);          // column tiles of a cluster
   p.k_blocks = a.K / kBK;
   p.rows_max = a.rows_max;
   p.sfb_group_bytes = static_cast<int64_t>(a.N / 128) * (a.K / 64) * 512;
@@ -636,9 +662,10 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
   const int64_t max_pairs = (blocks + 1) / 2 + (p.G > 1 ? p.G : 0);
   const int64_t max_tiles = max_pairs * p.n_tiles;
   if (max_tiles <= 0) return NVFP4_OK;
-#define NVFP4_PAIR_LAUNCH(E, GA, P) launch_pair<E, GA, P>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
+#define NVFP4_PAIR_LAUNCH(E, GA, P) launch_pair<E, GA, P, 256>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
   const cudaError_t e =
-      gather ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true, 1)
+      bn == 128 ? launch_pair<NVFP4_EPI_BF16, false, 1, 128>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
+      : gather ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true, 1)
       : pairs == 2
           ? (swiglu                                  ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false, 2)
              : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false, 2)

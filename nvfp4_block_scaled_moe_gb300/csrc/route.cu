@@ -6,11 +6,12 @@
 //
 // The permutation is deterministic although it counts with atomics: tokens are
 // cut into chunks of kRouteChunk; the top-k kernel counts each chunk's rows per
-// expert (atomic increments commute), one block turns the chunk counts into
-// per-chunk bases and the 128-padded expert offsets, and each chunk then
-// assigns ranks by walking its tokens in order.  Rows of an expert therefore
-// come in ascending token order.  x is quantised once per token and the bytes
-// are written straight into the token's k permuted rows.
+// expert (shared-memory atomic increments commute), one block turns the chunk
+// counts into per-chunk bases and the 128-padded expert offsets, and each chunk
+// then ranks its rows of every expert by token order (bit masks of the tokens
+// that picked it).  Rows of an expert therefore come in ascending token order.
+// x is quantised once per token and the bytes are written straight into the
+// token's k permuted rows; the same launch zeroes the padding rows.
 #include <float.h>
 
 #include "common.cuh"
@@ -41,17 +42,17 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 }
 
 // ------------------------------------------------------------------ top-k --
-// One warp per token: each lane holds the logits of experts lane + 32j
-// (j < kKeys, kKeys = ceil(E / 32)) and its best remaining key; k rounds of a warp
-// max over the lanes' best keys.
+// One block per chunk of kRouteChunk tokens, one warp per token at a time: each
+// lane holds the logits of experts lane + 32j (j < kKeys, kKeys = ceil(E / 32))
+// and its best remaining key; k rounds of a warp max over the lanes' best keys.
+// The chunk's per-expert counts gather in shared memory and leave as one row of
+// the chunk histogram (no global atomics, nothing to clear beforehand).
+constexpr int kTopkThreads = 1024;
+
 template <int kKeys>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int32_t T,
-                                                         int32_t E, int32_t k, int32_t* __restrict__ ids,
-                                                         float* __restrict__ w,
-                                                         int32_t* __restrict__ chunk_hist) {
-  const int lane = threadIdx.x & 31;
-  const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
+__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int64_t t, int32_t E, int32_t k,
+                                           int lane, int32_t* __restrict__ ids, float* __restrict__ w,
+                                           int32_t* sh_hist) {
   uint64_t key[kKeys];
 #pragma unroll
   for (int j = 0; j < kKeys; ++j) {
@@ -93,12 +94,28 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   if (lane < k) {
     ids[t * k + lane] = my_e;
     w[t * k + lane] = z / sum;
-    atomicAdd(&chunk_hist[(t / kRouteChunk) * E + my_e], 1);
+    atomicAdd(&sh_hist[my_e], 1);
   }
 }
 
+template <int kKeys>
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* __restrict__ logits, int32_t T,
+                                                                  int32_t E, int32_t k, int32_t* __restrict__ ids,
+                                                                  float* __restrict__ w,
+                                                                  int32_t* __restrict__ chunk_hist) {
+  __shared__ int32_t sh_hist[1024];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
+  for (int i = warp; i < kRouteChunk && t0 + i < T; i += kTopkThreads / 32)
+    topk_token<kKeys>(logits, t0 + i, E, k, lane, ids, w, sh_hist);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_hist[e];
+}
+
 static cudaError_t launch_topk(const RouteBuffers& b, cudaStream_t stream) {
-  const dim3 grid((b.T + 7) / 8), block(256);
+  const dim3 grid((b.T + kRouteChunk - 1) / kRouteChunk), block(kTopkThreads);
   const int keys = (b.E + 31) / 32;
   if (keys <= 1) route_topk_kernel<1><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
   else if (keys <= 2) route_topk_kernel<2><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
@@ -112,7 +129,9 @@ static cudaError_t launch_topk(const RouteBuffers& b, cudaStream_t stream) {
 // ---------------------------------------------------------------- offsets --
 // One block: per expert, turn chunk counts into exclusive per-chunk bases (in
 // place) and the total count; then the padded exclusive scan over experts and
-// the -1 marks of the padding rows.
+// the -1 marks of the padding rows.  The chunk walk is split over P threads per
+// expert (P a power of two, P * E <= 1024; thread p + P-ary part q takes a
+// contiguous run of chunks), so the walk is P times shorter.
 __global__ void __launch_bounds__(1024) route_offsets_kernel(int32_t* __restrict__ chunk_hist,
                                                              int32_t n_chunks, int32_t E,
                                                              int32_t* __restrict__ counts,
@@ -120,31 +139,40 @@ __global__ void __launch_bounds__(1024) route_offsets_kernel(int32_t* __restrict
                                                              int32_t* __restrict__ perm_token) {
   __shared__ int32_t sh_off[1025];
   __shared__ int32_t sh_cnt[1024];
+  __shared__ int32_t sh_part[1024];
   __shared__ int32_t sh_warp[32];
   const int tid = threadIdx.x;
-  int32_t padded = 0;
-  if (tid < E) {
-    int32_t run = 0;
-    int32_t c = 0;
-    for (; c + 8 <= n_chunks; c += 8) {         // eight independent loads in flight
-      int32_t h[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = chunk_hist[static_cast<int64_t>(c + i) * E + tid];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        chunk_hist[static_cast<int64_t>(c + i) * E + tid] = run;
-        run += h[i];
-      }
+  int parts = 1;
+  while (parts < 32 && 2 * parts * E <= 1024) parts *= 2;
+  const int e = tid % E, q = tid / E;                 // consecutive threads: consecutive experts
+  const bool walker = tid < parts * E;
+  const int per = (n_chunks + parts - 1) / parts;
+  const int c0 = q * per, c1 = c0 + per < n_chunks ? c0 + per : n_chunks;
+  int32_t sum = 0;
+  if (walker)
+    for (int c = c0; c < c1; ++c) sum += chunk_hist[static_cast<int64_t>(c) * E + e];
+  if (walker) sh_part[tid] = sum;
+  __syncthreads();
+  if (walker) {
+    int32_t run = 0, total = 0;
+    for (int r = 0; r < parts; ++r) {
+      const int32_t v = sh_part[r * E + e];
+      run += r < q ? v : 0;
+      total += v;
     }
-    for (; c < n_chunks; ++c) {
-      const int32_t h = chunk_hist[static_cast<int64_t>(c) * E + tid];
-      chunk_hist[static_cast<int64_t>(c) * E + tid] = run;
+    for (int c = c0; c < c1; ++c) {
+      const int64_t i = static_cast<int64_t>(c) * E + e;
+      const int32_t h = chunk_hist[i];
+      chunk_hist[i] = run;
       run += h;
     }
-    counts[tid] = run;
-    sh_cnt[tid] = run;
-    padded = ((run + 127) / 128) * 128;
+    if (q == 0) {
+      counts[e] = total;
+      sh_cnt[e] = total;
+    }
   }
+  __syncthreads();
+  const int32_t padded = tid < E ? ((sh_cnt[tid] + 127) / 128) * 128 : 0;
   // block-wide inclusive scan of `padded` (warp shuffles, then warp totals)
   const int lane = tid & 31, warp = tid >> 5;
   int32_t x = padded;
@@ -176,66 +204,99 @@ __global__ void __launch_bounds__(1024) route_offsets_kernel(int32_t* __restrict
   }
   __syncthreads();
   // padding rows of each group: one warp per expert
-  for (int e = warp; e < E; e += 32)
-    for (int32_t r = sh_off[e] + sh_cnt[e] + lane; r < sh_off[e + 1]; r += 32) perm_token[r] = -1;
+  for (int g = warp; g < E; g += 32)
+    for (int32_t r = sh_off[g] + sh_cnt[g] + lane; r < sh_off[g + 1]; r += 32) perm_token[r] = -1;
 }
 
 // ----------------------------------------------------------------- assign --
-// One block per chunk: stage the chunk's expert ids, per-chunk bases and the
-// offsets in shared memory, then one warp walks the tokens in order; lane j
-// places slot j.  A token picks each expert at most once, so the lanes never
-// touch the same counter.
-__global__ void __launch_bounds__(128) route_assign_kernel(const int32_t* __restrict__ ids, int32_t T,
-                                                           int32_t E, int32_t k,
-                                                           const int32_t* __restrict__ chunk_base,
-                                                           const int32_t* __restrict__ offsets,
-                                                           int32_t* __restrict__ perm_token,
-                                                           int32_t* __restrict__ inv_perm) {
+// One block per chunk, one thread per token.  A token picks each expert at most
+// once, so the rank of (token, expert) among the chunk's rows of that expert is
+// the number of earlier tokens of the chunk that picked it: each 32-token group
+// sets one bit per token in a per-expert mask, and the rank is the population
+// count of the lower bits of its own group's mask plus the full counts of the
+// earlier groups' masks.  Rows of an expert therefore come in ascending token order.
+constexpr int kAssignGroups = kRouteChunk / 32;
+
+__global__ void __launch_bounds__(kRouteChunk) route_assign_kernel(const int32_t* __restrict__ ids, int32_t T,
+                                                                   int32_t E, int32_t k,
+                                                                   const int32_t* __restrict__ chunk_base,
+                                                                   const int32_t* __restrict__ offsets,
+                                                                   int32_t* __restrict__ perm_token,
+                                                                   int32_t* __restrict__ inv_perm) {
   extern __shared__ int32_t sh[];
-  int32_t* sh_local = sh;                // [E] running count per expert
-  int32_t* sh_start = sh + E;            // [E] offsets[e] + chunk base
-  int32_t* sh_ids = sh + 2 * E;          // [kRouteChunk * k]
+  int32_t* sh_start = sh;                                          // [E] offsets[e] + chunk base
+  uint32_t* sh_mask = reinterpret_cast<uint32_t*>(sh + E);         // [kAssignGroups][E]
   const int64_t chunk = blockIdx.x;
-  const int64_t t0 = chunk * kRouteChunk;
-  const int n_tok = static_cast<int>(T - t0 < kRouteChunk ? T - t0 : kRouteChunk);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    sh_local[e] = 0;
     sh_start[e] = __ldg(offsets + e) + chunk_base[chunk * E + e];
+#pragma unroll
+    for (int g = 0; g < kAssignGroups; ++g) sh_mask[g * E + e] = 0u;
   }
-  for (int i = threadIdx.x; i < n_tok * k; i += blockDim.x) sh_ids[i] = __ldg(ids + t0 * k + i);
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    for (int i = 0; i < n_tok; ++i) {
-      if (lane < k) {
-        const int32_t e = sh_ids[i * k + lane];
-        const int32_t row = sh_start[e] + sh_local[e];
-        sh_local[e] += 1;
-        perm_token[row] = static_cast<int32_t>(t0 + i);
-        inv_perm[(t0 + i) * k + lane] = row;
-      }
-      __syncwarp();
+  const int i = threadIdx.x, g = i >> 5, lane = i & 31;
+  const int64_t t = chunk * kRouteChunk + i;
+  const bool live = t < T;
+  if (live)
+    for (int j = 0; j < k; ++j) atomicOr(&sh_mask[g * E + __ldg(ids + t * k + j)], 1u << lane);
+  __syncthreads();
+  if (live) {
+    for (int j = 0; j < k; ++j) {
+      const int32_t e = __ldg(ids + t * k + j);
+      int32_t rank = __popc(sh_mask[g * E + e] & ((1u << lane) - 1u));
+      for (int h = 0; h < g; ++h) rank += __popc(sh_mask[h * E + e]);
+      const int32_t row = sh_start[e] + rank;
+      perm_token[row] = static_cast<int32_t>(t);
+      inv_perm[t * k + j] = row;
     }
   }
 }
 
 // ---------------------------------------------------------------- scatter --
+// Zero the scale words (and, when the permuted copy is written, the nibbles) of
+// the padding rows [offsets[e] + counts[e], offsets[e+1]) of expert e: one block
+// (at most 127 rows).
+__device__ __forceinline__ void padfill_expert(int e, const int32_t* __restrict__ counts,
+                                               const int32_t* __restrict__ offsets, int32_t H,
+                                               uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf) {
+  const int64_t lo = __ldg(offsets + e) + __ldg(counts + e);
+  const int64_t hi = __ldg(offsets + e + 1);
+  const int n16 = H / 32;                 // 16-byte chunks per row
+  const int k4_total = H / 64;
+  const int64_t nq = a_q != nullptr ? (hi - lo) * n16 : 0;     // no permuted copy: scales only
+  for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
+    const int64_t r = lo + i / n16;
+    reinterpret_cast<uint4*>(a_q + r * (H / 2))[i % n16] = make_uint4(0, 0, 0, 0);
+  }
+  const int64_t ns = (hi - lo) * k4_total;
+  for (int64_t i = threadIdx.x; i < ns; i += blockDim.x) {
+    const int64_t r = lo + i / k4_total;
+    *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, static_cast<uint32_t>(i % k4_total), k4_total)) = 0u;
+  }
+}
+
 // Quantise x (PLAIN, per 16 along H) and write the bytes into each of the token's
-// k permuted rows.  Grid (T, ceil(H/1024 / warps)); one warp per 1024-value
-// segment, one thread per two 16-blocks: its 16 bytes of nibbles go to each row
-// in one store (a warp writes 512 contiguous bytes), and a lane pair's four
-// scale bytes form one word of the swizzled layout.  H % 64 == 0, so a lane pair
-// is either wholly inside the row or wholly past its end.
+// k permuted rows.  Grid (E + T, ceil(H/1024 / warps)): blocks x < E (with y = 0)
+// fill expert x's padding rows, the others quantise token x - E; one warp per
+// 1024-value segment, one thread per two 16-blocks: its 16 bytes of nibbles go
+// to each row in one store (a warp writes 512 contiguous bytes), and a lane
+// pair's four scale bytes form one word of the swizzled layout.  H % 64 == 0, so
+// a lane pair is either wholly inside the row or wholly past its end.
 __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int32_t H,
-                                                            int32_t k, const int32_t* __restrict__ inv_perm,
+                                                            int32_t k, int32_t E, const int32_t* __restrict__ inv_perm,
+                                                            const int32_t* __restrict__ counts,
+                                                            const int32_t* __restrict__ offsets,
                                                             const float* __restrict__ gscale,
                                                             uint8_t* __restrict__ a_q,
                                                             uint8_t* __restrict__ a_sf,
                                                             uint8_t* __restrict__ x_q) {
+  if (blockIdx.x < static_cast<unsigned>(E)) {
+    if (blockIdx.y == 0) padfill_expert(static_cast<int>(blockIdx.x), counts, offsets, H, a_q, a_sf);
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (seg * 1024 >= H) return;
-  const int64_t t = blockIdx.x;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) - E;
   const int64_t c0 = seg * 1024 + lane * 32;
   const bool active = c0 < H;
   uint4 nib = make_uint4(0, 0, 0, 0);
@@ -285,55 +346,23 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
   }
 }
 
-// -------------------------------------------------------------- pad fill --
-// Zero the scale words (and, when the permuted copy is written, the nibbles) of
-// the padding rows [offsets[e] + counts[e], offsets[e+1]) of every expert:
-// blockIdx.y = expert, blockIdx.x strides over its padding (at most 127 rows).
-__global__ void __launch_bounds__(256) route_padfill_kernel(const int32_t* __restrict__ counts,
-                                                            const int32_t* __restrict__ offsets, int32_t H,
-                                                            uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf) {
-  const int e = blockIdx.y;
-  const int64_t lo = __ldg(offsets + e) + __ldg(counts + e);
-  const int64_t hi = __ldg(offsets + e + 1);
-  const int n16 = H / 32;                 // 16-byte chunks per row
-  const int k4_total = H / 64;
-  const int64_t nq = a_q != nullptr ? (hi - lo) * n16 : 0;     // no permuted copy: scales only
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (int64_t i = first; i < nq; i += stride) {
-    const int64_t r = lo + i / n16;
-    reinterpret_cast<uint4*>(a_q + r * (H / 2))[i % n16] = make_uint4(0, 0, 0, 0);
-  }
-  const int64_t ns = (hi - lo) * k4_total;
-  for (int64_t i = first; i < ns; i += stride) {
-    const int64_t r = lo + i / k4_total;
-    *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, static_cast<uint32_t>(i % k4_total), k4_total)) = 0u;
-  }
-}
-
 cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
   const int32_t n_chunks = (b.T + kRouteChunk - 1) / kRouteChunk;
   if (n_chunks > 0) {
-    cudaError_t e = cudaMemsetAsync(b.chunk_hist, 0, static_cast<size_t>(n_chunks) * b.E * sizeof(int32_t), stream);
-    if (e != cudaSuccess) return e;
-    e = launch_topk(b, stream);
+    const cudaError_t e = launch_topk(b, stream);      // writes every row of the chunk histogram
     if (e != cudaSuccess) return e;
   }
   route_offsets_kernel<<<1, 1024, 0, stream>>>(b.chunk_hist, n_chunks, b.E, b.counts, b.offsets, b.perm_token);
   if (n_chunks > 0) {
-    const size_t smem = (2 * static_cast<size_t>(b.E) + static_cast<size_t>(kRouteChunk) * b.top_k) * sizeof(int32_t);
-    route_assign_kernel<<<n_chunks, 128, smem, stream>>>(b.topk_ids, b.T, b.E, b.top_k, b.chunk_hist, b.offsets,
-                                                         b.perm_token, b.inv_perm);
-    // up to 127 padding rows per expert: enough blocks per expert to cover them
-    const int64_t pad_chunks = 127LL * (b.H / 32);
-    const unsigned per_expert = static_cast<unsigned>((pad_chunks + 256 * 8 - 1) / (256 * 8));
-    route_padfill_kernel<<<dim3(per_expert, static_cast<unsigned>(b.E)), 256, 0, stream>>>(b.counts, b.offsets, b.H,
-                                                                                          b.a1_q, b.a1_sf);
+    const size_t smem = static_cast<size_t>(b.E) * (1 + kAssignGroups) * sizeof(int32_t);
+    route_assign_kernel<<<n_chunks, kRouteChunk, smem, stream>>>(b.topk_ids, b.T, b.E, b.top_k, b.chunk_hist,
+                                                                 b.offsets, b.perm_token, b.inv_perm);
     const int64_t segs = (b.H + 1023) / 1024;
     const int warps = static_cast<int>(segs < 8 ? segs : 8);     // no idle warps on short rows
-    const dim3 grid(static_cast<unsigned>(b.T), static_cast<unsigned>((segs + warps - 1) / warps));
-    route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k,
-                                                          b.inv_perm, b.x_gscale, b.a1_q, b.a1_sf, b.x_q);
+    const dim3 grid(static_cast<unsigned>(b.E + b.T), static_cast<unsigned>((segs + warps - 1) / warps));
+    route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k, b.E,
+                                                          b.inv_perm, b.counts, b.offsets, b.x_gscale, b.a1_q,
+                                                          b.a1_sf, b.x_q);
   }
   return cudaGetLastError();
 }
