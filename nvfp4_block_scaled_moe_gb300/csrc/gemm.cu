@@ -477,11 +477,7 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     // a third less operand traffic per SM, but clusters of 4 leave 8 of the 152
     // SMs idle, which costs more than the traffic saves on these tiles
     const bool quad = mode == NVFP4_GEMM_TILES_QUAD && a.N % 512 == 0 && a.a_gather == nullptr;
-#ifndef NVFP4_PAIR_BF16_BN
-#define NVFP4_PAIR_BF16_BN 256
-#endif
-    const int pair_bn = (!quad && a.epilogue == NVFP4_EPI_BF16 && a.a_gather == nullptr) ? NVFP4_PAIR_BF16_BN : 256;
-    return gemm_pair_launch(a, quad ? 2 : 1, pair_bn, info.sms, dev, stream);
+    return gemm_pair_launch(a, quad ? 2 : 1, info.sms, dev, stream);
   }
   CUtensorMap ma, mb;
   const bool gather = a.a_gather != nullptr;      // gathered A rows: a one-row box for tile::gather4

@@ -53,8 +53,10 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns per CTA (a second does not fit beside the scale factors), so the
 // MMAs of the next tile wait for the epilogue to drain it.  kBNP = 128 (BF16
 // epilogue only): two accumulators of 128 columns, so the next tile's MMAs run
-// while the epilogue drains the last one, at the price of more operand traffic
-// per output (each CTA loads 64 B rows per 128 columns instead of 128 per 256).
+// while the epilogue drains the last one, at the price of half as much operand
+// reuse per byte staged in shared memory.  Shared-memory bandwidth (TMA writes
+// plus MMA operand reads) bounds this kernel, so the 128-column form is slower
+// on every shape measured, and the launcher instantiates 256 only.
 //
 // Per epilogue: the staging buffer of one warp's output slice.
 //   SwiGLU: 32 rows x 32 bytes of nibbles (one 1 KiB TMA-store box per tile);
@@ -543,8 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct PairDeviceInfo {
-  bool attr_set[8] = {};
-  int max_clusters[8] = {};
+  bool attr_set[7] = {};
+  int max_clusters[7] = {};
 };
 
 PairDeviceInfo& pair_info(int dev) {
@@ -561,9 +563,8 @@ template <int kEpi, bool kGather, int kPairs, int kBNP>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  constexpr int slot = kBNP == 128 ? 7
-                       : kGather   ? 3
-                                   : (kPairs == 2 ? 4 : 0) + (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0
+  static_assert(kBNP == 256, "the launcher runs 256-column pair tiles");
+  constexpr int slot = kGather ? 3 : (kPairs == 2 ? 4 : 0) + (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0
                                                               : kEpi == NVFP4_EPI_BF16        ? 1
                                                                                               : 2);
   constexpr int kCtas = 2 * kPairs;
@@ -605,12 +606,11 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
 
 }  // namespace
 
-nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int bn, int sms, int dev, cudaStream_t stream) {
+nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cudaStream_t stream) {
   if (a.G > kMaxGroups) return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: G=%d exceeds %d", a.G, kMaxGroups);
-  if (pairs != 1 && (pairs != 2 || a.a_gather != nullptr || a.N % 512 != 0 || bn != 256))
+  if (pairs != 1 && (pairs != 2 || a.a_gather != nullptr || a.N % 512 != 0))
     return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: no %d-pair clusters for this call", pairs);
-  if (bn != 256 && (bn != 128 || a.epilogue != NVFP4_EPI_BF16 || a.a_gather != nullptr))
-    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: no %d-column pair tiles for this call", bn);
+  constexpr int bn = 256;                  // pair tile columns (see PairCfg)
   const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
   CUtensorMap ma, mb, msa, msb, mo;
   const uint64_t sfa_bytes = static_cast<uint64_t>(a.rows_max / 128) * (a.K / 64) * 512;
@@ -664,8 +664,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int bn, int sms, int
   if (max_tiles <= 0) return NVFP4_OK;
 #define NVFP4_PAIR_LAUNCH(E, GA, P) launch_pair<E, GA, P, 256>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
   const cudaError_t e =
-      bn == 128 ? launch_pair<NVFP4_EPI_BF16, false, 1, 128>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
-      : gather ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true, 1)
+      gather ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true, 1)
       : pairs == 2
           ? (swiglu                                  ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false, 2)
              : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false, 2)
