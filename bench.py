@@ -42,8 +42,8 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # single-pass ncu capture summarised in profiles/nvf4_gemm_prefill_dram.md, and
 # the hash of the kernel sources it was taken on.  Reported as roofline.traffic
 # only while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "43b04c79aa6019783ae5467222d28e2a54aa0022d077142cd1c2f0d46c506a41",
-                     "bytes": 1728798976 + 154662656}
+L1_TRAFFIC_RECORD = {"sources_sha256": "ce1f5f1fc0ae785c710924d762c9b8f2b951d875c593f0a54f807c218c550d9a",
+                     "bytes": 1728730880 + 151463424}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
 
