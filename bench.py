@@ -221,6 +221,16 @@ def run_reference(args, world: int, rank: int) -> None:
     print(json.dumps(line))
 
 
+def mma_ceiling(nv) -> dict:
+    """The measured issue ceiling of the GEMMs' FP4 MMA (nvfp4_mma_peak_probe: the
+    CTA-pair instruction stream with resident operands on every SM pair), run once
+    before the timed region; the roofline objects add the achieved fraction of it."""
+    tf, mhz = nv.nvfp4_mma_peak_probe(20000)
+    return {"value": tf, "unit": "TFLOP/s", "sm_mhz": mhz,
+            "what": "tcgen05.mma.cta_group::2.kind::mxf4nvf4 M=256 N=256 K=64 with the GEMM's scale-factor "
+                    "copies and commits, operands resident in shared memory, every SM pair"}
+
+
 def _workload_name(spec: dict, name: str = WORKLOAD) -> str:
     routing = "Zipf(1.2)-skewed routing" if spec.get("zipf") else "N(0,1) routing logits"
     return (f"{name} NVFP4 MoE FFN T={spec['T']} H={spec['H']} I={spec['I']} E={spec['E']} "
@@ -297,6 +307,7 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         if events:
             events[5].record(stream)
 
+    ceiling = mma_ceiling(nv)
     # the clock sampler starts before the warm-up so that no idle gap (in which the
     # GPU drops its clocks) separates the warm-up from the timed region
     clocks = ClockSampler(local)
@@ -387,7 +398,8 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                                     "(nominal FP4/BF16 dense ratio)",
                      "algorithmic": "2*T*k*(2I)*H FLOP per launch (real rows only)",
                      "traffic": l1_traffic() if args.workload == WORKLOAD else None,
-                     "traffic_unit": "bytes per launch (dram read + write)"},
+                     "traffic_unit": "bytes per launch (dram read + write)",
+                     "instruction_ceiling": dict(ceiling, frac=achieved / ceiling["value"])},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
                 "d2h_bytes_per_step": T * H * 2},
         "gpu_launches": (8 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps,
@@ -441,6 +453,7 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
                                   out_q=out_q, out_sf=out_sf)
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ceiling = mma_ceiling(nv)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -482,7 +495,8 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
                      "achieved": tflops,
                      "peak": fp4_peak, "unit": "TFLOP/s", "frac": tflops / fp4_peak,
                      "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} x {FP4_OVER_BF16:g}",
-                     "algorithmic": "2*M*N*K FLOP per launch", "traffic": None},
+                     "algorithmic": "2*M*N*K FLOP per launch", "traffic": None,
+                     "instruction_ceiling": dict(ceiling, frac=tflops / ceiling["value"])},
         "gpu_launches": args.steps, "clocks": clk}))
 
 

@@ -279,6 +279,26 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 int64_t a_gather_rows, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * nvfp4_mma_peak_probe -- measures the issue ceiling of the block-scaled FP4
+ * MMA that the CTA-pair GEMM uses (tcgen05.mma.cta_group::2.kind::mxf4nvf4
+ * .block_scale.scale_vec::4X, M=256 N=256 K=64): on every SM pair, `iters`
+ * groups of the GEMM's per-K-stage instruction stream (twelve scale-factor
+ * copies, four MMAs, one commit) with operands resident in shared memory, no
+ * loads and no epilogue.  A measurement aid with no counterpart in the source
+ * pages (the roofline of "Blackwell NVFP4 GEMM" kernels is this instruction's
+ * rate); results are discarded.
+ *   iters    1 .. 1048576 (each costs ~128 SM cycles x 4 per SM pair)
+ *   tflops   out (host): 2*256*256*64 FLOP per MMA over the span from the first
+ *            to the last pair's last MMA (globaltimer)
+ *   sm_mhz   out (host): the SM clock seen by the issuing threads (clock64 over
+ *            globaltimer), mean over the pairs
+ * Synchronous: it synchronises `stream` and reads the device error word
+ * (NVFP4_ERR_TIMEOUT if a bounded wait gave up).  NVFP4_ERR_INVALID_ARG for a
+ * null result pointer or iters out of range.
+ * -------------------------------------------------------------------------- */
+nvfp4_status nvfp4_mma_peak_probe(int32_t iters, double* tflops, double* sm_mhz, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * nvfp4_set_gemm_tiles -- process-wide choice of nvfp4_grouped_gemm's tile kernel
  * (also used by nvfp4_moe_ffn_forward): NVFP4_GEMM_TILES_AUTO (the default),
  * _SINGLE, _PAIR or _QUAD (_PAIR and _QUAD fall back to single CTAs where

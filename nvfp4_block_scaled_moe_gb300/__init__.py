@@ -20,7 +20,7 @@ __all__ = [
     "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
     "moe_route_permute", "moe_route_permute_static", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
     "moe_combine", "nvfp4_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_set_gemm_tiles",
-    "nvfp4_global_scale",
+    "nvfp4_global_scale", "nvfp4_mma_peak_probe",
     "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
 ]
 
@@ -67,6 +67,8 @@ _SIGS = {
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
     "nvfp4_set_gemm_tiles": (ctypes.c_int, [ctypes.c_int32]),
+    "nvfp4_mma_peak_probe": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_double),
+                                            ctypes.POINTER(ctypes.c_double), _vp]),
 }
 
 
@@ -194,6 +196,14 @@ GEMM_TILES_AUTO, GEMM_TILES_SINGLE, GEMM_TILES_PAIR, GEMM_TILES_QUAD = 0, 1, 2, 
 
 def nvfp4_set_gemm_tiles(mode):
     _check(load().nvfp4_set_gemm_tiles(mode))
+
+
+def nvfp4_mma_peak_probe(iters=20000, stream=None):
+    """(TFLOP/s, SM MHz) of the CTA-pair GEMM's FP4 MMA stream with resident
+    operands on every SM pair: the instruction ceiling. Synchronises the stream."""
+    tf, mhz = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check(load().nvfp4_mma_peak_probe(iters, ctypes.byref(tf), ctypes.byref(mhz), _stream(stream)))
+    return tf.value, mhz.value
 
 
 def nvfp4_selftest_bounded_wait(flag, limit_ns, stream=None):

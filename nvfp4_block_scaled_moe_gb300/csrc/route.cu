@@ -44,45 +44,57 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 // ------------------------------------------------------------------ top-k --
 // One block per chunk of kRouteChunk tokens, one warp per token at a time: each
 // lane holds the logits of experts lane + 32j (j < kKeys, kKeys = ceil(E / 32))
-// and its best remaining key; k rounds of a warp max over the lanes' best keys.
+// as order-preserving 32-bit codes, and its best remaining one (the lowest j
+// among equal codes).  Each of the k rounds takes the warp's largest code with
+// one redux.sync max, then the lowest expert holding it with one redux.sync min:
+// larger logit first, lower expert index among equal logits.
 // The chunk's per-expert counts gather in shared memory and leave as one row of
 // the chunk histogram (no global atomics, nothing to clear beforehand).
 constexpr int kTopkThreads = 1024;
 
+// This lane's logits of token t as codes; 0 sorts below every finite logit
+// (absent experts, and later the taken ones).
 template <int kKeys>
-__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int64_t t, int32_t E, int32_t k,
-                                           int lane, int32_t* __restrict__ ids, float* __restrict__ w,
-                                           int32_t* sh_hist) {
-  uint64_t key[kKeys];
+__device__ __forceinline__ void topk_load(const float* __restrict__ logits, int64_t t, int32_t E, int lane,
+                                          uint32_t (&code)[kKeys]) {
 #pragma unroll
   for (int j = 0; j < kKeys; ++j) {
     const int e = lane + 32 * j;
-    key[j] = e < E ? topk_key(__ldg(logits + t * E + e), e) : 0ull;
+    code[j] = e < E ? static_cast<uint32_t>(topk_key(__ldg(logits + t * E + e), e) >> 32) : 0u;
   }
-  uint32_t taken = 0;
+}
+
+template <int kKeys>
+__device__ __forceinline__ void topk_token(uint32_t (&code)[kKeys], int64_t t, int32_t k, int lane,
+                                           int32_t* __restrict__ ids, float* __restrict__ w, int32_t* sh_hist) {
+  uint32_t best = 0, best_j = 0;
   auto local_best = [&]() {
-    uint64_t b = 0;
+    best = 0;
+    best_j = 0;
 #pragma unroll
     for (int j = 0; j < kKeys; ++j)
-      if (!((taken >> j) & 1u) && key[j] > b) b = key[j];
-    return b;
+      if (code[j] > best) {
+        best = code[j];
+        best_j = j;
+      }
   };
-  uint64_t best = local_best();
-  uint64_t mine = 0;
+  local_best();
+  uint32_t mine_code = 0, mine_e = 0;
   for (int s = 0; s < k; ++s) {
-    uint64_t m = best;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-      m = o > m ? o : m;
-    }
-    const uint32_t e_win = 0xFFFFFFFFu - static_cast<uint32_t>(m);
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, best);
+    const uint32_t e_win = __reduce_min_sync(0xFFFFFFFFu, best == m ? lane + 32u * best_j : 0xFFFFFFFFu);
     if (static_cast<int>(e_win & 31u) == lane) {
-      taken |= 1u << (e_win >> 5);
-      best = local_best();
+#pragma unroll
+      for (int j = 0; j < kKeys; ++j)
+        if (j == static_cast<int>(e_win >> 5)) code[j] = 0u;
+      local_best();
     }
-    if (lane == s) mine = m;
+    if (lane == s) {
+      mine_code = m;
+      mine_e = e_win;
+    }
   }
+  const uint64_t mine = (static_cast<uint64_t>(mine_code) << 32) | (0xFFFFFFFFu - mine_e);
   // softmax over the selected logits; slot 0 holds the maximum
   const float my_v = key_value(mine);
   const int my_e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
@@ -108,8 +120,27 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
-  for (int i = warp; i < kRouteChunk && t0 + i < T; i += kTopkThreads / 32)
-    topk_token<kKeys>(logits, t0 + i, E, k, lane, ids, w, sh_hist);
+  const int n = static_cast<int>(T - t0 < kRouteChunk ? T - t0 : kRouteChunk);
+  constexpr int kStep = kTopkThreads / 32;
+  if (warp < n) {
+    uint32_t code[kKeys];
+    topk_load<kKeys>(logits, t0 + warp, E, lane, code);
+    for (int i = warp; i < n; i += kStep) {
+      // the next token's logits are in flight while this one is ranked (up to
+      // E = 256; wider rows would not fit twice in registers)
+      uint32_t next[kKeys <= 8 ? kKeys : 1];
+      if constexpr (kKeys <= 8) {
+        if (i + kStep < n) topk_load<kKeys>(logits, t0 + i + kStep, E, lane, next);
+      }
+      topk_token<kKeys>(code, t0 + i, k, lane, ids, w, sh_hist);
+      if constexpr (kKeys <= 8) {
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) code[j] = next[j];
+      } else {
+        if (i + kStep < n) topk_load<kKeys>(logits, t0 + i + kStep, E, lane, code);
+      }
+    }
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_hist[e];
 }
@@ -149,8 +180,10 @@ __global__ void __launch_bounds__(1024) route_offsets_kernel(int32_t* __restrict
   const int per = (n_chunks + parts - 1) / parts;
   const int c0 = q * per, c1 = c0 + per < n_chunks ? c0 + per : n_chunks;
   int32_t sum = 0;
-  if (walker)
+  if (walker) {
+#pragma unroll 8
     for (int c = c0; c < c1; ++c) sum += chunk_hist[static_cast<int64_t>(c) * E + e];
+  }
   if (walker) sh_part[tid] = sum;
   __syncthreads();
   if (walker) {
@@ -160,6 +193,7 @@ __global__ void __launch_bounds__(1024) route_offsets_kernel(int32_t* __restrict
       run += r < q ? v : 0;
       total += v;
     }
+#pragma unroll 8
     for (int c = c0; c < c1; ++c) {
       const int64_t i = static_cast<int64_t>(c) * E + e;
       const int32_t h = chunk_hist[i];

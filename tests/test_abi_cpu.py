@@ -104,6 +104,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None, 0, None) == 2
     assert lib.moe_combine(p, p, p, 4, 12, 2, None, p, None) == 2
     assert lib.moe_combine(p, p, p, 4, 16, 2, vp(base + 8), p, None) == 3     # misaligned shared rows
+    d = ctypes.c_double(0.0)
+    assert lib.nvfp4_mma_peak_probe(100, None, ctypes.byref(d), None) == 1       # null result pointer
+    assert lib.nvfp4_mma_peak_probe(0, ctypes.byref(d), ctypes.byref(d), None) == 1
+    assert lib.nvfp4_mma_peak_probe(1 << 21, ctypes.byref(d), ctypes.byref(d), None) == 1
     assert lib.nvfp4_selftest_bounded_wait(None, 10, None) == 1
     assert b"selftest" in lib.nvfp4_last_error()
     # tile-kernel choice: four modes, anything else refused; the default restored
