@@ -281,12 +281,15 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     gs2 = dict(a_global_scale=b.a2_gs, b_global_scale=w.w2_gs) if two else {}
     gather1 = dict(a_gather=b.perm_token, a_gather_rows=T) if b.gather else {}
 
-    def step(events=None):
+    def step(events=None, x_in=None, logits_in=None, y_out=None):
+        x_in = x_d if x_in is None else x_in
+        logits_in = logits_d if logits_in is None else logits_in
+        y_out = b.y if y_out is None else y_out
         if events:
             events[0].record(stream)
         if two:                                  # x's encode scale, per batch (timed with routing)
-            nv.nvfp4_global_scale(x_d, b.x_gs)
-        nv.moe_route_permute(logits_d, x_d, k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
+            nv.nvfp4_global_scale(x_in, b.x_gs)
+        nv.moe_route_permute(logits_in, x_in, k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
                              b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_global_scale=b.x_gs if two else None,
                              x_q=b.x_q)
         if events:
@@ -300,10 +303,10 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                               nv.EPI_BF16, out_bf16=b.rows_out, **gs2)
         if events:
             events[3].record(stream)
-        shared_rows = None if sh is None else sh.forward(x_d)
+        shared_rows = None if sh is None else sh.forward(x_in)
         if events:
             events[4].record(stream)
-        nv.moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y, shared=shared_rows)
+        nv.moe_combine(b.rows_out, b.inv_perm, b.topk_w, y_out, shared=shared_rows)
         if events:
             events[5].record(stream)
 
@@ -344,21 +347,52 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     value = world * args.steps * step_flops / (ms * 1e-3) / 1e12
     tokens_per_s = world * args.steps * T / (ms * 1e-3)
 
-    # ---- end to end: pinned host inputs copied in, y copied out, every step
+    # ---- end to end: every step copies its inputs in from pinned host memory and
+    # its y out to pinned host memory.  The copies run on two copy streams (one per
+    # direction) with double-buffered x, logits and y on the device: step i+1's
+    # inputs come in and step i-1's y goes out while step i computes.
     x_h = x_t.pin_memory()
     logits_h = torch.from_numpy(logits_np).pin_memory()
     y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    xs, lgs, ys = [x_d, torch.empty_like(x_d)], [logits_d, torch.empty_like(logits_d)], [b.y, torch.empty_like(b.y)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer j have landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # step on buffer j finished (inputs free, y ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # y of buffer j has left
     barrier(world)
     torch.cuda.synchronize()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record(stream)
-    for _ in range(args.steps):
-        x_d.copy_(x_h, non_blocking=True)
-        logits_d.copy_(logits_h, non_blocking=True)
-        step()
-        y_h.copy_(b.y, non_blocking=True)
+
+    def fetch(j):
+        h2d.wait_event(ev_done[j]) if fetched[j] else h2d.wait_event(s0)
+        with torch.cuda.stream(h2d):
+            xs[j].copy_(x_h, non_blocking=True)
+            lgs[j].copy_(logits_h, non_blocking=True)
+        ev_in[j].record(h2d)
+        fetched[j] = True
+
+    fetched = [False, False]
+    fetch(0)
+    for i in range(args.steps):
+        j = i & 1
+        if i + 1 < args.steps:
+            fetch(1 - j)
+        stream.wait_event(ev_in[j])
+        if i >= 2:
+            stream.wait_event(ev_out[j])                 # y buffer j: its previous copy-out is done
+        step(x_in=xs[j], logits_in=lgs[j], y_out=ys[j])
+        ev_done[j].record(stream)
+        d2h.wait_event(ev_done[j])
+        with torch.cuda.stream(d2h):
+            y_h.copy_(ys[j], non_blocking=True)
+        ev_out[j].record(d2h)
+    stream.wait_stream(d2h)
     s1.record(stream)
     torch.cuda.synchronize()
+    # the copied-out y of the last step equals the resident run's (same inputs)
+    if not torch.equal(y_h, ys[0].cpu()):
+        raise RuntimeError("end-to-end pipeline: the copied-out y differs from the resident run's")
     barrier(world)
     e2e_ms = max_over_ranks(s0.elapsed_time(s1), world)
     e2e_value = world * args.steps * step_flops / (e2e_ms * 1e-3) / 1e12
@@ -401,7 +435,9 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                      "traffic_unit": "bytes per launch (dram read + write)",
                      "instruction_ceiling": dict(ceiling, frac=achieved / ceiling["value"])},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
-                "d2h_bytes_per_step": T * H * 2},
+                "d2h_bytes_per_step": T * H * 2,
+                "copies": "pinned host x and logits in, y out, every step; H2D and D2H on two copy streams "
+                          "overlapping the neighbouring steps' compute (double-buffered device x, logits, y)"},
         "gpu_launches": (8 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
