@@ -42,8 +42,8 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # single-pass ncu capture summarised in profiles/nvf4_gemm_prefill_dram.md, and
 # the hash of the kernel sources it was taken on.  Reported as roofline.traffic
 # only while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "ce1f5f1fc0ae785c710924d762c9b8f2b951d875c593f0a54f807c218c550d9a",
-                     "bytes": 1728730880 + 151463424}
+L1_TRAFFIC_RECORD = {"sources_sha256": "c32689fe3c75edb47f98d4a2e00596c426c8f878535aaf8250001caf6a53c350",
+                     "bytes": 1729302528 + 151471872}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
 

@@ -514,22 +514,6 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, float (&v)[4][32]) 
   for (int i = 0; i < 128; ++i) v[i >> 5][i & 31] = __uint_as_float(r[i]);
 }
 
-// Load 64 consecutive fp32 columns of this thread's TMEM lane (one instruction)
-// and wait for them.
-__device__ __forceinline__ void tmem_load64(uint32_t taddr, float (&v)[2][32]) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
-      "%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,"
-      "%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : NVFP4_R32(0), NVFP4_R32(32)
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i >> 5][i & 31] = __uint_as_float(r[i]);
-}
 #undef NVFP4_R32
 
 // Load 32 consecutive fp32 columns of this thread's TMEM lane and wait for them.

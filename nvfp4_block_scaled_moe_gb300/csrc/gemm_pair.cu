@@ -49,31 +49,28 @@ constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
 constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms
 constexpr uint32_t kTmemCols = 512;
 
-// A pair tile is 256 rows x kBNP columns.  kBNP = 256: one accumulator of 256
-// TMEM columns per CTA (a second does not fit beside the scale factors), so the
-// MMAs of the next tile wait for the epilogue to drain it.  kBNP = 128 (BF16
-// epilogue only): two accumulators of 128 columns, so the next tile's MMAs run
-// while the epilogue drains the last one, at the price of half as much operand
-// reuse per byte staged in shared memory.  Shared-memory bandwidth (TMA writes
-// plus MMA operand reads) bounds this kernel, so the 128-column form is slower
-// on every shape measured, and the launcher instantiates 256 only.
+// A pair tile is 256 rows x 256 columns, with one accumulator of 256 TMEM
+// columns per CTA: a second does not fit beside the scale factors, so the MMAs
+// of the next tile wait for the epilogue to drain it.  (Tiles of 256 x 128 with
+// two accumulators would hide that wait but halve the operand reuse per byte
+// staged in shared memory, whose bandwidth bounds this kernel; they measured
+// slower on every shape.)
 //
 // Per epilogue: the staging buffer of one warp's output slice.
 //   SwiGLU: 32 rows x 32 bytes of nibbles (one 1 KiB TMA-store box per tile);
 //   BF16:   32 rows x 64 columns (4 KiB, 16-byte chunks XOR-swizzled by row).
-template <int kEpi, int kBNP>
+template <int kEpi>
 struct PairCfg {
-  static_assert(kBNP == 256 || (kBNP == 128 && kEpi == NVFP4_EPI_BF16), "tile widths");
   static constexpr bool kSwiglu = kEpi == NVFP4_EPI_SWIGLU_NVFP4;
-  static constexpr int kBN = kBNP;                                   // columns of a pair tile
-  static constexpr int kAcc = kBNP == 256 ? 1 : 2;                   // accumulators in TMEM
-  static constexpr int kBands = kBNP / 128;                          // 128-row bands of B's scale atoms
-  static constexpr int kChunks = kBNP / 64;                          // 32-column chunks per epilogue warp
-  static constexpr uint32_t kBBytes = (kBNP / 2) * kBK / 2;          // this CTA's half of the B rows
-  static constexpr uint32_t kSfbBytes = kBNP * (kBK / 16);           // scale atoms of every B row
-  static constexpr uint32_t kTmemSf = kAcc * kBNP;                   // scale columns follow the accumulators
+  static constexpr int kBN = 256;                                    // columns of a pair tile
+  static constexpr int kAcc = 1;                                     // accumulators in TMEM
+  static constexpr int kBands = kBN / 128;                           // 128-row bands of B's scale atoms
+  static constexpr int kChunks = kBN / 64;                           // 32-column chunks per epilogue warp
+  static constexpr uint32_t kBBytes = (kBN / 2) * kBK / 2;           // this CTA's half of the B rows
+  static constexpr uint32_t kSfbBytes = kBN * (kBK / 16);            // scale atoms of every B row
+  static constexpr uint32_t kTmemSf = kAcc * kBN;                    // scale columns follow the accumulator
   static constexpr uint32_t kTmemSfStage = 16 + 16 * kBands;         // A: 4 atoms x 4 columns; B: 4 per band
-  static constexpr int kStages = kBNP == 256 ? 5 : 6;
+  static constexpr int kStages = 5;
   static constexpr uint32_t kStageBufBytes = kSwiglu ? 1024 : 4096;
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
@@ -202,22 +199,20 @@ __device__ __forceinline__ void swiglu_row(const float (&v)[4][32], float alpha,
 constexpr int kSfRow = 256;
 
 // kGather: A rows come through p.a_gather (tile::gather4); a separate
-// instantiation, so the default kernels carry none of its code.  kBNP: the pair
-// tile's columns (see PairCfg).
+// instantiation, so the default kernels carry none of its code.
 // kPairs = 2: clusters of two pairs (4 CTAs) side by side along N.  Both pairs
 // multiply the same A rows, so each CTA loads half of its 128 A rows (and half
 // of their scale atoms) and multicasts them to its counterpart in the other
 // pair: a third less operand traffic per SM than a lone pair.
-template <int kEpi, bool kGather, int kPairs, int kBNP>
+template <int kEpi, bool kGather, int kPairs>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                           const __grid_constant__ CUtensorMap tmap_out, const PairParams p) {
-  using C = PairCfg<kEpi, kBNP>;
+  using C = PairCfg<kEpi>;
   constexpr int kStages = C::kStages, kAcc = C::kAcc, kBN = C::kBN, kBands = C::kBands;
   constexpr uint32_t kBBytes = C::kBBytes, kSfbBytes = C::kSfbBytes;
   constexpr uint32_t kTmemSf = C::kTmemSf, kTmemSfStage = C::kTmemSfStage;
-  static_assert(kPairs == 1 || kBNP == 256, "two-pair clusters use 256-column pair tiles");
   extern __shared__ __align__(1024) uint8_t smem[];
   // the swizzled tiles need a 1 KiB-aligned base; every CTA sees the same base,
   // so a misaligned one stops all of them here, before any pair traffic
@@ -350,10 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tma_load_2d_pair(smem + C::kOffB + stage * kBBytes, &tmap_b, bar, kb * (kBK / 2),
                            g * p.N + t.nt * kBN + static_cast<int32_t>(rank) * (kBN / 2));
-          // B's scale atoms: this CTA loads half of them (band `rank` of two, or
-          // atoms 2*rank, +1 of one band) into both CTAs of the pair
-          const int64_t sfb_src = kBands == 2 ? (static_cast<int64_t>(rank) * k4 + kb * 4) * 512
-                                              : (static_cast<int64_t>(kb) * 4 + 2 * rank) * 512;
+          // B's scale atoms: this CTA loads band `rank` into both CTAs of the pair
+          const int64_t sfb_src = (static_cast<int64_t>(rank) * k4 + kb * 4) * 512;
           tma_load_2d_pair_mc(smem + C::kOffSfb + stage * kSfbBytes + rank * (kSfbBytes / 2), &tmap_sfb, bar, 0,
                               static_cast<int32_t>((sfb_base + sfb_src) / kSfRow), pair_mask);
         }
@@ -449,8 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       float v[C::kChunks][32];
       const uint32_t t_row = tmem_base + ((quad * 32u) << 16) + acc * kBN + half * (kBN / 2);
-      if constexpr (C::kChunks == 4) tmem_load128(t_row, v);
-      else tmem_load64(t_row, v);
+      tmem_load128(t_row, v);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(leader_tempty + 8u * acc);
@@ -559,16 +551,15 @@ std::mutex& pair_mutex() {
   return mu;
 }
 
-template <int kEpi, bool kGather, int kPairs, int kBNP>
+template <int kEpi, bool kGather, int kPairs>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  static_assert(kBNP == 256, "the launcher runs 256-column pair tiles");
   constexpr int slot = kGather ? 3 : (kPairs == 2 ? 4 : 0) + (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0
                                                               : kEpi == NVFP4_EPI_BF16        ? 1
                                                                                               : 2);
   constexpr int kCtas = 2 * kPairs;
-  constexpr uint32_t smem = PairCfg<kEpi, kBNP>::kSmemBytes;
+  constexpr uint32_t smem = PairCfg<kEpi>::kSmemBytes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -585,12 +576,12 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     std::lock_guard<std::mutex> lock(pair_mutex());
     PairDeviceInfo& info = pair_info(dev);
     if (!info.attr_set[slot]) {
-      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather, kPairs, kBNP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       cfg.gridDim = dim3(static_cast<unsigned>(sms / kCtas * kCtas), 1, 1);
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs, kBNP>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, &cfg);
       if (e != cudaSuccess) return e;
       info.max_clusters[slot] = n;
       info.attr_set[slot] = true;
@@ -601,7 +592,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   int64_t clusters = max_clusters < num_tiles ? max_clusters : num_tiles;
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(static_cast<unsigned>(kCtas * clusters), 1, 1);
-  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs, kBNP>, ma, mb, msa, msb, mo, p);
+  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, ma, mb, msa, msb, mo, p);
 }
 
 }  // namespace
@@ -610,7 +601,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
   if (a.G > kMaxGroups) return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: G=%d exceeds %d", a.G, kMaxGroups);
   if (pairs != 1 && (pairs != 2 || a.a_gather != nullptr || a.N % 512 != 0))
     return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: no %d-pair clusters for this call", pairs);
-  constexpr int bn = 256;                  // pair tile columns (see PairCfg)
+  constexpr int bn = PairCfg<NVFP4_EPI_BF16>::kBN;      // pair tile columns
   const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
   CUtensorMap ma, mb, msa, msb, mo;
   const uint64_t sfa_bytes = static_cast<uint64_t>(a.rows_max / 128) * (a.K / 64) * 512;
@@ -662,7 +653,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
   const int64_t max_pairs = (blocks + 1) / 2 + (p.G > 1 ? p.G : 0);
   const int64_t max_tiles = max_pairs * p.n_tiles;
   if (max_tiles <= 0) return NVFP4_OK;
-#define NVFP4_PAIR_LAUNCH(E, GA, P) launch_pair<E, GA, P, 256>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
+#define NVFP4_PAIR_LAUNCH(E, GA, P) launch_pair<E, GA, P>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
   const cudaError_t e =
       gather ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true, 1)
       : pairs == 2
