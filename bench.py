@@ -438,7 +438,9 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                 "d2h_bytes_per_step": T * H * 2,
                 "copies": "pinned host x and logits in, y out, every step; H2D and D2H on two copy streams "
                           "overlapping the neighbouring steps' compute (double-buffered device x, logits, y)"},
-        "gpu_launches": (8 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps,
+        # per step: top-k, offsets, assign, scatter, L1, L2, combine (+ x's amax and
+        # its finalisation with --two-level; + the shared expert's quantise, L1, L2)
+        "gpu_launches": (7 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
