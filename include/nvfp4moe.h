@@ -264,7 +264,8 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  * Two kernels compute this (nvfp4_set_gemm_tiles): 128-row tiles on single CTAs,
  * or, when N % 256 == 0, 256-row tiles on CTA pairs (a 2-CTA cluster sharing one
  * cta_group::2 MMA, each CTA loading half of B), which pairs consecutive 128-row
- * blocks of a group.  Both give the same results bit for bit.
+ * blocks of a group; on request the pairs run two to a cluster, sharing A.  All
+ * forms give the same results bit for bit.
  * Limits: K a positive multiple of 256, N a positive multiple of 256 (the SwiGLU
  * epilogues) or 128 (BF16), rows_max a
  * positive multiple of 128, all pointers 16-byte aligned.
@@ -285,8 +286,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
  * groups of the GEMM's per-K-stage instruction stream (twelve scale-factor
  * copies, four MMAs, one commit) with operands resident in shared memory, no
  * loads and no epilogue.  A measurement aid with no counterpart in the source
- * pages (the roofline of "Blackwell NVFP4 GEMM" kernels is this instruction's
- * rate); results are discarded.
+ * pages: it gives the GEMMs' roofline the rate of the instruction they issue.
+ * The MMA results are discarded.
  *   iters    1 .. 1048576 (each costs ~128 SM cycles x 4 per SM pair)
  *   tflops   out (host): 2*256*256*64 FLOP per MMA over the span from the first
  *            to the last pair's last MMA (globaltimer)
