@@ -464,9 +464,10 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
 
     nvbuild.build()
     torch.cuda.set_device(local)
-    spec = dict(inputs.CONFIGS[args.workload])
+    spec = dict(inputs.CONFIGS["dense" if args.workload == "dense_swiglu_bf16" else args.workload])
     M, N, K = spec["M"], spec["N"], spec["K"]
     bf16_out = spec.get("epilogue") == "bf16"
+    compact = args.workload == "dense_swiglu_bf16"     # the compact BF16 SwiGLU output (compatibility path)
     a, bw = inputs.dense_inputs(spec)
     a_d, b_d = torch.from_numpy(a).cuda(), torch.from_numpy(bw).cuda()
     a_q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
@@ -478,13 +479,17 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
     del a_d, b_d
     out_q = torch.empty((M, N // 4), dtype=torch.uint8, device="cuda")
     out_sf = torch.empty(nv.sf_bytes(M, N // 2), dtype=torch.uint8, device="cuda")
-    out_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda") if bf16_out else None
+    out_bf16 = (torch.empty((M, N), dtype=torch.bfloat16, device="cuda") if bf16_out else
+                torch.empty((M, N // 2), dtype=torch.bfloat16, device="cuda") if compact else None)
     flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step():
         if bf16_out:
             nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_BF16,
+                                  out_bf16=out_bf16)
+        elif compact:
+            nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_SWIGLU_BF16,
                                   out_bf16=out_bf16)
         else:
             nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_SWIGLU_NVFP4,
@@ -525,10 +530,12 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16) -> fp32 accum", "data": "synthetic",
         "config": {"workload": f"dense NVFP4 GEMM M={M} N={N} K={K} + "
-                               + ("BF16 output" if bf16_out else "SwiGLU + NVFP4 requant"),
+                               + ("BF16 output" if bf16_out else "SwiGLU -> compact BF16 output" if compact
+                                  else "SwiGLU + NVFP4 requant"),
                    "l2_policy": "L2 flushed (256 MiB write) before every step; per-step CUDA events",
                    "launch": "each step a one-launch CUDA graph replayed after the flush"},
         "roofline": {"kernel": ("nvf4_gemm_pair_kernel<1> (BF16 epilogue, CTA pairs)" if bf16_out else
+                                "nvf4_gemm_pair_kernel<2> (compact BF16 SwiGLU epilogue, CTA pairs)" if compact else
                                 "nvf4_gemm_pair_kernel<0> (SwiGLU + NVFP4 epilogue, CTA pairs)"), "bound": "tensor",
                      "achieved": tflops,
                      "peak": fp4_peak, "unit": "TFLOP/s", "frac": tflops / fp4_peak,
@@ -540,7 +547,11 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
 
 def run_quantizer(args, world: int, rank: int, local: int) -> None:
     """The standalone SwiGLU + NVFP4 quantiser on BF16 gate/up (32768, 2 x 2048):
-    HBM-bound, 306 MB moved per launch (inputs larger than L2)."""
+    HBM-bound, 306 MB moved per launch (inputs larger than L2).  With --workload
+    quantizer_deinterleave, the compatibility mode that quantises the kept 8 of
+    every 16 interleaved slots of the same buffer (an L1 output whose up slots
+    already hold SwiGLU values): the kept and dropped halves alternate every 16
+    bytes, below the 32-byte DRAM sector, so the whole buffer is read."""
     import torch
 
     import nvfp4_block_scaled_moe_gb300 as nv
@@ -556,8 +567,12 @@ def run_quantizer(args, world: int, rank: int, local: int) -> None:
     sf = torch.empty(nv.sf_bytes(rows, cols), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
+    deinterleave = args.workload == "quantizer_deinterleave"
+    mode = nv.MODE_DEINTERLEAVE_GU8 if deinterleave else nv.MODE_SWIGLU_GU8
+    kernel = "quantize_kernel<DEINTERLEAVE_GU8>" if deinterleave else "quantize_kernel<SWIGLU_GU8>"
+
     def step():
-        nv.nvfp4_quantize(gu_d, cols, nv.MODE_SWIGLU_GU8, q, sf)
+        nv.nvfp4_quantize(gu_d, cols, mode, q, sf)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -591,10 +606,11 @@ def run_quantizer(args, world: int, rank: int, local: int) -> None:
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> nvfp4",
         "data": "synthetic",
-        "config": {"workload": f"SwiGLU+NVFP4 quantiser BF16 gate/up ({rows}, 2x{cols})",
+        "config": {"workload": (f"deinterleave + NVFP4 quantiser of the kept slots, BF16 ({rows}, 2x{cols})"
+                                if deinterleave else f"SwiGLU+NVFP4 quantiser BF16 gate/up ({rows}, 2x{cols})"),
                    "l2_policy": "inputs larger than L2 (268 MB read per step)",
                    "launch": "the K steps replayed from one CUDA graph"},
-        "roofline": {"kernel": "quantize_kernel<SWIGLU_GU8>", "bound": "hbm", "achieved": gbs,
+        "roofline": {"kernel": kernel, "bound": "hbm", "achieved": gbs,
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                      "algorithmic": f"{nbytes} bytes per launch (input read + nibbles + SF written)",
                      "traffic": None},
@@ -618,19 +634,21 @@ def main():
     ap.add_argument("--two-level", action="store_true",
                     help="prefill/decode with the two-level scale (per-tensor encode scales next to the per-16 "
                          "ones); the CPU baseline stays the one-level oracle")
-    ap.add_argument("--workload", choices=("prefill", "decode", "dense", "dense_l2", "quantizer"), default=WORKLOAD,
+    ap.add_argument("--workload", choices=("prefill", "decode", "dense", "dense_l2", "dense_swiglu_bf16", "quantizer",
+                                           "quantizer_deinterleave"), default=WORKLOAD,
                     help="prefill (default) and decode time the whole MoE FFN step; dense times the L1 GEMM of "
                          "one 8192-row expert, dense_l2 the prefill L2 GEMM shape as one group; quantizer the "
-                         "standalone SwiGLU + NVFP4 quantiser")
+                         "standalone SwiGLU + NVFP4 quantiser; dense_swiglu_bf16 and quantizer_deinterleave the "
+                         "compatibility paths (the compact BF16 SwiGLU output; deinterleave + quantise)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
-    elif args.workload in ("dense", "dense_l2"):
+    elif args.workload in ("dense", "dense_l2", "dense_swiglu_bf16"):
         run_dense(args, world, rank, local)
-    elif args.workload == "quantizer":
+    elif args.workload in ("quantizer", "quantizer_deinterleave"):
         run_quantizer(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
