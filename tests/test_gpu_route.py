@@ -37,7 +37,8 @@ def _route(nv, pipeline, x_t, logits, top_k, H):
 
 @pytest.mark.parametrize("T,H,E,k,zipf", [(128, 512, 8, 2, False), (300, 256, 8, 2, False),
                                           (1000, 128, 64, 6, True), (77, 64, 256, 8, False),
-                                          (5, 128, 3, 3, False), (513, 1024, 130, 4, True)])
+                                          (5, 128, 3, 3, False), (513, 1024, 130, 4, True),
+                                          (260, 128, 1024, 16, True), (200, 64, 500, 32, False)])
 def test_route_permute_matches_oracle(nv, T, H, E, k, zipf):
     nv, pipeline = nv
     spec = inputs.moe_spec(T=T, H=H, I=256, E=E, top_k=k, seed=T + E, zipf=zipf)
