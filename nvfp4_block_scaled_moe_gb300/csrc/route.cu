@@ -49,7 +49,9 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 // one redux.sync max, then the lowest expert holding it with one redux.sync min:
 // larger logit first, lower expert index among equal logits.
 // The chunk's per-expert counts gather in shared memory and leave as one row of
-// the chunk histogram (no global atomics, nothing to clear beforehand).
+// the chunk histogram (no global atomics, nothing to clear beforehand).  Short
+// batches (few chunks) split each chunk over gridDim.y blocks, so that every
+// warp ranks one token; those blocks add their counts into the cleared row.
 constexpr int kTopkThreads = 1024;
 
 // This lane's logits of token t as codes; 0 sorts below every finite logit
@@ -119,8 +121,9 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
-  const int n = static_cast<int>(T - t0 < kRouteChunk ? T - t0 : kRouteChunk);
+  const int per = kRouteChunk / static_cast<int>(gridDim.y);          // tokens of this block
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouteChunk + static_cast<int64_t>(blockIdx.y) * per;
+  const int n = static_cast<int>(T - t0 < per ? (T - t0 > 0 ? T - t0 : 0) : per);
   constexpr int kStep = kTopkThreads / 32;
   if (warp < n) {
     uint32_t code[kKeys];
@@ -142,11 +145,26 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_hist[e];
+  int32_t* row = chunk_hist + static_cast<int64_t>(blockIdx.x) * E;
+  if (gridDim.y == 1) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) row[e] = sh_hist[e];
+  } else {
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      if (sh_hist[e] != 0) atomicAdd(&row[e], sh_hist[e]);
+  }
 }
 
-static cudaError_t launch_topk(const RouteBuffers& b, cudaStream_t stream) {
-  const dim3 grid((b.T + kRouteChunk - 1) / kRouteChunk), block(kTopkThreads);
+static cudaError_t launch_topk(const RouteBuffers& b, int sms, cudaStream_t stream) {
+  const int n_chunks = (b.T + kRouteChunk - 1) / kRouteChunk;
+  // a short batch: four blocks per chunk (32 tokens each, one per warp) adding
+  // into a cleared histogram, instead of one block walking 128 tokens
+  const int split = 4 * n_chunks <= sms ? 4 : 1;
+  if (split > 1) {
+    const cudaError_t e = cudaMemsetAsync(b.chunk_hist, 0, static_cast<size_t>(n_chunks) * b.E * sizeof(int32_t),
+                                          stream);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(static_cast<unsigned>(n_chunks), static_cast<unsigned>(split)), block(kTopkThreads);
   const int keys = (b.E + 31) / 32;
   if (keys <= 1) route_topk_kernel<1><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
   else if (keys <= 2) route_topk_kernel<2><<<grid, block, 0, stream>>>(b.logits, b.T, b.E, b.top_k, b.topk_ids, b.topk_w, b.chunk_hist);
@@ -383,7 +401,10 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
 cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
   const int32_t n_chunks = (b.T + kRouteChunk - 1) / kRouteChunk;
   if (n_chunks > 0) {
-    const cudaError_t e = launch_topk(b, stream);      // writes every row of the chunk histogram
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = launch_topk(b, sms, stream);       // every row of the chunk histogram
     if (e != cudaSuccess) return e;
   }
   route_offsets_kernel<<<1, 1024, 0, stream>>>(b.chunk_hist, n_chunks, b.E, b.counts, b.offsets, b.perm_token);
