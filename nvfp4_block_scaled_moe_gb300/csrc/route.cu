@@ -305,30 +305,35 @@ __global__ void __launch_bounds__(kRouteChunk) route_assign_kernel(const int32_t
 
 // ---------------------------------------------------------------- scatter --
 // Zero the scale words (and, when the permuted copy is written, the nibbles) of
-// the padding rows [offsets[e] + counts[e], offsets[e+1]) of expert e: one block
-// (at most 127 rows).
-__device__ __forceinline__ void padfill_expert(int e, const int32_t* __restrict__ counts,
+// the padding rows [offsets[e] + counts[e], offsets[e+1]) of expert e (at most
+// 127 rows): part `part` of `parts` blocks, interleaved by thread.
+constexpr int kPadParts = 4;
+
+__device__ __forceinline__ void padfill_expert(int e, int part, const int32_t* __restrict__ counts,
                                                const int32_t* __restrict__ offsets, int32_t H,
                                                uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf) {
   const int64_t lo = __ldg(offsets + e) + __ldg(counts + e);
   const int64_t hi = __ldg(offsets + e + 1);
   const int n16 = H / 32;                 // 16-byte chunks per row
   const int k4_total = H / 64;
+  const int64_t first = static_cast<int64_t>(part) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(kPadParts) * blockDim.x;
   const int64_t nq = a_q != nullptr ? (hi - lo) * n16 : 0;     // no permuted copy: scales only
-  for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
+  for (int64_t i = first; i < nq; i += stride) {
     const int64_t r = lo + i / n16;
     reinterpret_cast<uint4*>(a_q + r * (H / 2))[i % n16] = make_uint4(0, 0, 0, 0);
   }
   const int64_t ns = (hi - lo) * k4_total;
-  for (int64_t i = threadIdx.x; i < ns; i += blockDim.x) {
+  for (int64_t i = first; i < ns; i += stride) {
     const int64_t r = lo + i / k4_total;
     *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, static_cast<uint32_t>(i % k4_total), k4_total)) = 0u;
   }
 }
 
 // Quantise x (PLAIN, per 16 along H) and write the bytes into each of the token's
-// k permuted rows.  Grid (E + T, ceil(H/1024 / warps)): blocks x < E (with y = 0)
-// fill expert x's padding rows, the others quantise token x - E; one warp per
+// k permuted rows.  Grid (kPadParts*E + T, ceil(H/1024 / warps)): blocks
+// x < kPadParts*E (with y = 0) fill part x % kPadParts of expert x / kPadParts's
+// padding rows, the others quantise token x - kPadParts*E; one warp per
 // 1024-value segment, one thread per two 16-blocks: its 16 bytes of nibbles go
 // to each row in one store (a warp writes 512 contiguous bytes), and a lane
 // pair's four scale bytes form one word of the swizzled layout.  H % 64 == 0, so
@@ -341,14 +346,16 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
                                                             uint8_t* __restrict__ a_q,
                                                             uint8_t* __restrict__ a_sf,
                                                             uint8_t* __restrict__ x_q) {
-  if (blockIdx.x < static_cast<unsigned>(E)) {
-    if (blockIdx.y == 0) padfill_expert(static_cast<int>(blockIdx.x), counts, offsets, H, a_q, a_sf);
+  if (blockIdx.x < static_cast<unsigned>(kPadParts * E)) {
+    if (blockIdx.y == 0)
+      padfill_expert(static_cast<int>(blockIdx.x) / kPadParts, static_cast<int>(blockIdx.x) % kPadParts, counts,
+                     offsets, H, a_q, a_sf);
     return;
   }
   const int lane = threadIdx.x & 31;
   const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (seg * 1024 >= H) return;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) - E;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) - static_cast<int64_t>(kPadParts) * E;
   const int64_t c0 = seg * 1024 + lane * 32;
   const bool active = c0 < H;
   uint4 nib = make_uint4(0, 0, 0, 0);
@@ -414,7 +421,7 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
                                                                  b.offsets, b.perm_token, b.inv_perm);
     const int64_t segs = (b.H + 1023) / 1024;
     const int warps = static_cast<int>(segs < 8 ? segs : 8);     // no idle warps on short rows
-    const dim3 grid(static_cast<unsigned>(b.E + b.T), static_cast<unsigned>((segs + warps - 1) / warps));
+    const dim3 grid(static_cast<unsigned>(kPadParts * b.E + b.T), static_cast<unsigned>((segs + warps - 1) / warps));
     route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k, b.E,
                                                           b.inv_perm, b.counts, b.offsets, b.x_gscale, b.a1_q,
                                                           b.a1_sf, b.x_q);
