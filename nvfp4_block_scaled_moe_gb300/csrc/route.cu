@@ -430,9 +430,11 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------- combine --
-// One block per token; each thread accumulates 8 columns over the k slots in
-// slot order (fp32 FMA), then the token's shared-expert row if there is one, and
-// rounds once to BF16.
+// Block (t, s) of token t takes the 8-column chunks s*blockDim + thread,
+// (s + gridDim.y)*blockDim + thread, ...; each thread accumulates its 8 columns
+// over the k slots in slot order (fp32 FMA), then the token's shared-expert row
+// if there is one, and rounds once to BF16.  Short batches split a token's row
+// over several blocks so that enough loads are in flight.
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ rows,
                                                       const int32_t* __restrict__ inv_perm,
                                                       const float* __restrict__ w, int32_t H, int32_t k,
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
                                                       __nv_bfloat16* __restrict__ y) {
   const int64_t t = blockIdx.x;
   const int n8 = H / 8;
-  for (int c = threadIdx.x; c < n8; c += blockDim.x) {
+  for (int c = blockIdx.y * blockDim.x + threadIdx.x; c < n8; c += gridDim.y * blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -470,7 +472,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
 cudaError_t combine_launch(const void* rows, const int32_t* inv_perm, const float* w, int32_t T, int32_t H,
                            int32_t top_k, const void* shared, void* y, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(rows), inv_perm, w, H, top_k,
+  // a token's row over up to ceil(H / 1024) blocks of 128 threads while the batch
+  // has fewer than 4096 tokens (one 16-byte chunk per thread)
+  const int split = T < 4096 ? (H / 8 + 127) / 128 : 1;
+  combine_kernel<<<dim3(T, split), 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(rows), inv_perm, w, H, top_k,
                                         static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(y));
   return cudaGetLastError();
 }
