@@ -38,7 +38,8 @@ def _route(nv, pipeline, x_t, logits, top_k, H):
 @pytest.mark.parametrize("T,H,E,k,zipf", [(128, 512, 8, 2, False), (300, 256, 8, 2, False),
                                           (1000, 128, 64, 6, True), (77, 64, 256, 8, False),
                                           (5, 128, 3, 3, False), (513, 1024, 130, 4, True),
-                                          (260, 128, 1024, 16, True), (200, 64, 500, 32, False)])
+                                          (260, 128, 1024, 16, True), (200, 64, 500, 32, False),
+                                          (5000, 64, 256, 8, True)])   # >= 38 chunks: one top-k block per chunk
 def test_route_permute_matches_oracle(nv, T, H, E, k, zipf):
     nv, pipeline = nv
     spec = inputs.moe_spec(T=T, H=H, I=256, E=E, top_k=k, seed=T + E, zipf=zipf)
@@ -80,7 +81,8 @@ def test_route_permute_zero_tokens(nv):
     assert host(b.offsets).tolist() == [0] * 5 and host(b.counts).tolist() == [0] * 4
 
 
-@pytest.mark.parametrize("T,H,k", [(1, 8, 1), (64, 512, 2), (33, 7168, 8)])
+@pytest.mark.parametrize("T,H,k", [(1, 8, 1), (64, 512, 2), (33, 7168, 8),
+                                   (4100, 256, 4)])              # >= 4096 tokens: one block per token
 def test_combine_matches_oracle(nv, T, H, k):
     nv, _ = nv
     rng = np.random.default_rng(T * H + k)
