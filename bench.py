@@ -545,6 +545,90 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
         "gpu_launches": args.steps, "clocks": clk}))
 
 
+def run_hbm_stage(args, world: int, rank: int, local: int) -> None:
+    """One HBM-bound stage of the prefill step on its own: --workload route times
+    moe_route_permute (top-k, offsets, ranks, x quantised into its k permuted
+    rows, padding zeroed) on the prefill batch's logits and x; --workload combine
+    times moe_combine on that batch's routing with seeded random BF16 rows in
+    place of the L2 output.  Inputs are larger than L2; the K timed launches are
+    replayed from one CUDA graph."""
+    import torch
+
+    import nvfp4_block_scaled_moe_gb300 as nv
+    from nvfp4_block_scaled_moe_gb300 import build as nvbuild
+    from nvfp4_block_scaled_moe_gb300 import pipeline
+
+    nvbuild.build()
+    torch.cuda.set_device(local)
+    spec = dict(inputs.CONFIGS["prefill"])
+    T, H, I, E, k = spec["T"], spec["H"], spec["I"], spec["E"], spec["top_k"]
+    s = pipeline.MoeShape(T=T, H=H, I=I, E=E, top_k=k)
+    b = pipeline.MoeBuffers(s)
+    x_t, _ = inputs.moe_x(spec)
+    x_d = x_t.cuda()
+    logits_d = torch.from_numpy(inputs.moe_logits(spec)).cuda()
+
+    def route():
+        nv.moe_route_permute(logits_d, x_d, k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
+                             b.inv_perm, b.a1_q, b.a1_sf, b.workspace)
+
+    route()
+    nv.nvfp4_device_status()
+    R_pad = int(b.offsets[-1].item())
+    if args.workload == "route":
+        step = route
+        nbytes = (T * E * 4 + T * H * 2 + R_pad * (H // 2 + H // 16) + T * k * 12 + R_pad * 4)
+        kernel = "route_scatter_kernel (with top-k, offsets and rank kernels)"
+        what = ("logits + x read, the permuted NVFP4 rows and scale words (padding rows included), "
+                "ids, weights, inv_perm and perm_token written")
+    else:
+        g = torch.Generator(device="cuda").manual_seed(spec["seed"] + 7)
+        b.rows_out.copy_(torch.randn(b.rows_out.shape, generator=g, device="cuda", dtype=torch.bfloat16))
+        del x_d
+        torch.cuda.empty_cache()
+
+        def step():
+            nv.moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
+        nbytes = T * k * H * 2 + T * H * 2 + T * k * 8
+        kernel = "combine_kernel"
+        what = "the k BF16 rows of every token read, y written, inv_perm and weights read"
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    nv.nvfp4_device_status()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            step()
+    graph.replay()                      # untimed
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    nv.nvfp4_device_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    pk = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 -> nvfp4" if args.workload == "route" else "bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": f"{args.workload} stage of the prefill MoE FFN (T={T}, H={H}, E={E}, top-{k})",
+                   "l2_policy": "inputs larger than L2", "launch": "the K steps replayed from one CUDA graph"},
+        "roofline": {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "algorithmic": f"{nbytes} bytes per step ({what})",
+                     "traffic": None},
+        "gpu_launches": args.steps * (4 if args.workload == "route" else 1), "clocks": clk}))
+
+
 def run_quantizer(args, world: int, rank: int, local: int) -> None:
     """The standalone SwiGLU + NVFP4 quantiser on BF16 gate/up (32768, 2 x 2048):
     HBM-bound, 306 MB moved per launch (inputs larger than L2).  With --workload
@@ -635,11 +719,12 @@ def main():
                     help="prefill/decode with the two-level scale (per-tensor encode scales next to the per-16 "
                          "ones); the CPU baseline stays the one-level oracle")
     ap.add_argument("--workload", choices=("prefill", "decode", "dense", "dense_l2", "dense_swiglu_bf16", "quantizer",
-                                           "quantizer_deinterleave"), default=WORKLOAD,
+                                           "quantizer_deinterleave", "route", "combine"), default=WORKLOAD,
                     help="prefill (default) and decode time the whole MoE FFN step; dense times the L1 GEMM of "
                          "one 8192-row expert, dense_l2 the prefill L2 GEMM shape as one group; quantizer the "
                          "standalone SwiGLU + NVFP4 quantiser; dense_swiglu_bf16 and quantizer_deinterleave the "
-                         "compatibility paths (the compact BF16 SwiGLU output; deinterleave + quantise)")
+                         "compatibility paths (the compact BF16 SwiGLU output; deinterleave + quantise); route and "
+                         "combine the prefill step's HBM-bound stages on their own")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -650,6 +735,8 @@ def main():
         run_dense(args, world, rank, local)
     elif args.workload in ("quantizer", "quantizer_deinterleave"):
         run_quantizer(args, world, rank, local)
+    elif args.workload in ("route", "combine"):
+        run_hbm_stage(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 
