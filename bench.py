@@ -42,8 +42,8 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # single-pass ncu capture summarised in profiles/nvf4_gemm_prefill_dram.md, and
 # the hash of the kernel sources it was taken on.  Reported as roofline.traffic
 # only while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "c32689fe3c75edb47f98d4a2e00596c426c8f878535aaf8250001caf6a53c350",
-                     "bytes": 1729302528 + 151471872}
+L1_TRAFFIC_RECORD = {"sources_sha256": "f5c37d778923ed30ae9b6ce747748f7a4ff2d1aeabbd1edb09119bcaca5d49e9",
+                     "bytes": 1728698880 + 151449856}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
 
