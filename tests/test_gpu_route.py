@@ -39,7 +39,10 @@ def _route(nv, pipeline, x_t, logits, top_k, H):
                                           (1000, 128, 64, 6, True), (77, 64, 256, 8, False),
                                           (5, 128, 3, 3, False), (513, 1024, 130, 4, True),
                                           (260, 128, 1024, 16, True), (200, 64, 500, 32, False),
-                                          (5000, 64, 256, 8, True)])   # >= 38 chunks: one top-k block per chunk
+                                          (5000, 64, 256, 8, True),    # >= 38 chunks: one top-k block per chunk
+                                          # short batches (split top-k), E = 1024, k = 32
+                                          (256, 7168, 256, 8, False), (1, 64, 1024, 8, False),
+                                          (256, 64, 1024, 32, True), (255, 128, 64, 6, True)])
 def test_route_permute_matches_oracle(nv, T, H, E, k, zipf):
     nv, pipeline = nv
     spec = inputs.moe_spec(T=T, H=H, I=256, E=E, top_k=k, seed=T + E, zipf=zipf)
