@@ -119,11 +119,26 @@ __device__ __forceinline__ float group_alpha(float alpha, const float* ga, const
   return __fdiv_rn(alpha, a * b);
 }
 
+// signed_halfstep of two values at once: the same IEEE round-to-nearest
+// multiplies and FMAs, issued as packed two-lane fp32 instructions (sm_100 and
+// later), so each lane's result is bit-identical to the scalar form.
+__device__ __forceinline__ float2 signed_halfstep2(float2 x, const BlockScale& s) {
+  const float2 r2 = make_float2(s.r2, s.r2);
+  const float2 q0 = __fmul2_rn(x, r2);
+  const float2 rem = __ffma2_rn(q0, make_float2(s.d2, s.d2), make_float2(-x.x, -x.y));
+  const float2 q = __ffma2_rn(make_float2(-rem.x, -rem.y), r2, q0);
+  return __fmul2_rn(make_float2(rintf(q.x), rintf(q.y)), make_float2(0.5f, 0.5f));
+}
+
 // Quantise eight values of one half-block with that block's scale.
 __device__ __forceinline__ uint32_t quantize8(const float (&h)[8], const BlockScale& s) {
   float v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = signed_halfstep(h[i], s);
+  for (int i = 0; i < 8; i += 2) {
+    const float2 t = signed_halfstep2(make_float2(h[i], h[i + 1]), s);
+    v[i] = t.x;
+    v[i + 1] = t.y;
+  }
   return e2m1x8_from_halfsteps(v);
 }
 
@@ -134,6 +149,19 @@ __device__ __forceinline__ float swiglu(float g, float u) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
   return g * r * u;
+}
+
+// swiglu of two pairs: the same operations, the multiplies and the add issued
+// as packed two-lane fp32 instructions (bit-identical per lane).
+__device__ __forceinline__ float2 swiglu2(float2 g, float2 u) {
+  const float2 t = __fmul2_rn(g, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  float e0, e1, r0, r1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t.y));
+  const float2 den = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(e0, e1));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(den.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(den.y));
+  return __fmul2_rn(__fmul2_rn(g, make_float2(r0, r1)), u);
 }
 
 // Byte offset of the SF word holding scales (row, 4*k4 .. 4*k4+3) in the

@@ -153,10 +153,17 @@ __device__ __forceinline__ void swiglu_row(const float (&v)[4][32], float alpha,
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     float h0[8], h1[8];
+    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      h0[i] = swiglu(alpha * v[c][i], alpha * v[c][8 + i]);
-      h1[i] = swiglu(alpha * v[c][16 + i], alpha * v[c][24 + i]);
+    for (int i = 0; i < 8; i += 2) {
+      const float2 t0 = swiglu2(__fmul2_rn(a2, make_float2(v[c][i], v[c][i + 1])),
+                                __fmul2_rn(a2, make_float2(v[c][8 + i], v[c][9 + i])));
+      const float2 t1 = swiglu2(__fmul2_rn(a2, make_float2(v[c][16 + i], v[c][17 + i])),
+                                __fmul2_rn(a2, make_float2(v[c][24 + i], v[c][25 + i])));
+      h0[i] = t0.x;
+      h0[i + 1] = t0.y;
+      h1[i] = t1.x;
+      h1[i + 1] = t1.y;
     }
     if (valid && p.h_debug != nullptr) {
       float4* hp = reinterpret_cast<float4*>(p.h_debug + grow * out_cols + col0 + 16 * c);

@@ -31,11 +31,19 @@ __device__ __forceinline__ void load_block(const void* in, int64_t row, int64_t 
     bf16x8_to_f32(g0, g);
     bf16x8_to_f32(u0, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = swiglu(g[i], u[i]);
+    for (int i = 0; i < 8; i += 2) {
+      const float2 t = swiglu2(make_float2(g[i], g[i + 1]), make_float2(u[i], u[i + 1]));
+      h[i] = t.x;
+      h[i + 1] = t.y;
+    }
     bf16x8_to_f32(g1, g);
     bf16x8_to_f32(u1, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[8 + i] = swiglu(g[i], u[i]);
+    for (int i = 0; i < 8; i += 2) {
+      const float2 t = swiglu2(make_float2(g[i], g[i + 1]), make_float2(u[i], u[i + 1]));
+      h[8 + i] = t.x;
+      h[8 + i + 1] = t.y;
+    }
   } else if (kMode == NVFP4_MODE_DEINTERLEAVE_GU8) {
     // interleaved columns 2*c0 .. 2*c0+31: keep u0(8) and u1(8) as they are
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + row * ld + 2 * c0);
