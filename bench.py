@@ -42,8 +42,8 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # single-pass ncu capture summarised in profiles/nvf4_gemm_prefill_dram.md, and
 # the hash of the kernel sources it was taken on.  Reported as roofline.traffic
 # only while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "f5c37d778923ed30ae9b6ce747748f7a4ff2d1aeabbd1edb09119bcaca5d49e9",
-                     "bytes": 1728698880 + 151449856}
+L1_TRAFFIC_RECORD = {"sources_sha256": "89279474ce31d370b09d2dc4c6a988a341f21e0c28ad41176e3effdffb308cfd",
+                     "bytes": 1728573440 + 151392256}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
 
@@ -84,17 +84,71 @@ def ffn_flops(T: int, H: int, I: int, k: int) -> tuple:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """SM clock and clock-event reasons sampled during the timed region.
+
+    A background thread polls NVML (read-only queries through ctypes) every
+    2 ms and stamps each sample with the host clock; stop(t0, t1) keeps the
+    samples taken inside the timed region [t0, t1], so even a 50 ms region
+    gets a few dozen.  Without NVML it falls back to `nvidia-smi -lms 100`,
+    whose samples cover the sampler's whole lifetime (it needs a few hundred
+    ms to start)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits that mark a throttled run (power capping is kept and noted)
+    REASON_BITS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"), (0x20, "sw_thermal_slowdown"),
+                   (0x80, "hw_power_brake_slowdown"), (0x4, "sw_power_cap"))
+    PERIOD_S = 0.002
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.tmp = None
+        self.nvml = None
+        self.thread = None
+        self.samples = []           # (host time, sm MHz, max sm MHz, reason bits)
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.gpu)
+        bus = getattr(props, "pci_bus_id", None)
+        ok = -1
+        if bus is not None:
+            pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), bus, getattr(props, "pci_device_id", 0))
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(handle))
+        if ok != 0:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(handle))
+        if ok != 0:
+            raise OSError("no NVML handle for the device")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return ctypes, lib, handle, reasons
+
+    def _poll(self):
+        ctypes, lib, handle, reasons_fn = self.nvml
+        mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stopping.is_set():
+            t = time.time()
+            if (lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(mhz)) == 0 and           # NVML_CLOCK_SM
+                    lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0 and
+                    reasons_fn(handle, ctypes.byref(bits)) == 0):
+                self.samples.append((t, mhz.value, mx.value, bits.value))
+            self.stopping.wait(self.PERIOD_S)
 
     def start(self):
+        import threading
+        try:
+            self.nvml = self._nvml_open()
+            self.stopping = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError, RuntimeError):
+            self.nvml = None
         try:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -103,7 +157,21 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self) -> dict:
+    def stop(self, t0=None, t1=None) -> dict:
+        if self.nvml is not None:
+            self.stopping.set()
+            self.thread.join(timeout=5)
+            self.nvml[1].nvmlShutdown()
+            inside = [x for x in self.samples if t0 is None or t0 <= x[0] <= t1]
+            window = "timed region"
+            if not inside:                       # a region shorter than the poll period
+                inside = sorted(self.samples, key=lambda x: abs(x[0] - (t0 + t1) / 2))[:1] if t0 else self.samples
+                window = "nearest sample to the timed region"
+            reasons = sorted({name for bit, name in self.REASON_BITS for x in inside if x[3] & bit})
+            return {"sm_mhz": statistics.median(x[1] for x in inside) if inside else None,
+                    "sm_max_mhz": max(x[2] for x in inside) if inside else None,
+                    "samples": len(inside), "reasons": reasons,
+                    "source": f"NVML every {self.PERIOD_S * 1e3:g} ms, {window}"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -130,7 +198,7 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "reasons": sorted(reasons), "source": "nvidia-smi -lms 100, sampler lifetime"}
 
 
 def dist_setup():
@@ -324,14 +392,15 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     # ---- timed region: inputs resident in HBM
     barrier(world)
     torch.cuda.synchronize()
+    t_region = time.time()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(args.steps):
         step(ev[i])
     end.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop(t_region, time.time())
     barrier(world)
-    clk = clocks.stop()
     nv.nvfp4_device_status()
     ms_local = start.elapsed_time(end)
     ms = max_over_ranks(ms_local, world)
@@ -512,13 +581,14 @@ def run_dense(args, world: int, rank: int, local: int) -> None:
         step()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+    t_region = time.time()
     for e0, e1 in evs:
         _flush_l2(flush)
         e0.record(stream)
         graph.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clk = clocks.stop(t_region, time.time())
     nv.nvfp4_device_status()
     ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     flops = 2.0 * M * N * K
@@ -608,11 +678,12 @@ def run_hbm_stage(args, world: int, rank: int, local: int) -> None:
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_region = time.time()
     e0.record(stream)
     graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clk = clocks.stop(t_region, time.time())
     nv.nvfp4_device_status()
     ms = e0.elapsed_time(e1) / args.steps
     gbs = nbytes / (ms * 1e-3) / 1e9
@@ -676,11 +747,12 @@ def run_quantizer(args, world: int, rank: int, local: int) -> None:
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_region = time.time()
     e0.record(stream)
     graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clk = clocks.stop(t_region, time.time())
     nv.nvfp4_device_status()
     ms = e0.elapsed_time(e1) / args.steps
     nbytes = rows * 2 * cols * 2 + rows * cols // 2 + nv.sf_bytes(rows, cols)
