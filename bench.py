@@ -110,6 +110,8 @@ class ClockSampler:
 
     def _nvml_open(self):
         import ctypes
+
+        import torch
         lib = ctypes.CDLL("libnvidia-ml.so.1")
         if lib.nvmlInit_v2() != 0:
             raise OSError("nvmlInit failed")
@@ -147,7 +149,7 @@ class ClockSampler:
             self.thread = threading.Thread(target=self._poll, daemon=True)
             self.thread.start()
             return
-        except (OSError, AttributeError, RuntimeError):
+        except Exception:                  # no NVML: fall back to nvidia-smi
             self.nvml = None
         try:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
