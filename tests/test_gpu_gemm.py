@@ -89,6 +89,9 @@ CASES_BF16 = [
     ([128, 0, 384, 128], [100, 0, 300, 128], 768, 768, 0.75),
     ([128] * 40, [128 - (i % 7) for i in range(40)], 1024, 1280, 1.0),   # > one wave of tiles
     ([1024, 384, 640], [1024, 383, 600], 1792, 768, 1.0),                 # pairs, odd tails, > one wave
+    # more groups than the CTA-pair kernel takes (single-CTA kernel), a third of them empty
+    ([0 if i % 3 == 0 else 128 for i in range(600)], [0 if i % 3 == 0 else 1 + (i * 37) % 128 for i in range(600)],
+     256, 256, 1.0),
     # long K: the epilogue's store spacing reaches its 320-cycle cap
     ([512, 256], [512, 250], 512, 2048, 1.0),
     ([256], None, 256, 4096, 0.5),

@@ -42,10 +42,12 @@ def _gpu_setup(pipeline, spec):
 
 SMALL = [dict(inputs.CONFIGS["tiny"]),
          inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=21),
-         inputs.moe_spec(T=200, H=256, I=512, E=5, top_k=3, seed=22, zipf=True)]
+         inputs.moe_spec(T=200, H=256, I=512, E=5, top_k=3, seed=22, zipf=True),
+         # more experts than the CTA-pair kernel takes groups: the GEMMs use the single-CTA kernel
+         inputs.moe_spec(T=400, H=256, I=256, E=600, top_k=4, seed=23)]
 
 
-@pytest.mark.parametrize("spec", SMALL, ids=["tiny", "ragged300", "zipf200"])
+@pytest.mark.parametrize("spec", SMALL, ids=["tiny", "ragged300", "zipf200", "e600"])
 def test_moe_end_to_end_small(nv, spec):
     nv, pipeline = nv
     s, w, b = _gpu_setup(pipeline, spec)
