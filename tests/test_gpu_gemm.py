@@ -255,3 +255,38 @@ def test_dense_config_full_size_sampled_rows(nv):
     assert res["ok"], res
     hq, hsf = onv.quantize_rows(gh)
     assert np.array_equal(hq, gq) and np.array_equal(hsf, gsf)
+
+
+def test_dense_l2_shape_full_size_sampled_rows(nv):
+    """The L2-shaped dense workload at full size (16384 x 7168 x 2048, BF16 rows,
+    seeded as bench.py runs it, the same launch): every tile spaces its epilogue
+    stores at the 320-cycle cap.  On sampled output rows (the first, the last and
+    rows of 32-row slices at tile edges) the BF16 rows match the float64 GEMM of
+    the oracle-quantised operands, rounded once to BF16; a second launch writes
+    the same bytes."""
+    spec = dict(inputs.CONFIGS["dense_l2"])
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    a, bw = inputs.dense_inputs(spec)
+    a_d, b_d = torch.from_numpy(a).cuda(), torch.from_numpy(bw).cuda()
+    a_q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    a_sf = torch.empty(nv.sf_bytes(M, K), dtype=torch.uint8, device="cuda")
+    b_q = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    b_sf = torch.empty(nv.sf_bytes(N, K), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_quantize(a_d, K, nv.MODE_PLAIN, a_q, a_sf)
+    nv.nvfp4_quantize(b_d, K, nv.MODE_PLAIN, b_q, b_sf)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty_like(out)
+    for o in (out, out2):
+        nv.nvfp4_grouped_gemm(a_q, a_sf, M, None, None, 1, N, K, b_q, b_sf[None], 1.0, nv.EPI_BF16, out_bf16=o)
+    nv.nvfp4_device_status()
+    assert torch.equal(out, out2)
+    ob_q, ob_sf = onv.quantize_rows(bw)
+    assert np.array_equal(host(b_q), ob_q)
+    edges = [255, 256, 8191, 8192, 16128 + 31, 16128 + 32]
+    pick = np.unique(np.concatenate([np.random.default_rng(13).choice(M, 16, replace=False), [0, M - 1], edges]))
+    oa_q, oa_sf = onv.quantize_rows(a[pick])
+    assert np.array_equal(host(a_q)[pick], oa_q)
+    ref = omoe.round_to_bf16(onv.dequantize_rows(oa_q, oa_sf) @ onv.dequantize_rows(ob_q, ob_sf).T)
+    got = out.float().cpu().numpy()[pick]
+    assert rel_frobenius(got, ref) <= 2e-3
+    assert np.mean(got == ref) > 0.97
