@@ -38,12 +38,13 @@ import inputs  # noqa: E402
 
 METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs HBM"
 
-# DRAM bytes (read + write) of one L1 launch on the prefill workload, from the
-# single-pass ncu capture summarised in profiles/nvf4_gemm_prefill_dram.md, and
-# the hash of the kernel sources it was taken on.  Reported as roofline.traffic
-# only while the sources still hash the same (a changed kernel reports null).
+# DRAM bytes (read + write) of one L1 launch per workload, from the single-pass
+# ncu launch lists summarised in profiles/nvf4_gemm_prefill_dram.md and
+# profiles/decode_step_launches.md, and the hash of the kernel sources they were
+# taken on.  Reported as roofline.traffic only while the sources still hash the
+# same (a changed kernel reports null).
 L1_TRAFFIC_RECORD = {"sources_sha256": "89279474ce31d370b09d2dc4c6a988a341f21e0c28ad41176e3effdffb308cfd",
-                     "bytes": 1728573440 + 151392256}
+                     "bytes": {"prefill": 1728573440 + 151392256, "decode": 4350776064 + 3182592}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
 
@@ -57,11 +58,13 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def l1_traffic():
+def l1_traffic(workload: str = "prefill"):
     rec = L1_TRAFFIC_RECORD
-    if rec["bytes"] is not None and rec["sources_sha256"] == kernel_sources_sha256():
-        return rec["bytes"]
+    if rec["sources_sha256"] == kernel_sources_sha256():
+        return rec["bytes"].get(workload)
     return None
+
+
 WORKLOAD = "prefill"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense ratio (FP4 / BF16 tensor peak)
 
@@ -480,6 +483,34 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         cpu = {"value": r["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{r['tokens']} sampled tokens of the {args.workload} batch in {r['seconds']:.1f} s "
                          "(float64 numpy; BLAS threads = cores, elementwise single-threaded)"}
+    # the traffic records were taken on the plain prefill and decode steps
+    plain = not (args.gather or args.two_level or args.shared_expert)
+    tensor_view = {"achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
+                   "peak_source": f"{pk['source']} bf16 sustained {pk['bf16_sustained']} x {FP4_OVER_BF16:g} "
+                                  "(nominal FP4/BF16 dense ratio)",
+                   "algorithmic": "2*T*k*(2I)*H FLOP per launch (real rows only)"}
+    if args.workload == "decode":
+        # a few rows per expert: the L1 GEMM streams the touched experts' weights
+        touched = int((b.counts > 0).sum().item())
+        rows = T * k
+        l1_bytes = touched * (2 * I) * (H // 2 + H // 16) + rows * (H // 2 + H // 16) + rows * (I // 2 + I // 16)
+        gbs = l1_bytes / (l1_ms * 1e-3) / 1e9
+        roofline = {"kernel": "L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_kernel<0, 256> (single CTAs)",
+                    "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / pk["hbm_gbs"], "peak_source": f"{pk['source']} copy bandwidth",
+                    "algorithmic": (f"W1 and its scales of the {touched} experts the batch touches, plus A1 read "
+                                    f"and A2 written for the T*k real rows: {l1_bytes} bytes per launch"),
+                    "traffic": l1_traffic("decode") if plain else None,
+                    "traffic_unit": "bytes per launch (dram read + write)",
+                    "tensor_view": dict(tensor_view, instruction_ceiling=ceiling["value"])}
+    else:
+        roofline = dict({"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
+                                    if args.workload == WORKLOAD else
+                                    "L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_kernel<0, 256> (single CTAs)"),
+                         "bound": "tensor"}, **tensor_view,
+                        traffic=l1_traffic("prefill") if plain and args.workload == WORKLOAD else None,
+                        traffic_unit="bytes per launch (dram read + write)",
+                        instruction_ceiling=dict(ceiling, frac=achieved / ceiling["value"]))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -494,17 +525,7 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                                      if args.shared_expert else "none")},
         "tokens_per_s": tokens_per_s,
         "kernel_ms": per,
-        "roofline": {"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
-                                if args.workload == WORKLOAD else
-                                "L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_kernel<0, 256> (single CTAs)"),
-                     "bound": "tensor",
-                     "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
-                     "peak_source": f"{pk['source']} bf16 sustained {pk['bf16_sustained']} x {FP4_OVER_BF16:g} "
-                                    "(nominal FP4/BF16 dense ratio)",
-                     "algorithmic": "2*T*k*(2I)*H FLOP per launch (real rows only)",
-                     "traffic": l1_traffic() if args.workload == WORKLOAD else None,
-                     "traffic_unit": "bytes per launch (dram read + write)",
-                     "instruction_ceiling": dict(ceiling, frac=achieved / ceiling["value"])},
+        "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
                 "d2h_bytes_per_step": T * H * 2,
                 "copies": "pinned host x and logits in, y out, every step; H2D and D2H on two copy streams "
