@@ -83,10 +83,8 @@ typedef enum {
 typedef enum {
   NVFP4_GEMM_TILES_AUTO = 0,   /* by shape: CTA pairs when groups average >= 256 rows */
   NVFP4_GEMM_TILES_SINGLE = 1, /* one CTA per 128-row tile */
-  NVFP4_GEMM_TILES_PAIR = 2,   /* two CTAs (a cluster) per 256-row tile, where N % 256 == 0
+  NVFP4_GEMM_TILES_PAIR = 2    /* two CTAs (a cluster) per 256-row tile, where N % 256 == 0
                                   and G <= 512 */
-  NVFP4_GEMM_TILES_QUAD = 3    /* clusters of two such pairs side by side along N, sharing
-                                  the A rows, where also N % 512 == 0 (else as _PAIR) */
 } nvfp4_gemm_tiles;
 
 /* Bytes of a swizzled SF buffer for a rows x cols matrix (cols in elements):
@@ -135,8 +133,8 @@ nvfp4_status nvfp4_global_scale(const void* in, nvfp4_in_dtype dtype, int64_t ro
  *               BF16 only: columns [g0(8) u0(8) g1(8) u1(8) ...]).  16-byte
  *               aligned, and in_ld_elems * element size a multiple of 16.
  *   out_cols    quantised columns per row, a positive multiple of 16.
- *   q_out       rows x out_cols/2 bytes, row-major (written).
- *   sf_out      nvfp4_sf_bytes(rows, out_cols) bytes, swizzled (every byte written,
+ *   q_out       rows x out_cols/2 bytes, row-major (written); 8-byte aligned.
+ *   sf_out      nvfp4_sf_bytes(rows, out_cols) bytes, swizzled, 4-byte aligned (every byte written,
  *               padding as zero).
  *   global_scale  NULL or the device fp32 encode scale g (two-level scale): the
  *               quantised values are fp32(h * g).
@@ -181,10 +179,14 @@ nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_s
  *               expert_offsets[E] are not written.  Within an expert, rows are in
  *               ascending token order (deterministic, no atomics in the order).
  *   inv_perm    int32 [T, top_k]: padded row of each (token, slot).
- *   a1_q        [R_max, H/2] NVFP4 rows of x in permuted order; padding rows
- *               inside groups are zero.  May be NULL when x_q is given (the
- *               permuted copy is then not written).
- *   a1_sf       nvfp4_sf_bytes(R_max, H) bytes, swizzled, zero on padding rows.
+ *   a1_q        [R_max, H/2] NVFP4 rows of x in permuted order.  The nibbles of
+ *               padding rows inside groups are not written: their scales are
+ *               zero, and a zero scale dequantises every E2M1 code to 0, so a
+ *               padding row is an exact zero row of the GEMMs whatever its
+ *               nibbles hold.  May be NULL when x_q is given (the permuted copy
+ *               is then not written).
+ *   a1_sf       nvfp4_sf_bytes(R_max, H) bytes, swizzled; every byte of the
+ *               groups' 128-row bands is written, zero on padding rows.
  *   x_q         NULL, or [T, H/2]: the same NVFP4 rows in token order, for an L1
  *               GEMM that gathers its A rows through perm_token (the
  *               permuted copy of a1_q is then never materialised).
@@ -217,7 +219,8 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
  *   call clears the part it counts into first); calls that overlap
  *   on the GPU race on the array.  The first call on each device looks up the
  *   array's device address (cudaGetSymbolAddress, with that device current):
- *   make that first call before any stream capture.
+ *   make that first call before any stream capture.  The address is kept until
+ *   the process exits; do not call this again on a device after cudaDeviceReset.
  * -------------------------------------------------------------------------- */
 nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, int32_t T, int32_t H,
                                       int32_t E, int32_t top_k, int32_t* topk_ids, float* topk_w,
@@ -264,8 +267,9 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  * Two kernels compute this (nvfp4_set_gemm_tiles): 128-row tiles on single CTAs,
  * or, when N % 256 == 0, 256-row tiles on CTA pairs (a 2-CTA cluster sharing one
  * cta_group::2 MMA, each CTA loading half of B), which pairs consecutive 128-row
- * blocks of a group; on request the pairs run two to a cluster, sharing A.  All
- * forms give the same results bit for bit.
+ * blocks of a group.  Both forms give the same results bit for bit.  Every TMA
+ * load reads this GPU's memory into the issuing CTA's own shared memory (no
+ * cluster multicast).
  * Limits: K a positive multiple of 256, N a positive multiple of 256 (the SwiGLU
  * epilogues) or 128 (BF16), rows_max a
  * positive multiple of 128, all pointers 16-byte aligned.
@@ -302,10 +306,9 @@ nvfp4_status nvfp4_mma_peak_probe(int32_t iters, double* tflops, double* sm_mhz,
 /* ---------------------------------------------------------------------------
  * nvfp4_set_gemm_tiles -- process-wide choice of nvfp4_grouped_gemm's tile kernel
  * (also used by nvfp4_moe_ffn_forward): NVFP4_GEMM_TILES_AUTO (the default),
- * _SINGLE, _PAIR or _QUAD (_PAIR and _QUAD fall back to single CTAs where
- * N % 256 != 0 or G > 512; _QUAD falls back to lone pairs where N % 512 != 0
- * or A rows are gathered; _AUTO never uses _QUAD's clusters).  A
- * tuning and testing control with no counterpart in the source pages; results
+ * _SINGLE or _PAIR (_PAIR falls back to single CTAs where N % 256 != 0 or
+ * G > 512).  A tuning and testing control with no counterpart in the source
+ * pages; results
  * do not depend on it.  Takes effect for calls made after it returns;
  * NVFP4_ERR_INVALID_ARG for another value.
  * -------------------------------------------------------------------------- */

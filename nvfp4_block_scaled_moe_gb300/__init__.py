@@ -191,7 +191,7 @@ def nvfp4_device_status(stream=None):
     _check(load().nvfp4_device_status(_stream(stream)))
 
 
-GEMM_TILES_AUTO, GEMM_TILES_SINGLE, GEMM_TILES_PAIR, GEMM_TILES_QUAD = 0, 1, 2, 3
+GEMM_TILES_AUTO, GEMM_TILES_SINGLE, GEMM_TILES_PAIR = 0, 1, 2
 
 
 def nvfp4_set_gemm_tiles(mode):

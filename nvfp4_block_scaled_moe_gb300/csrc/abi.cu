@@ -114,8 +114,9 @@ nvfp4_status nvfp4_quantize(const void* in, nvfp4_in_dtype dtype, nvfp4_quant_mo
             (long long)in_cols);
   const int64_t esize = dtype == NVFP4_IN_BF16 ? 2 : 4;
   CHECK_AL(al16(in) && (in_ld_elems * esize) % 16 == 0, "nvfp4_quantize: input not 16-byte aligned");
-  CHECK_AL((reinterpret_cast<uintptr_t>(q_out) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sf_out) & 3u) == 0,
-           "nvfp4_quantize: outputs must be 4-byte aligned");
+  // a 16-block's eight nibble bytes leave as one 8-byte store, a row's four scales as one word
+  CHECK_AL((reinterpret_cast<uintptr_t>(q_out) & 7u) == 0 && (reinterpret_cast<uintptr_t>(sf_out) & 3u) == 0,
+           "nvfp4_quantize: q_out must be 8-byte and sf_out 4-byte aligned");
   CHECK_AL(h_debug == nullptr || al16(h_debug), "nvfp4_quantize: h_debug not 16-byte aligned");
   CHECK_AL(al4(global_scale), "nvfp4_quantize: global_scale not 4-byte aligned");
   cudaError_t e = quantize_launch(in, dtype, mode, rows, out_cols, in_ld_elems, q_out, sf_out, 0, global_scale,

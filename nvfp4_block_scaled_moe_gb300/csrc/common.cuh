@@ -333,18 +333,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// The same tile written to every CTA of cta_mask (each at dst's offset in its
-// own shared memory); the completion of each copy is counted on the barrier at
-// `bar`'s offset in the even CTA of the destination's pair (cta_group::2).
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map, uint32_t bar, int32_t x,
-                                                    int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 // Gather of four rows y.x .. y.w (each one 128-byte box row of a map whose box
 // is 128 bytes x 1 row) into consecutive 128-byte rows at dst (which keeps the
 // map's swizzle, as a 4-row tile at that address would); x as for tma_load_2d.

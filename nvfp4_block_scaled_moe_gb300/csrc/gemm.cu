@@ -477,15 +477,9 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   const int mode = g_gemm_tiles.load(std::memory_order_relaxed);
   const int64_t groups = a.offsets != nullptr ? a.G : 1;
   const bool pair = bn == 256 && groups <= kPairMaxGroups &&
-                    (mode == NVFP4_GEMM_TILES_PAIR || mode == NVFP4_GEMM_TILES_QUAD ||
+                    (mode == NVFP4_GEMM_TILES_PAIR ||
                      (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
-  if (pair) {
-    // two pairs per cluster (sharing A) on request, where N is a multiple of 512:
-    // a third less operand traffic per SM, but clusters of 4 leave 8 of the 152
-    // SMs idle, which costs more than the traffic saves on these tiles
-    const bool quad = mode == NVFP4_GEMM_TILES_QUAD && a.N % 512 == 0 && a.a_gather == nullptr;
-    return gemm_pair_launch(a, quad ? 2 : 1, info.sms, dev, stream);
-  }
+  if (pair) return gemm_pair_launch(a, info.sms, dev, stream);
   CUtensorMap ma, mb;
   const bool gather = a.a_gather != nullptr;      // gathered A rows: a one-row box for tile::gather4
   if (!make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q,
@@ -532,8 +526,7 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
 }
 
 nvfp4_status set_gemm_tiles(int mode) {
-  if (mode != NVFP4_GEMM_TILES_AUTO && mode != NVFP4_GEMM_TILES_SINGLE && mode != NVFP4_GEMM_TILES_PAIR &&
-      mode != NVFP4_GEMM_TILES_QUAD)
+  if (mode != NVFP4_GEMM_TILES_AUTO && mode != NVFP4_GEMM_TILES_SINGLE && mode != NVFP4_GEMM_TILES_PAIR)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_set_gemm_tiles: unknown mode %d", mode);
   g_gemm_tiles.store(mode, std::memory_order_relaxed);
   return NVFP4_OK;

@@ -17,10 +17,10 @@
 //
 // Roles (320 threads per CTA, one CTA per SM):
 //   warp 0     producer: TMA loads of A (128 rows), this CTA's 128 rows of B,
-//              this CTA's A scale atoms and one 128-row band of B's scale atoms,
-//              multicast to both CTAs (every CTA multiplies against all 256 B
-//              rows, so each needs both bands).  Both CTAs' loads complete on
-//              the even CTA's full barrier, which expects the pair's bytes
+//              this CTA's A scale atoms and both 128-row bands of B's scale
+//              atoms (every CTA multiplies against all 256 B rows, so each needs
+//              both bands in its own TMEM).  Both CTAs' loads complete on the
+//              even CTA's full barrier, which expects the pair's bytes
 //              (cta_group::2 TMA);
 //   warp 1     even CTA: TMEM owner and MMA issuer (scale copies and MMAs for
 //              the pair, commits multicast to both CTAs' barriers); idle on the
@@ -120,22 +120,20 @@ __device__ __forceinline__ int last_le(const int32_t* tab, int G, int64_t v) {
   return lo;
 }
 
-// Where a tile's rows live for CTA `rank` of pair `pair_id` of the cluster.  A
-// cluster of kPairs pairs owns 256 rows x kPairs*256 columns: every pair the same
-// rows, pair q the q-th 256-column tile (p.n_tiles counts cluster column tiles).
+// Where a tile's rows live for CTA `rank` of the pair: tile = pair index (the
+// group's consecutive 128-row block pairs) * n_tiles + 256-column tile.
 struct TileRows {
   int g;            // group
-  int32_t nt;       // this pair's 256-column tile
+  int32_t nt;       // the 256-column tile
   int64_t block;    // this CTA's 128-row block
   bool has_rows;    // the block belongs to group g (and to the allocation)
 };
 
-template <int kPairs>
 __device__ __forceinline__ TileRows tile_rows(const int32_t* s_off, const int32_t* s_pair, const PairParams& p,
-                                              int64_t tile, uint32_t rank, uint32_t pair_id) {
+                                              int64_t tile, uint32_t rank) {
   TileRows t;
   const int64_t pair = tile / p.n_tiles;
-  t.nt = static_cast<int32_t>(tile - pair * p.n_tiles) * kPairs + static_cast<int32_t>(pair_id);
+  t.nt = static_cast<int32_t>(tile - pair * p.n_tiles);
   t.g = last_le(s_pair, p.G, pair);
   t.block = s_off[t.g] / kBM + 2 * (pair - s_pair[t.g]) + rank;
   t.has_rows = t.block < s_off[t.g + 1] / kBM && t.block < p.rows_max / kBM;
@@ -213,11 +211,7 @@ __device__ __forceinline__ void wait_until_clock(long long due) {
 
 // kGather: A rows come through p.a_gather (tile::gather4); a separate
 // instantiation, so the default kernels carry none of its code.
-// kPairs = 2: clusters of two pairs (4 CTAs) side by side along N.  Both pairs
-// multiply the same A rows, so each CTA loads half of its 128 A rows (and half
-// of their scale atoms) and multicasts them to its counterpart in the other
-// pair: a third less operand traffic per SM than a lone pair.
-template <int kEpi, bool kGather, int kPairs>
+template <int kEpi, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
@@ -244,17 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* s_pair = s_off + (kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  static_assert(kPairs == 1 || (kPairs == 2 && !kGather), "clusters of one pair, or two pairs without gathering");
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u, pair_id = crank >> 1;     // rank within the pair; the pair in the cluster
+  const uint32_t rank = cluster_ctarank();         // 0: the even CTA (MMA issuer), 1: the odd CTA
   const bool leader = rank == 0;
-  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair_id));
-  const int64_t cluster_id = blockIdx.x / (2 * kPairs), n_clusters = gridDim.x / (2 * kPairs);
+  const int64_t cluster_id = blockIdx.x / 2, n_clusters = gridDim.x / 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);                // the even CTA's: expect_tx of the pair's bytes
-      mbar_init(&empty[s], kPairs);          // every pair's MMA commit: the stage is refilled across pairs
+      mbar_init(&empty[s], 1);               // the pair's MMA commit (multicast to both CTAs)
     }
     for (int a = 0; a < kAcc; ++a) {
       mbar_init(&tfull[a], 1);
@@ -318,11 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0, filled = 0, fill_parity = 0;
-    const uint32_t leader_full = mapa_shared(full, crank & ~1u);
+    const uint32_t leader_full = mapa_shared(full, 0);
     bool ok = true;
     for (int64_t tile = cluster_id; tile < tiles_u && ok; tile += n_clusters) {
-      const TileRows t = tile_rows<kPairs>(s_off, s_pair, p, tile, rank, pair_id);
-      const TileRows odd = tile_rows<kPairs>(s_off, s_pair, p, tile, 1, pair_id);
+      const TileRows t = tile_rows(s_off, s_pair, p, tile, rank);
+      const TileRows odd = tile_rows(s_off, s_pair, p, tile, 1);
       const int g = __shfl_sync(0xFFFFFFFFu, t.g, 0);
       const int64_t block = __shfl_sync(0xFFFFFFFFu, t.block, 0);
       const bool has_rows = __shfl_sync(0xFFFFFFFFu, t.has_rows, 0);
@@ -342,26 +333,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
           if (leader) mbar_arrive_expect_tx(&full[stage], tx);
           if (has_rows) {
-            if constexpr (kPairs == 2) {
-              // rows 64*pair_id .. +63 of this block and scale atoms 2*pair_id, +1, for both pairs
-              const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + 2)));
-              tma_load_2d_pair_mc(smem + C::kOffA + stage * kABytes + pair_id * (kABytes / 2), &tmap_a, bar,
-                                  kb * (kBK / 2), static_cast<int32_t>(block * kBM + pair_id * 64), mask);
-              tma_load_2d_pair_mc(smem + C::kOffSfa + stage * kSfaBytes + pair_id * (kSfaBytes / 2), &tmap_sfa, bar,
-                                  0, sfa_row + kb * 8 + static_cast<int32_t>(pair_id) * 4, mask);
-            } else {
-              if (!gather)
-                tma_load_2d_pair(smem + C::kOffA + stage * kABytes, &tmap_a, bar, kb * (kBK / 2),
-                                 static_cast<int32_t>(block * kBM));
-              tma_load_2d_pair(smem + C::kOffSfa + stage * kSfaBytes, &tmap_sfa, bar, 0, sfa_row + kb * 8);
-            }
+            if (!gather)
+              tma_load_2d_pair(smem + C::kOffA + stage * kABytes, &tmap_a, bar, kb * (kBK / 2),
+                               static_cast<int32_t>(block * kBM));
+            tma_load_2d_pair(smem + C::kOffSfa + stage * kSfaBytes, &tmap_sfa, bar, 0, sfa_row + kb * 8);
           }
           tma_load_2d_pair(smem + C::kOffB + stage * kBBytes, &tmap_b, bar, kb * (kBK / 2),
                            g * p.N + t.nt * kBN + static_cast<int32_t>(rank) * (kBN / 2));
-          // B's scale atoms: this CTA loads band `rank` into both CTAs of the pair
-          const int64_t sfb_src = (static_cast<int64_t>(rank) * k4 + kb * 4) * 512;
-          tma_load_2d_pair_mc(smem + C::kOffSfb + stage * kSfbBytes + rank * (kSfbBytes / 2), &tmap_sfb, bar, 0,
-                              static_cast<int32_t>((sfb_base + sfb_src) / kSfRow), pair_mask);
+          // B's scale atoms: both bands (one 2 KiB run of four atoms each) into this CTA
+#pragma unroll
+          for (int b = 0; b < kBands; ++b) {
+            const int64_t sfb_src = (static_cast<int64_t>(b) * k4 + kb * 4) * 512;
+            tma_load_2d_pair(smem + C::kOffSfb + stage * kSfbBytes + b * 2048, &tmap_sfb, bar, 0,
+                             static_cast<int32_t>((sfb_base + sfb_src) / kSfRow));
+          }
         }
         __syncwarp();
         // gathered A: every lane copies its 4 rows (the bytes are in the pair's expect_tx)
@@ -420,13 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j)
             tc_mma_nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 4 * kBands * j,
                              (kb | j) != 0 ? 1u : 0u);
-          tc_commit_pair_mc(&empty[stage], kPairs == 2 ? 0xF : 0x3);
+          tc_commit_pair_mc(&empty[stage], 0x3);
         }
         __syncwarp();
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      if (elect_one()) tc_commit_pair_mc(&tfull[acc], pair_mask);
+      if (elect_one()) tc_commit_pair_mc(&tfull[acc], 0x3);
       __syncwarp();
       if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
     }
@@ -442,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quad = warp & 3;                // TMEM lanes 32*quad .. +31
     const uint32_t half = (warp - 2) >> 2;         // accumulator columns (kBN/2)*half .. +kBN/2-1
     const uint32_t row_in_tile = quad * 32 + lane;
-    const uint32_t leader_tempty = mapa_shared(tempty, crank & ~1u);
+    const uint32_t leader_tempty = mapa_shared(tempty, 0);
     uint8_t* stage_buf = smem + C::kOffOut + (warp - 2) * C::kStageBufBytes;
     uint32_t acc = 0, acc_phase = 0;
     bool stores_pending = false;
@@ -453,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // at K = 2048: the burst holds up the TMA loads of the next tile's stages.
     const long long store_gap = min(static_cast<long long>(p.k_blocks) * 40, 320LL);
     for (int64_t tile = cluster_id; tile < num_tiles; tile += n_clusters) {
-      const TileRows t = tile_rows<kPairs>(s_off, s_pair, p, tile, rank, pair_id);
+      const TileRows t = tile_rows(s_off, s_pair, p, tile, rank);
       const int64_t grow = t.block * kBM + row_in_tile;
       bool valid = t.has_rows;
       if (valid && p.counts != nullptr) valid = (grow - s_off[t.g]) < __ldg(p.counts + t.g);
@@ -558,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct PairDeviceInfo {
-  bool attr_set[7] = {};
-  int max_clusters[7] = {};
+  bool attr_set[4] = {};
+  int max_clusters[4] = {};
 };
 
 PairDeviceInfo& pair_info(int dev) {
@@ -572,19 +557,16 @@ std::mutex& pair_mutex() {
   return mu;
 }
 
-template <int kEpi, bool kGather, int kPairs>
+template <int kEpi, bool kGather>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  constexpr int slot = kGather ? 3 : (kPairs == 2 ? 4 : 0) + (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0
-                                                              : kEpi == NVFP4_EPI_BF16        ? 1
-                                                                                              : 2);
-  constexpr int kCtas = 2 * kPairs;
+  constexpr int slot = kGather ? 3 : (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2);
   constexpr uint32_t smem = PairCfg<kEpi>::kSmemBytes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCtas;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -597,12 +579,12 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     std::lock_guard<std::mutex> lock(pair_mutex());
     PairDeviceInfo& info = pair_info(dev);
     if (!info.attr_set[slot]) {
-      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
-      cfg.gridDim = dim3(static_cast<unsigned>(sms / kCtas * kCtas), 1, 1);
+      cfg.gridDim = dim3(static_cast<unsigned>(sms / 2 * 2), 1, 1);
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather>, &cfg);
       if (e != cudaSuccess) return e;
       info.max_clusters[slot] = n;
       info.attr_set[slot] = true;
@@ -612,16 +594,14 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   // every cluster resident at once (the tile loop strides by the cluster count)
   int64_t clusters = max_clusters < num_tiles ? max_clusters : num_tiles;
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3(static_cast<unsigned>(kCtas * clusters), 1, 1);
-  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather, kPairs>, ma, mb, msa, msb, mo, p);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather>, ma, mb, msa, msb, mo, p);
 }
 
 }  // namespace
 
-nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cudaStream_t stream) {
+nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t stream) {
   if (a.G > kMaxGroups) return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: G=%d exceeds %d", a.G, kMaxGroups);
-  if (pairs != 1 && (pairs != 2 || a.a_gather != nullptr || a.N % 512 != 0))
-    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: no %d-pair clusters for this call", pairs);
   constexpr int bn = PairCfg<NVFP4_EPI_BF16>::kBN;      // pair tile columns
   const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
   CUtensorMap ma, mb, msa, msb, mo;
@@ -630,13 +610,13 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
   const bool gather = a.a_gather != nullptr;      // gathered A rows: a one-row box for tile::gather4
   bool ok = make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q,
                          static_cast<uint64_t>(gather ? a.a_rows : a.rows_max), static_cast<uint64_t>(a.K) / 2, 1,
-                         128, gather ? 1 : 128 / pairs, true) &&
+                         128, gather ? 1 : 128, true) &&
             make_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_q, static_cast<uint64_t>(a.G) * a.N,
                          static_cast<uint64_t>(a.K) / 2, 1, 128, static_cast<uint32_t>(bn / 2), true) &&
-            make_tmap_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_sf, sfa_bytes / kSfRow, kSfRow, 1, kSfRow,
-                         8 / pairs, false) &&
-            make_tmap_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_sf, sfb_bytes / kSfRow, kSfRow, 1, kSfRow,
-                         static_cast<uint32_t>(bn / 32), false);      // half of a tile's B scale atoms
+            make_tmap_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_sf, sfa_bytes / kSfRow, kSfRow, 1, kSfRow, 8,
+                         false) &&
+            make_tmap_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_sf, sfb_bytes / kSfRow, kSfRow, 1, kSfRow, 8,
+                         false);      // one 128-row band's four atoms per box
   if (swiglu)
     ok = ok && make_tmap_2d(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.out_q, static_cast<uint64_t>(a.rows_max),
                             static_cast<uint64_t>(a.N) / 4, 1, 32, 32, false);
@@ -655,7 +635,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
   p.G = a.offsets != nullptr ? a.G : 1;
   p.N = a.N;
   p.K = a.K;
-  p.n_tiles = a.N / (bn * pairs);          // column tiles of a cluster
+  p.n_tiles = a.N / bn;
   p.k_blocks = a.K / kBK;
   p.rows_max = a.rows_max;
   p.sfb_group_bytes = static_cast<int64_t>(a.N / 128) * (a.K / 64) * 512;
@@ -674,16 +654,11 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cu
   const int64_t max_pairs = (blocks + 1) / 2 + (p.G > 1 ? p.G : 0);
   const int64_t max_tiles = max_pairs * p.n_tiles;
   if (max_tiles <= 0) return NVFP4_OK;
-#define NVFP4_PAIR_LAUNCH(E, GA, P) launch_pair<E, GA, P>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
-  const cudaError_t e =
-      gather ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true, 1)
-      : pairs == 2
-          ? (swiglu                                  ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false, 2)
-             : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false, 2)
-                                                   : NVFP4_PAIR_LAUNCH(NVFP4_EPI_BF16, false, 2))
-          : (swiglu                                  ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false, 1)
-             : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false, 1)
-                                                   : NVFP4_PAIR_LAUNCH(NVFP4_EPI_BF16, false, 1));
+#define NVFP4_PAIR_LAUNCH(E, GA) launch_pair<E, GA>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
+  const cudaError_t e = gather                                ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true)
+                        : swiglu                              ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false)
+                        : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false)
+                                                              : NVFP4_PAIR_LAUNCH(NVFP4_EPI_BF16, false);
 #undef NVFP4_PAIR_LAUNCH
   if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm (CTA pairs) launch");
   return NVFP4_OK;

@@ -76,11 +76,10 @@ struct GemmArgs {
 
 // Returns a status; writes a message with set_error_message on failure.
 nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
-// The CTA-pair kernel (N % 256 == 0, at most kPairMaxGroups groups) in clusters
-// of `pairs` pairs (2: N % 512 == 0, no gathered A); sms and dev of the current
-// device.
+// The CTA-pair kernel (N % 256 == 0, at most kPairMaxGroups groups); sms and
+// dev of the current device.
 constexpr int kPairMaxGroups = 512;
-nvfp4_status gemm_pair_launch(const GemmArgs& a, int pairs, int sms, int dev, cudaStream_t stream);
+nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t stream);
 nvfp4_status set_gemm_tiles(int mode);
 
 // 2-D tensor map of a row-major rows x cols matrix (gemm.cu).

@@ -11,7 +11,7 @@
 // then ranks its rows of every expert by token order (bit masks of the tokens
 // that picked it).  Rows of an expert therefore come in ascending token order.
 // x is quantised once per token and the bytes are written straight into the
-// token's k permuted rows; the same launch zeroes the padding rows.
+// token's k permuted rows; the same launch zeroes the padding rows' scales.
 #include <float.h>
 
 #include "common.cuh"
@@ -304,36 +304,47 @@ __global__ void __launch_bounds__(kRouteChunk) route_assign_kernel(const int32_t
 }
 
 // ---------------------------------------------------------------- scatter --
-// Zero the scale words (and, when the permuted copy is written, the nibbles) of
-// the padding rows [offsets[e] + counts[e], offsets[e+1]) of expert e (at most
-// 127 rows): part `part` of `parts` blocks, interleaved by thread.
+// The padding rows [offsets[e] + counts[e], offsets[e+1]) of expert e (at most
+// 127 rows, all inside the group's last 128-row band) get zero scale words and
+// no nibbles: a zero E4M3 scale dequantises every E2M1 code (which has no NaN or
+// infinity) to zero, so a padding row is an exact zero row of the GEMM whatever
+// its nibbles hold.  Writing only the scales moves 1/9 of the bytes.
+// In a band's scale atom (512 bytes per 64 columns), 16-byte line l holds the
+// words of rows l, l+32, l+64, l+96; work item (k4, l) of the band zeroes the
+// line with one 16-byte store when all four rows are padding, else the words of
+// its padding rows.  Part `part` of kPadParts blocks takes every kPadParts-th
+// block's worth of items.
 constexpr int kPadParts = 4;
 
 __device__ __forceinline__ void padfill_expert(int e, int part, const int32_t* __restrict__ counts,
                                                const int32_t* __restrict__ offsets, int32_t H,
-                                               uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf) {
+                                               uint8_t* __restrict__ a_sf) {
   const int64_t lo = __ldg(offsets + e) + __ldg(counts + e);
   const int64_t hi = __ldg(offsets + e + 1);
-  const int n16 = H / 32;                 // 16-byte chunks per row
+  if (hi <= lo) return;
+  const int64_t band = (hi - 1) >> 7;
+  const int first_pad = static_cast<int>(lo - band * 128);    // band-relative first padding row (1..127)
   const int k4_total = H / 64;
-  const int64_t first = static_cast<int64_t>(part) * blockDim.x + threadIdx.x;
-  const int64_t stride = static_cast<int64_t>(kPadParts) * blockDim.x;
-  const int64_t nq = a_q != nullptr ? (hi - lo) * n16 : 0;     // no permuted copy: scales only
-  for (int64_t i = first; i < nq; i += stride) {
-    const int64_t r = lo + i / n16;
-    reinterpret_cast<uint4*>(a_q + r * (H / 2))[i % n16] = make_uint4(0, 0, 0, 0);
-  }
-  const int64_t ns = (hi - lo) * k4_total;
-  for (int64_t i = first; i < ns; i += stride) {
-    const int64_t r = lo + i / k4_total;
-    *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, static_cast<uint32_t>(i % k4_total), k4_total)) = 0u;
+  const int64_t items = static_cast<int64_t>(k4_total) * 32;
+  for (int64_t i = static_cast<int64_t>(part) * blockDim.x + threadIdx.x; i < items;
+       i += static_cast<int64_t>(kPadParts) * blockDim.x) {
+    const int l = static_cast<int>(i & 31);
+    const int64_t k4 = i >> 5;
+    uint8_t* line = a_sf + (band * k4_total + k4) * 512 + l * 16;
+    if (l >= first_pad) {
+      *reinterpret_cast<uint4*>(line) = make_uint4(0, 0, 0, 0);
+    } else {
+#pragma unroll
+      for (int c = 1; c < 4; ++c)
+        if (l + 32 * c >= first_pad) *reinterpret_cast<uint32_t*>(line + 4 * c) = 0u;
+    }
   }
 }
 
 // Quantise x (PLAIN, per 16 along H) and write the bytes into each of the token's
 // k permuted rows.  Grid (kPadParts*E + T, ceil(H/1024 / warps)): blocks
-// x < kPadParts*E (with y = 0) fill part x % kPadParts of expert x / kPadParts's
-// padding rows, the others quantise token x - kPadParts*E; one warp per
+// x < kPadParts*E (with y = 0) zero part x % kPadParts of expert x / kPadParts's
+// padding scales, the others quantise token x - kPadParts*E; one warp per
 // 1024-value segment, one thread per two 16-blocks: its 16 bytes of nibbles go
 // to each row in one store (a warp writes 512 contiguous bytes), and a lane
 // pair's four scale bytes form one word of the swizzled layout.  H % 64 == 0, so
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
   if (blockIdx.x < static_cast<unsigned>(kPadParts * E)) {
     if (blockIdx.y == 0)
       padfill_expert(static_cast<int>(blockIdx.x) / kPadParts, static_cast<int>(blockIdx.x) % kPadParts, counts,
-                     offsets, H, a_q, a_sf);
+                     offsets, H, a_sf);
     return;
   }
   const int lane = threadIdx.x & 31;

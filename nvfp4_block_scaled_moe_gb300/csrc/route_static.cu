@@ -22,7 +22,10 @@
 //     streams, or from two host threads without ordering) race on the array;
 //   * the first call on each device looks up the array's device address with
 //     cudaGetSymbolAddress (with that device current); make that first call
-//     before any stream capture.
+//     before any stream capture.  The address is kept for the life of the
+//     process: after cudaDeviceReset on a device the library's module is loaded
+//     anew, so this entry point must not be used on that device again (the
+//     per-device error word of the other calls is cached the same way).
 #include <mutex>
 
 #include "common.cuh"

@@ -73,6 +73,9 @@ def test_host_validation_without_gpu(lib):
     # SwiGLU mode needs BF16
     assert lib.nvfp4_quantize(p, 1, 1, 4, 16, 32, p, p, None, None, None) == 2
     assert lib.nvfp4_quantize(p, 0, 0, 4, 16, 16, p, p, vp(base + 2), None, None) == 3    # misaligned scale
+    # the nibbles of a 16-block leave as one 8-byte store: q_out must be 8-byte aligned
+    assert lib.nvfp4_quantize(p, 0, 0, 4, 16, 16, vp(base + 4), p, None, None, None) == 3
+    assert lib.nvfp4_quantize(p, 0, 0, 4, 16, 16, p, vp(base + 2), None, None, None) == 3   # SF words: 4 bytes
     # global scale: null input, cols not a multiple of 8, misaligned output
     assert lib.nvfp4_global_scale(None, 0, 4, 16, 16, p, None) == 1
     assert lib.nvfp4_global_scale(p, 0, 4, 12, 12, p, None) == 2
@@ -110,9 +113,9 @@ def test_host_validation_without_gpu(lib):
     assert lib.nvfp4_mma_peak_probe(1 << 21, ctypes.byref(d), ctypes.byref(d), None) == 1
     assert lib.nvfp4_selftest_bounded_wait(None, 10, None) == 1
     assert b"selftest" in lib.nvfp4_last_error()
-    # tile-kernel choice: four modes, anything else refused; the default restored
-    assert lib.nvfp4_set_gemm_tiles(4) == 1 and lib.nvfp4_set_gemm_tiles(-1) == 1
-    for mode in (3, 2, 1, 0):
+    # tile-kernel choice: three modes, anything else refused; the default restored
+    assert lib.nvfp4_set_gemm_tiles(3) == 1 and lib.nvfp4_set_gemm_tiles(-1) == 1
+    for mode in (2, 1, 0):
         assert lib.nvfp4_set_gemm_tiles(mode) == 0
     with pytest.raises(nv.Nvfp4Error) as ei:
         nv._check(2)

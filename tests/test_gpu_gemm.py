@@ -62,10 +62,10 @@ def _tiles(nv, mode):
 
 
 def _both_kernels(nv, run):
-    """run() -> tuple of host arrays, on each tile kernel (single CTAs, lone CTA
-    pairs, two-pair clusters where N allows); asserts they are identical."""
+    """run() -> tuple of host arrays, on each tile kernel (single CTAs and CTA
+    pairs); asserts they are identical."""
     outs = []
-    for mode in (nv.GEMM_TILES_SINGLE, nv.GEMM_TILES_PAIR, nv.GEMM_TILES_QUAD):
+    for mode in (nv.GEMM_TILES_SINGLE, nv.GEMM_TILES_PAIR):
         with _tiles(nv, mode):
             outs.append(run())
     for o in outs[1:]:

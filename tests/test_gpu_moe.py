@@ -70,8 +70,8 @@ def test_moe_end_to_end_small(nv, spec):
     R = int(o["offsets"][-1])
     assert np.array_equal(host(b.perm_token)[:R], o["perm_token"])
     assert np.array_equal(host(b.inv_perm), o["inv_perm"])
-    assert np.array_equal(host(b.a1_q)[:R], o["a1_q"])
     real = o["perm_token"] >= 0
+    assert np.array_equal(host(b.a1_q)[:R][real], o["a1_q"][real])     # padding rows: zero scales only
     # fused L1 epilogue
     gh = host(b.h_debug)[:R]
     assert rel_frobenius(gh[real], o["h"][real]) <= 2e-3

@@ -134,12 +134,12 @@ def test_grouped_gemm_two_level_both_kernels(nv):
     ga, gb, gout = np.float32(3.7), np.array([0.9, 12.5, 0.031], np.float32), np.float32(41.0)
     alpha = 1.25
     outs = {}
-    for mode in ("single", "pair", "quad"):
+    for mode in ("single", "pair"):
         out = torch.zeros((rows_max, N), dtype=torch.bfloat16, device="cuda")
         oq = torch.full((rows_max, N // 4), 0x77, dtype=torch.uint8, device="cuda")
         osf = torch.zeros(nv.sf_bytes(rows_max, N // 2), dtype=torch.uint8, device="cuda")
         h = torch.zeros((rows_max, N // 2), dtype=torch.float32, device="cuda")
-        with _tiles(nv, {"single": nv.GEMM_TILES_SINGLE, "pair": nv.GEMM_TILES_PAIR, "quad": nv.GEMM_TILES_QUAD}[mode]):
+        with _tiles(nv, {"single": nv.GEMM_TILES_SINGLE, "pair": nv.GEMM_TILES_PAIR}[mode]):
             kw = dict(a_global_scale=_scalar(ga), b_global_scale=dev(gb))
             nv.nvfp4_grouped_gemm(a_q_d, a_sf_d, rows_max, offs, cnt, G, N, K, b_q_d, b_sf_d, alpha, nv.EPI_BF16,
                                   out_bf16=out, **kw)
@@ -148,8 +148,8 @@ def test_grouped_gemm_two_level_both_kernels(nv):
                                   out_global_scale=_scalar(gout), **kw)
         nv.nvfp4_device_status()
         outs[mode] = (out.float().cpu().numpy(), host(oq), host(osf), host(h))
-    for x, y, z in zip(outs["single"], outs["pair"], outs["quad"]):
-        assert np.array_equal(x, y) and np.array_equal(x, z)
+    for x, y in zip(outs["single"], outs["pair"]):
+        assert np.array_equal(x, y)
     got, gq, gsf_sw, gh = outs["single"]
     valid = np.concatenate([np.arange(offs_np[g], offs_np[g] + counts[g]) for g in range(G)])
     a_deq = onv.dequantize_rows(a_q, a_sf)
@@ -199,9 +199,9 @@ def test_moe_two_level_end_to_end_small(nv, spec):
     assert np.array_equal(w1_sf, o["w1_sf"])
     R = int(o["offsets"][-1])
     assert np.array_equal(host(b.offsets), o["offsets"])
-    assert np.array_equal(host(b.a1_q)[:R], o["a1_q"])
-    assert np.array_equal(onv.unswizzle_sf(host(b.a1_sf), b.rows_max, H // 16)[:R], o["a1_sf"])
     real = o["perm_token"] >= 0
+    assert np.array_equal(host(b.a1_q)[:R][real], o["a1_q"][real])     # padding rows: zero scales only
+    assert np.array_equal(onv.unswizzle_sf(host(b.a1_sf), b.rows_max, H // 16)[:R], o["a1_sf"])
     assert rel_frobenius(host(b.h_debug)[:R][real], o["h"][real]) <= 2e-3
     a2_sf = onv.unswizzle_sf(host(b.a2_sf), b.rows_max, I // 16)[:R]
     res = compare_requantised(host(b.a2_q)[:R][real], a2_sf[real], o["a2_q"][real], o["a2_sf"][real])

@@ -5,8 +5,12 @@ not call cudaMalloc mid-step).  It keeps its scratch in a fixed device array
 inside the library instead of a caller workspace.
 
 Checked through the C ABI against moe_route_permute (the workspace version) on
-two calls in a row with different inputs: every output is identical, so the
-array's leftover contents from the first call do not leak into the second.
+calls in a row with different inputs and sizes: every output is identical, so
+the array's leftover contents from one call do not leak into the next.  The
+sequence covers both ways the routing fills its per-chunk histograms: short
+batches clear the histogram and add into it, long ones (more than four chunks
+per SM's worth, here 8192 tokens) overwrite every row, and a short call right
+after a long one must not see the long call's counts.
 This file is collected last so that a failure here stops a `-x` run only after
 every other test has run.
 """
@@ -27,8 +31,10 @@ def _buffers(pipeline, spec):
 
 
 def _outputs(b, R):
+    perm = host(b.perm_token)[:R]
+    # padding rows carry zero scales and unwritten nibbles: compare the real rows' nibbles
     return dict(ids=host(b.topk_ids), w=host(b.topk_w), counts=host(b.counts), offsets=host(b.offsets),
-                perm=host(b.perm_token)[:R], inv=host(b.inv_perm), a1_q=host(b.a1_q)[:R], a1_sf=host(b.a1_sf))
+                perm=perm, inv=host(b.inv_perm), a1_q=host(b.a1_q)[:R][perm >= 0], a1_sf=host(b.a1_sf))
 
 
 def test_static_scratch_route_permute_matches_workspace_version_twice():
@@ -37,7 +43,9 @@ def test_static_scratch_route_permute_matches_workspace_version_twice():
     from nvfp4_block_scaled_moe_gb300 import pipeline
 
     specs = [inputs.moe_spec(T=1000, H=1024, I=256, E=64, top_k=6, seed=41, zipf=True),
-             inputs.moe_spec(T=256, H=7168, I=256, E=256, top_k=8, seed=42)]      # decode-sized second call
+             inputs.moe_spec(T=256, H=7168, I=256, E=256, top_k=8, seed=42),      # decode-sized second call
+             inputs.moe_spec(T=8192, H=256, I=256, E=32, top_k=4, seed=43, zipf=True),   # histogram rows overwritten
+             inputs.moe_spec(T=300, H=512, I=256, E=32, top_k=4, seed=44)]       # short again, same E as before
     for spec in specs:
         logits = dev(inputs.moe_logits(spec))
         x_t, _ = inputs.moe_x(spec)
