@@ -144,6 +144,23 @@ def moe_w2(spec: dict, e: int) -> np.ndarray:
     return (pool[w2_off[e]:w2_off[e] + n] * WEIGHT_STD).reshape(spec["H"], spec["I"])
 
 
+def moe_w1_rows(spec: dict, e: int, rows) -> np.ndarray:
+    """fp32 [len(rows), H]: the given rows of expert e's W1 (``moe_w1(spec, e)[rows]``
+    without materialising the whole matrix)."""
+    pool, w1_off, _ = moe_weight_pool(spec)
+    H = spec["H"]
+    idx = w1_off[e] + np.asarray(rows, dtype=np.int64)[:, None] * H + np.arange(H)[None, :]
+    return pool[idx] * WEIGHT_STD
+
+
+def moe_w2_rows(spec: dict, e: int, rows) -> np.ndarray:
+    """fp32 [len(rows), I]: the given rows of expert e's W2 (``moe_w2(spec, e)[rows]``)."""
+    pool, _, w2_off = moe_weight_pool(spec)
+    I = spec["I"]
+    idx = w2_off[e] + np.asarray(rows, dtype=np.int64)[:, None] * I + np.arange(I)[None, :]
+    return pool[idx] * WEIGHT_STD
+
+
 def moe_shared_weights(spec: dict, i_shared: int | None = None):
     """A shared expert's fp32 weights (W1 [2*Is, H] interleaved 8|8 like the routed
     experts, W2 [H, Is]), N(0, 0.02) on their own stream; Is defaults to I."""

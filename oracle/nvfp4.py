@@ -322,30 +322,6 @@ def unswizzle_sf(sf_swz: np.ndarray, mn: int, k_sf: int) -> np.ndarray:
     return sf_swz[off]
 
 
-def sf_tiled_bytes(mn: int, k_elems: int, tile_rows: int) -> int:
-    """Bytes of the tile-padded SF layout (``tile_sf``) of an mn x k matrix."""
-    n_tiles = -(-mn // tile_rows)
-    return n_tiles * sf_padded_bytes(tile_rows, k_elems)
-
-
-def tile_sf(sf_lin: np.ndarray, tile_rows: int) -> np.ndarray:
-    """Tile-padded SF layout: rows [t*tile_rows, (t+1)*tile_rows) of the row-major
-    SF [mn, k_sf] form tile t, a matrix of their own that is swizzled as above
-    (its rows padded with zeros to a multiple of 128), and the tiles follow one
-    another.  A layout of this library's kernels for weight tiles whose height
-    is not a multiple of the 128-row atom (the pages have no counterpart); for a
-    tile height that is a multiple of 128 it is the plain swizzled layout."""
-    sf_lin = np.asarray(sf_lin, dtype=np.uint8)
-    mn, k_sf = sf_lin.shape
-    parts = []
-    for t in range(-(-mn // tile_rows)):
-        tile = np.zeros((tile_rows, k_sf), dtype=np.uint8)
-        rows = sf_lin[t * tile_rows:(t + 1) * tile_rows]
-        tile[:len(rows)] = rows
-        parts.append(swizzle_sf_fast(tile))
-    return np.concatenate(parts) if parts else np.zeros(0, dtype=np.uint8)
-
-
 # ------------------------------------------------------- SwiGLU quantiser --
 def deinterleave_gu8(gu: np.ndarray) -> tuple:
     """Split columns interleaved at granularity 8 ([g0(8) u0(8) g1(8) u1(8) ...])

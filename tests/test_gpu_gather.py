@@ -7,11 +7,15 @@ copy of the activations is never written).
 * a grouped GEMM on gathered rows gives the same bytes as on the materialised
   permuted rows, on both tile kernels, with padding entries (-1) in the index
   (gathering is the L1 GEMM's, so its SwiGLU + NVFP4 epilogue; any other
-  epilogue with an index is refused as unsupported);
+  epilogue with an index is refused as unsupported), and its codes are within
+  the re-quantisation bound of the oracle's float64 GEMM on the rows the index
+  selects;
 * an index past the end sets the device error word and copies nothing from
   outside the matrix;
 * whole forwards with and without gathering give the same bytes (small and
-  the full-size prefill batch).
+  the full-size prefill batch), and a gathered forward matches the fully
+  CPU-quantised oracle (routing bit-exact, re-quantised codes within the bound,
+  y within relative Frobenius 2e-2).
 """
 import contextlib
 
@@ -20,9 +24,10 @@ import pytest
 import torch
 
 import inputs
+from oracle import moe as omoe
 from oracle import nvfp4 as onv
 
-from gpu_util import built_lib, dev, host
+from gpu_util import built_lib, compare_requantised, dev, host, rel_frobenius
 
 pytestmark = pytest.mark.gpu
 
@@ -125,6 +130,42 @@ def test_gathered_gemm_equals_materialised(nv):
     for r in results[1:]:
         for a, b_ in zip(results[0], r):
             assert np.array_equal(a, b_)
+    # the oracle: the rows the index selects (zero rows for -1), float64 GEMM, SwiGLU, requantisation
+    offs_np = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    a_deq = onv.dequantize_rows(a_q, a_sf)
+    b_deq = np.stack([onv.dequantize_rows(*x) for x in b])
+    oq, osf, _ = omoe.l1_swiglu_requant(omoe.grouped_gemm(a_deq, offs_np, b_deq, 1.0))
+    valid = np.concatenate([np.arange(offs_np[g], offs_np[g] + counts[g]) for g in range(G)])
+    gq, gsf_sw = results[1]                                # gathered, single CTAs (equal to every other form)
+    gsf = onv.unswizzle_sf(gsf_sw, rows_max, N // 32)
+    res = compare_requantised(gq[valid], gsf[valid], oq[valid], osf[valid])
+    assert res["ok"], res
+
+
+def test_gathered_forward_matches_oracle(nv):
+    nv, pipeline = nv
+    spec = inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=99, zipf=True)
+    s = pipeline.MoeShape(T=spec["T"], H=spec["H"], I=spec["I"], E=spec["E"], top_k=spec["top_k"])
+    w = pipeline.MoeWeights(s)
+    pool, o1, o2 = inputs.moe_weight_pool(spec)
+    w.set_from_pool(torch.from_numpy(pool).cuda(), o1, o2, float(inputs.WEIGHT_STD))
+    b = pipeline.MoeBuffers(s, gather=True)
+    x_t, x = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    y = pipeline.moe_forward(x_t.cuda(), dev(logits), w, b)
+    nv.nvfp4_device_status()
+    w1, w2 = inputs.moe_all_weights(spec)
+    o = omoe.moe_ffn(x, logits, w1, w2, spec["top_k"])
+    assert np.array_equal(host(b.topk_ids), o["ids"]) and np.array_equal(host(b.offsets), o["offsets"])
+    R = int(o["offsets"][-1])
+    assert np.array_equal(host(b.perm_token)[:R], o["perm_token"])
+    oq, _ = onv.quantize_rows(x)
+    assert np.array_equal(host(b.x_q), oq)                 # the token-order rows the L1 gathers
+    real = o["perm_token"] >= 0
+    gsf = onv.unswizzle_sf(host(b.a2_sf), R, spec["I"] // 16)
+    res = compare_requantised(host(b.a2_q)[:R][real], gsf[real], o["a2_q"][real], o["a2_sf"][real])
+    assert res["ok"], res
+    assert rel_frobenius(y.float().cpu().numpy(), o["y"]) <= 2e-2
 
 
 def test_gather_index_past_the_end_is_flagged(nv):

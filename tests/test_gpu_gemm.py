@@ -241,7 +241,9 @@ def test_dense_config_full_size_sampled_rows(nv):
     ob_q, ob_sf = onv.quantize_rows(bw)
     assert np.array_equal(host(b_q), ob_q)
     assert np.array_equal(onv.unswizzle_sf(host(b_sf), N, K // 16), ob_sf)
-    pick = np.unique(np.concatenate([np.random.default_rng(12).choice(M, 22, replace=False), [0, M - 1]]))
+    # random rows, and the last row of every 128-row band (the edge of each tile's A block)
+    pick = np.unique(np.concatenate([np.random.default_rng(12).choice(M, 22, replace=False), [0, M - 1],
+                                     np.arange(127, M, 128)]))
     oa_q, oa_sf = onv.quantize_rows(a[pick])
     assert np.array_equal(host(a_q)[pick], oa_q)
     assert np.array_equal(onv.unswizzle_sf(host(a_sf), M, K // 16)[pick], oa_sf)

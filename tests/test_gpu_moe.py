@@ -103,8 +103,9 @@ def test_moe_full_size_sampled_tokens(nv, name):
     assert np.array_equal(perm[inv.ravel()], np.repeat(np.arange(T), k))
     e_of_row = np.searchsorted(offs, inv, side="right") - 1
     assert np.array_equal(e_of_row, ids)
-    # sampled tokens, computed one by one by the oracle
-    pick = np.random.default_rng(spec["seed"]).choice(T, size=4, replace=False)
+    # sampled tokens, computed one by one by the oracle (prefill tokens mostly share
+    # the hot experts, so more of them cost little; decode tokens touch 8 new experts each)
+    pick = np.random.default_rng(spec["seed"]).choice(T, size=16 if name == "prefill" else 6, replace=False)
     tok = omoe.moe_ffn_tokens(x[pick], logits[pick], lambda e: inputs.moe_w1(spec, e),
                               lambda e: inputs.moe_w2(spec, e), k)
     assert np.array_equal(ids[pick], tok["ids"])

@@ -190,29 +190,3 @@ def test_sf_bands_concatenate():
     whole = nvfp4.swizzle_sf_fast(np.concatenate([a, b]))
     assert np.array_equal(whole, np.concatenate([nvfp4.swizzle_sf_fast(a), nvfp4.swizzle_sf_fast(b)]))
 
-
-@pytest.mark.parametrize("tile_rows,tiles", [(128, 3), (256, 2)])
-def test_tiled_sf_is_the_plain_layout_for_whole_bands(tile_rows, tiles):
-    # tiles of whole 128-row atom bands: every tile starts a band, so nothing moves
-    rng = np.random.default_rng(tile_rows)
-    lin = rng.integers(0, 256, (tile_rows * tiles, 12), dtype=np.uint8)
-    assert np.array_equal(nvfp4.tile_sf(lin, tile_rows), nvfp4.swizzle_sf_fast(lin))
-    assert nvfp4.sf_tiled_bytes(tile_rows * tiles, 16 * 12, tile_rows) == nvfp4.sf_padded_bytes(tile_rows * tiles,
-                                                                                                16 * 12)
-
-
-@pytest.mark.parametrize("mn,k_sf,tile_rows", [(672, 8, 224), (500, 5, 224), (96, 4, 32), (330, 12, 160)])
-def test_tiled_sf_each_tile_is_its_own_padded_matrix(mn, k_sf, tile_rows):
-    rng = np.random.default_rng(mn + k_sf)
-    lin = rng.integers(1, 256, (mn, k_sf), dtype=np.uint8)          # no zero scale: padding is the only zero
-    tiled = nvfp4.tile_sf(lin, tile_rows)
-    n_tiles = -(-mn // tile_rows)
-    per = nvfp4.sf_padded_bytes(tile_rows, 16 * k_sf)
-    assert len(tiled) == nvfp4.sf_tiled_bytes(mn, 16 * k_sf, tile_rows) == n_tiles * per
-    assert per == -(-tile_rows // 128) * -(-k_sf // 4) * 512
-    for t in range(n_tiles):
-        rows = lin[t * tile_rows:(t + 1) * tile_rows]
-        got = nvfp4.unswizzle_sf(tiled[t * per:(t + 1) * per], tile_rows, k_sf)
-        assert np.array_equal(got[:len(rows)], rows)
-        assert not got[len(rows):].any()                             # a ragged last tile's missing rows
-    assert np.count_nonzero(tiled) == mn * k_sf                      # padding rows and columns stay zero
