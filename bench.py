@@ -310,6 +310,92 @@ def _workload_name(spec: dict, name: str = WORKLOAD) -> str:
 
 
 # ------------------------------------------------------------ our GPU arm --
+def e2e_host_call(nv, pipeline, s, w, b, x_h, logits_h, k, steps, world, y_ref):
+    """Each step is one nvfp4_moe_forward_host call: host x and logits copied in,
+    route, FFN, combine, y copied out to host, all on one stream.  Steps alternate
+    between two device buffer sets on two streams, so one step's copies run beside
+    its neighbour's kernels.  The last step's y must equal the resident run's."""
+    import torch
+    sets = [b.enable_host_io(), pipeline.MoeBuffers(s).enable_host_io()]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    y_h = [torch.empty((s.T, s.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    main = torch.cuda.current_stream()
+    nv.nvfp4_moe_forward_host(x_h, logits_h, y_h[0], k, w, sets[1], stream=streams[1])    # warm the second set
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(main)
+    for st in streams:
+        st.wait_event(s0)
+    for i in range(steps):
+        j = i & 1
+        nv.nvfp4_moe_forward_host(x_h, logits_h, y_h[j], k, w, sets[j], stream=streams[j])
+    for st in streams:
+        main.wait_stream(st)
+    s1.record(main)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_status()
+    if not (torch.equal(y_h[(steps - 1) & 1], y_ref) and torch.equal(y_h[steps & 1], y_ref)):
+        raise RuntimeError("end-to-end: the copied-out y differs from the resident run's")
+    barrier(world)
+    del sets[1]
+    return (max_over_ranks(s0.elapsed_time(s1), world),
+            "one nvfp4_moe_forward_host C-ABI call per step: pinned host x and logits copied in, route, L1, L2, "
+            "combine, y copied out to pinned host memory, on one stream; steps alternate between two device "
+            "buffer sets on two streams, so one step's copies overlap its neighbour's kernels")
+
+
+def e2e_copy_streams(step, x_d, logits_d, b, x_h, logits_h, T, H, stream, steps, world):
+    """The variant workloads (gathering L1, two-level scale, shared expert): host
+    copies on two copy streams around the device-pointer calls, double-buffered
+    device x, logits and y; the last y must equal the resident run's."""
+    import torch
+    y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    xs, lgs, ys = [x_d, torch.empty_like(x_d)], [logits_d, torch.empty_like(logits_d)], [b.y, torch.empty_like(b.y)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer j have landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # step on buffer j finished (inputs free, y ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # y of buffer j has left
+    barrier(world)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    fetched = [False, False]
+
+    def fetch(j):
+        h2d.wait_event(ev_done[j]) if fetched[j] else h2d.wait_event(s0)
+        with torch.cuda.stream(h2d):
+            xs[j].copy_(x_h, non_blocking=True)
+            lgs[j].copy_(logits_h, non_blocking=True)
+        ev_in[j].record(h2d)
+        fetched[j] = True
+
+    fetch(0)
+    for i in range(steps):
+        j = i & 1
+        if i + 1 < steps:
+            fetch(1 - j)
+        stream.wait_event(ev_in[j])
+        if i >= 2:
+            stream.wait_event(ev_out[j])                 # y buffer j: its previous copy-out is done
+        step(x_in=xs[j], logits_in=lgs[j], y_out=ys[j])
+        ev_done[j].record(stream)
+        d2h.wait_event(ev_done[j])
+        with torch.cuda.stream(d2h):
+            y_h.copy_(ys[j], non_blocking=True)
+        ev_out[j].record(d2h)
+    stream.wait_stream(d2h)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    if not torch.equal(y_h, ys[0].cpu()):
+        raise RuntimeError("end-to-end pipeline: the copied-out y differs from the resident run's")
+    barrier(world)
+    return (max_over_ranks(s0.elapsed_time(s1), world),
+            "pinned host x and logits in, y out, every step; H2D and D2H on two copy streams overlapping the "
+            "neighbouring steps' compute (double-buffered device x, logits, y)")
+
+
 def run_ours(args, world: int, rank: int, local: int) -> None:
     import torch
 
@@ -421,59 +507,22 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     tokens_per_s = world * args.steps * T / (ms * 1e-3)
 
     # ---- end to end: every step copies its inputs in from pinned host memory and
-    # its y out to pinned host memory.  The copies run on two copy streams (one per
-    # direction) with double-buffered x, logits and y on the device: step i+1's
-    # inputs come in and step i-1's y goes out while step i computes.
+    # its y out to pinned host memory, inside the timed region.
     x_h = x_t.pin_memory()
     logits_h = torch.from_numpy(logits_np).pin_memory()
-    y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    xs, lgs, ys = [x_d, torch.empty_like(x_d)], [logits_d, torch.empty_like(logits_d)], [b.y, torch.empty_like(b.y)]
-    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer j have landed
-    ev_done = [torch.cuda.Event() for _ in range(2)]    # step on buffer j finished (inputs free, y ready)
-    ev_out = [torch.cuda.Event() for _ in range(2)]     # y of buffer j has left
-    barrier(world)
-    torch.cuda.synchronize()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-
-    def fetch(j):
-        h2d.wait_event(ev_done[j]) if fetched[j] else h2d.wait_event(s0)
-        with torch.cuda.stream(h2d):
-            xs[j].copy_(x_h, non_blocking=True)
-            lgs[j].copy_(logits_h, non_blocking=True)
-        ev_in[j].record(h2d)
-        fetched[j] = True
-
-    fetched = [False, False]
-    fetch(0)
-    for i in range(args.steps):
-        j = i & 1
-        if i + 1 < args.steps:
-            fetch(1 - j)
-        stream.wait_event(ev_in[j])
-        if i >= 2:
-            stream.wait_event(ev_out[j])                 # y buffer j: its previous copy-out is done
-        step(x_in=xs[j], logits_in=lgs[j], y_out=ys[j])
-        ev_done[j].record(stream)
-        d2h.wait_event(ev_done[j])
-        with torch.cuda.stream(d2h):
-            y_h.copy_(ys[j], non_blocking=True)
-        ev_out[j].record(d2h)
-    stream.wait_stream(d2h)
-    s1.record(stream)
-    torch.cuda.synchronize()
-    # the copied-out y of the last step equals the resident run's (same inputs)
-    if not torch.equal(y_h, ys[0].cpu()):
-        raise RuntimeError("end-to-end pipeline: the copied-out y differs from the resident run's")
-    barrier(world)
-    e2e_ms = max_over_ranks(s0.elapsed_time(s1), world)
-    e2e_value = world * args.steps * step_flops / (e2e_ms * 1e-3) / 1e12
+    plain = not (args.gather or args.two_level or args.shared_expert)
+    e2e_steps = max(args.steps, 2)             # both buffer sets take part
+    if plain:
+        y_ref = b.y.cpu()                      # the resident run's y (the same inputs every step)
+        e2e_ms, e2e_how = e2e_host_call(nv, pipeline, s, w, b, x_h, logits_h, k, e2e_steps, world, y_ref)
+    else:
+        e2e_ms, e2e_how = e2e_copy_streams(step, x_d, logits_d, b, x_h, logits_h, T, H, stream, e2e_steps, world)
+    e2e_value = world * e2e_steps * step_flops / (e2e_ms * 1e-3) / 1e12
 
     # the metric's second half: the standalone SwiGLU + NVFP4 quantiser on its own
     # workload (BF16 gate/up 32768 x 2x2048), timed after the FFN step with its own
     # clock samples, against the HBM copy bandwidth
-    del xs, lgs, ys, x_h, logits_h, y_h
+    del x_h, logits_h
     torch.cuda.empty_cache()
     q_ms, q_bytes, q_clk = time_quantizer(nv, local, steps=50, warmup=5)
 
@@ -508,7 +557,6 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                "sample": f"{r['tokens']} sampled tokens of the {args.workload} batch in {r['seconds']:.1f} s "
                          "(float64 numpy; BLAS threads = cores, elementwise single-threaded)"}
     # the traffic records were taken on the plain prefill and decode steps
-    plain = not (args.gather or args.two_level or args.shared_expert)
     tensor_view = {"achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
                    "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} x {FP4_OVER_BF16:g} "
                                   "(nominal FP4/BF16 dense ratio)",
@@ -560,9 +608,8 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         "kernel_ms": per,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
-                "d2h_bytes_per_step": T * H * 2,
-                "copies": "pinned host x and logits in, y out, every step; H2D and D2H on two copy streams "
-                          "overlapping the neighbouring steps' compute (double-buffered device x, logits, y)"},
+                "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                "copies": e2e_how},
         # per step: top-k, offsets, assign, scatter, L1, L2, combine (+ x's amax and
         # its finalisation with --two-level; + the shared expert's quantise, L1, L2)
         "gpu_launches": (7 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps,

@@ -363,6 +363,63 @@ nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const f
                          int32_t T, int32_t H, int32_t top_k, const void* shared_bf16,
                          void* y_bf16, nvfp4_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * nvfp4_moe_forward_host -- the whole path for activations and router logits
+ * in HOST memory, with the output written back to host memory ("NVFP4 MegaMoE
+ * Debug Log", "NVFP4 MoE Pipeline": stage_activation, the two GEMMs and the
+ * scatter with routing weights), as one call:
+ *   x_host -> buf->x, logits_host -> buf->logits (cudaMemcpyAsync host to
+ *   device), moe_route_permute, nvfp4_moe_ffn_forward, moe_combine, then
+ *   buf->y -> y_host (device to host), all enqueued on `stream` in that order.
+ * The call returns once the work is enqueued; y_host is complete when the
+ * stream reaches that point (synchronise the stream or record an event).
+ * Host buffers should be pinned (cudaHostAlloc / cudaHostRegister) for the
+ * copies to run asynchronously; pageable ones work but the runtime then
+ * stages them synchronously.  Overlapping consecutive calls needs two
+ * buffer sets on two streams: the copies of one then run beside the other's
+ * kernels.
+ *   x_host      BF16 [T, H]; logits_host fp32 [T, E]; y_host BF16 [T, H].
+ *   w           the expert weights (device): W1 [E, 2I, H/2] + SF, W2 [E, H, I/2] + SF,
+ *               as for nvfp4_moe_ffn_forward (one-level scales, alpha 1).
+ *   buf         device buffers, as for the three calls it makes: x [T, H] BF16,
+ *               logits [T, E], y [T, H], the routing outputs, a1 (permuted
+ *               copy) and a2 with their scales, the BF16 L2 rows and the
+ *               routing workspace; rows_max = moe_padded_rows_max(T, E, top_k).
+ * Limits and errors: those of the calls it makes (checked before anything is
+ * enqueued); NVFP4_ERR_INVALID_ARG for a null pointer or T < 1.
+ * -------------------------------------------------------------------------- */
+typedef struct {
+  const uint8_t* w1_q;
+  const uint8_t* w1_sf;
+  const uint8_t* w2_q;
+  const uint8_t* w2_sf;
+} nvfp4_moe_weights;
+
+typedef struct {
+  void* x_bf16;
+  float* logits;
+  void* y_bf16;
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* expert_counts;
+  int32_t* expert_offsets;
+  int32_t* perm_token;
+  int32_t* inv_perm;
+  uint8_t* a1_q;
+  uint8_t* a1_sf;
+  uint8_t* a2_q;
+  uint8_t* a2_sf;
+  void* rows_bf16;
+  void* workspace;
+  size_t workspace_bytes;
+  int64_t rows_max;
+} nvfp4_moe_buffers;
+
+nvfp4_status nvfp4_moe_forward_host(const void* x_host, const float* logits_host, void* y_host,
+                                    int32_t T, int32_t H, int32_t I, int32_t E, int32_t top_k,
+                                    const nvfp4_moe_weights* w, const nvfp4_moe_buffers* buf,
+                                    nvfp4_stream_t stream);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* nvfp4_last_error(void);
 

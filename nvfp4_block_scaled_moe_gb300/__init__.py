@@ -19,8 +19,8 @@ __all__ = [
     "Nvfp4Error", "lib_path", "load", "sf_bytes", "moe_padded_rows_max",
     "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
     "moe_route_permute", "moe_route_permute_static", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
-    "moe_combine", "nvfp4_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_set_gemm_tiles",
-    "nvfp4_global_scale", "nvfp4_mma_peak_probe",
+    "moe_combine", "nvfp4_moe_forward_host", "nvfp4_device_status", "nvfp4_selftest_bounded_wait",
+    "nvfp4_set_gemm_tiles", "nvfp4_global_scale", "nvfp4_mma_peak_probe",
     "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
 ]
 
@@ -45,6 +45,19 @@ def lib_path() -> str:
 
 
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+
+class _MoeWeightsC(ctypes.Structure):
+    """nvfp4_moe_weights (include/nvfp4moe.h)."""
+    _fields_ = [("w1_q", _vp), ("w1_sf", _vp), ("w2_q", _vp), ("w2_sf", _vp)]
+
+
+class _MoeBuffersC(ctypes.Structure):
+    """nvfp4_moe_buffers (include/nvfp4moe.h)."""
+    _fields_ = [("x_bf16", _vp), ("logits", _vp), ("y_bf16", _vp), ("topk_ids", _vp), ("topk_w", _vp),
+                ("expert_counts", _vp), ("expert_offsets", _vp), ("perm_token", _vp), ("inv_perm", _vp),
+                ("a1_q", _vp), ("a1_sf", _vp), ("a2_q", _vp), ("a2_sf", _vp), ("rows_bf16", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz), ("rows_max", _i64)]
 _SIGS = {
     "nvfp4_sf_bytes": (_sz, [_i64, _i64]),
     "moe_padded_rows_max": (_i64, [_i32, _i32, _i32]),
@@ -63,6 +76,8 @@ _SIGS = {
     "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_route_permute_static": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                                 _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_moe_forward_host": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                              ctypes.POINTER(_MoeWeightsC), ctypes.POINTER(_MoeBuffersC), _vp]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
@@ -178,6 +193,28 @@ def nvfp4_moe_ffn_forward(a1_q, a1_sf, expert_offsets, expert_counts, E, H, I, r
                                         _p(x_global_scale), _p(w1_global_scale), _p(a2_global_scale),
                                         _p(w2_global_scale), _p(a2_q), _p(a2_sf), _p(rows_out), _p(h_debug),
                                         _p(a1_gather), a1_gather_rows, _stream(stream)))
+
+
+def nvfp4_moe_forward_host(x_host, logits_host, y_host, top_k, weights, buffers, stream=None):
+    """The whole path from host x [T, H] BF16 and logits [T, E] fp32 to host y [T, H]
+    BF16 in one C-ABI call (copies in, route, FFN, combine, copy out, all on
+    `stream`).  Host tensors should be pinned.  ``weights`` has w1_q, w1_sf, w2_q,
+    w2_sf; ``buffers`` the device tensors x, logits, y, topk_ids, topk_w, counts,
+    offsets, perm_token, inv_perm, a1_q, a1_sf, a2_q, a2_sf, rows_out, workspace
+    and the int rows_max (pipeline.MoeBuffers with host I/O enabled)."""
+    T, H = x_host.shape
+    E = logits_host.shape[1]
+    I = 2 * buffers.a2_q.shape[1]
+    w = _MoeWeightsC(weights.w1_q.data_ptr(), weights.w1_sf.data_ptr(), weights.w2_q.data_ptr(),
+                     weights.w2_sf.data_ptr())
+    b = buffers
+    c = _MoeBuffersC(b.x.data_ptr(), b.logits.data_ptr(), b.y.data_ptr(), b.topk_ids.data_ptr(),
+                     b.topk_w.data_ptr(), b.counts.data_ptr(), b.offsets.data_ptr(), b.perm_token.data_ptr(),
+                     b.inv_perm.data_ptr(), b.a1_q.data_ptr(), b.a1_sf.data_ptr(), b.a2_q.data_ptr(),
+                     b.a2_sf.data_ptr(), b.rows_out.data_ptr(), b.workspace.data_ptr(),
+                     b.workspace.numel() * b.workspace.element_size(), b.rows_max)
+    _check(load().nvfp4_moe_forward_host(_p(x_host), _p(logits_host), _p(y_host), T, H, I, E, top_k,
+                                         ctypes.byref(w), ctypes.byref(c), _stream(stream)))
 
 
 def moe_combine(rows, inv_perm, topk_w, y, stream=None, shared=None):

@@ -285,6 +285,51 @@ nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const f
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_combine");
 }
 
+nvfp4_status nvfp4_moe_forward_host(const void* x_host, const float* logits_host, void* y_host, int32_t T,
+                                    int32_t H, int32_t I, int32_t E, int32_t top_k, const nvfp4_moe_weights* w,
+                                    const nvfp4_moe_buffers* b, nvfp4_stream_t stream) {
+  CHECK_ARG(x_host && logits_host && y_host && w && b, "nvfp4_moe_forward_host: null pointer");
+  CHECK_ARG(T >= 1, "nvfp4_moe_forward_host: T=%d", T);
+  CHECK_ARG(b->x_bf16 && b->logits && b->y_bf16 && b->rows_bf16 && b->topk_ids && b->topk_w && b->expert_counts &&
+                b->expert_offsets && b->perm_token && b->inv_perm && b->a1_q && b->a1_sf && b->a2_q && b->a2_sf &&
+                b->workspace && w->w1_q && w->w1_sf && w->w2_q && w->w2_sf,
+            "nvfp4_moe_forward_host: null device buffer");
+  // the checks of the three calls, before anything is enqueued
+  CHECK_SUP(E >= 1 && E <= 1024, "nvfp4_moe_forward_host: E=%d outside [1, 1024]", E);
+  CHECK_SUP(top_k >= 1 && top_k <= E && top_k <= 32, "nvfp4_moe_forward_host: top_k=%d", top_k);
+  CHECK_SUP(H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0,
+            "nvfp4_moe_forward_host: H=%d and I=%d must be positive multiples of 256", H, I);
+  CHECK_ARG(b->rows_max >= moe_padded_rows_max(T, E, top_k),
+            "nvfp4_moe_forward_host: rows_max=%lld < moe_padded_rows_max", (long long)b->rows_max);
+  CHECK_ARG(b->workspace_bytes >= moe_route_permute_workspace(T, H, E, top_k),
+            "nvfp4_moe_forward_host: workspace too small");
+  CHECK_AL(al16(b->x_bf16) && al16(b->y_bf16) && al16(b->rows_bf16) && al16(b->a1_q) && al16(b->a1_sf) &&
+               al16(b->a2_q) && al16(b->a2_sf) && al16(b->workspace) && al16(w->w1_q) && al16(w->w1_sf) &&
+               al16(w->w2_q) && al16(w->w2_sf),
+           "nvfp4_moe_forward_host: device buffers must be 16-byte aligned");
+  CHECK_SUP(b->rows_max % 128 == 0 && b->rows_max < (int64_t(1) << 31),
+            "nvfp4_moe_forward_host: rows_max=%lld is not a multiple of 128", (long long)b->rows_max);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t xy_bytes = static_cast<size_t>(T) * H * 2;
+  cudaError_t e = cudaMemcpyAsync(b->x_bf16, x_host, xy_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b->logits, logits_host, static_cast<size_t>(T) * E * sizeof(float), cudaMemcpyHostToDevice,
+                        s);
+  if (e != cudaSuccess) return fail_cuda(e, "nvfp4_moe_forward_host: copy in");
+  nvfp4_status st = moe_route_permute(b->logits, b->x_bf16, T, H, E, top_k, b->topk_ids, b->topk_w,
+                                      b->expert_counts, b->expert_offsets, b->perm_token, b->inv_perm, b->a1_q,
+                                      b->a1_sf, nullptr, nullptr, b->workspace, b->workspace_bytes, stream);
+  if (st != NVFP4_OK) return st;
+  st = nvfp4_moe_ffn_forward(b->a1_q, b->a1_sf, b->expert_offsets, b->expert_counts, E, H, I, b->rows_max, w->w1_q,
+                             w->w1_sf, w->w2_q, w->w2_sf, 1.0f, 1.0f, nullptr, nullptr, nullptr, nullptr, b->a2_q,
+                             b->a2_sf, b->rows_bf16, nullptr, nullptr, 0, stream);
+  if (st != NVFP4_OK) return st;
+  st = moe_combine(b->rows_bf16, b->inv_perm, b->topk_w, T, H, top_k, nullptr, b->y_bf16, stream);
+  if (st != NVFP4_OK) return st;
+  e = cudaMemcpyAsync(y_host, b->y_bf16, xy_bytes, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_moe_forward_host: copy out");
+}
+
 nvfp4_status nvfp4_device_status(nvfp4_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "nvfp4_device_status: stream");

@@ -64,6 +64,15 @@ class MoeBuffers:
         self.x_gs = torch.ones(1, dtype=f32, device=device)       # x's encode scale (two-level forwards)
         self.a2_gs = None                                         # L1 output's encode scale, once calibrated
 
+    def enable_host_io(self):
+        """Device x and logits for the host-buffer call (nvfp4_moe_forward_host), which
+        copies the host inputs into them; y is the output row buffer above."""
+        s = self.shape
+        dev = self.y.device
+        self.x = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
+        self.logits = torch.empty((s.T, s.E), dtype=torch.float32, device=dev)
+        return self
+
     def enable_h_debug(self):
         # zeros: the GEMM writes h only for real rows
         self.h_debug = torch.zeros((self.rows_max, self.shape.I), dtype=torch.float32, device=self.a2_sf.device)

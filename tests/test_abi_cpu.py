@@ -105,6 +105,20 @@ def test_host_validation_without_gpu(lib):
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
                                   None, p, 64, None) == 2
     assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None, 0, None) == 2
+    # the host-buffer forward: null pointers, no tokens, a short workspace, an unaligned buffer
+    import nvfp4_block_scaled_moe_gb300 as nvb
+    wts = nvb._MoeWeightsC(base, base, base, base)
+    bufs = nvb._MoeBuffersC(*([base] * 15), 1 << 20, 1024)
+    assert lib.nvfp4_moe_forward_host(None, p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(bufs),
+                                      None) == 1
+    assert lib.nvfp4_moe_forward_host(p, p, p, 0, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(bufs), None) == 1
+    assert lib.nvfp4_moe_forward_host(p, p, p, 4, 500, 256, 8, 2, ctypes.byref(wts), ctypes.byref(bufs), None) == 2
+    short = nvb._MoeBuffersC(*([base] * 15), 4, 1024)
+    assert lib.nvfp4_moe_forward_host(p, p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(short),
+                                      None) == 1
+    odd_buf = nvb._MoeBuffersC(*([base] * 9 + [base + 8] + [base] * 5), 1 << 20, 1024)
+    assert lib.nvfp4_moe_forward_host(p, p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(odd_buf),
+                                      None) == 3
     assert lib.moe_combine(p, p, p, 4, 12, 2, None, p, None) == 2
     assert lib.moe_combine(p, p, p, 4, 16, 2, vp(base + 8), p, None) == 3     # misaligned shared rows
     d = ctypes.c_double(0.0)

@@ -117,3 +117,28 @@ def test_moe_full_size_sampled_tokens(nv, name):
     assert res["ok"], res
     got = y.float().cpu().numpy()[pick]
     assert rel_frobenius(got, tok["y"]) <= 2e-2
+
+
+def test_forward_from_host_buffers(nv):
+    """nvfp4_moe_forward_host: host x and logits in, host y out, one C-ABI call.
+    Its y equals the device-pointer forward's bit for bit (the same kernels on
+    the same inputs) and is within the oracle bound; two calls in a row on
+    alternating buffer sets and streams give the same bytes."""
+    nv, pipeline = nv
+    spec = inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=24, zipf=True)
+    s, w, b = _gpu_setup(pipeline, spec)
+    x_t, x = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    y_dev = pipeline.moe_forward(x_t.cuda(), dev(logits), w, b).cpu()
+    x_h, logits_h = x_t.pin_memory(), torch.from_numpy(logits).pin_memory()
+    sets = [pipeline.MoeBuffers(s).enable_host_io(), pipeline.MoeBuffers(s).enable_host_io()]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.zeros((spec["T"], spec["H"]), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    for j in range(2):
+        nv.nvfp4_moe_forward_host(x_h, logits_h, outs[j], spec["top_k"], w, sets[j], stream=streams[j])
+    torch.cuda.synchronize()
+    nv.nvfp4_device_status()
+    assert torch.equal(outs[0], y_dev) and torch.equal(outs[1], y_dev)
+    w1, w2 = inputs.moe_all_weights(spec)
+    ref = omoe.moe_ffn(x, logits, w1, w2, spec["top_k"])["y"]
+    assert rel_frobenius(outs[0].float().numpy(), ref) <= 2e-2
