@@ -42,8 +42,8 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # of that single launch (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # hash of the kernel sources it was taken on.  Reported as roofline.traffic only
 # while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "89279474ce31d370b09d2dc4c6a988a341f21e0c28ad41176e3effdffb308cfd",
-                     "bytes": {"prefill": 1728573440 + 151392256, "decode": 4350776064 + 3182592}}
+L1_TRAFFIC_RECORD = {"sources_sha256": "180c6522392c80241a36c2311516414d2099c5ce87ab905126b84a7229bba0ad",
+                     "bytes": {"prefill": 1728777984 + 154623744, "decode": 4350365440 + 6521600}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
 

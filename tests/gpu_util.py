@@ -33,7 +33,7 @@ def e2m1_step_distance(a_nib, b_nib):
 
 
 def compare_requantised(gpu_q, gpu_sf_rows, ora_q, ora_sf_rows, max_frac=1e-3):
-    """The benchmark spec's bound for re-quantised NVFP4: at most 0.1% of nibbles differ,
+    """The path's bound for re-quantised NVFP4: at most 0.1% of nibbles differ,
     each by at most one E2M1 step (a nibble of a block whose scale code differs
     is compared after that block is excluded; such blocks are also <= 0.1%)."""
     gn, on = onv.unpack_nibbles(gpu_q), onv.unpack_nibbles(ora_q)

@@ -19,7 +19,7 @@ For each picked row (token t, slot j of expert e):
     random ones, against the oracle's float64 GEMM
     of the GPU's own a2 row (dequantised by the oracle) with the W2 rows of
     those columns, rounded once to BF16.  Bound: relative Frobenius 2e-3 (the
-    spec bound for fused-path GEMM outputs fed the GPU's own quantised
+    path's bound for fused-path GEMM outputs fed the GPU's own quantised
     intermediates) and nearly all values identical.
 The dense L1 workload's rows and the end-to-end y of sampled tokens are
 checked against the fully CPU-quantised oracle in test_gpu_gemm.py and
