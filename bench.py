@@ -2,15 +2,23 @@
 
 One step = one pass of the whole path over one batch: moe_route_permute
 (top-k routing, padded permutation, NVFP4 staging of x) -> L1 grouped GEMM with
-the fused SwiGLU + NVFP4 epilogue -> L2 grouped GEMM -> moe_combine.  The
-default workload is the prefill batch: T=16384 tokens, H=7168, I=2048, E=256
-experts, top-8, Zipf-skewed routing (seeded synthetic data).
+the fused SwiGLU + NVFP4 epilogue -> L2 grouped GEMM -> the routing-weighted
+combine.  By default a batch's combine runs inside the next step's L1 GEMM, on
+two spare warps per CTA (batches alternate between two buffer sets); the last
+batch's combine runs after the last step, inside the timed region, so the
+region holds every batch's whole path (and one combine more).
+`--no-overlap-combine` runs each batch's combine as its own launch at the end
+of its step.  The default workload is the prefill batch: T=16384 tokens,
+H=7168, I=2048, E=256 experts, top-8, Zipf-skewed routing (seeded synthetic
+data).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` is whole-job TFLOP/s of the FFN
 (algorithmic FLOPs 6*k*H*I per token, padding rows not credited) with inputs
-resident in HBM; `e2e` repeats the measurement with the inputs copied from
+resident in HBM; `e2e` repeats the measurement through the library's
+host-buffer calls (nvfp4_moe_step_host / nvfp4_moe_finish_host, or
+nvfp4_moe_forward_host without the overlap), with the inputs copied from
 pinned host memory and the output copied back inside the timed region.
 Under torchrun each rank runs its own batch (weak scaling, no data-path
 collective); the timed region is bracketed by barriers and the max over ranks
@@ -42,8 +50,8 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # of that single launch (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # hash of the kernel sources it was taken on.  Reported as roofline.traffic only
 # while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "180c6522392c80241a36c2311516414d2099c5ce87ab905126b84a7229bba0ad",
-                     "bytes": {"prefill": 1728777984 + 154623744, "decode": 4350365440 + 6521600}}
+L1_TRAFFIC_RECORD = {"sources_sha256": None,
+                     "bytes": {}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
 
@@ -57,10 +65,12 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def l1_traffic(workload: str = "prefill"):
+def l1_traffic(key: str = "prefill"):
+    """The recorded traffic of one L1 launch: key is the workload, with
+    "_overlap" when the launch also runs the previous batch's combine."""
     rec = L1_TRAFFIC_RECORD
     if rec["sources_sha256"] == kernel_sources_sha256():
-        return rec["bytes"].get(workload)
+        return rec["bytes"].get(key)
     return None
 
 
@@ -346,6 +356,59 @@ def e2e_host_call(nv, pipeline, s, w, b, x_h, logits_h, k, steps, world, y_ref):
             "buffer sets on two streams, so one step's copies overlap its neighbour's kernels")
 
 
+def e2e_step_host(nv, pipeline, s, w, b, x_h, logits_h, k, steps, world, y_ref):
+    """Each step is one nvfp4_moe_step_host C-ABI call: host x and logits copied in,
+    route, L1 (also running the previous batch's combine on spare warps), L2, and
+    the previous batch's y copied out to host; one nvfp4_moe_finish_host call
+    after the last step combines the last batch and copies its y out.  Steps
+    rotate over three device buffer sets on three streams, each step's kernels
+    waiting for the previous step's.  On one stream a step's copy-in queues
+    behind the copy-out of the step three back, so each copy pair has two steps'
+    kernels to hide behind.  Every batch's y must equal the resident run's."""
+    import torch
+    n_sets = 3
+    sets = [b.enable_host_io()] + [pipeline.MoeBuffers(s).enable_host_io() for _ in range(n_sets - 1)]
+    streams = [torch.cuda.Stream() for _ in range(n_sets)]
+    done = [torch.cuda.Event() for _ in range(n_sets)]
+    for ev, st in zip(done, streams):
+        ev.record(st)                              # the events exist from here on
+    y_h = [torch.zeros((s.T, s.H), dtype=torch.bfloat16).pin_memory() for _ in range(n_sets)]
+    main = torch.cuda.current_stream()
+
+    def run(n):
+        for i in range(n):
+            j, p = i % n_sets, (i - 1) % n_sets
+            nv.nvfp4_moe_step_host(x_h, logits_h, k, w, sets[j], prev=sets[p] if i else None,
+                                   prev_y_host=y_h[p] if i else None, compute_after=done[p] if i else None,
+                                   compute_done=done[j], stream=streams[j])
+        last = (n - 1) % n_sets
+        nv.nvfp4_moe_finish_host(sets[last], k, y_h[last], stream=streams[last])
+
+    run(n_sets)                                    # warm every set (untimed)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(main)
+    for st in streams:
+        st.wait_event(s0)
+    run(steps)
+    for st in streams:
+        main.wait_stream(st)
+    s1.record(main)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_status()
+    if not all(torch.equal(y, y_ref) for y in y_h):
+        raise RuntimeError("end-to-end: a copied-out y differs from the resident run's")
+    barrier(world)
+    del sets[1:]
+    return (max_over_ranks(s0.elapsed_time(s1), world),
+            "one nvfp4_moe_step_host C-ABI call per step: pinned host x and logits copied in, route, L1 (also "
+            "combining the previous batch on spare warps), L2, the previous batch's y copied out to pinned host "
+            "memory; one nvfp4_moe_finish_host call for the last batch; steps rotate over three device buffer sets "
+            "on three streams (each step's kernels wait for the previous step's), so copies overlap kernels")
+
+
 def e2e_copy_streams(step, x_d, logits_d, b, x_h, logits_h, T, H, stream, steps, world):
     """The variant workloads (gathering L1, two-level scale, shared expert): host
     copies on two copy streams around the device-pointer calls, double-buffered
@@ -468,6 +531,42 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         if events:
             events[5].record(stream)
 
+    # --overlap-combine: batches alternate between two buffer sets, and each step's
+    # L1 GEMM also runs the previous batch's combine on two spare warps per CTA;
+    # the last batch's combine runs after the last step, inside the timed region
+    ov = args.overlap_combine
+    sets = [b, pipeline.MoeBuffers(s)] if ov else [b]
+    n_done = [0]                       # batches stepped so far (their parity picks the set)
+
+    def step_ov(events=None):
+        i = n_done[0]
+        cur, prev = sets[i & 1], (sets[(i - 1) & 1] if i > 0 else None)
+        if events:
+            events[0].record(stream)
+        nv.moe_route_permute(logits_d, x_d, k, cur.topk_ids, cur.topk_w, cur.counts, cur.offsets, cur.perm_token,
+                             cur.inv_perm, cur.a1_q, cur.a1_sf, cur.workspace)
+        if events:
+            events[1].record(stream)
+        job = None if prev is None else (prev.rows_out, prev.inv_perm, prev.topk_w, prev.y)
+        nv.nvfp4_grouped_gemm(cur.a1_q, cur.a1_sf, R, cur.offsets, cur.counts, E, 2 * I, H, w.w1_q, w.w1_sf, 1.0,
+                              nv.EPI_SWIGLU_NVFP4, out_q=cur.a2_q, out_sf=cur.a2_sf, side_combine=job)
+        if events:
+            events[2].record(stream)
+        nv.nvfp4_grouped_gemm(cur.a2_q, cur.a2_sf, R, cur.offsets, cur.counts, E, H, I, w.w2_q, w.w2_sf, 1.0,
+                              nv.EPI_BF16, out_bf16=cur.rows_out)
+        if events:
+            events[3].record(stream)
+            events[4].record(stream)
+            events[5].record(stream)
+        n_done[0] += 1
+
+    def finish_ov():
+        last = sets[(n_done[0] - 1) & 1]
+        nv.moe_combine(last.rows_out, last.inv_perm, last.topk_w, last.y)
+
+    if ov:
+        step = step_ov                 # noqa: F811 (the overlapped step replaces the plain one)
+
     ceiling = mma_ceiling(nv)
     # the clock sampler starts before the warm-up so that no idle gap (in which the
     # GPU drops its clocks) separates the warm-up from the timed region
@@ -487,6 +586,10 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     start.record(stream)
     for i in range(args.steps):
         step(ev[i])
+    if ov:
+        tail0 = torch.cuda.Event(enable_timing=True)
+        tail0.record(stream)
+        finish_ov()
     end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop(t_region, time.time())
@@ -497,6 +600,24 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     names = ("route_permute", "l1_gemm_swiglu_nvfp4", "l2_gemm_bf16", "shared_expert", "combine")
     per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
            for j, name in enumerate(names) if name != "shared_expert" or sh is not None}
+    if ov:
+        per["combine"] = 0.0           # inside each step's L1 (the previous batch's)
+        per["last_batch_combine_once"] = tail0.elapsed_time(end)
+
+
+    # with the overlap, each L1 launch also streams the previous batch's combine:
+    # time the L1 GEMM alone too (live, after the timed region, 5 launches)
+    l1_alone_ms = None
+    if ov:
+        cur = sets[(n_done[0] - 1) & 1]
+        evs_alone = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+        for e0, e1 in evs_alone:
+            e0.record(stream)
+            nv.nvfp4_grouped_gemm(cur.a1_q, cur.a1_sf, R, cur.offsets, cur.counts, E, 2 * I, H, w.w1_q, w.w1_sf,
+                                  1.0, nv.EPI_SWIGLU_NVFP4, out_q=cur.a2_q, out_sf=cur.a2_sf)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        l1_alone_ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs_alone)
 
     l1, l2 = ffn_flops(T, H, I, k)
     step_flops = l1 + l2
@@ -514,7 +635,8 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     e2e_steps = max(args.steps, 2)             # both buffer sets take part
     if plain:
         y_ref = b.y.cpu()                      # the resident run's y (the same inputs every step)
-        e2e_ms, e2e_how = e2e_host_call(nv, pipeline, s, w, b, x_h, logits_h, k, e2e_steps, world, y_ref)
+        e2e = e2e_step_host if ov else e2e_host_call
+        e2e_ms, e2e_how = e2e(nv, pipeline, s, w, b, x_h, logits_h, k, e2e_steps, world, y_ref)
     else:
         e2e_ms, e2e_how = e2e_copy_streams(step, x_d, logits_d, b, x_h, logits_h, T, H, stream, e2e_steps, world)
     e2e_value = world * e2e_steps * step_flops / (e2e_ms * 1e-3) / 1e12
@@ -584,11 +706,20 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                     "traffic_gbs": traffic / (l1_ms * 1e-3) / 1e9 if traffic else None,
                     "tensor_view": dict(tensor_view, instruction_ceiling=ceil_tf)}
     else:
+        side = None
+        if ov and args.workload == WORKLOAD:
+            comb_bytes = T * k * H * 2 + T * H * 2 + T * k * 8
+            side = {"what": "each L1 launch also runs the previous batch's combine on two spare warps per CTA",
+                    "bytes": comb_bytes, "gbs_over_launch": comb_bytes / (l1_ms * 1e-3) / 1e9,
+                    "l1_alone_ms": l1_alone_ms,
+                    "l1_alone_achieved": l1 / (l1_alone_ms * 1e-3) / 1e12,
+                    "l1_alone_frac": l1 / (l1_alone_ms * 1e-3) / 1e12 / fp4_peak}
         roofline = dict({"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
                                     if args.workload == WORKLOAD else
                                     "L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_kernel<0, 256> (single CTAs)"),
-                         "bound": "tensor"}, **tensor_view,
-                        traffic=l1_traffic("prefill") if plain and args.workload == WORKLOAD else None,
+                         "bound": "tensor"}, **tensor_view, side_job=side,
+                        traffic=(l1_traffic("prefill_overlap" if ov else "prefill")
+                                 if plain and args.workload == WORKLOAD else None),
                         traffic_unit="bytes per launch (dram read + write)",
                         gemms=gemms,
                         instruction_ceiling=dict(ceiling, frac=achieved / ceil_tf))
@@ -603,7 +734,10 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                               "(per expert) and the L1 output (calibrated once), plus the per-16 E4M3 scales"
                               if args.two_level else "per-16 E4M3 block scales (global scale 1)"),
                    "shared_expert": (f"one shared expert (I={I}) on every token, FLOPs credited"
-                                     if args.shared_expert else "none")},
+                                     if args.shared_expert else "none"),
+                   "combine": ("each batch's combine runs inside the next step's L1 GEMM (two spare warps per CTA); "
+                               "the last batch's after the last step, inside the timed region"
+                               if ov else "its own launch at the end of each step")},
         "tokens_per_s": tokens_per_s,
         "kernel_ms": per,
         "roofline": roofline,
@@ -612,7 +746,8 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                 "copies": e2e_how},
         # per step: top-k, offsets, assign, scatter, L1, L2, combine (+ x's amax and
         # its finalisation with --two-level; + the shared expert's quantise, L1, L2)
-        "gpu_launches": (7 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps,
+        "gpu_launches": ((6 if ov else 7) + (2 if args.two_level else 0) + (3 if args.shared_expert else 0))
+                        * args.steps + (1 if ov else 0),
         "clocks": clk,
         "quantize": quantize,
         "cpu_baseline": cpu,
@@ -909,6 +1044,10 @@ def main():
     ap.add_argument("--shared-expert", action="store_true",
                     help="prefill/decode plus one shared expert (a dense NVFP4 FFN of every token, I = the "
                          "routed experts' I) added in the combine")
+    ap.add_argument("--overlap-combine", action=argparse.BooleanOptionalAction, default=None,
+                    help="prefill/decode: each step's L1 GEMM also runs the previous batch's combine on spare warps "
+                         "(batches alternate between two buffer sets; the last batch's combine runs after the last "
+                         "step, inside the timed region). On by default for the plain prefill step")
     ap.add_argument("--two-level", action="store_true",
                     help="prefill/decode with the two-level scale (per-tensor encode scales next to the per-16 "
                          "ones); the CPU baseline stays the one-level oracle")
@@ -922,6 +1061,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    variant = args.gather or args.two_level or args.shared_expert
+    if args.overlap_combine and variant:
+        ap.error("--overlap-combine runs the plain path (no --gather, --two-level or --shared-expert)")
+    if args.overlap_combine is None:
+        # on by default where L1 runs on CTA pairs (prefill); a decode batch's L1
+        # runs on single CTAs, where the combine would be its own launch anyway
+        args.overlap_combine = not variant and args.workload == "prefill"
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

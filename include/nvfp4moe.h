@@ -99,6 +99,20 @@ int64_t moe_padded_rows_max(int32_t T, int32_t E, int32_t top_k);
 /* Bytes of device workspace moe_route_permute needs. */
 size_t moe_route_permute_workspace(int32_t T, int32_t H, int32_t E, int32_t top_k);
 
+/* A combine left over from an earlier batch: moe_combine's arguments without
+ * shared rows, y = bf16( sum_j w[t, j] * rows[inv_perm[t, j], :] ).  The
+ * CTA-pair L1 GEMM (the SwiGLU + NVFP4 epilogue) can run it on two spare warps
+ * per CTA while it computes; see nvfp4_grouped_gemm's side_combine. */
+typedef struct {
+  const void* rows_bf16;       /* BF16 [*, H]: the earlier batch's L2 rows (16-byte aligned) */
+  const int32_t* inv_perm;     /* int32 [T, top_k] */
+  const float* topk_w;         /* fp32 [T, top_k] */
+  int32_t T;                   /* tokens of the earlier batch (0: no job) */
+  int32_t top_k;               /* 1 .. 32 */
+  int32_t H;                   /* row length, a positive multiple of 8 */
+  void* y_bf16;                /* BF16 [T, H], written (16-byte aligned) */
+} nvfp4_combine_job;
+
 /* Two-level scale.  The pages' pipeline carries a per-tensor fp32 global scale
  * beside the per-16 E4M3 scales ("NVFP4 MegaMoE Debug Log", "NVFP4 MoE Pipeline":
  * stage_activation returns an input_global_scale; each GEMM's alpha is
@@ -257,6 +271,15 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *               the end reads row 0 and sets the device error word.  a_sf keeps
  *               the rows_max-row layout.  Supported with NVFP4_EPI_SWIGLU_NVFP4
  *               (the L1 GEMM); NVFP4_ERR_UNSUPPORTED otherwise.
+ *   side_combine  NULL, or the combine of an EARLIER batch to run alongside
+ *               (see nvfp4_combine_job).  Its inputs must be complete when this
+ *               call's work starts on `stream`, and its buffers must not
+ *               overlap this call's.  With the SwiGLU + NVFP4 epilogue on CTA
+ *               pairs, two extra warps per CTA stream it while the GEMM runs:
+ *               the GEMM moves little DRAM traffic of its own, so the combine's
+ *               HBM time mostly hides.  Otherwise it runs as its own launch
+ *               first.  Either way y equals moe_combine's bit for bit (the
+ *               same fp32 slot-order sum and one rounding).
  *   epilogue    NVFP4_EPI_SWIGLU_NVFP4: N columns interleaved 8|8 as gate/up;
  *               h = silu(alpha*g) * (alpha*u) quantised as in nvfp4_quantize ->
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
@@ -281,7 +304,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 const float* b_global_scale, const float* out_global_scale,
                                 nvfp4_epilogue epilogue, uint8_t* out_q, uint8_t* out_sf,
                                 void* out_bf16, float* h_debug, const int32_t* a_gather,
-                                int64_t a_gather_rows, nvfp4_stream_t stream);
+                                int64_t a_gather_rows, const nvfp4_combine_job* side_combine,
+                                nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_mma_peak_probe -- measures the issue ceiling of the block-scaled FP4
@@ -314,6 +338,7 @@ nvfp4_status nvfp4_mma_peak_probe(int32_t iters, double* tflops, double* sm_mhz,
  * -------------------------------------------------------------------------- */
 nvfp4_status nvfp4_set_gemm_tiles(int32_t mode);
 
+
 /* ---------------------------------------------------------------------------
  * nvfp4_moe_ffn_forward -- L1 GEMM with the fused SwiGLU + NVFP4 epilogue, then
  * the L2 GEMM ("NVFP4 MegaMoE Debug Log", "NVFP4 MoE Pipeline"; the fused FP4
@@ -336,6 +361,10 @@ nvfp4_status nvfp4_set_gemm_tiles(int32_t mode);
  *   a1_gather, a1_gather_rows  NULL, or L1 gathers its A rows: a1_q is
  *                moe_route_permute's x_q [T, H/2] and a1_gather its perm_token
  *                (a1_gather_rows = T); see nvfp4_grouped_gemm.
+ *   prev_combine NULL, or the combine of an EARLIER batch with the same H,
+ *                handed to the L1 GEMM as its side_combine (nvfp4_grouped_gemm).
+ *                A serving loop then runs route(i), ffn(i) with combine(i-1), and
+ *                so on, and one plain moe_combine after the last batch.
  * Limits: H and I positive multiples of 256, rows_max a positive multiple of 128.
  * -------------------------------------------------------------------------- */
 nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
@@ -347,7 +376,8 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf,
                                    const float* w1_global_scale, const float* a2_global_scale,
                                    const float* w2_global_scale, uint8_t* a2_q, uint8_t* a2_sf,
                                    void* rows_out_bf16, float* h_debug, const int32_t* a1_gather,
-                                   int64_t a1_gather_rows, nvfp4_stream_t stream);
+                                   int64_t a1_gather_rows, const nvfp4_combine_job* prev_combine,
+                                   nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_combine -- "scatter with routing weights" ("NVFP4 MegaMoE Debug Log",
@@ -419,6 +449,38 @@ nvfp4_status nvfp4_moe_forward_host(const void* x_host, const float* logits_host
                                     int32_t T, int32_t H, int32_t I, int32_t E, int32_t top_k,
                                     const nvfp4_moe_weights* w, const nvfp4_moe_buffers* buf,
                                     nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_moe_step_host / nvfp4_moe_finish_host -- a serving loop over batches in
+ * host memory, in which each batch's combine runs inside the NEXT batch's L1
+ * GEMM (see nvfp4_grouped_gemm's side_combine).  One step, enqueued on `stream`:
+ *   1. x_host -> buf->x_bf16, logits_host -> buf->logits (host to device);
+ *   2. if compute_after is not NULL, wait for it (cudaStreamWaitEvent);
+ *   3. moe_route_permute and nvfp4_moe_ffn_forward of this batch into buf; if
+ *      prev is not NULL, the L1 GEMM also runs the pending combine of the
+ *      batch in prev (prev_T tokens) into prev->y_bf16;
+ *   4. if compute_done is not NULL, record it;
+ *   5. if prev is not NULL, prev->y_bf16 -> prev_y_host (device to host).
+ * This batch's combine stays pending in buf: a later step passes buf as its
+ * prev, or nvfp4_moe_finish_host runs it (moe_combine, then y -> y_host).
+ * Alternating two buffer sets on two streams, with each step's compute_after
+ * the previous step's compute_done, lets one step's copies run beside the
+ * other's kernels while the combines hide inside the L1 GEMMs.  The caller owns
+ * the events (cudaEventCreateWithFlags(..., cudaEventDisableTiming) will do)
+ * and keeps a set's buffers alive until its y has been copied out.  Arguments
+ * as for nvfp4_moe_forward_host; prev, when given, must have the same H and
+ * top_k.  Everything is checked before anything is enqueued.
+ * -------------------------------------------------------------------------- */
+typedef struct CUevent_st* nvfp4_event_t;   /* identical to cudaEvent_t */
+
+nvfp4_status nvfp4_moe_step_host(const void* x_host, const float* logits_host, int32_t T, int32_t H,
+                                 int32_t I, int32_t E, int32_t top_k, const nvfp4_moe_weights* w,
+                                 const nvfp4_moe_buffers* buf, const nvfp4_moe_buffers* prev,
+                                 int32_t prev_T, void* prev_y_host, nvfp4_event_t compute_after,
+                                 nvfp4_event_t compute_done, nvfp4_stream_t stream);
+
+nvfp4_status nvfp4_moe_finish_host(const nvfp4_moe_buffers* buf, int32_t T, int32_t H, int32_t top_k,
+                                   void* y_host, nvfp4_stream_t stream);
 
 /* Message of the last failing call on this host thread ("" if none). */
 const char* nvfp4_last_error(void);

@@ -19,7 +19,8 @@ __all__ = [
     "Nvfp4Error", "lib_path", "load", "sf_bytes", "moe_padded_rows_max",
     "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
     "moe_route_permute", "moe_route_permute_static", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
-    "moe_combine", "nvfp4_moe_forward_host", "nvfp4_device_status", "nvfp4_selftest_bounded_wait",
+    "moe_combine", "nvfp4_moe_forward_host", "nvfp4_moe_step_host", "nvfp4_moe_finish_host",
+    "nvfp4_device_status", "nvfp4_selftest_bounded_wait",
     "nvfp4_set_gemm_tiles", "nvfp4_global_scale", "nvfp4_mma_peak_probe",
     "MODE_PLAIN", "MODE_SWIGLU_GU8", "EPI_SWIGLU_NVFP4", "EPI_BF16",
 ]
@@ -52,6 +53,12 @@ class _MoeWeightsC(ctypes.Structure):
     _fields_ = [("w1_q", _vp), ("w1_sf", _vp), ("w2_q", _vp), ("w2_sf", _vp)]
 
 
+class _CombineJobC(ctypes.Structure):
+    """nvfp4_combine_job (include/nvfp4moe.h)."""
+    _fields_ = [("rows_bf16", _vp), ("inv_perm", _vp), ("topk_w", _vp), ("T", _i32), ("top_k", _i32),
+                ("H", _i32), ("y_bf16", _vp)]
+
+
 class _MoeBuffersC(ctypes.Structure):
     """nvfp4_moe_buffers (include/nvfp4moe.h)."""
     _fields_ = [("x_bf16", _vp), ("logits", _vp), ("y_bf16", _vp), ("topk_ids", _vp), ("topk_w", _vp),
@@ -69,15 +76,20 @@ _SIGS = {
     "moe_route_permute": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp, _vp, _sz, _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _f32,
-                                          _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
+                                          _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64,
+                                          ctypes.POINTER(_CombineJobC), _vp]),
     "nvfp4_moe_ffn_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp,
                                              _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
-                                             _vp]),
+                                             ctypes.POINTER(_CombineJobC), _vp]),
     "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_route_permute_static": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                                 _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_moe_forward_host": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                               ctypes.POINTER(_MoeWeightsC), ctypes.POINTER(_MoeBuffersC), _vp]),
+    "nvfp4_moe_step_host": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_MoeWeightsC),
+                                           ctypes.POINTER(_MoeBuffersC), ctypes.POINTER(_MoeBuffersC), _i32, _vp,
+                                           _vp, _vp, _vp]),
+    "nvfp4_moe_finish_host": (ctypes.c_int, [ctypes.POINTER(_MoeBuffersC), _i32, _i32, _i32, _vp, _vp]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
@@ -175,24 +187,83 @@ def moe_route_permute_static(logits, x, top_k, topk_ids, topk_w, expert_counts, 
                                            _p(a1_q), _p(a1_sf), _p(x_q), _p(x_global_scale), _stream(stream)))
 
 
+def _combine_job(job):
+    """(rows, inv_perm, topk_w, y) tensors -> a pointer to nvfp4_combine_job (None -> NULL)."""
+    if job is None:
+        return None
+    rows, inv, w, y = job
+    return ctypes.byref(_CombineJobC(rows.data_ptr(), inv.data_ptr(), w.data_ptr(), inv.shape[0], inv.shape[1],
+                                     y.shape[1], y.data_ptr()))
+
+
 def nvfp4_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, alpha, epilogue,
                        out_q=None, out_sf=None, out_bf16=None, h_debug=None, stream=None, a_global_scale=None,
-                       b_global_scale=None, out_global_scale=None, a_gather=None, a_gather_rows=0):
+                       b_global_scale=None, out_global_scale=None, a_gather=None, a_gather_rows=0,
+                       side_combine=None):
+    """side_combine: None, or (rows, inv_perm, topk_w, y) of an earlier batch to
+    combine alongside (run on spare warps of the CTA-pair SwiGLU kernel)."""
     _check(load().nvfp4_grouped_gemm(_p(a_q), _p(a_sf), rows_max, _p(group_offsets), _p(group_counts), G, N, K,
                                      _p(b_q), _p(b_sf), alpha, _p(a_global_scale), _p(b_global_scale),
                                      _p(out_global_scale), epilogue, _p(out_q), _p(out_sf), _p(out_bf16),
-                                     _p(h_debug), _p(a_gather), a_gather_rows, _stream(stream)))
+                                     _p(h_debug), _p(a_gather), a_gather_rows, _combine_job(side_combine),
+                                     _stream(stream)))
 
 
 def nvfp4_moe_ffn_forward(a1_q, a1_sf, expert_offsets, expert_counts, E, H, I, rows_max, w1_q, w1_sf, w2_q, w2_sf,
                           alpha1, alpha2, a2_q, a2_sf, rows_out, h_debug=None, stream=None, x_global_scale=None,
                           w1_global_scale=None, a2_global_scale=None, w2_global_scale=None, a1_gather=None,
-                          a1_gather_rows=0):
+                          a1_gather_rows=0, prev_combine=None):
+    """prev_combine: None, or (rows, inv_perm, topk_w, y) of an earlier batch whose
+    combine the L1 GEMM runs on spare warps (y = moe_combine(rows, inv_perm, topk_w))."""
+    job = _combine_job(prev_combine)
     _check(load().nvfp4_moe_ffn_forward(_p(a1_q), _p(a1_sf), _p(expert_offsets), _p(expert_counts), E, H, I,
                                         rows_max, _p(w1_q), _p(w1_sf), _p(w2_q), _p(w2_sf), alpha1, alpha2,
                                         _p(x_global_scale), _p(w1_global_scale), _p(a2_global_scale),
                                         _p(w2_global_scale), _p(a2_q), _p(a2_sf), _p(rows_out), _p(h_debug),
-                                        _p(a1_gather), a1_gather_rows, _stream(stream)))
+                                        _p(a1_gather), a1_gather_rows, job, _stream(stream)))
+
+
+def _weights_c(weights):
+    return _MoeWeightsC(weights.w1_q.data_ptr(), weights.w1_sf.data_ptr(), weights.w2_q.data_ptr(),
+                        weights.w2_sf.data_ptr())
+
+
+def _buffers_c(b):
+    return _MoeBuffersC(b.x.data_ptr(), b.logits.data_ptr(), b.y.data_ptr(), b.topk_ids.data_ptr(),
+                        b.topk_w.data_ptr(), b.counts.data_ptr(), b.offsets.data_ptr(), b.perm_token.data_ptr(),
+                        b.inv_perm.data_ptr(), b.a1_q.data_ptr(), b.a1_sf.data_ptr(), b.a2_q.data_ptr(),
+                        b.a2_sf.data_ptr(), b.rows_out.data_ptr(), b.workspace.data_ptr(),
+                        b.workspace.numel() * b.workspace.element_size(), b.rows_max)
+
+
+def _event(ev):
+    """torch.cuda.Event (already recorded once, so that it exists) -> its handle."""
+    return None if ev is None else ctypes.c_void_p(ev.cuda_event)
+
+
+def nvfp4_moe_step_host(x_host, logits_host, top_k, weights, buffers, prev=None, prev_y_host=None,
+                        compute_after=None, compute_done=None, stream=None):
+    """One step of a serving loop from host buffers: copy this batch in, route,
+    L1 (+ the pending combine of the batch in ``prev``) and L2 into ``buffers``,
+    then copy prev's y out to ``prev_y_host``.  This batch's combine stays
+    pending (a later step's prev, or nvfp4_moe_finish_host).  Events are
+    torch.cuda.Event objects (recorded once beforehand) or None."""
+    T, H = x_host.shape
+    E = logits_host.shape[1]
+    I = 2 * buffers.a2_q.shape[1]
+    prev_c = ctypes.byref(_buffers_c(prev)) if prev is not None else None
+    prev_T = prev.shape.T if prev is not None else 0
+    _check(load().nvfp4_moe_step_host(_p(x_host), _p(logits_host), T, H, I, E, top_k,
+                                      ctypes.byref(_weights_c(weights)), ctypes.byref(_buffers_c(buffers)), prev_c,
+                                      prev_T, _p(prev_y_host), _event(compute_after), _event(compute_done),
+                                      _stream(stream)))
+
+
+def nvfp4_moe_finish_host(buffers, top_k, y_host, stream=None):
+    """The pending combine of the batch in ``buffers``, then its y copied out to y_host."""
+    T, H = y_host.shape
+    _check(load().nvfp4_moe_finish_host(ctypes.byref(_buffers_c(buffers)), T, H, top_k, _p(y_host),
+                                        _stream(stream)))
 
 
 def nvfp4_moe_forward_host(x_host, logits_host, y_host, top_k, weights, buffers, stream=None):
@@ -205,16 +276,9 @@ def nvfp4_moe_forward_host(x_host, logits_host, y_host, top_k, weights, buffers,
     T, H = x_host.shape
     E = logits_host.shape[1]
     I = 2 * buffers.a2_q.shape[1]
-    w = _MoeWeightsC(weights.w1_q.data_ptr(), weights.w1_sf.data_ptr(), weights.w2_q.data_ptr(),
-                     weights.w2_sf.data_ptr())
-    b = buffers
-    c = _MoeBuffersC(b.x.data_ptr(), b.logits.data_ptr(), b.y.data_ptr(), b.topk_ids.data_ptr(),
-                     b.topk_w.data_ptr(), b.counts.data_ptr(), b.offsets.data_ptr(), b.perm_token.data_ptr(),
-                     b.inv_perm.data_ptr(), b.a1_q.data_ptr(), b.a1_sf.data_ptr(), b.a2_q.data_ptr(),
-                     b.a2_sf.data_ptr(), b.rows_out.data_ptr(), b.workspace.data_ptr(),
-                     b.workspace.numel() * b.workspace.element_size(), b.rows_max)
     _check(load().nvfp4_moe_forward_host(_p(x_host), _p(logits_host), _p(y_host), T, H, I, E, top_k,
-                                         ctypes.byref(w), ctypes.byref(c), _stream(stream)))
+                                         ctypes.byref(_weights_c(weights)), ctypes.byref(_buffers_c(buffers)),
+                                         _stream(stream)))
 
 
 def moe_combine(rows, inv_perm, topk_w, y, stream=None, shared=None):

@@ -194,13 +194,17 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_route_permute");
 }
 
-nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,
+}  // extern "C"
+
+namespace {
+
+// nvfp4_grouped_gemm's argument checks (status and message; nothing launched)
+nvfp4_status check_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,
                                 const int32_t* group_offsets, const int32_t* group_counts, int32_t G, int32_t N,
-                                int32_t K, const uint8_t* b_q, const uint8_t* b_sf, float alpha,
-                                const float* a_global_scale, const float* b_global_scale,
-                                const float* out_global_scale, nvfp4_epilogue epilogue, uint8_t* out_q,
-                                uint8_t* out_sf, void* out_bf16, float* h_debug, const int32_t* a_gather,
-                                int64_t a_gather_rows, nvfp4_stream_t stream) {
+                                int32_t K, const uint8_t* b_q, const uint8_t* b_sf, const float* a_global_scale,
+                                const float* b_global_scale, const float* out_global_scale, nvfp4_epilogue epilogue,
+                                uint8_t* out_q, uint8_t* out_sf, void* out_bf16, float* h_debug,
+                                const int32_t* a_gather, int64_t a_gather_rows) {
   CHECK_ARG(a_q && a_sf && b_q && b_sf, "nvfp4_grouped_gemm: null operand");
   CHECK_ARG(!a_gather || (a_gather_rows > 0 && a_gather_rows < (int64_t(1) << 31)),
             "nvfp4_grouped_gemm: a_gather_rows=%lld", (long long)a_gather_rows);
@@ -226,6 +230,25 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
            "nvfp4_grouped_gemm: outputs not 16-byte aligned");
   CHECK_AL(al4(a_global_scale) && al4(b_global_scale) && al4(out_global_scale),
            "nvfp4_grouped_gemm: global scales not 4-byte aligned");
+  return NVFP4_OK;
+}
+
+// a side combine job's checks (moe_combine's, without shared rows)
+nvfp4_status check_combine_job(const nvfp4_combine_job* c) {
+  if (c == nullptr) return NVFP4_OK;
+  CHECK_ARG(c->T >= 0 && c->top_k >= 1 && c->top_k <= 32, "combine job: T=%d top_k=%d", c->T, c->top_k);
+  if (c->T == 0) return NVFP4_OK;
+  CHECK_ARG(c->rows_bf16 && c->inv_perm && c->topk_w && c->y_bf16, "combine job: null pointer");
+  CHECK_SUP(c->H > 0 && c->H % 8 == 0, "combine job: H=%d is not a positive multiple of 8", c->H);
+  CHECK_AL(al16(c->rows_bf16) && al16(c->y_bf16), "combine job: rows and y must be 16-byte aligned");
+  return NVFP4_OK;
+}
+
+GemmArgs make_gemm_args(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max, const int32_t* group_offsets,
+                        const int32_t* group_counts, int32_t G, int32_t N, int32_t K, const uint8_t* b_q,
+                        const uint8_t* b_sf, float alpha, const float* a_global_scale, const float* b_global_scale,
+                        const float* out_global_scale, nvfp4_epilogue epilogue, uint8_t* out_q, uint8_t* out_sf,
+                        void* out_bf16, float* h_debug, const int32_t* a_gather, int64_t a_gather_rows) {
   GemmArgs a;
   a.a_q = a_q;
   a.a_sf = a_sf;
@@ -248,6 +271,38 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
   a.out_sf = out_sf;
   a.out_bf16 = out_bf16;
   a.h_debug = h_debug;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max,
+                                const int32_t* group_offsets, const int32_t* group_counts, int32_t G, int32_t N,
+                                int32_t K, const uint8_t* b_q, const uint8_t* b_sf, float alpha,
+                                const float* a_global_scale, const float* b_global_scale,
+                                const float* out_global_scale, nvfp4_epilogue epilogue, uint8_t* out_q,
+                                uint8_t* out_sf, void* out_bf16, float* h_debug, const int32_t* a_gather,
+                                int64_t a_gather_rows, const nvfp4_combine_job* side_combine, nvfp4_stream_t stream) {
+  nvfp4_status st = check_combine_job(side_combine);
+  if (st != NVFP4_OK) return st;
+  st = check_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, a_global_scale,
+                         b_global_scale, out_global_scale, epilogue, out_q, out_sf, out_bf16, h_debug, a_gather,
+                         a_gather_rows);
+  if (st != NVFP4_OK) return st;
+  GemmArgs a = make_gemm_args(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, alpha,
+                              a_global_scale, b_global_scale, out_global_scale, epilogue, out_q, out_sf, out_bf16,
+                              h_debug, a_gather, a_gather_rows);
+  if (side_combine != nullptr && side_combine->T > 0) {
+    a.side_rows = side_combine->rows_bf16;
+    a.side_inv = side_combine->inv_perm;
+    a.side_w = side_combine->topk_w;
+    a.side_y = side_combine->y_bf16;
+    a.side_T = side_combine->T;
+    a.side_H = side_combine->H;
+    a.side_k = side_combine->top_k;
+  }
   return gemm_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -258,19 +313,21 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf, co
                                    const float* w1_global_scale, const float* a2_global_scale,
                                    const float* w2_global_scale, uint8_t* a2_q, uint8_t* a2_sf, void* rows_out_bf16,
                                    float* h_debug, const int32_t* a1_gather, int64_t a1_gather_rows,
-                                   nvfp4_stream_t stream) {
+                                   const nvfp4_combine_job* prev_combine, nvfp4_stream_t stream) {
   CHECK_ARG(expert_offsets && expert_counts, "nvfp4_moe_ffn_forward: null expert offsets/counts");
+  CHECK_ARG(prev_combine == nullptr || prev_combine->T == 0 || prev_combine->H == H,
+            "nvfp4_moe_ffn_forward: prev_combine H=%d differs from H=%d", prev_combine ? prev_combine->H : 0, H);
   CHECK_ARG(a2_q && a2_sf && rows_out_bf16, "nvfp4_moe_ffn_forward: null output");
   CHECK_SUP(H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0,
             "nvfp4_moe_ffn_forward: H=%d and I=%d must be positive multiples of 256", H, I);
   nvfp4_status st = nvfp4_grouped_gemm(a1_q, a1_sf, rows_max, expert_offsets, expert_counts, E, 2 * I, H, w1_q,
                                        w1_sf, alpha1, x_global_scale, w1_global_scale, a2_global_scale,
                                        NVFP4_EPI_SWIGLU_NVFP4, a2_q, a2_sf, nullptr, h_debug, a1_gather,
-                                       a1_gather_rows, stream);
+                                       a1_gather_rows, prev_combine, stream);
   if (st != NVFP4_OK) return st;
   return nvfp4_grouped_gemm(a2_q, a2_sf, rows_max, expert_offsets, expert_counts, E, H, I, w2_q, w2_sf, alpha2,
                             a2_global_scale, w2_global_scale, nullptr, NVFP4_EPI_BF16, nullptr, nullptr,
-                            rows_out_bf16, nullptr, nullptr, 0, stream);
+                            rows_out_bf16, nullptr, nullptr, 0, nullptr, stream);
 }
 
 nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w, int32_t T,
@@ -285,49 +342,114 @@ nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const f
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_combine");
 }
 
-nvfp4_status nvfp4_moe_forward_host(const void* x_host, const float* logits_host, void* y_host, int32_t T,
-                                    int32_t H, int32_t I, int32_t E, int32_t top_k, const nvfp4_moe_weights* w,
-                                    const nvfp4_moe_buffers* b, nvfp4_stream_t stream) {
-  CHECK_ARG(x_host && logits_host && y_host && w && b, "nvfp4_moe_forward_host: null pointer");
-  CHECK_ARG(T >= 1, "nvfp4_moe_forward_host: T=%d", T);
+}  // extern "C"
+
+namespace {
+
+// the checks of a host-buffer step for T tokens into buffer set b
+nvfp4_status check_host_step(const void* x_host, const float* logits_host, int32_t T, int32_t H, int32_t I, int32_t E,
+                             int32_t top_k, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b) {
+  CHECK_ARG(x_host && logits_host && w && b, "host step: null pointer");
+  CHECK_ARG(T >= 1, "host step: T=%d", T);
   CHECK_ARG(b->x_bf16 && b->logits && b->y_bf16 && b->rows_bf16 && b->topk_ids && b->topk_w && b->expert_counts &&
                 b->expert_offsets && b->perm_token && b->inv_perm && b->a1_q && b->a1_sf && b->a2_q && b->a2_sf &&
                 b->workspace && w->w1_q && w->w1_sf && w->w2_q && w->w2_sf,
-            "nvfp4_moe_forward_host: null device buffer");
+            "host step: null device buffer");
   // the checks of the three calls, before anything is enqueued
-  CHECK_SUP(E >= 1 && E <= 1024, "nvfp4_moe_forward_host: E=%d outside [1, 1024]", E);
-  CHECK_SUP(top_k >= 1 && top_k <= E && top_k <= 32, "nvfp4_moe_forward_host: top_k=%d", top_k);
+  CHECK_SUP(E >= 1 && E <= 1024, "host step: E=%d outside [1, 1024]", E);
+  CHECK_SUP(top_k >= 1 && top_k <= E && top_k <= 32, "host step: top_k=%d", top_k);
   CHECK_SUP(H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0,
-            "nvfp4_moe_forward_host: H=%d and I=%d must be positive multiples of 256", H, I);
-  CHECK_ARG(b->rows_max >= moe_padded_rows_max(T, E, top_k),
-            "nvfp4_moe_forward_host: rows_max=%lld < moe_padded_rows_max", (long long)b->rows_max);
-  CHECK_ARG(b->workspace_bytes >= moe_route_permute_workspace(T, H, E, top_k),
-            "nvfp4_moe_forward_host: workspace too small");
+            "host step: H=%d and I=%d must be positive multiples of 256", H, I);
+  CHECK_ARG(b->rows_max >= moe_padded_rows_max(T, E, top_k), "host step: rows_max=%lld < moe_padded_rows_max",
+            (long long)b->rows_max);
+  CHECK_ARG(b->workspace_bytes >= moe_route_permute_workspace(T, H, E, top_k), "host step: workspace too small");
   CHECK_AL(al16(b->x_bf16) && al16(b->y_bf16) && al16(b->rows_bf16) && al16(b->a1_q) && al16(b->a1_sf) &&
                al16(b->a2_q) && al16(b->a2_sf) && al16(b->workspace) && al16(w->w1_q) && al16(w->w1_sf) &&
                al16(w->w2_q) && al16(w->w2_sf),
-           "nvfp4_moe_forward_host: device buffers must be 16-byte aligned");
-  CHECK_SUP(b->rows_max % 128 == 0 && b->rows_max < (int64_t(1) << 31),
-            "nvfp4_moe_forward_host: rows_max=%lld is not a multiple of 128", (long long)b->rows_max);
+           "host step: device buffers must be 16-byte aligned");
+  CHECK_SUP(b->rows_max % 128 == 0 && b->rows_max < (int64_t(1) << 31), "host step: rows_max=%lld",
+            (long long)b->rows_max);
+  return NVFP4_OK;
+}
+
+// copy-in, then (after an optional wait) route + L1 (+ a side combine) + L2
+nvfp4_status enqueue_host_step(const void* x_host, const float* logits_host, int32_t T, int32_t H, int32_t I,
+                               int32_t E, int32_t top_k, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b,
+                               const nvfp4_combine_job* side, cudaEvent_t compute_after, nvfp4_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t xy_bytes = static_cast<size_t>(T) * H * 2;
-  cudaError_t e = cudaMemcpyAsync(b->x_bf16, x_host, xy_bytes, cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaMemcpyAsync(b->x_bf16, x_host, static_cast<size_t>(T) * H * 2, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(b->logits, logits_host, static_cast<size_t>(T) * E * sizeof(float), cudaMemcpyHostToDevice,
                         s);
-  if (e != cudaSuccess) return fail_cuda(e, "nvfp4_moe_forward_host: copy in");
+  if (e == cudaSuccess && compute_after != nullptr) e = cudaStreamWaitEvent(s, compute_after, 0);
+  if (e != cudaSuccess) return fail_cuda(e, "host step: copy in");
   nvfp4_status st = moe_route_permute(b->logits, b->x_bf16, T, H, E, top_k, b->topk_ids, b->topk_w,
                                       b->expert_counts, b->expert_offsets, b->perm_token, b->inv_perm, b->a1_q,
                                       b->a1_sf, nullptr, nullptr, b->workspace, b->workspace_bytes, stream);
   if (st != NVFP4_OK) return st;
-  st = nvfp4_moe_ffn_forward(b->a1_q, b->a1_sf, b->expert_offsets, b->expert_counts, E, H, I, b->rows_max, w->w1_q,
-                             w->w1_sf, w->w2_q, w->w2_sf, 1.0f, 1.0f, nullptr, nullptr, nullptr, nullptr, b->a2_q,
-                             b->a2_sf, b->rows_bf16, nullptr, nullptr, 0, stream);
+  return nvfp4_moe_ffn_forward(b->a1_q, b->a1_sf, b->expert_offsets, b->expert_counts, E, H, I, b->rows_max,
+                               w->w1_q, w->w1_sf, w->w2_q, w->w2_sf, 1.0f, 1.0f, nullptr, nullptr, nullptr, nullptr,
+                               b->a2_q, b->a2_sf, b->rows_bf16, nullptr, nullptr, 0, side, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+nvfp4_status nvfp4_moe_forward_host(const void* x_host, const float* logits_host, void* y_host, int32_t T,
+                                    int32_t H, int32_t I, int32_t E, int32_t top_k, const nvfp4_moe_weights* w,
+                                    const nvfp4_moe_buffers* b, nvfp4_stream_t stream) {
+  CHECK_ARG(y_host, "nvfp4_moe_forward_host: null y_host");
+  nvfp4_status st = check_host_step(x_host, logits_host, T, H, I, E, top_k, w, b);
+  if (st != NVFP4_OK) return st;
+  st = enqueue_host_step(x_host, logits_host, T, H, I, E, top_k, w, b, nullptr, nullptr, stream);
   if (st != NVFP4_OK) return st;
   st = moe_combine(b->rows_bf16, b->inv_perm, b->topk_w, T, H, top_k, nullptr, b->y_bf16, stream);
   if (st != NVFP4_OK) return st;
-  e = cudaMemcpyAsync(y_host, b->y_bf16, xy_bytes, cudaMemcpyDeviceToHost, s);
+  const cudaError_t e = cudaMemcpyAsync(y_host, b->y_bf16, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost,
+                                        reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_moe_forward_host: copy out");
+}
+
+nvfp4_status nvfp4_moe_step_host(const void* x_host, const float* logits_host, int32_t T, int32_t H, int32_t I,
+                                 int32_t E, int32_t top_k, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b,
+                                 const nvfp4_moe_buffers* prev, int32_t prev_T, void* prev_y_host,
+                                 nvfp4_event_t compute_after, nvfp4_event_t compute_done, nvfp4_stream_t stream) {
+  nvfp4_status st = check_host_step(x_host, logits_host, T, H, I, E, top_k, w, b);
+  if (st != NVFP4_OK) return st;
+  nvfp4_combine_job job = {};
+  if (prev != nullptr) {
+    CHECK_ARG(prev != b, "nvfp4_moe_step_host: prev is this step's buffer set");
+    CHECK_ARG(prev_T >= 1 && prev_y_host && prev->rows_bf16 && prev->inv_perm && prev->topk_w && prev->y_bf16,
+              "nvfp4_moe_step_host: prev needs prev_T >= 1, prev_y_host and its rows, inv_perm, topk_w and y");
+    CHECK_AL(al16(prev->rows_bf16) && al16(prev->y_bf16), "nvfp4_moe_step_host: prev rows and y not 16-byte aligned");
+    job.rows_bf16 = prev->rows_bf16;
+    job.inv_perm = prev->inv_perm;
+    job.topk_w = prev->topk_w;
+    job.T = prev_T;
+    job.top_k = top_k;
+    job.H = H;
+    job.y_bf16 = prev->y_bf16;
+  }
+  st = enqueue_host_step(x_host, logits_host, T, H, I, E, top_k, w, b, prev != nullptr ? &job : nullptr,
+                         reinterpret_cast<cudaEvent_t>(compute_after), stream);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = compute_done != nullptr ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(compute_done), s)
+                                          : cudaSuccess;
+  if (e == cudaSuccess && prev != nullptr)
+    e = cudaMemcpyAsync(prev_y_host, prev->y_bf16, static_cast<size_t>(prev_T) * H * 2, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_moe_step_host: event or copy out");
+}
+
+nvfp4_status nvfp4_moe_finish_host(const nvfp4_moe_buffers* b, int32_t T, int32_t H, int32_t top_k, void* y_host,
+                                   nvfp4_stream_t stream) {
+  CHECK_ARG(b && y_host && T >= 1, "nvfp4_moe_finish_host: null pointer or T < 1");
+  const nvfp4_status st = moe_combine(b->rows_bf16, b->inv_perm, b->topk_w, T, H, top_k, nullptr, b->y_bf16, stream);
+  if (st != NVFP4_OK) return st;
+  const cudaError_t e = cudaMemcpyAsync(y_host, b->y_bf16, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_moe_finish_host: copy out");
 }
 
 nvfp4_status nvfp4_device_status(nvfp4_stream_t stream) {

@@ -205,6 +205,56 @@ __device__ __forceinline__ void swiglu_bf16_row(const float (&v)[4][32], float a
   }
 }
 
+// The routing-weighted sum of token t's k rows (moe_combine's arithmetic: fp32
+// FMA in slot order starting from 0, one rounding to BF16) over the 8-column
+// chunks c0 + 32 i (i < kNC, those below `chunks`) of the row.  Every slot's
+// 16-byte loads are issued before the FMAs use them (8 kNC per lane in flight),
+// which is what lets a few warps stream the rows at HBM rate.
+template <int kNC>
+__device__ __forceinline__ void combine_chunks(const __nv_bfloat16* __restrict__ rows,
+                                               const int32_t* __restrict__ inv_perm, const float* __restrict__ w,
+                                               int32_t H, int32_t k, int64_t t, int c0, int chunks,
+                                               __nv_bfloat16* __restrict__ y) {
+  float acc[kNC][8];
+#pragma unroll
+  for (int n = 0; n < kNC; ++n)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[n][i] = 0.0f;
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    uint4 v[8][kNC];
+    float wj[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (j0 + q < k) {
+        const int64_t r = __ldg(inv_perm + t * k + j0 + q);
+        wj[q] = __ldg(w + t * k + j0 + q);
+        const uint4* src = reinterpret_cast<const uint4*>(rows + r * H);
+#pragma unroll
+        for (int n = 0; n < kNC; ++n)
+          v[q][n] = c0 + 32 * n < chunks ? __ldg(src + c0 + 32 * n) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (j0 + q < k) {
+#pragma unroll
+        for (int n = 0; n < kNC; ++n) {
+          float f[8];
+          bf16x8_to_f32(v[q][n], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[n][i] = fmaf(wj[q], f[i], acc[n][i]);
+        }
+      }
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(y + t * H);
+#pragma unroll
+  for (int n = 0; n < kNC; ++n)
+    if (c0 + 32 * n < chunks)
+      dst[c0 + 32 * n] = make_uint4(pack_bf16x2(acc[n][0], acc[n][1]), pack_bf16x2(acc[n][2], acc[n][3]),
+                                    pack_bf16x2(acc[n][4], acc[n][5]), pack_bf16x2(acc[n][6], acc[n][7]));
+}
+
 // ------------------------------------------------------------- mbarriers --
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -479,6 +479,15 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   const bool pair = bn == 256 && groups <= kPairMaxGroups &&
                     (mode == NVFP4_GEMM_TILES_PAIR ||
                      (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
+  // a side job (the combine of an earlier batch) runs inside the CTA-pair SwiGLU
+  // kernel; with any other kernel it runs as its own launch first
+  if (a.side_T > 0 && !(pair && a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 && a.a_gather == nullptr)) {
+    e = combine_launch(a.side_rows, a.side_inv, a.side_w, a.side_T, a.side_H, a.side_k, nullptr, a.side_y, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "nvfp4_moe_ffn_forward: combine of the earlier batch");
+    GemmArgs plain = a;
+    plain.side_T = 0;
+    return gemm_launch(plain, stream);
+  }
   if (pair) return gemm_pair_launch(a, info.sms, dev, stream);
   CUtensorMap ma, mb;
   const bool gather = a.a_gather != nullptr;      // gathered A rows: a one-row box for tile::gather4

@@ -45,6 +45,8 @@ namespace {
 constexpr int kBM = 128, kBK = 256;                    // rows per CTA, K per stage
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kSideWarps = 2;                          // the side job's warps (kSide instantiations)
+constexpr int kThreadsSide = kThreads + 32 * kSideWarps;
 constexpr int kMaxGroups = kPairMaxGroups;             // larger G uses the single-CTA kernel
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
 constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms
@@ -108,6 +110,13 @@ struct PairParams {
   __nv_bfloat16* out_bf16;
   float* h_debug;
   unsigned* err;
+  // side job (kSide): the combine of an earlier batch, run by the two side warps
+  // of every CTA while the GEMM runs; side_T == 0: none
+  const __nv_bfloat16* side_rows;
+  const int32_t* side_inv;
+  const float* side_w;
+  __nv_bfloat16* side_y;
+  int32_t side_T, side_H, side_k;
 };
 
 // last g < G with tab[g] <= v (tab non-decreasing, tab[0] = 0 <= v)
@@ -211,8 +220,12 @@ __device__ __forceinline__ void wait_until_clock(long long due) {
 
 // kGather: A rows come through p.a_gather (tile::gather4); a separate
 // instantiation, so the default kernels carry none of its code.
-template <int kEpi, bool kGather>
-__global__ void __launch_bounds__(kThreads, 1)
+// kSide: two more warps per CTA run a side job (the combine of an earlier batch,
+// HBM-bound) while the producer, MMA and epilogue warps run the GEMM, which
+// moves little DRAM traffic of its own; tokens are dealt to the side warps of
+// all CTAs in turn.
+template <int kEpi, bool kGather, bool kSide>
+__global__ void __launch_bounds__(kSide ? kThreadsSide : kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                           const __grid_constant__ CUtensorMap tmap_out, const PairParams p) {
@@ -422,6 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // odd CTA: nothing to issue (the even CTA's MMAs read this CTA's stages)
+  } else if (kSide && warp >= 2 + kEpiWarps) {
+    // ----------------------------------------------------------- side job
+    const int64_t sw = static_cast<int64_t>(blockIdx.x) * kSideWarps + (warp - 2 - kEpiWarps);
+    const int64_t n_sw = static_cast<int64_t>(gridDim.x) * kSideWarps;
+    const int chunks = p.side_H / 8;
+    for (int64_t t = sw; t < p.side_T; t += n_sw)
+      for (int c0 = lane; c0 < chunks; c0 += 32 * 3)
+        combine_chunks<3>(p.side_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t, c0, chunks, p.side_y);
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t quad = warp & 3;                // TMEM lanes 32*quad .. +31
@@ -543,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct PairDeviceInfo {
-  bool attr_set[4] = {};
-  int max_clusters[4] = {};
+  bool attr_set[5] = {};
+  int max_clusters[5] = {};
 };
 
 PairDeviceInfo& pair_info(int dev) {
@@ -557,11 +578,11 @@ std::mutex& pair_mutex() {
   return mu;
 }
 
-template <int kEpi, bool kGather>
+template <int kEpi, bool kGather, bool kSide = false>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  constexpr int slot = kGather ? 3 : (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2);
+  constexpr int slot = kSide ? 4 : kGather ? 3 : (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2);
   constexpr uint32_t smem = PairCfg<kEpi>::kSmemBytes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -569,7 +590,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kSide ? kThreadsSide : kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -579,12 +600,12 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     std::lock_guard<std::mutex> lock(pair_mutex());
     PairDeviceInfo& info = pair_info(dev);
     if (!info.attr_set[slot]) {
-      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather>,
+      cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_pair_kernel<kEpi, kGather, kSide>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       cfg.gridDim = dim3(static_cast<unsigned>(sms / 2 * 2), 1, 1);
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, nvf4_gemm_pair_kernel<kEpi, kGather, kSide>, &cfg);
       if (e != cudaSuccess) return e;
       info.max_clusters[slot] = n;
       info.attr_set[slot] = true;
@@ -595,7 +616,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   int64_t clusters = max_clusters < num_tiles ? max_clusters : num_tiles;
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather>, ma, mb, msa, msb, mo, p);
+  return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather, kSide>, ma, mb, msa, msb, mo, p);
 }
 
 }  // namespace
@@ -648,6 +669,14 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   p.out_bf16 = static_cast<__nv_bfloat16*>(a.out_bf16);
   p.h_debug = a.h_debug;
   p.err = device_error_word();
+  const bool side = a.side_T > 0;
+  p.side_rows = static_cast<const __nv_bfloat16*>(a.side_rows);
+  p.side_inv = a.side_inv;
+  p.side_w = a.side_w;
+  p.side_y = static_cast<__nv_bfloat16*>(a.side_y);
+  p.side_T = a.side_T;
+  p.side_H = a.side_H;
+  p.side_k = a.side_k;
 
   // tiles that can exist: every group's pairs, at most ceil(blocks / 2) + G
   const int64_t blocks = a.rows_max / kBM;
@@ -655,7 +684,9 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   const int64_t max_tiles = max_pairs * p.n_tiles;
   if (max_tiles <= 0) return NVFP4_OK;
 #define NVFP4_PAIR_LAUNCH(E, GA) launch_pair<E, GA>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
-  const cudaError_t e = gather                                ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true)
+  const cudaError_t e = side ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4, false, true>(ma, mb, msa, msb, mo, p, max_tiles,
+                                                                                sms, dev, stream)
+                        : gather                              ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true)
                         : swiglu                              ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false)
                         : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false)
                                                               : NVFP4_PAIR_LAUNCH(NVFP4_EPI_BF16, false);

@@ -72,6 +72,13 @@ struct GemmArgs {
   uint8_t* out_sf;
   void* out_bf16;
   float* h_debug;
+  // side job of the CTA-pair SwiGLU kernel: the combine of an earlier batch
+  // (moe_combine without shared rows); side_T == 0: none
+  const void* side_rows = nullptr;
+  const int32_t* side_inv = nullptr;
+  const float* side_w = nullptr;
+  void* side_y = nullptr;
+  int32_t side_T = 0, side_H = 0, side_k = 0;
 };
 
 // Returns a status; writes a message with set_error_message on failure.

@@ -182,6 +182,33 @@ def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuff
     return b.y
 
 
+def moe_forward_deferred(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
+                         prev: MoeBuffers | None = None, alpha1: float = 1.0, alpha2: float = 1.0) -> None:
+    """Route + permute + stage, L1 + SwiGLU + requant + L2 of this batch into ``b``,
+    with its combine left pending; if ``prev`` holds an earlier batch whose combine
+    is pending, the L1 GEMM runs that combine on spare warps (into prev.y).  A
+    serving loop alternates two buffer sets and ends with moe_combine_deferred on
+    the last one.  One-level scales, no shared expert."""
+    s = b.shape
+    moe_route_permute(logits, x, s.top_k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
+                      b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_q=b.x_q)
+    job = None if prev is None else (prev.rows_out, prev.inv_perm, prev.topk_w, prev.y)
+    if s.T > 0:
+        gather = dict(a1_gather=b.perm_token, a1_gather_rows=s.T) if b.gather else {}
+        nvfp4_moe_ffn_forward(b.x_q if b.gather else b.a1_q, b.a1_sf, b.offsets, b.counts, s.E, s.H, s.I,
+                              b.rows_max, w.w1_q, w.w1_sf, w.w2_q, w.w2_sf, alpha1, alpha2, b.a2_q, b.a2_sf,
+                              b.rows_out, b.h_debug, prev_combine=job, **gather)
+    elif job is not None:
+        moe_combine(*job)
+
+
+def moe_combine_deferred(b: MoeBuffers) -> torch.Tensor:
+    """The pending combine of the batch in ``b`` (after moe_forward_deferred)."""
+    if b.shape.T > 0:
+        moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
+    return b.y
+
+
 def calibrate_a2_scale(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
                        alpha1: float = 1.0) -> torch.Tensor:
     """Set b.a2_gs = 2688 / amax of the L1 output h of this batch (two-level): one

@@ -56,6 +56,11 @@ def test_size_helpers(lib):
     assert lib.moe_route_permute_workspace(16384, 7168, 256, 8) >= 128 * 256 * 4
 
 
+def nvb_job(rows, inv, w, T, k, H, y):
+    import nvfp4_block_scaled_moe_gb300 as nvb
+    return nvb._CombineJobC(rows, inv, w, T, k, H, y)
+
+
 @needs_nvcc
 def test_host_validation_without_gpu(lib):
     import nvfp4_block_scaled_moe_gb300 as nv
@@ -82,11 +87,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.nvfp4_global_scale(p, 0, 4, 16, 16, vp(base + 2), None) == 3
     assert lib.nvfp4_sf_swizzle(p, 4, 4, 0, 1, p, 0, None) == 1
     # K not a multiple of 256; N not a multiple of 128 (BF16) / 256 (SwiGLU); G without offsets
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 200, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 192, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, None, None, None, 0, p, p, None, None, None, 0, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 7, None, None, p, None, None, 0, None) == 1
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 200, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 192, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, None, None, None, 0, p, p, None, None, None, 0, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 7, None, None, p, None, None, 0, None, None) == 1
     # routing limits
     assert lib.moe_route_permute(p, p, 8, 64, 2000, 2, p, p, p, p, p, p, p, p, None, None, p, 1 << 20, None) == 2
     assert lib.moe_route_permute(p, p, 8, 64, 8, 9, p, p, p, p, p, p, p, p, None, None, p, 1 << 20, None) == 2
@@ -98,13 +103,25 @@ def test_host_validation_without_gpu(lib):
                                  None) == 3
     # gathered A: a row count is required, the index must be 16-byte aligned
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
-                                  None, p, 0, None) == 1
+                                  None, p, 0, None, None) == 1
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
-                                  None, vp(base + 4), 64, None) == 3
+                                  None, vp(base + 4), 64, None, None) == 3
     # gathered A with an epilogue other than SwiGLU + NVFP4 (the L1 GEMM's) is not built
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
-                                  None, p, 64, None) == 2
-    assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None, 0, None) == 2
+                                  None, p, 64, None, None) == 2
+    assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None, 0, None, None) == 2
+    # a side combine job: its own checks, before anything is launched
+    job_bad_k = nvb_job(base, base, base, 4, 40, 512, base)
+    job_null = nvb_job(base, None, base, 4, 2, 512, base)
+    job_odd_y = nvb_job(base, base, base, 4, 2, 512, base + 8)
+    job_odd_h = nvb_job(base, base, base, 4, 2, 500, base)
+    for job, st in ((job_bad_k, 1), (job_null, 1), (job_odd_y, 3), (job_odd_h, 2)):
+        assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 0, p, p,
+                                      None, None, None, 0, ctypes.byref(job), None) == st
+    # the forward's job must have the forward's H
+    job_h = nvb_job(base, base, base, 4, 2, 768, base)
+    assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 256, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p,
+                                     p, None, None, 0, ctypes.byref(job_h), None) == 1
     # the host-buffer forward: null pointers, no tokens, a short workspace, an unaligned buffer
     import nvfp4_block_scaled_moe_gb300 as nvb
     wts = nvb._MoeWeightsC(base, base, base, base)

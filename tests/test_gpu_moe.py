@@ -142,3 +142,36 @@ def test_forward_from_host_buffers(nv):
     w1, w2 = inputs.moe_all_weights(spec)
     ref = omoe.moe_ffn(x, logits, w1, w2, spec["top_k"])["y"]
     assert rel_frobenius(outs[0].float().numpy(), ref) <= 2e-2
+
+
+def test_serving_loop_from_host_buffers(nv):
+    """nvfp4_moe_step_host / nvfp4_moe_finish_host over three different batches on
+    two buffer sets and two streams: each step's L1 runs the previous batch's
+    combine, each step copies the previous batch's y out.  Every y equals the
+    plain forward's bit for bit."""
+    nv, pipeline = nv
+    spec = inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=25, zipf=True)
+    s, w, _ = _gpu_setup(pipeline, spec)
+    x_t, _ = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    xs = [x_t, x_t.flip(0).contiguous(), x_t.roll(7, 0).contiguous()]
+    lgs = [logits, np.ascontiguousarray(logits[::-1]), np.ascontiguousarray(np.roll(logits, 7, 0))]
+    plain = [pipeline.moe_forward(xs[i].cuda(), dev(lgs[i]), w, pipeline.MoeBuffers(s)).cpu() for i in range(3)]
+    x_h = [x.pin_memory() for x in xs]
+    l_h = [torch.from_numpy(l).pin_memory() for l in lgs]
+    sets = [pipeline.MoeBuffers(s).enable_host_io(), pipeline.MoeBuffers(s).enable_host_io()]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    for ev, st in zip(done, streams):
+        ev.record(st)
+    y_h = [torch.zeros((spec["T"], spec["H"]), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    for i in range(3):
+        j = i & 1
+        nv.nvfp4_moe_step_host(x_h[i], l_h[i], spec["top_k"], w, sets[j], prev=sets[1 - j] if i else None,
+                               prev_y_host=y_h[i - 1] if i else None, compute_after=done[1 - j] if i else None,
+                               compute_done=done[j], stream=streams[j])
+    nv.nvfp4_moe_finish_host(sets[0], spec["top_k"], y_h[2], stream=streams[0])
+    torch.cuda.synchronize()
+    nv.nvfp4_device_status()
+    for i in range(3):
+        assert torch.equal(y_h[i], plain[i]), i
