@@ -3,12 +3,14 @@
 One step = one pass of the whole path over one batch: moe_route_permute
 (top-k routing, padded permutation, NVFP4 staging of x) -> L1 grouped GEMM with
 the fused SwiGLU + NVFP4 epilogue -> L2 grouped GEMM -> the routing-weighted
-combine.  By default a batch's combine runs inside the next step's L1 GEMM, on
-two spare warps per CTA (batches alternate between two buffer sets); the last
-batch's combine runs after the last step, inside the timed region, so the
-region holds every batch's whole path (and one combine more).
-`--no-overlap-combine` runs each batch's combine as its own launch at the end
-of its step.  The default workload is the prefill batch: T=16384 tokens,
+combine.  By default the steps form a serving pipeline (batches alternate
+between two buffer sets): step i routes batch i, runs the L2 GEMM of batch i-1
+with batch i's activation staging on two spare warps per CTA, then the L1 GEMM
+of batch i with batch i-1's combine on two spare warps per CTA.  The timed
+region starts the pipeline empty (its first step routes, stages and runs L1
+only) and ends with the last batch's L2 GEMM and combine, so it holds exactly
+the steps' batches.  `--no-overlap-combine` runs each batch's whole path in
+its own step, every stage its own launch.  The default workload is the prefill batch: T=16384 tokens,
 H=7168, I=2048, E=256 experts, top-8, Zipf-skewed routing (seeded synthetic
 data).
 
@@ -17,8 +19,8 @@ data).
 Prints one JSON line (rank 0).  `value` is whole-job TFLOP/s of the FFN
 (algorithmic FLOPs 6*k*H*I per token, padding rows not credited) with inputs
 resident in HBM; `e2e` repeats the measurement through the library's
-host-buffer calls (nvfp4_moe_step_host / nvfp4_moe_finish_host, or
-nvfp4_moe_forward_host without the overlap), with the inputs copied from
+host-buffer calls (nvfp4_moe_step_host / nvfp4_moe_finish_host, which run the
+same pipeline, or nvfp4_moe_forward_host without it), with the inputs copied from
 pinned host memory and the output copied back inside the timed region.
 Under torchrun each rank runs its own batch (weak scaling, no data-path
 collective); the timed region is bracketed by barriers and the max over ranks
@@ -50,11 +52,12 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # of that single launch (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # hash of the kernel sources it was taken on.  Reported as roofline.traffic only
 # while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "233a8421faddf76c5a6227fa77da3def7073dd368d41219baa7deef67fbafa8e",
-                     "bytes": {"prefill": 1728704256 + 154728960, "prefill_overlap": 3642500096 + 389483520,
-                               "decode": 4350999040 + 6295808}}
+L1_TRAFFIC_RECORD = {"sources_sha256": "411792dcc532faa7140c1b15d4ea4df85873e0b257e4fc11d6f50265c3ba2b42",
+                     "bytes": {"prefill": 1728673536 + 151784960, "prefill_overlap": 3887530496 + 386673920,
+                               "decode": 4349432832 + 3508480}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
-                  "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h")
+                  "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h",
+                  "nvfp4_block_scaled_moe_gb300/csrc/stage.cuh")
 
 
 def kernel_sources_sha256() -> str:
@@ -359,9 +362,11 @@ def e2e_host_call(nv, pipeline, s, w, b, x_h, logits_h, k, steps, world, y_ref):
 
 def e2e_step_host(nv, pipeline, s, w, b, x_h, logits_h, k, steps, world, y_ref):
     """Each step is one nvfp4_moe_step_host C-ABI call: host x and logits copied in,
-    route, L1 (also running the previous batch's combine on spare warps), L2, and
-    the previous batch's y copied out to host; one nvfp4_moe_finish_host call
-    after the last step combines the last batch and copies its y out.  Steps
+    routing, the previous batch's L2 (also staging this batch on spare warps),
+    this batch's L1 (also running the previous batch's combine on spare warps),
+    and the previous batch's y copied out to host; one nvfp4_moe_finish_host
+    call after the last step runs the last batch's L2 and combine and copies its
+    y out, so the region holds exactly the steps' batches.  Steps
     rotate over three device buffer sets on three streams, each step's kernels
     waiting for the previous step's.  On one stream a step's copy-in queues
     behind the copy-out of the step three back, so each copy pair has two steps'
@@ -383,7 +388,7 @@ def e2e_step_host(nv, pipeline, s, w, b, x_h, logits_h, k, steps, world, y_ref):
                                    prev_y_host=y_h[p] if i else None, compute_after=done[p] if i else None,
                                    compute_done=done[j], stream=streams[j])
         last = (n - 1) % n_sets
-        nv.nvfp4_moe_finish_host(sets[last], k, y_h[last], stream=streams[last])
+        nv.nvfp4_moe_finish_host(w, sets[last], k, y_h[last], stream=streams[last])
 
     run(n_sets)                                    # warm every set (untimed)
     torch.cuda.synchronize()
@@ -404,10 +409,11 @@ def e2e_step_host(nv, pipeline, s, w, b, x_h, logits_h, k, steps, world, y_ref):
     barrier(world)
     del sets[1:]
     return (max_over_ranks(s0.elapsed_time(s1), world),
-            "one nvfp4_moe_step_host C-ABI call per step: pinned host x and logits copied in, route, L1 (also "
-            "combining the previous batch on spare warps), L2, the previous batch's y copied out to pinned host "
-            "memory; one nvfp4_moe_finish_host call for the last batch; steps rotate over three device buffer sets "
-            "on three streams (each step's kernels wait for the previous step's), so copies overlap kernels")
+            "one nvfp4_moe_step_host C-ABI call per step: pinned host x and logits copied in, routing, the previous "
+            "batch's L2 (staging this batch on spare warps), this batch's L1 (combining the previous batch on spare "
+            "warps), the previous batch's y copied out to pinned host memory; one nvfp4_moe_finish_host call for "
+            "the last batch's L2, combine and copy-out; steps rotate over three device buffer sets on three streams "
+            "(each step's kernels wait for the previous step's), so copies overlap kernels")
 
 
 def e2e_copy_streams(step, x_d, logits_d, b, x_h, logits_h, T, H, stream, steps, world):
@@ -532,12 +538,21 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         if events:
             events[5].record(stream)
 
-    # --overlap-combine: batches alternate between two buffer sets, and each step's
-    # L1 GEMM also runs the previous batch's combine on two spare warps per CTA;
-    # the last batch's combine runs after the last step, inside the timed region
+    # --overlap-combine (the serving pipeline): batches alternate between two
+    # buffer sets; step i routes batch i, runs batch i-1's L2 GEMM with batch i's
+    # staging on its side warps, then batch i's L1 GEMM with batch i-1's combine
+    # on its side warps; finish_ov runs the last batch's L2 GEMM and combine
     ov = args.overlap_combine
     sets = [b, pipeline.MoeBuffers(s)] if ov else [b]
-    n_done = [0]                       # batches stepped so far (their parity picks the set)
+    n_done = [0]                       # batches stepped since the pipeline was empty
+
+    def l1_call(cur, job=None):
+        nv.nvfp4_grouped_gemm(cur.a1_q, cur.a1_sf, R, cur.offsets, cur.counts, E, 2 * I, H, w.w1_q, w.w1_sf, 1.0,
+                              nv.EPI_SWIGLU_NVFP4, out_q=cur.a2_q, out_sf=cur.a2_sf, side_combine=job)
+
+    def l2_call(cur, stage=None):
+        nv.nvfp4_grouped_gemm(cur.a2_q, cur.a2_sf, R, cur.offsets, cur.counts, E, H, I, w.w2_q, w.w2_sf, 1.0,
+                              nv.EPI_BF16, out_bf16=cur.rows_out, side_stage=stage)
 
     def step_ov(events=None):
         i = n_done[0]
@@ -545,25 +560,25 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         if events:
             events[0].record(stream)
         nv.moe_route_permute(logits_d, x_d, k, cur.topk_ids, cur.topk_w, cur.counts, cur.offsets, cur.perm_token,
-                             cur.inv_perm, cur.a1_q, cur.a1_sf, cur.workspace)
+                             cur.inv_perm, cur.a1_q if prev is None else None,
+                             cur.a1_sf if prev is None else None, cur.workspace)
         if events:
             events[1].record(stream)
-        job = None if prev is None else (prev.rows_out, prev.inv_perm, prev.topk_w, prev.y)
-        nv.nvfp4_grouped_gemm(cur.a1_q, cur.a1_sf, R, cur.offsets, cur.counts, E, 2 * I, H, w.w1_q, w.w1_sf, 1.0,
-                              nv.EPI_SWIGLU_NVFP4, out_q=cur.a2_q, out_sf=cur.a2_sf, side_combine=job)
+        if prev is not None:
+            l2_call(prev, dict(x=x_d, inv_perm=cur.inv_perm, counts=cur.counts, offsets=cur.offsets,
+                               a1_q=cur.a1_q, a1_sf=cur.a1_sf))
         if events:
             events[2].record(stream)
-        nv.nvfp4_grouped_gemm(cur.a2_q, cur.a2_sf, R, cur.offsets, cur.counts, E, H, I, w.w2_q, w.w2_sf, 1.0,
-                              nv.EPI_BF16, out_bf16=cur.rows_out)
+        l1_call(cur, None if prev is None else (prev.rows_out, prev.inv_perm, prev.topk_w, prev.y))
         if events:
             events[3].record(stream)
-            events[4].record(stream)
-            events[5].record(stream)
         n_done[0] += 1
 
     def finish_ov():
         last = sets[(n_done[0] - 1) & 1]
+        l2_call(last)
         nv.moe_combine(last.rows_out, last.inv_perm, last.topk_w, last.y)
+        n_done[0] = 0
 
     if ov:
         step = step_ov                 # noqa: F811 (the overlapped step replaces the plain one)
@@ -576,6 +591,8 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     time.sleep(0.3)
     for _ in range(args.warmup):
         step()
+    if ov:
+        finish_ov()                    # the timed region starts with the pipeline empty
     nv.nvfp4_device_status()
     torch.cuda.synchronize()
 
@@ -598,27 +615,40 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     nv.nvfp4_device_status()
     ms_local = start.elapsed_time(end)
     ms = max_over_ranks(ms_local, world)
-    names = ("route_permute", "l1_gemm_swiglu_nvfp4", "l2_gemm_bf16", "shared_expert", "combine")
-    per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-           for j, name in enumerate(names) if name != "shared_expert" or sh is not None}
     if ov:
+        # steps 1.. (the first has no previous batch): routing without staging, the
+        # previous batch's L2 with this batch's staging, this batch's L1 with the
+        # previous batch's combine
+        full = range(1, args.steps) if args.steps > 1 else range(args.steps)
+        per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in full)
+               for j, name in enumerate(("route_permute", "l2_gemm_bf16", "l1_gemm_swiglu_nvfp4"))}
         per["combine"] = 0.0           # inside each step's L1 (the previous batch's)
-        per["last_batch_combine_once"] = tail0.elapsed_time(end)
+        per["first_step_route_with_staging"] = ev[0][0].elapsed_time(ev[0][1])
+        per["last_batch_l2_and_combine_once"] = tail0.elapsed_time(end)
+    else:
+        names = ("route_permute", "l1_gemm_swiglu_nvfp4", "l2_gemm_bf16", "shared_expert", "combine")
+        per = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+               for j, name in enumerate(names) if name != "shared_expert" or sh is not None}
 
 
-    # with the overlap, each L1 launch also streams the previous batch's combine:
-    # time the L1 GEMM alone too (live, after the timed region, 5 launches)
-    l1_alone_ms = None
+    # in the pipeline each L1 launch also streams the previous batch's combine and
+    # each L2 launch stages the next batch: time both GEMMs alone too (live, after
+    # the timed region, 5 launches each)
+    l1_alone_ms = l2_alone_ms = None
     if ov:
-        cur = sets[(n_done[0] - 1) & 1]
-        evs_alone = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
-        for e0, e1 in evs_alone:
-            e0.record(stream)
-            nv.nvfp4_grouped_gemm(cur.a1_q, cur.a1_sf, R, cur.offsets, cur.counts, E, 2 * I, H, w.w1_q, w.w1_sf,
-                                  1.0, nv.EPI_SWIGLU_NVFP4, out_q=cur.a2_q, out_sf=cur.a2_sf)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        l1_alone_ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs_alone)
+        cur = sets[0]
+
+        def alone(fn):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+            for e0, e1 in evs:
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+        l1_alone_ms = alone(lambda: l1_call(cur))
+        l2_alone_ms = alone(lambda: l2_call(cur))
 
     l1, l2 = ffn_flops(T, H, I, k)
     step_flops = l1 + l2
@@ -636,6 +666,8 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
     e2e_steps = max(args.steps, 2)             # both buffer sets take part
     if plain:
         y_ref = b.y.cpu()                      # the resident run's y (the same inputs every step)
+        if ov and not torch.equal(sets[1].y.cpu(), y_ref):
+            raise RuntimeError("pipeline: the two buffer sets' y differ")
         e2e = e2e_step_host if ov else e2e_host_call
         e2e_ms, e2e_how = e2e(nv, pipeline, s, w, b, x_h, logits_h, k, e2e_steps, world, y_ref)
     else:
@@ -710,11 +742,19 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         side = None
         if ov and args.workload == WORKLOAD:
             comb_bytes = T * k * H * 2 + T * H * 2 + T * k * 8
-            side = {"what": "each L1 launch also runs the previous batch's combine on two spare warps per CTA",
-                    "bytes": comb_bytes, "gbs_over_launch": comb_bytes / (l1_ms * 1e-3) / 1e9,
-                    "l1_alone_ms": l1_alone_ms,
-                    "l1_alone_achieved": l1 / (l1_alone_ms * 1e-3) / 1e12,
-                    "l1_alone_frac": l1 / (l1_alone_ms * 1e-3) / 1e12 / fp4_peak}
+            n_real = int(b.counts.sum().item())
+            stage_bytes = T * H * 2 + n_real * (H // 2 + H // 16) + T * k * 4
+            side = {"l1": {"what": "each L1 launch also runs the previous batch's combine on two spare warps per CTA",
+                           "bytes": comb_bytes, "gbs_over_launch": comb_bytes / (l1_ms * 1e-3) / 1e9,
+                           "l1_alone_ms": l1_alone_ms,
+                           "l1_alone_achieved": l1 / (l1_alone_ms * 1e-3) / 1e12,
+                           "l1_alone_frac": l1 / (l1_alone_ms * 1e-3) / 1e12 / fp4_peak},
+                    "l2": {"what": "each L2 launch also stages the next batch's activation (x quantised once per "
+                                   "token, written into its k permuted rows) on two spare warps per CTA",
+                           "bytes": stage_bytes, "gbs_over_launch": stage_bytes / (l2_ms * 1e-3) / 1e9,
+                           "l2_alone_ms": l2_alone_ms,
+                           "l2_alone_achieved": l2 / (l2_alone_ms * 1e-3) / 1e12,
+                           "l2_alone_frac": l2 / (l2_alone_ms * 1e-3) / 1e12 / fp4_peak}}
         roofline = dict({"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
                                     if args.workload == WORKLOAD else
                                     "L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_kernel<0, 256> (single CTAs)"),
@@ -736,9 +776,10 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                               if args.two_level else "per-16 E4M3 block scales (global scale 1)"),
                    "shared_expert": (f"one shared expert (I={I}) on every token, FLOPs credited"
                                      if args.shared_expert else "none"),
-                   "combine": ("each batch's combine runs inside the next step's L1 GEMM (two spare warps per CTA); "
-                               "the last batch's after the last step, inside the timed region"
-                               if ov else "its own launch at the end of each step")},
+                   "combine": ("serving pipeline: each batch's staging runs inside the previous batch's L2 GEMM and "
+                               "its combine inside the next batch's L1 GEMM (two spare warps per CTA each); the "
+                               "region starts with the pipeline empty and ends with the last batch's L2 and combine"
+                               if ov else "every stage its own launch, each batch's whole path in its own step")},
         "tokens_per_s": tokens_per_s,
         "kernel_ms": per,
         "roofline": roofline,
@@ -746,9 +787,11 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                 "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
                 "copies": e2e_how},
         # per step: top-k, offsets, assign, scatter, L1, L2, combine (+ x's amax and
-        # its finalisation with --two-level; + the shared expert's quantise, L1, L2)
-        "gpu_launches": ((6 if ov else 7) + (2 if args.two_level else 0) + (3 if args.shared_expert else 0))
-                        * args.steps + (1 if ov else 0),
+        # its finalisation with --two-level; + the shared expert's quantise, L1, L2);
+        # the pipeline: top-k, offsets, assign, L2 (+ staging), L1 (+ combine) per
+        # step (the first: scatter in place of L2), then the last L2 and combine
+        "gpu_launches": (5 * args.steps + 2 if ov else
+                         (7 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps),
         "clocks": clk,
         "quantize": quantize,
         "cpu_baseline": cpu,

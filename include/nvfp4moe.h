@@ -5,6 +5,7 @@
  * The path (the "NVFP4 MegaMoE Debug Log", section "NVFP4 MoE Pipeline"):
  *   moe_route_permute      top-k routing, 128-padded expert grouping, and the
  *                          activation staged to NVFP4 in permuted row order
+ *                          (the staging alone: moe_stage_activation)
  *   nvfp4_moe_ffn_forward  L1 block-scaled grouped GEMM -> fused SwiGLU + NVFP4
  *                          re-quantisation -> L2 block-scaled grouped GEMM
  *   moe_combine            routing-weighted sum of each token's expert rows
@@ -113,6 +114,27 @@ typedef struct {
   void* y_bf16;                /* BF16 [T, H], written (16-byte aligned) */
 } nvfp4_combine_job;
 
+/* The activation staging of a routed batch (moe_route_permute's second half,
+ * "stage_activation" into the padded per-expert layout): x quantised once per
+ * token (per 16 along H, as fp32(x * g) under a two-level scale) and its bytes
+ * written into the token's top_k permuted rows of a1_q / a1_sf; every expert's
+ * padding rows get zero scales (their nibbles are not written).  The CTA-pair
+ * L2 GEMM (the BF16 epilogue) can run it on two spare warps per CTA while it
+ * computes; see nvfp4_grouped_gemm's side_stage. */
+typedef struct {
+  const void* x_bf16;              /* BF16 [T, H] (16-byte aligned) */
+  const float* x_global_scale;     /* NULL or x's device encode scale g */
+  const int32_t* inv_perm;         /* int32 [T, top_k]: moe_route_permute's */
+  const int32_t* expert_counts;    /* int32 [E]: moe_route_permute's */
+  const int32_t* expert_offsets;   /* int32 [E+1]: moe_route_permute's */
+  uint8_t* a1_q;                   /* [R_max, H/2], written (16-byte aligned) */
+  uint8_t* a1_sf;                  /* nvfp4_sf_bytes(R_max, H), swizzled, written (16-byte aligned) */
+  int32_t T;                       /* tokens (0: no job) */
+  int32_t H;                       /* a positive multiple of 64 */
+  int32_t E;                       /* 1 .. 1024 */
+  int32_t top_k;                   /* 1 .. min(E, 32) */
+} nvfp4_stage_job;
+
 /* Two-level scale.  The pages' pipeline carries a per-tensor fp32 global scale
  * beside the per-16 E4M3 scales ("NVFP4 MegaMoE Debug Log", "NVFP4 MoE Pipeline":
  * stage_activation returns an input_global_scale; each GEMM's alpha is
@@ -201,6 +223,9 @@ nvfp4_status nvfp4_sf_swizzle(const uint8_t* sf_in, int64_t mn_rows, int64_t k_s
  *               is then not written).
  *   a1_sf       nvfp4_sf_bytes(R_max, H) bytes, swizzled; every byte of the
  *               groups' 128-row bands is written, zero on padding rows.
+ *               NULL (with a1_q and x_q NULL): routing only -- ids, weights,
+ *               counts, offsets, perm_token and inv_perm; the staging then comes
+ *               from moe_stage_activation or an L2 GEMM's side_stage.
  *   x_q         NULL, or [T, H/2]: the same NVFP4 rows in token order, for an L1
  *               GEMM that gathers its A rows through perm_token (the
  *               permuted copy of a1_q is then never materialised).
@@ -244,6 +269,15 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
                                       nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_stage_activation -- the staging half of moe_route_permute on its own
+ * (see nvfp4_stage_job), for a batch routed with a1_sf NULL.  The bytes it
+ * writes equal those of moe_route_permute with staging.
+ * Limits and errors: those of moe_route_permute; NVFP4_ERR_INVALID_ARG for a
+ * null job or a null pointer in a job with T > 0.
+ * -------------------------------------------------------------------------- */
+nvfp4_status moe_stage_activation(const nvfp4_stage_job* job, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * nvfp4_grouped_gemm -- block-scaled NVFP4 grouped GEMM on the tcgen05 tensor
  * cores (the L1 "fused_swiglu" and L2 GEMMs of "NVFP4-1.1 Approach, Part 2"):
  *   acc[r, n] = sum_k dq(A)[r, k] * dq(B_g)[n, k] for the group g owning row r,
@@ -280,6 +314,13 @@ nvfp4_status moe_route_permute_static(const float* logits, const void* x_bf16, i
  *               HBM time mostly hides.  Otherwise it runs as its own launch
  *               first.  Either way y equals moe_combine's bit for bit (the
  *               same fp32 slot-order sum and one rounding).
+ *   side_stage  NULL, or the activation staging of a LATER batch to run
+ *               alongside (see nvfp4_stage_job), under the same rules: inputs
+ *               complete when this call's work starts, buffers disjoint from
+ *               this call's.  With the BF16 epilogue on CTA pairs (the L2
+ *               GEMM), two extra warps per CTA run it while the GEMM computes;
+ *               otherwise it runs as its own launch first.  Either way the
+ *               bytes equal moe_stage_activation's.
  *   epilogue    NVFP4_EPI_SWIGLU_NVFP4: N columns interleaved 8|8 as gate/up;
  *               h = silu(alpha*g) * (alpha*u) quantised as in nvfp4_quantize ->
  *               out_q [rows_max, N/4] bytes and out_sf = SF(rows_max x N/2)
@@ -305,7 +346,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 nvfp4_epilogue epilogue, uint8_t* out_q, uint8_t* out_sf,
                                 void* out_bf16, float* h_debug, const int32_t* a_gather,
                                 int64_t a_gather_rows, const nvfp4_combine_job* side_combine,
-                                nvfp4_stream_t stream);
+                                const nvfp4_stage_job* side_stage, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_mma_peak_probe -- measures the issue ceiling of the block-scaled FP4
@@ -452,24 +493,32 @@ nvfp4_status nvfp4_moe_forward_host(const void* x_host, const float* logits_host
 
 /* ---------------------------------------------------------------------------
  * nvfp4_moe_step_host / nvfp4_moe_finish_host -- a serving loop over batches in
- * host memory, in which each batch's combine runs inside the NEXT batch's L1
- * GEMM (see nvfp4_grouped_gemm's side_combine).  One step, enqueued on `stream`:
+ * host memory, in which each batch's L2 GEMM and combine run in the NEXT step,
+ * overlapped with the next batch's work: the L2 GEMM stages the next batch's
+ * activation on two spare warps per CTA (nvfp4_grouped_gemm's side_stage), and
+ * the next batch's L1 GEMM runs the combine on two spare warps per CTA
+ * (side_combine).  One step, enqueued on `stream`:
  *   1. x_host -> buf->x_bf16, logits_host -> buf->logits (host to device);
  *   2. if compute_after is not NULL, wait for it (cudaStreamWaitEvent);
- *   3. moe_route_permute and nvfp4_moe_ffn_forward of this batch into buf; if
- *      prev is not NULL, the L1 GEMM also runs the pending combine of the
- *      batch in prev (prev_T tokens) into prev->y_bf16;
+ *   3. without prev: moe_route_permute (with staging) and the L1 GEMM of this
+ *      batch into buf.  With prev (the earlier batch, prev_T tokens, whose L2
+ *      and combine are pending): moe_route_permute of this batch without
+ *      staging, the L2 GEMM of prev staging this batch into buf->a1_q / a1_sf
+ *      alongside, then the L1 GEMM of this batch running prev's combine into
+ *      prev->y_bf16 alongside;
  *   4. if compute_done is not NULL, record it;
  *   5. if prev is not NULL, prev->y_bf16 -> prev_y_host (device to host).
- * This batch's combine stays pending in buf: a later step passes buf as its
- * prev, or nvfp4_moe_finish_host runs it (moe_combine, then y -> y_host).
- * Alternating two buffer sets on two streams, with each step's compute_after
- * the previous step's compute_done, lets one step's copies run beside the
- * other's kernels while the combines hide inside the L1 GEMMs.  The caller owns
- * the events (cudaEventCreateWithFlags(..., cudaEventDisableTiming) will do)
- * and keeps a set's buffers alive until its y has been copied out.  Arguments
- * as for nvfp4_moe_forward_host; prev, when given, must have the same H and
- * top_k.  Everything is checked before anything is enqueued.
+ * This batch's L2 and combine stay pending in buf: a later step passes buf as
+ * its prev, or nvfp4_moe_finish_host runs them (L2, moe_combine, then
+ * y -> y_host).  The results equal nvfp4_moe_forward_host's bit for bit.
+ * Rotating three buffer sets over three streams, with each step's
+ * compute_after the previous step's compute_done, lets the copies of one step
+ * run beside the kernels of the next two.  The caller owns the events
+ * (cudaEventCreateWithFlags(..., cudaEventDisableTiming) will do) and keeps a
+ * set's buffers alive until its y has been copied out.  Arguments as for
+ * nvfp4_moe_forward_host; prev, when given, is another buffer set (no buffer
+ * shared with buf) for the same H, I, E and top_k.  Everything is checked
+ * before anything is enqueued.
  * -------------------------------------------------------------------------- */
 typedef struct CUevent_st* nvfp4_event_t;   /* identical to cudaEvent_t */
 
@@ -479,8 +528,9 @@ nvfp4_status nvfp4_moe_step_host(const void* x_host, const float* logits_host, i
                                  int32_t prev_T, void* prev_y_host, nvfp4_event_t compute_after,
                                  nvfp4_event_t compute_done, nvfp4_stream_t stream);
 
-nvfp4_status nvfp4_moe_finish_host(const nvfp4_moe_buffers* buf, int32_t T, int32_t H, int32_t top_k,
-                                   void* y_host, nvfp4_stream_t stream);
+nvfp4_status nvfp4_moe_finish_host(const nvfp4_moe_weights* w, const nvfp4_moe_buffers* buf, int32_t T,
+                                   int32_t H, int32_t I, int32_t E, int32_t top_k, void* y_host,
+                                   nvfp4_stream_t stream);
 
 /* Message of the last failing call on this host thread ("" if none). */
 const char* nvfp4_last_error(void);

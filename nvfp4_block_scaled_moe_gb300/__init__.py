@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "Nvfp4Error", "lib_path", "load", "sf_bytes", "moe_padded_rows_max",
     "moe_route_permute_workspace", "nvfp4_quantize", "nvfp4_sf_swizzle",
-    "moe_route_permute", "moe_route_permute_static", "nvfp4_grouped_gemm", "nvfp4_moe_ffn_forward",
+    "moe_route_permute", "moe_route_permute_static", "moe_stage_activation", "nvfp4_grouped_gemm",
+    "nvfp4_moe_ffn_forward",
     "moe_combine", "nvfp4_moe_forward_host", "nvfp4_moe_step_host", "nvfp4_moe_finish_host",
     "nvfp4_device_status", "nvfp4_selftest_bounded_wait",
     "nvfp4_set_gemm_tiles", "nvfp4_global_scale", "nvfp4_mma_peak_probe",
@@ -59,6 +60,13 @@ class _CombineJobC(ctypes.Structure):
                 ("H", _i32), ("y_bf16", _vp)]
 
 
+class _StageJobC(ctypes.Structure):
+    """nvfp4_stage_job (include/nvfp4moe.h)."""
+    _fields_ = [("x_bf16", _vp), ("x_global_scale", _vp), ("inv_perm", _vp), ("expert_counts", _vp),
+                ("expert_offsets", _vp), ("a1_q", _vp), ("a1_sf", _vp), ("T", _i32), ("H", _i32), ("E", _i32),
+                ("top_k", _i32)]
+
+
 class _MoeBuffersC(ctypes.Structure):
     """nvfp4_moe_buffers (include/nvfp4moe.h)."""
     _fields_ = [("x_bf16", _vp), ("logits", _vp), ("y_bf16", _vp), ("topk_ids", _vp), ("topk_w", _vp),
@@ -77,7 +85,8 @@ _SIGS = {
                                          _vp, _vp, _vp, _vp, _sz, _vp]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _f32,
                                           _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64,
-                                          ctypes.POINTER(_CombineJobC), _vp]),
+                                          ctypes.POINTER(_CombineJobC), ctypes.POINTER(_StageJobC), _vp]),
+    "moe_stage_activation": (ctypes.c_int, [ctypes.POINTER(_StageJobC), _vp]),
     "nvfp4_moe_ffn_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp,
                                              _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                              ctypes.POINTER(_CombineJobC), _vp]),
@@ -89,7 +98,8 @@ _SIGS = {
     "nvfp4_moe_step_host": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_MoeWeightsC),
                                            ctypes.POINTER(_MoeBuffersC), ctypes.POINTER(_MoeBuffersC), _i32, _vp,
                                            _vp, _vp, _vp]),
-    "nvfp4_moe_finish_host": (ctypes.c_int, [ctypes.POINTER(_MoeBuffersC), _i32, _i32, _i32, _vp, _vp]),
+    "nvfp4_moe_finish_host": (ctypes.c_int, [ctypes.POINTER(_MoeWeightsC), ctypes.POINTER(_MoeBuffersC), _i32, _i32,
+                                             _i32, _i32, _i32, _vp, _vp]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_device_status": (ctypes.c_int, [_vp]),
     "nvfp4_selftest_bounded_wait": (ctypes.c_int, [_vp, _i64, _vp]),
@@ -196,17 +206,38 @@ def _combine_job(job):
                                      y.shape[1], y.data_ptr()))
 
 
+def _stage_job(job):
+    """dict(x, inv_perm, counts, offsets, a1_q, a1_sf[, x_global_scale]) of
+    device tensors -> a pointer to nvfp4_stage_job (None -> NULL)."""
+    if job is None:
+        return None
+    x, inv = job["x"], job["inv_perm"]
+    return ctypes.byref(_StageJobC(x.data_ptr(), _p(job.get("x_global_scale")), inv.data_ptr(),
+                                   job["counts"].data_ptr(), job["offsets"].data_ptr(), job["a1_q"].data_ptr(),
+                                   job["a1_sf"].data_ptr(), x.shape[0], x.shape[1], job["counts"].shape[0],
+                                   inv.shape[1]))
+
+
+def moe_stage_activation(job, stream=None):
+    """The staging half of moe_route_permute for a batch routed with a1_sf None
+    (``job`` as for nvfp4_grouped_gemm's side_stage)."""
+    _check(load().moe_stage_activation(_stage_job(job), _stream(stream)))
+
+
 def nvfp4_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, alpha, epilogue,
                        out_q=None, out_sf=None, out_bf16=None, h_debug=None, stream=None, a_global_scale=None,
                        b_global_scale=None, out_global_scale=None, a_gather=None, a_gather_rows=0,
-                       side_combine=None):
+                       side_combine=None, side_stage=None):
     """side_combine: None, or (rows, inv_perm, topk_w, y) of an earlier batch to
-    combine alongside (run on spare warps of the CTA-pair SwiGLU kernel)."""
+    combine alongside (run on spare warps of the CTA-pair SwiGLU kernel).
+    side_stage: None, or dict(x, inv_perm, counts, offsets, a1_q, a1_sf[,
+    x_global_scale]) of a later batch to stage alongside (spare warps of the
+    CTA-pair BF16 kernel)."""
     _check(load().nvfp4_grouped_gemm(_p(a_q), _p(a_sf), rows_max, _p(group_offsets), _p(group_counts), G, N, K,
                                      _p(b_q), _p(b_sf), alpha, _p(a_global_scale), _p(b_global_scale),
                                      _p(out_global_scale), epilogue, _p(out_q), _p(out_sf), _p(out_bf16),
                                      _p(h_debug), _p(a_gather), a_gather_rows, _combine_job(side_combine),
-                                     _stream(stream)))
+                                     _stage_job(side_stage), _stream(stream)))
 
 
 def nvfp4_moe_ffn_forward(a1_q, a1_sf, expert_offsets, expert_counts, E, H, I, rows_max, w1_q, w1_sf, w2_q, w2_sf,
@@ -243,11 +274,13 @@ def _event(ev):
 
 def nvfp4_moe_step_host(x_host, logits_host, top_k, weights, buffers, prev=None, prev_y_host=None,
                         compute_after=None, compute_done=None, stream=None):
-    """One step of a serving loop from host buffers: copy this batch in, route,
-    L1 (+ the pending combine of the batch in ``prev``) and L2 into ``buffers``,
-    then copy prev's y out to ``prev_y_host``.  This batch's combine stays
-    pending (a later step's prev, or nvfp4_moe_finish_host).  Events are
-    torch.cuda.Event objects (recorded once beforehand) or None."""
+    """One step of a serving loop from host buffers: copy this batch in and route
+    it; with ``prev`` (an earlier batch whose L2 and combine are pending), prev's
+    L2 GEMM stages this batch alongside and this batch's L1 GEMM runs prev's
+    combine alongside, then prev's y is copied out to ``prev_y_host``; without,
+    route with staging and L1.  This batch's L2 and combine stay pending (a
+    later step's prev, or nvfp4_moe_finish_host).  Events are torch.cuda.Event
+    objects (recorded once beforehand) or None."""
     T, H = x_host.shape
     E = logits_host.shape[1]
     I = 2 * buffers.a2_q.shape[1]
@@ -259,11 +292,14 @@ def nvfp4_moe_step_host(x_host, logits_host, top_k, weights, buffers, prev=None,
                                       _stream(stream)))
 
 
-def nvfp4_moe_finish_host(buffers, top_k, y_host, stream=None):
-    """The pending combine of the batch in ``buffers``, then its y copied out to y_host."""
+def nvfp4_moe_finish_host(weights, buffers, top_k, y_host, stream=None):
+    """The pending L2 GEMM and combine of the batch in ``buffers``, then its y
+    copied out to y_host."""
     T, H = y_host.shape
-    _check(load().nvfp4_moe_finish_host(ctypes.byref(_buffers_c(buffers)), T, H, top_k, _p(y_host),
-                                        _stream(stream)))
+    E = buffers.counts.shape[0]
+    I = 2 * buffers.a2_q.shape[1]
+    _check(load().nvfp4_moe_finish_host(ctypes.byref(_weights_c(weights)), ctypes.byref(_buffers_c(buffers)), T, H,
+                                        I, E, top_k, _p(y_host), _stream(stream)))
 
 
 def nvfp4_moe_forward_host(x_host, logits_host, y_host, top_k, weights, buffers, stream=None):

@@ -161,8 +161,10 @@ nvfp4_status moe_route_permute(const float* logits, const void* x_bf16, int32_t 
                                size_t workspace_bytes, nvfp4_stream_t stream) {
   CHECK_ARG(T >= 0, "moe_route_permute: T=%d", T);
   CHECK_ARG(expert_counts && expert_offsets && workspace, "moe_route_permute: null pointer");
-  CHECK_ARG(T == 0 || (logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_sf && (a1_q || x_q)),
-            "moe_route_permute: null pointer (a1_q and x_q may not both be null)");
+  CHECK_ARG(T == 0 || (logits && topk_ids && topk_w && perm_token && inv_perm), "moe_route_permute: null pointer");
+  // a1_sf NULL: routing only (a1_q and x_q NULL too); else x and a1_q and / or x_q
+  CHECK_ARG(T == 0 || (a1_sf ? (x_bf16 && (a1_q || x_q)) : (!a1_q && !x_q)),
+            "moe_route_permute: staging needs x, a1_sf and a1_q or x_q (routing only: all four NULL)");
   CHECK_SUP(E >= 1 && E <= 1024, "moe_route_permute: E=%d outside [1, 1024]", E);
   CHECK_SUP(top_k >= 1 && top_k <= E && top_k <= 32, "moe_route_permute: top_k=%d outside [1, min(E, 32)]", top_k);
   CHECK_SUP(H > 0 && H % 64 == 0, "moe_route_permute: H=%d is not a positive multiple of 64", H);
@@ -244,6 +246,39 @@ nvfp4_status check_combine_job(const nvfp4_combine_job* c) {
   return NVFP4_OK;
 }
 
+// a staging job's checks (moe_route_permute's, for the staging half)
+nvfp4_status check_stage_job(const nvfp4_stage_job* j) {
+  if (j == nullptr) return NVFP4_OK;
+  CHECK_ARG(j->T >= 0, "stage job: T=%d", j->T);
+  if (j->T == 0) return NVFP4_OK;
+  CHECK_ARG(j->x_bf16 && j->inv_perm && j->expert_counts && j->expert_offsets && j->a1_q && j->a1_sf,
+            "stage job: null pointer");
+  CHECK_SUP(j->E >= 1 && j->E <= 1024, "stage job: E=%d outside [1, 1024]", j->E);
+  CHECK_SUP(j->top_k >= 1 && j->top_k <= j->E && j->top_k <= 32, "stage job: top_k=%d outside [1, min(E, 32)]",
+            j->top_k);
+  CHECK_SUP(j->H > 0 && j->H % 64 == 0, "stage job: H=%d is not a positive multiple of 64", j->H);
+  CHECK_AL(al16(j->x_bf16) && al16(j->a1_q) && al16(j->a1_sf), "stage job: x, a1_q and a1_sf must be 16-byte aligned");
+  CHECK_AL(al4(j->x_global_scale), "stage job: x_global_scale not 4-byte aligned");
+  return NVFP4_OK;
+}
+
+StageJob stage_job(const nvfp4_stage_job& j) {
+  StageJob s;
+  s.x = j.x_bf16;
+  s.x_gscale = j.x_global_scale;
+  s.inv_perm = j.inv_perm;
+  s.counts = j.expert_counts;
+  s.offsets = j.expert_offsets;
+  s.a_q = j.a1_q;
+  s.a_sf = j.a1_sf;
+  s.x_q = nullptr;
+  s.T = j.T;
+  s.H = j.H;
+  s.E = j.E;
+  s.k = j.top_k;
+  return s;
+}
+
 GemmArgs make_gemm_args(const uint8_t* a_q, const uint8_t* a_sf, int64_t rows_max, const int32_t* group_offsets,
                         const int32_t* group_counts, int32_t G, int32_t N, int32_t K, const uint8_t* b_q,
                         const uint8_t* b_sf, float alpha, const float* a_global_scale, const float* b_global_scale,
@@ -284,8 +319,10 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                                 const float* a_global_scale, const float* b_global_scale,
                                 const float* out_global_scale, nvfp4_epilogue epilogue, uint8_t* out_q,
                                 uint8_t* out_sf, void* out_bf16, float* h_debug, const int32_t* a_gather,
-                                int64_t a_gather_rows, const nvfp4_combine_job* side_combine, nvfp4_stream_t stream) {
+                                int64_t a_gather_rows, const nvfp4_combine_job* side_combine,
+                                const nvfp4_stage_job* side_stage, nvfp4_stream_t stream) {
   nvfp4_status st = check_combine_job(side_combine);
+  if (st == NVFP4_OK) st = check_stage_job(side_stage);
   if (st != NVFP4_OK) return st;
   st = check_grouped_gemm(a_q, a_sf, rows_max, group_offsets, group_counts, G, N, K, b_q, b_sf, a_global_scale,
                          b_global_scale, out_global_scale, epilogue, out_q, out_sf, out_bf16, h_debug, a_gather,
@@ -303,7 +340,16 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
     a.side_H = side_combine->H;
     a.side_k = side_combine->top_k;
   }
+  if (side_stage != nullptr && side_stage->T > 0) a.stage = stage_job(*side_stage);
   return gemm_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status moe_stage_activation(const nvfp4_stage_job* job, nvfp4_stream_t stream) {
+  CHECK_ARG(job != nullptr, "moe_stage_activation: null job");
+  const nvfp4_status st = check_stage_job(job);
+  if (st != NVFP4_OK) return st;
+  const cudaError_t e = stage_launch(stage_job(*job), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_stage_activation");
 }
 
 nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf, const int32_t* expert_offsets,
@@ -323,11 +369,11 @@ nvfp4_status nvfp4_moe_ffn_forward(const uint8_t* a1_q, const uint8_t* a1_sf, co
   nvfp4_status st = nvfp4_grouped_gemm(a1_q, a1_sf, rows_max, expert_offsets, expert_counts, E, 2 * I, H, w1_q,
                                        w1_sf, alpha1, x_global_scale, w1_global_scale, a2_global_scale,
                                        NVFP4_EPI_SWIGLU_NVFP4, a2_q, a2_sf, nullptr, h_debug, a1_gather,
-                                       a1_gather_rows, prev_combine, stream);
+                                       a1_gather_rows, prev_combine, nullptr, stream);
   if (st != NVFP4_OK) return st;
   return nvfp4_grouped_gemm(a2_q, a2_sf, rows_max, expert_offsets, expert_counts, E, H, I, w2_q, w2_sf, alpha2,
                             a2_global_scale, w2_global_scale, nullptr, NVFP4_EPI_BF16, nullptr, nullptr,
-                            rows_out_bf16, nullptr, nullptr, 0, nullptr, stream);
+                            rows_out_bf16, nullptr, nullptr, 0, nullptr, nullptr, stream);
 }
 
 nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const float* topk_w, int32_t T,
@@ -346,16 +392,16 @@ nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const f
 
 namespace {
 
-// the checks of a host-buffer step for T tokens into buffer set b
-nvfp4_status check_host_step(const void* x_host, const float* logits_host, int32_t T, int32_t H, int32_t I, int32_t E,
-                             int32_t top_k, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b) {
-  CHECK_ARG(x_host && logits_host && w && b, "host step: null pointer");
+// the checks of buffer set b for a batch of T tokens (device buffers and sizes)
+nvfp4_status check_buffers(int32_t T, int32_t H, int32_t I, int32_t E, int32_t top_k, const nvfp4_moe_weights* w,
+                           const nvfp4_moe_buffers* b) {
+  CHECK_ARG(w && b, "host step: null pointer");
   CHECK_ARG(T >= 1, "host step: T=%d", T);
   CHECK_ARG(b->x_bf16 && b->logits && b->y_bf16 && b->rows_bf16 && b->topk_ids && b->topk_w && b->expert_counts &&
                 b->expert_offsets && b->perm_token && b->inv_perm && b->a1_q && b->a1_sf && b->a2_q && b->a2_sf &&
                 b->workspace && w->w1_q && w->w1_sf && w->w2_q && w->w2_sf,
             "host step: null device buffer");
-  // the checks of the three calls, before anything is enqueued
+  // the checks of the calls, before anything is enqueued
   CHECK_SUP(E >= 1 && E <= 1024, "host step: E=%d outside [1, 1024]", E);
   CHECK_SUP(top_k >= 1 && top_k <= E && top_k <= 32, "host step: top_k=%d", top_k);
   CHECK_SUP(H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0,
@@ -372,24 +418,43 @@ nvfp4_status check_host_step(const void* x_host, const float* logits_host, int32
   return NVFP4_OK;
 }
 
-// copy-in, then (after an optional wait) route + L1 (+ a side combine) + L2
-nvfp4_status enqueue_host_step(const void* x_host, const float* logits_host, int32_t T, int32_t H, int32_t I,
-                               int32_t E, int32_t top_k, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b,
-                               const nvfp4_combine_job* side, cudaEvent_t compute_after, nvfp4_stream_t stream) {
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+// host x and logits -> b's device x and logits, then an optional wait
+nvfp4_status enqueue_copy_in(const void* x_host, const float* logits_host, int32_t T, int32_t H, int32_t E,
+                             const nvfp4_moe_buffers* b, cudaEvent_t compute_after, cudaStream_t s) {
   cudaError_t e = cudaMemcpyAsync(b->x_bf16, x_host, static_cast<size_t>(T) * H * 2, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(b->logits, logits_host, static_cast<size_t>(T) * E * sizeof(float), cudaMemcpyHostToDevice,
                         s);
   if (e == cudaSuccess && compute_after != nullptr) e = cudaStreamWaitEvent(s, compute_after, 0);
-  if (e != cudaSuccess) return fail_cuda(e, "host step: copy in");
-  nvfp4_status st = moe_route_permute(b->logits, b->x_bf16, T, H, E, top_k, b->topk_ids, b->topk_w,
-                                      b->expert_counts, b->expert_offsets, b->perm_token, b->inv_perm, b->a1_q,
-                                      b->a1_sf, nullptr, nullptr, b->workspace, b->workspace_bytes, stream);
-  if (st != NVFP4_OK) return st;
-  return nvfp4_moe_ffn_forward(b->a1_q, b->a1_sf, b->expert_offsets, b->expert_counts, E, H, I, b->rows_max,
-                               w->w1_q, w->w1_sf, w->w2_q, w->w2_sf, 1.0f, 1.0f, nullptr, nullptr, nullptr, nullptr,
-                               b->a2_q, b->a2_sf, b->rows_bf16, nullptr, nullptr, 0, side, stream);
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "host step: copy in");
+}
+
+// routing of b's batch; staged into a1 unless `stage` is false (routing only)
+nvfp4_status enqueue_route(int32_t T, int32_t H, int32_t E, int32_t top_k, const nvfp4_moe_buffers* b, bool stage,
+                           nvfp4_stream_t stream) {
+  return moe_route_permute(b->logits, b->x_bf16, T, H, E, top_k, b->topk_ids, b->topk_w, b->expert_counts,
+                           b->expert_offsets, b->perm_token, b->inv_perm, stage ? b->a1_q : nullptr,
+                           stage ? b->a1_sf : nullptr, nullptr, nullptr, b->workspace, b->workspace_bytes, stream);
+}
+
+nvfp4_status enqueue_l1(int32_t H, int32_t I, int32_t E, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b,
+                        const nvfp4_combine_job* side, nvfp4_stream_t stream) {
+  return nvfp4_grouped_gemm(b->a1_q, b->a1_sf, b->rows_max, b->expert_offsets, b->expert_counts, E, 2 * I, H,
+                            w->w1_q, w->w1_sf, 1.0f, nullptr, nullptr, nullptr, NVFP4_EPI_SWIGLU_NVFP4, b->a2_q,
+                            b->a2_sf, nullptr, nullptr, nullptr, 0, side, nullptr, stream);
+}
+
+nvfp4_status enqueue_l2(int32_t H, int32_t I, int32_t E, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b,
+                        const nvfp4_stage_job* side, nvfp4_stream_t stream) {
+  return nvfp4_grouped_gemm(b->a2_q, b->a2_sf, b->rows_max, b->expert_offsets, b->expert_counts, E, H, I, w->w2_q,
+                            w->w2_sf, 1.0f, nullptr, nullptr, nullptr, NVFP4_EPI_BF16, nullptr, nullptr,
+                            b->rows_bf16, nullptr, nullptr, 0, nullptr, side, stream);
+}
+
+nvfp4_status copy_out(const nvfp4_moe_buffers* b, int32_t T, int32_t H, void* y_host, cudaStream_t s,
+                      const char* where) {
+  const cudaError_t e = cudaMemcpyAsync(y_host, b->y_bf16, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, where);
 }
 
 }  // namespace
@@ -399,57 +464,80 @@ extern "C" {
 nvfp4_status nvfp4_moe_forward_host(const void* x_host, const float* logits_host, void* y_host, int32_t T,
                                     int32_t H, int32_t I, int32_t E, int32_t top_k, const nvfp4_moe_weights* w,
                                     const nvfp4_moe_buffers* b, nvfp4_stream_t stream) {
-  CHECK_ARG(y_host, "nvfp4_moe_forward_host: null y_host");
-  nvfp4_status st = check_host_step(x_host, logits_host, T, H, I, E, top_k, w, b);
+  CHECK_ARG(x_host && logits_host && y_host, "nvfp4_moe_forward_host: null host pointer");
+  nvfp4_status st = check_buffers(T, H, I, E, top_k, w, b);
   if (st != NVFP4_OK) return st;
-  st = enqueue_host_step(x_host, logits_host, T, H, I, E, top_k, w, b, nullptr, nullptr, stream);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = enqueue_copy_in(x_host, logits_host, T, H, E, b, nullptr, s);
+  if (st == NVFP4_OK) st = enqueue_route(T, H, E, top_k, b, true, stream);
+  if (st == NVFP4_OK) st = enqueue_l1(H, I, E, w, b, nullptr, stream);
+  if (st == NVFP4_OK) st = enqueue_l2(H, I, E, w, b, nullptr, stream);
+  if (st == NVFP4_OK) st = moe_combine(b->rows_bf16, b->inv_perm, b->topk_w, T, H, top_k, nullptr, b->y_bf16, stream);
   if (st != NVFP4_OK) return st;
-  st = moe_combine(b->rows_bf16, b->inv_perm, b->topk_w, T, H, top_k, nullptr, b->y_bf16, stream);
-  if (st != NVFP4_OK) return st;
-  const cudaError_t e = cudaMemcpyAsync(y_host, b->y_bf16, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost,
-                                        reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_moe_forward_host: copy out");
+  return copy_out(b, T, H, y_host, s, "nvfp4_moe_forward_host: copy out");
 }
 
 nvfp4_status nvfp4_moe_step_host(const void* x_host, const float* logits_host, int32_t T, int32_t H, int32_t I,
                                  int32_t E, int32_t top_k, const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b,
                                  const nvfp4_moe_buffers* prev, int32_t prev_T, void* prev_y_host,
                                  nvfp4_event_t compute_after, nvfp4_event_t compute_done, nvfp4_stream_t stream) {
-  nvfp4_status st = check_host_step(x_host, logits_host, T, H, I, E, top_k, w, b);
+  CHECK_ARG(x_host && logits_host, "nvfp4_moe_step_host: null host pointer");
+  nvfp4_status st = check_buffers(T, H, I, E, top_k, w, b);
   if (st != NVFP4_OK) return st;
-  nvfp4_combine_job job = {};
   if (prev != nullptr) {
     CHECK_ARG(prev != b, "nvfp4_moe_step_host: prev is this step's buffer set");
-    CHECK_ARG(prev_T >= 1 && prev_y_host && prev->rows_bf16 && prev->inv_perm && prev->topk_w && prev->y_bf16,
-              "nvfp4_moe_step_host: prev needs prev_T >= 1, prev_y_host and its rows, inv_perm, topk_w and y");
-    CHECK_AL(al16(prev->rows_bf16) && al16(prev->y_bf16), "nvfp4_moe_step_host: prev rows and y not 16-byte aligned");
-    job.rows_bf16 = prev->rows_bf16;
-    job.inv_perm = prev->inv_perm;
-    job.topk_w = prev->topk_w;
-    job.T = prev_T;
-    job.top_k = top_k;
-    job.H = H;
-    job.y_bf16 = prev->y_bf16;
+    CHECK_ARG(prev_y_host, "nvfp4_moe_step_host: prev needs prev_y_host");
+    st = check_buffers(prev_T, H, I, E, top_k, w, prev);
+    if (st != NVFP4_OK) return st;
   }
-  st = enqueue_host_step(x_host, logits_host, T, H, I, E, top_k, w, b, prev != nullptr ? &job : nullptr,
-                         reinterpret_cast<cudaEvent_t>(compute_after), stream);
-  if (st != NVFP4_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = compute_done != nullptr ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(compute_done), s)
-                                          : cudaSuccess;
-  if (e == cudaSuccess && prev != nullptr)
-    e = cudaMemcpyAsync(prev_y_host, prev->y_bf16, static_cast<size_t>(prev_T) * H * 2, cudaMemcpyDeviceToHost, s);
-  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_moe_step_host: event or copy out");
+  st = enqueue_copy_in(x_host, logits_host, T, H, E, b, reinterpret_cast<cudaEvent_t>(compute_after), s);
+  if (st != NVFP4_OK) return st;
+  if (prev == nullptr) {
+    st = enqueue_route(T, H, E, top_k, b, true, stream);
+    if (st == NVFP4_OK) st = enqueue_l1(H, I, E, w, b, nullptr, stream);
+  } else {
+    // routing only; prev's L2 stages this batch on its spare warps; this batch's
+    // L1 runs prev's combine on its spare warps
+    nvfp4_stage_job stage = {};
+    stage.x_bf16 = b->x_bf16;
+    stage.inv_perm = b->inv_perm;
+    stage.expert_counts = b->expert_counts;
+    stage.expert_offsets = b->expert_offsets;
+    stage.a1_q = b->a1_q;
+    stage.a1_sf = b->a1_sf;
+    stage.T = T;
+    stage.H = H;
+    stage.E = E;
+    stage.top_k = top_k;
+    nvfp4_combine_job comb = {};
+    comb.rows_bf16 = prev->rows_bf16;
+    comb.inv_perm = prev->inv_perm;
+    comb.topk_w = prev->topk_w;
+    comb.T = prev_T;
+    comb.top_k = top_k;
+    comb.H = H;
+    comb.y_bf16 = prev->y_bf16;
+    st = enqueue_route(T, H, E, top_k, b, false, stream);
+    if (st == NVFP4_OK) st = enqueue_l2(H, I, E, w, prev, &stage, stream);
+    if (st == NVFP4_OK) st = enqueue_l1(H, I, E, w, b, &comb, stream);
+  }
+  if (st != NVFP4_OK) return st;
+  if (compute_done != nullptr) {
+    const cudaError_t e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(compute_done), s);
+    if (e != cudaSuccess) return fail_cuda(e, "nvfp4_moe_step_host: event");
+  }
+  return prev != nullptr ? copy_out(prev, prev_T, H, prev_y_host, s, "nvfp4_moe_step_host: copy out") : NVFP4_OK;
 }
 
-nvfp4_status nvfp4_moe_finish_host(const nvfp4_moe_buffers* b, int32_t T, int32_t H, int32_t top_k, void* y_host,
-                                   nvfp4_stream_t stream) {
-  CHECK_ARG(b && y_host && T >= 1, "nvfp4_moe_finish_host: null pointer or T < 1");
-  const nvfp4_status st = moe_combine(b->rows_bf16, b->inv_perm, b->topk_w, T, H, top_k, nullptr, b->y_bf16, stream);
+nvfp4_status nvfp4_moe_finish_host(const nvfp4_moe_weights* w, const nvfp4_moe_buffers* b, int32_t T, int32_t H,
+                                   int32_t I, int32_t E, int32_t top_k, void* y_host, nvfp4_stream_t stream) {
+  CHECK_ARG(y_host, "nvfp4_moe_finish_host: null y_host");
+  nvfp4_status st = check_buffers(T, H, I, E, top_k, w, b);
+  if (st == NVFP4_OK) st = enqueue_l2(H, I, E, w, b, nullptr, stream);
+  if (st == NVFP4_OK) st = moe_combine(b->rows_bf16, b->inv_perm, b->topk_w, T, H, top_k, nullptr, b->y_bf16, stream);
   if (st != NVFP4_OK) return st;
-  const cudaError_t e = cudaMemcpyAsync(y_host, b->y_bf16, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost,
-                                        reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "nvfp4_moe_finish_host: copy out");
+  return copy_out(b, T, H, y_host, reinterpret_cast<cudaStream_t>(stream), "nvfp4_moe_finish_host: copy out");
 }
 
 nvfp4_status nvfp4_device_status(nvfp4_stream_t stream) {

@@ -479,14 +479,24 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   const bool pair = bn == 256 && groups <= kPairMaxGroups &&
                     (mode == NVFP4_GEMM_TILES_PAIR ||
                      (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
-  // a side job (the combine of an earlier batch) runs inside the CTA-pair SwiGLU
-  // kernel; with any other kernel it runs as its own launch first
-  if (a.side_T > 0 && !(pair && a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 && a.a_gather == nullptr)) {
-    e = combine_launch(a.side_rows, a.side_inv, a.side_w, a.side_T, a.side_H, a.side_k, nullptr, a.side_y, stream);
-    if (e != cudaSuccess) return fail_cuda(e, "nvfp4_moe_ffn_forward: combine of the earlier batch");
-    GemmArgs plain = a;
-    plain.side_T = 0;
-    return gemm_launch(plain, stream);
+  // side jobs: the combine of an earlier batch runs inside the CTA-pair SwiGLU
+  // kernel, the activation staging of a later batch inside the CTA-pair BF16
+  // kernel; a job the chosen kernel does not host runs as its own launch first
+  const bool host_combine = pair && a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 && a.a_gather == nullptr;
+  const bool host_stage = pair && a.epilogue == NVFP4_EPI_BF16 && a.a_gather == nullptr;
+  if ((a.side_T > 0 && !host_combine) || (a.stage.T > 0 && !host_stage)) {
+    GemmArgs rest = a;
+    if (a.side_T > 0 && !host_combine) {
+      e = combine_launch(a.side_rows, a.side_inv, a.side_w, a.side_T, a.side_H, a.side_k, nullptr, a.side_y, stream);
+      if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm: combine of the earlier batch");
+      rest.side_T = 0;
+    }
+    if (a.stage.T > 0 && !host_stage) {
+      e = stage_launch(a.stage, stream);
+      if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm: staging of the later batch");
+      rest.stage.T = 0;
+    }
+    return gemm_launch(rest, stream);
   }
   if (pair) return gemm_pair_launch(a, info.sms, dev, stream);
   CUtensorMap ma, mb;

@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "stage.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -46,6 +47,8 @@ constexpr int kBM = 128, kBK = 256;                    // rows per CTA, K per st
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSideWarps = 2;                          // the side job's warps (kSide instantiations)
+constexpr int kSideNone = 0, kSideCombine = 1, kSideStage = 2;
+constexpr int kStageSegs = 4;                          // staging segments a side warp has in flight
 constexpr int kThreadsSide = kThreads + 32 * kSideWarps;
 constexpr int kMaxGroups = kPairMaxGroups;             // larger G uses the single-CTA kernel
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
@@ -110,13 +113,15 @@ struct PairParams {
   __nv_bfloat16* out_bf16;
   float* h_debug;
   unsigned* err;
-  // side job (kSide): the combine of an earlier batch, run by the two side warps
-  // of every CTA while the GEMM runs; side_T == 0: none
+  // side jobs, run by the two side warps of every CTA while the GEMM runs:
+  // kSideCombine, the combine of an earlier batch (side_T == 0: none);
+  // kSideStage, the activation staging of a later batch
   const __nv_bfloat16* side_rows;
   const int32_t* side_inv;
   const float* side_w;
   __nv_bfloat16* side_y;
   int32_t side_T, side_H, side_k;
+  StageJob stage;
 };
 
 // last g < G with tab[g] <= v (tab non-decreasing, tab[0] = 0 <= v)
@@ -220,12 +225,13 @@ __device__ __forceinline__ void wait_until_clock(long long due) {
 
 // kGather: A rows come through p.a_gather (tile::gather4); a separate
 // instantiation, so the default kernels carry none of its code.
-// kSide: two more warps per CTA run a side job (the combine of an earlier batch,
-// HBM-bound) while the producer, MMA and epilogue warps run the GEMM, which
-// moves little DRAM traffic of its own; tokens are dealt to the side warps of
-// all CTAs in turn.
-template <int kEpi, bool kGather, bool kSide>
-__global__ void __launch_bounds__(kSide ? kThreadsSide : kThreads, 1)
+// kSide: two more warps per CTA run an HBM-bound side job while the producer,
+// MMA and epilogue warps run the GEMM, whose own DRAM traffic leaves room for
+// it: the combine of an earlier batch (kSideCombine, in the SwiGLU L1 kernel)
+// or the activation staging of a later batch (kSideStage, in the BF16 L2
+// kernel).  Tokens (or segments) are dealt to the side warps of all CTAs in turn.
+template <int kEpi, bool kGather, int kSide>
+__global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                           const __grid_constant__ CUtensorMap tmap_out, const PairParams p) {
@@ -435,14 +441,27 @@ __global__ void __launch_bounds__(kSide ? kThreadsSide : kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // odd CTA: nothing to issue (the even CTA's MMAs read this CTA's stages)
-  } else if (kSide && warp >= 2 + kEpiWarps) {
+  } else if (kSide != kSideNone && warp >= 2 + kEpiWarps) {
     // ----------------------------------------------------------- side job
     const int64_t sw = static_cast<int64_t>(blockIdx.x) * kSideWarps + (warp - 2 - kEpiWarps);
     const int64_t n_sw = static_cast<int64_t>(gridDim.x) * kSideWarps;
-    const int chunks = p.side_H / 8;
-    for (int64_t t = sw; t < p.side_T; t += n_sw)
-      for (int c0 = lane; c0 < chunks; c0 += 32 * 3)
-        combine_chunks<3>(p.side_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t, c0, chunks, p.side_y);
+    if constexpr (kSide == kSideCombine) {
+      const int chunks = p.side_H / 8;
+      for (int64_t t = sw; t < p.side_T; t += n_sw)
+        for (int c0 = lane; c0 < chunks; c0 += 32 * 3)
+          combine_chunks<3>(p.side_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t, c0, chunks, p.side_y);
+    } else {
+      // the padding scales of expert e (one warp per expert), then the
+      // segments: side warp sw takes items sw + n_sw (kStageSegs i + n)
+      for (int e = static_cast<int>(sw); e < p.stage.E; e += static_cast<int>(n_sw)) stage_padding(p.stage, e, lane, 32);
+      const int64_t n_items = static_cast<int64_t>(p.stage.T) * ((p.stage.H + 1023) / 1024);
+      for (int64_t i = sw; i < n_items; i += kStageSegs * n_sw) {
+        int64_t item[kStageSegs];
+#pragma unroll
+        for (int n = 0; n < kStageSegs; ++n) item[n] = i + n * n_sw < n_items ? i + n * n_sw : -1;
+        stage_segments<kStageSegs>(p.stage, item, lane);
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t quad = warp & 3;                // TMEM lanes 32*quad .. +31
@@ -564,8 +583,8 @@ __global__ void __launch_bounds__(kSide ? kThreadsSide : kThreads, 1)
 }
 
 struct PairDeviceInfo {
-  bool attr_set[5] = {};
-  int max_clusters[5] = {};
+  bool attr_set[6] = {};
+  int max_clusters[6] = {};
 };
 
 PairDeviceInfo& pair_info(int dev) {
@@ -578,11 +597,13 @@ std::mutex& pair_mutex() {
   return mu;
 }
 
-template <int kEpi, bool kGather, bool kSide = false>
+template <int kEpi, bool kGather, int kSide = kSideNone>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                         const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
                         cudaStream_t stream) {
-  constexpr int slot = kSide ? 4 : kGather ? 3 : (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2);
+  constexpr int slot = kSide != kSideNone ? 3 + kSide
+                       : kGather          ? 3
+                                          : (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2);
   constexpr uint32_t smem = PairCfg<kEpi>::kSmemBytes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -590,7 +611,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kSide ? kThreadsSide : kThreads, 1, 1);
+  cfg.blockDim = dim3(kSide != kSideNone ? kThreadsSide : kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -670,6 +691,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   p.h_debug = a.h_debug;
   p.err = device_error_word();
   const bool side = a.side_T > 0;
+  const bool stage = a.stage.T > 0;
   p.side_rows = static_cast<const __nv_bfloat16*>(a.side_rows);
   p.side_inv = a.side_inv;
   p.side_w = a.side_w;
@@ -677,6 +699,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   p.side_T = a.side_T;
   p.side_H = a.side_H;
   p.side_k = a.side_k;
+  p.stage = a.stage;
 
   // tiles that can exist: every group's pairs, at most ceil(blocks / 2) + G
   const int64_t blocks = a.rows_max / kBM;
@@ -684,8 +707,10 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   const int64_t max_tiles = max_pairs * p.n_tiles;
   if (max_tiles <= 0) return NVFP4_OK;
 #define NVFP4_PAIR_LAUNCH(E, GA) launch_pair<E, GA>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
-  const cudaError_t e = side ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4, false, true>(ma, mb, msa, msb, mo, p, max_tiles,
-                                                                                sms, dev, stream)
+  const cudaError_t e = side ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4, false, kSideCombine>(ma, mb, msa, msb, mo, p,
+                                                                                        max_tiles, sms, dev, stream)
+                        : stage ? launch_pair<NVFP4_EPI_BF16, false, kSideStage>(ma, mb, msa, msb, mo, p, max_tiles,
+                                                                                 sms, dev, stream)
                         : gather                              ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true)
                         : swiglu                              ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false)
                         : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false)

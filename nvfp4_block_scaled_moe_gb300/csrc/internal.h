@@ -47,7 +47,26 @@ constexpr int kRouteChunk = 128;   // tokens per routing chunk
 size_t route_workspace_bytes(int32_t T, int32_t E);
 void route_carve_workspace(RouteBuffers& b, void* workspace);
 
+// Routing, and the activation staging when b.a1_sf is set.
 cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream);
+
+// The activation staging of a routed batch: x quantised once per token (per 16
+// along H, optionally after the two-level scale) and its bytes written into
+// each of the token's k permuted rows of a_q / a_sf; the padding rows of every
+// expert get zero scale words.  T == 0: nothing.
+struct StageJob {
+  const void* x;              // [T, H] BF16
+  const float* x_gscale;      // two-level encode scale of x (device scalar) or null
+  const int32_t* inv_perm;    // [T, k]
+  const int32_t* counts;      // [E]
+  const int32_t* offsets;     // [E + 1]
+  uint8_t* a_q;               // permuted rows (null: not written)
+  uint8_t* a_sf;              // their swizzled scales
+  uint8_t* x_q;               // token-order rows of x (null: not written)
+  int32_t T, H, E, k;
+};
+
+cudaError_t stage_launch(const StageJob& s, cudaStream_t stream);
 
 cudaError_t combine_launch(const void* rows, const int32_t* inv_perm, const float* w, int32_t T, int32_t H,
                            int32_t top_k, const void* shared, void* y, cudaStream_t stream);
@@ -79,6 +98,9 @@ struct GemmArgs {
   const float* side_w = nullptr;
   void* side_y = nullptr;
   int32_t side_T = 0, side_H = 0, side_k = 0;
+  // side job of the CTA-pair BF16 kernel: the activation staging of a later
+  // batch (x_q null); stage.T == 0: none
+  StageJob stage = {};
 };
 
 // Returns a status; writes a message with set_error_message on failure.

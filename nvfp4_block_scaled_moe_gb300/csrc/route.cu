@@ -10,12 +10,13 @@
 // counts into per-chunk bases and the 128-padded expert offsets, and each chunk
 // then ranks its rows of every expert by token order (bit masks of the tokens
 // that picked it).  Rows of an expert therefore come in ascending token order.
-// x is quantised once per token and the bytes are written straight into the
-// token's k permuted rows; the same launch zeroes the padding rows' scales.
+// The activation staging (stage.cuh) follows as its own launch, or runs later
+// on the side warps of an L2 GEMM.
 #include <float.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "stage.cuh"
 
 namespace nvfp4 {
 
@@ -304,116 +305,35 @@ __global__ void __launch_bounds__(kRouteChunk) route_assign_kernel(const int32_t
 }
 
 // ---------------------------------------------------------------- scatter --
-// The padding rows [offsets[e] + counts[e], offsets[e+1]) of expert e (at most
-// 127 rows, all inside the group's last 128-row band) get zero scale words and
-// no nibbles: a zero E4M3 scale dequantises every E2M1 code (which has no NaN or
-// infinity) to zero, so a padding row is an exact zero row of the GEMM whatever
-// its nibbles hold.  Writing only the scales moves 1/9 of the bytes.
-// In a band's scale atom (512 bytes per 64 columns), 16-byte line l holds the
-// words of rows l, l+32, l+64, l+96; work item (k4, l) of the band zeroes the
-// line with one 16-byte store when all four rows are padding, else the words of
-// its padding rows.  Part `part` of kPadParts blocks takes every kPadParts-th
-// block's worth of items.
 constexpr int kPadParts = 4;
 
-__device__ __forceinline__ void padfill_expert(int e, int part, const int32_t* __restrict__ counts,
-                                               const int32_t* __restrict__ offsets, int32_t H,
-                                               uint8_t* __restrict__ a_sf) {
-  const int64_t lo = __ldg(offsets + e) + __ldg(counts + e);
-  const int64_t hi = __ldg(offsets + e + 1);
-  if (hi <= lo) return;
-  const int64_t band = (hi - 1) >> 7;
-  const int first_pad = static_cast<int>(lo - band * 128);    // band-relative first padding row (1..127)
-  const int k4_total = H / 64;
-  const int64_t items = static_cast<int64_t>(k4_total) * 32;
-  for (int64_t i = static_cast<int64_t>(part) * blockDim.x + threadIdx.x; i < items;
-       i += static_cast<int64_t>(kPadParts) * blockDim.x) {
-    const int l = static_cast<int>(i & 31);
-    const int64_t k4 = i >> 5;
-    uint8_t* line = a_sf + (band * k4_total + k4) * 512 + l * 16;
-    if (l >= first_pad) {
-      *reinterpret_cast<uint4*>(line) = make_uint4(0, 0, 0, 0);
-    } else {
-#pragma unroll
-      for (int c = 1; c < 4; ++c)
-        if (l + 32 * c >= first_pad) *reinterpret_cast<uint32_t*>(line + 4 * c) = 0u;
+// Grid (kPadParts*E + T, ceil(H/1024 / warps)): blocks x < kPadParts*E (with
+// y = 0) zero part x % kPadParts of expert x / kPadParts's padding scales, the
+// others stage token x - kPadParts*E, one warp per 1024-column segment.
+__global__ void __launch_bounds__(256) route_scatter_kernel(const StageJob s) {
+  if (blockIdx.x < static_cast<unsigned>(kPadParts * s.E)) {
+    if (blockIdx.y == 0) {
+      const int part = static_cast<int>(blockIdx.x) % kPadParts;
+      stage_padding(s, static_cast<int>(blockIdx.x) / kPadParts, static_cast<int64_t>(part) * blockDim.x + threadIdx.x,
+                    static_cast<int64_t>(kPadParts) * blockDim.x);
     }
-  }
-}
-
-// Quantise x (PLAIN, per 16 along H) and write the bytes into each of the token's
-// k permuted rows.  Grid (kPadParts*E + T, ceil(H/1024 / warps)): blocks
-// x < kPadParts*E (with y = 0) zero part x % kPadParts of expert x / kPadParts's
-// padding scales, the others quantise token x - kPadParts*E; one warp per
-// 1024-value segment, one thread per two 16-blocks: its 16 bytes of nibbles go
-// to each row in one store (a warp writes 512 contiguous bytes), and a lane
-// pair's four scale bytes form one word of the swizzled layout.  H % 64 == 0, so
-// a lane pair is either wholly inside the row or wholly past its end.
-__global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int32_t H,
-                                                            int32_t k, int32_t E, const int32_t* __restrict__ inv_perm,
-                                                            const int32_t* __restrict__ counts,
-                                                            const int32_t* __restrict__ offsets,
-                                                            const float* __restrict__ gscale,
-                                                            uint8_t* __restrict__ a_q,
-                                                            uint8_t* __restrict__ a_sf,
-                                                            uint8_t* __restrict__ x_q) {
-  if (blockIdx.x < static_cast<unsigned>(kPadParts * E)) {
-    if (blockIdx.y == 0)
-      padfill_expert(static_cast<int>(blockIdx.x) / kPadParts, static_cast<int>(blockIdx.x) % kPadParts, counts,
-                     offsets, H, a_sf);
     return;
   }
-  const int lane = threadIdx.x & 31;
+  const int64_t segs = (s.H + 1023) / 1024;
   const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (seg * 1024 >= H) return;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) - static_cast<int64_t>(kPadParts) * E;
-  const int64_t c0 = seg * 1024 + lane * 32;
-  const bool active = c0 < H;
-  uint4 nib = make_uint4(0, 0, 0, 0);
-  uint32_t codes = 0;
-  if (active) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + t * H + c0);
-    uint4 raw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
-    uint32_t w[4];
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {            // two 16-blocks of 16 values
-      float lo[8], hi[8];
-      bf16x8_to_f32(raw[2 * b], lo);
-      bf16x8_to_f32(raw[2 * b + 1], hi);
-      if (gscale != nullptr) {               // two-level scale: quantise fp32(x * g)
-        const float g = __ldg(gscale);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          lo[i] *= g;
-          hi[i] *= g;
-        }
-      }
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
-      const BlockScale s = block_scale(amax);
-      w[2 * b] = quantize8(lo, s);
-      w[2 * b + 1] = quantize8(hi, s);
-      codes |= s.code << (8 * b);
-    }
-    nib = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  // lanes 2m, 2m+1 own one 64-column group: codes of its four blocks in order
-  const uint32_t word = codes | (__shfl_down_sync(0xFFFFFFFFu, codes, 1) << 16);
-  const uint32_t k4 = static_cast<uint32_t>(c0 / 64);
-  const uint32_t k4_total = static_cast<uint32_t>(H / 64);
-  // token-order rows (read by a gathering L1) and / or the permuted copies; the
-  // scale words always go to the permuted, padded layout
-  if (active && x_q != nullptr) *reinterpret_cast<uint4*>(x_q + t * (H / 2) + c0 / 2) = nib;
-  for (int j = 0; j < k; ++j) {
-    const int64_t r = __ldg(inv_perm + t * k + j);
-    if (active) {
-      if (a_q != nullptr) *reinterpret_cast<uint4*>(a_q + r * (H / 2) + c0 / 2) = nib;
-      if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_word_offset(r, k4, k4_total)) = word;
-    }
-  }
+  if (seg >= segs) return;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) - static_cast<int64_t>(kPadParts) * s.E;
+  const int64_t item[1] = {t * segs + seg};
+  stage_segments<1>(s, item, threadIdx.x & 31);
+}
+
+cudaError_t stage_launch(const StageJob& s, cudaStream_t stream) {
+  if (s.T == 0) return cudaSuccess;
+  const int64_t segs = (s.H + 1023) / 1024;
+  const int warps = static_cast<int>(segs < 8 ? segs : 8);     // no idle warps on short rows
+  const dim3 grid(static_cast<unsigned>(kPadParts * s.E + s.T), static_cast<unsigned>((segs + warps - 1) / warps));
+  route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(s);
+  return cudaGetLastError();
 }
 
 cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
@@ -430,12 +350,22 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(b.E) * (1 + kAssignGroups) * sizeof(int32_t);
     route_assign_kernel<<<n_chunks, kRouteChunk, smem, stream>>>(b.topk_ids, b.T, b.E, b.top_k, b.chunk_hist,
                                                                  b.offsets, b.perm_token, b.inv_perm);
-    const int64_t segs = (b.H + 1023) / 1024;
-    const int warps = static_cast<int>(segs < 8 ? segs : 8);     // no idle warps on short rows
-    const dim3 grid(static_cast<unsigned>(kPadParts * b.E + b.T), static_cast<unsigned>((segs + warps - 1) / warps));
-    route_scatter_kernel<<<grid, 32 * warps, 0, stream>>>(static_cast<const __nv_bfloat16*>(b.x), b.H, b.top_k, b.E,
-                                                          b.inv_perm, b.counts, b.offsets, b.x_gscale, b.a1_q,
-                                                          b.a1_sf, b.x_q);
+    if (b.a1_sf != nullptr) {
+      StageJob s;
+      s.x = b.x;
+      s.x_gscale = b.x_gscale;
+      s.inv_perm = b.inv_perm;
+      s.counts = b.counts;
+      s.offsets = b.offsets;
+      s.a_q = b.a1_q;
+      s.a_sf = b.a1_sf;
+      s.x_q = b.x_q;
+      s.T = b.T;
+      s.H = b.H;
+      s.E = b.E;
+      s.k = b.top_k;
+      return stage_launch(s, stream);
+    }
   }
   return cudaGetLastError();
 }

@@ -69,8 +69,12 @@ extern "C" nvfp4_status moe_route_permute_static(const float* logits, const void
   if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: T=%d", T);
   if (!expert_counts || !expert_offsets)
     return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: null pointer");
-  if (T > 0 && !(logits && x_bf16 && topk_ids && topk_w && perm_token && inv_perm && a1_sf && (a1_q || x_q)))
-    return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: null pointer (a1_q and x_q may not both be null)");
+  if (T > 0 && !(logits && topk_ids && topk_w && perm_token && inv_perm))
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_route_permute_static: null pointer");
+  // a1_sf NULL: routing only (a1_q and x_q NULL too); else x and a1_q and / or x_q
+  if (T > 0 && !(a1_sf ? (x_bf16 && (a1_q || x_q)) : (!a1_q && !x_q)))
+    return fail(NVFP4_ERR_INVALID_ARG,
+                "moe_route_permute_static: staging needs x, a1_sf and a1_q or x_q (routing only: all four NULL)");
   if (E < 1 || E > 1024) return fail(NVFP4_ERR_UNSUPPORTED, "moe_route_permute_static: E=%d outside [1, 1024]", E);
   if (top_k < 1 || top_k > E || top_k > 32)
     return fail(NVFP4_ERR_UNSUPPORTED, "moe_route_permute_static: top_k=%d outside [1, min(E, 32)]", top_k);

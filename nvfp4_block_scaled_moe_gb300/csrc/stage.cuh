@@ -1,0 +1,128 @@
+// Activation staging of a routed batch ("NVFP4 MegaMoE Debug Log", section
+// "NVFP4 MoE Pipeline": stage_activation; "NVFP4-1.1 Approach, Part 2": the
+// padded per-expert layout), as device functions shared by the routing launch
+// (route.cu) and by the side warps of the CTA-pair BF16 GEMM (gemm_pair.cu),
+// which stage a later batch while the L2 GEMM of an earlier one runs.
+//
+// x is quantised once per token (PLAIN, per 16 along H) and the bytes are
+// written into each of the token's k permuted rows.  The work comes in
+// 1024-column segments of one token: lane i of a warp takes columns 32i..32i+31
+// (two 16-blocks), so a warp's 16-byte nibble stores cover 512 contiguous bytes
+// of each row, and a lane pair's four scale bytes form one word of the swizzled
+// layout.  H % 64 == 0, so a lane pair is wholly inside the row or wholly past it.
+//
+// The padding rows [offsets[e] + counts[e], offsets[e+1]) of expert e (at most
+// 127 rows, all inside the group's last 128-row band) get zero scale words and
+// no nibbles: a zero E4M3 scale dequantises every E2M1 code (which has no NaN or
+// infinity) to zero, so a padding row is an exact zero row of the GEMM whatever
+// its nibbles hold.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+// Zero the padding scales of expert e: work items first, first + stride, ... of
+// the band's H/64 x 32 items.  In a band's scale atom (512 bytes per 64
+// columns), 16-byte line l holds the words of rows l, l+32, l+64, l+96; item
+// (k4, l) zeroes the line with one 16-byte store when all four rows are
+// padding, else the words of its padding rows (real rows' words are never
+// touched, so this may run concurrently with the rows' own stores).
+__device__ __forceinline__ void stage_padding(const StageJob& s, int e, int64_t first, int64_t stride) {
+  const int64_t lo = __ldg(s.offsets + e) + __ldg(s.counts + e);
+  const int64_t hi = __ldg(s.offsets + e + 1);
+  if (hi <= lo) return;
+  const int64_t band = (hi - 1) >> 7;
+  const int first_pad = static_cast<int>(lo - band * 128);    // band-relative first padding row (1..127)
+  const int k4_total = s.H / 64;
+  const int64_t items = static_cast<int64_t>(k4_total) * 32;
+  for (int64_t i = first; i < items; i += stride) {
+    const int l = static_cast<int>(i & 31);
+    const int64_t k4 = i >> 5;
+    uint8_t* line = s.a_sf + (band * k4_total + k4) * 512 + l * 16;
+    if (l >= first_pad) {
+      *reinterpret_cast<uint4*>(line) = make_uint4(0, 0, 0, 0);
+    } else {
+#pragma unroll
+      for (int c = 1; c < 4; ++c)
+        if (l + 32 * c >= first_pad) *reinterpret_cast<uint32_t*>(line + 4 * c) = 0u;
+    }
+  }
+}
+
+// One warp stages the segments item[0..kNS) (item = token * segs + segment,
+// segs = ceil(H / 1024); item < 0: none).  Every segment's x loads, and its
+// token's k row indices (lane j loads slot j; k <= 32), are issued before any
+// is used, so a warp keeps kNS x 2 KiB of reads in flight and never waits on
+// one index load per row.  The caller's whole warp takes part (the scale words
+// are paired, the row indices broadcast, by shuffle); item[] is warp-uniform.
+template <int kNS>
+__device__ __forceinline__ void stage_segments(const StageJob& s, const int64_t (&item)[kNS], int lane) {
+  const int64_t segs = (s.H + 1023) / 1024;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(s.x);
+  uint4 raw[kNS][4];
+  int64_t tok[kNS];
+  int64_t c0[kNS];
+  int32_t rows[kNS];
+#pragma unroll
+  for (int n = 0; n < kNS; ++n) {
+    tok[n] = item[n] >= 0 ? item[n] / segs : 0;
+    c0[n] = item[n] >= 0 ? (item[n] - tok[n] * segs) * 1024 + lane * 32 : s.H;
+    rows[n] = item[n] >= 0 && lane < s.k ? __ldg(s.inv_perm + tok[n] * s.k + lane) : 0;
+    if (c0[n] < s.H) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + tok[n] * s.H + c0[n]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) raw[n][i] = __ldg(src + i);
+    }
+  }
+  const float g = s.x_gscale != nullptr ? __ldg(s.x_gscale) : 1.0f;
+  const uint32_t k4_total = static_cast<uint32_t>(s.H / 64);
+#pragma unroll
+  for (int n = 0; n < kNS; ++n) {
+    if (item[n] < 0) continue;               // warp-uniform
+    const bool active = c0[n] < s.H;
+    uint4 nib = make_uint4(0, 0, 0, 0);
+    uint32_t codes = 0;
+    if (active) {
+      uint32_t w[4];
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {          // two 16-blocks of 16 values
+        float lo[8], hi[8];
+        bf16x8_to_f32(raw[n][2 * b], lo);
+        bf16x8_to_f32(raw[n][2 * b + 1], hi);
+        if (s.x_gscale != nullptr) {         // two-level scale: quantise fp32(x * g)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            lo[i] *= g;
+            hi[i] *= g;
+          }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
+        const BlockScale bs = block_scale(amax);
+        w[2 * b] = quantize8(lo, bs);
+        w[2 * b + 1] = quantize8(hi, bs);
+        codes |= bs.code << (8 * b);
+      }
+      nib = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    // lanes 2m, 2m+1 own one 64-column group: codes of its four blocks in order
+    const uint32_t word = codes | (__shfl_down_sync(0xFFFFFFFFu, codes, 1) << 16);
+    const uint32_t k4 = static_cast<uint32_t>(c0[n] / 64);
+    const int64_t t = tok[n];
+    // token-order rows (read by a gathering L1) and / or the permuted copies; the
+    // scale words always go to the permuted, padded layout
+    if (active && s.x_q != nullptr) *reinterpret_cast<uint4*>(s.x_q + t * (s.H / 2) + c0[n] / 2) = nib;
+    for (int j = 0; j < s.k; ++j) {
+      const int64_t r = __shfl_sync(0xFFFFFFFFu, rows[n], j);
+      if (active) {
+        if (s.a_q != nullptr) *reinterpret_cast<uint4*>(s.a_q + r * (s.H / 2) + c0[n] / 2) = nib;
+        if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(s.a_sf + sf_word_offset(r, k4, k4_total)) = word;
+      }
+    }
+  }
+}
+
+}  // namespace nvfp4

@@ -1,7 +1,10 @@
 """Device buffers and the three-call forward of the NVFP4 MoE expert FFN.
 
 Plumbing only: PyTorch allocates device memory; every step is one call into
-libnvfp4moe.so (route + permute + stage, L1/SwiGLU/requant/L2, combine).
+libnvfp4moe.so (route + permute + stage, L1/SwiGLU/requant/L2, combine), and
+the serving-loop step (moe_forward_deferred) orders the same calls so that each
+batch's staging runs inside the previous batch's L2 GEMM and each batch's
+combine inside the next batch's L1 GEMM.
 
 Two-level scale (optional): the pages' pipeline carries per-tensor global scales
 ("NVFP4 MoE Pipeline": stage_activation returns an input_global_scale; alpha =
@@ -182,29 +185,50 @@ def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuff
     return b.y
 
 
-def moe_forward_deferred(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
-                         prev: MoeBuffers | None = None, alpha1: float = 1.0, alpha2: float = 1.0) -> None:
-    """Route + permute + stage, L1 + SwiGLU + requant + L2 of this batch into ``b``,
-    with its combine left pending; if ``prev`` holds an earlier batch whose combine
-    is pending, the L1 GEMM runs that combine on spare warps (into prev.y).  A
-    serving loop alternates two buffer sets and ends with moe_combine_deferred on
-    the last one.  One-level scales, no shared expert."""
+def _l1(w: MoeWeights, b: MoeBuffers, side_combine=None) -> None:
     s = b.shape
-    moe_route_permute(logits, x, s.top_k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token,
-                      b.inv_perm, b.a1_q, b.a1_sf, b.workspace, x_q=b.x_q)
-    job = None if prev is None else (prev.rows_out, prev.inv_perm, prev.topk_w, prev.y)
+    nvfp4_grouped_gemm(b.a1_q, b.a1_sf, b.rows_max, b.offsets, b.counts, s.E, 2 * s.I, s.H, w.w1_q, w.w1_sf, 1.0,
+                       EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf, h_debug=b.h_debug, side_combine=side_combine)
+
+
+def _l2(w: MoeWeights, b: MoeBuffers, side_stage=None) -> None:
+    s = b.shape
+    nvfp4_grouped_gemm(b.a2_q, b.a2_sf, b.rows_max, b.offsets, b.counts, s.E, s.H, s.I, w.w2_q, w.w2_sf, 1.0,
+                       EPI_BF16, out_bf16=b.rows_out, side_stage=side_stage)
+
+
+def moe_forward_deferred(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
+                         prev: MoeBuffers | None = None) -> None:
+    """One step of a serving loop.  Without ``prev``: route + permute + stage and
+    the L1 GEMM of this batch into ``b``.  With ``prev`` (an earlier batch whose
+    L2 and combine are pending): routing of this batch without staging; prev's
+    L2 GEMM, which stages this batch on spare warps; this batch's L1 GEMM, which
+    runs prev's combine on spare warps (into prev.y).  This batch's L2 and
+    combine stay pending: a later step's prev, or moe_finish_deferred.  A loop
+    alternates two buffer sets.  One-level scales, alpha 1, no shared expert,
+    no gathered L1."""
+    s = b.shape
+    if b.gather or (prev is not None and prev.gather):
+        raise ValueError("the deferred serving step stages permuted rows (no gathered L1)")
+    live_prev = prev is not None and prev.shape.T > 0
+    moe_route_permute(logits, x, s.top_k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token, b.inv_perm,
+                      None if live_prev else b.a1_q, None if live_prev else b.a1_sf, b.workspace)
+    job = None
+    if live_prev:
+        stage = (dict(x=x, inv_perm=b.inv_perm, counts=b.counts, offsets=b.offsets, a1_q=b.a1_q, a1_sf=b.a1_sf)
+                 if s.T > 0 else None)
+        _l2(w, prev, side_stage=stage)
+        job = (prev.rows_out, prev.inv_perm, prev.topk_w, prev.y)
     if s.T > 0:
-        gather = dict(a1_gather=b.perm_token, a1_gather_rows=s.T) if b.gather else {}
-        nvfp4_moe_ffn_forward(b.x_q if b.gather else b.a1_q, b.a1_sf, b.offsets, b.counts, s.E, s.H, s.I,
-                              b.rows_max, w.w1_q, w.w1_sf, w.w2_q, w.w2_sf, alpha1, alpha2, b.a2_q, b.a2_sf,
-                              b.rows_out, b.h_debug, prev_combine=job, **gather)
+        _l1(w, b, side_combine=job)
     elif job is not None:
         moe_combine(*job)
 
 
-def moe_combine_deferred(b: MoeBuffers) -> torch.Tensor:
-    """The pending combine of the batch in ``b`` (after moe_forward_deferred)."""
+def moe_finish_deferred(w: MoeWeights, b: MoeBuffers) -> torch.Tensor:
+    """The pending L2 GEMM and combine of the batch in ``b`` (after moe_forward_deferred)."""
     if b.shape.T > 0:
+        _l2(w, b)
         moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
     return b.y
 

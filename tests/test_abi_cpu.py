@@ -61,6 +61,11 @@ def nvb_job(rows, inv, w, T, k, H, y):
     return nvb._CombineJobC(rows, inv, w, T, k, H, y)
 
 
+def nvb_stage(x, gs, inv, counts, offsets, a1_q, a1_sf, T, H, E, k):
+    import nvfp4_block_scaled_moe_gb300 as nvb
+    return nvb._StageJobC(x, gs, inv, counts, offsets, a1_q, a1_sf, T, H, E, k)
+
+
 @needs_nvcc
 def test_host_validation_without_gpu(lib):
     import nvfp4_block_scaled_moe_gb300 as nv
@@ -87,11 +92,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.nvfp4_global_scale(p, 0, 4, 16, 16, vp(base + 2), None) == 3
     assert lib.nvfp4_sf_swizzle(p, 4, 4, 0, 1, p, 0, None) == 1
     # K not a multiple of 256; N not a multiple of 128 (BF16) / 256 (SwiGLU); G without offsets
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 200, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 192, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, None, None, None, 0, p, p, None, None, None, 0, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None) == 2
-    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 7, None, None, p, None, None, 0, None, None) == 1
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 200, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 192, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 128, 256, p, p, 1.0, None, None, None, 0, p, p, None, None, None, 0, None, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 4, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p, None, None, 0, None, None, None) == 2
+    assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 7, None, None, p, None, None, 0, None, None, None) == 1
     # routing limits
     assert lib.moe_route_permute(p, p, 8, 64, 2000, 2, p, p, p, p, p, p, p, p, None, None, p, 1 << 20, None) == 2
     assert lib.moe_route_permute(p, p, 8, 64, 8, 9, p, p, p, p, p, p, p, p, None, None, p, 1 << 20, None) == 2
@@ -103,12 +108,12 @@ def test_host_validation_without_gpu(lib):
                                  None) == 3
     # gathered A: a row count is required, the index must be 16-byte aligned
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
-                                  None, p, 0, None, None) == 1
+                                  None, p, 0, None, None, None) == 1
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
-                                  None, vp(base + 4), 64, None, None) == 3
+                                  None, vp(base + 4), 64, None, None, None) == 3
     # gathered A with an epilogue other than SwiGLU + NVFP4 (the L1 GEMM's) is not built
     assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None, p,
-                                  None, p, 64, None, None) == 2
+                                  None, p, 64, None, None, None) == 2
     assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 200, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p, p, None, None, 0, None, None) == 2
     # a side combine job: its own checks, before anything is launched
     job_bad_k = nvb_job(base, base, base, 4, 40, 512, base)
@@ -117,7 +122,20 @@ def test_host_validation_without_gpu(lib):
     job_odd_h = nvb_job(base, base, base, 4, 2, 500, base)
     for job, st in ((job_bad_k, 1), (job_null, 1), (job_odd_y, 3), (job_odd_h, 2)):
         assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 0, p, p,
-                                      None, None, None, 0, ctypes.byref(job), None) == st
+                                      None, None, None, 0, ctypes.byref(job), None, None) == st
+    # a side staging job: its own checks, before anything is launched
+    def stage(x=base, inv=base, cnt=base, off=base, q=base, sf=base, T=4, H=512, E=8, k=2):
+        return nvb_stage(x, None, inv, cnt, off, q, sf, T, H, E, k)
+    for job, st in ((stage(inv=None), 1), (stage(sf=None), 1), (stage(E=2000), 2), (stage(k=9), 2),
+                    (stage(k=40, E=64), 2), (stage(H=96), 2), (stage(x=base + 8), 3), (stage(q=base + 4), 3)):
+        assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None,
+                                      p, None, None, 0, None, ctypes.byref(job), None) == st
+        assert lib.moe_stage_activation(ctypes.byref(job), None) == st
+    assert lib.moe_stage_activation(None, None) == 1
+    # routing only (a1_sf NULL) takes neither a1_q nor x_q
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, p, None, None, None, p, 1 << 20, None) == 1
+    assert lib.moe_route_permute(p, p, 8, 64, 8, 2, p, p, p, p, p, p, None, None, p, None, p, 1 << 20, None) == 1
+    assert lib.moe_route_permute_static(p, p, 8, 64, 8, 2, p, p, p, p, p, p, p, None, None, None, None) == 1
     # the forward's job must have the forward's H
     job_h = nvb_job(base, base, base, 4, 2, 768, base)
     assert lib.nvfp4_moe_ffn_forward(p, p, p, p, 8, 512, 256, 128, p, p, p, p, 1.0, 1.0, None, None, None, None, p, p,
@@ -136,6 +154,18 @@ def test_host_validation_without_gpu(lib):
     odd_buf = nvb._MoeBuffersC(*([base] * 9 + [base + 8] + [base] * 5), 1 << 20, 1024)
     assert lib.nvfp4_moe_forward_host(p, p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(odd_buf),
                                       None) == 3
+    # serving-loop steps: prev may not be this step's set, needs a y buffer on the host and its own checks
+    assert lib.nvfp4_moe_step_host(p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(bufs),
+                                   ctypes.byref(bufs), 4, p, None, None, None) == 1
+    other = nvb._MoeBuffersC(*([base] * 15), 1 << 20, 1024)
+    assert lib.nvfp4_moe_step_host(p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(bufs),
+                                   ctypes.byref(other), 4, None, None, None, None) == 1
+    assert lib.nvfp4_moe_step_host(p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(bufs),
+                                   ctypes.byref(short), 4, p, None, None, None) == 1
+    assert lib.nvfp4_moe_step_host(p, p, 4, 512, 256, 8, 2, ctypes.byref(wts), ctypes.byref(bufs),
+                                   ctypes.byref(other), 0, p, None, None, None) == 1
+    assert lib.nvfp4_moe_finish_host(ctypes.byref(wts), ctypes.byref(bufs), 4, 512, 256, 8, 2, None, None) == 1
+    assert lib.nvfp4_moe_finish_host(ctypes.byref(wts), ctypes.byref(odd_buf), 4, 512, 256, 8, 2, p, None) == 3
     assert lib.moe_combine(p, p, p, 4, 12, 2, None, p, None) == 2
     assert lib.moe_combine(p, p, p, 4, 16, 2, vp(base + 8), p, None) == 3     # misaligned shared rows
     d = ctypes.c_double(0.0)

@@ -146,9 +146,10 @@ def test_forward_from_host_buffers(nv):
 
 def test_serving_loop_from_host_buffers(nv):
     """nvfp4_moe_step_host / nvfp4_moe_finish_host over three different batches on
-    two buffer sets and two streams: each step's L1 runs the previous batch's
-    combine, each step copies the previous batch's y out.  Every y equals the
-    plain forward's bit for bit."""
+    two buffer sets and two streams: each step routes its batch, runs the
+    previous batch's L2 (staging this batch alongside) and its own L1 (running
+    the previous batch's combine alongside), and copies the previous batch's y
+    out.  Every y equals the plain forward's bit for bit."""
     nv, pipeline = nv
     spec = inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=25, zipf=True)
     s, w, _ = _gpu_setup(pipeline, spec)
@@ -170,7 +171,7 @@ def test_serving_loop_from_host_buffers(nv):
         nv.nvfp4_moe_step_host(x_h[i], l_h[i], spec["top_k"], w, sets[j], prev=sets[1 - j] if i else None,
                                prev_y_host=y_h[i - 1] if i else None, compute_after=done[1 - j] if i else None,
                                compute_done=done[j], stream=streams[j])
-    nv.nvfp4_moe_finish_host(sets[0], spec["top_k"], y_h[2], stream=streams[0])
+    nv.nvfp4_moe_finish_host(w, sets[0], spec["top_k"], y_h[2], stream=streams[0])
     torch.cuda.synchronize()
     nv.nvfp4_device_status()
     for i in range(3):
