@@ -18,7 +18,8 @@ order and notation of the source pages ("nvfp4-megamoe-kernel" notes):
 Parity pins: every function is pinned in ``tests/test_oracle_*.py`` against
 values the pages print (``tests/golden/``), closed forms, library routines
 (PyTorch's float8_e4m3fn cast, numpy matmul) and brute force on tiny inputs.
-Parity unpinned: the E2M1 half-step table entries hs=5 and hs=7 (the pages print
-only hs=10 and hs=11); they follow the ties-to-even reading stated in
-``oracle.nvfp4.step_to_idx``.
+The E2M1 half-step table entries hs=5 and hs=7 are not printed by the pages
+(they print hs=10 and hs=11); they follow the ties-to-even reading stated in
+``oracle.nvfp4.step_to_idx``, which the tests pin to PyTorch's independent
+reference rounding to E2M1.
 """

@@ -142,7 +142,7 @@ def step_to_idx() -> tuple:
     table maps it to the nearest E2M1 magnitude with ties to the even index.
     The pages pin hs=10 -> 6 and hs=11 -> 7; ties-to-even is the only simple
     rule consistent with hs=10 -> 6 (ties-away would give 7), and it fixes the
-    unpinned tie entries hs=5 -> 4 and hs=7 -> 6.
+    unprinted tie entries hs=5 -> 4 and hs=7 -> 6.
     """
     return tuple(_nearest_e2m1_index(hs / 2.0) for hs in range(13))
 

@@ -35,6 +35,11 @@ def _ties_away_table():
     return (0, 1, 2, 3, 4, 5, 5, 6, 6, 6, 7, 7, 7)
 
 
+def _hs5_up_table():
+    # only the unprinted tie hs = 5 (2.5) rounded up to 3
+    return (0, 1, 2, 3, 4, 5, 5, 6, 6, 6, 6, 7, 7)
+
+
 def _half_up(s):
     return int(math.floor(2.0 * min(abs(float(s)), 6.0) + 0.5))
 
@@ -68,6 +73,7 @@ MUTATIONS = [
     ("e4m3 bias 8", "e4m3_decode", _decode_bias8, codecs.test_e4m3_golden_values_from_pages),
     ("e4m3 truncating encode", "e4m3_encode", _encode_truncating, codecs.test_e4m3_golden_values_from_pages),
     ("step table ties away", "STEP_TO_IDX", _ties_away_table(), codecs.test_e2m1_golden_from_pages),
+    ("step table hs=5 up", "STEP_TO_IDX", _hs5_up_table(), codecs.test_step_table_is_rne_onto_the_e2m1_grid),
     ("half-up half step", "half_step", _half_up, codecs.test_e2m1_golden_from_pages),
     ("SF atoms M-innermost", "sf_offset", _offset_m_inner, quant.test_sf_closed_form_equals_cute_atom_tiling),
     ("nibble order high-first", "dequantize_rows", _dequant_high_first,
