@@ -273,19 +273,24 @@ def _event(ev):
 
 
 def nvfp4_moe_step_host(x_host, logits_host, top_k, weights, buffers, prev=None, prev_y_host=None,
-                        compute_after=None, compute_done=None, stream=None):
+                        compute_after=None, compute_done=None, stream=None, prev_T=None):
     """One step of a serving loop from host buffers: copy this batch in and route
     it; with ``prev`` (an earlier batch whose L2 and combine are pending), prev's
     L2 GEMM stages this batch alongside and this batch's L1 GEMM runs prev's
     combine alongside, then prev's y is copied out to ``prev_y_host``; without,
     route with staging and L1.  This batch's L2 and combine stay pending (a
     later step's prev, or nvfp4_moe_finish_host).  Events are torch.cuda.Event
-    objects (recorded once beforehand) or None."""
+    objects (recorded once beforehand) or None.  Batches may differ in size up
+    to the buffers' T: prev_T is the earlier batch's token count (default: the
+    rows of prev_y_host)."""
     T, H = x_host.shape
     E = logits_host.shape[1]
     I = 2 * buffers.a2_q.shape[1]
     prev_c = ctypes.byref(_buffers_c(prev)) if prev is not None else None
-    prev_T = prev.shape.T if prev is not None else 0
+    if prev is None:
+        prev_T = 0
+    elif prev_T is None:
+        prev_T = prev_y_host.shape[0]
     _check(load().nvfp4_moe_step_host(_p(x_host), _p(logits_host), T, H, I, E, top_k,
                                       ctypes.byref(_weights_c(weights)), ctypes.byref(_buffers_c(buffers)), prev_c,
                                       prev_T, _p(prev_y_host), _event(compute_after), _event(compute_done),

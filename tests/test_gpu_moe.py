@@ -176,3 +176,43 @@ def test_serving_loop_from_host_buffers(nv):
     nv.nvfp4_device_status()
     for i in range(3):
         assert torch.equal(y_h[i], plain[i]), i
+
+
+def test_serving_loop_with_batches_of_different_sizes(nv):
+    """The serving loop over batches of 300, 37, 1 and 200 tokens through buffer
+    sets sized for 300: each batch's y equals the plain forward of that batch
+    alone, bit for bit.  (Buffers this small send the GEMMs to the single-CTA
+    kernel, so the side jobs run as their own launches before each GEMM;
+    test_gpu_side_jobs.py covers them inside the CTA-pair kernels.)"""
+    nv, pipeline = nv
+    spec = inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=26, zipf=True)
+    s, w, _ = _gpu_setup(pipeline, spec)
+    x_t, _ = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    sizes = [300, 37, 1, 200]
+    starts = [0, 11, 299, 50]
+    xs = [x_t[a:a + n].contiguous() for a, n in zip(starts, sizes)]
+    lgs = [np.ascontiguousarray(logits[a:a + n]) for a, n in zip(starts, sizes)]
+    plain = []
+    for x, lg in zip(xs, lgs):
+        si = pipeline.MoeShape(T=x.shape[0], H=s.H, I=s.I, E=s.E, top_k=s.top_k)
+        plain.append(pipeline.moe_forward(x.cuda(), dev(lg), w, pipeline.MoeBuffers(si)).cpu())
+    x_h = [x.pin_memory() for x in xs]
+    l_h = [torch.from_numpy(l).pin_memory() for l in lgs]
+    sets = [pipeline.MoeBuffers(s).enable_host_io() for _ in range(3)]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    done = [torch.cuda.Event() for _ in range(3)]
+    for ev, st in zip(done, streams):
+        ev.record(st)
+    y_h = [torch.zeros((n, spec["H"]), dtype=torch.bfloat16).pin_memory() for n in sizes]
+    for i in range(len(sizes)):
+        j, p = i % 3, (i - 1) % 3
+        nv.nvfp4_moe_step_host(x_h[i], l_h[i], spec["top_k"], w, sets[j], prev=sets[p] if i else None,
+                               prev_y_host=y_h[i - 1] if i else None, compute_after=done[p] if i else None,
+                               compute_done=done[j], stream=streams[j])
+    last = (len(sizes) - 1) % 3
+    nv.nvfp4_moe_finish_host(w, sets[last], spec["top_k"], y_h[-1], stream=streams[last])
+    torch.cuda.synchronize()
+    nv.nvfp4_device_status()
+    for i in range(len(sizes)):
+        assert torch.equal(y_h[i], plain[i]), i

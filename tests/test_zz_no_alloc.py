@@ -67,6 +67,37 @@ def test_static_scratch_route_permute_matches_workspace_version_twice():
                 assert np.array_equal(a[key], b[key]), key
 
 
+def test_static_scratch_routing_only_then_staging():
+    """Routing only (a1_q, a1_sf NULL) through the static-scratch call, then the
+    staging on its own (moe_stage_activation, which allocates nothing either):
+    the same bytes as the workspace version's routing with staging."""
+    built_lib()
+    import nvfp4_block_scaled_moe_gb300 as nv
+    from nvfp4_block_scaled_moe_gb300 import pipeline
+
+    spec = inputs.moe_spec(T=700, H=1088, I=256, E=48, top_k=5, seed=45, zipf=True)
+    logits = dev(inputs.moe_logits(spec))
+    x = inputs.moe_x(spec)[0].cuda()
+    ref = _buffers(pipeline, spec)
+    nv.moe_route_permute(logits, x, spec["top_k"], ref.topk_ids, ref.topk_w, ref.counts, ref.offsets,
+                         ref.perm_token, ref.inv_perm, ref.a1_q, ref.a1_sf, ref.workspace)
+    got = _buffers(pipeline, spec)
+    got.a1_sf.copy_(ref.a1_sf)
+    got.a1_sf[:int(host(ref.offsets)[-1]) // 128 * 512 * (spec["H"] // 64)].fill_(0xEE)   # the groups' bands
+    nv.moe_route_permute_static(logits, x, spec["top_k"], got.topk_ids, got.topk_w, got.counts, got.offsets,
+                                got.perm_token, got.inv_perm, None, None)
+    nv.moe_stage_activation(dict(x=x, inv_perm=got.inv_perm, counts=got.counts, offsets=got.offsets,
+                                 a1_q=got.a1_q, a1_sf=got.a1_sf))
+    nv.nvfp4_device_status()
+    R = int(host(ref.offsets)[-1])
+    a, b = _outputs(ref, R), _outputs(got, R)
+    for key in a:
+        if key == "w":
+            assert np.allclose(a[key], b[key], rtol=2e-6, atol=1e-7), key
+        else:
+            assert np.array_equal(a[key], b[key]), key
+
+
 def test_static_scratch_rejects_problems_beyond_its_array():
     built_lib()
     import nvfp4_block_scaled_moe_gb300 as nv
