@@ -311,15 +311,16 @@ nvfp4_status moe_stage_activation(const nvfp4_stage_job* job, nvfp4_stream_t str
  *               overlap this call's.  With the SwiGLU + NVFP4 epilogue on CTA
  *               pairs, two extra warps per CTA stream it while the GEMM runs:
  *               the GEMM moves little DRAM traffic of its own, so the combine's
- *               HBM time mostly hides.  Otherwise it runs as its own launch
- *               first.  Either way y equals moe_combine's bit for bit (the
+ *               HBM time mostly hides.  Otherwise (or when the GEMM has tiles
+ *               for fewer than half the SMs) it runs as its own launch first.  Either way y equals moe_combine's bit for bit (the
  *               same fp32 slot-order sum and one rounding).
  *   side_stage  NULL, or the activation staging of a LATER batch to run
  *               alongside (see nvfp4_stage_job), under the same rules: inputs
  *               complete when this call's work starts, buffers disjoint from
  *               this call's.  With the BF16 epilogue on CTA pairs (the L2
  *               GEMM), two extra warps per CTA run it while the GEMM computes;
- *               otherwise it runs as its own launch first.  Either way the
+ *               otherwise (or with tiles for fewer than half the SMs) it runs
+ *               as its own launch first.  Either way the
  *               bytes equal moe_stage_activation's.
  *   epilogue    NVFP4_EPI_SWIGLU_NVFP4: N columns interleaved 8|8 as gate/up;
  *               h = silu(alpha*g) * (alpha*u) quantised as in nvfp4_quantize ->

@@ -481,9 +481,13 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
                      (mode == NVFP4_GEMM_TILES_AUTO && a.rows_max >= 2 * kBM * groups));
   // side jobs: the combine of an earlier batch runs inside the CTA-pair SwiGLU
   // kernel, the activation staging of a later batch inside the CTA-pair BF16
-  // kernel; a job the chosen kernel does not host runs as its own launch first
-  const bool host_combine = pair && a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 && a.a_gather == nullptr;
-  const bool host_stage = pair && a.epilogue == NVFP4_EPI_BF16 && a.a_gather == nullptr;
+  // kernel; a job the chosen kernel does not host runs as its own launch first,
+  // and so does one whose GEMM has tiles for fewer than half the SMs (the side
+  // warps would then be too few to stream it)
+  const int64_t pair_tiles = ((a.rows_max / kBM + 1) / 2 + (groups > 1 ? groups : 0)) * (a.N / 256);
+  const bool wide = pair_tiles * 2 >= info.sms / 2;
+  const bool host_combine = pair && wide && a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 && a.a_gather == nullptr;
+  const bool host_stage = pair && wide && a.epilogue == NVFP4_EPI_BF16 && a.a_gather == nullptr;
   if ((a.side_T > 0 && !host_combine) || (a.stage.T > 0 && !host_stage)) {
     GemmArgs rest = a;
     if (a.side_T > 0 && !host_combine) {

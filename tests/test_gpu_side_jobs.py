@@ -8,7 +8,9 @@
   nibbles, every scale byte of the groups' 128-row bands), padding nibbles
   are left untouched, with and without the two-level scale;
 * either way the GEMM's own outputs are the bytes it writes without the side
-  job, on both tile kernels, for short and long batches and top-k up to 32;
+  job, on both tile kernels (a GEMM with tiles for fewer than half the SMs
+  runs the job as its own launch, like the single-CTA kernel), for short and
+  long batches and top-k up to 32;
 * the serving pipeline (route(i); L2(i-1) staging batch i; L1(i) combining
   batch i-1; the last batch's L2 and combine at the end) gives every batch the
   y of the plain forward, bit for bit.
@@ -55,7 +57,8 @@ def _swizzled(nv, sf_lin):
 @pytest.mark.parametrize("T,H,k", [(300, 1024, 8), (4100, 512, 4), (33, 7168, 32), (1, 64, 1)])
 def test_side_combine_equals_combine(nv, T, H, k):
     nv, _ = nv
-    sizes, counts, N, K = [512, 384, 256], [500, 300, 256], 512, 768
+    # N = 2048: enough tiles (64) that the pair kernel hosts the job on its own warps
+    sizes, counts, N, K = [512, 384, 256], [500, 300, 256], 2048, 768
     rows_max, G = sum(sizes), len(sizes)
     a_q, a_sf = inputs.random_nvfp4_operand(61, 0, rows_max, K)
     b = [inputs.random_nvfp4_operand(61, 1 + g, N, K) for g in range(G)]
@@ -130,8 +133,9 @@ def test_side_stage_equals_route_staging(nv, T, H, E, k, zipf, two_level):
     job = dict(x=x_d, inv_perm=b.inv_perm, counts=b.counts, offsets=b.offsets, a1_q=b.a1_q, a1_sf=b.a1_sf,
                x_global_scale=gsa)
 
-    # a BF16 grouped GEMM (N % 256 == 0: CTA pairs) to host the job
-    sizes, N, K = [512, 384, 256], 512, 768
+    # a BF16 grouped GEMM to host the job (N % 256 == 0: CTA pairs; 64 tiles, so
+    # the pair kernel runs it on its own warps)
+    sizes, N, K = [512, 384, 256], 2048, 768
     rows_max, G = sum(sizes), len(sizes)
     a_q, a_sf = inputs.random_nvfp4_operand(63, 0, rows_max, K)
     bw = [inputs.random_nvfp4_operand(63, 1 + g, N, K) for g in range(G)]
