@@ -112,6 +112,8 @@ typedef struct {
   int32_t top_k;               /* 1 .. 32 */
   int32_t H;                   /* row length, a positive multiple of 8 */
   void* y_bf16;                /* BF16 [T, H], written (16-byte aligned) */
+  int64_t rows;                /* rows of rows_bf16 (>= 1): a slot whose inv_perm entry lies outside
+                                  [0, rows) reads nothing, adds 0 and sets the device error word */
 } nvfp4_combine_job;
 
 /* The activation staging of a routed batch (moe_route_permute's second half,
@@ -133,6 +135,9 @@ typedef struct {
   int32_t H;                       /* a positive multiple of 64 */
   int32_t E;                       /* 1 .. 1024 */
   int32_t top_k;                   /* 1 .. min(E, 32) */
+  int64_t rows_max;                /* rows of a1_q (R_max, a positive multiple of 128): a row index, or an
+                                      expert's last band, outside it is not written and sets the
+                                      device error word */
 } nvfp4_stage_job;
 
 /* Two-level scale.  The pages' pipeline carries a per-tensor fp32 global scale

@@ -57,14 +57,14 @@ class _MoeWeightsC(ctypes.Structure):
 class _CombineJobC(ctypes.Structure):
     """nvfp4_combine_job (include/nvfp4moe.h)."""
     _fields_ = [("rows_bf16", _vp), ("inv_perm", _vp), ("topk_w", _vp), ("T", _i32), ("top_k", _i32),
-                ("H", _i32), ("y_bf16", _vp)]
+                ("H", _i32), ("y_bf16", _vp), ("rows", _i64)]
 
 
 class _StageJobC(ctypes.Structure):
     """nvfp4_stage_job (include/nvfp4moe.h)."""
     _fields_ = [("x_bf16", _vp), ("x_global_scale", _vp), ("inv_perm", _vp), ("expert_counts", _vp),
                 ("expert_offsets", _vp), ("a1_q", _vp), ("a1_sf", _vp), ("T", _i32), ("H", _i32), ("E", _i32),
-                ("top_k", _i32)]
+                ("top_k", _i32), ("rows_max", _i64)]
 
 
 class _MoeBuffersC(ctypes.Structure):
@@ -203,19 +203,20 @@ def _combine_job(job):
         return None
     rows, inv, w, y = job
     return ctypes.byref(_CombineJobC(rows.data_ptr(), inv.data_ptr(), w.data_ptr(), inv.shape[0], inv.shape[1],
-                                     y.shape[1], y.data_ptr()))
+                                     y.shape[1], y.data_ptr(), rows.shape[0]))
 
 
 def _stage_job(job):
-    """dict(x, inv_perm, counts, offsets, a1_q, a1_sf[, x_global_scale]) of
-    device tensors -> a pointer to nvfp4_stage_job (None -> NULL)."""
+    """dict(x, inv_perm, counts, offsets, a1_q, a1_sf[, x_global_scale, rows_max])
+    of device tensors -> a pointer to nvfp4_stage_job (None -> NULL); rows_max
+    defaults to a1_q's rows."""
     if job is None:
         return None
     x, inv = job["x"], job["inv_perm"]
     return ctypes.byref(_StageJobC(x.data_ptr(), _p(job.get("x_global_scale")), inv.data_ptr(),
                                    job["counts"].data_ptr(), job["offsets"].data_ptr(), job["a1_q"].data_ptr(),
                                    job["a1_sf"].data_ptr(), x.shape[0], x.shape[1], job["counts"].shape[0],
-                                   inv.shape[1]))
+                                   inv.shape[1], job.get("rows_max", job["a1_q"].shape[0])))
 
 
 def moe_stage_activation(job, stream=None):

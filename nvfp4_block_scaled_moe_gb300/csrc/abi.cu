@@ -241,6 +241,7 @@ nvfp4_status check_combine_job(const nvfp4_combine_job* c) {
   CHECK_ARG(c->T >= 0 && c->top_k >= 1 && c->top_k <= 32, "combine job: T=%d top_k=%d", c->T, c->top_k);
   if (c->T == 0) return NVFP4_OK;
   CHECK_ARG(c->rows_bf16 && c->inv_perm && c->topk_w && c->y_bf16, "combine job: null pointer");
+  CHECK_ARG(c->rows >= 1, "combine job: rows=%lld", (long long)c->rows);
   CHECK_SUP(c->H > 0 && c->H % 8 == 0, "combine job: H=%d is not a positive multiple of 8", c->H);
   CHECK_AL(al16(c->rows_bf16) && al16(c->y_bf16), "combine job: rows and y must be 16-byte aligned");
   return NVFP4_OK;
@@ -257,6 +258,8 @@ nvfp4_status check_stage_job(const nvfp4_stage_job* j) {
   CHECK_SUP(j->top_k >= 1 && j->top_k <= j->E && j->top_k <= 32, "stage job: top_k=%d outside [1, min(E, 32)]",
             j->top_k);
   CHECK_SUP(j->H > 0 && j->H % 64 == 0, "stage job: H=%d is not a positive multiple of 64", j->H);
+  CHECK_SUP(j->rows_max > 0 && j->rows_max % 128 == 0 && j->rows_max < (int64_t(1) << 31),
+            "stage job: rows_max=%lld is not a positive multiple of 128", (long long)j->rows_max);
   CHECK_AL(al16(j->x_bf16) && al16(j->a1_q) && al16(j->a1_sf), "stage job: x, a1_q and a1_sf must be 16-byte aligned");
   CHECK_AL(al4(j->x_global_scale), "stage job: x_global_scale not 4-byte aligned");
   return NVFP4_OK;
@@ -276,6 +279,8 @@ StageJob stage_job(const nvfp4_stage_job& j) {
   s.H = j.H;
   s.E = j.E;
   s.k = j.top_k;
+  s.rows_max = j.rows_max;
+  s.err = device_error_word();
   return s;
 }
 
@@ -333,6 +338,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sf, int64_t
                               h_debug, a_gather, a_gather_rows);
   if (side_combine != nullptr && side_combine->T > 0) {
     a.side_rows = side_combine->rows_bf16;
+    a.side_n_rows = side_combine->rows;
     a.side_inv = side_combine->inv_perm;
     a.side_w = side_combine->topk_w;
     a.side_y = side_combine->y_bf16;
@@ -383,7 +389,8 @@ nvfp4_status moe_combine(const void* rows_bf16, const int32_t* inv_perm, const f
   CHECK_SUP(H > 0 && H % 8 == 0, "moe_combine: H=%d is not a positive multiple of 8", H);
   CHECK_AL(T == 0 || (al16(rows_bf16) && al16(y_bf16)), "moe_combine: rows and y must be 16-byte aligned");
   CHECK_AL(al16(shared_bf16), "moe_combine: shared rows must be 16-byte aligned");
-  cudaError_t e = combine_launch(rows_bf16, inv_perm, topk_w, T, H, top_k, shared_bf16, y_bf16,
+  // rows_bf16's row count is not an argument: only negative rows are caught
+  cudaError_t e = combine_launch(rows_bf16, INT64_MAX, inv_perm, topk_w, T, H, top_k, shared_bf16, y_bf16,
                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : fail_cuda(e, "moe_combine");
 }
@@ -510,6 +517,7 @@ nvfp4_status nvfp4_moe_step_host(const void* x_host, const float* logits_host, i
     stage.H = H;
     stage.E = E;
     stage.top_k = top_k;
+    stage.rows_max = b->rows_max;
     nvfp4_combine_job comb = {};
     comb.rows_bf16 = prev->rows_bf16;
     comb.inv_perm = prev->inv_perm;
@@ -518,6 +526,7 @@ nvfp4_status nvfp4_moe_step_host(const void* x_host, const float* logits_host, i
     comb.top_k = top_k;
     comb.H = H;
     comb.y_bf16 = prev->y_bf16;
+    comb.rows = prev->rows_max;
     st = enqueue_route(T, H, E, top_k, b, false, stream);
     if (st == NVFP4_OK) st = enqueue_l2(H, I, E, w, prev, &stage, stream);
     if (st == NVFP4_OK) st = enqueue_l1(H, I, E, w, b, &comb, stream);

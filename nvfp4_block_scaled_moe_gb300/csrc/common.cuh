@@ -209,12 +209,13 @@ __device__ __forceinline__ void swiglu_bf16_row(const float (&v)[4][32], float a
 // FMA in slot order starting from 0, one rounding to BF16) over the 8-column
 // chunks c0 + 32 i (i < kNC, those below `chunks`) of the row.  Every slot's
 // 16-byte loads are issued before the FMAs use them (8 kNC per lane in flight),
-// which is what lets a few warps stream the rows at HBM rate.
+// which is what lets a few warps stream the rows at HBM rate.  A slot whose row
+// lies outside [0, n_rows) loads nothing, adds 0 and sets kErrBounds.
 template <int kNC>
-__device__ __forceinline__ void combine_chunks(const __nv_bfloat16* __restrict__ rows,
+__device__ __forceinline__ void combine_chunks(const __nv_bfloat16* __restrict__ rows, int64_t n_rows,
                                                const int32_t* __restrict__ inv_perm, const float* __restrict__ w,
                                                int32_t H, int32_t k, int64_t t, int c0, int chunks,
-                                               __nv_bfloat16* __restrict__ y) {
+                                               __nv_bfloat16* __restrict__ y, unsigned* err) {
   float acc[kNC][8];
 #pragma unroll
   for (int n = 0; n < kNC; ++n)
@@ -228,10 +229,12 @@ __device__ __forceinline__ void combine_chunks(const __nv_bfloat16* __restrict__
       if (j0 + q < k) {
         const int64_t r = __ldg(inv_perm + t * k + j0 + q);
         wj[q] = __ldg(w + t * k + j0 + q);
-        const uint4* src = reinterpret_cast<const uint4*>(rows + r * H);
+        const bool in = r >= 0 && r < n_rows;
+        if (!in) raise_error(err, kErrBounds);
+        const uint4* src = reinterpret_cast<const uint4*>(rows + (in ? r : 0) * H);
 #pragma unroll
         for (int n = 0; n < kNC; ++n)
-          v[q][n] = c0 + 32 * n < chunks ? __ldg(src + c0 + 32 * n) : make_uint4(0, 0, 0, 0);
+          v[q][n] = in && c0 + 32 * n < chunks ? __ldg(src + c0 + 32 * n) : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll

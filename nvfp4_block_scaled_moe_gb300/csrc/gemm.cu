@@ -491,7 +491,8 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   if ((a.side_T > 0 && !host_combine) || (a.stage.T > 0 && !host_stage)) {
     GemmArgs rest = a;
     if (a.side_T > 0 && !host_combine) {
-      e = combine_launch(a.side_rows, a.side_inv, a.side_w, a.side_T, a.side_H, a.side_k, nullptr, a.side_y, stream);
+      e = combine_launch(a.side_rows, a.side_n_rows, a.side_inv, a.side_w, a.side_T, a.side_H, a.side_k, nullptr,
+                         a.side_y, stream);
       if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm: combine of the earlier batch");
       rest.side_T = 0;
     }

@@ -117,6 +117,7 @@ struct PairParams {
   // kSideCombine, the combine of an earlier batch (side_T == 0: none);
   // kSideStage, the activation staging of a later batch
   const __nv_bfloat16* side_rows;
+  int64_t side_n_rows;
   const int32_t* side_inv;
   const float* side_w;
   __nv_bfloat16* side_y;
@@ -449,7 +450,8 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
       const int chunks = p.side_H / 8;
       for (int64_t t = sw; t < p.side_T; t += n_sw)
         for (int c0 = lane; c0 < chunks; c0 += 32 * 3)
-          combine_chunks<3>(p.side_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t, c0, chunks, p.side_y);
+          combine_chunks<3>(p.side_rows, p.side_n_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t, c0, chunks,
+                            p.side_y, p.err);
     } else {
       // the padding scales of expert e (one warp per expert), then the
       // segments: side warp sw takes items sw + n_sw (kStageSegs i + n)
@@ -693,6 +695,7 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   const bool side = a.side_T > 0;
   const bool stage = a.stage.T > 0;
   p.side_rows = static_cast<const __nv_bfloat16*>(a.side_rows);
+  p.side_n_rows = a.side_n_rows;
   p.side_inv = a.side_inv;
   p.side_w = a.side_w;
   p.side_y = static_cast<__nv_bfloat16*>(a.side_y);

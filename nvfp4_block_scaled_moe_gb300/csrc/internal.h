@@ -64,12 +64,15 @@ struct StageJob {
   uint8_t* a_sf;              // their swizzled scales
   uint8_t* x_q;               // token-order rows of x (null: not written)
   int32_t T, H, E, k;
+  int64_t rows_max;           // rows of a_q / a_sf: rows outside are not written (error word)
+  unsigned* err;              // the device error word
 };
 
 cudaError_t stage_launch(const StageJob& s, cudaStream_t stream);
 
-cudaError_t combine_launch(const void* rows, const int32_t* inv_perm, const float* w, int32_t T, int32_t H,
-                           int32_t top_k, const void* shared, void* y, cudaStream_t stream);
+// n_rows: rows of `rows`; a slot outside [0, n_rows) adds 0 and sets the error word
+cudaError_t combine_launch(const void* rows, int64_t n_rows, const int32_t* inv_perm, const float* w, int32_t T,
+                           int32_t H, int32_t top_k, const void* shared, void* y, cudaStream_t stream);
 
 struct GemmArgs {
   const uint8_t* a_q;
@@ -94,6 +97,7 @@ struct GemmArgs {
   // side job of the CTA-pair SwiGLU kernel: the combine of an earlier batch
   // (moe_combine without shared rows); side_T == 0: none
   const void* side_rows = nullptr;
+  int64_t side_n_rows = 0;    // rows of side_rows (index check)
   const int32_t* side_inv = nullptr;
   const float* side_w = nullptr;
   void* side_y = nullptr;

@@ -364,6 +364,8 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
       s.H = b.H;
       s.E = b.E;
       s.k = b.top_k;
+      s.rows_max = b.rows_max;
+      s.err = device_error_word();
       return stage_launch(s, stream);
     }
   }
@@ -375,12 +377,13 @@ cudaError_t route_permute_launch(const RouteBuffers& b, cudaStream_t stream) {
 // (s + gridDim.y)*blockDim + thread, ...; each thread accumulates its 8 columns
 // over the k slots in slot order (fp32 FMA), then the token's shared-expert row
 // if there is one, and rounds once to BF16.  Short batches split a token's row
-// over several blocks so that enough loads are in flight.
-__global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ rows,
+// over several blocks so that enough loads are in flight.  A slot whose row lies
+// outside [0, n_rows) loads nothing, adds 0 and sets kErrBounds.
+__global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ rows, int64_t n_rows,
                                                       const int32_t* __restrict__ inv_perm,
                                                       const float* __restrict__ w, int32_t H, int32_t k,
                                                       const __nv_bfloat16* __restrict__ shared,
-                                                      __nv_bfloat16* __restrict__ y) {
+                                                      __nv_bfloat16* __restrict__ y, unsigned* err) {
   const int64_t t = blockIdx.x;
   const int n8 = H / 8;
   for (int c = blockIdx.y * blockDim.x + threadIdx.x; c < n8; c += gridDim.y * blockDim.x) {
@@ -390,6 +393,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
     for (int j = 0; j < k; ++j) {
       const int64_t r = __ldg(inv_perm + t * k + j);
       const float wj = __ldg(w + t * k + j);
+      if (r < 0 || r >= n_rows) {
+        raise_error(err, kErrBounds);
+        continue;
+      }
       float v[8];
       bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(rows + r * H) + c), v);
 #pragma unroll
@@ -410,14 +417,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
   }
 }
 
-cudaError_t combine_launch(const void* rows, const int32_t* inv_perm, const float* w, int32_t T, int32_t H,
-                           int32_t top_k, const void* shared, void* y, cudaStream_t stream) {
+cudaError_t combine_launch(const void* rows, int64_t n_rows, const int32_t* inv_perm, const float* w, int32_t T,
+                           int32_t H, int32_t top_k, const void* shared, void* y, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   // a token's row over up to ceil(H / 1024) blocks of 128 threads while the batch
   // has fewer than 4096 tokens (one 16-byte chunk per thread)
   const int split = T < 4096 ? (H / 8 + 127) / 128 : 1;
-  combine_kernel<<<dim3(T, split), 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(rows), inv_perm, w, H, top_k,
-                                        static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(y));
+  combine_kernel<<<dim3(T, split), 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(rows), n_rows, inv_perm, w, H,
+                                                     top_k, static_cast<const __nv_bfloat16*>(shared),
+                                                     static_cast<__nv_bfloat16*>(y), device_error_word());
   return cudaGetLastError();
 }
 

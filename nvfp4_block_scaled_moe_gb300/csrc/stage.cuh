@@ -34,6 +34,10 @@ __device__ __forceinline__ void stage_padding(const StageJob& s, int e, int64_t 
   const int64_t hi = __ldg(s.offsets + e + 1);
   if (hi <= lo) return;
   const int64_t band = (hi - 1) >> 7;
+  if (hi > s.rows_max) {                                      // the group's band lies past a_sf
+    if (first == 0) raise_error(s.err, kErrBounds);
+    return;
+  }
   const int first_pad = static_cast<int>(lo - band * 128);    // band-relative first padding row (1..127)
   const int k4_total = s.H / 64;
   const int64_t items = static_cast<int64_t>(k4_total) * 32;
@@ -57,6 +61,8 @@ __device__ __forceinline__ void stage_padding(const StageJob& s, int e, int64_t 
 // is used, so a warp keeps kNS x 2 KiB of reads in flight and never waits on
 // one index load per row.  The caller's whole warp takes part (the scale words
 // are paired, the row indices broadcast, by shuffle); item[] is warp-uniform.
+// A row index outside [0, rows_max) is not written and sets kErrBounds (the x_q
+// row, which needs no index, still is).
 template <int kNS>
 __device__ __forceinline__ void stage_segments(const StageJob& s, const int64_t (&item)[kNS], int lane) {
   const int64_t segs = (s.H + 1023) / 1024;
@@ -117,6 +123,10 @@ __device__ __forceinline__ void stage_segments(const StageJob& s, const int64_t 
     if (active && s.x_q != nullptr) *reinterpret_cast<uint4*>(s.x_q + t * (s.H / 2) + c0[n] / 2) = nib;
     for (int j = 0; j < s.k; ++j) {
       const int64_t r = __shfl_sync(0xFFFFFFFFu, rows[n], j);
+      if (r < 0 || r >= s.rows_max) {                        // warp-uniform: not written
+        if (lane == 0) raise_error(s.err, kErrBounds);
+        continue;
+      }
       if (active) {
         if (s.a_q != nullptr) *reinterpret_cast<uint4*>(s.a_q + r * (s.H / 2) + c0[n] / 2) = nib;
         if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(s.a_sf + sf_word_offset(r, k4, k4_total)) = word;

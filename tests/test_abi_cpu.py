@@ -56,14 +56,14 @@ def test_size_helpers(lib):
     assert lib.moe_route_permute_workspace(16384, 7168, 256, 8) >= 128 * 256 * 4
 
 
-def nvb_job(rows, inv, w, T, k, H, y):
+def nvb_job(rows, inv, w, T, k, H, y, n_rows=1024):
     import nvfp4_block_scaled_moe_gb300 as nvb
-    return nvb._CombineJobC(rows, inv, w, T, k, H, y)
+    return nvb._CombineJobC(rows, inv, w, T, k, H, y, n_rows)
 
 
-def nvb_stage(x, gs, inv, counts, offsets, a1_q, a1_sf, T, H, E, k):
+def nvb_stage(x, gs, inv, counts, offsets, a1_q, a1_sf, T, H, E, k, rows_max=1024):
     import nvfp4_block_scaled_moe_gb300 as nvb
-    return nvb._StageJobC(x, gs, inv, counts, offsets, a1_q, a1_sf, T, H, E, k)
+    return nvb._StageJobC(x, gs, inv, counts, offsets, a1_q, a1_sf, T, H, E, k, rows_max)
 
 
 @needs_nvcc
@@ -120,14 +120,16 @@ def test_host_validation_without_gpu(lib):
     job_null = nvb_job(base, None, base, 4, 2, 512, base)
     job_odd_y = nvb_job(base, base, base, 4, 2, 512, base + 8)
     job_odd_h = nvb_job(base, base, base, 4, 2, 500, base)
-    for job, st in ((job_bad_k, 1), (job_null, 1), (job_odd_y, 3), (job_odd_h, 2)):
+    job_no_rows = nvb_job(base, base, base, 4, 2, 512, base, 0)
+    for job, st in ((job_bad_k, 1), (job_null, 1), (job_odd_y, 3), (job_odd_h, 2), (job_no_rows, 1)):
         assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 0, p, p,
                                       None, None, None, 0, ctypes.byref(job), None, None) == st
     # a side staging job: its own checks, before anything is launched
-    def stage(x=base, inv=base, cnt=base, off=base, q=base, sf=base, T=4, H=512, E=8, k=2):
-        return nvb_stage(x, None, inv, cnt, off, q, sf, T, H, E, k)
+    def stage(x=base, inv=base, cnt=base, off=base, q=base, sf=base, T=4, H=512, E=8, k=2, rows_max=1024):
+        return nvb_stage(x, None, inv, cnt, off, q, sf, T, H, E, k, rows_max)
     for job, st in ((stage(inv=None), 1), (stage(sf=None), 1), (stage(E=2000), 2), (stage(k=9), 2),
-                    (stage(k=40, E=64), 2), (stage(H=96), 2), (stage(x=base + 8), 3), (stage(q=base + 4), 3)):
+                    (stage(k=40, E=64), 2), (stage(H=96), 2), (stage(x=base + 8), 3), (stage(q=base + 4), 3),
+                    (stage(rows_max=0), 2), (stage(rows_max=200), 2)):
         assert lib.nvfp4_grouped_gemm(p, p, 128, None, None, 1, 256, 256, p, p, 1.0, None, None, None, 1, None, None,
                                       p, None, None, 0, None, ctypes.byref(job), None) == st
         assert lib.moe_stage_activation(ctypes.byref(job), None) == st

@@ -201,3 +201,61 @@ def test_pipelined_forward_equals_plain(nv):
     w1, w2 = inputs.moe_all_weights(spec)
     ref = omoe.moe_ffn(x, logits, w1, w2, spec["top_k"])["y"]
     assert rel_frobenius(ys[0].float().cpu().numpy(), ref) <= 2e-2
+
+
+def test_side_jobs_check_their_row_indices(nv):
+    """A staging job whose rows_max is below the routed rows writes nothing past
+    it and reports a device index error; so does a side combine whose row count
+    is below an inv_perm entry (those slots add nothing).  The buffers behind
+    both jobs are full size, so the checks, not the memory, are what is tested."""
+    nv, pipeline = nv
+    spec = inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=64, zipf=True)
+    s = pipeline.MoeShape(T=300, H=512, I=256, E=8, top_k=2)
+    x_d, lg = inputs.moe_x(spec)[0].cuda(), dev(inputs.moe_logits(spec))
+    ref, b = pipeline.MoeBuffers(s), pipeline.MoeBuffers(s)
+    nv.moe_route_permute(lg, x_d, 2, ref.topk_ids, ref.topk_w, ref.counts, ref.offsets, ref.perm_token,
+                         ref.inv_perm, ref.a1_q, ref.a1_sf, ref.workspace)
+    nv.moe_route_permute(lg, x_d, 2, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token, b.inv_perm,
+                         None, None, b.workspace)
+    nv.nvfp4_device_status()
+    R = int(host(ref.offsets)[-1])
+    assert R > 256
+    b.a1_q.fill_(0x5A)
+    nv.moe_stage_activation(dict(x=x_d, inv_perm=b.inv_perm, counts=b.counts, offsets=b.offsets, a1_q=b.a1_q,
+                                 a1_sf=b.a1_sf, rows_max=256))
+    with pytest.raises(nv.Nvfp4Error) as ei:
+        nv.nvfp4_device_status()
+    assert ei.value.status == 6                                    # NVFP4_ERR_DEVICE
+    perm = host(ref.perm_token)[:R]
+    real = perm >= 0
+    got = host(b.a1_q)
+    lo = real & (np.arange(R) < 256)
+    assert np.array_equal(got[:R][lo], host(ref.a1_q)[:R][lo])    # rows below rows_max staged
+    assert np.all(got[256:] == 0x5A)                               # nothing past it
+    nv.nvfp4_device_status()                                       # the word was cleared
+
+    # a side combine told rows_bf16 has fewer rows (a view of the full rows) than
+    # some tokens' slots reach: inside the CTA-pair SwiGLU GEMM (64 tiles) and as
+    # its own launch (single CTAs)
+    rows = torch.randn((R, 512), device="cuda").to(torch.bfloat16)
+    y_full = torch.empty((300, 512), dtype=torch.bfloat16, device="cuda")
+    nv.moe_combine(rows, ref.inv_perm, ref.topk_w, y_full)
+    a_q, a_sf = inputs.random_nvfp4_operand(65, 0, 2048, 256)
+    bq, bsf = inputs.random_nvfp4_operand(65, 1, 2048, 256)
+    a_q_d, a_sf_d, bq_d, bsf_d = dev(a_q), _swizzled(nv, a_sf), dev(bq), _swizzled(nv, bsf)
+    inv = host(ref.inv_perm)
+    n_rows = int(np.median(inv.max(axis=1)))
+    ok = torch.from_numpy(inv.max(axis=1) < n_rows).cuda()
+    assert ok.any() and not ok.all()
+    for mode in (nv.GEMM_TILES_PAIR, nv.GEMM_TILES_SINGLE):
+        y = torch.zeros_like(y_full)
+        oq = torch.empty((2048, 512), dtype=torch.uint8, device="cuda")
+        osf = torch.empty(nv.sf_bytes(2048, 1024), dtype=torch.uint8, device="cuda")
+        with _tiles(nv, mode):
+            nv.nvfp4_grouped_gemm(a_q_d, a_sf_d, 2048, None, None, 1, 2048, 256, bq_d, bsf_d, 1.0,
+                                  nv.EPI_SWIGLU_NVFP4, out_q=oq, out_sf=osf,
+                                  side_combine=(rows[:n_rows], ref.inv_perm, ref.topk_w, y))
+        with pytest.raises(nv.Nvfp4Error) as ei:
+            nv.nvfp4_device_status()
+        assert ei.value.status == 6, mode
+        assert torch.equal(y[ok], y_full[ok]), mode
