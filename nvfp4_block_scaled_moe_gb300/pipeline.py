@@ -208,6 +208,8 @@ def moe_forward_deferred(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b
     alternates two buffer sets.  One-level scales, alpha 1, no shared expert,
     no gathered L1."""
     s = b.shape
+    if prev is b:
+        raise ValueError("prev must be another buffer set: this batch's staging runs beside prev's L2 GEMM")
     if b.gather or (prev is not None and prev.gather):
         raise ValueError("the deferred serving step stages permuted rows (no gathered L1)")
     live_prev = prev is not None and prev.shape.T > 0
