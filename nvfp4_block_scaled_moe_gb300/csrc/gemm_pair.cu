@@ -48,7 +48,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSideWarps = 2;                          // the side job's warps (kSide instantiations)
 constexpr int kSideNone = 0, kSideCombine = 1, kSideStage = 2;
-constexpr int kStageSegs = 4;                          // staging segments a side warp has in flight
+constexpr int kStageSegs = 2;                          // staging segments per batch (two batches in flight)
 constexpr int kThreadsSide = kThreads + 32 * kSideWarps;
 constexpr int kMaxGroups = kPairMaxGroups;             // larger G uses the single-CTA kernel
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
@@ -454,14 +454,23 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
                             p.side_y, p.err);
     } else {
       // the padding scales of expert e (one warp per expert), then the
-      // segments: side warp sw takes items sw + n_sw (kStageSegs i + n)
+      // segments: side warp sw takes items sw + n_sw (kStageSegs i + n), the
+      // loads of each batch issued before the previous batch is quantised and
+      // written (two batches in registers)
       for (int e = static_cast<int>(sw); e < p.stage.E; e += static_cast<int>(n_sw)) stage_padding(p.stage, e, lane, 32);
       const int64_t n_items = static_cast<int64_t>(p.stage.T) * ((p.stage.H + 1023) / 1024);
-      for (int64_t i = sw; i < n_items; i += kStageSegs * n_sw) {
-        int64_t item[kStageSegs];
+      StageBatch<kStageSegs> cur, nxt;
+      auto items = [&](StageBatch<kStageSegs>& b, int64_t i) {
 #pragma unroll
-        for (int n = 0; n < kStageSegs; ++n) item[n] = i + n * n_sw < n_items ? i + n * n_sw : -1;
-        stage_segments<kStageSegs>(p.stage, item, lane);
+        for (int n = 0; n < kStageSegs; ++n) b.item[n] = i + n * n_sw < n_items ? i + n * n_sw : -1;
+      };
+      items(cur, sw);
+      stage_load(p.stage, cur, lane);
+      for (int64_t i = sw; i < n_items; i += kStageSegs * n_sw) {
+        items(nxt, i + kStageSegs * n_sw);
+        stage_load(p.stage, nxt, lane);
+        stage_store(p.stage, cur, lane);
+        cur = nxt;
       }
     }
   } else {

@@ -323,8 +323,10 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const StageJob s) {
   const int64_t seg = static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (seg >= segs) return;
   const int64_t t = static_cast<int64_t>(blockIdx.x) - static_cast<int64_t>(kPadParts) * s.E;
-  const int64_t item[1] = {t * segs + seg};
-  stage_segments<1>(s, item, threadIdx.x & 31);
+  StageBatch<1> b;
+  b.item[0] = t * segs + seg;
+  stage_load(s, b, threadIdx.x & 31);
+  stage_store(s, b, threadIdx.x & 31);
 }
 
 cudaError_t stage_launch(const StageJob& s, cudaStream_t stream) {

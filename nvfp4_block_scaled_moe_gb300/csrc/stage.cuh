@@ -55,48 +55,58 @@ __device__ __forceinline__ void stage_padding(const StageJob& s, int e, int64_t 
   }
 }
 
-// One warp stages the segments item[0..kNS) (item = token * segs + segment,
-// segs = ceil(H / 1024); item < 0: none).  Every segment's x loads, and its
-// token's k row indices (lane j loads slot j; k <= 32), are issued before any
-// is used, so a warp keeps kNS x 2 KiB of reads in flight and never waits on
-// one index load per row.  The caller's whole warp takes part (the scale words
-// are paired, the row indices broadcast, by shuffle); item[] is warp-uniform.
-// A row index outside [0, rows_max) is not written and sets kErrBounds (the x_q
-// row, which needs no index, still is).
+// One warp's batch of segments item[0..kNS) (item = token * segs + segment,
+// segs = ceil(H / 1024); item < 0: none) with its loads: each segment's x
+// (2 KiB) and its token's k row indices (lane j loads slot j; k <= 32, broadcast
+// later by shuffle), so a warp never waits on one index load per row.
 template <int kNS>
-__device__ __forceinline__ void stage_segments(const StageJob& s, const int64_t (&item)[kNS], int lane) {
+struct StageBatch {
+  int64_t item[kNS];
+  int64_t tok[kNS];
+  int64_t c0[kNS];          // this lane's first column; >= H: inactive lane or no item
+  int32_t rows[kNS];
+  uint4 raw[kNS][4];
+};
+
+// Issue the batch's loads (item[] set by the caller, warp-uniform).
+template <int kNS>
+__device__ __forceinline__ void stage_load(const StageJob& s, StageBatch<kNS>& b, int lane) {
   const int64_t segs = (s.H + 1023) / 1024;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(s.x);
-  uint4 raw[kNS][4];
-  int64_t tok[kNS];
-  int64_t c0[kNS];
-  int32_t rows[kNS];
 #pragma unroll
   for (int n = 0; n < kNS; ++n) {
-    tok[n] = item[n] >= 0 ? item[n] / segs : 0;
-    c0[n] = item[n] >= 0 ? (item[n] - tok[n] * segs) * 1024 + lane * 32 : s.H;
-    rows[n] = item[n] >= 0 && lane < s.k ? __ldg(s.inv_perm + tok[n] * s.k + lane) : 0;
-    if (c0[n] < s.H) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + tok[n] * s.H + c0[n]);
+    b.tok[n] = b.item[n] >= 0 ? b.item[n] / segs : 0;
+    b.c0[n] = b.item[n] >= 0 ? (b.item[n] - b.tok[n] * segs) * 1024 + lane * 32 : s.H;
+    b.rows[n] = b.item[n] >= 0 && lane < s.k ? __ldg(s.inv_perm + b.tok[n] * s.k + lane) : 0;
+    if (b.c0[n] < s.H) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + b.tok[n] * s.H + b.c0[n]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) raw[n][i] = __ldg(src + i);
+      for (int i = 0; i < 4; ++i) b.raw[n][i] = __ldg(src + i);
     }
   }
+}
+
+// Quantise the batch's segments and write them into their k rows.  The whole
+// warp takes part (the scale words are paired, the row indices broadcast, by
+// shuffle).  A row index outside [0, rows_max) is not written and sets
+// kErrBounds (the x_q row, which needs no index, still is).
+template <int kNS>
+__device__ __forceinline__ void stage_store(const StageJob& s, const StageBatch<kNS>& b, int lane) {
   const float g = s.x_gscale != nullptr ? __ldg(s.x_gscale) : 1.0f;
   const uint32_t k4_total = static_cast<uint32_t>(s.H / 64);
 #pragma unroll
   for (int n = 0; n < kNS; ++n) {
-    if (item[n] < 0) continue;               // warp-uniform
-    const bool active = c0[n] < s.H;
+    if (b.item[n] < 0) continue;             // warp-uniform
+    const bool active = b.c0[n] < s.H;
     uint4 nib = make_uint4(0, 0, 0, 0);
     uint32_t codes = 0;
     if (active) {
       uint32_t w[4];
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {          // two 16-blocks of 16 values
+      for (int q = 0; q < 2; ++q) {          // two 16-blocks of 16 values
         float lo[8], hi[8];
-        bf16x8_to_f32(raw[n][2 * b], lo);
-        bf16x8_to_f32(raw[n][2 * b + 1], hi);
+        bf16x8_to_f32(b.raw[n][2 * q], lo);
+        bf16x8_to_f32(b.raw[n][2 * q + 1], hi);
         if (s.x_gscale != nullptr) {         // two-level scale: quantise fp32(x * g)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -108,27 +118,27 @@ __device__ __forceinline__ void stage_segments(const StageJob& s, const int64_t 
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
         const BlockScale bs = block_scale(amax);
-        w[2 * b] = quantize8(lo, bs);
-        w[2 * b + 1] = quantize8(hi, bs);
-        codes |= bs.code << (8 * b);
+        w[2 * q] = quantize8(lo, bs);
+        w[2 * q + 1] = quantize8(hi, bs);
+        codes |= bs.code << (8 * q);
       }
       nib = make_uint4(w[0], w[1], w[2], w[3]);
     }
     // lanes 2m, 2m+1 own one 64-column group: codes of its four blocks in order
     const uint32_t word = codes | (__shfl_down_sync(0xFFFFFFFFu, codes, 1) << 16);
-    const uint32_t k4 = static_cast<uint32_t>(c0[n] / 64);
-    const int64_t t = tok[n];
+    const uint32_t k4 = static_cast<uint32_t>(b.c0[n] / 64);
+    const int64_t t = b.tok[n];
     // token-order rows (read by a gathering L1) and / or the permuted copies; the
     // scale words always go to the permuted, padded layout
-    if (active && s.x_q != nullptr) *reinterpret_cast<uint4*>(s.x_q + t * (s.H / 2) + c0[n] / 2) = nib;
+    if (active && s.x_q != nullptr) *reinterpret_cast<uint4*>(s.x_q + t * (s.H / 2) + b.c0[n] / 2) = nib;
     for (int j = 0; j < s.k; ++j) {
-      const int64_t r = __shfl_sync(0xFFFFFFFFu, rows[n], j);
+      const int64_t r = __shfl_sync(0xFFFFFFFFu, b.rows[n], j);
       if (r < 0 || r >= s.rows_max) {                        // warp-uniform: not written
         if (lane == 0) raise_error(s.err, kErrBounds);
         continue;
       }
       if (active) {
-        if (s.a_q != nullptr) *reinterpret_cast<uint4*>(s.a_q + r * (s.H / 2) + c0[n] / 2) = nib;
+        if (s.a_q != nullptr) *reinterpret_cast<uint4*>(s.a_q + r * (s.H / 2) + b.c0[n] / 2) = nib;
         if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(s.a_sf + sf_word_offset(r, k4, k4_total)) = word;
       }
     }
