@@ -426,6 +426,12 @@ __device__ __forceinline__ int4 gather_rows4(const int32_t* index, int64_t block
 }
 
 // Contiguous global -> shared copy; both addresses 16-byte aligned, bytes % 16 == 0.
+// Asynchronous prefetch of `bytes` (a multiple of 16, from a 16-byte aligned
+// address of valid global memory) into L2; nothing is written or waited for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

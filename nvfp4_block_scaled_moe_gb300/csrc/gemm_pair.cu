@@ -447,11 +447,44 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
     const int64_t sw = static_cast<int64_t>(blockIdx.x) * kSideWarps + (warp - 2 - kEpiWarps);
     const int64_t n_sw = static_cast<int64_t>(gridDim.x) * kSideWarps;
     if constexpr (kSide == kSideCombine) {
+      // groups of 96 8-column chunks (three per lane) of token t, tokens dealt
+      // in turn; before a group is combined, lanes q < k prefetch a later
+      // group's 1.5 KiB of slot q's row into L2 (one bulk prefetch each), so
+      // that the group's loads, the warp's only way to keep bytes in flight,
+      // meet L2 rather than HBM
+      constexpr int kGroup = 32 * 3;
       const int chunks = p.side_H / 8;
-      for (int64_t t = sw; t < p.side_T; t += n_sw)
-        for (int c0 = lane; c0 < chunks; c0 += 32 * 3)
-          combine_chunks<3>(p.side_rows, p.side_n_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t, c0, chunks,
-                            p.side_y, p.err);
+      const int groups = (chunks + kGroup - 1) / kGroup;
+      auto prefetch = [&](int64_t t, int g) {
+        if (t >= p.side_T || lane >= p.side_k) return;
+        const int64_t r = __ldg(p.side_inv + t * p.side_k + lane);
+        if (r < 0 || r >= p.side_n_rows) return;             // combine_chunks reports it
+        const int c = g * kGroup;
+        const int n = chunks - c < kGroup ? chunks - c : kGroup;
+        bulk_prefetch_l2(p.side_rows + r * p.side_H + static_cast<int64_t>(c) * 8, static_cast<uint32_t>(n) * 16u);
+      };
+      // groups prefetched ahead of the one combined (1 and 2 measured alike,
+      // 3 and 4 slower: the prefetched bytes then crowd the GEMM's operands)
+      constexpr int kAhead = 1;
+      int64_t t = sw, tp = sw;
+      int g = 0, gp = 0;
+      auto advance = [&](int64_t& tt, int& gg) {
+        if (++gg == groups) {
+          gg = 0;
+          tt += n_sw;
+        }
+      };
+      for (int i = 0; i < kAhead; ++i) {
+        prefetch(tp, gp);
+        advance(tp, gp);
+      }
+      while (t < p.side_T) {
+        prefetch(tp, gp);
+        advance(tp, gp);
+        combine_chunks<3>(p.side_rows, p.side_n_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t,
+                          g * kGroup + lane, chunks, p.side_y, p.err);
+        advance(t, g);
+      }
     } else {
       // the padding scales of expert e (one warp per expert), then the
       // segments: side warp sw takes items sw + n_sw (kStageSegs i + n), the
