@@ -205,57 +205,85 @@ __device__ __forceinline__ void swiglu_bf16_row(const float (&v)[4][32], float a
   }
 }
 
-// The routing-weighted sum of token t's k rows (moe_combine's arithmetic: fp32
-// FMA in slot order starting from 0, one rounding to BF16) over the 8-column
-// chunks c0 + 32 i (i < kNC, those below `chunks`) of the row.  Every slot's
-// 16-byte loads are issued before the FMAs use them (8 kNC per lane in flight),
-// which is what lets a few warps stream the rows at HBM rate.  A slot whose row
-// lies outside [0, n_rows) loads nothing, adds 0 and sets kErrBounds.
+// Asynchronous prefetch of `bytes` (a multiple of 16, from a 16-byte aligned
+// address of valid global memory) into L2; nothing is written or waited for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// One warp's share of the combine of token t (moe_combine's arithmetic: fp32
+// FMA in slot order starting from 0, one rounding to BF16), in groups of
+// 32 kNC 8-column chunks.  Lane q < k holds slot q's row index and weight
+// (r_lane, w_lane, loaded once per token) and the next token's row index
+// (r_next, -1: none); every group takes them by shuffle, so no load waits on
+// an index.  Before a group is combined, lanes q < k prefetch slot q's share
+// of the next group (or the next token's first group) into L2 with one bulk
+// prefetch, so the group's loads, the warp's only bytes in flight, meet L2.
+// Pairs of values are accumulated with two-lane FMAs (each lane the same IEEE
+// fmaf).  A slot whose row lies outside [0, n_rows) loads nothing, adds 0 and
+// sets kErrBounds.
 template <int kNC>
-__device__ __forceinline__ void combine_chunks(const __nv_bfloat16* __restrict__ rows, int64_t n_rows,
-                                               const int32_t* __restrict__ inv_perm, const float* __restrict__ w,
-                                               int32_t H, int32_t k, int64_t t, int c0, int chunks,
-                                               __nv_bfloat16* __restrict__ y, unsigned* err) {
-  float acc[kNC][8];
+__device__ __forceinline__ void combine_token_warp(const __nv_bfloat16* __restrict__ rows, int64_t n_rows,
+                                                   int32_t r_lane, float w_lane, int32_t r_next, int32_t H,
+                                                   int32_t k, int64_t t, __nv_bfloat16* __restrict__ y, int lane,
+                                                   unsigned* err) {
+  constexpr int kGroup = 32 * kNC;
+  const int chunks = H / 8;
+  const int groups = (chunks + kGroup - 1) / kGroup;
+  if (__any_sync(0xFFFFFFFFu, lane < k && (r_lane < 0 || r_lane >= n_rows)) && lane == 0)
+    raise_error(err, kErrBounds);
+  for (int g = 0; g < groups; ++g) {
+    {
+      const bool next_token = g + 1 == groups;
+      const int32_t rq = next_token ? r_next : r_lane;
+      const int c = next_token ? 0 : (g + 1) * kGroup;
+      if (lane < k && rq >= 0 && rq < n_rows) {
+        const int n = chunks - c < kGroup ? chunks - c : kGroup;
+        bulk_prefetch_l2(rows + static_cast<int64_t>(rq) * H + static_cast<int64_t>(c) * 8,
+                         static_cast<uint32_t>(n) * 16u);
+      }
+    }
+    const int c0 = g * kGroup + lane;
+    float2 acc[kNC][4];
 #pragma unroll
-  for (int n = 0; n < kNC; ++n)
+    for (int n = 0; n < kNC; ++n)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[n][i] = 0.0f;
-  for (int j0 = 0; j0 < k; j0 += 8) {
-    uint4 v[8][kNC];
-    float wj[8];
+      for (int i = 0; i < 4; ++i) acc[n][i] = make_float2(0.0f, 0.0f);
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 v[8][kNC];
+      float wj[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (j0 + q < k) {
-        const int64_t r = __ldg(inv_perm + t * k + j0 + q);
-        wj[q] = __ldg(w + t * k + j0 + q);
-        const bool in = r >= 0 && r < n_rows;
-        if (!in) raise_error(err, kErrBounds);
-        const uint4* src = reinterpret_cast<const uint4*>(rows + (in ? r : 0) * H);
+      for (int q = 0; q < 8; ++q) {
+        const int j = j0 + q < k ? j0 + q : 0;                 // warp-uniform
+        const int32_t r = __shfl_sync(0xFFFFFFFFu, r_lane, j);
+        wj[q] = __shfl_sync(0xFFFFFFFFu, w_lane, j);
+        const bool in = j0 + q < k && r >= 0 && r < n_rows;
+        const uint4* src = reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(in ? r : 0) * H);
 #pragma unroll
         for (int n = 0; n < kNC; ++n)
           v[q][n] = in && c0 + 32 * n < chunks ? __ldg(src + c0 + 32 * n) : make_uint4(0, 0, 0, 0);
       }
-    }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (j0 + q < k) {
+      for (int q = 0; q < 8; ++q) {
+        if (j0 + q < k) {
+          const float2 w2 = make_float2(wj[q], wj[q]);
 #pragma unroll
-        for (int n = 0; n < kNC; ++n) {
-          float f[8];
-          bf16x8_to_f32(v[q][n], f);
+          for (int n = 0; n < kNC; ++n) {
+            float f[8];
+            bf16x8_to_f32(v[q][n], f);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[n][i] = fmaf(wj[q], f[i], acc[n][i]);
+            for (int i = 0; i < 4; ++i) acc[n][i] = __ffma2_rn(w2, make_float2(f[2 * i], f[2 * i + 1]), acc[n][i]);
+          }
         }
       }
     }
-  }
-  uint4* dst = reinterpret_cast<uint4*>(y + t * H);
+    uint4* dst = reinterpret_cast<uint4*>(y + t * H);
 #pragma unroll
-  for (int n = 0; n < kNC; ++n)
-    if (c0 + 32 * n < chunks)
-      dst[c0 + 32 * n] = make_uint4(pack_bf16x2(acc[n][0], acc[n][1]), pack_bf16x2(acc[n][2], acc[n][3]),
-                                    pack_bf16x2(acc[n][4], acc[n][5]), pack_bf16x2(acc[n][6], acc[n][7]));
+    for (int n = 0; n < kNC; ++n)
+      if (c0 + 32 * n < chunks)
+        dst[c0 + 32 * n] = make_uint4(pack_bf16x2(acc[n][0].x, acc[n][0].y), pack_bf16x2(acc[n][1].x, acc[n][1].y),
+                                      pack_bf16x2(acc[n][2].x, acc[n][2].y), pack_bf16x2(acc[n][3].x, acc[n][3].y));
+  }
 }
 
 // ------------------------------------------------------------- mbarriers --
@@ -426,12 +454,6 @@ __device__ __forceinline__ int4 gather_rows4(const int32_t* index, int64_t block
 }
 
 // Contiguous global -> shared copy; both addresses 16-byte aligned, bytes % 16 == 0.
-// Asynchronous prefetch of `bytes` (a multiple of 16, from a 16-byte aligned
-// address of valid global memory) into L2; nothing is written or waited for.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

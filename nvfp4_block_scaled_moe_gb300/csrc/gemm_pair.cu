@@ -447,43 +447,28 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
     const int64_t sw = static_cast<int64_t>(blockIdx.x) * kSideWarps + (warp - 2 - kEpiWarps);
     const int64_t n_sw = static_cast<int64_t>(gridDim.x) * kSideWarps;
     if constexpr (kSide == kSideCombine) {
-      // groups of 96 8-column chunks (three per lane) of token t, tokens dealt
-      // in turn; before a group is combined, lanes q < k prefetch a later
-      // group's 1.5 KiB of slot q's row into L2 (one bulk prefetch each), so
-      // that the group's loads, the warp's only way to keep bytes in flight,
-      // meet L2 rather than HBM
-      constexpr int kGroup = 32 * 3;
-      const int chunks = p.side_H / 8;
-      const int groups = (chunks + kGroup - 1) / kGroup;
-      auto prefetch = [&](int64_t t, int g) {
-        if (t >= p.side_T || lane >= p.side_k) return;
-        const int64_t r = __ldg(p.side_inv + t * p.side_k + lane);
-        if (r < 0 || r >= p.side_n_rows) return;             // combine_chunks reports it
-        const int c = g * kGroup;
-        const int n = chunks - c < kGroup ? chunks - c : kGroup;
-        bulk_prefetch_l2(p.side_rows + r * p.side_H + static_cast<int64_t>(c) * 8, static_cast<uint32_t>(n) * 16u);
-      };
-      // groups prefetched ahead of the one combined (1 and 2 measured alike,
-      // 3 and 4 slower: the prefetched bytes then crowd the GEMM's operands)
-      constexpr int kAhead = 1;
-      int64_t t = sw, tp = sw;
-      int g = 0, gp = 0;
-      auto advance = [&](int64_t& tt, int& gg) {
-        if (++gg == groups) {
-          gg = 0;
-          tt += n_sw;
+      // tokens dealt to the side warps in turn; lane q < k loads slot q's row
+      // and weight of its warp's current and next token once
+      auto slot = [&](int64_t t, int32_t& r, float& w) {
+        r = -1;
+        w = 0.0f;
+        if (t < p.side_T && lane < p.side_k) {
+          r = __ldg(p.side_inv + t * p.side_k + lane);
+          w = __ldg(p.side_w + t * p.side_k + lane);
         }
       };
-      for (int i = 0; i < kAhead; ++i) {
-        prefetch(tp, gp);
-        advance(tp, gp);
-      }
-      while (t < p.side_T) {
-        prefetch(tp, gp);
-        advance(tp, gp);
-        combine_chunks<3>(p.side_rows, p.side_n_rows, p.side_inv, p.side_w, p.side_H, p.side_k, t,
-                          g * kGroup + lane, chunks, p.side_y, p.err);
-        advance(t, g);
+      int32_t r_cur, r_nxt;
+      float w_cur, w_nxt;
+      slot(sw, r_cur, w_cur);
+      if (lane < p.side_k && r_cur >= 0 && r_cur < p.side_n_rows)       // the first group of the first token
+        bulk_prefetch_l2(p.side_rows + static_cast<int64_t>(r_cur) * p.side_H,
+                         static_cast<uint32_t>(min(p.side_H / 8, 96)) * 16u);
+      for (int64_t t = sw; t < p.side_T; t += n_sw) {
+        slot(t + n_sw, r_nxt, w_nxt);
+        combine_token_warp<3>(p.side_rows, p.side_n_rows, r_cur, w_cur, r_nxt, p.side_H, p.side_k, t, p.side_y,
+                              lane, p.err);
+        r_cur = r_nxt;
+        w_cur = w_nxt;
       }
     } else {
       // the padding scales of expert e (one warp per expert), then the
