@@ -48,7 +48,6 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSideWarps = 2;                          // the side job's warps (kSide instantiations)
 constexpr int kSideNone = 0, kSideCombine = 1, kSideStage = 2;
-constexpr int kStageSegs = 2;                          // staging segments per batch (two batches in flight)
 constexpr int kThreadsSide = kThreads + 32 * kSideWarps;
 constexpr int kMaxGroups = kPairMaxGroups;             // larger G uses the single-CTA kernel
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
@@ -471,24 +470,18 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
         w_cur = w_nxt;
       }
     } else {
-      // the padding scales of expert e (one warp per expert), then the
-      // segments: side warp sw takes items sw + n_sw (kStageSegs i + n), the
-      // loads of each batch issued before the previous batch is quantised and
-      // written (two batches in registers)
+      // the padding scales of expert e (one warp per expert), then the tokens,
+      // dealt to the side warps in turn; lane q < k loads slot q's row of the
+      // warp's next token while the current one is staged
       for (int e = static_cast<int>(sw); e < p.stage.E; e += static_cast<int>(n_sw)) stage_padding(p.stage, e, lane, 32);
-      const int64_t n_items = static_cast<int64_t>(p.stage.T) * ((p.stage.H + 1023) / 1024);
-      StageBatch<kStageSegs> cur, nxt;
-      auto items = [&](StageBatch<kStageSegs>& b, int64_t i) {
-#pragma unroll
-        for (int n = 0; n < kStageSegs; ++n) b.item[n] = i + n * n_sw < n_items ? i + n * n_sw : -1;
+      auto row = [&](int64_t t) {
+        return t < p.stage.T && lane < p.stage.k ? __ldg(p.stage.inv_perm + t * p.stage.k + lane) : -1;
       };
-      items(cur, sw);
-      stage_load(p.stage, cur, lane);
-      for (int64_t i = sw; i < n_items; i += kStageSegs * n_sw) {
-        items(nxt, i + kStageSegs * n_sw);
-        stage_load(p.stage, nxt, lane);
-        stage_store(p.stage, cur, lane);
-        cur = nxt;
+      int32_t r_cur = row(sw);
+      for (int64_t t = sw; t < p.stage.T; t += n_sw) {
+        const int32_t r_nxt = row(t + n_sw);
+        stage_token_warp(p.stage, t, r_cur, lane);
+        r_cur = r_nxt;
       }
     }
   } else {
@@ -505,10 +498,7 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
     // ceiling (128 cycles per MMA, 4 MMAs per K stage), at most 320 cycles
     // apart.  Issued back to back by all eight warps they measured 6-8% slower
     // at K = 2048: the burst holds up the TMA loads of the next tile's stages.
-    // (With the side staging, whose writes share the path, a 400-cycle cap
-    // measured 1.3% faster than 320; 360 and 440 were slower than 400.)
-    constexpr long long kGapCap = kSide == kSideStage ? 400LL : 320LL;
-    const long long store_gap = min(static_cast<long long>(p.k_blocks) * 40 * kGapCap / 320, kGapCap);
+    const long long store_gap = min(static_cast<long long>(p.k_blocks) * 40, 320LL);
     for (int64_t tile = cluster_id; tile < num_tiles; tile += n_clusters) {
       const TileRows t = tile_rows(s_off, s_pair, p, tile, rank);
       const int64_t grow = t.block * kBM + row_in_tile;

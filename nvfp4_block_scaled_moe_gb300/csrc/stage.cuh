@@ -55,6 +55,36 @@ __device__ __forceinline__ void stage_padding(const StageJob& s, int e, int64_t 
   }
 }
 
+// One lane's 32 values (two 16-blocks, four 16-byte BF16 loads in raw) ->
+// their 16 bytes of nibbles and the two blocks' scale codes (byte q for block
+// q); with a two-level scale the values quantised are fp32(x * g).
+__device__ __forceinline__ void stage_quantize(const uint4 (&raw)[4], bool scaled, float g, uint4& nib,
+                                               uint32_t& codes) {
+  uint32_t w[4];
+  codes = 0;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    float lo[8], hi[8];
+    bf16x8_to_f32(raw[2 * q], lo);
+    bf16x8_to_f32(raw[2 * q + 1], hi);
+    if (scaled) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        lo[i] *= g;
+        hi[i] *= g;
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
+    const BlockScale bs = block_scale(amax);
+    w[2 * q] = quantize8(lo, bs);
+    w[2 * q + 1] = quantize8(hi, bs);
+    codes |= bs.code << (8 * q);
+  }
+  nib = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // One warp's batch of segments item[0..kNS) (item = token * segs + segment,
 // segs = ceil(H / 1024); item < 0: none) with its loads: each segment's x
 // (2 KiB) and its token's k row indices (lane j loads slot j; k <= 32, broadcast
@@ -100,30 +130,7 @@ __device__ __forceinline__ void stage_store(const StageJob& s, const StageBatch<
     const bool active = b.c0[n] < s.H;
     uint4 nib = make_uint4(0, 0, 0, 0);
     uint32_t codes = 0;
-    if (active) {
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {          // two 16-blocks of 16 values
-        float lo[8], hi[8];
-        bf16x8_to_f32(b.raw[n][2 * q], lo);
-        bf16x8_to_f32(b.raw[n][2 * q + 1], hi);
-        if (s.x_gscale != nullptr) {         // two-level scale: quantise fp32(x * g)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            lo[i] *= g;
-            hi[i] *= g;
-          }
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
-        const BlockScale bs = block_scale(amax);
-        w[2 * q] = quantize8(lo, bs);
-        w[2 * q + 1] = quantize8(hi, bs);
-        codes |= bs.code << (8 * q);
-      }
-      nib = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    if (active) stage_quantize(b.raw[n], s.x_gscale != nullptr, g, nib, codes);
     // lanes 2m, 2m+1 own one 64-column group: codes of its four blocks in order
     const uint32_t word = codes | (__shfl_down_sync(0xFFFFFFFFu, codes, 1) << 16);
     const uint32_t k4 = static_cast<uint32_t>(b.c0[n] / 64);
@@ -142,6 +149,65 @@ __device__ __forceinline__ void stage_store(const StageJob& s, const StageBatch<
         if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(s.a_sf + sf_word_offset(r, k4, k4_total)) = word;
       }
     }
+  }
+}
+
+// One warp stages all of token t (the side warps of the L2 GEMM): lane q < k
+// holds slot q's row index (r_lane, loaded once per token by the caller), from
+// which it forms the row's byte offsets in a_q and a_sf once; each segment
+// takes them by shuffle.  The token's segments go in pairs, the loads of the
+// next pair issued before the current pair is quantised and written.  A row
+// outside [0, rows_max) is not written and sets kErrBounds.  (x_q is not
+// written: the side job stages permuted rows only.)
+__device__ __forceinline__ void stage_token_warp(const StageJob& s, int64_t t, int32_t r_lane, int lane) {
+  const int segs = (s.H + 1023) / 1024;
+  const int64_t k4_total = s.H / 64;
+  const bool ok = lane < s.k && r_lane >= 0 && r_lane < s.rows_max;
+  if (__any_sync(0xFFFFFFFFu, lane < s.k && !ok) && lane == 0) raise_error(s.err, kErrBounds);
+  const int64_t q_off = ok ? static_cast<int64_t>(r_lane) * (s.H / 2) : -1;
+  const int64_t sf_off = ok ? (static_cast<int64_t>(r_lane >> 7) * k4_total) * 512 + (r_lane & 31) * 16 +
+                                  ((r_lane >> 5) & 3) * 4
+                            : -1;
+  const float g = s.x_gscale != nullptr ? __ldg(s.x_gscale) : 1.0f;
+  const uint4* xrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(s.x) + t * s.H);
+  auto load = [&](int seg, uint4 (&raw)[4]) {
+    const int c0 = seg * 1024 + lane * 32;
+    if (seg < segs && c0 < s.H) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) raw[i] = __ldg(xrow + c0 / 8 + i);
+    }
+  };
+  auto store = [&](int seg, const uint4 (&raw)[4]) {
+    if (seg >= segs) return;                   // warp-uniform
+    const int c0 = seg * 1024 + lane * 32;
+    const bool active = c0 < s.H;
+    uint4 nib = make_uint4(0, 0, 0, 0);
+    uint32_t codes = 0;
+    if (active) stage_quantize(raw, s.x_gscale != nullptr, g, nib, codes);
+    const uint32_t word = codes | (__shfl_down_sync(0xFFFFFFFFu, codes, 1) << 16);
+    const int64_t sf_col = static_cast<int64_t>(c0 / 64) * 512;
+    for (int j = 0; j < s.k; ++j) {
+      const int64_t qo = __shfl_sync(0xFFFFFFFFu, q_off, j);
+      const int64_t so = __shfl_sync(0xFFFFFFFFu, sf_off, j);
+      if (qo < 0) continue;                    // warp-uniform: reported above
+      if (active) {
+        *reinterpret_cast<uint4*>(s.a_q + qo + c0 / 2) = nib;
+        if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(s.a_sf + so + sf_col) = word;
+      }
+    }
+  };
+  uint4 ra[2][4], rb[2][4];
+  load(0, ra[0]);
+  load(1, ra[1]);
+  for (int seg = 0; seg < segs; seg += 4) {
+    load(seg + 2, rb[0]);
+    load(seg + 3, rb[1]);
+    store(seg, ra[0]);
+    store(seg + 1, ra[1]);
+    load(seg + 4, ra[0]);
+    load(seg + 5, ra[1]);
+    store(seg + 2, rb[0]);
+    store(seg + 3, rb[1]);
   }
 }
 
