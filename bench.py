@@ -52,9 +52,9 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # of that single launch (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # hash of the kernel sources it was taken on.  Reported as roofline.traffic only
 # while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "411792dcc532faa7140c1b15d4ea4df85873e0b257e4fc11d6f50265c3ba2b42",
-                     "bytes": {"prefill": 1728673536 + 151784960, "prefill_overlap": 3887530496 + 386673920,
-                               "decode": 4349432832 + 3508480}}
+L1_TRAFFIC_RECORD = {"sources_sha256": "ef940bc11033a78de6a7b7fc46d3ffd82094f152fac315dbed454c50bc6dd8bc",
+                     "bytes": {"prefill": 1728616960 + 151494656, "prefill_overlap": 3982069504 + 386397184,
+                               "decode": 4351460608 + 3159808}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h",
                   "nvfp4_block_scaled_moe_gb300/csrc/stage.cuh")
