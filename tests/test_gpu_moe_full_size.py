@@ -23,7 +23,8 @@ For each picked row (token t, slot j of expert e):
     intermediates) and nearly all values identical.
 The dense L1 workload's rows and the end-to-end y of sampled tokens are
 checked against the fully CPU-quantised oracle in test_gpu_gemm.py and
-test_gpu_moe.py.
+test_gpu_moe.py.  The serving pipeline at both sizes gives the plain
+forward's y bit for bit.
 """
 import numpy as np
 import pytest
@@ -120,3 +121,33 @@ def test_every_touched_expert_at_full_size(nv, name):
     got, ref = np.concatenate([a.ravel() for a in l2_got]), np.concatenate([a.ravel() for a in l2_ref])
     assert rel_frobenius(got, ref) <= 2e-3
     assert np.mean(got == ref) > 0.97
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_serving_pipeline_equals_plain_forward_at_full_size(nv, name):
+    """The serving pipeline over two full-size batches (batch 1's staging inside
+    batch 0's L2 GEMM, batch 0's combine inside batch 1's L1 GEMM; on the
+    prefill batch both run on the CTA-pair kernels' side warps, on the decode
+    batch as their own launches) gives each batch the plain forward's y, bit
+    for bit."""
+    nv, pipeline = nv
+    spec = dict(inputs.CONFIGS[name])
+    s = pipeline.MoeShape(T=spec["T"], H=spec["H"], I=spec["I"], E=spec["E"], top_k=spec["top_k"])
+    w = pipeline.MoeWeights(s)
+    pool, o1, o2 = inputs.moe_weight_pool(spec)
+    w.set_from_pool(torch.from_numpy(pool).cuda(), o1, o2, float(inputs.WEIGHT_STD))
+    del pool
+    x_t, _ = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    xs = [x_t.cuda(), x_t.flip(0).contiguous().cuda()]
+    lgs = [dev(logits), dev(np.ascontiguousarray(logits[::-1]))]
+    plain = pipeline.MoeBuffers(s)
+    ys = [pipeline.moe_forward(xs[i], lgs[i], w, plain).clone() for i in range(2)]
+    del plain
+    bufs = [pipeline.MoeBuffers(s), pipeline.MoeBuffers(s)]
+    pipeline.moe_forward_deferred(xs[0], lgs[0], w, bufs[0])
+    pipeline.moe_forward_deferred(xs[1], lgs[1], w, bufs[1], prev=bufs[0])
+    y1 = pipeline.moe_finish_deferred(w, bufs[1])
+    nv.nvfp4_device_status()
+    assert torch.equal(bufs[0].y, ys[0])
+    assert torch.equal(y1, ys[1])
