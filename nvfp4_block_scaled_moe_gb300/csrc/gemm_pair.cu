@@ -15,7 +15,7 @@
 // group; a group with an odd block count ends in a tile whose odd CTA has no
 // rows (it loads no A, computes a discarded half and stores nothing).
 //
-// Roles (320 threads per CTA, one CTA per SM):
+// Roles (320 threads per CTA, 384 with a side job; one CTA per SM):
 //   warp 0     producer: TMA loads of A (128 rows), this CTA's 128 rows of B,
 //              this CTA's A scale atoms and both 128-row bands of B's scale
 //              atoms (every CTA multiplies against all 256 B rows, so each needs
@@ -30,7 +30,10 @@
 //              BF16 rows are staged 64 columns at a time and written back with
 //              each store instruction covering four whole 128-byte lines (instead
 //              of 32 partial lines), the stores spaced out over the next tile's
-//              mainloop; SwiGLU nibble rows leave by TMA store.
+//              mainloop; SwiGLU nibble rows leave by TMA store;
+//   warps 10-11  (side-job instantiations only) an HBM-bound job of another
+//              batch: the combine of an earlier batch beside the SwiGLU GEMM,
+//              the activation staging of a later batch beside the BF16 GEMM.
 // Every wait is bounded; a timeout sets the error word and the pair drains
 // and exits together (the final cluster barrier keeps each CTA's shared
 // memory alive while the other may still address it).
@@ -229,7 +232,8 @@ __device__ __forceinline__ void wait_until_clock(long long due) {
 // MMA and epilogue warps run the GEMM, whose own DRAM traffic leaves room for
 // it: the combine of an earlier batch (kSideCombine, in the SwiGLU L1 kernel)
 // or the activation staging of a later batch (kSideStage, in the BF16 L2
-// kernel).  Tokens (or segments) are dealt to the side warps of all CTAs in turn.
+// kernel).  Tokens are dealt to the side warps of all CTAs in turn, a warp
+// taking a whole token.
 template <int kEpi, bool kGather, int kSide>
 __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 1)
     nvf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
