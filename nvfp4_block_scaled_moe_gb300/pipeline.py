@@ -185,52 +185,65 @@ def moe_forward(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuff
     return b.y
 
 
-def _l1(w: MoeWeights, b: MoeBuffers, side_combine=None) -> None:
+def _l1(w: MoeWeights, b: MoeBuffers, side_combine=None, two_level: bool = False) -> None:
     s = b.shape
+    gs = dict(a_global_scale=b.x_gs, b_global_scale=w.w1_gs, out_global_scale=b.a2_gs) if two_level else {}
     nvfp4_grouped_gemm(b.a1_q, b.a1_sf, b.rows_max, b.offsets, b.counts, s.E, 2 * s.I, s.H, w.w1_q, w.w1_sf, 1.0,
-                       EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf, h_debug=b.h_debug, side_combine=side_combine)
+                       EPI_SWIGLU_NVFP4, out_q=b.a2_q, out_sf=b.a2_sf, h_debug=b.h_debug, side_combine=side_combine,
+                       **gs)
 
 
-def _l2(w: MoeWeights, b: MoeBuffers, side_stage=None) -> None:
+def _l2(w: MoeWeights, b: MoeBuffers, side_stage=None, two_level: bool = False) -> None:
     s = b.shape
+    gs = dict(a_global_scale=b.a2_gs, b_global_scale=w.w2_gs) if two_level else {}
     nvfp4_grouped_gemm(b.a2_q, b.a2_sf, b.rows_max, b.offsets, b.counts, s.E, s.H, s.I, w.w2_q, w.w2_sf, 1.0,
-                       EPI_BF16, out_bf16=b.rows_out, side_stage=side_stage)
+                       EPI_BF16, out_bf16=b.rows_out, side_stage=side_stage, **gs)
 
 
 def moe_forward_deferred(x: torch.Tensor, logits: torch.Tensor, w: MoeWeights, b: MoeBuffers,
-                         prev: MoeBuffers | None = None) -> None:
+                         prev: MoeBuffers | None = None, two_level: bool = False) -> None:
     """One step of a serving loop.  Without ``prev``: route + permute + stage and
     the L1 GEMM of this batch into ``b``.  With ``prev`` (an earlier batch whose
     L2 and combine are pending): routing of this batch without staging; prev's
     L2 GEMM, which stages this batch on spare warps; this batch's L1 GEMM, which
     runs prev's combine on spare warps (into prev.y).  This batch's L2 and
     combine stay pending: a later step's prev, or moe_finish_deferred.  A loop
-    alternates two buffer sets.  One-level scales, alpha 1, no shared expert,
-    no gathered L1."""
+    alternates two buffer sets.  two_level: as moe_forward's (x's encode scale
+    computed here into b.x_gs, the weights' from ``w``, the L1 output's
+    ``b.a2_gs``; every step of a loop must pass the same value).  Alpha 1, no
+    shared expert, no gathered L1."""
     s = b.shape
     if prev is b:
         raise ValueError("prev must be another buffer set: this batch's staging runs beside prev's L2 GEMM")
     if b.gather or (prev is not None and prev.gather):
         raise ValueError("the deferred serving step stages permuted rows (no gathered L1)")
+    if two_level and w.w1_gs is None:
+        raise ValueError("two-level forward needs weights quantised with two_level=True")
+    x_gs = None
+    if two_level:
+        if s.T > 0:
+            nvfp4_global_scale(x, b.x_gs)
+        x_gs = b.x_gs
     live_prev = prev is not None and prev.shape.T > 0
     moe_route_permute(logits, x, s.top_k, b.topk_ids, b.topk_w, b.counts, b.offsets, b.perm_token, b.inv_perm,
-                      None if live_prev else b.a1_q, None if live_prev else b.a1_sf, b.workspace)
+                      None if live_prev else b.a1_q, None if live_prev else b.a1_sf, b.workspace,
+                      x_global_scale=None if live_prev else x_gs)
     job = None
     if live_prev:
-        stage = (dict(x=x, inv_perm=b.inv_perm, counts=b.counts, offsets=b.offsets, a1_q=b.a1_q, a1_sf=b.a1_sf)
-                 if s.T > 0 else None)
-        _l2(w, prev, side_stage=stage)
+        stage = (dict(x=x, inv_perm=b.inv_perm, counts=b.counts, offsets=b.offsets, a1_q=b.a1_q, a1_sf=b.a1_sf,
+                      x_global_scale=x_gs) if s.T > 0 else None)
+        _l2(w, prev, side_stage=stage, two_level=two_level)
         job = (prev.rows_out, prev.inv_perm, prev.topk_w, prev.y)
     if s.T > 0:
-        _l1(w, b, side_combine=job)
+        _l1(w, b, side_combine=job, two_level=two_level)
     elif job is not None:
         moe_combine(*job)
 
 
-def moe_finish_deferred(w: MoeWeights, b: MoeBuffers) -> torch.Tensor:
+def moe_finish_deferred(w: MoeWeights, b: MoeBuffers, two_level: bool = False) -> torch.Tensor:
     """The pending L2 GEMM and combine of the batch in ``b`` (after moe_forward_deferred)."""
     if b.shape.T > 0:
-        _l2(w, b)
+        _l2(w, b, two_level=two_level)
         moe_combine(b.rows_out, b.inv_perm, b.topk_w, b.y)
     return b.y
 

@@ -244,3 +244,38 @@ def test_moe_two_level_full_size_sampled_tokens(nv):
                               tok["a2_sf"].reshape(len(rows), -1))
     assert res["ok"], res
     assert rel_frobenius(y.float().cpu().numpy()[pick], tok["y"]) <= 2e-2
+
+
+def test_serving_pipeline_two_level_equals_plain(nv):
+    """The serving pipeline with two-level scales (each batch's x scale computed
+    in its own step; the staging, with x's scale, inside the previous batch's L2
+    GEMM; the combine inside the next batch's L1 GEMM) gives every batch the
+    plain two-level forward's y bit for bit, over three batches on two buffer
+    sets sharing one calibrated L1-output scale."""
+    from nvfp4_block_scaled_moe_gb300 import pipeline
+    spec = inputs.moe_spec(T=600, H=1024, I=512, E=16, top_k=4, seed=66, zipf=True)
+    s, w, b0 = _setup(pipeline, spec)
+    x_t, _ = inputs.moe_x(spec)
+    logits = inputs.moe_logits(spec)
+    xs = [x_t.cuda(), (x_t.flip(0) * 3).contiguous().cuda(), (x_t.roll(5, 0) * 0.25).contiguous().cuda()]
+    lgs = [dev(logits), dev(np.ascontiguousarray(logits[::-1])), dev(np.ascontiguousarray(np.roll(logits, 5, 0)))]
+    a2_gs = pipeline.calibrate_a2_scale(xs[0], lgs[0], w, b0).clone()
+    b0.h_debug = None
+    plain = []
+    for i in range(3):
+        bp = pipeline.MoeBuffers(s)
+        bp.a2_gs = a2_gs
+        plain.append(pipeline.moe_forward(xs[i], lgs[i], w, bp, two_level=True).clone())
+    bufs = [pipeline.MoeBuffers(s), pipeline.MoeBuffers(s)]
+    for bb in bufs:
+        bb.a2_gs = a2_gs
+    ys = []
+    for i in range(3):
+        pipeline.moe_forward_deferred(xs[i], lgs[i], w, bufs[i & 1], prev=bufs[(i - 1) & 1] if i else None,
+                                      two_level=True)
+        if i:
+            ys.append(bufs[(i - 1) & 1].y.clone())
+    ys.append(pipeline.moe_finish_deferred(w, bufs[0], two_level=True).clone())
+    nv.nvfp4_device_status()
+    for i in range(3):
+        assert torch.equal(ys[i], plain[i]), i
