@@ -52,9 +52,9 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # of that single launch (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # hash of the kernel sources it was taken on.  Reported as roofline.traffic only
 # while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "ef940bc11033a78de6a7b7fc46d3ffd82094f152fac315dbed454c50bc6dd8bc",
-                     "bytes": {"prefill": 1728616960 + 151494656, "prefill_overlap": 3982069504 + 386397184,
-                               "decode": 4351460608 + 3159808}}
+L1_TRAFFIC_RECORD = {"sources_sha256": "b33ffbae4371943fd8f59fe709c679cd7be38ceb0abc84f02aef953ec1a2da09",
+                     "bytes": {"prefill": 1728959488 + 151915008, "prefill_overlap": 4019266560 + 386813184,
+                               "decode": 4351670272 + 3221760}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h",
                   "nvfp4_block_scaled_moe_gb300/csrc/stage.cuh")
