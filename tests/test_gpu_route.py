@@ -43,8 +43,7 @@ def _route(nv, pipeline, x_t, logits, top_k, H):
                                           # short batches (split top-k), E = 1024, k = 32
                                           (256, 7168, 256, 8, False), (1, 64, 1024, 8, False),
                                           (256, 64, 1024, 32, True), (255, 128, 64, 6, True),
-                                          # more than 65536 chunk-histogram entries: the separate offsets
-                                          # kernel (fewer: offsets and ranks in one launch)
+                                          # 258 chunks: a long chunk walk in the offsets kernel
                                           (33000, 64, 256, 4, True)])
 def test_route_permute_matches_oracle(nv, T, H, E, k, zipf):
     nv, pipeline = nv
