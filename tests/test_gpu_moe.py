@@ -44,10 +44,19 @@ SMALL = [dict(inputs.CONFIGS["tiny"]),
          inputs.moe_spec(T=300, H=512, I=256, E=8, top_k=2, seed=21),
          inputs.moe_spec(T=200, H=256, I=512, E=5, top_k=3, seed=22, zipf=True),
          # more experts than the CTA-pair kernel takes groups: the GEMMs use the single-CTA kernel
-         inputs.moe_spec(T=400, H=256, I=256, E=600, top_k=4, seed=23)]
+         inputs.moe_spec(T=400, H=256, I=256, E=600, top_k=4, seed=23),
+         # one expert, every token on it (one group of ceil(T/128) blocks)
+         inputs.moe_spec(T=300, H=256, I=256, E=1, top_k=1, seed=27),
+         # every token on every expert (k = E)
+         inputs.moe_spec(T=150, H=256, I=256, E=4, top_k=4, seed=28),
+         # 512 groups, the most the CTA-pair kernel takes, with top-32
+         inputs.moe_spec(T=2100, H=256, I=256, E=512, top_k=32, seed=29, zipf=True),
+         # a single token
+         inputs.moe_spec(T=1, H=512, I=256, E=16, top_k=8, seed=30)]
 
 
-@pytest.mark.parametrize("spec", SMALL, ids=["tiny", "ragged300", "zipf200", "e600"])
+@pytest.mark.parametrize("spec", SMALL, ids=["tiny", "ragged300", "zipf200", "e600", "e1", "k_eq_e", "e512k32",
+                                             "t1"])
 def test_moe_end_to_end_small(nv, spec):
     nv, pipeline = nv
     s, w, b = _gpu_setup(pipeline, spec)
