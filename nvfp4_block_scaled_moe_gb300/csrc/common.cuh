@@ -205,44 +205,26 @@ __device__ __forceinline__ void swiglu_bf16_row(const float (&v)[4][32], float a
   }
 }
 
-// Asynchronous prefetch of `bytes` (a multiple of 16, from a 16-byte aligned
-// address of valid global memory) into L2; nothing is written or waited for.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // One warp's share of the combine of token t (moe_combine's arithmetic: fp32
 // FMA in slot order starting from 0, one rounding to BF16), in groups of
 // 32 kNC 8-column chunks.  Lane q < k holds slot q's row index and weight
-// (r_lane, w_lane, loaded once per token) and the next token's row index
-// (r_next, -1: none); every group takes them by shuffle, so no load waits on
-// an index.  Before a group is combined, lanes q < k prefetch slot q's share
-// of the next group (or the next token's first group) into L2 with one bulk
-// prefetch, so the group's loads, the warp's only bytes in flight, meet L2.
-// Pairs of values are accumulated with two-lane FMAs (each lane the same IEEE
-// fmaf).  A slot whose row lies outside [0, n_rows) loads nothing, adds 0 and
-// sets kErrBounds.
+// (r_lane, w_lane, loaded once per token); every group takes them by shuffle,
+// so no load waits on an index.  Pairs of values are accumulated with two-lane
+// FMAs (each lane the same IEEE fmaf).  The rows are read once, with the
+// evict-first hint (ld.global.cs): with plain loads the stream pushed the
+// GEMM's reused operands out of L2 and the launch read 0.38 GB more from DRAM.
+// A slot whose row lies outside [0, n_rows) loads nothing, adds 0 and sets
+// kErrBounds.
 template <int kNC>
 __device__ __forceinline__ void combine_token_warp(const __nv_bfloat16* __restrict__ rows, int64_t n_rows,
-                                                   int32_t r_lane, float w_lane, int32_t r_next, int32_t H,
-                                                   int32_t k, int64_t t, __nv_bfloat16* __restrict__ y, int lane,
-                                                   unsigned* err) {
+                                                   int32_t r_lane, float w_lane, int32_t H, int32_t k, int64_t t,
+                                                   __nv_bfloat16* __restrict__ y, int lane, unsigned* err) {
   constexpr int kGroup = 32 * kNC;
   const int chunks = H / 8;
   const int groups = (chunks + kGroup - 1) / kGroup;
   if (__any_sync(0xFFFFFFFFu, lane < k && (r_lane < 0 || r_lane >= n_rows)) && lane == 0)
     raise_error(err, kErrBounds);
   for (int g = 0; g < groups; ++g) {
-    {
-      const bool next_token = g + 1 == groups;
-      const int32_t rq = next_token ? r_next : r_lane;
-      const int c = next_token ? 0 : (g + 1) * kGroup;
-      if (lane < k && rq >= 0 && rq < n_rows) {
-        const int n = chunks - c < kGroup ? chunks - c : kGroup;
-        bulk_prefetch_l2(rows + static_cast<int64_t>(rq) * H + static_cast<int64_t>(c) * 8,
-                         static_cast<uint32_t>(n) * 16u);
-      }
-    }
     const int c0 = g * kGroup + lane;
     float2 acc[kNC][4];
 #pragma unroll
@@ -261,7 +243,7 @@ __device__ __forceinline__ void combine_token_warp(const __nv_bfloat16* __restri
         const uint4* src = reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(in ? r : 0) * H);
 #pragma unroll
         for (int n = 0; n < kNC; ++n)
-          v[q][n] = in && c0 + 32 * n < chunks ? __ldg(src + c0 + 32 * n) : make_uint4(0, 0, 0, 0);
+          v[q][n] = in && c0 + 32 * n < chunks ? __ldcs(src + c0 + 32 * n) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {

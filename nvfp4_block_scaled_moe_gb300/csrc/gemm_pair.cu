@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
     const int64_t n_sw = static_cast<int64_t>(gridDim.x) * kSideWarps;
     if constexpr (kSide == kSideCombine) {
       // tokens dealt to the side warps in turn; lane q < k loads slot q's row
-      // and weight of its warp's current and next token once
+      // and weight of its warp's next token while the current one is combined
       auto slot = [&](int64_t t, int32_t& r, float& w) {
         r = -1;
         w = 0.0f;
@@ -463,13 +463,10 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
       int32_t r_cur, r_nxt;
       float w_cur, w_nxt;
       slot(sw, r_cur, w_cur);
-      if (lane < p.side_k && r_cur >= 0 && r_cur < p.side_n_rows)       // the first group of the first token
-        bulk_prefetch_l2(p.side_rows + static_cast<int64_t>(r_cur) * p.side_H,
-                         static_cast<uint32_t>(min(p.side_H / 8, 96)) * 16u);
       for (int64_t t = sw; t < p.side_T; t += n_sw) {
         slot(t + n_sw, r_nxt, w_nxt);
-        combine_token_warp<3>(p.side_rows, p.side_n_rows, r_cur, w_cur, r_nxt, p.side_H, p.side_k, t, p.side_y,
-                              lane, p.err);
+        combine_token_warp<3>(p.side_rows, p.side_n_rows, r_cur, w_cur, p.side_H, p.side_k, t, p.side_y, lane,
+                              p.err);
         r_cur = r_nxt;
         w_cur = w_nxt;
       }
