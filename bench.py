@@ -52,9 +52,9 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # of that single launch (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # hash of the kernel sources it was taken on.  Reported as roofline.traffic only
 # while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "b33ffbae4371943fd8f59fe709c679cd7be38ceb0abc84f02aef953ec1a2da09",
-                     "bytes": {"prefill": 1728959488 + 151915008, "prefill_overlap": 4019266560 + 386813184,
-                               "decode": 4351670272 + 3221760}}
+L1_TRAFFIC_RECORD = {"sources_sha256": "2f3706eeb3ce38274ebbe9cada6e3df3468d81e025fb1f9c401e364e6fe3e007",
+                     "bytes": {"prefill": 1728708608 + 151533056, "prefill_overlap": 3610125568 + 386414080,
+                               "decode": 4349521408 + 3249920}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h",
                   "nvfp4_block_scaled_moe_gb300/csrc/stage.cuh")
