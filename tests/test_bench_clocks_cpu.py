@@ -79,3 +79,26 @@ def test_region_shorter_than_the_poll_period_takes_the_nearest_sample():
     out = s.stop(1.9, 1.95)
     assert out["samples"] == 1 and out["sm_mhz"] == 2070
     assert "nearest" in out["source"]
+
+
+def test_window_summarises_a_span_and_keeps_polling(monkeypatch):
+    """window(t0, t1) gives the samples of one span while the sampler runs on
+    (the timed region, then the GEMMs timed alone after it, from one sampler)."""
+    lib = FakeNvml()
+    s = _sampler(monkeypatch, lib)
+    s.start()
+    lib.mhz = 2070
+    t0 = time.time()
+    time.sleep(0.04)
+    t1 = time.time()
+    region = s.window(t0, t1)
+    assert not lib.shutdown and s.thread.is_alive()
+    lib.mhz, lib.bits = 1700, 0x4
+    t2 = time.time()
+    time.sleep(0.04)
+    t3 = time.time()
+    later = s.stop(t2, t3)
+    assert lib.shutdown
+    assert region["sm_mhz"] == 2070 and region["reasons"] == []
+    assert later["sm_mhz"] == 1700 and later["reasons"] == ["sw_power_cap"]
+    assert region["samples"] >= 3 and later["samples"] >= 3
