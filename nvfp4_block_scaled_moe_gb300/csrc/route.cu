@@ -392,17 +392,34 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int64_t r = __ldg(inv_perm + t * k + j);
-      const float wj = __ldg(w + t * k + j);
-      if (r < 0 || r >= n_rows) {
-        raise_error(err, kErrBounds);
-        continue;
-      }
-      float v[8];
-      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(rows + r * H) + c), v);
+    // slots in groups of eight: the group's row loads are all issued before the
+    // first is used (an index check inside one slot-at-a-time loop kept the
+    // compiler from issuing them ahead)
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 v[8];
+      float wj[8];
+      bool in[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+      for (int q = 0; q < 8; ++q) {
+        int64_t r = 0;
+        wj[q] = 0.0f;
+        in[q] = false;
+        if (j0 + q < k) {
+          r = __ldg(inv_perm + t * k + j0 + q);
+          wj[q] = __ldg(w + t * k + j0 + q);
+          in[q] = r >= 0 && r < n_rows;
+          if (!in[q]) raise_error(err, kErrBounds);
+        }
+        v[q] = in[q] ? __ldg(reinterpret_cast<const uint4*>(rows + (in[q] ? r : 0) * H) + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (!in[q]) continue;
+        float f[8];
+        bf16x8_to_f32(v[q], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[q], f[i], acc[i]);
+      }
     }
     if (shared != nullptr) {
       float v[8];
