@@ -736,6 +736,10 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
 
     if rank != 0:
         return
+    # launches per grouped GEMM: the prefill batch's are split (CTA pairs beside a
+    # single-CTA launch), a gathering L1 is not
+    l2_n = 2 if args.workload == WORKLOAD else 1
+    l1_n = 2 if args.workload == WORKLOAD and not args.gather else 1
     pk = peaks()
     # a sub-second region at the maximum SM clock: the burst BF16 figure x the
     # nominal FP4 / BF16 dense ratio
@@ -812,7 +816,9 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
                     "measured": ("after the timed region: 3 untimed rounds, then the median of 10 rounds of L1 "
                                  "alone, L2 alone, L1 with a combine, L2 with a staging (interleaved)"),
                     "clocks": a["clocks"]}
-        roofline = dict({"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs)"
+        roofline = dict({"kernel": ("L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_pair_kernel<0> (CTA pairs, all but "
+                                    "8 SMs) with nvf4_gemm_kernel<0, 256> beside it on 8 SMs (the last block of the "
+                                    "thinnest odd groups)"
                                     if args.workload == WORKLOAD else
                                     "L1 GEMM + SwiGLU + NVFP4 epilogue: nvf4_gemm_kernel<0, 256> (single CTAs)"),
                          "bound": "tensor"}, **tensor_view, side_job=side,
@@ -846,9 +852,13 @@ def run_ours(args, world: int, rank: int, local: int) -> None:
         # per step: top-k, offsets, assign, scatter, L1, L2, combine (+ x's amax and
         # its finalisation with --two-level; + the shared expert's quantise, L1, L2);
         # the pipeline: top-k, offsets, assign, L2 (+ staging), L1 (+ combine) per
-        # step (the first: scatter in place of L2), then the last L2 and combine
-        "gpu_launches": (5 * args.steps + 2 if ov else
-                         (7 + (2 if args.two_level else 0) + (3 if args.shared_expert else 0)) * args.steps),
+        # step (the first: scatter in place of L2), then the last L2 and combine.
+        # On the prefill batch each grouped GEMM is two launches (CTA pairs, and
+        # the single-CTA launch beside it over the thinnest odd groups' last
+        # blocks), except a gathering L1
+        "gpu_launches": (4 + l1_n + (args.steps - 1) * (3 + l1_n + l2_n) + l2_n + 1 if ov else
+                         (5 + l1_n + l2_n + (2 if args.two_level else 0) + (3 if args.shared_expert else 0))
+                         * args.steps),
         "clocks": clk,
         "quantize": quantize,
         "sustained": sustained,

@@ -268,6 +268,61 @@ __device__ __forceinline__ void combine_token_warp(const __nv_bfloat16* __restri
   }
 }
 
+// --------------------------------------------------------- leftover blocks --
+// The CTA-pair GEMM pairs consecutive 128-row blocks of a group, so a group with
+// an odd block count ends in a pair tile whose odd CTA has no rows: the pair
+// still stages and multiplies a whole tile for half of one.  With a split, a
+// single-CTA launch on S SMs runs beside the pair launch of P clusters and takes
+// the last block of some of those groups: the last n_take odd groups in group
+// order (experts with few rows come last under a skewed routing, so the split
+// takes the thin, weight-streaming ones first, whose DRAM time then overlaps the
+// pair launch's compute-bound tiles instead of forming its tail), n_take chosen
+// so that both launches end together.  A single-CTA 128-row tile costs its SM
+// about kLeftCostNum / kLeftCostDen times what a full pair tile costs each of its
+// two SMs (it stages all 256 weight rows itself: 54 instead of 38 KiB per K
+// stage), so
+//   n_take = min(n_odd, floor(S * (pairs + n_odd) / (P * cost + S))),
+// pairs the full pairs over all groups.  Both kernels compute the same split
+// from the offsets alone; S == 0: none.
+constexpr int64_t kLeftCostNum = 3, kLeftCostDen = 2;
+struct LeftoverSplit {
+  int32_t n_odd;
+  int32_t n_take;
+};
+
+// One warp, all lanes: the split over the G groups of the block offsets s_off.
+__device__ __forceinline__ LeftoverSplit leftover_split(const int32_t* s_off, int G, int P, int S, int lane) {
+  uint32_t pairs = 0, odd = 0;
+  for (int g = lane; g < G; g += 32) {
+    const int32_t blocks = (s_off[g + 1] - s_off[g]) / 128;
+    if (blocks > 0) {
+      pairs += static_cast<uint32_t>(blocks >> 1);
+      odd += static_cast<uint32_t>(blocks & 1);
+    }
+  }
+  pairs = __reduce_add_sync(0xFFFFFFFFu, pairs);
+  odd = __reduce_add_sync(0xFFFFFFFFu, odd);
+  LeftoverSplit ls;
+  ls.n_odd = static_cast<int32_t>(odd);
+  ls.n_take = 0;
+  if (S > 0 && P > 0) {
+    const int64_t fit = static_cast<int64_t>(S) * kLeftCostDen * (static_cast<int64_t>(pairs) + odd) /
+                        (static_cast<int64_t>(P) * kLeftCostNum + static_cast<int64_t>(S) * kLeftCostDen);
+    ls.n_take = static_cast<int32_t>(fit < static_cast<int64_t>(odd) ? fit : static_cast<int64_t>(odd));
+  }
+  return ls;
+}
+
+// Inclusive warp scan of v (lane order).
+__device__ __forceinline__ int32_t warp_scan_incl(int32_t v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
 // ------------------------------------------------------------- mbarriers --
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

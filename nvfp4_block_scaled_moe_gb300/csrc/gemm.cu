@@ -45,6 +45,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK / 2;            // 16 KiB
 constexpr uint32_t kSfaBytes = kBM * (kBK / 16);       // 2 KiB: 4 atoms of 512 B
 constexpr int kMaxGroups = 1024;
+constexpr int kSplitCtas = 8;          // SMs of a split's single-CTA launch (four pair slots)
 constexpr uint32_t kTmemCols = 512;
 
 // Tile configuration by output-tile width BN:
@@ -71,7 +72,8 @@ struct Cfg {
   static constexpr uint32_t kNumBars = 2 * kStages + 2 * kAcc + 1;   // full, empty, tfull, tempty, drain
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;     // tmem slot, abort flag
   static constexpr uint32_t kOffGroups = kOffMisc + 16;
-  static constexpr uint32_t kSmemBytes = kOffGroups + (kMaxGroups + 1) * 4 + 1024;   // + alignment slack
+  static constexpr uint32_t kOffLeft = kOffGroups + (kMaxGroups + 1) * 4;  // a split's leftover blocks, count
+  static constexpr uint32_t kSmemBytes = kOffLeft + (kPairMaxGroups + 1) * 4 + 1024;   // + alignment slack
   static constexpr uint32_t kTmemSf = kAcc * BN;
   static constexpr uint32_t kTmemSfStage = 16 + 16 * kBands;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -99,6 +101,10 @@ struct Params {
   __nv_bfloat16* out_bf16;
   float* h_debug;
   unsigned* err;
+  // left_ctas > 0: this launch is a split's single-CTA half (common.cuh:
+  // leftover_split, beside a pair launch of pair_clusters clusters) and computes
+  // only the last block of the odd groups it takes, thinnest groups first
+  int32_t left_ctas, pair_clusters;
 };
 
 __device__ __forceinline__ int find_group(const int32_t* off, int G, int64_t row) {
@@ -230,11 +236,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
+  // a split's leftover blocks: s_left[i] is the last block of the i-th group
+  // taken, counting from the last odd group down; s_left[kPairMaxGroups] the count
+  int32_t* s_left = reinterpret_cast<int32_t*>(smem + C::kOffLeft);
+  if (p.left_ctas > 0) {
+    if (warp == 2) {
+      const LeftoverSplit ls = leftover_split(s_off, p.G, p.pair_clusters, p.left_ctas, lane);
+      int32_t carry_odd = 0;
+      for (int base = 0; base < p.G; base += 32) {
+        const int g = base + lane;
+        int32_t blocks = 0;
+        if (g < p.G) blocks = (s_off[g + 1] - s_off[g]) / kBM;
+        if (blocks < 0) blocks = 0;
+        const int32_t odd = blocks & 1;
+        const int32_t rank = carry_odd + warp_scan_incl(odd, lane) - odd;     // odd groups before g
+        const int32_t from_last = ls.n_odd - 1 - rank;
+        if (odd != 0 && from_last < ls.n_take && from_last < kPairMaxGroups)
+          s_left[from_last] = s_off[g + 1] / kBM - 1;
+        carry_odd += __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(odd));
+      }
+      if (lane == 0) s_left[kPairMaxGroups] = ls.n_take < kPairMaxGroups ? ls.n_take : kPairMaxGroups;
+    }
+    __syncthreads();
+  }
+
   // the grouped rows must be a 128-aligned prefix of the allocation
   const int64_t total_rows = s_off[p.G];
   int64_t num_tiles = 0;
   if (total_rows >= 0 && total_rows <= p.rows_max && (total_rows % kBM) == 0) {
-    num_tiles = (total_rows / kBM) * p.n_tiles;
+    num_tiles = (p.left_ctas > 0 ? s_left[kPairMaxGroups] : total_rows / kBM) * p.n_tiles;
   } else if (threadIdx.x == 0) {
     raise_error(p.err, kErrBounds);
   }
@@ -250,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, filled = 0, fill_parity = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; tile < tiles_u && ok; tile += gridDim.x) {
-      const int64_t mt = tile / p.n_tiles;
-      const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
+      const int64_t mi = tile / p.n_tiles;
+      const int32_t nt = static_cast<int32_t>(tile - mi * p.n_tiles);
+      const int64_t mt = p.left_ctas > 0 ? s_left[mi] : mi;
       const int g = __shfl_sync(0xFFFFFFFFu, find_group(s_off, p.G, mt * kBM), 0);
       const uint8_t* sfa = p.a_sf + (mt * k4) * 512;
       const uint8_t* sfb = p.b_sf + g * p.sfb_group_bytes + (static_cast<int64_t>(kBands * nt) * k4) * 512;
@@ -347,8 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t row_in_tile = quad * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int64_t mt = tile / p.n_tiles;
-      const int32_t nt = static_cast<int32_t>(tile - mt * p.n_tiles);
+      const int64_t mi = tile / p.n_tiles;
+      const int32_t nt = static_cast<int32_t>(tile - mi * p.n_tiles);
+      const int64_t mt = p.left_ctas > 0 ? s_left[mi] : mi;
       const int64_t grow = mt * kBM + row_in_tile;
       const int g = find_group(s_off, p.G, mt * kBM);
       bool valid = true;
@@ -440,6 +472,47 @@ DeviceInfo& device_info(int dev) {
   return d;
 }
 
+// The stream a split's single-CTA launch runs on, one per device (created on
+// first use, never destroyed; the caller's stream forks to it and joins it back
+// through events, so calls on any streams and under capture stay ordered).
+cudaStream_t split_stream(int dev) {
+  static cudaStream_t streams[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  cudaStream_t& s = streams[dev & 63];
+  if (s == nullptr && cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) s = nullptr;
+  return s;
+}
+
+// A split's single-CTA half: 128-row tiles over the leftover blocks, on `ctas`
+// CTAs launched as clusters of two, so that they take whole pair slots and the
+// pair launch beside them keeps all of its clusters resident.
+template <int kEpi>
+cudaError_t launch_left(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int ctas, cudaStream_t stream,
+                        DeviceInfo& info) {
+  constexpr int slot = kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_SWIGLU_BF16 ? 3 : 1;
+  if (!info.attr_set[slot]) {
+    cudaError_t e = cudaFuncSetAttribute(nvf4_gemm_kernel<kEpi, 256, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg<256>::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    info.attr_set[slot] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<256>::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, nvf4_gemm_kernel<kEpi, 256, false>, ma, mb, p);
+}
+
 template <int kEpi, int BN, bool kGather = false>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t stream,
                    DeviceInfo& info) {
@@ -503,7 +576,12 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     }
     return gemm_launch(rest, stream);
   }
-  if (pair) return gemm_pair_launch(a, info.sms, dev, stream);
+  // a grouped CTA-pair GEMM (auto tiles) is split: kSplitCtas SMs run a
+  // single-CTA launch over the last block of the thinnest odd groups beside
+  // the pair launch, which skips those groups' half-empty pair tiles
+  const bool split = pair && mode == NVFP4_GEMM_TILES_AUTO && a.offsets != nullptr && a.G > 1 &&
+                     a.a_gather == nullptr && info.sms >= 8 * kSplitCtas;
+  if (pair && !split) return gemm_pair_launch(a, info.sms, dev, stream);
   CUtensorMap ma, mb;
   const bool gather = a.a_gather != nullptr;      // gathered A rows: a one-row box for tile::gather4
   if (!make_tmap_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_q,
@@ -536,6 +614,35 @@ nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
   p.out_bf16 = static_cast<__nv_bfloat16*>(a.out_bf16);
   p.h_debug = a.h_debug;
   p.err = device_error_word();
+  p.left_ctas = 0;
+  p.pair_clusters = 0;
+
+  if (split) {
+    cudaStream_t side = split_stream(dev);
+    if (side == nullptr) return fail(NVFP4_ERR_CUDA, "nvfp4_grouped_gemm: no split stream");
+    cudaEvent_t fork = nullptr, join = nullptr;
+    e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+    nvfp4_status st = NVFP4_OK;
+    int clusters = 0;
+    if (e == cudaSuccess) st = gemm_pair_launch(a, info.sms, dev, stream, kSplitCtas, &clusters);
+    if (e == cudaSuccess && st == NVFP4_OK) {
+      p.left_ctas = kSplitCtas;
+      p.pair_clusters = clusters;
+      e = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4 ? launch_left<NVFP4_EPI_SWIGLU_NVFP4>(ma, mb, p, kSplitCtas, side, info)
+          : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? launch_left<NVFP4_EPI_SWIGLU_BF16>(ma, mb, p, kSplitCtas, side, info)
+                                                : launch_left<NVFP4_EPI_BF16>(ma, mb, p, kSplitCtas, side, info);
+      if (e == cudaSuccess) e = cudaEventRecord(join, side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, join, 0);
+    }
+    if (fork != nullptr) cudaEventDestroy(fork);
+    if (join != nullptr) cudaEventDestroy(join);
+    if (st != NVFP4_OK) return st;
+    if (e != cudaSuccess) return fail_cuda(e, "nvfp4_grouped_gemm: split launch");
+    return NVFP4_OK;
+  }
 
   const int64_t max_tiles = (a.rows_max / kBM) * p.n_tiles;
   const int grid = static_cast<int>(max_tiles < info.sms ? max_tiles : info.sms);

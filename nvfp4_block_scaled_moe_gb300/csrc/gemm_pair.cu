@@ -125,6 +125,11 @@ struct PairParams {
   __nv_bfloat16* side_y;
   int32_t side_T, side_H, side_k;
   StageJob stage;
+  // split: a single-CTA launch of left_ctas CTAs runs beside this one (of
+  // pair_clusters clusters) and takes the last block of some odd groups, whose
+  // half-empty pair tiles this launch then skips (common.cuh: leftover_split);
+  // left_ctas == 0: no split
+  int32_t left_ctas, pair_clusters;
 };
 
 // last g < G with tab[g] <= v (tab non-decreasing, tab[0] = 0 <= v)
@@ -293,23 +298,23 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
   }
   __syncthreads();
   if (warp == 2) {
-    // pair prefix: s_pair[g] = sum over groups before g of ceil(blocks / 2)
-    int32_t carry = 0;
+    // pair prefix: s_pair[g] = sum over groups before g of ceil(blocks / 2),
+    // less the half-empty pair of each odd group a split's single-CTA launch takes
+    const LeftoverSplit ls = leftover_split(s_off, p.G, p.pair_clusters, p.left_ctas, lane);
+    int32_t carry = 0, carry_odd = 0;
     if (lane == 0) s_pair[0] = 0;
     for (int base = 0; base < p.G; base += 32) {
       const int g = base + lane;
-      int32_t v = 0;
-      if (g < p.G) {
-        const int32_t blocks = (s_off[g + 1] - s_off[g]) / kBM;
-        v = blocks > 0 ? (blocks + 1) >> 1 : 0;
-      }
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int32_t o = __shfl_up_sync(0xFFFFFFFFu, v, d);
-        if (lane >= d) v += o;
-      }
+      int32_t blocks = 0;
+      if (g < p.G) blocks = (s_off[g + 1] - s_off[g]) / kBM;
+      if (blocks < 0) blocks = 0;
+      const int32_t odd = blocks & 1;
+      const int32_t odd_incl = warp_scan_incl(odd, lane);
+      const bool taken = odd != 0 && carry_odd + odd_incl - odd >= ls.n_odd - ls.n_take;
+      const int32_t v = warp_scan_incl((blocks >> 1) + (odd != 0 && !taken ? 1 : 0), lane);
       if (g < p.G) s_pair[g + 1] = carry + v;
       carry += __shfl_sync(0xFFFFFFFFu, v, 31);
+      carry_odd += __shfl_sync(0xFFFFFFFFu, odd_incl, 31);
     }
   }
   tc_fence_before_sync();
@@ -620,10 +625,12 @@ std::mutex& pair_mutex() {
   return mu;
 }
 
+// reserve: clusters' worth of SMs left free for a split's single-CTA launch (the
+// launch's cluster count goes to p.pair_clusters and *clusters_out)
 template <int kEpi, bool kGather, int kSide = kSideNone>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
-                        const CUtensorMap& mo, const PairParams& p, int64_t num_tiles, int sms, int dev,
-                        cudaStream_t stream) {
+                        const CUtensorMap& mo, PairParams p, int64_t num_tiles, int sms, int dev,
+                        cudaStream_t stream, int reserve, int* clusters_out) {
   constexpr int slot = kSide != kSideNone ? 3 + kSide
                        : kGather          ? 3
                                           : (kEpi == NVFP4_EPI_SWIGLU_NVFP4 ? 0 : kEpi == NVFP4_EPI_BF16 ? 1 : 2);
@@ -657,15 +664,19 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     max_clusters = info.max_clusters[slot];
   }
   // every cluster resident at once (the tile loop strides by the cluster count)
-  int64_t clusters = max_clusters < num_tiles ? max_clusters : num_tiles;
+  const int64_t avail = static_cast<int64_t>(max_clusters) - reserve;
+  int64_t clusters = avail < num_tiles ? avail : num_tiles;
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
+  p.pair_clusters = static_cast<int32_t>(clusters);
+  if (clusters_out != nullptr) *clusters_out = static_cast<int>(clusters);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   return cudaLaunchKernelEx(&cfg, nvf4_gemm_pair_kernel<kEpi, kGather, kSide>, ma, mb, msa, msb, mo, p);
 }
 
 }  // namespace
 
-nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t stream) {
+nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t stream, int left_ctas,
+                              int* clusters_out) {
   if (a.G > kMaxGroups) return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_grouped_gemm: G=%d exceeds %d", a.G, kMaxGroups);
   constexpr int bn = PairCfg<NVFP4_EPI_BF16>::kBN;      // pair tile columns
   const bool swiglu = a.epilogue == NVFP4_EPI_SWIGLU_NVFP4;
@@ -724,17 +735,21 @@ nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t 
   p.side_H = a.side_H;
   p.side_k = a.side_k;
   p.stage = a.stage;
+  p.left_ctas = left_ctas;
+  p.pair_clusters = 0;
 
   // tiles that can exist: every group's pairs, at most ceil(blocks / 2) + G
   const int64_t blocks = a.rows_max / kBM;
   const int64_t max_pairs = (blocks + 1) / 2 + (p.G > 1 ? p.G : 0);
   const int64_t max_tiles = max_pairs * p.n_tiles;
   if (max_tiles <= 0) return NVFP4_OK;
-#define NVFP4_PAIR_LAUNCH(E, GA) launch_pair<E, GA>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream)
-  const cudaError_t e = side ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4, false, kSideCombine>(ma, mb, msa, msb, mo, p,
-                                                                                        max_tiles, sms, dev, stream)
-                        : stage ? launch_pair<NVFP4_EPI_BF16, false, kSideStage>(ma, mb, msa, msb, mo, p, max_tiles,
-                                                                                 sms, dev, stream)
+  const int reserve = (left_ctas + 1) / 2;
+#define NVFP4_PAIR_LAUNCH(E, GA) \
+  launch_pair<E, GA>(ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream, reserve, clusters_out)
+  const cudaError_t e = side ? launch_pair<NVFP4_EPI_SWIGLU_NVFP4, false, kSideCombine>(
+                                   ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream, reserve, clusters_out)
+                        : stage ? launch_pair<NVFP4_EPI_BF16, false, kSideStage>(
+                                      ma, mb, msa, msb, mo, p, max_tiles, sms, dev, stream, reserve, clusters_out)
                         : gather                              ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, true)
                         : swiglu                              ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_NVFP4, false)
                         : a.epilogue == NVFP4_EPI_SWIGLU_BF16 ? NVFP4_PAIR_LAUNCH(NVFP4_EPI_SWIGLU_BF16, false)

@@ -110,9 +110,13 @@ struct GemmArgs {
 // Returns a status; writes a message with set_error_message on failure.
 nvfp4_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
 // The CTA-pair kernel (N % 256 == 0, at most kPairMaxGroups groups); sms and
-// dev of the current device.
+// dev of the current device.  left_ctas > 0: a split (common.cuh:
+// leftover_split) whose single-CTA launch of left_ctas CTAs the caller makes
+// beside this one; the launch leaves their SMs free and returns its cluster
+// count in *clusters_out.
 constexpr int kPairMaxGroups = 512;
-nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t stream);
+nvfp4_status gemm_pair_launch(const GemmArgs& a, int sms, int dev, cudaStream_t stream, int left_ctas = 0,
+                              int* clusters_out = nullptr);
 nvfp4_status set_gemm_tiles(int mode);
 
 // 2-D tensor map of a row-major rows x cols matrix (gemm.cu).

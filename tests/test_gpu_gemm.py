@@ -63,9 +63,11 @@ def _tiles(nv, mode):
 
 def _both_kernels(nv, run):
     """run() -> tuple of host arrays, on each tile kernel (single CTAs and CTA
-    pairs); asserts they are identical."""
+    pairs) and with the automatic choice (which splits a grouped pair GEMM's
+    odd groups' last blocks off to a single-CTA launch beside it); asserts they
+    are identical."""
     outs = []
-    for mode in (nv.GEMM_TILES_SINGLE, nv.GEMM_TILES_PAIR):
+    for mode in (nv.GEMM_TILES_SINGLE, nv.GEMM_TILES_PAIR, nv.GEMM_TILES_AUTO):
         with _tiles(nv, mode):
             outs.append(run())
     for o in outs[1:]:
@@ -123,6 +125,49 @@ def test_gemm_bf16_epilogue(nv, sizes, counts, N, K, alpha):
     mask = np.ones(rows_max, bool)
     mask[valid] = False
     assert np.all(got[mask] == 12288.0)               # nothing stored outside the real rows
+
+
+@pytest.mark.parametrize("epi", ["bf16", "swiglu"])
+def test_split_gemm_equals_pair_and_single(nv, epi):
+    """A grouped pair GEMM with many odd groups (auto tiles: the pair launch on
+    all but eight SMs skips the half-empty pair tiles of the thinnest odd
+    groups, which a single-CTA launch on those eight SMs computes beside it)
+    gives the bytes of the pair kernel alone and of the single-CTA kernel
+    alone, and the oracle's values."""
+    blocks = [1, 3, 2, 0, 5, 1, 1, 4, 7, 1, 2, 3, 1, 0, 1, 9, 1, 1, 3, 1, 2, 1, 1, 6]   # 15 odd groups
+    sizes = [128 * b for b in blocks]
+    counts = [max(0, s - (i * 29) % 128) for i, s in enumerate(sizes)]
+    rows_max = sum(sizes)
+    assert rows_max >= 2 * 128 * len(sizes)            # the automatic choice takes CTA pairs
+    N, K = 512, 512
+    d, offs, a_deq, b_deq = _operands(nv, 91, rows_max, sizes, N, K)
+    cnt = dev(np.array(counts, np.int32))
+
+    def run():
+        if epi == "bf16":
+            out = torch.full((rows_max, N), 12288.0, dtype=torch.bfloat16, device="cuda")
+            nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), cnt, len(sizes), N, K, d["b_q"],
+                                  d["b_sf"], 1.0, nv.EPI_BF16, out_bf16=out)
+            nv.nvfp4_device_status()
+            return (out.float().cpu().numpy(),)
+        q = torch.full((rows_max, N // 4), 0x77, dtype=torch.uint8, device="cuda")
+        sf = torch.zeros(nv.sf_bytes(rows_max, N // 2), dtype=torch.uint8, device="cuda")
+        nv.nvfp4_grouped_gemm(d["a_q"], d["a_sf"], rows_max, dev(offs), cnt, len(sizes), N, K, d["b_q"], d["b_sf"],
+                              1.0, nv.EPI_SWIGLU_NVFP4, out_q=q, out_sf=sf)
+        nv.nvfp4_device_status()
+        return host(q), host(sf)
+
+    outs = _both_kernels(nv, run)
+    valid = _valid_rows(offs, counts)
+    g_full = omoe.grouped_gemm(a_deq, offs, b_deq, 1.0)
+    if epi == "bf16":
+        ref = omoe.round_to_bf16(g_full)
+        assert rel_frobenius(outs[0][valid], ref[valid]) <= 2e-3
+    else:
+        oq, osf, _ = omoe.l1_swiglu_requant(g_full)
+        gsf = onv.unswizzle_sf(outs[1], rows_max, N // 32)
+        res = compare_requantised(outs[0][valid], gsf[valid], oq[valid], osf[valid])
+        assert res["ok"], res
 
 
 CASES_SWIGLU = [

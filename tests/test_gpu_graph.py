@@ -64,7 +64,7 @@ def _tiles(nv, mode):
         nv.nvfp4_set_gemm_tiles(nv.GEMM_TILES_AUTO)
 
 
-@pytest.mark.parametrize("mode", ["single", "pair"])
+@pytest.mark.parametrize("mode", ["single", "pair", "auto"])
 def test_grouped_gemm_in_graph(nv, mode):
     sizes, counts, N, K = [512, 128, 384], [500, 128, 300], 1024, 768
     rows_max = sum(sizes)
@@ -92,7 +92,9 @@ def test_grouped_gemm_in_graph(nv, mode):
         nv.nvfp4_grouped_gemm(a_q_d, a_sf_d, rows_max, offs, cnt, len(sizes), N, K, b_q_d, b_sf_d, 1.0,
                               nv.EPI_SWIGLU_NVFP4, out_q=oq, out_sf=osf)
 
-    with _tiles(nv, {"single": nv.GEMM_TILES_SINGLE, "pair": nv.GEMM_TILES_PAIR}[mode]):
+    # auto: CTA pairs split with a single-CTA launch on a second stream (forked
+    # and joined inside the captured call)
+    with _tiles(nv, {"single": nv.GEMM_TILES_SINGLE, "pair": nv.GEMM_TILES_PAIR, "auto": nv.GEMM_TILES_AUTO}[mode]):
         _replayed(run, [out, oq, osf])
     nv.nvfp4_device_status()
 
