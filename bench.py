@@ -49,12 +49,15 @@ import inputs  # noqa: E402
 METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs HBM"
 
 # DRAM bytes (read + write) of one L1 launch per workload, from an ncu capture
-# of that single launch (dram__bytes_read.sum + dram__bytes_write.sum), and the
-# hash of the kernel sources it was taken on.  Reported as roofline.traffic only
-# while the sources still hash the same (a changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "2f3706eeb3ce38274ebbe9cada6e3df3468d81e025fb1f9c401e364e6fe3e007",
-                     "bytes": {"prefill": 1728708608 + 151533056, "prefill_overlap": 3610125568 + 386414080,
-                               "decode": 4349521408 + 3249920}}
+# of that launch (dram__bytes_read.sum + dram__bytes_write.sum; on the prefill
+# batch the CTA-pair launch plus the single-CTA launch beside it, captured one
+# after the other), and the hash of the kernel sources it was taken on.
+# Reported as roofline.traffic only while the sources still hash the same (a
+# changed kernel reports null).
+L1_TRAFFIC_RECORD = {"sources_sha256": "7fe6176b793f9898ebc10a635916dd6fc5d1c9939954f27fc25cbd9b15daf92c",
+                     "bytes": {"prefill": (1064688640 + 152835072) + (664393728 + 791808),
+                               "prefill_overlap": (2945248768 + 384499968) + (664398592 + 389376),
+                               "decode": 4350664192 + 3250176}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h",
                   "nvfp4_block_scaled_moe_gb300/csrc/stage.cuh")
