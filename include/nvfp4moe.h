@@ -82,10 +82,11 @@ typedef enum {
 
 /* Output-tile kernels of nvfp4_grouped_gemm (see nvfp4_set_gemm_tiles). */
 typedef enum {
-  NVFP4_GEMM_TILES_AUTO = 0,   /* by shape: CTA pairs when groups average >= 256 rows */
+  NVFP4_GEMM_TILES_AUTO = 0,   /* by shape: CTA pairs when groups average >= 256 rows; with
+                                  more than one group, split (see nvfp4_grouped_gemm) */
   NVFP4_GEMM_TILES_SINGLE = 1, /* one CTA per 128-row tile */
   NVFP4_GEMM_TILES_PAIR = 2    /* two CTAs (a cluster) per 256-row tile, where N % 256 == 0
-                                  and G <= 512 */
+                                  and G <= 512; never split */
 } nvfp4_gemm_tiles;
 
 /* Bytes of a swizzled SF buffer for a rows x cols matrix (cols in elements):
@@ -337,7 +338,13 @@ nvfp4_status moe_stage_activation(const nvfp4_stage_job* job, nvfp4_stream_t str
  * Two kernels compute this (nvfp4_set_gemm_tiles): 128-row tiles on single CTAs,
  * or, when N % 256 == 0, 256-row tiles on CTA pairs (a 2-CTA cluster sharing one
  * cta_group::2 MMA, each CTA loading half of B), which pairs consecutive 128-row
- * blocks of a group.  Both forms give the same results bit for bit.  Every TMA
+ * blocks of a group.  With the automatic choice, a grouped GEMM (G > 1, offsets
+ * given, no gather) on CTA pairs is split: the single-CTA kernel runs on 8 SMs
+ * beside the pair kernel, on a stream of the library's own forked from `stream`
+ * and joined back to it through events (so the call stays ordered on `stream`,
+ * also under stream capture), and computes the last 128-row block of the
+ * thinnest groups with an odd block count, whose half-empty pair tiles the pair
+ * kernel then skips.  Every form gives the same results bit for bit.  Every TMA
  * load reads this GPU's memory into the issuing CTA's own shared memory (no
  * cluster multicast).
  * Limits: K a positive multiple of 256, N a positive multiple of 256 (the SwiGLU
