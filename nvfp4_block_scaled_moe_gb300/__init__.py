@@ -338,6 +338,9 @@ GEMM_TILES_AUTO, GEMM_TILES_SINGLE, GEMM_TILES_PAIR = 0, 1, 2
 
 
 def nvfp4_set_gemm_tiles(mode):
+    """Process-wide tile choice of nvfp4_grouped_gemm: GEMM_TILES_AUTO (by shape;
+    grouped CTA-pair GEMMs split with a single-CTA launch beside them),
+    GEMM_TILES_SINGLE or GEMM_TILES_PAIR (the pair kernel alone)."""
     _check(load().nvfp4_set_gemm_tiles(mode))
 
 
