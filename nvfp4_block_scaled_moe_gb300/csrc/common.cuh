@@ -278,20 +278,25 @@ __device__ __forceinline__ void combine_token_warp(const __nv_bfloat16* __restri
 // takes the thin, weight-streaming ones first, whose DRAM time then overlaps the
 // pair launch's compute-bound tiles instead of forming its tail), n_take chosen
 // so that both launches end together.  A single-CTA 128-row tile costs its SM
-// about kLeftCostNum / kLeftCostDen times what a full pair tile costs each of its
-// two SMs (it stages all 256 weight rows itself: 54 instead of 38 KiB per K
-// stage), so
+// `cost` times what a full pair tile costs each of its two SMs, as it stages
+// all 256 weight rows itself (54 instead of 38 KiB per K stage): measured best
+// at 3/2 with a long K (at least kLeftLongK stages: the L1 GEMM) and 5/4 with a
+// short one (the L2 GEMM, where the pair tile's accumulator hand-off weighs
+// more).  So
 //   n_take = min(n_odd, floor(S * (pairs + n_odd) / (P * cost + S))),
 // pairs the full pairs over all groups.  Both kernels compute the same split
-// from the offsets alone; S == 0: none.
-constexpr int64_t kLeftCostNum = 3, kLeftCostDen = 2;
+// from the offsets and K alone; S == 0: none.
+constexpr int kLeftLongK = 16;                                  // K stages of 256
+constexpr int64_t kLeftCostLongNum = 3, kLeftCostLongDen = 2;
+constexpr int64_t kLeftCostShortNum = 5, kLeftCostShortDen = 4;
 struct LeftoverSplit {
   int32_t n_odd;
   int32_t n_take;
 };
 
 // One warp, all lanes: the split over the G groups of the block offsets s_off.
-__device__ __forceinline__ LeftoverSplit leftover_split(const int32_t* s_off, int G, int P, int S, int lane) {
+__device__ __forceinline__ LeftoverSplit leftover_split(const int32_t* s_off, int G, int P, int S, int k_blocks,
+                                                        int lane) {
   uint32_t pairs = 0, odd = 0;
   for (int g = lane; g < G; g += 32) {
     const int32_t blocks = (s_off[g + 1] - s_off[g]) / 128;
@@ -306,8 +311,11 @@ __device__ __forceinline__ LeftoverSplit leftover_split(const int32_t* s_off, in
   ls.n_odd = static_cast<int32_t>(odd);
   ls.n_take = 0;
   if (S > 0 && P > 0) {
-    const int64_t fit = static_cast<int64_t>(S) * kLeftCostDen * (static_cast<int64_t>(pairs) + odd) /
-                        (static_cast<int64_t>(P) * kLeftCostNum + static_cast<int64_t>(S) * kLeftCostDen);
+    const bool long_k = k_blocks >= kLeftLongK;
+    const int64_t num = long_k ? kLeftCostLongNum : kLeftCostShortNum;
+    const int64_t den = long_k ? kLeftCostLongDen : kLeftCostShortDen;
+    const int64_t fit = static_cast<int64_t>(S) * den * (static_cast<int64_t>(pairs) + odd) /
+                        (static_cast<int64_t>(P) * num + static_cast<int64_t>(S) * den);
     ls.n_take = static_cast<int32_t>(fit < static_cast<int64_t>(odd) ? fit : static_cast<int64_t>(odd));
   }
   return ls;

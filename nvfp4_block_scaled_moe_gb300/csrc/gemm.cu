@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* s_left = reinterpret_cast<int32_t*>(smem + C::kOffLeft);
   if (p.left_ctas > 0) {
     if (warp == 2) {
-      const LeftoverSplit ls = leftover_split(s_off, p.G, p.pair_clusters, p.left_ctas, lane);
+      const LeftoverSplit ls = leftover_split(s_off, p.G, p.pair_clusters, p.left_ctas, p.k_blocks, lane);
       int32_t carry_odd = 0;
       for (int base = 0; base < p.G; base += 32) {
         const int g = base + lane;

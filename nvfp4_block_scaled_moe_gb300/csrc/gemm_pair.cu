@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kSide != kSideNone ? kThreadsSide : kThreads, 
   if (warp == 2) {
     // pair prefix: s_pair[g] = sum over groups before g of ceil(blocks / 2),
     // less the half-empty pair of each odd group a split's single-CTA launch takes
-    const LeftoverSplit ls = leftover_split(s_off, p.G, p.pair_clusters, p.left_ctas, lane);
+    const LeftoverSplit ls = leftover_split(s_off, p.G, p.pair_clusters, p.left_ctas, p.k_blocks, lane);
     int32_t carry = 0, carry_odd = 0;
     if (lane == 0) s_pair[0] = 0;
     for (int base = 0; base < p.G; base += 32) {
