@@ -54,10 +54,10 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # after the other), and the hash of the kernel sources it was taken on.
 # Reported as roofline.traffic only while the sources still hash the same (a
 # changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "7fe6176b793f9898ebc10a635916dd6fc5d1c9939954f27fc25cbd9b15daf92c",
-                     "bytes": {"prefill": (1064688640 + 152835072) + (664393728 + 791808),
-                               "prefill_overlap": (2945248768 + 384499968) + (664398592 + 389376),
-                               "decode": 4350664192 + 3250176}}
+L1_TRAFFIC_RECORD = {"sources_sha256": "597c2862f07e0dcdf1c8a0b101dbe0099bf5c1f9d64a30f8289365f188ebf5fd",
+                     "bytes": {"prefill": (1064234240 + 153088000) + (664541184 + 498176),
+                               "prefill_overlap": (2945267968 + 384792320) + (664382208 + 409344),
+                               "decode": 4351559168 + 3329792}}
 KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scaled_moe_gb300/csrc/gemm_pair.cu",
                   "nvfp4_block_scaled_moe_gb300/csrc/common.cuh", "nvfp4_block_scaled_moe_gb300/csrc/internal.h",
                   "nvfp4_block_scaled_moe_gb300/csrc/stage.cuh")
