@@ -51,10 +51,11 @@ METRIC = "NVFP4 MoE FFN TFLOPS & tokens/s (frac of FP4 peak); quantize GB/s vs H
 # DRAM bytes (read + write) of one L1 launch per workload, from an ncu capture
 # of that launch (dram__bytes_read.sum + dram__bytes_write.sum; on the prefill
 # batch the CTA-pair launch plus the single-CTA launch beside it, captured one
-# after the other), and the hash of the kernel sources it was taken on.
-# Reported as roofline.traffic only while the sources still hash the same (a
-# changed kernel reports null).
-L1_TRAFFIC_RECORD = {"sources_sha256": "597c2862f07e0dcdf1c8a0b101dbe0099bf5c1f9d64a30f8289365f188ebf5fd",
+# after the other), and the hash of the kernel sources' code it was taken on
+# (comments and blank lines left out: kernel_code).  Reported as
+# roofline.traffic only while the code still hashes the same (a changed kernel
+# reports null).
+L1_TRAFFIC_RECORD = {"sources_sha256": "e58cf74a9954716401cccb58b8e3a5e620e555dac638d5193b94021efbdf2121",
                      "bytes": {"prefill": (1064234240 + 153088000) + (664541184 + 498176),
                                "prefill_overlap": (2945267968 + 384792320) + (664382208 + 409344),
                                "decode": 4351559168 + 3329792}}
@@ -63,12 +64,22 @@ KERNEL_SOURCES = ("nvfp4_block_scaled_moe_gb300/csrc/gemm.cu", "nvfp4_block_scal
                   "nvfp4_block_scaled_moe_gb300/csrc/stage.cuh")
 
 
+def kernel_code(text: str) -> str:
+    """A CUDA source without its comments and blank lines: what the hash of the
+    traffic record covers (a comment edit leaves the kernels, and the record,
+    as they were; any code edit changes the hash)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_sources_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(kernel_code(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -12,7 +12,10 @@
 // the tensor pipe busiest); the K loop runs in stages of 256 elements (128
 // bytes of E2M1 per row = one 128-byte swizzle row).  Rows are grouped
 // (experts): group g owns rows [offsets[g], offsets[g+1]) (multiples of 128)
-// and multiplies with B_g.
+// and multiplies with B_g.  As a split's single-CTA half (Params::left_ctas) the
+// kernel computes only the last block of some odd groups, beside the CTA-pair
+// kernel on the rest of the GPU (gemm_pair.cu; the rule is common.cuh's
+// leftover_split).
 //
 // One persistent CTA per SM, 10 warps, warp-specialised:
 //   warp 0     TMA producer: A (128 rows) and B (256 rows) tiles through 2-D tensor

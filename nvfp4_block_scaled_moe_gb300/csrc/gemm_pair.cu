@@ -13,7 +13,10 @@
 // Rows are grouped (experts) as in gemm.cu: group g owns the 128-row blocks
 // [offsets[g]/128, offsets[g+1]/128).  Tiles pair consecutive blocks of one
 // group; a group with an odd block count ends in a tile whose odd CTA has no
-// rows (it loads no A, computes a discarded half and stores nothing).
+// rows (it loads no A, computes a discarded half and stores nothing), unless a
+// split's single-CTA launch beside this one takes that group's last block
+// (PairParams::left_ctas; common.cuh: leftover_split), in which case the tile
+// is skipped.
 //
 // Roles (320 threads per CTA, 384 with a side job; one CTA per SM):
 //   warp 0     producer: TMA loads of A (128 rows), this CTA's 128 rows of B,

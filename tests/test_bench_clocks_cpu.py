@@ -102,3 +102,14 @@ def test_window_summarises_a_span_and_keeps_polling(monkeypatch):
     assert region["sm_mhz"] == 2070 and region["reasons"] == []
     assert later["sm_mhz"] == 1700 and later["reasons"] == ["sw_power_cap"]
     assert region["samples"] >= 3 and later["samples"] >= 3
+
+
+def test_traffic_record_hash_covers_code_not_comments():
+    """The traffic record's hash follows the kernels' code: a comment or a blank
+    line changes nothing, a changed statement changes the hash."""
+    import bench
+    a = "int f(int x) {\n  return x + 1;   // one more\n}\n"
+    b = "/* the successor */\nint f(int x) {\n\n  return x + 1;\n}\n// end\n"
+    c = "int f(int x) {\n  return x + 2;   // one more\n}\n"
+    assert bench.kernel_code(a) == bench.kernel_code(b)
+    assert bench.kernel_code(a) != bench.kernel_code(c)
