@@ -1,5 +1,6 @@
-"""bench.py's clock sampler on CPU, against a fake NVML: the polling thread, the
-timed-region filter and the clock-event reason bits (read-only queries; no GPU)."""
+"""bench.py on CPU: its clock sampler against a fake NVML (the polling thread,
+the timed-region filter and the clock-event reason bits; read-only queries, no
+GPU), and the code hash that keys its traffic record."""
 import ctypes
 import threading
 import time
